@@ -1,0 +1,152 @@
+/*
+ * mhc_pre.h -- C ABI of the GB300 (sm_103a) mHC pre-mapping forward.
+ *
+ * The operation (per token t of T; n residual streams of width D; K = n*D):
+ *
+ *   invRms      = (mean_k x[t,k]^2 + normEps)^(-1/2)            raw x, k < n*D
+ *   hMix[t,:]   = (x[t,:] (.) gamma) . phi^T                     phi [R, K] fp32
+ *   w           = hMix * invRms, split [pre n | post n | res n*n]
+ *   hPre        = sigmoid(alpha0*pre  + bias[0:n])  + hcEps
+ *   hPost       = 2*sigmoid(alpha1*post + bias[n:2n])   (+ hcEps, two-gate only)
+ *   H           = alpha2*res + bias[2n:], reshaped row-major to [n, n]
+ *   comb        = Sinkhorn(H): softmax over each row + hcEps, then a column
+ *                 normalisation, then (row, column) x (numIters - 1); every
+ *                 normalisation divides by (sum + hcEps)
+ *   y[t,d]      = bf16( sum_i m_i * x[t,i,d] ),  m = pre_mix[t] if given else hPre
+ *
+ * Sources: "CANN ops-transformer 中 aclnnMhcPreV2 算子接口全解析：MHC 架构 H
+ * 投影矩阵与 hIn 计算实战指南" §三 (formula), §四 (two-phase call), §5.1-§5.4
+ * (tensors, optional output group, status codes), §7.3 (n in {4,6,8}, D
+ * multiple of 16, two-gate shapes); "CANN ops-transformer 算子详解：
+ * aclnnMhcPreSinkhorn 接口与 MhcPreSinkhorn 实现剖析" §3.2 (Sinkhorn), §5.1
+ * (sumOut / normOut shapes), §6 (status codes); "CANN HcPre 融合算子解析：
+ * custom.npu_hc_pre 与 npu_hc_pre_v2 实战指南" (pre_mix).
+ *
+ * Conventions
+ *  - Every tensor pointer in mhc_pre_args is a DEVICE pointer owned by the
+ *    caller, dense and row-major (no strides).  x and y must be 16-byte
+ *    aligned, the workspace 256-byte aligned, fp32 tensors 4-byte aligned.
+ *  - The handle owns host-side configuration only.  It holds no device
+ *    memory and may be used from one host thread at a time.
+ *  - mhc_pre_run validates on the host, then enqueues kernels on `stream`
+ *    and returns without waiting.  Results are deterministic: the same
+ *    inputs give bit-identical outputs, run after run.
+ *  - Nothing here falls back to the CPU.  If the device is not an sm_103
+ *    part, mhc_pre_run returns MHC_ERR_RUNTIME.
+ */
+#ifndef MHC_PRE_H
+#define MHC_PRE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#if defined(__GNUC__)
+#define MHC_API __attribute__((visibility("default")))
+#else
+#define MHC_API
+#endif
+
+/* Status codes, numerically equal to the aclnn codes the pages list. */
+typedef int32_t mhc_status_t;
+#define MHC_OK                0
+#define MHC_ERR_NULLPTR       161001  /* a required pointer is NULL            */
+#define MHC_ERR_PARAM_INVALID 161002  /* shape, mode, alignment or group error  */
+#define MHC_ERR_RUNTIME       361001  /* CUDA launch / device-side failure      */
+
+/* Precision of the projection (opImplMode on the MhcPreV2 page, §二). */
+#define MHC_IMPL_FP32 0   /* phi used at full fp32 precision (exact products)   */
+#define MHC_IMPL_TF32 1   /* phi truncated toward zero to 10 mantissa bits
+                             (the pages' HF32 mode); x (bf16) is exact in both */
+
+typedef struct mhc_pre_s *mhc_pre_t;
+
+/* Fixed per handle.  Defaults (mhc_pre_config_default): n = 4, D = 0 (must be
+ * set), alpha_len = 3, num_iters = 20, norm_eps = hc_eps = 1e-6,
+ * impl_mode = MHC_IMPL_FP32, need_backward = 0. */
+typedef struct {
+    int64_t n;              /* residual streams: 4, 6 or 8                          */
+    int64_t D;              /* stream width: 16 <= D <= 16384, D % 16 == 0          */
+    int32_t alpha_len;      /* 3 (pre/post/res) or 2 (no residual path)             */
+    int32_t num_iters;      /* Sinkhorn iterations, 1..100 (pages: 20)              */
+    double  norm_eps;       /* RMS epsilon, > 0 not required                        */
+    double  hc_eps;         /* gate / Sinkhorn epsilon                              */
+    int32_t impl_mode;      /* MHC_IMPL_FP32 or MHC_IMPL_TF32                       */
+    int32_t need_backward;  /* 1: also write inv_rms, h_mix, sum_out, norm_out      */
+} mhc_pre_config;
+
+/* Per call.  R = n*n + 2n (alpha_len 3) or 2n (alpha_len 2); I = num_iters. */
+typedef struct {
+    int64_t      T;         /* tokens; 0 returns MHC_OK at once (pointers unchecked)  */
+    const void  *x;         /* bf16 [T, n, D]                          required       */
+    const float *phi;       /* fp32 [R, n*D]                           required       */
+    const float *alpha;     /* fp32 [alpha_len]                        required       */
+    const float *bias;      /* fp32 [R]                                required       */
+    const float *gamma;     /* fp32 [n, D] or NULL (no scaling)                       */
+    const float *pre_mix;   /* fp32 [T, n] or NULL (y weights = hPre)                 */
+    void        *y;         /* bf16 [T, D]                             required       */
+    float       *h_post;    /* fp32 [T, n]                             required       */
+    float       *h_res;     /* fp32 [T, n, n] comb after Sinkhorn; required when
+                               alpha_len == 3; optional (filled with 0) when 2        */
+    float       *h_pre;     /* fp32 [T, n]; required when need_backward or pre_mix,
+                               else optional                                         */
+    float       *inv_rms;   /* fp32 [T]          } need_backward == 1: all required  */
+    float       *h_mix;     /* fp32 [T, R]       } (sum_out / norm_out only when     */
+    float       *sum_out;   /* fp32 [2I, T, n]   }  alpha_len == 3);                  */
+    float       *norm_out;  /* fp32 [2I, T, n, n]} need_backward == 0: all NULL       */
+    void        *workspace;       /* device scratch, >= mhc_pre_workspace_size bytes   */
+    size_t       workspace_bytes; /* its size                                          */
+} mhc_pre_args;
+
+/* Fill *cfg with the defaults listed above.  NULL cfg is ignored. */
+MHC_API void mhc_pre_config_default(mhc_pre_config *cfg);
+
+/* Validate cfg and create a handle.  MHC_ERR_NULLPTR if out or cfg is NULL;
+ * MHC_ERR_PARAM_INVALID for a value outside the ranges above (the handle is
+ * then not created and *out is set to NULL). */
+MHC_API mhc_status_t mhc_pre_create(mhc_pre_t *out, const mhc_pre_config *cfg);
+
+/* Bytes of device workspace a call with T tokens needs (first phase of the
+ * pages' two-phase call).  Depends on the handle's shape and mode and on T;
+ * T == 0 gives 0.  MHC_ERR_NULLPTR / MHC_ERR_PARAM_INVALID (T < 0). */
+MHC_API mhc_status_t mhc_pre_workspace_size(mhc_pre_t h, int64_t T, size_t *bytes);
+
+/* Second phase: check args, then enqueue the forward on `stream` (a
+ * cudaStream_t; NULL = legacy default stream).  Host-side checks return
+ * before anything is enqueued:
+ *   MHC_ERR_NULLPTR        a required pointer is NULL;
+ *   MHC_ERR_PARAM_INVALID  T < 0, an optional-group violation, a pointer
+ *                          not aligned as stated, or workspace too small;
+ *   MHC_ERR_RUNTIME        no usable sm_103 device, or a launch failed.
+ * Device-side waits are bounded; a wait that gives up sets an error word in
+ * the workspace that mhc_pre_status reports. */
+MHC_API mhc_status_t mhc_pre_run(mhc_pre_t h, const mhc_pre_args *args, void *stream);
+
+/* Synchronise `stream`, then report MHC_ERR_RUNTIME if a CUDA error is
+ * pending or the last run's device error word (in `workspace`, which may be
+ * NULL to skip that check) is set; else MHC_OK. */
+MHC_API mhc_status_t mhc_pre_status(mhc_pre_t h, const void *workspace, void *stream);
+
+/* Optional timing hooks.  When set, mhc_pre_run records `before` on its
+ * stream just before it launches the fused forward kernel and `after` just
+ * after (both cudaEvent_t; pass NULL, NULL to clear).  This lets a caller time
+ * that kernel alone, with CUDA events on the stream it runs on.  The events
+ * are borrowed, not owned.  MHC_ERR_NULLPTR if h is NULL. */
+MHC_API mhc_status_t mhc_pre_set_profile_events(mhc_pre_t h, void *before, void *after);
+
+/* Release the handle (NULL is ignored). */
+MHC_API void mhc_pre_destroy(mhc_pre_t h);
+
+/* Static description of a status code. */
+MHC_API const char *mhc_pre_status_string(mhc_status_t s);
+
+/* Text of the last validation failure on this host thread ("" if none). */
+MHC_API const char *mhc_pre_last_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* MHC_PRE_H */

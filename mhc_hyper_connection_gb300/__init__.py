@@ -1,0 +1,12 @@
+"""GB300 (sm_103a) mHC pre-mapping forward: C ABI + thin ctypes binding.
+
+The compute lives in ``libmhc_pre.so`` (built from ``csrc/`` by
+``python -m mhc_hyper_connection_gb300.build``).  This package only loads it
+and marshals arguments; importing it does not load the library until a
+function is called.
+"""
+from ._binding import (  # noqa: F401
+    LIB_PATH, MHC_ERR_NULLPTR, MHC_ERR_PARAM_INVALID, MHC_ERR_RUNTIME, MHC_IMPL_FP32,
+    MHC_IMPL_TF32, MHC_OK, MhcError, MhcPre, MhcPreArgs, MhcPreConfig, last_error, library,
+    mhc_pre_config_default, mhc_pre_create, mhc_pre_destroy, mhc_pre_run, mhc_pre_set_profile_events, mhc_pre_status,
+    mhc_pre_workspace_size, status_string)

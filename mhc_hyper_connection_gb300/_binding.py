@@ -1,0 +1,224 @@
+"""ctypes binding of include/mhc_pre.h -- argument marshalling only.
+
+Every function of the C ABI is exposed under its own name.  ``MhcPre`` wraps
+a handle and turns torch tensors into the pointer struct; all computation
+happens in the CUDA library.  If the library has not been built this module
+raises on first use: there is no other code path.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+from typing import Optional
+
+MHC_OK = 0
+MHC_ERR_NULLPTR = 161001
+MHC_ERR_PARAM_INVALID = 161002
+MHC_ERR_RUNTIME = 361001
+MHC_IMPL_FP32 = 0
+MHC_IMPL_TF32 = 1
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libmhc_pre.so")
+
+
+class MhcPreConfig(ctypes.Structure):
+    _fields_ = [("n", ctypes.c_int64), ("D", ctypes.c_int64), ("alpha_len", ctypes.c_int32),
+                ("num_iters", ctypes.c_int32), ("norm_eps", ctypes.c_double),
+                ("hc_eps", ctypes.c_double), ("impl_mode", ctypes.c_int32),
+                ("need_backward", ctypes.c_int32)]
+
+
+_P = ctypes.c_void_p
+
+
+class MhcPreArgs(ctypes.Structure):
+    _fields_ = [("T", ctypes.c_int64), ("x", _P), ("phi", _P), ("alpha", _P), ("bias", _P),
+                ("gamma", _P), ("pre_mix", _P), ("y", _P), ("h_post", _P), ("h_res", _P),
+                ("h_pre", _P), ("inv_rms", _P), ("h_mix", _P), ("sum_out", _P),
+                ("norm_out", _P), ("workspace", _P), ("workspace_bytes", ctypes.c_size_t)]
+
+
+class MhcError(RuntimeError):
+    def __init__(self, status: int, where: str, detail: str = ""):
+        self.status = status
+        super().__init__(f"{where}: status {status} ({status_string(status)})"
+                         + (f": {detail}" if detail else ""))
+
+
+_lib = None
+_lock = threading.Lock()
+
+
+def library() -> ctypes.CDLL:
+    """Load libmhc_pre.so (built in-tree).  Raises if it is missing."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(LIB_PATH):
+                raise RuntimeError(f"{LIB_PATH} is missing: build it with "
+                                   "`python -m mhc_hyper_connection_gb300.build`")
+            lib = ctypes.CDLL(LIB_PATH)
+            lib.mhc_pre_config_default.argtypes = [ctypes.POINTER(MhcPreConfig)]
+            lib.mhc_pre_config_default.restype = None
+            lib.mhc_pre_create.argtypes = [ctypes.POINTER(_P), ctypes.POINTER(MhcPreConfig)]
+            lib.mhc_pre_create.restype = ctypes.c_int32
+            lib.mhc_pre_workspace_size.argtypes = [_P, ctypes.c_int64, ctypes.POINTER(ctypes.c_size_t)]
+            lib.mhc_pre_workspace_size.restype = ctypes.c_int32
+            lib.mhc_pre_run.argtypes = [_P, ctypes.POINTER(MhcPreArgs), _P]
+            lib.mhc_pre_run.restype = ctypes.c_int32
+            lib.mhc_pre_status.argtypes = [_P, _P, _P]
+            lib.mhc_pre_status.restype = ctypes.c_int32
+            lib.mhc_pre_set_profile_events.argtypes = [_P, _P, _P]
+            lib.mhc_pre_set_profile_events.restype = ctypes.c_int32
+            lib.mhc_pre_destroy.argtypes = [_P]
+            lib.mhc_pre_destroy.restype = None
+            lib.mhc_pre_status_string.argtypes = [ctypes.c_int32]
+            lib.mhc_pre_status_string.restype = ctypes.c_char_p
+            lib.mhc_pre_last_error.argtypes = []
+            lib.mhc_pre_last_error.restype = ctypes.c_char_p
+            _lib = lib
+    return _lib
+
+
+# ----------------------------------------------------------- raw C entry points
+
+def mhc_pre_config_default() -> MhcPreConfig:
+    c = MhcPreConfig()
+    library().mhc_pre_config_default(ctypes.byref(c))
+    return c
+
+
+def mhc_pre_create(cfg: MhcPreConfig):
+    """Returns (status, handle-or-None)."""
+    h = _P()
+    st = library().mhc_pre_create(ctypes.byref(h), ctypes.byref(cfg))
+    return st, (h if st == MHC_OK else None)
+
+
+def mhc_pre_workspace_size(handle, T: int):
+    n = ctypes.c_size_t(0)
+    st = library().mhc_pre_workspace_size(handle, int(T), ctypes.byref(n))
+    return st, n.value
+
+
+def mhc_pre_run(handle, args: MhcPreArgs, stream: int = 0) -> int:
+    return library().mhc_pre_run(handle, ctypes.byref(args), _P(stream or None))
+
+
+def mhc_pre_status(handle, workspace: int = 0, stream: int = 0) -> int:
+    return library().mhc_pre_status(handle, _P(workspace or None), _P(stream or None))
+
+
+def mhc_pre_set_profile_events(handle, before: int = 0, after: int = 0) -> int:
+    return library().mhc_pre_set_profile_events(handle, _P(before or None), _P(after or None))
+
+
+def mhc_pre_destroy(handle) -> None:
+    library().mhc_pre_destroy(handle)
+
+
+def status_string(status: int) -> str:
+    return library().mhc_pre_status_string(int(status)).decode()
+
+
+def last_error() -> str:
+    return library().mhc_pre_last_error().decode()
+
+
+# ------------------------------------------------------------- torch marshalling
+
+def _ptr(t) -> Optional[int]:
+    return None if t is None else int(t.data_ptr())
+
+
+class MhcPre:
+    """One configured forward (n, D, alpha_len, num_iters, eps, mode, backward)."""
+
+    def __init__(self, n: int, D: int, *, alpha_len: int = 3, num_iters: int = 20,
+                 norm_eps: float = 1e-6, hc_eps: float = 1e-6, impl_mode: int = MHC_IMPL_FP32,
+                 need_backward: bool = False):
+        cfg = mhc_pre_config_default()
+        cfg.n, cfg.D, cfg.alpha_len, cfg.num_iters = n, D, alpha_len, num_iters
+        cfg.norm_eps, cfg.hc_eps = norm_eps, hc_eps
+        cfg.impl_mode, cfg.need_backward = impl_mode, int(bool(need_backward))
+        st, h = mhc_pre_create(cfg)
+        if st != MHC_OK:
+            raise MhcError(st, "mhc_pre_create", last_error())
+        self.handle = h
+        self.n, self.D, self.alpha_len, self.num_iters = n, D, alpha_len, num_iters
+        self.need_backward = bool(need_backward)
+        self.R = n * n + 2 * n if alpha_len == 3 else 2 * n
+
+    def close(self):
+        if self.handle is not None:
+            mhc_pre_destroy(self.handle)
+            self.handle = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    def workspace_size(self, T: int) -> int:
+        st, n = mhc_pre_workspace_size(self.handle, T)
+        if st != MHC_OK:
+            raise MhcError(st, "mhc_pre_workspace_size", last_error())
+        return n
+
+    def allocate(self, T: int, device, *, h_res: bool = True, h_pre: bool = True):
+        """Output and workspace tensors for T tokens (torch supplies the memory)."""
+        import torch
+        n, D, R, I = self.n, self.D, self.R, self.num_iters
+        f32 = dict(dtype=torch.float32, device=device)
+        out = {"y": torch.empty((T, D), dtype=torch.bfloat16, device=device),
+               "h_post": torch.empty((T, n), **f32),
+               "h_res": torch.empty((T, n, n), **f32) if (h_res or self.alpha_len == 3) else None,
+               "h_pre": torch.empty((T, n), **f32) if (h_pre or self.need_backward) else None,
+               "inv_rms": None, "h_mix": None, "sum_out": None, "norm_out": None}
+        if self.need_backward:
+            out["inv_rms"] = torch.empty((T,), **f32)
+            out["h_mix"] = torch.empty((T, R), **f32)
+            if self.alpha_len == 3:
+                out["sum_out"] = torch.empty((2 * I, T, n), **f32)
+                out["norm_out"] = torch.empty((2 * I, T, n, n), **f32)
+        ws = self.workspace_size(T)
+        # At least the 256-byte header, zeroed, so a status read is defined even for T = 0.
+        out["workspace"] = torch.zeros((max(ws, 256),), dtype=torch.uint8, device=device)
+        return out
+
+    def make_args(self, x, phi, alpha, bias, out, gamma=None, pre_mix=None) -> MhcPreArgs:
+        a = MhcPreArgs()
+        a.T = int(x.shape[0]) if x is not None else 0
+        a.x, a.phi, a.alpha, a.bias = _ptr(x), _ptr(phi), _ptr(alpha), _ptr(bias)
+        a.gamma, a.pre_mix = _ptr(gamma), _ptr(pre_mix)
+        for k in ("y", "h_post", "h_res", "h_pre", "inv_rms", "h_mix", "sum_out", "norm_out"):
+            setattr(a, k, _ptr(out.get(k)))
+        ws = out.get("workspace")
+        a.workspace = _ptr(ws)
+        a.workspace_bytes = 0 if ws is None else ws.numel() * ws.element_size()
+        return a
+
+    def run(self, x, phi, alpha, bias, out, gamma=None, pre_mix=None, stream=None):
+        """Enqueue the forward on `stream` (torch stream or raw handle; default:
+        torch's current stream).  Raises MhcError on a host-side rejection."""
+        args = self.make_args(x, phi, alpha, bias, out, gamma, pre_mix)
+        if stream is None:
+            import torch
+            stream = torch.cuda.current_stream(x.device).cuda_stream
+        elif hasattr(stream, "cuda_stream"):
+            stream = stream.cuda_stream
+        st = mhc_pre_run(self.handle, args, int(stream))
+        if st != MHC_OK:
+            raise MhcError(st, "mhc_pre_run", last_error())
+        return out
+
+    def status(self, out=None, stream=None) -> int:
+        ws = None if out is None else out.get("workspace")
+        if stream is None:
+            stream = 0
+        elif hasattr(stream, "cuda_stream"):
+            stream = stream.cuda_stream
+        return mhc_pre_status(self.handle, _ptr(ws) or 0, int(stream))

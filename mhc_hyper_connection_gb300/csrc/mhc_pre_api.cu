@@ -1,0 +1,336 @@
+// mhc_pre_api.cu -- host side of the C ABI declared in include/mhc_pre.h:
+// argument checks, workspace sizing, tensor maps, launch configuration.
+//
+// The two-phase shape of the API (size the workspace, then run on a stream)
+// and the status codes follow "aclnnMhcPreSinkhorn 接口与 MhcPreSinkhorn 实现
+// 剖析" §4, §6 and "aclnnMhcPreV2 算子接口全解析" §四, §5.4; the optional
+// output group (all or none) follows the same page's §7.3.
+#include <cstdarg>
+#include <cstdio>
+#include <cstdlib>
+#include <cstring>
+#include <mutex>
+
+#include "mhc_common.cuh"
+#include "../../include/mhc_pre.h"
+
+namespace mhc {
+int tc_np(int R, int P);
+}
+
+struct mhc_pre_s {
+  mhc_pre_config cfg;
+  int R;        // projection rows
+  int P;        // precision planes (3: fp32, 2: tf32)
+  int NP;       // MMA N = P*R rounded up to 16
+  cudaEvent_t ev_before = nullptr, ev_after = nullptr;   // optional timing hooks
+};
+
+namespace {
+
+thread_local char g_last_error[512] = "";
+
+mhc_status_t fail(mhc_status_t code, const char* fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(g_last_error, sizeof g_last_error, fmt, ap);
+  va_end(ap);
+  return code;
+}
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*,
+                                  CUtensorMapInterleave, CUtensorMapSwizzle, CUtensorMapL2promotion,
+                                  CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  });
+  return fn;
+}
+
+// 3-D bf16 map over [dim2][dim1][dim0] (dim0 contiguous), box (64, 1, box2),
+// 128-byte swizzle, zero fill outside the tensor.
+bool encode_3d(CUtensorMap* map, const void* base, uint64_t dim0, uint64_t dim1, uint64_t dim2,
+               uint32_t box2) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[3] = {dim0, dim1, dim2};
+  cuuint64_t strides[2] = {dim0 * 2, dim0 * dim1 * 2};
+  cuuint32_t box[3] = {(cuuint32_t)mhc::kChunkK, 1, box2};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+struct DeviceInfo {
+  bool ok = false;
+  int sms = 0;
+  size_t max_smem = 0;
+};
+
+DeviceInfo device_info(int dev) {
+  static std::mutex mu;
+  static DeviceInfo cache[64];
+  static bool known[64] = {};
+  std::lock_guard<std::mutex> lk(mu);
+  if (dev < 0 || dev >= 64) return DeviceInfo{};
+  if (!known[dev]) {
+    DeviceInfo d;
+    cudaDeviceProp prop;
+    if (cudaGetDeviceProperties(&prop, dev) == cudaSuccess) {
+      d.ok = (prop.major == 10 && prop.minor == 3);
+      d.sms = prop.multiProcessorCount;
+      d.max_smem = prop.sharedMemPerBlockOptin;
+    }
+    cache[dev] = d;
+    known[dev] = true;
+  }
+  return cache[dev];
+}
+
+bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+size_t planes_bytes(const mhc_pre_s* h) {
+  const size_t K = (size_t)(h->cfg.n * h->cfg.D);
+  return ((size_t)h->NP * K * 2 + 255) & ~size_t(255);
+}
+
+int env_int(const char* name, int dflt) {
+  const char* v = getenv(name);
+  if (!v || !*v) return dflt;
+  return atoi(v);
+}
+
+// Shared-memory bytes of the tensor-core kernel for `stages` pipeline stages.
+size_t tc_smem_bytes(int n, int R, int NP, int stages) {
+  size_t b = 1024;                                   // alignment slack
+  b += (size_t)stages * (mhc::kTileM * 128 + (size_t)NP * 128);
+  b += (size_t)mhc::kTileM * (R + 1) * 4;            // partial sums
+  b += 2 * (size_t)mhc::kTileM * 4;                  // sums of squares
+  b += 2 * (size_t)mhc::kTileM * n * 4;              // y weights
+  b += 16 + 256;                                     // barriers, flags
+  return b;
+}
+
+}  // namespace
+
+extern "C" {
+
+void mhc_pre_config_default(mhc_pre_config* c) {
+  if (!c) return;
+  c->n = 4;
+  c->D = 0;
+  c->alpha_len = 3;
+  c->num_iters = 20;
+  c->norm_eps = 1e-6;
+  c->hc_eps = 1e-6;
+  c->impl_mode = MHC_IMPL_FP32;
+  c->need_backward = 0;
+}
+
+const char* mhc_pre_last_error(void) { return g_last_error; }
+
+const char* mhc_pre_status_string(mhc_status_t s) {
+  switch (s) {
+    case MHC_OK: return "success";
+    case MHC_ERR_NULLPTR: return "a required pointer is NULL";
+    case MHC_ERR_PARAM_INVALID: return "invalid parameter (shape, mode, alignment or output group)";
+    case MHC_ERR_RUNTIME: return "CUDA runtime or device-side failure";
+    default: return "unknown status";
+  }
+}
+
+mhc_status_t mhc_pre_create(mhc_pre_t* out, const mhc_pre_config* cfg) {
+  g_last_error[0] = 0;
+  if (!out || !cfg) return fail(MHC_ERR_NULLPTR, "out and cfg must be non-NULL");
+  *out = nullptr;
+  const mhc_pre_config& c = *cfg;
+  if (c.n != 4 && c.n != 6 && c.n != 8) return fail(MHC_ERR_PARAM_INVALID, "n must be 4, 6 or 8 (got %lld)", (long long)c.n);
+  if (c.D < 16 || c.D > 16384 || (c.D % 16) != 0)
+    return fail(MHC_ERR_PARAM_INVALID, "D must be a multiple of 16 in [16, 16384] (got %lld)", (long long)c.D);
+  if (c.alpha_len != 2 && c.alpha_len != 3) return fail(MHC_ERR_PARAM_INVALID, "alpha_len must be 2 or 3");
+  if (c.num_iters < 1 || c.num_iters > 100) return fail(MHC_ERR_PARAM_INVALID, "num_iters must be in [1, 100]");
+  if (c.impl_mode != MHC_IMPL_FP32 && c.impl_mode != MHC_IMPL_TF32)
+    return fail(MHC_ERR_PARAM_INVALID, "impl_mode must be 0 (fp32) or 1 (tf32)");
+  if (c.need_backward != 0 && c.need_backward != 1) return fail(MHC_ERR_PARAM_INVALID, "need_backward must be 0 or 1");
+  if (!(c.norm_eps >= 0.0) || !(c.hc_eps >= 0.0)) return fail(MHC_ERR_PARAM_INVALID, "eps values must be >= 0");
+  mhc_pre_s* h = new (std::nothrow) mhc_pre_s;
+  if (!h) return fail(MHC_ERR_RUNTIME, "out of host memory");
+  h->cfg = c;
+  h->R = (int)(c.alpha_len == 3 ? c.n * c.n + 2 * c.n : 2 * c.n);
+  h->P = (c.impl_mode == MHC_IMPL_FP32) ? 3 : 2;
+  h->NP = mhc::tc_np(h->R, h->P);
+  *out = h;
+  return MHC_OK;
+}
+
+mhc_status_t mhc_pre_workspace_size(mhc_pre_t h, int64_t T, size_t* bytes) {
+  g_last_error[0] = 0;
+  if (!h || !bytes) return fail(MHC_ERR_NULLPTR, "handle and bytes must be non-NULL");
+  if (T < 0) return fail(MHC_ERR_PARAM_INVALID, "T must be >= 0");
+  *bytes = (T == 0) ? 0 : mhc::kWsHeader + planes_bytes(h);
+  return MHC_OK;
+}
+
+mhc_status_t mhc_pre_run(mhc_pre_t h, const mhc_pre_args* a, void* stream) {
+  g_last_error[0] = 0;
+  if (!h || !a) return fail(MHC_ERR_NULLPTR, "handle and args must be non-NULL");
+  const mhc_pre_config& c = h->cfg;
+  const int64_t T = a->T;
+  if (T < 0 || T > (int64_t(1) << 30)) return fail(MHC_ERR_PARAM_INVALID, "T must be in [0, 2^30]");
+  if (T == 0) return MHC_OK;   // empty input: nothing to check or launch (pointers may be NULL)
+  if (!a->x || !a->phi || !a->alpha || !a->bias || !a->y || !a->h_post)
+    return fail(MHC_ERR_NULLPTR, "x, phi, alpha, bias, y and h_post are required");
+  if (c.alpha_len == 3 && !a->h_res) return fail(MHC_ERR_NULLPTR, "h_res is required with alpha of length 3");
+  if (a->pre_mix && !a->h_pre) return fail(MHC_ERR_NULLPTR, "h_pre is required when pre_mix is given");
+  if (c.need_backward) {
+    if (!a->h_pre || !a->inv_rms || !a->h_mix)
+      return fail(MHC_ERR_NULLPTR, "need_backward: h_pre, inv_rms and h_mix are required");
+    if (c.alpha_len == 3 && (!a->sum_out || !a->norm_out))
+      return fail(MHC_ERR_NULLPTR, "need_backward: sum_out and norm_out are required");
+    if (c.alpha_len == 2 && (a->sum_out || a->norm_out))
+      return fail(MHC_ERR_PARAM_INVALID, "sum_out / norm_out do not exist without the residual path");
+  } else if (a->inv_rms || a->h_mix || a->sum_out || a->norm_out) {
+    return fail(MHC_ERR_PARAM_INVALID, "inv_rms, h_mix, sum_out, norm_out must be NULL unless need_backward");
+  }
+  if (!aligned(a->x, 16) || !aligned(a->y, 16))
+    return fail(MHC_ERR_PARAM_INVALID, "x and y must be 16-byte aligned");
+  const void* f32[] = {a->phi, a->alpha, a->bias, a->gamma, a->pre_mix, a->h_post, a->h_res,
+                       a->h_pre, a->inv_rms, a->h_mix, a->sum_out, a->norm_out};
+  for (const void* p : f32)
+    if (p && !aligned(p, 4)) return fail(MHC_ERR_PARAM_INVALID, "fp32 tensors must be 4-byte aligned");
+  size_t need = 0;
+  mhc_pre_workspace_size(h, T, &need);
+  if (!a->workspace) return fail(MHC_ERR_NULLPTR, "workspace is required (%zu bytes)", need);
+  if (!aligned(a->workspace, 256)) return fail(MHC_ERR_PARAM_INVALID, "workspace must be 256-byte aligned");
+  if (a->workspace_bytes < need)
+    return fail(MHC_ERR_PARAM_INVALID, "workspace too small: %zu < %zu bytes", a->workspace_bytes, need);
+
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return fail(MHC_ERR_RUNTIME, "no CUDA device");
+  const DeviceInfo di = device_info(dev);
+  if (!di.ok) return fail(MHC_ERR_RUNTIME, "device %d is not an sm_103 GPU", dev);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+
+  const int n = (int)c.n, D = (int)c.D, R = h->R, NP = h->NP;
+  uint8_t* ws = static_cast<uint8_t*>(a->workspace);
+  uint32_t* err = reinterpret_cast<uint32_t*>(ws);
+  __nv_bfloat16* planes = reinterpret_cast<__nv_bfloat16*>(ws + mhc::kWsHeader);
+
+  // 1. phi (x gamma) -> stacked bf16 precision planes; clears the error word.
+  mhc::PlaneParams pp;
+  pp.phi = a->phi;
+  pp.gamma = a->gamma;
+  pp.planes = planes;
+  pp.R = R;
+  pp.K = n * D;
+  pp.NP = NP;
+  pp.P = h->P;
+  pp.tf32 = (c.impl_mode == MHC_IMPL_TF32);
+  pp.err_word = err;
+  if (mhc::launch_prepare_planes(pp, s) != cudaSuccess)
+    return fail(MHC_ERR_RUNTIME, "plane preparation launch failed: %s", cudaGetErrorString(cudaGetLastError()));
+
+  // 2. the fused forward.
+  mhc::TcLaunch L;
+  memset(&L, 0, sizeof L);
+  mhc::EpiParams& e = L.epi;
+  e.T = (int)T;
+  e.n = n;
+  e.D = D;
+  e.R = R;
+  e.alpha_len = c.alpha_len;
+  e.num_iters = c.num_iters;
+  e.norm_eps = (float)c.norm_eps;
+  e.hc_eps = (float)c.hc_eps;
+  e.alpha = a->alpha;
+  e.bias = a->bias;
+  e.pre_mix = a->pre_mix;
+  e.y = static_cast<__nv_bfloat16*>(a->y);
+  e.h_post = a->h_post;
+  e.h_res = a->h_res;
+  e.h_pre = a->h_pre;
+  e.inv_rms = a->inv_rms;
+  e.h_mix = a->h_mix;
+  e.sum_out = a->sum_out;
+  e.norm_out = a->norm_out;
+  L.x = a->x;
+  L.NP = NP;
+  L.P = h->P;
+  L.err_word = err;
+  if (!encode_3d(&L.tmap_x, a->x, (uint64_t)D, (uint64_t)n, (uint64_t)T, mhc::kTileM) ||
+      !encode_3d(&L.tmap_w, planes, (uint64_t)D, (uint64_t)n, (uint64_t)NP, (uint32_t)NP))
+    return fail(MHC_ERR_RUNTIME, "tensor map encoding failed");
+
+  const int nd = (D + mhc::kChunkK - 1) / mhc::kChunkK;
+  const int num_tiles = (int)((T + mhc::kTileM - 1) / mhc::kTileM);
+  int stages = env_int("MHC_PRE_STAGES", 8);
+  const size_t budget = di.max_smem;
+  while (stages > 2 && tc_smem_bytes(n, R, NP, stages) > budget) --stages;
+  const size_t smem = tc_smem_bytes(n, R, NP, stages);
+  if (smem > budget) return fail(MHC_ERR_RUNTIME, "shape needs %zu bytes of shared memory", smem);
+
+  int want = env_int("MHC_PRE_CLUSTER", 16);
+  int cluster = 1;
+  int max_clusters = 0;
+  for (int cand : {16, 8, 4, 2, 1}) {
+    if (cand > want || cand > nd) continue;
+    int mc = 0;
+    if (mhc::tc_forward_occupancy(n, R, h->P, smem, cand, &mc) == cudaSuccess && mc > 0) {
+      cluster = cand;
+      max_clusters = mc;
+      break;
+    }
+    cudaGetLastError();
+  }
+  if (max_clusters <= 0) return fail(MHC_ERR_RUNTIME, "no cluster configuration fits this device");
+  L.cluster = cluster;
+  L.grid = (num_tiles < max_clusters ? num_tiles : max_clusters) * cluster;
+  L.stages = stages;
+  L.smem_bytes = smem;
+  if (h->ev_before && cudaEventRecord(h->ev_before, s) != cudaSuccess)
+    return fail(MHC_ERR_RUNTIME, "recording the timing event failed");
+  if (mhc::launch_tc_forward(L, s) != cudaSuccess)
+    return fail(MHC_ERR_RUNTIME, "forward launch failed: %s", cudaGetErrorString(cudaGetLastError()));
+  if (h->ev_after && cudaEventRecord(h->ev_after, s) != cudaSuccess)
+    return fail(MHC_ERR_RUNTIME, "recording the timing event failed");
+  return MHC_OK;
+}
+
+mhc_status_t mhc_pre_status(mhc_pre_t h, const void* workspace, void* stream) {
+  g_last_error[0] = 0;
+  if (!h) return fail(MHC_ERR_NULLPTR, "handle must be non-NULL");
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaError_t e = cudaStreamSynchronize(s);
+  if (e != cudaSuccess) return fail(MHC_ERR_RUNTIME, "stream error: %s", cudaGetErrorString(e));
+  if (workspace) {
+    uint32_t word = 0;
+    e = cudaMemcpy(&word, workspace, sizeof word, cudaMemcpyDeviceToHost);
+    if (e != cudaSuccess) return fail(MHC_ERR_RUNTIME, "reading the error word: %s", cudaGetErrorString(e));
+    if (word != 0) return fail(MHC_ERR_RUNTIME, "device-side wait gave up (error word 0x%x)", word);
+  }
+  return MHC_OK;
+}
+
+mhc_status_t mhc_pre_set_profile_events(mhc_pre_t h, void* before, void* after) {
+  g_last_error[0] = 0;
+  if (!h) return fail(MHC_ERR_NULLPTR, "handle must be non-NULL");
+  h->ev_before = static_cast<cudaEvent_t>(before);
+  h->ev_after = static_cast<cudaEvent_t>(after);
+  return MHC_OK;
+}
+
+void mhc_pre_destroy(mhc_pre_t h) { delete h; }
+
+}  // extern "C"

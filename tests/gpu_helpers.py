@@ -1,0 +1,93 @@
+"""Shared helpers of the GPU parity tests: run the CUDA path through the C ABI
+and the oracle on the same seeded inputs, and compare within the stated
+tolerances.
+
+Tolerances (against the double-precision oracle):
+  * hPre, hPost, comb: max |err| <= 1e-4 (fp32 mode), <= 3e-3 (tf32 mode);
+  * y (bf16): |err| <= 2^-7 |ref| + 1e-3 elementwise;
+  * intermediates (fp32 mode): invRms rel 1e-5; hMix |err| <= 2e-4 (1 + |ref|)
+    -- fp32 accumulation over n*D products; sumOut rel 1e-4; normOut 1e-4.
+"""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+import oracle
+from mhc_hyper_connection_gb300 import MhcPre
+
+TOL = {0: 1e-4, 1: 3e-3}
+
+
+def run_cuda(case, stream=None, out=None, op=None):
+    op = op or MhcPre(case.n, case.D, alpha_len=case.alpha_len, num_iters=case.num_iters,
+                      norm_eps=case.norm_eps, hc_eps=case.hc_eps, impl_mode=case.impl_mode,
+                      need_backward=case.need_backward)
+    if out is None:
+        out = op.allocate(case.T, case.x.device)
+    op.run(case.x, case.phi, case.alpha, case.bias, out, gamma=case.gamma,
+           pre_mix=case.pre_mix, stream=stream)
+    st = op.status(out)
+    assert st == 0, f"device status {st}"
+    return op, out
+
+
+def x_bits(x: torch.Tensor) -> np.ndarray:
+    return x.detach().view(torch.int16).cpu().numpy().view(np.uint16)
+
+
+def run_oracle(case, tokens=None, hf32=False):
+    x = case.x if tokens is None else case.x[torch.as_tensor(tokens, device=case.x.device)]
+    pm = None
+    if case.pre_mix is not None:
+        pm = case.pre_mix if tokens is None else case.pre_mix[torch.as_tensor(tokens, device=case.pre_mix.device)]
+        pm = pm.cpu().numpy()
+    return oracle.run(x_bits(x), case.phi.cpu().numpy(), case.alpha.cpu().numpy(),
+                      case.bias.cpu().numpy(),
+                      None if case.gamma is None else case.gamma.cpu().numpy(), pm,
+                      num_iters=case.num_iters, norm_eps=case.norm_eps, hc_eps=case.hc_eps,
+                      hf32=hf32, backward=case.need_backward)
+
+
+def _sel(t, tokens, axis=0):
+    a = t.float().cpu().numpy() if isinstance(t, torch.Tensor) else t
+    if tokens is None:
+        return a
+    return np.take(a, tokens, axis=axis)
+
+
+def compare(case, out, ref, tokens=None, tol=None, check_intermediates=True):
+    """Assert the CUDA outputs match the oracle; returns a dict of max errors."""
+    tol = TOL[case.impl_mode] if tol is None else tol
+    errs = {}
+    n = case.n
+    gp = _sel(out["h_post"], tokens)
+    errs["h_post"] = float(np.abs(gp - ref.h_post).max())
+    if out.get("h_pre") is not None:
+        errs["h_pre"] = float(np.abs(_sel(out["h_pre"], tokens) - ref.h_pre).max())
+    if out.get("h_res") is not None:
+        errs["comb"] = float(np.abs(_sel(out["h_res"], tokens) - ref.h_res).max())
+    for k in ("h_post", "h_pre", "comb"):
+        if k in errs:
+            assert errs[k] <= tol, f"{case.name}: {k} max err {errs[k]:.3g} > {tol}"
+    y = _sel(out["y"], tokens).astype(np.float64)
+    bound = 2.0 ** -7 * np.abs(ref.y) + 1e-3
+    bad = np.abs(y - ref.y) > bound
+    errs["y_viol"] = int(bad.sum())
+    errs["y"] = float(np.abs(y - ref.y).max())
+    assert not bad.any(), (f"{case.name}: {bad.sum()} y elements outside 2^-7|ref|+1e-3, "
+                           f"max err {errs['y']:.3g}")
+    if case.need_backward and check_intermediates and case.impl_mode == 0:
+        ir = _sel(out["inv_rms"], tokens)
+        errs["inv_rms"] = float(np.abs(ir / ref.inv_rms - 1).max())
+        assert errs["inv_rms"] <= 1e-5
+        hm = _sel(out["h_mix"], tokens)
+        errs["h_mix"] = float((np.abs(hm - ref.h_mix) / (1 + np.abs(ref.h_mix))).max())
+        assert errs["h_mix"] <= 2e-4
+        if case.alpha_len == 3:
+            so = _sel(out["sum_out"], tokens, axis=1)
+            no = _sel(out["norm_out"], tokens, axis=1)
+            errs["sum_out"] = float((np.abs(so - ref.sum_out) / np.abs(ref.sum_out)).max())
+            errs["norm_out"] = float(np.abs(no - ref.norm_out).max())
+            assert errs["sum_out"] <= 1e-4 and errs["norm_out"] <= 1e-4, errs
+    return errs

@@ -1,0 +1,176 @@
+"""The C ABI without a GPU: the library loads, exports every function that
+include/mhc_pre.h declares, and rejects bad arguments on the host, with the
+status codes of the pages, before any CUDA call."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import mhc_hyper_connection_gb300 as mp
+from mhc_hyper_connection_gb300 import build as mbuild
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "mhc_pre.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    mbuild.build()
+    return mp.library()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(mhc_pre_[a-z_]+)\s*\(", text)))
+
+
+def test_header_declares_the_api():
+    names = declared_functions()
+    for need in ("mhc_pre_create", "mhc_pre_workspace_size", "mhc_pre_run", "mhc_pre_status",
+                 "mhc_pre_destroy", "mhc_pre_config_default", "mhc_pre_status_string",
+                 "mhc_pre_last_error"):
+        assert need in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), f"{name} declared in mhc_pre.h but not exported"
+
+
+def test_struct_layouts_match_header():
+    # Field order/sizes in the binding mirror the header (x86-64 and aarch64 LP64).
+    assert ctypes.sizeof(mp.MhcPreConfig) == 8 + 8 + 4 + 4 + 8 + 8 + 4 + 4
+    assert ctypes.sizeof(mp.MhcPreArgs) == 8 + 15 * 8 + 8
+
+
+def test_defaults(lib):
+    c = mp.mhc_pre_config_default()
+    assert (c.n, c.D, c.alpha_len, c.num_iters, c.impl_mode, c.need_backward) == (4, 0, 3, 20, 0, 0)
+    assert c.norm_eps == 1e-6 and c.hc_eps == 1e-6
+
+
+@pytest.mark.parametrize("field,value", [("n", 5), ("n", 2), ("D", 0), ("D", 24), ("D", 16400),
+                                         ("alpha_len", 1), ("num_iters", 0), ("impl_mode", 2),
+                                         ("impl_mode", -1), ("need_backward", 2)])
+def test_create_rejects_bad_config(lib, field, value):
+    c = mp.mhc_pre_config_default()
+    c.D = 256
+    setattr(c, field, value)
+    st, h = mp.mhc_pre_create(c)
+    assert st == mp.MHC_ERR_PARAM_INVALID and h is None
+    assert mp.last_error()
+
+
+def test_create_null(lib):
+    h = ctypes.c_void_p()
+    assert lib.mhc_pre_create(ctypes.byref(h), None) == mp.MHC_ERR_NULLPTR
+    assert lib.mhc_pre_create(None, None) == mp.MHC_ERR_NULLPTR
+
+
+def test_status_strings(lib):
+    assert mp.status_string(0) == "success"
+    assert "NULL" in mp.status_string(161001)
+    assert mp.status_string(361001)
+
+
+def _handle(**kw):
+    c = mp.mhc_pre_config_default()
+    c.D = kw.pop("D", 256)
+    for k, v in kw.items():
+        setattr(c, k, v)
+    st, h = mp.mhc_pre_create(c)
+    assert st == mp.MHC_OK
+    return h
+
+
+def test_workspace_size(lib):
+    h = _handle()
+    st, n0 = mp.mhc_pre_workspace_size(h, 0)
+    assert st == 0 and n0 == 0
+    st, n1 = mp.mhc_pre_workspace_size(h, 64)
+    # header + stacked planes: NP = 3*24 rounded to 80 rows of n*D bf16
+    assert st == 0 and n1 == 256 + 80 * 4 * 256 * 2
+    st, _ = mp.mhc_pre_workspace_size(h, -1)
+    assert st == mp.MHC_ERR_PARAM_INVALID
+    h2 = _handle(impl_mode=1)
+    assert mp.mhc_pre_workspace_size(h2, 64)[1] == 256 + 48 * 4 * 256 * 2
+    mp.mhc_pre_destroy(h)
+    mp.mhc_pre_destroy(h2)
+
+
+def _args(T=64, **over):
+    a = mp.MhcPreArgs()
+    fake = 1 << 20          # aligned, never dereferenced: validation fails first
+    a.T = T
+    for k in ("x", "phi", "alpha", "bias", "y", "h_post", "h_res"):
+        setattr(a, k, fake)
+    a.workspace = fake
+    a.workspace_bytes = 1 << 30
+    for k, v in over.items():
+        setattr(a, k, v)
+    return a
+
+
+@pytest.mark.parametrize("field", ["x", "phi", "alpha", "bias", "y", "h_post", "h_res"])
+def test_run_null_required(lib, field):
+    h = _handle()
+    assert mp.mhc_pre_run(h, _args(**{field: None})) == mp.MHC_ERR_NULLPTR
+    mp.mhc_pre_destroy(h)
+
+
+def test_run_two_gate_h_res_optional_and_no_sinkhorn_outputs(lib):
+    h = _handle(alpha_len=2, need_backward=1)
+    a = _args(h_res=None, h_pre=1 << 20, inv_rms=1 << 20, h_mix=1 << 20, sum_out=1 << 20)
+    assert mp.mhc_pre_run(h, a) == mp.MHC_ERR_PARAM_INVALID     # sum_out has no meaning here
+    mp.mhc_pre_destroy(h)
+
+
+def test_run_optional_group(lib):
+    h = _handle(need_backward=1)
+    full = dict(h_pre=1 << 20, inv_rms=1 << 20, h_mix=1 << 20, sum_out=1 << 20, norm_out=1 << 20)
+    for drop in full:
+        part = dict(full)
+        part[drop] = None
+        assert mp.mhc_pre_run(h, _args(**part)) == mp.MHC_ERR_NULLPTR, drop
+    mp.mhc_pre_destroy(h)
+    h = _handle(need_backward=0)
+    assert mp.mhc_pre_run(h, _args(inv_rms=1 << 20)) == mp.MHC_ERR_PARAM_INVALID
+    assert mp.mhc_pre_run(h, _args(pre_mix=1 << 20)) == mp.MHC_ERR_NULLPTR   # needs h_pre
+    mp.mhc_pre_destroy(h)
+
+
+def test_run_alignment_and_workspace(lib):
+    h = _handle()
+    assert mp.mhc_pre_run(h, _args(x=(1 << 20) + 8)) == mp.MHC_ERR_PARAM_INVALID
+    assert mp.mhc_pre_run(h, _args(y=(1 << 20) + 2)) == mp.MHC_ERR_PARAM_INVALID
+    assert mp.mhc_pre_run(h, _args(phi=(1 << 20) + 2)) == mp.MHC_ERR_PARAM_INVALID
+    assert mp.mhc_pre_run(h, _args(workspace_bytes=100)) == mp.MHC_ERR_PARAM_INVALID
+    assert mp.mhc_pre_run(h, _args(workspace=None)) == mp.MHC_ERR_NULLPTR
+    assert mp.mhc_pre_run(h, _args(workspace=(1 << 20) + 16)) == mp.MHC_ERR_PARAM_INVALID
+    assert mp.mhc_pre_run(h, _args(T=-1)) == mp.MHC_ERR_PARAM_INVALID
+    mp.mhc_pre_destroy(h)
+
+
+def test_run_empty_is_ok_without_launch(lib):
+    h = _handle()
+    assert mp.mhc_pre_run(h, _args(T=0, workspace=None, workspace_bytes=0)) == mp.MHC_OK
+    mp.mhc_pre_destroy(h)
+
+
+def test_run_without_gpu_fails_loudly(lib):
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    h = _handle()
+    assert mp.mhc_pre_run(h, _args()) == mp.MHC_ERR_RUNTIME
+    mp.mhc_pre_destroy(h)
+
+
+def test_binding_raises_when_library_missing(monkeypatch, tmp_path):
+    from mhc_hyper_connection_gb300 import _binding
+    monkeypatch.setattr(_binding, "_lib", None)
+    monkeypatch.setattr(_binding, "LIB_PATH", str(tmp_path / "absent.so"))
+    with pytest.raises(RuntimeError, match="missing"):
+        _binding.library()

@@ -1,0 +1,135 @@
+"""CUDA path vs the oracle on the same seeded inputs, through the C ABI.
+
+Small cases are compared element by element on every token; full-size
+workloads (the bench configuration included) on sampled tokens, plus
+properties that hold for every token at any size.
+"""
+import numpy as np
+import pytest
+import torch
+
+from gpu_helpers import compare, run_cuda, run_oracle
+from mhc_synth import make_case, sample_tokens
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    from mhc_hyper_connection_gb300 import build
+    build.build()
+
+
+def _full(case):
+    _, out = run_cuda(case)
+    torch.cuda.synchronize()
+    return out, compare(case, out, run_oracle(case))
+
+
+# ------------------------------------------------------------ workloads
+
+@pytest.mark.parametrize("mode", [0, 1])
+def test_tiny(cuda_device, mode):
+    _full(make_case("tiny", device=cuda_device, impl_mode=mode))
+
+
+@pytest.mark.parametrize("iters", [1, 2, 7])
+def test_tiny_iterations(cuda_device, iters):
+    _full(make_case("tiny", device=cuda_device, num_iters=iters, need_backward=True))
+
+
+def test_training_shaped_with_backward_outputs(cuda_device):
+    out, errs = _full(make_case("training", device=cuda_device))
+    assert errs["inv_rms"] <= 1e-5
+
+
+def test_decode_shaped_outliers(cuda_device):
+    _full(make_case("decode", device=cuda_device))
+
+
+@pytest.mark.parametrize("mode", [0, 1])
+def test_prefill_sampled(cuda_device, mode):
+    case = make_case("prefill", device=cuda_device, impl_mode=mode)
+    _, out = run_cuda(case)
+    torch.cuda.synchronize()
+    tok = sample_tokens(case.T, 160, seed=mode)
+    compare(case, out, run_oracle(case, tok), tokens=tok)
+    _every_token_properties(case, out)
+
+
+def test_generic_n8_pre_mix(cuda_device):
+    _full(make_case("generic_a", device=cuda_device))
+
+
+def test_generic_n8_two_gates(cuda_device):
+    out, _ = _full(make_case("generic_b", device=cuda_device))
+    assert torch.all(out["h_res"] == 0)
+
+
+def _every_token_properties(case, out):
+    """Hold for every token: column sums of comb are S/(S+eps) ~ 1, rows near
+    1, gates in range, everything finite."""
+    comb = out["h_res"]
+    assert torch.isfinite(comb).all() and torch.isfinite(out["y"].float()).all()
+    col = comb.sum(dim=1)
+    assert (col - 1).abs().max().item() < 1e-6 + 8 * 2 ** -24 * case.n
+    assert (comb.sum(dim=2) - 1).abs().max().item() < 1e-3
+    hp = out["h_post"]
+    assert hp.min().item() >= 0 and hp.max().item() <= 2 + 1e-6
+
+
+# ------------------------------------------------------------ edge cases
+
+@pytest.mark.parametrize("T", [1, 5, 127, 129, 300])
+def test_ragged_token_counts(cuda_device, T):
+    _full(make_case("tiny", device=cuda_device, T=T, need_backward=True))
+
+
+@pytest.mark.parametrize("D", [16, 48, 80, 208, 1040])
+def test_ragged_widths(cuda_device, D):
+    _full(make_case("tiny", device=cuda_device, T=130, D=D))
+
+
+@pytest.mark.parametrize("alpha_len", [2, 3])
+@pytest.mark.parametrize("n", [4, 6, 8])
+@pytest.mark.parametrize("mode", [0, 1])
+def test_streams_gates_modes(cuda_device, n, alpha_len, mode):
+    _full(make_case("tiny", device=cuda_device, T=200, n=n, D=320, alpha_len=alpha_len,
+                    impl_mode=mode, need_backward=True, gamma=True, pre_mix=(n == 6)))
+
+
+def test_tf32_mode_is_the_pages_hf32(cuda_device):
+    """Without gamma the tf32 mode multiplies exactly the operands the pages'
+    HF32 simulation keeps, so it meets the fp32 tolerance against that oracle."""
+    case = make_case("tiny", device=cuda_device, T=256, D=1024, impl_mode=1, need_backward=True)
+    _, out = run_cuda(case)
+    torch.cuda.synchronize()
+    compare(case, out, run_oracle(case, hf32=True), tol=1e-4)
+
+
+def test_empty_input(cuda_device):
+    case = make_case("tiny", device=cuda_device, T=0)
+    op, out = run_cuda(case)
+    assert out["y"].numel() == 0
+
+
+def test_deterministic(cuda_device):
+    case = make_case("training", device=cuda_device, T=1000)
+    op, a = run_cuda(case)
+    _, b = run_cuda(case, op=op)
+    torch.cuda.synchronize()
+    for k in ("y", "h_post", "h_res", "h_pre", "inv_rms", "h_mix", "sum_out", "norm_out"):
+        assert torch.equal(a[k], b[k]), k
+
+
+def test_stream_and_reuse(cuda_device):
+    """Runs on a side stream, reusing one output set for two different inputs."""
+    s = torch.cuda.Stream()
+    c1 = make_case("tiny", device=cuda_device, seed=1)
+    c2 = make_case("tiny", device=cuda_device, seed=2)
+    op, out = run_cuda(c1, stream=s)
+    torch.cuda.synchronize()
+    compare(c1, out, run_oracle(c1))
+    run_cuda(c2, stream=s, out=out, op=op)
+    torch.cuda.synchronize()
+    compare(c2, out, run_oracle(c2))
