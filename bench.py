@@ -180,26 +180,24 @@ def recorded_traffic(T):
 # ----------------------------------------------------------------- CPU oracle
 
 def oracle_rate(case, budget_s: float, max_tokens: int):
-    """Tokens/s of the oracle on a bounded sample of the workload's tokens."""
+    """Tokens/s of the oracle, on all host cores, over passes of up to
+    max_tokens of the workload's tokens until about budget_s has elapsed."""
     import numpy as np
     import torch
     import oracle
     oracle.build()
     threads = os.cpu_count() or 1
     phi, alpha, bias = case.phi.cpu().numpy(), case.alpha.cpu().numpy(), case.bias.cpu().numpy()
-
-    def run(count, start=0):
-        x = case.x[start:start + count].view(torch.int16).cpu().numpy().view(np.uint16)
+    count = max(1, min(max_tokens, case.T))
+    x = case.x[:count].view(torch.int16).cpu().numpy().view(np.uint16)
+    done, t_total, passes = 0, 0.0, 0
+    while passes == 0 or t_total < budget_s:
         t0 = time.perf_counter()
         oracle.run(x, phi, alpha, bias, num_iters=case.num_iters, backward=False, threads=threads)
-        return time.perf_counter() - t0
-
-    calib = max(threads, 16)
-    dt = run(calib)
-    n = int(min(max_tokens, max(calib, budget_s * calib / max(dt, 1e-6))))
-    n = max(threads, (n // threads) * threads)
-    dt = run(n, start=calib)
-    return n / dt, threads, n, dt
+        t_total += time.perf_counter() - t0
+        done += count
+        passes += 1
+    return done / t_total, threads, f"{passes} pass(es) over {count} tokens", t_total
 
 
 # ----------------------------------------------------------------- main
@@ -240,20 +238,23 @@ def main():
         if rank != 0:
             return 0
         case = make_case("prefill", device=device, T=T, impl_mode=args.mode)
-        total_s = 60.0
-        rate, threads, sample, dt = oracle_rate(case, total_s / (args.steps + args.warmup), 4096)
+        # bounded: each step is a sample sized so the whole run takes about a minute
+        per_step = 60.0 / (args.steps + args.warmup)
+        probe, _, _, _ = oracle_rate(case, 0.0, 256)
+        tokens = int(max(1, min(case.T, probe * per_step)))
+        rate, threads, sample, dt = oracle_rate(case, 60.0 * args.steps / (args.steps + args.warmup), tokens)
         line = {"impl": "reference", "metric": METRIC, "value": rate, "unit": "tokens/s",
                 "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
                 "ms_per_step": 1e3 * T / rate, "higher_is_better": True, "scaling": "weak",
                 "vs_baseline": None, "dtype": "f64", "data": "synthetic", "config": cfg,
                 "cpu_baseline": {"value": rate, "unit": "tokens/s", "cores": threads, "kind": "oracle",
-                                 "sample": f"{sample} tokens of the workload per timed pass ({dt:.1f} s)"},
+                                 "sample": f"{sample} of the prefill workload ({dt:.1f} s)"},
                 "e2e": {"value": rate, "unit": "tokens/s", "h2d_bytes_per_step": 0,
                         "d2h_bytes_per_step": 0}}
         print(json.dumps(line))
         return 0
 
-    from mhc_hyper_connection_gb300 import MhcPre, mhc_pre_set_profile_events
+    from mhc_hyper_connection_gb300 import MhcPre, mhc_pre_last_launch, mhc_pre_set_profile_events
     from mhc_hyper_connection_gb300 import build as mbuild
     mbuild.build()
     case = make_case("prefill", device=device, T=T, impl_mode=args.mode, seed=rank)
@@ -301,6 +302,7 @@ def main():
     clocks.stop()
     if op.status(out) != 0:
         raise RuntimeError("device-side error during the timed steps")
+    cfg["launch"] = mhc_pre_last_launch(op.handle)[1]
     elapsed = e0.elapsed_time(e1) / 1e3
     kern = sum(a.elapsed_time(b) for a, b in ev_k) / K / 1e3
     elapsed_max = max_over_ranks(elapsed, world, device)
@@ -352,9 +354,9 @@ def main():
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        rate, threads, sample, dt = oracle_rate(case, 15.0, 4096)
+        rate, threads, sample, dt = oracle_rate(case, 10.0, case.T)
         cpu = {"value": rate, "unit": "tokens/s", "cores": threads, "kind": "oracle",
-               "sample": f"{sample} tokens of the prefill workload ({dt:.1f} s, double precision)"}
+               "sample": f"{sample} of the prefill workload ({dt:.1f} s, double precision)"}
 
     if rank == 0:
         line = {"metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,

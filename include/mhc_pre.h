@@ -137,6 +137,12 @@ MHC_API mhc_status_t mhc_pre_status(mhc_pre_t h, const void *workspace, void *st
  * are borrowed, not owned.  MHC_ERR_NULLPTR if h is NULL. */
 MHC_API mhc_status_t mhc_pre_set_profile_events(mhc_pre_t h, void *before, void *after);
 
+/* Launch shape chosen by the last successful mhc_pre_run on this handle:
+ * CTAs per cluster, grid size in CTAs, projection-ring and y-ring depths.
+ * All zero before the first run.  Any output pointer may be NULL. */
+MHC_API mhc_status_t mhc_pre_last_launch(mhc_pre_t h, int32_t *cluster, int32_t *grid,
+                                         int32_t *stages, int32_t *ystages);
+
 /* Release the handle (NULL is ignored). */
 MHC_API void mhc_pre_destroy(mhc_pre_t h);
 

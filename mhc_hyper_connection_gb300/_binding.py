@@ -72,6 +72,9 @@ def library() -> ctypes.CDLL:
             lib.mhc_pre_status.restype = ctypes.c_int32
             lib.mhc_pre_set_profile_events.argtypes = [_P, _P, _P]
             lib.mhc_pre_set_profile_events.restype = ctypes.c_int32
+            I32P = ctypes.POINTER(ctypes.c_int32)
+            lib.mhc_pre_last_launch.argtypes = [_P, I32P, I32P, I32P, I32P]
+            lib.mhc_pre_last_launch.restype = ctypes.c_int32
             lib.mhc_pre_destroy.argtypes = [_P]
             lib.mhc_pre_destroy.restype = None
             lib.mhc_pre_status_string.argtypes = [ctypes.c_int32]
@@ -113,6 +116,13 @@ def mhc_pre_status(handle, workspace: int = 0, stream: int = 0) -> int:
 
 def mhc_pre_set_profile_events(handle, before: int = 0, after: int = 0) -> int:
     return library().mhc_pre_set_profile_events(handle, _P(before or None), _P(after or None))
+
+
+def mhc_pre_last_launch(handle):
+    """(status, {cluster, grid, stages, ystages}) of the last run on this handle."""
+    v = [ctypes.c_int32(0) for _ in range(4)]
+    st = library().mhc_pre_last_launch(handle, *[ctypes.byref(x) for x in v])
+    return st, dict(zip(("cluster", "grid", "stages", "ystages"), (x.value for x in v)))
 
 
 def mhc_pre_destroy(handle) -> None:

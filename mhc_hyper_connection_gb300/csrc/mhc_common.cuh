@@ -41,24 +41,60 @@ struct EpiParams {
   const float* alpha;          // device alpha (read by kernels)
 };
 
-__device__ __forceinline__ float sigmoidf_(float z) { return 1.0f / (1.0f + expf(-z)); }
+__device__ __forceinline__ float sigmoidf_(float z) { return __fdividef(1.0f, 1.0f + expf(-z)); }
 
-// Gates and Sinkhorn for one token held by one thread.  mix[RR] is the
-// projection before the RMS scale (hMix), ssq the sum of squares over the
-// n*D elements.  Writes every per-token output when `write` is set and fills
-// coef[NS] with the weights of y (pre_mix row or hPre).  RR = NS*NS + 2*NS
-// selects the three-gate form, RR = 2*NS the two-gate form (no Sinkhorn).
+// Sum of v[0..N) as a balanced tree (shorter dependency chain than a scan).
+template <int N>
+__device__ __forceinline__ float tree_sum(const float* v) {
+  if constexpr (N == 1) {
+    return v[0];
+  } else {
+    return tree_sum<N / 2>(v) + tree_sum<N - N / 2>(v + N / 2);
+  }
+}
+
+// One Sinkhorn column step: every column divided by (its sum + eps).
+template <int NS>
+__device__ __forceinline__ void sinkhorn_col(float* P, float eps, bool wb, float* sums) {
+#pragma unroll
+  for (int j = 0; j < NS; ++j) {
+    float c[NS];
+#pragma unroll
+    for (int i = 0; i < NS; ++i) c[i] = P[i * NS + j];
+    const float s = tree_sum<NS>(c) + eps;
+    const float rs = __fdividef(1.0f, s);
+#pragma unroll
+    for (int i = 0; i < NS; ++i) P[i * NS + j] *= rs;
+    if (wb) sums[j] = s;
+  }
+}
+// One Sinkhorn row step: every row divided by (its sum + eps).
+template <int NS>
+__device__ __forceinline__ void sinkhorn_row(float* P, float eps, bool wb, float* sums) {
+#pragma unroll
+  for (int i = 0; i < NS; ++i) {
+    const float s = tree_sum<NS>(P + i * NS) + eps;
+    const float rs = __fdividef(1.0f, s);
+#pragma unroll
+    for (int j = 0; j < NS; ++j) P[i * NS + j] *= rs;
+    if (wb) sums[i] = s;
+  }
+}
+
+// Per-token gates ("aclnnMhcPreV2 算子接口全解析" §三): scales the projection
+// by the RMS reciprocal, writes invRms / hMix / hPre / hPost when `write`,
+// returns the weights of y in coef (pre_mix row when given, else hPre) and
+// the RMS reciprocal.  RR = NS*NS + 2*NS is the three-gate form, RR = 2*NS
+// the two-gate form (hPost + hcEps, no residual path).
 template <int NS, int RR>
-__device__ __forceinline__ void token_epilogue(const EpiParams& p, int t, const float (&mix)[RR],
-                                               float ssq, bool write, float (&coef)[NS]) {
-  constexpr int NN = NS * NS;
-  constexpr bool kThree = (RR == NN + 2 * NS);
+__device__ __forceinline__ float token_gates(const EpiParams& p, int t, const float (&mix)[RR], float ssq,
+                                             bool write, float (&coef)[NS]) {
+  constexpr bool kThree = (RR == NS * NS + 2 * NS);
   static_assert(kThree || RR == 2 * NS, "R must be n*n+2n or 2n");
   const float K = (float)(NS * p.D);
-  const float inv_rms = 1.0f / sqrtf(ssq / K + p.norm_eps);
+  const float inv_rms = __frsqrt_rn(ssq / K + p.norm_eps);
   const float hc_eps = p.hc_eps;
   const float a0 = __ldg(p.alpha), a1 = __ldg(p.alpha + 1);
-
   if (write) {
     if (p.inv_rms) p.inv_rms[t] = inv_rms;
     if (p.h_mix) {
@@ -68,7 +104,7 @@ __device__ __forceinline__ void token_epilogue(const EpiParams& p, int t, const 
   }
 #pragma unroll
   for (int i = 0; i < NS; ++i) {
-    float pre = sigmoidf_(a0 * (mix[i] * inv_rms) + __ldg(p.bias + i)) + hc_eps;
+    const float pre = sigmoidf_(a0 * (mix[i] * inv_rms) + __ldg(p.bias + i)) + hc_eps;
     float post = 2.0f * sigmoidf_(a1 * (mix[NS + i] * inv_rms) + __ldg(p.bias + NS + i));
     if (!kThree) post += hc_eps;
     coef[i] = pre;
@@ -81,74 +117,68 @@ __device__ __forceinline__ void token_epilogue(const EpiParams& p, int t, const 
 #pragma unroll
     for (int i = 0; i < NS; ++i) coef[i] = __ldg(p.pre_mix + (size_t)t * NS + i);
   }
+  return inv_rms;
+}
 
+// Residual mix of one token ("aclnnMhcPreSinkhorn 接口与 MhcPreSinkhorn 实现
+// 剖析" §3.2): logits H = alpha2 * pRes + bias2 (row-major n x n), softmax
+// over each row + eps, a column step, then (row, column) x (numIters - 1);
+// each step divides by (sum + eps).  Writes comb and, when sum_out is set,
+// every step's sums and matrices.  Two-gate form: comb is zero.
+template <int NS, int RR>
+__device__ __forceinline__ void token_sinkhorn(const EpiParams& p, int t, const float (&mix)[RR],
+                                               float inv_rms, bool write) {
+  constexpr int NN = NS * NS;
+  constexpr bool kThree = (RR == NN + 2 * NS);
   if constexpr (!kThree) {
     if (write && p.h_res) {
 #pragma unroll
       for (int e = 0; e < NN; ++e) p.h_res[(size_t)t * NN + e] = 0.0f;
     }
-    return;
   } else {
+    const float hc_eps = p.hc_eps;
     const float a2 = __ldg(p.alpha + 2);
     float P[NN];
 #pragma unroll
     for (int e = 0; e < NN; ++e)
       P[e] = a2 * (mix[2 * NS + e] * inv_rms) + __ldg(p.bias + 2 * NS + e);
-
     const size_t Tn = (size_t)p.T * NS, Tnn = (size_t)p.T * NN;
     const bool wb = write && (p.sum_out != nullptr);
-    // Step 0: softmax over each row (row maximum subtracted), then + eps.
+    float* sums = wb ? p.sum_out : nullptr;
 #pragma unroll
     for (int i = 0; i < NS; ++i) {
       float m = P[i * NS];
 #pragma unroll
       for (int j = 1; j < NS; ++j) m = fmaxf(m, P[i * NS + j]);
-      float s = 0.0f;
+      float e[NS];
 #pragma unroll
-      for (int j = 0; j < NS; ++j) {
-        P[i * NS + j] = expf(P[i * NS + j] - m);
-        s += P[i * NS + j];
-      }
-      const float rs = 1.0f / s;
+      for (int j = 0; j < NS; ++j) e[j] = expf(P[i * NS + j] - m);
+      const float s = tree_sum<NS>(e);
+      const float rs = __fdividef(1.0f, s);
 #pragma unroll
-      for (int j = 0; j < NS; ++j) P[i * NS + j] = fmaf(P[i * NS + j], rs, hc_eps);
-      if (wb) p.sum_out[(size_t)t * NS + i] = s;
+      for (int j = 0; j < NS; ++j) P[i * NS + j] = fmaf(e[j], rs, hc_eps);
+      if (wb) sums[(size_t)t * NS + i] = s;
     }
     if (wb) {
 #pragma unroll
       for (int e = 0; e < NN; ++e) p.norm_out[(size_t)t * NN + e] = P[e];
     }
-    // Steps 1 .. 2I-1: odd steps divide columns, even steps rows, by sum + eps.
-    const int steps = 2 * p.num_iters;
-    for (int k = 1; k < steps; ++k) {
-      if (k & 1) {
+    sinkhorn_col<NS>(P, hc_eps, wb, wb ? sums + Tn + (size_t)t * NS : nullptr);
+    if (wb) {
 #pragma unroll
-        for (int j = 0; j < NS; ++j) {
-          float s = 0.0f;
-#pragma unroll
-          for (int i = 0; i < NS; ++i) s += P[i * NS + j];
-          s += hc_eps;
-          const float rs = 1.0f / s;
-#pragma unroll
-          for (int i = 0; i < NS; ++i) P[i * NS + j] *= rs;
-          if (wb) p.sum_out[k * Tn + (size_t)t * NS + j] = s;
-        }
-      } else {
-#pragma unroll
-        for (int i = 0; i < NS; ++i) {
-          float s = 0.0f;
-#pragma unroll
-          for (int j = 0; j < NS; ++j) s += P[i * NS + j];
-          s += hc_eps;
-          const float rs = 1.0f / s;
-#pragma unroll
-          for (int j = 0; j < NS; ++j) P[i * NS + j] *= rs;
-          if (wb) p.sum_out[k * Tn + (size_t)t * NS + i] = s;
-        }
-      }
+      for (int e = 0; e < NN; ++e) p.norm_out[Tnn + (size_t)t * NN + e] = P[e];
+    }
+    for (int it = 1; it < p.num_iters; ++it) {
+      const int k = 2 * it;
+      sinkhorn_row<NS>(P, hc_eps, wb, wb ? sums + k * Tn + (size_t)t * NS : nullptr);
       if (wb) {
 #pragma unroll
         for (int e = 0; e < NN; ++e) p.norm_out[k * Tnn + (size_t)t * NN + e] = P[e];
+      }
+      sinkhorn_col<NS>(P, hc_eps, wb, wb ? sums + (k + 1) * Tn + (size_t)t * NS : nullptr);
+      if (wb) {
+#pragma unroll
+        for (int e = 0; e < NN; ++e) p.norm_out[(k + 1) * Tnn + (size_t)t * NN + e] = P[e];
       }
     }
     if (write && p.h_res) {
@@ -156,32 +186,6 @@ __device__ __forceinline__ void token_epilogue(const EpiParams& p, int t, const 
       for (int e = 0; e < NN; ++e) p.h_res[(size_t)t * NN + e] = P[e];
     }
   }
-}
-
-// y[t, d0 .. d0+8) = bf16(sum_i coef[i] * x[t, i, d0 .. d0+8)), one 16-byte
-// vector per stream, accumulated in fp32 in stream order.
-template <int NS>
-__device__ __forceinline__ void weighted_sum8(const __nv_bfloat16* __restrict__ x_tok, int D, int d0,
-                                              const float* coef, __nv_bfloat16* __restrict__ y_dst) {
-  float acc[8];
-#pragma unroll
-  for (int e = 0; e < 8; ++e) acc[e] = 0.0f;
-#pragma unroll
-  for (int i = 0; i < NS; ++i) {
-    uint4 v = __ldg(reinterpret_cast<const uint4*>(x_tok + (size_t)i * D + d0));
-    const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&v);
-#pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      float2 f = __bfloat1622float2(h[q]);
-      acc[2 * q] = fmaf(coef[i], f.x, acc[2 * q]);
-      acc[2 * q + 1] = fmaf(coef[i], f.y, acc[2 * q + 1]);
-    }
-  }
-  uint4 out;
-  __nv_bfloat162* o = reinterpret_cast<__nv_bfloat162*>(&out);
-#pragma unroll
-  for (int q = 0; q < 4; ++q) o[q] = __floats2bfloat162_rn(acc[2 * q], acc[2 * q + 1]);
-  *reinterpret_cast<uint4*>(y_dst + d0) = out;
 }
 
 // ---------------------------------------------------------------------------
@@ -199,28 +203,70 @@ struct PlaneParams {
 
 cudaError_t launch_prepare_planes(const PlaneParams& pp, cudaStream_t s);
 
+constexpr int kMmaM = 128;         // rows of one tcgen05.mma (TMEM lanes)
+constexpr int kTileT = 64;         // tokens per tile: MMA rows 0..63 (rows 64..127 unused)
+// x slot of one ring stage: the 64-token box (8 KB).  The 128-row MMA
+// operand starting there runs 8 KB into the next slot (or the first phi
+// slot after the last one); those rows only feed accumulator lanes 64..127,
+// which are never read.
+constexpr int kABytes = kTileT * 128;
+constexpr int kChunkK = 64;        // bf16 elements per 128-byte swizzle row
+constexpr int kThreads = 384;      // 12 warps: TMA, MMA, 2 sum-of-squares, 2 publish, 2 gates, 4 y
+constexpr int kMaxStages = 8;      // ring depth limit (barrier arrays)
+constexpr int kCoefBufs = 3;       // y-weight buffers between the epilogue and the y warps
+constexpr size_t kTailBytes = 512; // barriers and flags
+
+// Tokens per box of the y re-read ring: 64 columns x n streams x this many
+// tokens is 16 KB for n = 4 and n = 8, 12 KB for n = 6.
+__host__ __device__ constexpr int y_box_tokens(int n) { return n == 4 ? 32 : 16; }
+// Floats per published partial (R sums + the sum of squares), padded to 16 bytes.
+__host__ __device__ constexpr int partial_stride(int R) { return ((R + 1 + 3) / 4) * 4; }
+
+// Byte offsets of the forward kernel's shared-memory regions (after the
+// base is rounded up to 1024); `total` includes that rounding slack.
+struct SmemLayout {
+  size_t a, b, y, part, ssq, coef, tail, total;
+};
+__host__ __device__ inline SmemLayout smem_layout(int n, int R, int NP, int stages, int ystages) {
+  SmemLayout L;
+  size_t o = 0;
+  L.a = o;    o += (size_t)stages * kABytes;
+  L.b = o;    o += (size_t)stages * NP * 128;
+  L.y = o;    o += (size_t)ystages * kChunkK * 2 * n * y_box_tokens(n);
+  o = (o + 15) & ~size_t(15);
+  L.part = o; o += 2 * (size_t)kTileT * partial_stride(R) * 4;
+  L.ssq = o;  o += 2 * (size_t)kTileT * 4;
+  L.coef = o; o += (size_t)kCoefBufs * kTileT * n * 4;
+  o = (o + 15) & ~size_t(15);
+  L.tail = o; o += kTailBytes;
+  L.total = o + 1024;
+  return L;
+}
+
+struct Geometry {
+  int T, D;
+  int num_tiles, nd;           // token tiles; 64-wide d-chunks per stream
+  int cluster, stages, ystages;
+};
+
 struct TcLaunch {
   EpiParams epi;
-  const void* x;           // bf16 [T, n, D] (for the y pass)
-  CUtensorMap tmap_x;      // 3-D: (D, n, T), box (64, 1, 128), 128B swizzle
-  CUtensorMap tmap_w;      // 3-D: (D, n, NP), box (64, 1, NP), 128B swizzle
+  CUtensorMap tmap_x;      // 3-D (D, n, T), box (64, 1, 128), 128B swizzle: projection operand
+  CUtensorMap tmap_w;      // 3-D (D, n, NP), box (64, 1, NP), 128B swizzle: phi planes
+  CUtensorMap tmap_y;      // 3-D (D, n, T), box (64, n, TY), no swizzle: y re-read
   int NP, P;
   int cluster;             // CTAs per token tile (split over d-chunks)
   int grid;                // CTAs (multiple of cluster)
-  int stages;
+  int stages, ystages;
   size_t smem_bytes;
   uint32_t* err_word;
 };
 
 // Resolved by the kernel translation unit for the given (n, R, P).
 cudaError_t launch_tc_forward(const TcLaunch& L, cudaStream_t s);
-// Largest dynamic shared memory per CTA the kernel for this shape may use and
-// the number of clusters of the given size that fit at once (0: unsupported).
+// Clusters of the given size that fit on the device at once (0: unsupported).
 cudaError_t tc_forward_occupancy(int n, int R, int P, size_t smem_bytes, int cluster,
                                  int* max_clusters);
-
-constexpr int kTileM = 128;        // tokens per MMA tile (TMEM lanes)
-constexpr int kChunkK = 64;        // bf16 elements per 128-byte swizzle row
-constexpr int kThreads = 256;      // 8 warps: TMA, MMA, 2 x sum-of-squares, 4 x epilogue
+int tc_np(int R, int P);
 
 }  // namespace mhc

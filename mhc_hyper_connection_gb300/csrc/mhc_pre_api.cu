@@ -14,16 +14,13 @@
 #include "mhc_common.cuh"
 #include "../../include/mhc_pre.h"
 
-namespace mhc {
-int tc_np(int R, int P);
-}
-
 struct mhc_pre_s {
   mhc_pre_config cfg;
   int R;        // projection rows
   int P;        // precision planes (3: fp32, 2: tf32)
   int NP;       // MMA N = P*R rounded up to 16
   cudaEvent_t ev_before = nullptr, ev_after = nullptr;   // optional timing hooks
+  int last_cluster = 0, last_grid = 0, last_stages = 0, last_ystages = 0;   // last launch shape
 };
 
 namespace {
@@ -57,18 +54,19 @@ EncodeTiledFn encode_fn() {
   return fn;
 }
 
-// 3-D bf16 map over [dim2][dim1][dim0] (dim0 contiguous), box (64, 1, box2),
-// 128-byte swizzle, zero fill outside the tensor.
+// 3-D bf16 map over [dim2][dim1][dim0] (dim0 contiguous), box (64, box1,
+// box2), zero fill outside the tensor.
 bool encode_3d(CUtensorMap* map, const void* base, uint64_t dim0, uint64_t dim1, uint64_t dim2,
-               uint32_t box2) {
+               uint32_t box1, uint32_t box2, bool swizzle128) {
   EncodeTiledFn fn = encode_fn();
   if (!fn) return false;
   cuuint64_t dims[3] = {dim0, dim1, dim2};
   cuuint64_t strides[2] = {dim0 * 2, dim0 * dim1 * 2};
-  cuuint32_t box[3] = {(cuuint32_t)mhc::kChunkK, 1, box2};
+  cuuint32_t box[3] = {(cuuint32_t)mhc::kChunkK, box1, box2};
   cuuint32_t estr[3] = {1, 1, 1};
   CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
-                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE,
+                  swizzle128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
 }
@@ -110,17 +108,6 @@ int env_int(const char* name, int dflt) {
   const char* v = getenv(name);
   if (!v || !*v) return dflt;
   return atoi(v);
-}
-
-// Shared-memory bytes of the tensor-core kernel for `stages` pipeline stages.
-size_t tc_smem_bytes(int n, int R, int NP, int stages) {
-  size_t b = 1024;                                   // alignment slack
-  b += (size_t)stages * (mhc::kTileM * 128 + (size_t)NP * 128);
-  b += (size_t)mhc::kTileM * (R + 1) * 4;            // partial sums
-  b += 2 * (size_t)mhc::kTileM * 4;                  // sums of squares
-  b += 2 * (size_t)mhc::kTileM * n * 4;              // y weights
-  b += 16 + 256;                                     // barriers, flags
-  return b;
 }
 
 }  // namespace
@@ -265,21 +252,35 @@ mhc_status_t mhc_pre_run(mhc_pre_t h, const mhc_pre_args* a, void* stream) {
   e.h_mix = a->h_mix;
   e.sum_out = a->sum_out;
   e.norm_out = a->norm_out;
-  L.x = a->x;
   L.NP = NP;
   L.P = h->P;
   L.err_word = err;
-  if (!encode_3d(&L.tmap_x, a->x, (uint64_t)D, (uint64_t)n, (uint64_t)T, mhc::kTileM) ||
-      !encode_3d(&L.tmap_w, planes, (uint64_t)D, (uint64_t)n, (uint64_t)NP, (uint32_t)NP))
+  if (!encode_3d(&L.tmap_x, a->x, (uint64_t)D, (uint64_t)n, (uint64_t)T, 1, mhc::kTileT, true) ||
+      !encode_3d(&L.tmap_w, planes, (uint64_t)D, (uint64_t)n, (uint64_t)NP, 1, (uint32_t)NP, true) ||
+      !encode_3d(&L.tmap_y, a->x, (uint64_t)D, (uint64_t)n, (uint64_t)T, (uint32_t)n,
+                 (uint32_t)mhc::y_box_tokens(n), false))
     return fail(MHC_ERR_RUNTIME, "tensor map encoding failed");
 
+  // Ring depths: the projection ring carries x (8 KB) plus phi planes per
+  // stage from HBM/L2 and wants the most bytes in flight; the y ring
+  // re-reads from L2 and needs a few boxes.  Take the deepest projection
+  // ring beside a y ring of `want_y` boxes, shrinking the y ring to 2 last.
   const int nd = (D + mhc::kChunkK - 1) / mhc::kChunkK;
-  const int num_tiles = (int)((T + mhc::kTileM - 1) / mhc::kTileM);
-  int stages = env_int("MHC_PRE_STAGES", 8);
+  const int num_tiles = (int)((T + mhc::kTileT - 1) / mhc::kTileT);
   const size_t budget = di.max_smem;
-  while (stages > 2 && tc_smem_bytes(n, R, NP, stages) > budget) --stages;
-  const size_t smem = tc_smem_bytes(n, R, NP, stages);
-  if (smem > budget) return fail(MHC_ERR_RUNTIME, "shape needs %zu bytes of shared memory", smem);
+  int max_stages = env_int("MHC_PRE_STAGES", mhc::kMaxStages);
+  if (max_stages > mhc::kMaxStages) max_stages = mhc::kMaxStages;
+  int want_y = env_int("MHC_PRE_YSTAGES", 3);
+  if (want_y > mhc::kMaxStages) want_y = mhc::kMaxStages;
+  int stages = 0, ystages = 0;
+  for (int min_st : {6, 4, 2}) {
+    for (int ys = want_y; ys >= 2 && !stages; --ys)
+      for (int st = max_stages; st >= min_st; --st)
+        if (mhc::smem_layout(n, R, NP, st, ys).total <= budget) { stages = st; ystages = ys; break; }
+    if (stages) break;
+  }
+  if (!stages) return fail(MHC_ERR_RUNTIME, "shape does not fit in shared memory");
+  const size_t smem = mhc::smem_layout(n, R, NP, stages, ystages).total;
 
   int want = env_int("MHC_PRE_CLUSTER", 16);
   int cluster = 1;
@@ -298,7 +299,12 @@ mhc_status_t mhc_pre_run(mhc_pre_t h, const mhc_pre_args* a, void* stream) {
   L.cluster = cluster;
   L.grid = (num_tiles < max_clusters ? num_tiles : max_clusters) * cluster;
   L.stages = stages;
+  L.ystages = ystages;
   L.smem_bytes = smem;
+  h->last_cluster = cluster;
+  h->last_grid = L.grid;
+  h->last_stages = stages;
+  h->last_ystages = ystages;
   if (h->ev_before && cudaEventRecord(h->ev_before, s) != cudaSuccess)
     return fail(MHC_ERR_RUNTIME, "recording the timing event failed");
   if (mhc::launch_tc_forward(L, s) != cudaSuccess)
@@ -328,6 +334,17 @@ mhc_status_t mhc_pre_set_profile_events(mhc_pre_t h, void* before, void* after) 
   if (!h) return fail(MHC_ERR_NULLPTR, "handle must be non-NULL");
   h->ev_before = static_cast<cudaEvent_t>(before);
   h->ev_after = static_cast<cudaEvent_t>(after);
+  return MHC_OK;
+}
+
+mhc_status_t mhc_pre_last_launch(mhc_pre_t h, int32_t* cluster, int32_t* grid, int32_t* stages,
+                                 int32_t* ystages) {
+  g_last_error[0] = 0;
+  if (!h) return fail(MHC_ERR_NULLPTR, "handle must be non-NULL");
+  if (cluster) *cluster = h->last_cluster;
+  if (grid) *grid = h->last_grid;
+  if (stages) *stages = h->last_stages;
+  if (ystages) *ystages = h->last_ystages;
   return MHC_OK;
 }
 

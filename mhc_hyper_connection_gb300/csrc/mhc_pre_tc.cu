@@ -67,6 +67,18 @@ __device__ __forceinline__ bool mbar_test(uint64_t* bar, uint32_t parity) {
       : "memory");
   return ok != 0;
 }
+// Non-blocking probe (test_wait never suspends the thread), for polling loops.
+__device__ __forceinline__ bool mbar_poll(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
 __device__ __forceinline__ bool mbar_test_cluster(uint64_t* bar, uint32_t parity) {
   uint32_t ok;
   asm volatile(
@@ -103,13 +115,30 @@ __device__ __noinline__ bool wait_bar(uint64_t* bar, uint32_t parity, const Ctl&
   }
 }
 
-__device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* map, uint64_t* bar, int c0,
-                                            int c1, int c2) {
+__device__ __forceinline__ void tma_load_3d_hint(void* dst, const CUtensorMap* map, uint64_t* bar, int c0,
+                                                 int c1, int c2, uint64_t policy) {
   asm volatile(
-      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-      " [%0], [%1, {%3, %4, %5}], [%2];" ::"r"(smem_u32(dst)),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(c0), "r"(c1), "r"(c2)
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint"
+      " [%0], [%1, {%3, %4, %5}], [%2], %6;" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(c0), "r"(c1), "r"(c2), "l"(policy)
       : "memory");
+}
+// L2 policies: keep x resident between its first read and its re-read for y,
+// drop it (and the y stream) as soon as the re-read is done.
+__device__ __forceinline__ uint64_t policy_evict_last() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+__device__ __forceinline__ uint64_t policy_evict_first() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+__device__ __forceinline__ void st_global_v4_hint(void* ptr, uint4 v, uint64_t policy) {
+  asm volatile("st.global.L2::cache_hint.v4.b32 [%0], {%1, %2, %3, %4}, %5;" ::"l"(ptr), "r"(v.x), "r"(v.y),
+               "r"(v.z), "r"(v.w), "l"(policy)
+               : "memory");
 }
 __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap* map) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
@@ -172,16 +201,14 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
   for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
 }
 
-__device__ __forceinline__ float ld_dsmem_f32(const float* local, uint32_t rank) {
-  float v;
+// 16-byte store to the same shared-memory offset in cluster member `rank`.
+__device__ __forceinline__ void st_dsmem_v4(float* local, uint32_t rank, float4 v) {
   asm volatile(
       "{\n\t.reg .b32 ra;\n\t"
-      "mapa.shared::cluster.u32 ra, %1, %2;\n\t"
-      "ld.shared::cluster.f32 %0, [ra];\n\t}"
-      : "=f"(v)
-      : "r"(smem_u32(local)), "r"(rank)
+      "mapa.shared::cluster.u32 ra, %0, %1;\n\t"
+      "st.shared::cluster.v4.f32 [ra], {%2, %3, %4, %5};\n\t}" ::"r"(smem_u32(local)),
+      "r"(rank), "f"(v.x), "f"(v.y), "f"(v.z), "f"(v.w)
       : "memory");
-  return v;
 }
 __device__ __forceinline__ void st_dsmem_f32(float* local, uint32_t rank, float v) {
   asm volatile(
@@ -191,6 +218,7 @@ __device__ __forceinline__ void st_dsmem_f32(float* local, uint32_t rank, float 
       "r"(rank), "f"(v)
       : "memory");
 }
+
 __device__ __forceinline__ uint32_t cluster_rank() {
   uint32_t r;
   asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
@@ -200,79 +228,91 @@ __device__ __forceinline__ void cluster_sync_all() {
   asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::
                    : "memory");
 }
-__device__ __forceinline__ void epi_bar_sync() {   // the four epilogue warps only
-  asm volatile("bar.sync 1, 128;" ::: "memory");
+// Named barrier over one role's warps (ids 1.. are free; 0 is __syncthreads).
+template <int kId, int kCount>
+__device__ __forceinline__ void role_sync() {
+  asm volatile("bar.sync %0, %1;" ::"n"(kId), "n"(kCount) : "memory");
 }
-// Barrier among the four epilogue warps that also ANDs a flag across them, so
-// a wait that gave up in one thread makes all 128 leave together.
-__device__ __forceinline__ bool epi_all(bool ok) {
+// The same barrier ANDing a flag over the role, so a wait that gave up in one
+// thread makes the whole role leave its loop together.
+template <int kId, int kCount>
+__device__ __forceinline__ bool role_all(bool ok) {
   uint32_t r;
   asm volatile(
       "{\n\t.reg .pred p, q;\n\t"
       "setp.ne.u32 p, %1, 0;\n\t"
-      "bar.red.and.pred q, 1, 128, p;\n\t"
+      "bar.red.and.pred q, %2, %3, p;\n\t"
       "selp.u32 %0, 1, 0, q;\n\t}"
       : "=r"(r)
-      : "r"((uint32_t)ok)
+      : "r"((uint32_t)ok), "n"(kId), "n"(kCount)
       : "memory");
   return r != 0;
 }
 
 // ------------------------------------------------------------ kernel body
-struct Geometry {
-  int T, n, D, K;
-  int num_tiles, nd;           // token tiles; 64-wide d-chunks per stream
-  int cluster, stages, np;
-};
-
 template <int NS, int RR, int P>
 struct Cfg {
   static constexpr int kNP = ((P * RR + 15) / 16) * 16;
   static_assert(kNP <= 256, "N of one MMA is at most 256");
   static constexpr int kAccCols = kNP <= 32 ? 32 : kNP <= 64 ? 64 : kNP <= 128 ? 128 : 256;
   static constexpr uint32_t kTmemCols = 2 * kAccCols;   // two accumulator buffers
-  static constexpr int kABytes = kTileM * 128;           // 16 KB
+  static constexpr int kXBytes = kTileT * 128;           // TMA box of one x chunk (8 KB)
   static constexpr int kBBytes = kNP * 128;
-  static constexpr int kPartStride = RR + 1;             // odd: conflict-free rows
+  static constexpr int kTY = y_box_tokens(NS);           // tokens per y-ring box
+  static constexpr int kYBytes = kChunkK * 2 * NS * kTY;
+  static constexpr int kStr = partial_stride(RR);        // floats per published partial
+  static constexpr int kVecPerThread = kTY * (kChunkK / 8) / 128;
+  static_assert(kVecPerThread >= 1 && kTY * (kChunkK / 8) % 128 == 0, "y box must split over 128 threads");
+  static_assert(kTileT % kTY == 0, "y boxes tile the token tile");
 };
 
-struct SmemTail {                 // after the stage buffers
-  uint64_t full[8], empty[8];
+struct SmemTail {
+  uint64_t full[kMaxStages], empty[kMaxStages];
+  uint64_t y_full[kMaxStages], y_empty[kMaxStages];
   uint64_t acc_full[2], acc_empty[2];
   uint64_t ssq_full[2], ssq_empty[2];
-  uint64_t part_full, coef_full;
+  uint64_t part_full[2], part_free[2];
+  uint64_t coef_full[kCoefBufs], coef_free[kCoefBufs];
   uint64_t mma_done;
   uint32_t tmem_base;
   uint32_t abort;
 };
+static_assert(sizeof(SmemTail) <= kTailBytes, "barrier block outgrew its reservation");
+
+// Warp roles.
+constexpr int kWarpProducer = 0, kWarpMma = 1, kWarpSsq0 = 2, kWarpPub0 = 4, kWarpGate0 = 6, kWarpY0 = 8;
+// Named barriers: 1 = publish pair, 2 = gate pair (64 threads each), 3 = y warps (128).
+constexpr int kBarPub = 1, kBarGate = 2, kBarY = 3;
 
 template <int NS, int RR, int P>
 __global__ void __launch_bounds__(kThreads, 1)
     mhc_pre_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constant__ CUtensorMap tmap_w,
-                      const EpiParams ep, const __nv_bfloat16* __restrict__ xg, Geometry g, uint32_t* err) {
+                      const __grid_constant__ CUtensorMap tmap_y, const EpiParams ep, Geometry g,
+                      uint32_t* err) {
   using C = Cfg<NS, RR, P>;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
-  // Align the dynamic window to 1024 bytes (swizzle atoms).
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  const int S = g.stages;
-  uint8_t* sA = smem;
-  uint8_t* sB = sA + (size_t)S * C::kABytes;
-  float* part = reinterpret_cast<float*>(sB + (size_t)S * C::kBBytes);     // [128][RR+1]
-  float* ssq_buf = part + kTileM * C::kPartStride;                         // [2][128]
-  float* coef_buf = ssq_buf + 2 * kTileM;                                  // [2][128][NS]
-  SmemTail* tail = reinterpret_cast<SmemTail*>(
-      (reinterpret_cast<uintptr_t>(coef_buf + 2 * kTileM * NS) + 15) & ~uintptr_t(15));
+  const SmemLayout Ly = smem_layout(NS, RR, C::kNP, g.stages, g.ystages);
+  const int S = g.stages, YS = g.ystages;
+  uint8_t* sA = smem + Ly.a;
+  uint8_t* sB = smem + Ly.b;
+  uint8_t* sY = smem + Ly.y;
+  float* recv = reinterpret_cast<float*>(smem + Ly.part);     // [2][CL][64/CL][kStr]
+  float* ssq_buf = reinterpret_cast<float*>(smem + Ly.ssq);   // [2][64]
+  float* coef_buf = reinterpret_cast<float*>(smem + Ly.coef); // [kCoefBufs][64][NS]
+  SmemTail* tail = reinterpret_cast<SmemTail*>(smem + Ly.tail);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int CL = g.cluster;
-  const uint32_t rank = CL > 1 ? cluster_rank() : 0u;
+  const uint32_t rank = cluster_rank();
   const int cluster_id = blockIdx.x / CL;
   const int num_clusters = gridDim.x / CL;
   const int c0 = (int)((long long)rank * g.nd / CL);
   const int c1 = (int)((long long)(rank + 1) * g.nd / CL);
-  const int my_chunks_per_stream = c1 - c0;
-  const int chunks_per_tile = NS * my_chunks_per_stream;
+  const int my_chunks = c1 - c0;                  // d-chunks per stream owned by this CTA
+  const int chunks_per_tile = NS * my_chunks;
+  const int rpo = kTileT / CL;                    // tile rows each member reduces (owns)
   Ctl ctl{&tail->abort, err};
 
   // ---- set-up
@@ -281,21 +321,30 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&tail->full[s], 1);
       mbar_init(&tail->empty[s], 1 + 2);        // MMA commit + two sum-of-squares warps
     }
+    for (int s = 0; s < YS; ++s) {
+      mbar_init(&tail->y_full[s], 1);
+      mbar_init(&tail->y_empty[s], 4);          // four y warps
+    }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&tail->acc_full[b], 1);
-      mbar_init(&tail->acc_empty[b], 4);
+      mbar_init(&tail->acc_empty[b], 2);        // two publish warps
       mbar_init(&tail->ssq_full[b], 2);
-      mbar_init(&tail->ssq_empty[b], 4);
+      mbar_init(&tail->ssq_empty[b], 2);
+      mbar_init(&tail->part_full[b], CL);       // one arrival per cluster member
+      mbar_init(&tail->part_free[b], CL);
     }
-    mbar_init(&tail->part_full, CL);
-    mbar_init(&tail->coef_full, CL);
+    for (int b = 0; b < kCoefBufs; ++b) {
+      mbar_init(&tail->coef_full[b], CL);
+      mbar_init(&tail->coef_free[b], CL);
+    }
     mbar_init(&tail->mma_done, 1);
     tail->abort = 0u;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     tma_prefetch_desc(&tmap_x);
     tma_prefetch_desc(&tmap_w);
+    tma_prefetch_desc(&tmap_y);
   }
-  if (warp == 1) {
+  if (warp == kWarpMma) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
                      smem_u32(&tail->tmem_base)),
                  "r"(C::kTmemCols)
@@ -304,42 +353,93 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   tc_fence_before();
   __syncthreads();
-  if (CL > 1) cluster_sync_all();
+  cluster_sync_all();
   tc_fence_after();
   const uint32_t tmem_base = tail->tmem_base;
 
-  if (warp == 0) {
-    // ================================================= TMA producer
+  if (warp == kWarpProducer) {
+    // ================================================= TMA producer (both rings)
+    // The projection ring runs ahead freely; the y ring re-reads a tile's x
+    // only once every projection chunk of that tile has been issued, and is
+    // drained by the y warps, so neither ring ever blocks the other.
     if (lane == 0) {
-      const uint32_t tx = C::kABytes + C::kBBytes;
-      int stage = 0;
-      uint32_t phase = 0;
-      long long issued = 0;
-      bool ok = true;
-      for (int tile = cluster_id; tile < g.num_tiles && ok; tile += num_clusters) {
-        for (int q = 0; q < chunks_per_tile; ++q) {
-          const int i = q / my_chunks_per_stream;
-          const int j = c0 + (q - i * my_chunks_per_stream);
-          if (!wait_bar<false>(&tail->empty[stage], phase ^ 1u, ctl, kErrWaitTimeout)) { ok = false; break; }
-          mbar_expect_tx(&tail->full[stage], tx);
-          tma_load_3d(sA + (size_t)stage * C::kABytes, &tmap_x, &tail->full[stage], j * kChunkK, i,
-                      tile * kTileM);
-          tma_load_3d(sB + (size_t)stage * C::kBBytes, &tmap_w, &tail->full[stage], j * kChunkK, i, 0);
-          ++issued;
-          if (++stage == S) { stage = 0; phase ^= 1u; }
+      const uint32_t txA = C::kXBytes + C::kBBytes;
+      const uint64_t keep = policy_evict_last(), drop = policy_evict_first();
+      int mt = cluster_id, mq = 0, ms = 0;
+      uint32_t mph = 0, mk = 0;
+      int yt = cluster_id, yq = 0, ys = 0;
+      uint32_t yph = 0, yk = 0;
+      bool mdone = mt >= g.num_tiles, ydone = yt >= g.num_tiles;
+      long long missued = 0, yissued = 0;
+      uint32_t idle = 0;
+      uint64_t idle_since = 0;
+      while (!mdone || !ydone) {
+        bool prog = false;
+        if (!mdone && mbar_poll(&tail->empty[ms], mph ^ 1u)) {
+          // d-chunk outer, stream inner: all n streams of a chunk arrive together
+          const int j = c0 + mq / NS;
+          const int i = mq - (mq / NS) * NS;
+          mbar_expect_tx(&tail->full[ms], txA);
+          tma_load_3d_hint(sA + (size_t)ms * kABytes, &tmap_x, &tail->full[ms], j * kChunkK, i,
+                           mt * kTileT, keep);
+          tma_load_3d_hint(sB + (size_t)ms * C::kBBytes, &tmap_w, &tail->full[ms], j * kChunkK, i, 0, keep);
+          ++missued;
+          if (++mq == chunks_per_tile) {
+            mq = 0;
+            mt += num_clusters;
+            ++mk;
+            mdone = mt >= g.num_tiles;
+          }
+          if (++ms == S) { ms = 0; mph ^= 1u; }
+          prog = true;
+        }
+        if (!ydone && yk < mk && mbar_poll(&tail->y_empty[ys], yph ^ 1u)) {
+          const int rows = min(kTileT, g.T - yt * kTileT);
+          const int groups = (rows + C::kTY - 1) / C::kTY;
+          const int jj = c1 - 1 - yq / groups;     // newest d-chunk first (likeliest in L2)
+          const int tg = yq - (yq / groups) * groups;
+          mbar_expect_tx(&tail->y_full[ys], (uint32_t)C::kYBytes);
+          tma_load_3d_hint(sY + (size_t)ys * C::kYBytes, &tmap_y, &tail->y_full[ys], jj * kChunkK, 0,
+                           yt * kTileT + tg * C::kTY, drop);
+          ++yissued;
+          if (++yq == my_chunks * groups) {
+            yq = 0;
+            yt += num_clusters;
+            ++yk;
+            ydone = yt >= g.num_tiles;
+          }
+          if (++ys == YS) { ys = 0; yph ^= 1u; }
+          prog = true;
+        }
+        if (prog) {
+          idle = 0;
+        } else if ((++idle & 63u) != 0) {
+          __nanosleep(32);   // leave issue slots to the warps sharing this scheduler
+        } else {
+          if (*ctl.abort) break;
+          const uint64_t now = now_ns();
+          if (idle_since == 0 || idle == 64) idle_since = now;
+          if (now - idle_since > kWaitNs) {
+            atomicOr(err, kErrWaitTimeout);
+            *ctl.abort = 1u;
+            break;
+          }
         }
       }
       // Let every copy this thread started land before the CTA can exit.
-      const long long pending = issued < S ? issued : S;
-      for (long long k = 0; k < pending; ++k) {
-        if (--stage < 0) { stage = S - 1; phase ^= 1u; }
-        wait_bar<false>(&tail->full[stage], phase, ctl, kErrWaitTimeout);
+      for (long long q = 0; q < (missued < S ? missued : S); ++q) {
+        if (--ms < 0) { ms = S - 1; mph ^= 1u; }
+        wait_bar<false>(&tail->full[ms], mph, ctl, kErrWaitTimeout);
+      }
+      for (long long q = 0; q < (yissued < YS ? yissued : YS); ++q) {
+        if (--ys < 0) { ys = YS - 1; yph ^= 1u; }
+        wait_bar<false>(&tail->y_full[ys], yph, ctl, kErrWaitTimeout);
       }
     }
-  } else if (warp == 1) {
+  } else if (warp == kWarpMma) {
     // ================================================= MMA issuer
     if (lane == 0) {
-      constexpr uint32_t idesc = idesc_bf16(kTileM, C::kNP);
+      constexpr uint32_t idesc = idesc_bf16(kMmaM, C::kNP);
       int stage = 0;
       uint32_t phase = 0;
       int acc = 0;
@@ -352,7 +452,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int q = 0; q < chunks_per_tile; ++q) {
           if (!wait_bar<false>(&tail->full[stage], phase, ctl, kErrWaitTimeout)) { ok = false; break; }
           tc_fence_after();
-          const uint32_t a0 = smem_u32(sA + (size_t)stage * C::kABytes);
+          // 128-row operand: rows 0..63 are this tile's tokens; rows 64..127
+          // read the neighbouring slot and feed only lanes that are never read.
+          const uint32_t a0 = smem_u32(sA + (size_t)stage * kABytes);
           const uint32_t b0 = smem_u32(sB + (size_t)stage * C::kBBytes);
 #pragma unroll
           for (int kk = 0; kk < kChunkK / 16; ++kk) {
@@ -369,9 +471,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       mma_commit(&tail->mma_done);
       wait_bar<false>(&tail->mma_done, 0, ctl, kErrWaitTimeout);
     }
-  } else if (warp < 4) {
-    // ================================================= sum of squares
-    const int q = threadIdx.x - 64;                // rows q and q + 64
+  } else if (warp < kWarpPub0) {
+    // ================================================= sum of squares (thread = token row)
+    const int row = threadIdx.x - kWarpSsq0 * 32;  // 0..63
     int stage = 0;
     uint32_t phase = 0;
     int b = 0;
@@ -380,58 +482,54 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int tile = cluster_id; tile < g.num_tiles && ok; tile += num_clusters) {
       if (!__all_sync(0xffffffffu, wait_bar<false>(&tail->ssq_empty[b], bphase ^ 1u, ctl, kErrWaitTimeout)))
         break;
-      float s0 = 0.0f, s1 = 0.0f;
+      float acc = 0.0f;
       for (int c = 0; c < chunks_per_tile; ++c) {
         if (!__all_sync(0xffffffffu, wait_bar<false>(&tail->full[stage], phase, ctl, kErrWaitTimeout))) {
           ok = false;
           break;
         }
-        const uint8_t* tileA = sA + (size_t)stage * C::kABytes;
+        const uint8_t* rowp = sA + (size_t)stage * kABytes + row * 128;
+        float part8[8];
 #pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          const int row = q + 64 * h;
-          float acc = 0.0f;
+        for (int p = 0; p < 8; ++p) {
+          // Rotate the 16-byte column by row so a warp's loads hit distinct banks.
+          const int col = (p + row) & 7;
+          const uint4 v = *reinterpret_cast<const uint4*>(rowp + col * 16);
+          const __nv_bfloat162* hv = reinterpret_cast<const __nv_bfloat162*>(&v);
+          float a = 0.0f, bb = 0.0f;
 #pragma unroll
-          for (int p = 0; p < 8; ++p) {
-            // Rotate the 16-byte column by row so a warp's loads hit distinct banks.
-            const int col = (p + row) & 7;
-            const uint4 v = *reinterpret_cast<const uint4*>(tileA + row * 128 + col * 16);
-            const __nv_bfloat162* hv = reinterpret_cast<const __nv_bfloat162*>(&v);
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              const float2 f = __bfloat1622float2(hv[e]);
-              acc = fmaf(f.x, f.x, acc);
-              acc = fmaf(f.y, f.y, acc);
-            }
+          for (int e = 0; e < 4; ++e) {
+            const float2 f = __bfloat1622float2(hv[e]);
+            a = fmaf(f.x, f.x, a);
+            bb = fmaf(f.y, f.y, bb);
           }
-          if (h == 0) s0 += acc; else s1 += acc;
+          part8[p] = a + bb;
         }
+        acc += tree_sum<8>(part8);
         __syncwarp();
         if (lane == 0) mbar_arrive(&tail->empty[stage]);
         if (++stage == S) { stage = 0; phase ^= 1u; }
       }
       if (!ok) break;
-      ssq_buf[b * kTileM + q] = s0;
-      ssq_buf[b * kTileM + q + 64] = s1;
+      ssq_buf[b * kTileT + row] = acc;
       __syncwarp();
       if (lane == 0) mbar_arrive(&tail->ssq_full[b]);
       if (++b == 2) { b = 0; bphase ^= 1u; }
     }
-  } else {
-    // ================================================= epilogue + y
-    const int et = threadIdx.x - 128;              // 0..127 = TMEM lane = tile row
-    const int wq = warp & 3;                       // TMEM lane quarter of this warp
-    const int r0 = (int)((long long)rank * kTileM / CL);
-    const int r1 = (int)((long long)(rank + 1) * kTileM / CL);
-    const int dlo = c0 * kChunkK;
-    const int dhi = min(c1 * kChunkK, g.D);
-    const int w8 = (dhi - dlo) >> 3;               // 16-byte vectors per row
+  } else if (warp < kWarpGate0) {
+    // ================================================= publish partial sums
+    // Thread = tile row = TMEM lane.  Each row's partial projection (this
+    // member's d-range) and partial sum of squares go to the member that
+    // owns the row.
+    const int et = threadIdx.x - kWarpPub0 * 32;   // 0..63
+    const int wq = warp & 3;                       // TMEM lane quarter (0 or 1)
+    const int owner = et / rpo;
+    const int slot = et - owner * rpo;
     int acc = 0;
     uint32_t acc_phase = 0;
-    uint32_t k = 0;                                // tiles done by this cluster member
+    uint32_t k = 0;
     for (int tile = cluster_id; tile < g.num_tiles; tile += num_clusters, ++k) {
-      // --- accumulators and sum of squares for row et
-      if (!epi_all(wait_bar<false>(&tail->acc_full[acc], acc_phase, ctl, kErrWaitTimeout))) break;
+      if (!role_all<kBarPub, 64>(wait_bar<false>(&tail->acc_full[acc], acc_phase, ctl, kErrWaitTimeout))) break;
       tc_fence_after();
       float mix[RR];
 #pragma unroll
@@ -450,84 +548,171 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&tail->acc_empty[acc]);
+      if (++acc == 2) { acc = 0; acc_phase ^= 1u; }
       const int b = (int)(k & 1u);
-      if (!epi_all(wait_bar<false>(&tail->ssq_full[b], (k >> 1) & 1u, ctl, kErrWaitTimeout))) break;
-      float ssq = ssq_buf[b * kTileM + et];
+      if (!role_all<kBarPub, 64>(wait_bar<false>(&tail->ssq_full[b], (k >> 1) & 1u, ctl, kErrWaitTimeout))) break;
+      const float ssq = ssq_buf[b * kTileT + et];
       __syncwarp();
       if (lane == 0) mbar_arrive(&tail->ssq_empty[b]);
-      if (++acc == 2) { acc = 0; acc_phase ^= 1u; }
 
-      const int tok = tile * kTileM + et;
-      float* coef = coef_buf + (size_t)(k & 1u) * kTileM * NS;
-      if (CL == 1) {
-        float cf[NS];
-        token_epilogue<NS, RR>(ep, tok, mix, ssq, tok < g.T, cf);
+      const int pb = (int)(k & 1u);
+      const uint32_t use = k >> 1;                 // earlier uses of buffer pb
+      if (use > 0 &&
+          !role_all<kBarPub, 64>(wait_bar<true>(&tail->part_free[pb], (use - 1) & 1u, ctl, kErrClusterWait)))
+        break;
+      float* dst = recv + ((size_t)(pb * CL + (int)rank) * rpo + slot) * C::kStr;
 #pragma unroll
-        for (int i = 0; i < NS; ++i) coef[et * NS + i] = cf[i];
-        epi_bar_sync();
-      } else {
-        // --- publish this CTA's partial sums, then reduce the rows it owns
-        float* my = part + et * C::kPartStride;
-#pragma unroll
-        for (int r = 0; r < RR; ++r) my[r] = mix[r];
-        my[RR] = ssq;
-        epi_bar_sync();
-        if (et == 0) {
-          asm volatile("fence.acq_rel.cluster;" ::: "memory");
-          for (int cr = 0; cr < CL; ++cr) mbar_arrive_remote(&tail->part_full, (uint32_t)cr);
-        }
-        if (!epi_all(wait_bar<true>(&tail->part_full, k & 1u, ctl, kErrClusterWait))) break;
-        if (et >= r0 && et < r1) {
-          float tot[RR];
-          float tssq = 0.0f;
-#pragma unroll
-          for (int r = 0; r < RR; ++r) tot[r] = 0.0f;
-          for (int cr = 0; cr < CL; ++cr) {
-#pragma unroll
-            for (int r = 0; r < RR; ++r) tot[r] += ld_dsmem_f32(my + r, (uint32_t)cr);
-            tssq += ld_dsmem_f32(my + RR, (uint32_t)cr);
-          }
-          float cf[NS];
-          token_epilogue<NS, RR>(ep, tok, tot, tssq, tok < g.T, cf);
-          for (int cr = 0; cr < CL; ++cr) {
-#pragma unroll
-            for (int i = 0; i < NS; ++i) st_dsmem_f32(coef + et * NS + i, (uint32_t)cr, cf[i]);
-          }
-        }
-        epi_bar_sync();
-        if (et == 0) {
-          asm volatile("fence.acq_rel.cluster;" ::: "memory");
-          for (int cr = 0; cr < CL; ++cr) mbar_arrive_remote(&tail->coef_full, (uint32_t)cr);
-        }
-        if (!epi_all(wait_bar<true>(&tail->coef_full, k & 1u, ctl, kErrClusterWait))) break;
+      for (int r = 0; r < C::kStr; r += 4) {
+        float4 v;
+        v.x = r < RR ? mix[r] : (r == RR ? ssq : 0.0f);
+        v.y = r + 1 < RR ? mix[r + 1] : (r + 1 == RR ? ssq : 0.0f);
+        v.z = r + 2 < RR ? mix[r + 2] : (r + 2 == RR ? ssq : 0.0f);
+        v.w = r + 3 < RR ? mix[r + 3] : (r + 3 == RR ? ssq : 0.0f);
+        st_dsmem_v4(dst + r, (uint32_t)owner, v);
       }
+      role_sync<kBarPub, 64>();
+      if (et < CL) mbar_arrive_remote(&tail->part_full[pb], (uint32_t)et);
+    }
+  } else if (warp < kWarpY0) {
+    // ================================================= gates (critical for y), then Sinkhorn
+    // Owned rows: sum the members' partials in rank order, compute invRms
+    // and the gates, publish the y weights to every member, then run the
+    // Sinkhorn for comb, which y does not wait for.
+    const int ot = threadIdx.x - kWarpGate0 * 32;  // 0..63
+    uint32_t k = 0;
+    for (int tile = cluster_id; tile < g.num_tiles; tile += num_clusters, ++k) {
+      const int pb = (int)(k & 1u);
+      const uint32_t use = k >> 1;
+      if (!role_all<kBarGate, 64>(wait_bar<true>(&tail->part_full[pb], use & 1u, ctl, kErrClusterWait))) break;
+      const bool active = ot < rpo;
+      const int row = (int)rank * rpo + ot;
+      const int tok = tile * kTileT + row;
+      float mix[RR];
+      float ssq = 0.0f;
+      if (active) {
+        float tot[C::kStr];
+#pragma unroll
+        for (int r = 0; r < C::kStr; ++r) tot[r] = 0.0f;
+        for (int cr = 0; cr < CL; ++cr) {
+          const float* src = recv + ((size_t)(pb * CL + cr) * rpo + ot) * C::kStr;
+#pragma unroll
+          for (int r = 0; r < C::kStr; r += 4) {
+            const float4 v = *reinterpret_cast<const float4*>(src + r);
+            tot[r] += v.x;
+            tot[r + 1] += v.y;
+            tot[r + 2] += v.z;
+            tot[r + 3] += v.w;
+          }
+        }
+#pragma unroll
+        for (int r = 0; r < RR; ++r) mix[r] = tot[r];
+        ssq = tot[RR];
+      }
+      role_sync<kBarGate, 64>();
+      if (ot < CL) mbar_arrive_remote(&tail->part_free[pb], (uint32_t)ot);
 
-      // --- y for this CTA's d-range: re-read x (L2), weights from shared memory
-      const int rows = min(kTileM, g.T - tile * kTileM);
-      const int items = rows * w8;
-      for (int it = et; it < items; it += 128) {
-        const int row = it / w8;
-        const int v = it - row * w8;
-        const size_t t = (size_t)tile * kTileM + row;
+      const int cb = (int)(k % kCoefBufs);
+      const uint32_t cuse = k / kCoefBufs;
+      if (cuse > 0 &&
+          !role_all<kBarGate, 64>(wait_bar<true>(&tail->coef_free[cb], (cuse - 1) & 1u, ctl, kErrClusterWait)))
+        break;
+      float inv_rms = 0.0f;
+      if (active) {
+        const bool write = tok < g.T;
         float cf[NS];
+        inv_rms = token_gates<NS, RR>(ep, tok, mix, ssq, write, cf);
+        float* dst = coef_buf + ((size_t)cb * kTileT + row) * NS;
+        for (int cr = 0; cr < CL; ++cr) {
+          if constexpr (NS % 4 == 0) {
 #pragma unroll
-        for (int i = 0; i < NS; ++i) cf[i] = coef[row * NS + i];
-        weighted_sum8<NS>(xg + t * (size_t)g.K, g.D, dlo + 8 * v, cf, ep.y + t * (size_t)g.D);
+            for (int i = 0; i < NS; i += 4)
+              st_dsmem_v4(dst + i, (uint32_t)cr, make_float4(cf[i], cf[i + 1], cf[i + 2], cf[i + 3]));
+          } else {
+#pragma unroll
+            for (int i = 0; i < NS; ++i) st_dsmem_f32(dst + i, (uint32_t)cr, cf[i]);
+          }
+        }
       }
-      epi_bar_sync();
+      role_sync<kBarGate, 64>();
+      if (ot < CL) mbar_arrive_remote(&tail->coef_full[cb], (uint32_t)ot);
+      if (active) token_sinkhorn<NS, RR>(ep, tok, mix, inv_rms, tok < g.T);
+    }
+  } else {
+    // ================================================= y for this member's d-range
+    const int yt = threadIdx.x - kWarpY0 * 32;     // 0..127
+    const uint64_t ystore_policy = policy_evict_first();
+    int ys = 0;
+    uint32_t yph = 0;
+    uint32_t k = 0;
+    for (int tile = cluster_id; tile < g.num_tiles; tile += num_clusters, ++k) {
+      const int cb = (int)(k % kCoefBufs);
+      if (!role_all<kBarY, 128>(wait_bar<true>(&tail->coef_full[cb], (k / kCoefBufs) & 1u, ctl,
+                                               kErrClusterWait)))
+        break;
+      const float* coef = coef_buf + (size_t)cb * kTileT * NS;
+      const int rows = min(kTileT, g.T - tile * kTileT);
+      const int groups = (rows + C::kTY - 1) / C::kTY;
+      const int nyc = my_chunks * groups;
+      bool ok = true;
+      for (int yq = 0; yq < nyc; ++yq) {
+        if (!role_all<kBarY, 128>(wait_bar<false>(&tail->y_full[ys], yph, ctl, kErrWaitTimeout))) {
+          ok = false;
+          break;
+        }
+        const int jj = c1 - 1 - yq / groups;
+        const int tg = yq - (yq / groups) * groups;
+        const __nv_bfloat16* buf = reinterpret_cast<const __nv_bfloat16*>(sY + (size_t)ys * C::kYBytes);
+#pragma unroll
+        for (int u = 0; u < C::kVecPerThread; ++u) {
+          const int v = yt + 128 * u;
+          const int tl = v >> 3;                   // token within the box
+          const int c = v & 7;                     // 8-element column group
+          const int row = tg * C::kTY + tl;
+          const int d = jj * kChunkK + c * 8;
+          if (row < rows && d < g.D) {
+            float acc8[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) acc8[e] = 0.0f;
+#pragma unroll
+            for (int i = 0; i < NS; ++i) {
+              const float m = coef[row * NS + i];
+              const uint4 xv = *reinterpret_cast<const uint4*>(buf + ((size_t)(tl * NS + i) * kChunkK + c * 8));
+              const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&xv);
+#pragma unroll
+              for (int q2 = 0; q2 < 4; ++q2) {
+                const float2 f = __bfloat1622float2(h[q2]);
+                acc8[2 * q2] = fmaf(m, f.x, acc8[2 * q2]);
+                acc8[2 * q2 + 1] = fmaf(m, f.y, acc8[2 * q2 + 1]);
+              }
+            }
+            uint4 o;
+            __nv_bfloat162* ob = reinterpret_cast<__nv_bfloat162*>(&o);
+#pragma unroll
+            for (int q2 = 0; q2 < 4; ++q2) ob[q2] = __floats2bfloat162_rn(acc8[2 * q2], acc8[2 * q2 + 1]);
+            st_global_v4_hint(ep.y + ((size_t)(tile * kTileT + row) * g.D + d), o, ystore_policy);
+          }
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&tail->y_empty[ys]);
+        if (++ys == YS) { ys = 0; yph ^= 1u; }
+      }
+      if (!ok) break;
+      role_sync<kBarY, 128>();                     // every y thread is done with coef[cb]
+      if (yt < CL) mbar_arrive_remote(&tail->coef_free[cb], (uint32_t)yt);
     }
   }
 
   // ---- teardown
   tc_fence_before();
   __syncthreads();
-  if (warp == 1) {
+  if (warp == kWarpMma) {
+    __syncwarp();
     tc_fence_after();
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base),
                  "r"(C::kTmemCols)
                  : "memory");
   }
-  if (CL > 1) cluster_sync_all();
+  cluster_sync_all();
 }
 
 template <int NS, int RR, int P>
@@ -545,6 +730,22 @@ const void* select_kernel(int n, int R, int P) {
   return nullptr;
 }
 
+cudaLaunchConfig_t cluster_config(int cluster, int grid, size_t smem, cudaStream_t s,
+                                  cudaLaunchAttribute* attr) {
+  cudaLaunchConfig_t cfg = {};
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = cluster;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.gridDim = dim3(grid, 1, 1);
+  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cfg;
+}
+
 }  // namespace
 
 int tc_np(int R, int P) { return ((P * R + 15) / 16) * 16; }
@@ -559,17 +760,8 @@ cudaError_t tc_forward_occupancy(int n, int R, int P, size_t smem_bytes, int clu
     e = cudaFuncSetAttribute(k, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
     if (e != cudaSuccess) return e;
   }
-  cudaLaunchConfig_t cfg = {};
   cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = cluster;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  cfg.gridDim = dim3(cluster, 1, 1);
-  cfg.blockDim = dim3(kThreads, 1, 1);
-  cfg.dynamicSmemBytes = smem_bytes;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cudaLaunchConfig_t cfg = cluster_config(cluster, cluster, smem_bytes, nullptr, attr);
   return cudaOccupancyMaxActiveClusters(max_clusters, k, &cfg);
 }
 
@@ -579,29 +771,17 @@ cudaError_t launch_tc_forward(const TcLaunch& L, cudaStream_t s) {
   if (!k) return cudaErrorInvalidValue;
   Geometry g;
   g.T = L.epi.T;
-  g.n = n;
   g.D = L.epi.D;
-  g.K = n * L.epi.D;
-  g.num_tiles = (L.epi.T + kTileM - 1) / kTileM;
+  g.num_tiles = (L.epi.T + kTileT - 1) / kTileT;
   g.nd = (L.epi.D + kChunkK - 1) / kChunkK;
   g.cluster = L.cluster;
   g.stages = L.stages;
-  g.np = L.NP;
-  cudaLaunchConfig_t cfg = {};
+  g.ystages = L.ystages;
   cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = L.cluster;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  cfg.gridDim = dim3(L.grid, 1, 1);
-  cfg.blockDim = dim3(kThreads, 1, 1);
-  cfg.dynamicSmemBytes = L.smem_bytes;
-  cfg.stream = s;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  const __nv_bfloat16* xg = static_cast<const __nv_bfloat16*>(L.x);
+  cudaLaunchConfig_t cfg = cluster_config(L.cluster, L.grid, L.smem_bytes, s, attr);
   void* args[] = {const_cast<CUtensorMap*>(&L.tmap_x), const_cast<CUtensorMap*>(&L.tmap_w),
-                  const_cast<EpiParams*>(&L.epi), &xg, &g, const_cast<uint32_t**>(&L.err_word)};
+                  const_cast<CUtensorMap*>(&L.tmap_y), const_cast<EpiParams*>(&L.epi), &g,
+                  const_cast<uint32_t**>(&L.err_word)};
   return cudaLaunchKernelExC(&cfg, k, args);
 }
 
