@@ -205,35 +205,40 @@ cudaError_t launch_prepare_planes(const PlaneParams& pp, cudaStream_t s);
 
 constexpr int kMmaM = 128;         // rows of one tcgen05.mma (TMEM lanes)
 constexpr int kTileT = 64;         // tokens per tile: MMA rows 0..63 (rows 64..127 unused)
-// x slot of one ring stage: the 64-token box (8 KB).  The 128-row MMA
-// operand starting there runs 8 KB into the next slot (or the first phi
-// slot after the last one); those rows only feed accumulator lanes 64..127,
-// which are never read.
-constexpr int kABytes = kTileT * 128;
 constexpr int kChunkK = 64;        // bf16 elements per 128-byte swizzle row
+constexpr int kStreamTile = kTileT * 128;   // one stream of one d-chunk of a tile (8 KB)
 constexpr int kThreads = 384;      // 12 warps: TMA, MMA, 2 sum-of-squares, 2 publish, 2 gates, 4 y
 constexpr int kMaxStages = 8;      // ring depth limit (barrier arrays)
-constexpr int kCoefBufs = 3;       // y-weight buffers between the epilogue and the y warps
-constexpr size_t kTailBytes = 512; // barriers and flags
+constexpr int kCoefBufs = 3;       // y-weight buffers between the gate warps and the y warps
+constexpr size_t kTailBytes = 1024; // barriers and flags
 
-// Tokens per box of the y re-read ring: 64 columns x n streams x this many
-// tokens is 16 KB for n = 4 and n = 8, 12 KB for n = 6.
-__host__ __device__ constexpr int y_box_tokens(int n) { return n == 4 ? 32 : 16; }
+// Streams per projection-ring box: the box is (64 columns, 64 tokens, this
+// many streams), i.e. 32 KB for n = 4 and n = 8 (two boxes per d-chunk),
+// 24 KB for n = 6.  Large boxes are what keeps one issuing thread at full
+// HBM bandwidth.
+__host__ __device__ constexpr int stream_group(int n) { return n == 6 ? 3 : 4; }
+// Tokens per y-ring box (64 columns x all n streams x this many tokens).
+__host__ __device__ constexpr int y_box_tokens(int n) { return n == 4 ? 64 : 32; }
+// Rows of one phi-plane box: P*R rounded up to 8 (the MMA's N = P*R rounded
+// up to 16 reads the rest from the next slot; those columns are never read).
+__host__ __device__ constexpr int plane_box_rows(int R, int P) { return ((P * R + 7) / 8) * 8; }
 // Floats per published partial (R sums + the sum of squares), padded to 16 bytes.
 __host__ __device__ constexpr int partial_stride(int R) { return ((R + 1 + 3) / 4) * 4; }
 
 // Byte offsets of the forward kernel's shared-memory regions (after the
-// base is rounded up to 1024); `total` includes that rounding slack.
+// base is rounded up to 1024); `total` includes that rounding slack.  The
+// phi ring follows the x ring and the y ring follows the phi ring, so an
+// operand read that runs past a ring's last slot stays inside the window.
 struct SmemLayout {
-  size_t a, b, y, part, ssq, coef, tail, total;
+  size_t x, w, y, part, ssq, coef, tail, total;
 };
-__host__ __device__ inline SmemLayout smem_layout(int n, int R, int NP, int stages, int ystages) {
+__host__ __device__ inline SmemLayout smem_layout(int n, int R, int P, int xs, int ws, int ys) {
   SmemLayout L;
   size_t o = 0;
-  L.a = o;    o += (size_t)stages * kABytes;
-  L.b = o;    o += (size_t)stages * NP * 128;
-  L.y = o;    o += (size_t)ystages * kChunkK * 2 * n * y_box_tokens(n);
-  o = (o + 15) & ~size_t(15);
+  L.x = o;    o += (size_t)xs * stream_group(n) * kStreamTile;
+  L.w = o;    o += (size_t)ws * plane_box_rows(R, P) * 128;
+  o = (o + 1023) & ~size_t(1023);
+  L.y = o;    o += (size_t)ys * n * y_box_tokens(n) * 128;
   L.part = o; o += 2 * (size_t)kTileT * partial_stride(R) * 4;
   L.ssq = o;  o += 2 * (size_t)kTileT * 4;
   L.coef = o; o += (size_t)kCoefBufs * kTileT * n * 4;
@@ -246,18 +251,18 @@ __host__ __device__ inline SmemLayout smem_layout(int n, int R, int NP, int stag
 struct Geometry {
   int T, D;
   int num_tiles, nd;           // token tiles; 64-wide d-chunks per stream
-  int cluster, stages, ystages;
+  int cluster, xstages, wstages, ystages;
 };
 
 struct TcLaunch {
   EpiParams epi;
-  CUtensorMap tmap_x;      // 3-D (D, n, T), box (64, 1, 128), 128B swizzle: projection operand
-  CUtensorMap tmap_w;      // 3-D (D, n, NP), box (64, 1, NP), 128B swizzle: phi planes
-  CUtensorMap tmap_y;      // 3-D (D, n, T), box (64, n, TY), no swizzle: y re-read
+  CUtensorMap tmap_x;      // x as (D, T, n): box (64, 64 tokens, stream group), 128B swizzle
+  CUtensorMap tmap_w;      // planes as (D, NP, n): box (64, plane rows, 1), 128B swizzle
+  CUtensorMap tmap_y;      // x as (D, T, n): box (64, y tokens, n), 128B swizzle
   int NP, P;
   int cluster;             // CTAs per token tile (split over d-chunks)
   int grid;                // CTAs (multiple of cluster)
-  int stages, ystages;
+  int xstages, wstages, ystages;
   size_t smem_bytes;
   uint32_t* err_word;
 };

@@ -54,19 +54,18 @@ EncodeTiledFn encode_fn() {
   return fn;
 }
 
-// 3-D bf16 map over [dim2][dim1][dim0] (dim0 contiguous), box (64, box1,
-// box2), zero fill outside the tensor.
-bool encode_3d(CUtensorMap* map, const void* base, uint64_t dim0, uint64_t dim1, uint64_t dim2,
-               uint32_t box1, uint32_t box2, bool swizzle128) {
+// 3-D bf16 map: dims[0] contiguous, byte strides of dims 1 and 2 given
+// explicitly (they need not increase), 128-byte swizzle, zero fill outside.
+bool encode_3d(CUtensorMap* map, const void* base, const uint64_t dims[3], const uint64_t strides[2],
+               const uint32_t box[3]) {
   EncodeTiledFn fn = encode_fn();
   if (!fn) return false;
-  cuuint64_t dims[3] = {dim0, dim1, dim2};
-  cuuint64_t strides[2] = {dim0 * 2, dim0 * dim1 * 2};
-  cuuint32_t box[3] = {(cuuint32_t)mhc::kChunkK, box1, box2};
+  cuuint64_t d[3] = {dims[0], dims[1], dims[2]};
+  cuuint64_t st[2] = {strides[0], strides[1]};
+  cuuint32_t b[3] = {box[0], box[1], box[2]};
   cuuint32_t estr[3] = {1, 1, 1};
-  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
-                  CU_TENSOR_MAP_INTERLEAVE_NONE,
-                  swizzle128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), d, st, b, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
 }
@@ -255,32 +254,42 @@ mhc_status_t mhc_pre_run(mhc_pre_t h, const mhc_pre_args* a, void* stream) {
   L.NP = NP;
   L.P = h->P;
   L.err_word = err;
-  if (!encode_3d(&L.tmap_x, a->x, (uint64_t)D, (uint64_t)n, (uint64_t)T, 1, mhc::kTileT, true) ||
-      !encode_3d(&L.tmap_w, planes, (uint64_t)D, (uint64_t)n, (uint64_t)NP, 1, (uint32_t)NP, true) ||
-      !encode_3d(&L.tmap_y, a->x, (uint64_t)D, (uint64_t)n, (uint64_t)T, (uint32_t)n,
-                 (uint32_t)mhc::y_box_tokens(n), false))
-    return fail(MHC_ERR_RUNTIME, "tensor map encoding failed");
+  {
+    // x [T][n][D] seen as (D, T, n); the phi planes [NP][n][D] as (D, NP, n).
+    const uint64_t K2 = (uint64_t)n * D * 2;
+    const uint64_t xd[3] = {(uint64_t)D, (uint64_t)T, (uint64_t)n};
+    const uint64_t xs[2] = {K2, (uint64_t)D * 2};
+    const uint32_t xb[3] = {(uint32_t)mhc::kChunkK, (uint32_t)mhc::kTileT, (uint32_t)mhc::stream_group(n)};
+    const uint64_t wd[3] = {(uint64_t)D, (uint64_t)NP, (uint64_t)n};
+    const uint32_t wb[3] = {(uint32_t)mhc::kChunkK, (uint32_t)mhc::plane_box_rows(R, h->P), 1};
+    const uint32_t yb[3] = {(uint32_t)mhc::kChunkK, (uint32_t)mhc::y_box_tokens(n), (uint32_t)n};
+    if (!encode_3d(&L.tmap_x, a->x, xd, xs, xb) || !encode_3d(&L.tmap_w, planes, wd, xs, wb) ||
+        !encode_3d(&L.tmap_y, a->x, xd, xs, yb))
+      return fail(MHC_ERR_RUNTIME, "tensor map encoding failed");
+  }
 
-  // Ring depths: the projection ring carries x (8 KB) plus phi planes per
-  // stage from HBM/L2 and wants the most bytes in flight; the y ring
-  // re-reads from L2 and needs a few boxes.  Take the deepest projection
-  // ring beside a y ring of `want_y` boxes, shrinking the y ring to 2 last.
+  // Ring depths.  x boxes come from HBM and want the most bytes in flight;
+  // phi-plane and y boxes come from L2.  First try to keep >= 3 x boxes and
+  // 2 y boxes in flight (deepest x, then phi), then relax to (2, 2, 1).
   const int nd = (D + mhc::kChunkK - 1) / mhc::kChunkK;
   const int num_tiles = (int)((T + mhc::kTileT - 1) / mhc::kTileT);
   const size_t budget = di.max_smem;
-  int max_stages = env_int("MHC_PRE_STAGES", mhc::kMaxStages);
-  if (max_stages > mhc::kMaxStages) max_stages = mhc::kMaxStages;
-  int want_y = env_int("MHC_PRE_YSTAGES", 3);
-  if (want_y > mhc::kMaxStages) want_y = mhc::kMaxStages;
-  int stages = 0, ystages = 0;
-  for (int min_st : {6, 4, 2}) {
-    for (int ys = want_y; ys >= 2 && !stages; --ys)
-      for (int st = max_stages; st >= min_st; --st)
-        if (mhc::smem_layout(n, R, NP, st, ys).total <= budget) { stages = st; ystages = ys; break; }
-    if (stages) break;
-  }
-  if (!stages) return fail(MHC_ERR_RUNTIME, "shape does not fit in shared memory");
-  const size_t smem = mhc::smem_layout(n, R, NP, stages, ystages).total;
+  int xmax = env_int("MHC_PRE_XSTAGES", 4), wmax = env_int("MHC_PRE_WSTAGES", 4), ymax = env_int("MHC_PRE_YSTAGES", 2);
+  xmax = xmax < 2 ? 2 : (xmax > mhc::kMaxStages ? mhc::kMaxStages : xmax);
+  wmax = wmax < 2 ? 2 : (wmax > mhc::kMaxStages ? mhc::kMaxStages : wmax);
+  ymax = ymax < 1 ? 1 : (ymax > mhc::kMaxStages ? mhc::kMaxStages : ymax);
+  int xst = 0, wst = 0, yst = 0;
+  const int xmin_pass[2] = {xmax < 3 ? xmax : 3, 2};
+  for (int pass = 0; pass < 2 && !xst; ++pass)
+    for (int ysn = ymax; ysn >= (pass == 0 ? (ymax < 2 ? ymax : 2) : 1) && !xst; --ysn)
+      for (int xsn = xmax; xsn >= xmin_pass[pass] && !xst; --xsn)
+        for (int wsn = wmax; wsn >= 2; --wsn)
+          if (mhc::smem_layout(n, R, h->P, xsn, wsn, ysn).total <= budget) {
+            xst = xsn; wst = wsn; yst = ysn;
+            break;
+          }
+  if (!xst) return fail(MHC_ERR_RUNTIME, "shape does not fit in shared memory");
+  const size_t smem = mhc::smem_layout(n, R, h->P, xst, wst, yst).total;
 
   int want = env_int("MHC_PRE_CLUSTER", 16);
   int cluster = 1;
@@ -298,13 +307,14 @@ mhc_status_t mhc_pre_run(mhc_pre_t h, const mhc_pre_args* a, void* stream) {
   if (max_clusters <= 0) return fail(MHC_ERR_RUNTIME, "no cluster configuration fits this device");
   L.cluster = cluster;
   L.grid = (num_tiles < max_clusters ? num_tiles : max_clusters) * cluster;
-  L.stages = stages;
-  L.ystages = ystages;
+  L.xstages = xst;
+  L.wstages = wst;
+  L.ystages = yst;
   L.smem_bytes = smem;
   h->last_cluster = cluster;
   h->last_grid = L.grid;
-  h->last_stages = stages;
-  h->last_ystages = ystages;
+  h->last_stages = xst;
+  h->last_ystages = yst;
   if (h->ev_before && cudaEventRecord(h->ev_before, s) != cudaSuccess)
     return fail(MHC_ERR_RUNTIME, "recording the timing event failed");
   if (mhc::launch_tc_forward(L, s) != cudaSuccess)

@@ -252,22 +252,26 @@ __device__ __forceinline__ bool role_all(bool ok) {
 // ------------------------------------------------------------ kernel body
 template <int NS, int RR, int P>
 struct Cfg {
-  static constexpr int kNP = ((P * RR + 15) / 16) * 16;
+  static constexpr int kNP = ((P * RR + 15) / 16) * 16;          // MMA N
   static_assert(kNP <= 256, "N of one MMA is at most 256");
   static constexpr int kAccCols = kNP <= 32 ? 32 : kNP <= 64 ? 64 : kNP <= 128 ? 128 : 256;
   static constexpr uint32_t kTmemCols = 2 * kAccCols;   // two accumulator buffers
-  static constexpr int kXBytes = kTileT * 128;           // TMA box of one x chunk (8 KB)
-  static constexpr int kBBytes = kNP * 128;
-  static constexpr int kTY = y_box_tokens(NS);           // tokens per y-ring box
-  static constexpr int kYBytes = kChunkK * 2 * NS * kTY;
+  static constexpr int kSG = stream_group(NS);           // streams per x box
+  static constexpr int kGroups = NS / kSG;               // x boxes per d-chunk
+  static_assert(NS % kSG == 0, "stream groups tile the streams");
+  static constexpr int kXBytes = kSG * kStreamTile;      // one x box
+  static constexpr int kWRows = plane_box_rows(RR, P);
+  static constexpr int kWBytes = kWRows * 128;           // one phi-plane box (one stream)
+  static constexpr int kTY = y_box_tokens(NS);           // tokens per y box
+  static constexpr int kYBytes = NS * kTY * 128;
   static constexpr int kStr = partial_stride(RR);        // floats per published partial
   static constexpr int kVecPerThread = kTY * (kChunkK / 8) / 128;
   static_assert(kVecPerThread >= 1 && kTY * (kChunkK / 8) % 128 == 0, "y box must split over 128 threads");
-  static_assert(kTileT % kTY == 0, "y boxes tile the token tile");
 };
 
 struct SmemTail {
-  uint64_t full[kMaxStages], empty[kMaxStages];
+  uint64_t x_full[kMaxStages], x_empty[kMaxStages];
+  uint64_t w_full[kMaxStages], w_empty[kMaxStages];
   uint64_t y_full[kMaxStages], y_empty[kMaxStages];
   uint64_t acc_full[2], acc_empty[2];
   uint64_t ssq_full[2], ssq_empty[2];
@@ -284,6 +288,9 @@ constexpr int kWarpProducer = 0, kWarpMma = 1, kWarpSsq0 = 2, kWarpPub0 = 4, kWa
 // Named barriers: 1 = publish pair, 2 = gate pair (64 threads each), 3 = y warps (128).
 constexpr int kBarPub = 1, kBarGate = 2, kBarY = 3;
 
+// Offset of 16-byte column c of row r in a 128-byte-swizzled tile.
+__device__ __forceinline__ int sw128(int r, int c) { return r * 128 + ((c ^ (r & 7)) << 4); }
+
 template <int NS, int RR, int P>
 __global__ void __launch_bounds__(kThreads, 1)
     mhc_pre_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constant__ CUtensorMap tmap_w,
@@ -292,10 +299,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   using C = Cfg<NS, RR, P>;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  const SmemLayout Ly = smem_layout(NS, RR, C::kNP, g.stages, g.ystages);
-  const int S = g.stages, YS = g.ystages;
-  uint8_t* sA = smem + Ly.a;
-  uint8_t* sB = smem + Ly.b;
+  const SmemLayout Ly = smem_layout(NS, RR, P, g.xstages, g.wstages, g.ystages);
+  const int XS = g.xstages, WS = g.wstages, YS = g.ystages;
+  uint8_t* sX = smem + Ly.x;
+  uint8_t* sW = smem + Ly.w;
   uint8_t* sY = smem + Ly.y;
   float* recv = reinterpret_cast<float*>(smem + Ly.part);     // [2][CL][64/CL][kStr]
   float* ssq_buf = reinterpret_cast<float*>(smem + Ly.ssq);   // [2][64]
@@ -310,16 +317,21 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int num_clusters = gridDim.x / CL;
   const int c0 = (int)((long long)rank * g.nd / CL);
   const int c1 = (int)((long long)(rank + 1) * g.nd / CL);
-  const int my_chunks = c1 - c0;                  // d-chunks per stream owned by this CTA
-  const int chunks_per_tile = NS * my_chunks;
+  const int my_chunks = c1 - c0;                  // d-chunks owned by this CTA
+  const int xper_tile = my_chunks * C::kGroups;   // x boxes per tile
+  const int wper_tile = my_chunks * NS;           // phi-plane boxes per tile
   const int rpo = kTileT / CL;                    // tile rows each member reduces (owns)
   Ctl ctl{&tail->abort, err};
 
   // ---- set-up
   if (threadIdx.x == 0) {
-    for (int s = 0; s < S; ++s) {
-      mbar_init(&tail->full[s], 1);
-      mbar_init(&tail->empty[s], 1 + 2);        // MMA commit + two sum-of-squares warps
+    for (int s = 0; s < XS; ++s) {
+      mbar_init(&tail->x_full[s], 1);
+      mbar_init(&tail->x_empty[s], 1 + 2);      // MMA commit + two sum-of-squares warps
+    }
+    for (int s = 0; s < WS; ++s) {
+      mbar_init(&tail->w_full[s], 1);
+      mbar_init(&tail->w_empty[s], 1);          // MMA commit
     }
     for (int s = 0; s < YS; ++s) {
       mbar_init(&tail->y_full[s], 1);
@@ -358,56 +370,56 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tmem_base = tail->tmem_base;
 
   if (warp == kWarpProducer) {
-    // ================================================= TMA producer (both rings)
-    // The projection ring runs ahead freely; the y ring re-reads a tile's x
-    // only once every projection chunk of that tile has been issued, and is
-    // drained by the y warps, so neither ring ever blocks the other.
+    // ================================================= TMA producer (three rings)
+    // x ring: (d-chunk, stream group) boxes of a tile, from HBM.  phi ring:
+    // (d-chunk, stream) plane boxes, from L2.  y ring: (d-chunk, token half)
+    // boxes of all streams, re-read from L2 once all of the tile's x boxes
+    // were issued.  Rings are polled without blocking, so none stalls another.
     if (lane == 0) {
-      const uint32_t txA = C::kXBytes + C::kBBytes;
       const uint64_t keep = policy_evict_last(), drop = policy_evict_first();
-      int mt = cluster_id, mq = 0, ms = 0;
-      uint32_t mph = 0, mk = 0;
+      int xt = cluster_id, xq = 0, xs = 0;
+      uint32_t xph = 0, xk = 0;
+      int wt = cluster_id, wq = 0, ws = 0;
+      uint32_t wph = 0;
       int yt = cluster_id, yq = 0, ys = 0;
       uint32_t yph = 0, yk = 0;
-      bool mdone = mt >= g.num_tiles, ydone = yt >= g.num_tiles;
-      long long missued = 0, yissued = 0;
+      bool xdone = xt >= g.num_tiles, wdone = wt >= g.num_tiles, ydone = yt >= g.num_tiles;
+      long long xiss = 0, wiss = 0, yiss = 0;
       uint32_t idle = 0;
       uint64_t idle_since = 0;
-      while (!mdone || !ydone) {
+      while (!xdone || !wdone || !ydone) {
         bool prog = false;
-        if (!mdone && mbar_poll(&tail->empty[ms], mph ^ 1u)) {
-          // d-chunk outer, stream inner: all n streams of a chunk arrive together
-          const int j = c0 + mq / NS;
-          const int i = mq - (mq / NS) * NS;
-          mbar_expect_tx(&tail->full[ms], txA);
-          tma_load_3d_hint(sA + (size_t)ms * kABytes, &tmap_x, &tail->full[ms], j * kChunkK, i,
-                           mt * kTileT, keep);
-          tma_load_3d_hint(sB + (size_t)ms * C::kBBytes, &tmap_w, &tail->full[ms], j * kChunkK, i, 0, keep);
-          ++missued;
-          if (++mq == chunks_per_tile) {
-            mq = 0;
-            mt += num_clusters;
-            ++mk;
-            mdone = mt >= g.num_tiles;
-          }
-          if (++ms == S) { ms = 0; mph ^= 1u; }
+        if (!xdone && mbar_poll(&tail->x_empty[xs], xph ^ 1u)) {
+          const int j = c0 + xq / C::kGroups;
+          const int grp = xq - (xq / C::kGroups) * C::kGroups;
+          mbar_expect_tx(&tail->x_full[xs], (uint32_t)C::kXBytes);
+          tma_load_3d_hint(sX + (size_t)xs * C::kXBytes, &tmap_x, &tail->x_full[xs], j * kChunkK,
+                           xt * kTileT, grp * C::kSG, keep);
+          ++xiss;
+          if (++xq == xper_tile) { xq = 0; xt += num_clusters; ++xk; xdone = xt >= g.num_tiles; }
+          if (++xs == XS) { xs = 0; xph ^= 1u; }
           prog = true;
         }
-        if (!ydone && yk < mk && mbar_poll(&tail->y_empty[ys], yph ^ 1u)) {
+        if (!wdone && mbar_poll(&tail->w_empty[ws], wph ^ 1u)) {
+          const int j = c0 + wq / NS;
+          const int i = wq - (wq / NS) * NS;
+          mbar_expect_tx(&tail->w_full[ws], (uint32_t)C::kWBytes);
+          tma_load_3d_hint(sW + (size_t)ws * C::kWBytes, &tmap_w, &tail->w_full[ws], j * kChunkK, 0, i, keep);
+          ++wiss;
+          if (++wq == wper_tile) { wq = 0; wt += num_clusters; wdone = wt >= g.num_tiles; }
+          if (++ws == WS) { ws = 0; wph ^= 1u; }
+          prog = true;
+        }
+        if (!ydone && yk < xk && mbar_poll(&tail->y_empty[ys], yph ^ 1u)) {
           const int rows = min(kTileT, g.T - yt * kTileT);
-          const int groups = (rows + C::kTY - 1) / C::kTY;
-          const int jj = c1 - 1 - yq / groups;     // newest d-chunk first (likeliest in L2)
-          const int tg = yq - (yq / groups) * groups;
+          const int halves = (rows + C::kTY - 1) / C::kTY;
+          const int jj = c1 - 1 - yq / halves;     // newest d-chunk first (likeliest in L2)
+          const int h = yq - (yq / halves) * halves;
           mbar_expect_tx(&tail->y_full[ys], (uint32_t)C::kYBytes);
-          tma_load_3d_hint(sY + (size_t)ys * C::kYBytes, &tmap_y, &tail->y_full[ys], jj * kChunkK, 0,
-                           yt * kTileT + tg * C::kTY, drop);
-          ++yissued;
-          if (++yq == my_chunks * groups) {
-            yq = 0;
-            yt += num_clusters;
-            ++yk;
-            ydone = yt >= g.num_tiles;
-          }
+          tma_load_3d_hint(sY + (size_t)ys * C::kYBytes, &tmap_y, &tail->y_full[ys], jj * kChunkK,
+                           yt * kTileT + h * C::kTY, 0, drop);
+          ++yiss;
+          if (++yq == my_chunks * halves) { yq = 0; yt += num_clusters; ++yk; ydone = yt >= g.num_tiles; }
           if (++ys == YS) { ys = 0; yph ^= 1u; }
           prog = true;
         }
@@ -427,11 +439,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       // Let every copy this thread started land before the CTA can exit.
-      for (long long q = 0; q < (missued < S ? missued : S); ++q) {
-        if (--ms < 0) { ms = S - 1; mph ^= 1u; }
-        wait_bar<false>(&tail->full[ms], mph, ctl, kErrWaitTimeout);
+      for (long long q = 0; q < (xiss < XS ? xiss : XS); ++q) {
+        if (--xs < 0) { xs = XS - 1; xph ^= 1u; }
+        wait_bar<false>(&tail->x_full[xs], xph, ctl, kErrWaitTimeout);
       }
-      for (long long q = 0; q < (yissued < YS ? yissued : YS); ++q) {
+      for (long long q = 0; q < (wiss < WS ? wiss : WS); ++q) {
+        if (--ws < 0) { ws = WS - 1; wph ^= 1u; }
+        wait_bar<false>(&tail->w_full[ws], wph, ctl, kErrWaitTimeout);
+      }
+      for (long long q = 0; q < (yiss < YS ? yiss : YS); ++q) {
         if (--ys < 0) { ys = YS - 1; yph ^= 1u; }
         wait_bar<false>(&tail->y_full[ys], yph, ctl, kErrWaitTimeout);
       }
@@ -440,29 +456,35 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ================================================= MMA issuer
     if (lane == 0) {
       constexpr uint32_t idesc = idesc_bf16(kMmaM, C::kNP);
-      int stage = 0;
-      uint32_t phase = 0;
-      int acc = 0;
-      uint32_t acc_phase = 0;
+      int xs = 0, ws = 0, acc = 0;
+      uint32_t xph = 0, wph = 0, acc_phase = 0;
       bool ok = true;
       for (int tile = cluster_id; tile < g.num_tiles && ok; tile += num_clusters) {
         if (!wait_bar<false>(&tail->acc_empty[acc], acc_phase ^ 1u, ctl, kErrWaitTimeout)) break;
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + (uint32_t)(acc * C::kAccCols);
-        for (int q = 0; q < chunks_per_tile; ++q) {
-          if (!wait_bar<false>(&tail->full[stage], phase, ctl, kErrWaitTimeout)) { ok = false; break; }
-          tc_fence_after();
-          // 128-row operand: rows 0..63 are this tile's tokens; rows 64..127
-          // read the neighbouring slot and feed only lanes that are never read.
-          const uint32_t a0 = smem_u32(sA + (size_t)stage * kABytes);
-          const uint32_t b0 = smem_u32(sB + (size_t)stage * C::kBBytes);
+        bool first = true;
+        for (int q = 0; q < xper_tile && ok; ++q) {
+          if (!wait_bar<false>(&tail->x_full[xs], xph, ctl, kErrWaitTimeout)) { ok = false; break; }
+          const uint32_t xbase = smem_u32(sX + (size_t)xs * C::kXBytes);
+          for (int il = 0; il < C::kSG; ++il) {
+            if (!wait_bar<false>(&tail->w_full[ws], wph, ctl, kErrWaitTimeout)) { ok = false; break; }
+            tc_fence_after();
+            // 128-row operand: rows 0..63 are this stream's tokens; rows 64..127
+            // read on into the next stream (or ring) and feed only lanes never read.
+            const uint32_t a0 = xbase + il * kStreamTile;
+            const uint32_t b0 = smem_u32(sW + (size_t)ws * C::kWBytes);
 #pragma unroll
-          for (int kk = 0; kk < kChunkK / 16; ++kk) {
-            mma_bf16(d_tmem, sw128_desc(a0 + kk * 32), sw128_desc(b0 + kk * 32), idesc,
-                     (q > 0 || kk > 0) ? 1u : 0u);
+            for (int kk = 0; kk < kChunkK / 16; ++kk) {
+              mma_bf16(d_tmem, sw128_desc(a0 + kk * 32), sw128_desc(b0 + kk * 32), idesc, first ? 0u : 1u);
+              first = false;
+            }
+            mma_commit(&tail->w_empty[ws]);       // frees the plane slot when these MMAs finish
+            if (++ws == WS) { ws = 0; wph ^= 1u; }
           }
-          mma_commit(&tail->empty[stage]);       // frees the stage when these MMAs finish
-          if (++stage == S) { stage = 0; phase ^= 1u; }
+          if (!ok) break;
+          mma_commit(&tail->x_empty[xs]);
+          if (++xs == XS) { xs = 0; xph ^= 1u; }
         }
         if (!ok) break;
         mma_commit(&tail->acc_full[acc]);          // accumulator complete
@@ -474,8 +496,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp < kWarpPub0) {
     // ================================================= sum of squares (thread = token row)
     const int row = threadIdx.x - kWarpSsq0 * 32;  // 0..63
-    int stage = 0;
-    uint32_t phase = 0;
+    int xs = 0;
+    uint32_t xph = 0;
     int b = 0;
     uint32_t bphase = 0;
     bool ok = true;
@@ -483,32 +505,36 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!__all_sync(0xffffffffu, wait_bar<false>(&tail->ssq_empty[b], bphase ^ 1u, ctl, kErrWaitTimeout)))
         break;
       float acc = 0.0f;
-      for (int c = 0; c < chunks_per_tile; ++c) {
-        if (!__all_sync(0xffffffffu, wait_bar<false>(&tail->full[stage], phase, ctl, kErrWaitTimeout))) {
+      for (int q = 0; q < xper_tile; ++q) {
+        if (!__all_sync(0xffffffffu, wait_bar<false>(&tail->x_full[xs], xph, ctl, kErrWaitTimeout))) {
           ok = false;
           break;
         }
-        const uint8_t* rowp = sA + (size_t)stage * kABytes + row * 128;
-        float part8[8];
+        const uint8_t* box = sX + (size_t)xs * C::kXBytes;
 #pragma unroll
-        for (int p = 0; p < 8; ++p) {
-          // Rotate the 16-byte column by row so a warp's loads hit distinct banks.
-          const int col = (p + row) & 7;
-          const uint4 v = *reinterpret_cast<const uint4*>(rowp + col * 16);
-          const __nv_bfloat162* hv = reinterpret_cast<const __nv_bfloat162*>(&v);
-          float a = 0.0f, bb = 0.0f;
+        for (int il = 0; il < C::kSG; ++il) {
+          const uint8_t* rowp = box + il * kStreamTile + row * 128;
+          float part8[8];
 #pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const float2 f = __bfloat1622float2(hv[e]);
-            a = fmaf(f.x, f.x, a);
-            bb = fmaf(f.y, f.y, bb);
+          for (int p = 0; p < 8; ++p) {
+            // Rotate the 16-byte column by row so a warp's loads hit distinct banks.
+            const int col = (p + row) & 7;
+            const uint4 v = *reinterpret_cast<const uint4*>(rowp + col * 16);
+            const __nv_bfloat162* hv = reinterpret_cast<const __nv_bfloat162*>(&v);
+            float a = 0.0f, bb = 0.0f;
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const float2 f = __bfloat1622float2(hv[e]);
+              a = fmaf(f.x, f.x, a);
+              bb = fmaf(f.y, f.y, bb);
+            }
+            part8[p] = a + bb;
           }
-          part8[p] = a + bb;
+          acc += tree_sum<8>(part8);
         }
-        acc += tree_sum<8>(part8);
         __syncwarp();
-        if (lane == 0) mbar_arrive(&tail->empty[stage]);
-        if (++stage == S) { stage = 0; phase ^= 1u; }
+        if (lane == 0) mbar_arrive(&tail->x_empty[xs]);
+        if (++xs == XS) { xs = 0; xph ^= 1u; }
       }
       if (!ok) break;
       ssq_buf[b * kTileT + row] = acc;
@@ -651,23 +677,23 @@ __global__ void __launch_bounds__(kThreads, 1)
         break;
       const float* coef = coef_buf + (size_t)cb * kTileT * NS;
       const int rows = min(kTileT, g.T - tile * kTileT);
-      const int groups = (rows + C::kTY - 1) / C::kTY;
-      const int nyc = my_chunks * groups;
+      const int halves = (rows + C::kTY - 1) / C::kTY;
+      const int nyc = my_chunks * halves;
       bool ok = true;
       for (int yq = 0; yq < nyc; ++yq) {
         if (!role_all<kBarY, 128>(wait_bar<false>(&tail->y_full[ys], yph, ctl, kErrWaitTimeout))) {
           ok = false;
           break;
         }
-        const int jj = c1 - 1 - yq / groups;
-        const int tg = yq - (yq / groups) * groups;
-        const __nv_bfloat16* buf = reinterpret_cast<const __nv_bfloat16*>(sY + (size_t)ys * C::kYBytes);
+        const int jj = c1 - 1 - yq / halves;
+        const int h = yq - (yq / halves) * halves;
+        const uint8_t* box = sY + (size_t)ys * C::kYBytes;   // [stream][token][128 B], swizzled
 #pragma unroll
         for (int u = 0; u < C::kVecPerThread; ++u) {
           const int v = yt + 128 * u;
           const int tl = v >> 3;                   // token within the box
-          const int c = v & 7;                     // 8-element column group
-          const int row = tg * C::kTY + tl;
+          const int c = v & 7;                     // 16-byte column group
+          const int row = h * C::kTY + tl;
           const int d = jj * kChunkK + c * 8;
           if (row < rows && d < g.D) {
             float acc8[8];
@@ -676,11 +702,11 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int i = 0; i < NS; ++i) {
               const float m = coef[row * NS + i];
-              const uint4 xv = *reinterpret_cast<const uint4*>(buf + ((size_t)(tl * NS + i) * kChunkK + c * 8));
-              const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&xv);
+              const uint4 xv = *reinterpret_cast<const uint4*>(box + sw128(i * C::kTY + tl, c));
+              const __nv_bfloat162* hh = reinterpret_cast<const __nv_bfloat162*>(&xv);
 #pragma unroll
               for (int q2 = 0; q2 < 4; ++q2) {
-                const float2 f = __bfloat1622float2(h[q2]);
+                const float2 f = __bfloat1622float2(hh[q2]);
                 acc8[2 * q2] = fmaf(m, f.x, acc8[2 * q2]);
                 acc8[2 * q2 + 1] = fmaf(m, f.y, acc8[2 * q2 + 1]);
               }
@@ -775,7 +801,8 @@ cudaError_t launch_tc_forward(const TcLaunch& L, cudaStream_t s) {
   g.num_tiles = (L.epi.T + kTileT - 1) / kTileT;
   g.nd = (L.epi.D + kChunkK - 1) / kChunkK;
   g.cluster = L.cluster;
-  g.stages = L.stages;
+  g.xstages = L.xstages;
+  g.wstages = L.wstages;
   g.ystages = L.ystages;
   cudaLaunchAttribute attr[1];
   cudaLaunchConfig_t cfg = cluster_config(L.cluster, L.grid, L.smem_bytes, s, attr);
