@@ -120,16 +120,30 @@ __device__ __forceinline__ float token_gates(const EpiParams& p, int t, const fl
   return inv_rms;
 }
 
-// Residual mix of one token ("aclnnMhcPreSinkhorn 接口与 MhcPreSinkhorn 实现
-// 剖析" §3.2): logits H = alpha2 * pRes + bias2 (row-major n x n), softmax
-// over each row + eps, a column step, then (row, column) x (numIters - 1);
-// each step divides by (sum + eps).  Writes comb and, when sum_out is set,
-// every step's sums and matrices.  Two-gate form: comb is zero.
+// Residual logits of one token: H = alpha2 * pRes + bias2, pRes the res
+// segment of the projection scaled by invRms, reshaped row-major to n x n.
 template <int NS, int RR>
-__device__ __forceinline__ void token_sinkhorn(const EpiParams& p, int t, const float (&mix)[RR],
-                                               float inv_rms, bool write) {
+__device__ __forceinline__ void residual_logits(const EpiParams& p, const float (&mix)[RR], float inv_rms,
+                                                float (&H)[NS * NS]) {
   constexpr int NN = NS * NS;
-  constexpr bool kThree = (RR == NN + 2 * NS);
+  if constexpr (RR == NN + 2 * NS) {
+    const float a2 = __ldg(p.alpha + 2);
+#pragma unroll
+    for (int e = 0; e < NN; ++e) H[e] = a2 * (mix[2 * NS + e] * inv_rms) + __ldg(p.bias + 2 * NS + e);
+  } else {
+#pragma unroll
+    for (int e = 0; e < NN; ++e) H[e] = 0.0f;
+  }
+}
+
+// Residual mix of one token ("aclnnMhcPreSinkhorn 接口与 MhcPreSinkhorn 实现
+// 剖析" §3.2) from its logits H: softmax over each row + eps, a column step,
+// then (row, column) x (numIters - 1); each step divides by (sum + eps).
+// Writes comb and, when sum_out is set, every step's sums and matrices.
+// Two-gate form (no residual path): comb is zero.
+template <int NS, bool kThree>
+__device__ __forceinline__ void token_sinkhorn(const EpiParams& p, int t, const float* H, bool write) {
+  constexpr int NN = NS * NS;
   if constexpr (!kThree) {
     if (write && p.h_res) {
 #pragma unroll
@@ -137,11 +151,9 @@ __device__ __forceinline__ void token_sinkhorn(const EpiParams& p, int t, const 
     }
   } else {
     const float hc_eps = p.hc_eps;
-    const float a2 = __ldg(p.alpha + 2);
     float P[NN];
 #pragma unroll
-    for (int e = 0; e < NN; ++e)
-      P[e] = a2 * (mix[2 * NS + e] * inv_rms) + __ldg(p.bias + 2 * NS + e);
+    for (int e = 0; e < NN; ++e) P[e] = H[e];
     const size_t Tn = (size_t)p.T * NS, Tnn = (size_t)p.T * NN;
     const bool wb = write && (p.sum_out != nullptr);
     float* sums = wb ? p.sum_out : nullptr;
@@ -207,41 +219,51 @@ constexpr int kMmaM = 128;         // rows of one tcgen05.mma (TMEM lanes)
 constexpr int kTileT = 64;         // tokens per tile: MMA rows 0..63 (rows 64..127 unused)
 constexpr int kChunkK = 64;        // bf16 elements per 128-byte swizzle row
 constexpr int kStreamTile = kTileT * 128;   // one stream of one d-chunk of a tile (8 KB)
-constexpr int kThreads = 384;      // 12 warps: TMA, MMA, 2 sum-of-squares, 2 publish, 2 gates, 4 y
+constexpr int kThreads = 384;      // 12 warps: 3 TMA producers, MMA, 2 publish, gates, Sinkhorn, 4 y
 constexpr int kMaxStages = 8;      // ring depth limit (barrier arrays)
 constexpr int kCoefBufs = 3;       // y-weight buffers between the gate warps and the y warps
 constexpr size_t kTailBytes = 1024; // barriers and flags
 
-// Streams per projection-ring box: the box is (64 columns, 64 tokens, this
-// many streams), i.e. 32 KB for n = 4 and n = 8 (two boxes per d-chunk),
-// 24 KB for n = 6.  Large boxes are what keeps one issuing thread at full
-// HBM bandwidth.
+// Streams per x box: the box is (64 columns, 64 tokens, this many
+// streams): 32 KB for n = 4 and n = 8 (two boxes per d-chunk), 24 KB for
+// n = 6.  Big boxes matter: one issuing thread completes only about two
+// boxes per microsecond, whatever their size.
 __host__ __device__ constexpr int stream_group(int n) { return n == 6 ? 3 : 4; }
-// Tokens per y-ring box (64 columns x all n streams x this many tokens).
+// Tokens per y box (64 columns x all n streams x this many tokens).
 __host__ __device__ constexpr int y_box_tokens(int n) { return n == 4 ? 64 : 32; }
-// Rows of one phi-plane box: P*R rounded up to 8 (the MMA's N = P*R rounded
-// up to 16 reads the rest from the next slot; those columns are never read).
+// Rows of one stream's phi planes in a w box: P*R rounded up to 8.  The
+// MMA's N = P*R rounded up to 16 reads the rest from the next stream (or
+// slot); those accumulator columns are never read.
 __host__ __device__ constexpr int plane_box_rows(int R, int P) { return ((P * R + 7) / 8) * 8; }
+// Streams per w box: the largest divisor of n whose planes stay within 36 KB.
+__host__ __device__ constexpr int w_group(int n, int R, int P) {
+  return (n % 4 == 0 && 4 * plane_box_rows(R, P) * 128 <= 36864)   ? 4
+         : (n % 3 == 0 && 3 * plane_box_rows(R, P) * 128 <= 36864) ? 3
+         : (n % 2 == 0 && 2 * plane_box_rows(R, P) * 128 <= 36864) ? 2
+                                                                    : 1;
+}
 // Floats per published partial (R sums + the sum of squares), padded to 16 bytes.
 __host__ __device__ constexpr int partial_stride(int R) { return ((R + 1 + 3) / 4) * 4; }
+// Floats per Sinkhorn hand-off entry: the n*n residual logits of one token.
+__host__ __device__ constexpr int sink_stride(int n) { return n * n; }
 
 // Byte offsets of the forward kernel's shared-memory regions (after the
 // base is rounded up to 1024); `total` includes that rounding slack.  The
-// phi ring follows the x ring and the y ring follows the phi ring, so an
-// operand read that runs past a ring's last slot stays inside the window.
+// rings are laid out x, w, y back to back, so an operand read that runs past
+// a slot stays inside the window.
 struct SmemLayout {
-  size_t x, w, y, part, ssq, coef, tail, total;
+  size_t x, w, y, part, coef, sink, tail, total;
 };
 __host__ __device__ inline SmemLayout smem_layout(int n, int R, int P, int xs, int ws, int ys) {
   SmemLayout L;
   size_t o = 0;
   L.x = o;    o += (size_t)xs * stream_group(n) * kStreamTile;
-  L.w = o;    o += (size_t)ws * plane_box_rows(R, P) * 128;
+  L.w = o;    o += (size_t)ws * w_group(n, R, P) * plane_box_rows(R, P) * 128;
   o = (o + 1023) & ~size_t(1023);
   L.y = o;    o += (size_t)ys * n * y_box_tokens(n) * 128;
-  L.part = o; o += 2 * (size_t)kTileT * partial_stride(R) * 4;
-  L.ssq = o;  o += 2 * (size_t)kTileT * 4;
+  L.part = o; o += (size_t)kTileT * partial_stride(R) * 4;
   L.coef = o; o += (size_t)kCoefBufs * kTileT * n * 4;
+  L.sink = o; o += 2 * (size_t)kTileT * sink_stride(n) * 4;
   o = (o + 15) & ~size_t(15);
   L.tail = o; o += kTailBytes;
   L.total = o + 1024;
@@ -257,7 +279,7 @@ struct Geometry {
 struct TcLaunch {
   EpiParams epi;
   CUtensorMap tmap_x;      // x as (D, T, n): box (64, 64 tokens, stream group), 128B swizzle
-  CUtensorMap tmap_w;      // planes as (D, NP, n): box (64, plane rows, 1), 128B swizzle
+  CUtensorMap tmap_w;      // planes as (D, NP, n): box (64, plane rows, n), 128B swizzle
   CUtensorMap tmap_y;      // x as (D, T, n): box (64, y tokens, n), 128B swizzle
   int NP, P;
   int cluster;             // CTAs per token tile (split over d-chunks)

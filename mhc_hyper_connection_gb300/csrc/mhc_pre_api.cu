@@ -261,7 +261,8 @@ mhc_status_t mhc_pre_run(mhc_pre_t h, const mhc_pre_args* a, void* stream) {
     const uint64_t xs[2] = {K2, (uint64_t)D * 2};
     const uint32_t xb[3] = {(uint32_t)mhc::kChunkK, (uint32_t)mhc::kTileT, (uint32_t)mhc::stream_group(n)};
     const uint64_t wd[3] = {(uint64_t)D, (uint64_t)NP, (uint64_t)n};
-    const uint32_t wb[3] = {(uint32_t)mhc::kChunkK, (uint32_t)mhc::plane_box_rows(R, h->P), 1};
+    const uint32_t wb[3] = {(uint32_t)mhc::kChunkK, (uint32_t)mhc::plane_box_rows(R, h->P),
+                            (uint32_t)mhc::w_group(n, R, h->P)};
     const uint32_t yb[3] = {(uint32_t)mhc::kChunkK, (uint32_t)mhc::y_box_tokens(n), (uint32_t)n};
     if (!encode_3d(&L.tmap_x, a->x, xd, xs, xb) || !encode_3d(&L.tmap_w, planes, wd, xs, wb) ||
         !encode_3d(&L.tmap_y, a->x, xd, xs, yb))

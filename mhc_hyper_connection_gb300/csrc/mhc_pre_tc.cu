@@ -252,19 +252,26 @@ __device__ __forceinline__ bool role_all(bool ok) {
 // ------------------------------------------------------------ kernel body
 template <int NS, int RR, int P>
 struct Cfg {
-  static constexpr int kNP = ((P * RR + 15) / 16) * 16;          // MMA N
+  static constexpr int kNP = ((P * RR + 15) / 16) * 16;          // MMA N of the projection
   static_assert(kNP <= 256, "N of one MMA is at most 256");
-  static constexpr int kAccCols = kNP <= 32 ? 32 : kNP <= 64 ? 64 : kNP <= 128 ? 128 : 256;
-  static constexpr uint32_t kTmemCols = 2 * kAccCols;   // two accumulator buffers
-  static constexpr int kSG = stream_group(NS);           // streams per x box
-  static constexpr int kGroups = NS / kSG;               // x boxes per d-chunk
+  static constexpr int kSsqCol = kNP;                            // x.x^T block (64 columns) after it
+  static constexpr int kCols = kNP + kTileT;
+  static constexpr int kAccCols = kCols <= 64 ? 64 : kCols <= 128 ? 128 : kCols <= 256 ? 256 : 512;
+  static constexpr int kAccBufs = 512 / kAccCols >= 2 ? 2 : 1;   // accumulator buffers
+  static constexpr uint32_t kTmemCols = (uint32_t)(kAccCols * kAccBufs);
+  static constexpr int kSG = stream_group(NS);                   // streams per x box
+  static constexpr int kGroups = NS / kSG;                       // x boxes per d-chunk
   static_assert(NS % kSG == 0, "stream groups tile the streams");
-  static constexpr int kXBytes = kSG * kStreamTile;      // one x box
+  static constexpr int kXBytes = kSG * kStreamTile;              // one x box
   static constexpr int kWRows = plane_box_rows(RR, P);
-  static constexpr int kWBytes = kWRows * 128;           // one phi-plane box (one stream)
-  static constexpr int kTY = y_box_tokens(NS);           // tokens per y box
+  static constexpr int kWG = w_group(NS, RR, P);                 // streams per w box
+  static constexpr int kWBoxes = NS / kWG;                       // w boxes per d-chunk
+  static constexpr int kWBytes = kWG * kWRows * 128;             // one w box
+  static constexpr int kTY = y_box_tokens(NS);                   // tokens per y box
   static constexpr int kYBytes = NS * kTY * 128;
-  static constexpr int kStr = partial_stride(RR);        // floats per published partial
+  static constexpr int kStr = partial_stride(RR);                // floats per published partial
+  static constexpr int kSink = sink_stride(NS);
+  static constexpr bool kThree = (RR == NS * NS + 2 * NS);
   static constexpr int kVecPerThread = kTY * (kChunkK / 8) / 128;
   static_assert(kVecPerThread >= 1 && kTY * (kChunkK / 8) % 128 == 0, "y box must split over 128 threads");
 };
@@ -274,22 +281,33 @@ struct SmemTail {
   uint64_t w_full[kMaxStages], w_empty[kMaxStages];
   uint64_t y_full[kMaxStages], y_empty[kMaxStages];
   uint64_t acc_full[2], acc_empty[2];
-  uint64_t ssq_full[2], ssq_empty[2];
-  uint64_t part_full[2], part_free[2];
+  uint64_t part_full, part_free;
   uint64_t coef_full[kCoefBufs], coef_free[kCoefBufs];
+  uint64_t sink_full[2], sink_free[2];
   uint64_t mma_done;
   uint32_t tmem_base;
   uint32_t abort;
+  uint32_t x_tiles_issued;      // tiles whose x boxes the x producer has issued
 };
 static_assert(sizeof(SmemTail) <= kTailBytes, "barrier block outgrew its reservation");
 
-// Warp roles.
-constexpr int kWarpProducer = 0, kWarpMma = 1, kWarpSsq0 = 2, kWarpPub0 = 4, kWarpGate0 = 6, kWarpY0 = 8;
-// Named barriers: 1 = publish pair, 2 = gate pair (64 threads each), 3 = y warps (128).
-constexpr int kBarPub = 1, kBarGate = 2, kBarY = 3;
+// Warp roles: one TMA producer per ring, so each ring has its own issuing thread.
+constexpr int kWarpX = 0, kWarpMma = 1, kWarpW = 2, kWarpY = 3, kWarpPub0 = 4, kWarpGate = 6,
+              kWarpSink = 7, kWarpYc0 = 8;
+// Named barriers: 1 = publish pair (64 threads), 2 = y warps (128).
+constexpr int kBarPub = 1, kBarY = 2;
 
 // Offset of 16-byte column c of row r in a 128-byte-swizzled tile.
 __device__ __forceinline__ int sw128(int r, int c) { return r * 128 + ((c ^ (r & 7)) << 4); }
+
+// 32 consecutive fp32 columns of this warp's 32 TMEM lanes (load + wait).
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
+  float a[16], b[16];
+  tmem_ld16(taddr, a);
+  tmem_ld16(taddr + 16, b);
+#pragma unroll
+  for (int i = 0; i < 16; ++i) { v[i] = a[i]; v[16 + i] = b[i]; }
+}
 
 template <int NS, int RR, int P>
 __global__ void __launch_bounds__(kThreads, 1)
@@ -304,9 +322,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t* sX = smem + Ly.x;
   uint8_t* sW = smem + Ly.w;
   uint8_t* sY = smem + Ly.y;
-  float* recv = reinterpret_cast<float*>(smem + Ly.part);     // [2][CL][64/CL][kStr]
-  float* ssq_buf = reinterpret_cast<float*>(smem + Ly.ssq);   // [2][64]
+  float* recv = reinterpret_cast<float*>(smem + Ly.part);     // [CL][64/CL][kStr]
   float* coef_buf = reinterpret_cast<float*>(smem + Ly.coef); // [kCoefBufs][64][NS]
+  float* sink_buf = reinterpret_cast<float*>(smem + Ly.sink); // [2][64][n*n] residual logits
   SmemTail* tail = reinterpret_cast<SmemTail*>(smem + Ly.tail);
 
   const int warp = threadIdx.x >> 5;
@@ -318,8 +336,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int c0 = (int)((long long)rank * g.nd / CL);
   const int c1 = (int)((long long)(rank + 1) * g.nd / CL);
   const int my_chunks = c1 - c0;                  // d-chunks owned by this CTA
-  const int xper_tile = my_chunks * C::kGroups;   // x boxes per tile
-  const int wper_tile = my_chunks * NS;           // phi-plane boxes per tile
   const int rpo = kTileT / CL;                    // tile rows each member reduces (owns)
   Ctl ctl{&tail->abort, err};
 
@@ -327,7 +343,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0) {
     for (int s = 0; s < XS; ++s) {
       mbar_init(&tail->x_full[s], 1);
-      mbar_init(&tail->x_empty[s], 1 + 2);      // MMA commit + two sum-of-squares warps
+      mbar_init(&tail->x_empty[s], 1);          // MMA commit
     }
     for (int s = 0; s < WS; ++s) {
       mbar_init(&tail->w_full[s], 1);
@@ -340,17 +356,18 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int b = 0; b < 2; ++b) {
       mbar_init(&tail->acc_full[b], 1);
       mbar_init(&tail->acc_empty[b], 2);        // two publish warps
-      mbar_init(&tail->ssq_full[b], 2);
-      mbar_init(&tail->ssq_empty[b], 2);
-      mbar_init(&tail->part_full[b], CL);       // one arrival per cluster member
-      mbar_init(&tail->part_free[b], CL);
+      mbar_init(&tail->sink_full[b], 1);
+      mbar_init(&tail->sink_free[b], 1);
     }
     for (int b = 0; b < kCoefBufs; ++b) {
       mbar_init(&tail->coef_full[b], CL);
       mbar_init(&tail->coef_free[b], CL);
     }
+    mbar_init(&tail->part_full, CL);            // one arrival per cluster member
+    mbar_init(&tail->part_free, CL);
     mbar_init(&tail->mma_done, 1);
     tail->abort = 0u;
+    tail->x_tiles_issued = 0u;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     tma_prefetch_desc(&tmap_x);
     tma_prefetch_desc(&tmap_w);
@@ -369,180 +386,158 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tmem_base = tail->tmem_base;
 
-  if (warp == kWarpProducer) {
-    // ================================================= TMA producer (three rings)
-    // x ring: (d-chunk, stream group) boxes of a tile, from HBM.  phi ring:
-    // (d-chunk, stream) plane boxes, from L2.  y ring: (d-chunk, token half)
-    // boxes of all streams, re-read from L2 once all of the tile's x boxes
-    // were issued.  Rings are polled without blocking, so none stalls another.
+  if (warp == kWarpX) {
+    // ================================================= x producer (HBM)
     if (lane == 0) {
-      const uint64_t keep = policy_evict_last(), drop = policy_evict_first();
-      int xt = cluster_id, xq = 0, xs = 0;
-      uint32_t xph = 0, xk = 0;
-      int wt = cluster_id, wq = 0, ws = 0;
-      uint32_t wph = 0;
-      int yt = cluster_id, yq = 0, ys = 0;
-      uint32_t yph = 0, yk = 0;
-      bool xdone = xt >= g.num_tiles, wdone = wt >= g.num_tiles, ydone = yt >= g.num_tiles;
-      long long xiss = 0, wiss = 0, yiss = 0;
-      uint32_t idle = 0;
-      uint64_t idle_since = 0;
-      while (!xdone || !wdone || !ydone) {
-        bool prog = false;
-        if (!xdone && mbar_poll(&tail->x_empty[xs], xph ^ 1u)) {
-          const int j = c0 + xq / C::kGroups;
-          const int grp = xq - (xq / C::kGroups) * C::kGroups;
-          mbar_expect_tx(&tail->x_full[xs], (uint32_t)C::kXBytes);
-          tma_load_3d_hint(sX + (size_t)xs * C::kXBytes, &tmap_x, &tail->x_full[xs], j * kChunkK,
-                           xt * kTileT, grp * C::kSG, keep);
-          ++xiss;
-          if (++xq == xper_tile) { xq = 0; xt += num_clusters; ++xk; xdone = xt >= g.num_tiles; }
-          if (++xs == XS) { xs = 0; xph ^= 1u; }
-          prog = true;
-        }
-        if (!wdone && mbar_poll(&tail->w_empty[ws], wph ^ 1u)) {
-          const int j = c0 + wq / NS;
-          const int i = wq - (wq / NS) * NS;
-          mbar_expect_tx(&tail->w_full[ws], (uint32_t)C::kWBytes);
-          tma_load_3d_hint(sW + (size_t)ws * C::kWBytes, &tmap_w, &tail->w_full[ws], j * kChunkK, 0, i, keep);
-          ++wiss;
-          if (++wq == wper_tile) { wq = 0; wt += num_clusters; wdone = wt >= g.num_tiles; }
-          if (++ws == WS) { ws = 0; wph ^= 1u; }
-          prog = true;
-        }
-        if (!ydone && yk < xk && mbar_poll(&tail->y_empty[ys], yph ^ 1u)) {
-          const int rows = min(kTileT, g.T - yt * kTileT);
-          const int halves = (rows + C::kTY - 1) / C::kTY;
-          const int jj = c1 - 1 - yq / halves;     // newest d-chunk first (likeliest in L2)
-          const int h = yq - (yq / halves) * halves;
-          mbar_expect_tx(&tail->y_full[ys], (uint32_t)C::kYBytes);
-          tma_load_3d_hint(sY + (size_t)ys * C::kYBytes, &tmap_y, &tail->y_full[ys], jj * kChunkK,
-                           yt * kTileT + h * C::kTY, 0, drop);
-          ++yiss;
-          if (++yq == my_chunks * halves) { yq = 0; yt += num_clusters; ++yk; ydone = yt >= g.num_tiles; }
-          if (++ys == YS) { ys = 0; yph ^= 1u; }
-          prog = true;
-        }
-        if (prog) {
-          idle = 0;
-        } else if ((++idle & 63u) != 0) {
-          __nanosleep(32);   // leave issue slots to the warps sharing this scheduler
-        } else {
-          if (*ctl.abort) break;
-          const uint64_t now = now_ns();
-          if (idle_since == 0 || idle == 64) idle_since = now;
-          if (now - idle_since > kWaitNs) {
-            atomicOr(err, kErrWaitTimeout);
-            *ctl.abort = 1u;
-            break;
+      const uint64_t keep = policy_evict_last();
+      int xs = 0;
+      uint32_t xph = 0, done_tiles = 0;
+      long long iss = 0;
+      bool ok = true;
+      for (int tile = cluster_id; tile < g.num_tiles && ok; tile += num_clusters) {
+        for (int j = c0; j < c1 && ok; ++j) {
+          for (int grp = 0; grp < C::kGroups; ++grp) {
+            if (!wait_bar<false>(&tail->x_empty[xs], xph ^ 1u, ctl, kErrWaitTimeout)) { ok = false; break; }
+            mbar_expect_tx(&tail->x_full[xs], (uint32_t)C::kXBytes);
+            tma_load_3d_hint(sX + (size_t)xs * C::kXBytes, &tmap_x, &tail->x_full[xs], j * kChunkK,
+                             tile * kTileT, grp * C::kSG, keep);
+            ++iss;
+            if (++xs == XS) { xs = 0; xph ^= 1u; }
           }
         }
+        if (ok) {
+          ++done_tiles;
+          *reinterpret_cast<volatile uint32_t*>(&tail->x_tiles_issued) = done_tiles;
+        }
       }
-      // Let every copy this thread started land before the CTA can exit.
-      for (long long q = 0; q < (xiss < XS ? xiss : XS); ++q) {
+      for (long long q = 0; q < (iss < XS ? iss : XS); ++q) {     // let issued copies land
         if (--xs < 0) { xs = XS - 1; xph ^= 1u; }
         wait_bar<false>(&tail->x_full[xs], xph, ctl, kErrWaitTimeout);
       }
-      for (long long q = 0; q < (wiss < WS ? wiss : WS); ++q) {
+    }
+  } else if (warp == kWarpW) {
+    // ================================================= phi-plane producer (L2)
+    if (lane == 0) {
+      const uint64_t keep = policy_evict_last();
+      int ws = 0;
+      uint32_t wph = 0;
+      long long iss = 0;
+      bool ok = true;
+      for (int tile = cluster_id; tile < g.num_tiles && ok; tile += num_clusters) {
+        for (int j = c0; j < c1 && ok; ++j) {
+          for (int wg = 0; wg < C::kWBoxes; ++wg) {
+            if (!wait_bar<false>(&tail->w_empty[ws], wph ^ 1u, ctl, kErrWaitTimeout)) { ok = false; break; }
+            mbar_expect_tx(&tail->w_full[ws], (uint32_t)C::kWBytes);
+            tma_load_3d_hint(sW + (size_t)ws * C::kWBytes, &tmap_w, &tail->w_full[ws], j * kChunkK, 0,
+                             wg * C::kWG, keep);
+            ++iss;
+            if (++ws == WS) { ws = 0; wph ^= 1u; }
+          }
+        }
+      }
+      for (long long q = 0; q < (iss < WS ? iss : WS); ++q) {
         if (--ws < 0) { ws = WS - 1; wph ^= 1u; }
         wait_bar<false>(&tail->w_full[ws], wph, ctl, kErrWaitTimeout);
       }
-      for (long long q = 0; q < (yiss < YS ? yiss : YS); ++q) {
+    }
+  } else if (warp == kWarpY) {
+    // ================================================= y re-read producer (L2)
+    // Re-reads a tile's x once its x boxes were all issued, newest d-chunk first.
+    if (lane == 0) {
+      const uint64_t drop = policy_evict_first();
+      int ys = 0;
+      uint32_t yph = 0, k = 0;
+      long long iss = 0;
+      bool ok = true;
+      for (int tile = cluster_id; tile < g.num_tiles && ok; tile += num_clusters, ++k) {
+        // wait (bounded) until the x producer has issued this tile
+        const uint64_t t0 = now_ns();
+        while (*reinterpret_cast<volatile uint32_t*>(&tail->x_tiles_issued) <= k) {
+          if (*ctl.abort) { ok = false; break; }
+          if (now_ns() - t0 > kWaitNs) {
+            atomicOr(err, kErrWaitTimeout);
+            *ctl.abort = 1u;
+            ok = false;
+            break;
+          }
+          __nanosleep(64);
+        }
+        if (!ok) break;
+        const int rows = min(kTileT, g.T - tile * kTileT);
+        const int halves = (rows + C::kTY - 1) / C::kTY;
+        for (int jj = c1 - 1; jj >= c0 && ok; --jj) {
+          for (int h = 0; h < halves; ++h) {
+            if (!wait_bar<false>(&tail->y_empty[ys], yph ^ 1u, ctl, kErrWaitTimeout)) { ok = false; break; }
+            mbar_expect_tx(&tail->y_full[ys], (uint32_t)C::kYBytes);
+            tma_load_3d_hint(sY + (size_t)ys * C::kYBytes, &tmap_y, &tail->y_full[ys], jj * kChunkK,
+                             tile * kTileT + h * C::kTY, 0, drop);
+            ++iss;
+            if (++ys == YS) { ys = 0; yph ^= 1u; }
+          }
+        }
+      }
+      for (long long q = 0; q < (iss < YS ? iss : YS); ++q) {
         if (--ys < 0) { ys = YS - 1; yph ^= 1u; }
         wait_bar<false>(&tail->y_full[ys], yph, ctl, kErrWaitTimeout);
       }
     }
   } else if (warp == kWarpMma) {
     // ================================================= MMA issuer
+    // Per stream of each d-chunk: the projection (N = NP) and x.x^T (N = 64,
+    // whose diagonal is each token's sum of squares), both into TMEM.
     if (lane == 0) {
-      constexpr uint32_t idesc = idesc_bf16(kMmaM, C::kNP);
+      constexpr uint32_t idesc_proj = idesc_bf16(kMmaM, C::kNP);
+      constexpr uint32_t idesc_ssq = idesc_bf16(kMmaM, kTileT);
       int xs = 0, ws = 0, acc = 0;
       uint32_t xph = 0, wph = 0, acc_phase = 0;
       bool ok = true;
       for (int tile = cluster_id; tile < g.num_tiles && ok; tile += num_clusters) {
         if (!wait_bar<false>(&tail->acc_empty[acc], acc_phase ^ 1u, ctl, kErrWaitTimeout)) break;
         tc_fence_after();
-        const uint32_t d_tmem = tmem_base + (uint32_t)(acc * C::kAccCols);
+        const uint32_t d_proj = tmem_base + (uint32_t)(acc * C::kAccCols);
+        const uint32_t d_ssq = d_proj + (uint32_t)C::kSsqCol;
         bool first = true;
-        for (int q = 0; q < xper_tile && ok; ++q) {
-          if (!wait_bar<false>(&tail->x_full[xs], xph, ctl, kErrWaitTimeout)) { ok = false; break; }
-          const uint32_t xbase = smem_u32(sX + (size_t)xs * C::kXBytes);
-          for (int il = 0; il < C::kSG; ++il) {
-            if (!wait_bar<false>(&tail->w_full[ws], wph, ctl, kErrWaitTimeout)) { ok = false; break; }
+        for (int j = c0; j < c1 && ok; ++j) {
+          uint32_t xbase = 0, wbase = 0;
+          for (int i = 0; i < NS; ++i) {
+            if (i % C::kWG == 0) {
+              if (!wait_bar<false>(&tail->w_full[ws], wph, ctl, kErrWaitTimeout)) { ok = false; break; }
+              wbase = smem_u32(sW + (size_t)ws * C::kWBytes);
+            }
+            if (i % C::kSG == 0) {
+              if (!wait_bar<false>(&tail->x_full[xs], xph, ctl, kErrWaitTimeout)) { ok = false; break; }
+              xbase = smem_u32(sX + (size_t)xs * C::kXBytes);
+            }
             tc_fence_after();
-            // 128-row operand: rows 0..63 are this stream's tokens; rows 64..127
-            // read on into the next stream (or ring) and feed only lanes never read.
-            const uint32_t a0 = xbase + il * kStreamTile;
-            const uint32_t b0 = smem_u32(sW + (size_t)ws * C::kWBytes);
+            // A: 128 rows from this stream's token tile (rows 64..127 run on
+            // into the next tile and feed lanes that are never read).
+            const uint32_t a0 = xbase + (uint32_t)((i % C::kSG) * kStreamTile);
+            const uint32_t b0 = wbase + (uint32_t)((i % C::kWG) * C::kWRows * 128);
 #pragma unroll
             for (int kk = 0; kk < kChunkK / 16; ++kk) {
-              mma_bf16(d_tmem, sw128_desc(a0 + kk * 32), sw128_desc(b0 + kk * 32), idesc, first ? 0u : 1u);
+              const uint32_t acc_in = first ? 0u : 1u;
+              mma_bf16(d_proj, sw128_desc(a0 + kk * 32), sw128_desc(b0 + kk * 32), idesc_proj, acc_in);
+              mma_bf16(d_ssq, sw128_desc(a0 + kk * 32), sw128_desc(a0 + kk * 32), idesc_ssq, acc_in);
               first = false;
             }
-            mma_commit(&tail->w_empty[ws]);       // frees the plane slot when these MMAs finish
-            if (++ws == WS) { ws = 0; wph ^= 1u; }
+            if (i % C::kSG == C::kSG - 1) {          // frees the x slot when these MMAs finish
+              mma_commit(&tail->x_empty[xs]);
+              if (++xs == XS) { xs = 0; xph ^= 1u; }
+            }
+            if (i % C::kWG == C::kWG - 1) {
+              mma_commit(&tail->w_empty[ws]);
+              if (++ws == WS) { ws = 0; wph ^= 1u; }
+            }
           }
-          if (!ok) break;
-          mma_commit(&tail->x_empty[xs]);
-          if (++xs == XS) { xs = 0; xph ^= 1u; }
         }
         if (!ok) break;
         mma_commit(&tail->acc_full[acc]);          // accumulator complete
-        if (++acc == 2) { acc = 0; acc_phase ^= 1u; }
+        if (++acc == C::kAccBufs) { acc = 0; acc_phase ^= 1u; }
       }
       mma_commit(&tail->mma_done);
       wait_bar<false>(&tail->mma_done, 0, ctl, kErrWaitTimeout);
     }
-  } else if (warp < kWarpPub0) {
-    // ================================================= sum of squares (thread = token row)
-    const int row = threadIdx.x - kWarpSsq0 * 32;  // 0..63
-    int xs = 0;
-    uint32_t xph = 0;
-    int b = 0;
-    uint32_t bphase = 0;
-    bool ok = true;
-    for (int tile = cluster_id; tile < g.num_tiles && ok; tile += num_clusters) {
-      if (!__all_sync(0xffffffffu, wait_bar<false>(&tail->ssq_empty[b], bphase ^ 1u, ctl, kErrWaitTimeout)))
-        break;
-      float acc = 0.0f;
-      for (int q = 0; q < xper_tile; ++q) {
-        if (!__all_sync(0xffffffffu, wait_bar<false>(&tail->x_full[xs], xph, ctl, kErrWaitTimeout))) {
-          ok = false;
-          break;
-        }
-        const uint8_t* box = sX + (size_t)xs * C::kXBytes;
-#pragma unroll
-        for (int il = 0; il < C::kSG; ++il) {
-          const uint8_t* rowp = box + il * kStreamTile + row * 128;
-          float part8[8];
-#pragma unroll
-          for (int p = 0; p < 8; ++p) {
-            // Rotate the 16-byte column by row so a warp's loads hit distinct banks.
-            const int col = (p + row) & 7;
-            const uint4 v = *reinterpret_cast<const uint4*>(rowp + col * 16);
-            const __nv_bfloat162* hv = reinterpret_cast<const __nv_bfloat162*>(&v);
-            float a = 0.0f, bb = 0.0f;
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              const float2 f = __bfloat1622float2(hv[e]);
-              a = fmaf(f.x, f.x, a);
-              bb = fmaf(f.y, f.y, bb);
-            }
-            part8[p] = a + bb;
-          }
-          acc += tree_sum<8>(part8);
-        }
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&tail->x_empty[xs]);
-        if (++xs == XS) { xs = 0; xph ^= 1u; }
-      }
-      if (!ok) break;
-      ssq_buf[b * kTileT + row] = acc;
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&tail->ssq_full[b]);
-      if (++b == 2) { b = 0; bphase ^= 1u; }
-    }
-  } else if (warp < kWarpGate0) {
+  } else if (warp < kWarpGate) {
     // ================================================= publish partial sums
     // Thread = tile row = TMEM lane.  Each row's partial projection (this
     // member's d-range) and partial sum of squares go to the member that
@@ -571,22 +566,22 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (col < P * RR) mix[col % RR] += v[e];
         }
       }
+      float ssq = 0.0f;
+      {
+        float v[32];
+        tmem_ld32(taddr + (uint32_t)(C::kSsqCol + wq * 32), v);
+#pragma unroll
+        for (int e = 0; e < 32; ++e) ssq = (e == lane) ? v[e] : ssq;   // diagonal of x.x^T
+      }
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&tail->acc_empty[acc]);
-      if (++acc == 2) { acc = 0; acc_phase ^= 1u; }
-      const int b = (int)(k & 1u);
-      if (!role_all<kBarPub, 64>(wait_bar<false>(&tail->ssq_full[b], (k >> 1) & 1u, ctl, kErrWaitTimeout))) break;
-      const float ssq = ssq_buf[b * kTileT + et];
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&tail->ssq_empty[b]);
+      if (++acc == C::kAccBufs) { acc = 0; acc_phase ^= 1u; }
 
-      const int pb = (int)(k & 1u);
-      const uint32_t use = k >> 1;                 // earlier uses of buffer pb
-      if (use > 0 &&
-          !role_all<kBarPub, 64>(wait_bar<true>(&tail->part_free[pb], (use - 1) & 1u, ctl, kErrClusterWait)))
+      // every owner must have consumed the previous tile's partials
+      if (k > 0 && !role_all<kBarPub, 64>(wait_bar<true>(&tail->part_free, (k - 1) & 1u, ctl, kErrClusterWait)))
         break;
-      float* dst = recv + ((size_t)(pb * CL + (int)rank) * rpo + slot) * C::kStr;
+      float* dst = recv + ((size_t)((int)rank * rpo + slot)) * C::kStr;
 #pragma unroll
       for (int r = 0; r < C::kStr; r += 4) {
         float4 v;
@@ -597,75 +592,114 @@ __global__ void __launch_bounds__(kThreads, 1)
         st_dsmem_v4(dst + r, (uint32_t)owner, v);
       }
       role_sync<kBarPub, 64>();
-      if (et < CL) mbar_arrive_remote(&tail->part_full[pb], (uint32_t)et);
+      if (et < CL) mbar_arrive_remote(&tail->part_full, (uint32_t)et);
     }
-  } else if (warp < kWarpY0) {
-    // ================================================= gates (critical for y), then Sinkhorn
-    // Owned rows: sum the members' partials in rank order, compute invRms
-    // and the gates, publish the y weights to every member, then run the
-    // Sinkhorn for comb, which y does not wait for.
-    const int ot = threadIdx.x - kWarpGate0 * 32;  // 0..63
+  } else if (warp == kWarpGate) {
+    // ================================================= gates (critical for y)
+    // Owned rows: sum the members' partials in rank order, compute invRms and
+    // the gates, publish the y weights to every member, hand the row to the
+    // Sinkhorn warp.
     uint32_t k = 0;
     for (int tile = cluster_id; tile < g.num_tiles; tile += num_clusters, ++k) {
-      const int pb = (int)(k & 1u);
-      const uint32_t use = k >> 1;
-      if (!role_all<kBarGate, 64>(wait_bar<true>(&tail->part_full[pb], use & 1u, ctl, kErrClusterWait))) break;
-      const bool active = ot < rpo;
-      const int row = (int)rank * rpo + ot;
-      const int tok = tile * kTileT + row;
-      float mix[RR];
-      float ssq = 0.0f;
-      if (active) {
-        float tot[C::kStr];
+      if (!__all_sync(0xffffffffu, wait_bar<true>(&tail->part_full, k & 1u, ctl, kErrClusterWait))) break;
+      float mix[2][RR];
+      float ssq[2] = {0.0f, 0.0f};
 #pragma unroll
-        for (int r = 0; r < C::kStr; ++r) tot[r] = 0.0f;
-        for (int cr = 0; cr < CL; ++cr) {
-          const float* src = recv + ((size_t)(pb * CL + cr) * rpo + ot) * C::kStr;
+      for (int h = 0; h < 2; ++h) {
+        const int ot = lane + 32 * h;
+        if (ot < rpo) {
+          float tot[C::kStr];
 #pragma unroll
-          for (int r = 0; r < C::kStr; r += 4) {
-            const float4 v = *reinterpret_cast<const float4*>(src + r);
-            tot[r] += v.x;
-            tot[r + 1] += v.y;
-            tot[r + 2] += v.z;
-            tot[r + 3] += v.w;
+          for (int r = 0; r < C::kStr; ++r) tot[r] = 0.0f;
+          for (int cr = 0; cr < CL; ++cr) {
+            const float* src = recv + ((size_t)(cr * rpo + ot)) * C::kStr;
+#pragma unroll
+            for (int r = 0; r < C::kStr; r += 4) {
+              const float4 v = *reinterpret_cast<const float4*>(src + r);
+              tot[r] += v.x;
+              tot[r + 1] += v.y;
+              tot[r + 2] += v.z;
+              tot[r + 3] += v.w;
+            }
           }
-        }
 #pragma unroll
-        for (int r = 0; r < RR; ++r) mix[r] = tot[r];
-        ssq = tot[RR];
+          for (int r = 0; r < RR; ++r) mix[h][r] = tot[r];
+          ssq[h] = tot[RR];
+        }
       }
-      role_sync<kBarGate, 64>();
-      if (ot < CL) mbar_arrive_remote(&tail->part_free[pb], (uint32_t)ot);
+      __syncwarp();
+      if (lane < CL) mbar_arrive_remote(&tail->part_free, (uint32_t)lane);
 
       const int cb = (int)(k % kCoefBufs);
       const uint32_t cuse = k / kCoefBufs;
       if (cuse > 0 &&
-          !role_all<kBarGate, 64>(wait_bar<true>(&tail->coef_free[cb], (cuse - 1) & 1u, ctl, kErrClusterWait)))
+          !__all_sync(0xffffffffu, wait_bar<true>(&tail->coef_free[cb], (cuse - 1) & 1u, ctl, kErrClusterWait)))
         break;
-      float inv_rms = 0.0f;
-      if (active) {
-        const bool write = tok < g.T;
-        float cf[NS];
-        inv_rms = token_gates<NS, RR>(ep, tok, mix, ssq, write, cf);
-        float* dst = coef_buf + ((size_t)cb * kTileT + row) * NS;
-        for (int cr = 0; cr < CL; ++cr) {
-          if constexpr (NS % 4 == 0) {
+      float inv_rms[2] = {0.0f, 0.0f};
 #pragma unroll
-            for (int i = 0; i < NS; i += 4)
-              st_dsmem_v4(dst + i, (uint32_t)cr, make_float4(cf[i], cf[i + 1], cf[i + 2], cf[i + 3]));
-          } else {
+      for (int h = 0; h < 2; ++h) {
+        const int ot = lane + 32 * h;
+        if (ot < rpo) {
+          const int row = (int)rank * rpo + ot;
+          const int tok = tile * kTileT + row;
+          float cf[NS];
+          inv_rms[h] = token_gates<NS, RR>(ep, tok, mix[h], ssq[h], tok < g.T, cf);
+          float* dst = coef_buf + ((size_t)cb * kTileT + row) * NS;
+          for (int cr = 0; cr < CL; ++cr) {
+            if constexpr (NS % 4 == 0) {
 #pragma unroll
-            for (int i = 0; i < NS; ++i) st_dsmem_f32(dst + i, (uint32_t)cr, cf[i]);
+              for (int i = 0; i < NS; i += 4)
+                st_dsmem_v4(dst + i, (uint32_t)cr, make_float4(cf[i], cf[i + 1], cf[i + 2], cf[i + 3]));
+            } else {
+#pragma unroll
+              for (int i = 0; i < NS; ++i) st_dsmem_f32(dst + i, (uint32_t)cr, cf[i]);
+            }
           }
         }
       }
-      role_sync<kBarGate, 64>();
-      if (ot < CL) mbar_arrive_remote(&tail->coef_full[cb], (uint32_t)ot);
-      if (active) token_sinkhorn<NS, RR>(ep, tok, mix, inv_rms, tok < g.T);
+      __syncwarp();
+      if (lane < CL) mbar_arrive_remote(&tail->coef_full[cb], (uint32_t)lane);
+      // hand the owned rows to the Sinkhorn warp
+      const int sb = (int)(k & 1u);
+      if ((k >> 1) > 0 &&
+          !__all_sync(0xffffffffu, wait_bar<false>(&tail->sink_free[sb], ((k >> 1) - 1) & 1u, ctl, kErrWaitTimeout)))
+        break;
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const int ot = lane + 32 * h;
+        if (ot < rpo) {
+          float H[NS * NS];
+          residual_logits<NS, RR>(ep, mix[h], inv_rms[h], H);
+          float* e = sink_buf + ((size_t)sb * kTileT + ot) * C::kSink;
+#pragma unroll
+          for (int r = 0; r < NS * NS; ++r) e[r] = H[r];
+        }
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&tail->sink_full[sb]);
+    }
+  } else if (warp == kWarpSink) {
+    // ================================================= Sinkhorn for comb (off y's path)
+    uint32_t k = 0;
+    for (int tile = cluster_id; tile < g.num_tiles; tile += num_clusters, ++k) {
+      const int sb = (int)(k & 1u);
+      if (!__all_sync(0xffffffffu, wait_bar<false>(&tail->sink_full[sb], (k >> 1) & 1u, ctl, kErrWaitTimeout)))
+        break;
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const int ot = lane + 32 * h;
+        if (ot < rpo) {
+          const float* e = sink_buf + ((size_t)sb * kTileT + ot) * C::kSink;
+          const int tok = tile * kTileT + (int)rank * rpo + ot;
+          token_sinkhorn<NS, C::kThree>(ep, tok, e, tok < g.T);
+        }
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&tail->sink_free[sb]);
     }
   } else {
     // ================================================= y for this member's d-range
-    const int yt = threadIdx.x - kWarpY0 * 32;     // 0..127
+    const int yt = threadIdx.x - kWarpYc0 * 32;    // 0..127
     const uint64_t ystore_policy = policy_evict_first();
     int ys = 0;
     uint32_t yph = 0;
@@ -678,49 +712,48 @@ __global__ void __launch_bounds__(kThreads, 1)
       const float* coef = coef_buf + (size_t)cb * kTileT * NS;
       const int rows = min(kTileT, g.T - tile * kTileT);
       const int halves = (rows + C::kTY - 1) / C::kTY;
-      const int nyc = my_chunks * halves;
       bool ok = true;
-      for (int yq = 0; yq < nyc; ++yq) {
-        if (!role_all<kBarY, 128>(wait_bar<false>(&tail->y_full[ys], yph, ctl, kErrWaitTimeout))) {
-          ok = false;
-          break;
-        }
-        const int jj = c1 - 1 - yq / halves;
-        const int h = yq - (yq / halves) * halves;
-        const uint8_t* box = sY + (size_t)ys * C::kYBytes;   // [stream][token][128 B], swizzled
-#pragma unroll
-        for (int u = 0; u < C::kVecPerThread; ++u) {
-          const int v = yt + 128 * u;
-          const int tl = v >> 3;                   // token within the box
-          const int c = v & 7;                     // 16-byte column group
-          const int row = h * C::kTY + tl;
-          const int d = jj * kChunkK + c * 8;
-          if (row < rows && d < g.D) {
-            float acc8[8];
-#pragma unroll
-            for (int e = 0; e < 8; ++e) acc8[e] = 0.0f;
-#pragma unroll
-            for (int i = 0; i < NS; ++i) {
-              const float m = coef[row * NS + i];
-              const uint4 xv = *reinterpret_cast<const uint4*>(box + sw128(i * C::kTY + tl, c));
-              const __nv_bfloat162* hh = reinterpret_cast<const __nv_bfloat162*>(&xv);
-#pragma unroll
-              for (int q2 = 0; q2 < 4; ++q2) {
-                const float2 f = __bfloat1622float2(hh[q2]);
-                acc8[2 * q2] = fmaf(m, f.x, acc8[2 * q2]);
-                acc8[2 * q2 + 1] = fmaf(m, f.y, acc8[2 * q2 + 1]);
-              }
-            }
-            uint4 o;
-            __nv_bfloat162* ob = reinterpret_cast<__nv_bfloat162*>(&o);
-#pragma unroll
-            for (int q2 = 0; q2 < 4; ++q2) ob[q2] = __floats2bfloat162_rn(acc8[2 * q2], acc8[2 * q2 + 1]);
-            st_global_v4_hint(ep.y + ((size_t)(tile * kTileT + row) * g.D + d), o, ystore_policy);
+      for (int jj = c1 - 1; jj >= c0 && ok; --jj) {
+        for (int h = 0; h < halves; ++h) {
+          if (!role_all<kBarY, 128>(wait_bar<false>(&tail->y_full[ys], yph, ctl, kErrWaitTimeout))) {
+            ok = false;
+            break;
           }
+          const uint8_t* box = sY + (size_t)ys * C::kYBytes;   // [stream][token][128 B], swizzled
+#pragma unroll
+          for (int u = 0; u < C::kVecPerThread; ++u) {
+            const int v = yt + 128 * u;
+            const int tl = v >> 3;                 // token within the box
+            const int c = v & 7;                   // 16-byte column group
+            const int row = h * C::kTY + tl;
+            const int d = jj * kChunkK + c * 8;
+            if (row < rows && d < g.D) {
+              float acc8[8];
+#pragma unroll
+              for (int e = 0; e < 8; ++e) acc8[e] = 0.0f;
+#pragma unroll
+              for (int i = 0; i < NS; ++i) {
+                const float m = coef[row * NS + i];
+                const uint4 xv = *reinterpret_cast<const uint4*>(box + sw128(i * C::kTY + tl, c));
+                const __nv_bfloat162* hh = reinterpret_cast<const __nv_bfloat162*>(&xv);
+#pragma unroll
+                for (int q2 = 0; q2 < 4; ++q2) {
+                  const float2 f = __bfloat1622float2(hh[q2]);
+                  acc8[2 * q2] = fmaf(m, f.x, acc8[2 * q2]);
+                  acc8[2 * q2 + 1] = fmaf(m, f.y, acc8[2 * q2 + 1]);
+                }
+              }
+              uint4 o;
+              __nv_bfloat162* ob = reinterpret_cast<__nv_bfloat162*>(&o);
+#pragma unroll
+              for (int q2 = 0; q2 < 4; ++q2) ob[q2] = __floats2bfloat162_rn(acc8[2 * q2], acc8[2 * q2 + 1]);
+              st_global_v4_hint(ep.y + ((size_t)(tile * kTileT + row) * g.D + d), o, ystore_policy);
+            }
+          }
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&tail->y_empty[ys]);
+          if (++ys == YS) { ys = 0; yph ^= 1u; }
         }
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&tail->y_empty[ys]);
-        if (++ys == YS) { ys = 0; yph ^= 1u; }
       }
       if (!ok) break;
       role_sync<kBarY, 128>();                     // every y thread is done with coef[cb]
