@@ -219,7 +219,7 @@ constexpr int kMmaM = 128;         // rows of one tcgen05.mma (TMEM lanes)
 constexpr int kTileT = 64;         // tokens per tile: MMA rows 0..63 (rows 64..127 unused)
 constexpr int kChunkK = 64;        // bf16 elements per 128-byte swizzle row
 constexpr int kStreamTile = kTileT * 128;   // one stream of one d-chunk of a tile (8 KB)
-constexpr int kThreads = 384;      // 12 warps: 3 TMA producers, MMA, 2 publish, gates, Sinkhorn, 4 y
+constexpr int kThreads = 512;      // 16 warps: 2 TMA producers, MMA, 2 publish, gates, Sinkhorn, 8 y
 constexpr int kMaxStages = 8;      // ring depth limit (barrier arrays)
 constexpr int kCoefBufs = 3;       // y-weight buffers between the gate warps and the y warps
 constexpr size_t kTailBytes = 1024; // barriers and flags
@@ -229,8 +229,6 @@ constexpr size_t kTailBytes = 1024; // barriers and flags
 // n = 6.  Big boxes matter: one issuing thread completes only about two
 // boxes per microsecond, whatever their size.
 __host__ __device__ constexpr int stream_group(int n) { return n == 6 ? 3 : 4; }
-// Tokens per y box (64 columns x all n streams x this many tokens).
-__host__ __device__ constexpr int y_box_tokens(int n) { return n == 4 ? 64 : 32; }
 // Rows of one stream's phi planes in a w box: P*R rounded up to 8.  The
 // MMA's N = P*R rounded up to 16 reads the rest from the next stream (or
 // slot); those accumulator columns are never read.
@@ -248,19 +246,18 @@ __host__ __device__ constexpr int partial_stride(int R) { return ((R + 1 + 3) / 
 __host__ __device__ constexpr int sink_stride(int n) { return n * n; }
 
 // Byte offsets of the forward kernel's shared-memory regions (after the
-// base is rounded up to 1024); `total` includes that rounding slack.  The
-// rings are laid out x, w, y back to back, so an operand read that runs past
-// a slot stays inside the window.
+// base is rounded up to 1024); `total` includes that rounding slack.  The x
+// and w rings are back to back, so an operand read that runs past a slot
+// stays inside the window.
 struct SmemLayout {
-  size_t x, w, y, part, coef, sink, tail, total;
+  size_t x, w, part, coef, sink, tail, total;
 };
-__host__ __device__ inline SmemLayout smem_layout(int n, int R, int P, int xs, int ws, int ys) {
+__host__ __device__ inline SmemLayout smem_layout(int n, int R, int P, int xs, int ws) {
   SmemLayout L;
   size_t o = 0;
   L.x = o;    o += (size_t)xs * stream_group(n) * kStreamTile;
   L.w = o;    o += (size_t)ws * w_group(n, R, P) * plane_box_rows(R, P) * 128;
-  o = (o + 1023) & ~size_t(1023);
-  L.y = o;    o += (size_t)ys * n * y_box_tokens(n) * 128;
+  o += 8192;  // operand reads that run past the last w slot stay inside the window
   L.part = o; o += (size_t)kTileT * partial_stride(R) * 4;
   L.coef = o; o += (size_t)kCoefBufs * kTileT * n * 4;
   L.sink = o; o += 2 * (size_t)kTileT * sink_stride(n) * 4;
@@ -271,20 +268,20 @@ __host__ __device__ inline SmemLayout smem_layout(int n, int R, int P, int xs, i
 }
 
 struct Geometry {
-  int T, D;
+  int T, D, n;
   int num_tiles, nd;           // token tiles; 64-wide d-chunks per stream
-  int cluster, xstages, wstages, ystages;
+  int cluster, xstages, wstages;
 };
 
 struct TcLaunch {
   EpiParams epi;
+  const void* x;           // bf16 [T, n, D] (re-read for y)
   CUtensorMap tmap_x;      // x as (D, T, n): box (64, 64 tokens, stream group), 128B swizzle
   CUtensorMap tmap_w;      // planes as (D, NP, n): box (64, plane rows, n), 128B swizzle
-  CUtensorMap tmap_y;      // x as (D, T, n): box (64, y tokens, n), 128B swizzle
   int NP, P;
   int cluster;             // CTAs per token tile (split over d-chunks)
   int grid;                // CTAs (multiple of cluster)
-  int xstages, wstages, ystages;
+  int xstages, wstages;
   size_t smem_bytes;
   uint32_t* err_word;
 };

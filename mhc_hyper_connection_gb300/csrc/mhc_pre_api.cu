@@ -263,59 +263,61 @@ mhc_status_t mhc_pre_run(mhc_pre_t h, const mhc_pre_args* a, void* stream) {
     const uint64_t wd[3] = {(uint64_t)D, (uint64_t)NP, (uint64_t)n};
     const uint32_t wb[3] = {(uint32_t)mhc::kChunkK, (uint32_t)mhc::plane_box_rows(R, h->P),
                             (uint32_t)mhc::w_group(n, R, h->P)};
-    const uint32_t yb[3] = {(uint32_t)mhc::kChunkK, (uint32_t)mhc::y_box_tokens(n), (uint32_t)n};
-    if (!encode_3d(&L.tmap_x, a->x, xd, xs, xb) || !encode_3d(&L.tmap_w, planes, wd, xs, wb) ||
-        !encode_3d(&L.tmap_y, a->x, xd, xs, yb))
+    if (!encode_3d(&L.tmap_x, a->x, xd, xs, xb) || !encode_3d(&L.tmap_w, planes, wd, xs, wb))
       return fail(MHC_ERR_RUNTIME, "tensor map encoding failed");
   }
 
-  // Ring depths.  x boxes come from HBM and want the most bytes in flight;
-  // phi-plane and y boxes come from L2.  First try to keep >= 3 x boxes and
-  // 2 y boxes in flight (deepest x, then phi), then relax to (2, 2, 1).
+  // Ring depths: x boxes come from HBM and want the most bytes in flight,
+  // phi-plane boxes come from L2; deepest x ring first, then phi.
   const int nd = (D + mhc::kChunkK - 1) / mhc::kChunkK;
   const int num_tiles = (int)((T + mhc::kTileT - 1) / mhc::kTileT);
   const size_t budget = di.max_smem;
-  int xmax = env_int("MHC_PRE_XSTAGES", 4), wmax = env_int("MHC_PRE_WSTAGES", 4), ymax = env_int("MHC_PRE_YSTAGES", 2);
+  int xmax = env_int("MHC_PRE_XSTAGES", 6), wmax = env_int("MHC_PRE_WSTAGES", 3);
   xmax = xmax < 2 ? 2 : (xmax > mhc::kMaxStages ? mhc::kMaxStages : xmax);
   wmax = wmax < 2 ? 2 : (wmax > mhc::kMaxStages ? mhc::kMaxStages : wmax);
-  ymax = ymax < 1 ? 1 : (ymax > mhc::kMaxStages ? mhc::kMaxStages : ymax);
-  int xst = 0, wst = 0, yst = 0;
-  const int xmin_pass[2] = {xmax < 3 ? xmax : 3, 2};
-  for (int pass = 0; pass < 2 && !xst; ++pass)
-    for (int ysn = ymax; ysn >= (pass == 0 ? (ymax < 2 ? ymax : 2) : 1) && !xst; --ysn)
-      for (int xsn = xmax; xsn >= xmin_pass[pass] && !xst; --xsn)
-        for (int wsn = wmax; wsn >= 2; --wsn)
-          if (mhc::smem_layout(n, R, h->P, xsn, wsn, ysn).total <= budget) {
-            xst = xsn; wst = wsn; yst = ysn;
-            break;
-          }
+  int xst = 0, wst = 0;
+  for (int xsn = xmax; xsn >= 2 && !xst; --xsn)
+    for (int wsn = wmax; wsn >= 2; --wsn)
+      if (mhc::smem_layout(n, R, h->P, xsn, wsn).total <= budget) {
+        xst = xsn;
+        wst = wsn;
+        break;
+      }
   if (!xst) return fail(MHC_ERR_RUNTIME, "shape does not fit in shared memory");
-  const size_t smem = mhc::smem_layout(n, R, h->P, xst, wst, yst).total;
+  const size_t smem = mhc::smem_layout(n, R, h->P, xst, wst).total;
 
-  int want = env_int("MHC_PRE_CLUSTER", 16);
-  int cluster = 1;
+  // Cluster size: the one that keeps the most SMs busy on this many tiles
+  // (ties go to the smaller cluster, which exchanges less).  Larger clusters
+  // split a tile's d-range over more SMs, which is what small T needs.
+  const int want = env_int("MHC_PRE_CLUSTER", 16);
+  int cluster = 0;
   int max_clusters = 0;
-  for (int cand : {16, 8, 4, 2, 1}) {
+  long long best_sms = -1;
+  for (int cand : {1, 2, 4, 8, 16}) {
     if (cand > want || cand > nd) continue;
     int mc = 0;
-    if (mhc::tc_forward_occupancy(n, R, h->P, smem, cand, &mc) == cudaSuccess && mc > 0) {
+    if (mhc::tc_forward_occupancy(n, R, h->P, smem, cand, &mc) != cudaSuccess || mc <= 0) {
+      cudaGetLastError();
+      continue;
+    }
+    const long long sms = (long long)(num_tiles < mc ? num_tiles : mc) * cand;
+    if (sms > best_sms) {
+      best_sms = sms;
       cluster = cand;
       max_clusters = mc;
-      break;
     }
-    cudaGetLastError();
   }
   if (max_clusters <= 0) return fail(MHC_ERR_RUNTIME, "no cluster configuration fits this device");
   L.cluster = cluster;
   L.grid = (num_tiles < max_clusters ? num_tiles : max_clusters) * cluster;
+  L.x = a->x;
   L.xstages = xst;
   L.wstages = wst;
-  L.ystages = yst;
   L.smem_bytes = smem;
   h->last_cluster = cluster;
   h->last_grid = L.grid;
   h->last_stages = xst;
-  h->last_ystages = yst;
+  h->last_ystages = wst;
   if (h->ev_before && cudaEventRecord(h->ev_before, s) != cudaSuccess)
     return fail(MHC_ERR_RUNTIME, "recording the timing event failed");
   if (mhc::launch_tc_forward(L, s) != cudaSuccess)

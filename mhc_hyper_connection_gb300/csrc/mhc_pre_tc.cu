@@ -135,6 +135,13 @@ __device__ __forceinline__ uint64_t policy_evict_first() {
   asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
   return p;
 }
+__device__ __forceinline__ uint4 ld_global_v4_hint(const void* ptr, uint64_t policy) {
+  uint4 v;
+  asm volatile("ld.global.nc.L1::no_allocate.L2::cache_hint.v4.u32 {%0, %1, %2, %3}, [%4], %5;"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(ptr), "l"(policy));
+  return v;
+}
 __device__ __forceinline__ void st_global_v4_hint(void* ptr, uint4 v, uint64_t policy) {
   asm volatile("st.global.L2::cache_hint.v4.b32 [%0], {%1, %2, %3, %4}, %5;" ::"l"(ptr), "r"(v.x), "r"(v.y),
                "r"(v.z), "r"(v.w), "l"(policy)
@@ -267,19 +274,15 @@ struct Cfg {
   static constexpr int kWG = w_group(NS, RR, P);                 // streams per w box
   static constexpr int kWBoxes = NS / kWG;                       // w boxes per d-chunk
   static constexpr int kWBytes = kWG * kWRows * 128;             // one w box
-  static constexpr int kTY = y_box_tokens(NS);                   // tokens per y box
-  static constexpr int kYBytes = NS * kTY * 128;
   static constexpr int kStr = partial_stride(RR);                // floats per published partial
   static constexpr int kSink = sink_stride(NS);
   static constexpr bool kThree = (RR == NS * NS + 2 * NS);
-  static constexpr int kVecPerThread = kTY * (kChunkK / 8) / 128;
-  static_assert(kVecPerThread >= 1 && kTY * (kChunkK / 8) % 128 == 0, "y box must split over 128 threads");
+  static constexpr int kYBatch = NS <= 4 ? 4 : 2;               // y items in flight per thread
 };
 
 struct SmemTail {
   uint64_t x_full[kMaxStages], x_empty[kMaxStages];
   uint64_t w_full[kMaxStages], w_empty[kMaxStages];
-  uint64_t y_full[kMaxStages], y_empty[kMaxStages];
   uint64_t acc_full[2], acc_empty[2];
   uint64_t part_full, part_free;
   uint64_t coef_full[kCoefBufs], coef_free[kCoefBufs];
@@ -287,14 +290,15 @@ struct SmemTail {
   uint64_t mma_done;
   uint32_t tmem_base;
   uint32_t abort;
-  uint32_t x_tiles_issued;      // tiles whose x boxes the x producer has issued
 };
 static_assert(sizeof(SmemTail) <= kTailBytes, "barrier block outgrew its reservation");
 
-// Warp roles: one TMA producer per ring, so each ring has its own issuing thread.
-constexpr int kWarpX = 0, kWarpMma = 1, kWarpW = 2, kWarpY = 3, kWarpPub0 = 4, kWarpGate = 6,
-              kWarpSink = 7, kWarpYc0 = 8;
-// Named barriers: 1 = publish pair (64 threads), 2 = y warps (128).
+// Warp roles: one TMA producer per ring, so each ring has its own issuing
+// thread; warp 3 has no role.
+constexpr int kWarpX = 0, kWarpMma = 1, kWarpW = 2, kWarpPub0 = 4, kWarpGate = 6, kWarpSink = 7,
+              kWarpYc0 = 8;
+constexpr int kYThreads = kThreads - kWarpYc0 * 32;   // 256
+// Named barriers: 1 = publish pair (64 threads), 2 = y warps.
 constexpr int kBarPub = 1, kBarY = 2;
 
 // Offset of 16-byte column c of row r in a 128-byte-swizzled tile.
@@ -312,16 +316,14 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
 template <int NS, int RR, int P>
 __global__ void __launch_bounds__(kThreads, 1)
     mhc_pre_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constant__ CUtensorMap tmap_w,
-                      const __grid_constant__ CUtensorMap tmap_y, const EpiParams ep, Geometry g,
-                      uint32_t* err) {
+                      const EpiParams ep, const __nv_bfloat16* __restrict__ xg, Geometry g, uint32_t* err) {
   using C = Cfg<NS, RR, P>;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  const SmemLayout Ly = smem_layout(NS, RR, P, g.xstages, g.wstages, g.ystages);
-  const int XS = g.xstages, WS = g.wstages, YS = g.ystages;
+  const SmemLayout Ly = smem_layout(NS, RR, P, g.xstages, g.wstages);
+  const int XS = g.xstages, WS = g.wstages;
   uint8_t* sX = smem + Ly.x;
   uint8_t* sW = smem + Ly.w;
-  uint8_t* sY = smem + Ly.y;
   float* recv = reinterpret_cast<float*>(smem + Ly.part);     // [CL][64/CL][kStr]
   float* coef_buf = reinterpret_cast<float*>(smem + Ly.coef); // [kCoefBufs][64][NS]
   float* sink_buf = reinterpret_cast<float*>(smem + Ly.sink); // [2][64][n*n] residual logits
@@ -349,10 +351,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&tail->w_full[s], 1);
       mbar_init(&tail->w_empty[s], 1);          // MMA commit
     }
-    for (int s = 0; s < YS; ++s) {
-      mbar_init(&tail->y_full[s], 1);
-      mbar_init(&tail->y_empty[s], 4);          // four y warps
-    }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&tail->acc_full[b], 1);
       mbar_init(&tail->acc_empty[b], 2);        // two publish warps
@@ -367,11 +365,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(&tail->part_free, CL);
     mbar_init(&tail->mma_done, 1);
     tail->abort = 0u;
-    tail->x_tiles_issued = 0u;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     tma_prefetch_desc(&tmap_x);
     tma_prefetch_desc(&tmap_w);
-    tma_prefetch_desc(&tmap_y);
   }
   if (warp == kWarpMma) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
@@ -391,7 +387,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       const uint64_t keep = policy_evict_last();
       int xs = 0;
-      uint32_t xph = 0, done_tiles = 0;
+      uint32_t xph = 0;
       long long iss = 0;
       bool ok = true;
       for (int tile = cluster_id; tile < g.num_tiles && ok; tile += num_clusters) {
@@ -404,10 +400,6 @@ __global__ void __launch_bounds__(kThreads, 1)
             ++iss;
             if (++xs == XS) { xs = 0; xph ^= 1u; }
           }
-        }
-        if (ok) {
-          ++done_tiles;
-          *reinterpret_cast<volatile uint32_t*>(&tail->x_tiles_issued) = done_tiles;
         }
       }
       for (long long q = 0; q < (iss < XS ? iss : XS); ++q) {     // let issued copies land
@@ -438,47 +430,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (long long q = 0; q < (iss < WS ? iss : WS); ++q) {
         if (--ws < 0) { ws = WS - 1; wph ^= 1u; }
         wait_bar<false>(&tail->w_full[ws], wph, ctl, kErrWaitTimeout);
-      }
-    }
-  } else if (warp == kWarpY) {
-    // ================================================= y re-read producer (L2)
-    // Re-reads a tile's x once its x boxes were all issued, newest d-chunk first.
-    if (lane == 0) {
-      const uint64_t drop = policy_evict_first();
-      int ys = 0;
-      uint32_t yph = 0, k = 0;
-      long long iss = 0;
-      bool ok = true;
-      for (int tile = cluster_id; tile < g.num_tiles && ok; tile += num_clusters, ++k) {
-        // wait (bounded) until the x producer has issued this tile
-        const uint64_t t0 = now_ns();
-        while (*reinterpret_cast<volatile uint32_t*>(&tail->x_tiles_issued) <= k) {
-          if (*ctl.abort) { ok = false; break; }
-          if (now_ns() - t0 > kWaitNs) {
-            atomicOr(err, kErrWaitTimeout);
-            *ctl.abort = 1u;
-            ok = false;
-            break;
-          }
-          __nanosleep(64);
-        }
-        if (!ok) break;
-        const int rows = min(kTileT, g.T - tile * kTileT);
-        const int halves = (rows + C::kTY - 1) / C::kTY;
-        for (int jj = c1 - 1; jj >= c0 && ok; --jj) {
-          for (int h = 0; h < halves; ++h) {
-            if (!wait_bar<false>(&tail->y_empty[ys], yph ^ 1u, ctl, kErrWaitTimeout)) { ok = false; break; }
-            mbar_expect_tx(&tail->y_full[ys], (uint32_t)C::kYBytes);
-            tma_load_3d_hint(sY + (size_t)ys * C::kYBytes, &tmap_y, &tail->y_full[ys], jj * kChunkK,
-                             tile * kTileT + h * C::kTY, 0, drop);
-            ++iss;
-            if (++ys == YS) { ys = 0; yph ^= 1u; }
-          }
-        }
-      }
-      for (long long q = 0; q < (iss < YS ? iss : YS); ++q) {
-        if (--ys < 0) { ys = YS - 1; yph ^= 1u; }
-        wait_bar<false>(&tail->y_full[ys], yph, ctl, kErrWaitTimeout);
       }
     }
   } else if (warp == kWarpMma) {
@@ -537,7 +488,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mma_commit(&tail->mma_done);
       wait_bar<false>(&tail->mma_done, 0, ctl, kErrWaitTimeout);
     }
-  } else if (warp < kWarpGate) {
+  } else if (warp >= kWarpPub0 && warp < kWarpGate) {
     // ================================================= publish partial sums
     // Thread = tile row = TMEM lane.  Each row's partial projection (this
     // member's d-range) and partial sum of squares go to the member that
@@ -697,66 +648,69 @@ __global__ void __launch_bounds__(kThreads, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(&tail->sink_free[sb]);
     }
-  } else {
+  } else if (warp >= kWarpYc0) {
     // ================================================= y for this member's d-range
-    const int yt = threadIdx.x - kWarpYc0 * 32;    // 0..127
+    // y[t, d] = sum_i m_i x[t, i, d] over the rows of the tile and this
+    // member's d-range, re-reading x from L2 with plain 16-byte loads (newest
+    // d first); kYBatch items per thread are in flight at once.
+    const int yt = threadIdx.x - kWarpYc0 * 32;
+    const uint64_t read_policy = policy_evict_first();
     const uint64_t ystore_policy = policy_evict_first();
-    int ys = 0;
-    uint32_t yph = 0;
+    const int dlo = c0 * kChunkK;
+    const int dhi = min(c1 * kChunkK, g.D);
+    const int w8 = (dhi - dlo) >> 3;              // 16-byte vectors per row
     uint32_t k = 0;
     for (int tile = cluster_id; tile < g.num_tiles; tile += num_clusters, ++k) {
       const int cb = (int)(k % kCoefBufs);
-      if (!role_all<kBarY, 128>(wait_bar<true>(&tail->coef_full[cb], (k / kCoefBufs) & 1u, ctl,
-                                               kErrClusterWait)))
+      if (!role_all<kBarY, kYThreads>(wait_bar<true>(&tail->coef_full[cb], (k / kCoefBufs) & 1u, ctl,
+                                                     kErrClusterWait)))
         break;
       const float* coef = coef_buf + (size_t)cb * kTileT * NS;
       const int rows = min(kTileT, g.T - tile * kTileT);
-      const int halves = (rows + C::kTY - 1) / C::kTY;
-      bool ok = true;
-      for (int jj = c1 - 1; jj >= c0 && ok; --jj) {
-        for (int h = 0; h < halves; ++h) {
-          if (!role_all<kBarY, 128>(wait_bar<false>(&tail->y_full[ys], yph, ctl, kErrWaitTimeout))) {
-            ok = false;
-            break;
+      const int items = rows * w8;
+      const __nv_bfloat16* xt = xg + (size_t)tile * kTileT * g.n * g.D;
+      __nv_bfloat16* yt_out = ep.y + (size_t)tile * kTileT * g.D;
+      for (int base = yt; base < items; base += kYThreads * C::kYBatch) {
+        uint4 xv[C::kYBatch][NS];
+        int rowv[C::kYBatch], dv[C::kYBatch];
+#pragma unroll
+        for (int b = 0; b < C::kYBatch; ++b) {
+          const int it = base + b * kYThreads;
+          const int row = it / w8;
+          const int v = w8 - 1 - (it - row * w8);  // newest columns first
+          rowv[b] = it < items ? row : -1;
+          dv[b] = dlo + 8 * v;
+          if (it < items) {
+            const __nv_bfloat16* src = xt + ((size_t)row * NS) * g.D + dv[b];
+#pragma unroll
+            for (int i = 0; i < NS; ++i) xv[b][i] = ld_global_v4_hint(src + (size_t)i * g.D, read_policy);
           }
-          const uint8_t* box = sY + (size_t)ys * C::kYBytes;   // [stream][token][128 B], swizzled
+        }
 #pragma unroll
-          for (int u = 0; u < C::kVecPerThread; ++u) {
-            const int v = yt + 128 * u;
-            const int tl = v >> 3;                 // token within the box
-            const int c = v & 7;                   // 16-byte column group
-            const int row = h * C::kTY + tl;
-            const int d = jj * kChunkK + c * 8;
-            if (row < rows && d < g.D) {
-              float acc8[8];
+        for (int b = 0; b < C::kYBatch; ++b) {
+          if (rowv[b] < 0) continue;
+          float acc8[8];
 #pragma unroll
-              for (int e = 0; e < 8; ++e) acc8[e] = 0.0f;
+          for (int e = 0; e < 8; ++e) acc8[e] = 0.0f;
 #pragma unroll
-              for (int i = 0; i < NS; ++i) {
-                const float m = coef[row * NS + i];
-                const uint4 xv = *reinterpret_cast<const uint4*>(box + sw128(i * C::kTY + tl, c));
-                const __nv_bfloat162* hh = reinterpret_cast<const __nv_bfloat162*>(&xv);
+          for (int i = 0; i < NS; ++i) {
+            const float m = coef[rowv[b] * NS + i];
+            const __nv_bfloat162* hh = reinterpret_cast<const __nv_bfloat162*>(&xv[b][i]);
 #pragma unroll
-                for (int q2 = 0; q2 < 4; ++q2) {
-                  const float2 f = __bfloat1622float2(hh[q2]);
-                  acc8[2 * q2] = fmaf(m, f.x, acc8[2 * q2]);
-                  acc8[2 * q2 + 1] = fmaf(m, f.y, acc8[2 * q2 + 1]);
-                }
-              }
-              uint4 o;
-              __nv_bfloat162* ob = reinterpret_cast<__nv_bfloat162*>(&o);
-#pragma unroll
-              for (int q2 = 0; q2 < 4; ++q2) ob[q2] = __floats2bfloat162_rn(acc8[2 * q2], acc8[2 * q2 + 1]);
-              st_global_v4_hint(ep.y + ((size_t)(tile * kTileT + row) * g.D + d), o, ystore_policy);
+            for (int q2 = 0; q2 < 4; ++q2) {
+              const float2 f = __bfloat1622float2(hh[q2]);
+              acc8[2 * q2] = fmaf(m, f.x, acc8[2 * q2]);
+              acc8[2 * q2 + 1] = fmaf(m, f.y, acc8[2 * q2 + 1]);
             }
           }
-          __syncwarp();
-          if (lane == 0) mbar_arrive(&tail->y_empty[ys]);
-          if (++ys == YS) { ys = 0; yph ^= 1u; }
+          uint4 o;
+          __nv_bfloat162* ob = reinterpret_cast<__nv_bfloat162*>(&o);
+#pragma unroll
+          for (int q2 = 0; q2 < 4; ++q2) ob[q2] = __floats2bfloat162_rn(acc8[2 * q2], acc8[2 * q2 + 1]);
+          st_global_v4_hint(yt_out + (size_t)rowv[b] * g.D + dv[b], o, ystore_policy);
         }
       }
-      if (!ok) break;
-      role_sync<kBarY, 128>();                     // every y thread is done with coef[cb]
+      role_sync<kBarY, kYThreads>();               // every y thread is done with coef[cb]
       if (yt < CL) mbar_arrive_remote(&tail->coef_free[cb], (uint32_t)yt);
     }
   }
@@ -834,14 +788,14 @@ cudaError_t launch_tc_forward(const TcLaunch& L, cudaStream_t s) {
   g.num_tiles = (L.epi.T + kTileT - 1) / kTileT;
   g.nd = (L.epi.D + kChunkK - 1) / kChunkK;
   g.cluster = L.cluster;
+  g.n = n;
   g.xstages = L.xstages;
   g.wstages = L.wstages;
-  g.ystages = L.ystages;
   cudaLaunchAttribute attr[1];
   cudaLaunchConfig_t cfg = cluster_config(L.cluster, L.grid, L.smem_bytes, s, attr);
+  const __nv_bfloat16* xg = static_cast<const __nv_bfloat16*>(L.x);
   void* args[] = {const_cast<CUtensorMap*>(&L.tmap_x), const_cast<CUtensorMap*>(&L.tmap_w),
-                  const_cast<CUtensorMap*>(&L.tmap_y), const_cast<EpiParams*>(&L.epi), &g,
-                  const_cast<uint32_t**>(&L.err_word)};
+                  const_cast<EpiParams*>(&L.epi), &xg, &g, const_cast<uint32_t**>(&L.err_word)};
   return cudaLaunchKernelExC(&cfg, k, args);
 }
 
