@@ -153,10 +153,12 @@ def hbm_peak():
         return 6800.0, "fallback"
 
 
-def csrc_hash():
+def kernel_hash():
+    """Hash of the fused kernel's device sources (the traffic record is void
+    once they change)."""
     h = hashlib.sha256()
     d = os.path.join(ROOT, "mhc_hyper_connection_gb300", "csrc")
-    for name in sorted(os.listdir(d)):
+    for name in ("mhc_common.cuh", "mhc_pre_tc.cu"):
         with open(os.path.join(d, name), "rb") as f:
             h.update(name.encode())
             h.update(f.read())
@@ -172,7 +174,7 @@ def recorded_traffic(T):
             rec = json.load(f)
     except (OSError, ValueError):
         return None
-    if rec.get("csrc_hash") != csrc_hash():
+    if rec.get("kernel_hash") != kernel_hash():
         return None
     return rec["dram_bytes_per_token"] * T + rec.get("dram_bytes_fixed", 0)
 

@@ -286,9 +286,9 @@ mhc_status_t mhc_pre_run(mhc_pre_t h, const mhc_pre_args* a, void* stream) {
   if (!xst) return fail(MHC_ERR_RUNTIME, "shape does not fit in shared memory");
   const size_t smem = mhc::smem_layout(n, R, h->P, xst, wst).total;
 
-  // Cluster size: the one that keeps the most SMs busy on this many tiles
-  // (ties go to the smaller cluster, which exchanges less).  Larger clusters
-  // split a tile's d-range over more SMs, which is what small T needs.
+  // Cluster size: the one that keeps the most SMs busy on this many tiles.
+  // Ties go to the larger cluster: each member then reduces and gates fewer
+  // rows of a tile, which shortens the per-tile critical path.
   const int want = env_int("MHC_PRE_CLUSTER", 16);
   int cluster = 0;
   int max_clusters = 0;
@@ -301,7 +301,7 @@ mhc_status_t mhc_pre_run(mhc_pre_t h, const mhc_pre_args* a, void* stream) {
       continue;
     }
     const long long sms = (long long)(num_tiles < mc ? num_tiles : mc) * cand;
-    if (sms > best_sms) {
+    if (sms >= best_sms) {
       best_sms = sms;
       cluster = cand;
       max_clusters = mc;
