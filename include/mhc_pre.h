@@ -143,6 +143,31 @@ MHC_API mhc_status_t mhc_pre_set_profile_events(mhc_pre_t h, void *before, void 
 MHC_API mhc_status_t mhc_pre_last_launch(mhc_pre_t h, int32_t *cluster, int32_t *grid,
                                          int32_t *stages, int32_t *ystages);
 
+/* Same forward as mhc_pre_run, for callers that cannot allocate device memory
+ * at all -- for instance code running under an allocator lock, a host
+ * runtime with no device allocator of its own, or a stream that is not
+ * allowed to block on cudaMalloc/cudaFree.  It takes no workspace:
+ * args->workspace must be NULL and args->workspace_bytes 0.  Instead the
+ * library keeps one fixed scratch array of MHC_PRE_STATIC_SCRATCH_BYTES in
+ * device memory (a file-scope __device__ variable, so every GPU that loads the
+ * library holds it until the process exits).  This entry point itself
+ * allocates nothing: it calls no cudaMalloc, cudaFree or allocating library
+ * routine.
+ *  - The first call on each device looks up the array's device address with
+ *    that device current; make that first call before any stream capture.
+ *  - A call whose mhc_pre_workspace_size exceeds the array is rejected with
+ *    MHC_ERR_PARAM_INVALID (mhc_pre_last_error says by how much).
+ *  - Every call shares the one array, and each run rewrites all of it that it
+ *    uses (the error word is cleared at the start of every run), so calls
+ *    whose work overlaps on the GPU (different streams, no ordering between
+ *    them) race on it: serialise them.
+ *  - The device error word lives in that array; check a run with
+ *    mhc_pre_status(h, NULL, stream), which reports CUDA errors only.
+ * This entry point is a property of this library; the pages' operator has no
+ * counterpart.  Other arguments and status codes as mhc_pre_run. */
+#define MHC_PRE_STATIC_SCRATCH_BYTES ((size_t)16 << 20)
+MHC_API mhc_status_t mhc_pre_run_noalloc(mhc_pre_t h, const mhc_pre_args *args, void *stream);
+
 /* Release the handle (NULL is ignored). */
 MHC_API void mhc_pre_destroy(mhc_pre_t h);
 

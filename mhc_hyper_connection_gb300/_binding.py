@@ -68,6 +68,8 @@ def library() -> ctypes.CDLL:
             lib.mhc_pre_workspace_size.restype = ctypes.c_int32
             lib.mhc_pre_run.argtypes = [_P, ctypes.POINTER(MhcPreArgs), _P]
             lib.mhc_pre_run.restype = ctypes.c_int32
+            lib.mhc_pre_run_noalloc.argtypes = [_P, ctypes.POINTER(MhcPreArgs), _P]
+            lib.mhc_pre_run_noalloc.restype = ctypes.c_int32
             lib.mhc_pre_status.argtypes = [_P, _P, _P]
             lib.mhc_pre_status.restype = ctypes.c_int32
             lib.mhc_pre_set_profile_events.argtypes = [_P, _P, _P]
@@ -108,6 +110,11 @@ def mhc_pre_workspace_size(handle, T: int):
 
 def mhc_pre_run(handle, args: MhcPreArgs, stream: int = 0) -> int:
     return library().mhc_pre_run(handle, ctypes.byref(args), _P(stream or None))
+
+
+def mhc_pre_run_noalloc(handle, args: MhcPreArgs, stream: int = 0) -> int:
+    """The forward on the library's fixed scratch array (no workspace)."""
+    return library().mhc_pre_run_noalloc(handle, ctypes.byref(args), _P(stream or None))
 
 
 def mhc_pre_status(handle, workspace: int = 0, stream: int = 0) -> int:

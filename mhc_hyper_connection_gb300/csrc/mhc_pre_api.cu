@@ -342,6 +342,62 @@ mhc_status_t mhc_pre_status(mhc_pre_t h, const void* workspace, void* stream) {
   return MHC_OK;
 }
 
+}  // extern "C"
+
+// Fixed scratch for mhc_pre_run_noalloc: one array per device, reused by every
+// call (the error word at its start is cleared by each run; the phi planes
+// after it are rewritten by each run).
+static __device__ __align__(256) unsigned char g_noalloc_scratch[MHC_PRE_STATIC_SCRATCH_BYTES];
+
+namespace {
+// Device address of g_noalloc_scratch, looked up once per device with that
+// device current (host code cannot use the symbol itself as a pointer).
+void* noalloc_scratch(int dev, cudaError_t* err) {
+  static std::mutex mu;
+  static void* addr[64] = {};
+  std::lock_guard<std::mutex> lk(mu);
+  *err = cudaSuccess;
+  if (dev < 0 || dev >= 64) {
+    *err = cudaErrorInvalidDevice;
+    return nullptr;
+  }
+  if (!addr[dev]) {
+    void* p = nullptr;
+    *err = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+    if (*err != cudaSuccess) return nullptr;
+    addr[dev] = p;
+  }
+  return addr[dev];
+}
+}  // namespace
+
+extern "C" {
+
+mhc_status_t mhc_pre_run_noalloc(mhc_pre_t h, const mhc_pre_args* a, void* stream) {
+  g_last_error[0] = 0;
+  if (!h || !a) return fail(MHC_ERR_NULLPTR, "handle and args must be non-NULL");
+  if (a->workspace || a->workspace_bytes)
+    return fail(MHC_ERR_PARAM_INVALID, "mhc_pre_run_noalloc takes no workspace (pass NULL, 0)");
+  if (a->T == 0) return MHC_OK;
+  size_t need = 0;
+  const mhc_status_t st = mhc_pre_workspace_size(h, a->T, &need);
+  if (st != MHC_OK) return st;
+  if (need > MHC_PRE_STATIC_SCRATCH_BYTES)
+    return fail(MHC_ERR_PARAM_INVALID,
+                "this shape needs %zu bytes of scratch, over the fixed %zu-byte array of "
+                "mhc_pre_run_noalloc; use mhc_pre_run with a workspace",
+                need, (size_t)MHC_PRE_STATIC_SCRATCH_BYTES);
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return fail(MHC_ERR_RUNTIME, "no CUDA device");
+  cudaError_t e;
+  void* scratch = noalloc_scratch(dev, &e);
+  if (!scratch) return fail(MHC_ERR_RUNTIME, "looking up the scratch array failed: %s", cudaGetErrorString(e));
+  mhc_pre_args b = *a;
+  b.workspace = scratch;
+  b.workspace_bytes = MHC_PRE_STATIC_SCRATCH_BYTES;
+  return mhc_pre_run(h, &b, stream);
+}
+
 mhc_status_t mhc_pre_set_profile_events(mhc_pre_t h, void* before, void* after) {
   g_last_error[0] = 0;
   if (!h) return fail(MHC_ERR_NULLPTR, "handle must be non-NULL");
