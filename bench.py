@@ -153,28 +153,31 @@ def hbm_peak():
         return 6800.0, "fallback"
 
 
-def kernel_hash():
-    """Hash of the fused kernel's device sources (the traffic record is void
+KERNEL_SOURCES = {"mhc_pre_tc_kernel": "mhc_pre_tc.cu", "mhc_pre_gw_kernel": "mhc_pre_gw.cu"}
+
+
+def kernel_hash(kernel):
+    """Hash of a fused kernel's device sources (its traffic record is void
     once they change)."""
     h = hashlib.sha256()
     d = os.path.join(ROOT, "mhc_hyper_connection_gb300", "csrc")
-    for name in ("mhc_common.cuh", "mhc_pre_tc.cu"):
+    for name in ("mhc_common.cuh", "mhc_ptx.cuh", KERNEL_SOURCES[kernel]):
         with open(os.path.join(d, name), "rb") as f:
             h.update(name.encode())
             h.update(f.read())
     return h.hexdigest()[:16]
 
 
-def recorded_traffic(T):
+def recorded_traffic(kernel, T):
     """DRAM bytes per launch of the fused kernel from the committed ncu summary,
     scaled to T tokens; None once the kernel source changed since capture."""
-    p = os.path.join(ROOT, "profiles", "mhc_pre_tc_traffic.json")
+    p = os.path.join(ROOT, "profiles", f"{kernel}_traffic.json")
     try:
         with open(p) as f:
             rec = json.load(f)
     except (OSError, ValueError):
         return None
-    if rec.get("kernel_hash") != kernel_hash():
+    if rec.get("kernel_hash") != kernel_hash(kernel):
         return None
     return rec["dram_bytes_per_token"] * T + rec.get("dram_bytes_fixed", 0)
 
@@ -349,9 +352,10 @@ def main():
     peak, peak_src = hbm_peak()
     lb = launch_bytes(T, n, D)
     achieved = lb / kern / 1e9
+    kernel = "mhc_pre_gw_kernel" if cfg["launch"]["cluster"] == 0 else "mhc_pre_tc_kernel"
     roof = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
-            "frac": achieved / peak, "traffic": recorded_traffic(T),
-            "kernel": "mhc_pre_tc_kernel", "kernel_ms": kern * 1e3,
+            "frac": achieved / peak, "traffic": recorded_traffic(kernel, T),
+            "kernel": kernel, "kernel_ms": kern * 1e3,
             "algorithmic_bytes": lb, "peak_source": f"hbm_gbs of {peak_src}"}
 
     cpu = None

@@ -19,10 +19,17 @@ namespace mhc {
 enum : uint32_t {
   kErrWaitTimeout = 1u << 0,   // an mbarrier wait gave up
   kErrClusterWait = 1u << 1,   // a cluster exchange wait gave up
+  kErrGridWait = 1u << 2,      // a wait on another CTA's global counter gave up
 };
 
-// Workspace layout: [0, 256) header (error word at 0), then the phi planes.
+// Workspace layout: [0, 256) header, then the phi planes, then the exchange
+// rings of the grid-wide forward.  Header words (uint32): 0 error word,
+// 1 grid-wide abort flag, [16, 32) partial-arrival counters, [32, 48)
+// gated-token counters, [48, 64) y-done counters, one per ring slot.  The
+// plane preparation kernel zeroes the whole header before every forward.
 constexpr size_t kWsHeader = 256;
+constexpr int kHdrWords = 64;
+constexpr int kHdrAbort = 1, kHdrArrive = 16, kHdrReady = 32, kHdrYdone = 48;
 
 struct EpiParams {
   int T;
@@ -210,7 +217,7 @@ struct PlaneParams {
   __nv_bfloat16* planes;   // [NP, K]
   int R, K, NP, P;         // P = 3 (fp32) or 2 (tf32)
   int tf32;
-  uint32_t* err_word;
+  uint32_t* err_word;      // workspace header: all kHdrWords words are zeroed
 };
 
 cudaError_t launch_prepare_planes(const PlaneParams& pp, cudaStream_t s);
@@ -292,5 +299,70 @@ cudaError_t launch_tc_forward(const TcLaunch& L, cudaStream_t s);
 cudaError_t tc_forward_occupancy(int n, int R, int P, size_t smem_bytes, int cluster,
                                  int* max_clusters);
 int tc_np(int R, int P);
+
+// ---------------------------------------------------------------------------
+// Grid-wide forward: every CTA (one per SM) owns a fixed set of (64-wide
+// d-chunk, stream) units and works on every 128-token tile; per-CTA partial
+// sums meet in a global ring, one CTA per token gates it, and y is formed by
+// each CTA for its own d-range.
+// ---------------------------------------------------------------------------
+constexpr int kGwTile = 128;                  // tokens per tile (MMA M, TMEM lanes)
+constexpr int kGwUnitBytes = kGwTile * 128;   // one (d-chunk, stream) x box: 16 KB
+constexpr int kGwSlots = 4;                   // exchange-ring depth in tiles (<= 16)
+
+__host__ __device__ constexpr int gw_np(int R, int P) { return ((P * R + 15) / 16) * 16; }
+
+struct GwLayout {
+  size_t phi, x, ycoef, sink, scnt, tail, total;
+};
+// Shared memory of the grid-wide kernel: the CTA's resident phi-plane blocks,
+// the x ring (xs slots of umax units), the y weights of one tile, the
+// Sinkhorn hand-off (two buffers of own_max tokens) and the barrier block.
+__host__ __device__ inline GwLayout gw_layout(int n, int R, int P, int umax, int xs, int own_max) {
+  GwLayout L;
+  size_t o = 0;
+  L.phi = o;   o += (size_t)umax * gw_np(R, P) * 128;
+  L.x = o;     o += (size_t)xs * umax * kGwUnitBytes;
+  L.ycoef = o; o += (size_t)kGwTile * n * 4;
+  L.sink = o;  o += 2 * (size_t)own_max * n * n * 4;
+  L.scnt = o;  o += 16;
+  o = (o + 15) & ~size_t(15);
+  L.tail = o;  o += kTailBytes;
+  L.total = o + 1024;
+  return L;
+}
+// Bytes of the exchange rings after the planes: partials [slots][128][grid][stride]
+// and y weights [slots][128][n].
+inline size_t gw_ring_bytes(int n, int R, int grid) {
+  return (size_t)kGwSlots * kGwTile * grid * partial_stride(R) * 4 + (size_t)kGwSlots * kGwTile * n * 4;
+}
+
+struct GwGeom {
+  int T, D, n;
+  int num_tiles;   // 128-token tiles
+  int nch;         // 64-wide d-chunks per stream
+  int umax;        // most units any CTA owns
+  int xstages;     // x ring depth
+  int own_max;     // most tokens of one tile any CTA gates
+};
+
+struct GwLaunch {
+  EpiParams epi;
+  const void* x;           // bf16 [T, n, D] (re-read for y)
+  CUtensorMap tmap_x;      // x as (D, T, n): box (64, 128 tokens, 1 stream), 128B swizzle
+  CUtensorMap tmap_p;      // planes as (D, NP, n): box (64, NP, 1), 128B swizzle
+  int P;
+  int grid;                // CTAs, all resident at once (cooperative launch)
+  GwGeom g;
+  size_t smem_bytes;
+  uint32_t* hdr;           // workspace header
+  float* partials;         // exchange ring of partial sums
+  float* coefs;            // exchange ring of y weights
+};
+
+// Largest number of CTAs of the grid-wide kernel resident at once for this
+// shared-memory size (0: it does not fit).
+cudaError_t gw_forward_capacity(int n, int R, int P, size_t smem_bytes, int* max_ctas);
+cudaError_t launch_gw_forward(const GwLaunch& L, cudaStream_t s);
 
 }  // namespace mhc

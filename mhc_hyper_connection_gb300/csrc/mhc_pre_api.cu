@@ -103,10 +103,118 @@ size_t planes_bytes(const mhc_pre_s* h) {
   return ((size_t)h->NP * K * 2 + 255) & ~size_t(255);
 }
 
+// Exchange rings of the grid-wide forward, sized for its largest grid so the
+// workspace does not depend on the device.
+constexpr int kGwMaxGrid = 160;
+size_t gw_rings_bytes(const mhc_pre_s* h) {
+  return mhc::gw_ring_bytes((int)h->cfg.n, h->R, kGwMaxGrid);
+}
+
 int env_int(const char* name, int dflt) {
   const char* v = getenv(name);
   if (!v || !*v) return dflt;
   return atoi(v);
+}
+
+// Returned by run_grid_wide when the shape or device does not suit it.
+constexpr mhc_status_t MHC_ERR_NOT_SUITABLE = -1;
+
+mhc::EpiParams epi_params(const mhc_pre_s* h, const mhc_pre_args* a) {
+  const mhc_pre_config& c = h->cfg;
+  mhc::EpiParams e;
+  memset(&e, 0, sizeof e);
+  e.T = (int)a->T;
+  e.n = (int)c.n;
+  e.D = (int)c.D;
+  e.R = h->R;
+  e.alpha_len = c.alpha_len;
+  e.num_iters = c.num_iters;
+  e.norm_eps = (float)c.norm_eps;
+  e.hc_eps = (float)c.hc_eps;
+  e.alpha = a->alpha;
+  e.bias = a->bias;
+  e.pre_mix = a->pre_mix;
+  e.y = static_cast<__nv_bfloat16*>(a->y);
+  e.h_post = a->h_post;
+  e.h_res = a->h_res;
+  e.h_pre = a->h_pre;
+  e.inv_rms = a->inv_rms;
+  e.h_mix = a->h_mix;
+  e.sum_out = a->sum_out;
+  e.norm_out = a->norm_out;
+  return e;
+}
+
+// The grid-wide forward: one CTA per SM, each owning a run of (d-chunk,
+// stream) units; MHC_ERR_NOT_SUITABLE when its resident phi blocks and a
+// two-slot x ring do not fit, or the grid cannot be resident at once.
+mhc_status_t run_grid_wide(mhc_pre_s* h, const mhc_pre_args* a, const DeviceInfo& di,
+                           __nv_bfloat16* planes, cudaStream_t s) {
+  const int n = (int)h->cfg.n, D = (int)h->cfg.D, R = h->R, NP = h->NP;
+  const int nch = (D + mhc::kChunkK - 1) / mhc::kChunkK;
+  const int units = nch * n;
+  int G = di.sms < kGwMaxGrid ? di.sms : kGwMaxGrid;
+  if (G > units) G = units;
+  if (G < 1) return MHC_ERR_NOT_SUITABLE;
+  const int umax = (units + G - 1) / G;
+  const int own_max = (mhc::kGwTile + G - 1) / G;
+  if (umax > 32) return MHC_ERR_NOT_SUITABLE;
+  int xmax = env_int("MHC_PRE_GW_XSTAGES", mhc::kMaxStages);
+  xmax = xmax < 2 ? 2 : (xmax > mhc::kMaxStages ? mhc::kMaxStages : xmax);
+  int xs = 0;
+  for (int c = xmax; c >= 2 && !xs; --c)
+    if (mhc::gw_layout(n, R, h->P, umax, c, own_max).total <= di.max_smem) xs = c;
+  if (!xs) return MHC_ERR_NOT_SUITABLE;
+  const size_t smem = mhc::gw_layout(n, R, h->P, umax, xs, own_max).total;
+  int cap = 0;
+  if (mhc::gw_forward_capacity(n, R, h->P, smem, &cap) != cudaSuccess) {
+    cudaGetLastError();
+    return MHC_ERR_NOT_SUITABLE;
+  }
+  if (cap < G) return MHC_ERR_NOT_SUITABLE;
+
+  mhc::GwLaunch L;
+  memset(&L, 0, sizeof L);
+  L.epi = epi_params(h, a);
+  L.x = a->x;
+  L.P = h->P;
+  L.grid = G;
+  L.g.T = (int)a->T;
+  L.g.D = D;
+  L.g.n = n;
+  L.g.num_tiles = (int)((a->T + mhc::kGwTile - 1) / mhc::kGwTile);
+  L.g.nch = nch;
+  L.g.umax = umax;
+  L.g.xstages = xs;
+  L.g.own_max = own_max;
+  L.smem_bytes = smem;
+  uint8_t* ws = static_cast<uint8_t*>(a->workspace);
+  L.hdr = reinterpret_cast<uint32_t*>(ws);
+  L.partials = reinterpret_cast<float*>(ws + mhc::kWsHeader + planes_bytes(h));
+  L.coefs = L.partials + (size_t)mhc::kGwSlots * mhc::kGwTile * G * mhc::partial_stride(R);
+  {
+    // x [T][n][D] seen as (D, T, n), box (64, 128 tokens, 1 stream); the phi
+    // planes [NP][n][D] as (D, NP, n), box (64, NP, 1).
+    const uint64_t K2 = (uint64_t)n * D * 2;
+    const uint64_t xd[3] = {(uint64_t)D, (uint64_t)a->T, (uint64_t)n};
+    const uint64_t st[2] = {K2, (uint64_t)D * 2};
+    const uint32_t xb[3] = {(uint32_t)mhc::kChunkK, (uint32_t)mhc::kGwTile, 1u};
+    const uint64_t pd[3] = {(uint64_t)D, (uint64_t)NP, (uint64_t)n};
+    const uint32_t pb[3] = {(uint32_t)mhc::kChunkK, (uint32_t)NP, 1u};
+    if (!encode_3d(&L.tmap_x, a->x, xd, st, xb) || !encode_3d(&L.tmap_p, planes, pd, st, pb))
+      return fail(MHC_ERR_RUNTIME, "tensor map encoding failed");
+  }
+  h->last_cluster = 0;
+  h->last_grid = G;
+  h->last_stages = xs;
+  h->last_ystages = umax;
+  if (h->ev_before && cudaEventRecord(h->ev_before, s) != cudaSuccess)
+    return fail(MHC_ERR_RUNTIME, "recording the timing event failed");
+  if (mhc::launch_gw_forward(L, s) != cudaSuccess)
+    return fail(MHC_ERR_RUNTIME, "forward launch failed: %s", cudaGetErrorString(cudaGetLastError()));
+  if (h->ev_after && cudaEventRecord(h->ev_after, s) != cudaSuccess)
+    return fail(MHC_ERR_RUNTIME, "recording the timing event failed");
+  return MHC_OK;
 }
 
 }  // namespace
@@ -165,7 +273,7 @@ mhc_status_t mhc_pre_workspace_size(mhc_pre_t h, int64_t T, size_t* bytes) {
   g_last_error[0] = 0;
   if (!h || !bytes) return fail(MHC_ERR_NULLPTR, "handle and bytes must be non-NULL");
   if (T < 0) return fail(MHC_ERR_PARAM_INVALID, "T must be >= 0");
-  *bytes = (T == 0) ? 0 : mhc::kWsHeader + planes_bytes(h);
+  *bytes = (T == 0) ? 0 : mhc::kWsHeader + planes_bytes(h) + gw_rings_bytes(h);
   return MHC_OK;
 }
 
@@ -228,29 +336,17 @@ mhc_status_t mhc_pre_run(mhc_pre_t h, const mhc_pre_args* a, void* stream) {
   if (mhc::launch_prepare_planes(pp, s) != cudaSuccess)
     return fail(MHC_ERR_RUNTIME, "plane preparation launch failed: %s", cudaGetErrorString(cudaGetLastError()));
 
-  // 2. the fused forward.
+  // 2. the fused forward: the cluster kernel, or the grid-wide kernel when
+  //    MHC_PRE_PATH=grid selects it (and its shared memory and residency allow).
+  const char* path = getenv("MHC_PRE_PATH");
+  if (path && !strcmp(path, "grid")) {
+    mhc_status_t st = run_grid_wide(h, a, di, planes, s);
+    if (st != MHC_ERR_NOT_SUITABLE) return st;
+    return fail(MHC_ERR_PARAM_INVALID, "the grid-wide forward does not fit this shape");
+  }
   mhc::TcLaunch L;
   memset(&L, 0, sizeof L);
-  mhc::EpiParams& e = L.epi;
-  e.T = (int)T;
-  e.n = n;
-  e.D = D;
-  e.R = R;
-  e.alpha_len = c.alpha_len;
-  e.num_iters = c.num_iters;
-  e.norm_eps = (float)c.norm_eps;
-  e.hc_eps = (float)c.hc_eps;
-  e.alpha = a->alpha;
-  e.bias = a->bias;
-  e.pre_mix = a->pre_mix;
-  e.y = static_cast<__nv_bfloat16*>(a->y);
-  e.h_post = a->h_post;
-  e.h_res = a->h_res;
-  e.h_pre = a->h_pre;
-  e.inv_rms = a->inv_rms;
-  e.h_mix = a->h_mix;
-  e.sum_out = a->sum_out;
-  e.norm_out = a->norm_out;
+  L.epi = epi_params(h, a);
   L.NP = NP;
   L.P = h->P;
   L.err_word = err;
@@ -289,12 +385,13 @@ mhc_status_t mhc_pre_run(mhc_pre_t h, const mhc_pre_args* a, void* stream) {
   // Cluster size: the one that keeps the most SMs busy on this many tiles.
   // Ties go to the larger cluster: each member then reduces and gates fewer
   // rows of a tile, which shortens the per-tile critical path.
-  const int want = env_int("MHC_PRE_CLUSTER", 16);
+  // MHC_PRE_CLUSTER=c forces cluster size c (for tuning runs).
+  const int forced = env_int("MHC_PRE_CLUSTER", 0);
   int cluster = 0;
   int max_clusters = 0;
   long long best_sms = -1;
   for (int cand : {1, 2, 4, 8, 16}) {
-    if (cand > want || cand > nd) continue;
+    if ((forced && cand != forced) || cand > nd) continue;
     int mc = 0;
     if (mhc::tc_forward_occupancy(n, R, h->P, smem, cand, &mc) != cudaSuccess || mc <= 0) {
       cudaGetLastError();

@@ -16,7 +16,7 @@ namespace mhc {
 __device__ __forceinline__ float bf16_round(float v) { return __bfloat162float(__float2bfloat16_rn(v)); }
 
 __global__ void __launch_bounds__(256) prepare_planes_kernel(PlaneParams pp) {
-  if (blockIdx.x == 0 && threadIdx.x == 0 && pp.err_word) *pp.err_word = 0u;
+  if (blockIdx.x == 0 && threadIdx.x < kHdrWords && pp.err_word) pp.err_word[threadIdx.x] = 0u;
   const long long total = (long long)pp.NP * pp.K;
   for (long long idx = (long long)blockIdx.x * blockDim.x + threadIdx.x; idx < total;
        idx += (long long)gridDim.x * blockDim.x) {

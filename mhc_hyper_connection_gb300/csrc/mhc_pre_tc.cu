@@ -5,256 +5,30 @@
 // 全解析" §三 and "aclnnMhcPreSinkhorn 接口与 MhcPreSinkhorn 实现剖析" §3.2;
 // how it is laid out on the GPU is this file's own design:
 //
-//  * A token tile is 128 tokens (the MMA's M, one TMEM lane per token).  A
-//    cluster of C CTAs shares one tile; CTA c owns a contiguous range of
-//    64-wide d-chunks and streams those chunks of all n streams, so each
-//    byte of x is read from HBM once per tile and the tile's footprint per
-//    SM stays small enough for the later re-read to hit L2.
-//  * Per chunk, TMA brings x[128 tokens][64] (bf16, 128-byte swizzle) and the
-//    matching 64 columns of the stacked phi planes [NP][64]; one thread issues
-//    four tcgen05.mma (K = 16 each), M = 128, N = NP, fp32 accumulate in TMEM.
-//  * Two warps sum x^2 for their token rows from the same shared-memory tile.
-//  * Four epilogue warps read the accumulators (thread = token), fold the
-//    precision planes, exchange per-CTA partial sums through distributed
-//    shared memory, run gates + Sinkhorn for the rows this CTA owns, publish
-//    the y weights to every CTA of the cluster, then form y for the CTA's
-//    d-range by re-reading x (now in L2).
+//  * A token tile is 64 tokens: rows 0..63 of an M = 128 MMA (rows 64..127
+//    are never read).  A cluster of C CTAs shares one tile; CTA c owns a
+//    contiguous range of 64-wide d-chunks and streams those chunks of all n
+//    streams, so each byte of x is read from HBM once per tile.
+//  * Per chunk, TMA brings x[64 tokens][64] of a group of streams (bf16,
+//    128-byte swizzle) and the matching 64 columns of the stacked phi planes;
+//    one thread issues tcgen05.mma (K = 16 each), N = NP into one TMEM block
+//    and x.x^T (N = 64) into another, whose diagonal is each token's sum of
+//    squares.
+//  * Two publish warps read the accumulators (thread = token), fold the
+//    precision planes and push the CTA's partial sums to the member that
+//    owns the row (distributed shared memory).  The owner's gate warp sums
+//    them in rank order, computes invRms and the gates, and sends the y
+//    weights to every member; a Sinkhorn warp produces comb off y's path.
+//  * Eight warps form y for the CTA's d-range by re-reading x from global
+//    memory, newest chunk first.
+//  * This kernel serves shapes whose phi blocks are too large to stay
+//    resident in the grid-wide kernel (mhc_pre_gw.cu).
 //  * Every wait is bounded by a timer; a wait that gives up sets the error
 //    word in the workspace and the kernel winds down instead of hanging.
-#include "mhc_common.cuh"
+#include "mhc_ptx.cuh"
 
 namespace mhc {
 namespace {
-
-constexpr uint64_t kWaitNs = 2000000000ull;   // 2 s per wait before giving up
-
-// ----------------------------------------------------------------- PTX glue
-__device__ __forceinline__ uint32_t smem_u32(const void* p) {
-  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
-}
-__device__ __forceinline__ uint64_t now_ns() {
-  uint64_t t;
-  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
-  return t;
-}
-__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
-  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
-}
-__device__ __forceinline__ void mbar_expect_tx(uint64_t* bar, uint32_t bytes) {
-  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
-               : "memory");
-}
-__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
-  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
-}
-// Arrive on the barrier at the same offset in CTA `rank` of this cluster.
-__device__ __forceinline__ void mbar_arrive_remote(uint64_t* bar, uint32_t rank) {
-  asm volatile(
-      "{\n\t.reg .b32 ra;\n\t"
-      "mapa.shared::cluster.u32 ra, %0, %1;\n\t"
-      "mbarrier.arrive.release.cluster.shared::cluster.b64 _, [ra];\n\t}" ::"r"(smem_u32(bar)),
-      "r"(rank)
-      : "memory");
-}
-__device__ __forceinline__ bool mbar_test(uint64_t* bar, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-      "selp.u32 %0, 1, 0, p;\n\t}"
-      : "=r"(ok)
-      : "r"(smem_u32(bar)), "r"(parity)
-      : "memory");
-  return ok != 0;
-}
-// Non-blocking probe (test_wait never suspends the thread), for polling loops.
-__device__ __forceinline__ bool mbar_poll(uint64_t* bar, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-      "selp.u32 %0, 1, 0, p;\n\t}"
-      : "=r"(ok)
-      : "r"(smem_u32(bar)), "r"(parity)
-      : "memory");
-  return ok != 0;
-}
-__device__ __forceinline__ bool mbar_test_cluster(uint64_t* bar, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
-      "selp.u32 %0, 1, 0, p;\n\t}"
-      : "=r"(ok)
-      : "r"(smem_u32(bar)), "r"(parity)
-      : "memory");
-  return ok != 0;
-}
-
-struct Ctl {
-  volatile uint32_t* abort;   // shared: set once any wait in this CTA gave up
-  uint32_t* err;              // global error word
-};
-
-// Wait for phase `parity` of `bar`.  Returns false (and raises the abort flag
-// and error word) after kWaitNs, or as soon as another role has aborted.
-template <bool kCluster>
-__device__ __noinline__ bool wait_bar(uint64_t* bar, uint32_t parity, const Ctl& c, uint32_t code) {
-  if (kCluster ? mbar_test_cluster(bar, parity) : mbar_test(bar, parity)) return true;
-  const uint64_t t0 = now_ns();
-  for (uint32_t it = 1;; ++it) {
-    if (kCluster ? mbar_test_cluster(bar, parity) : mbar_test(bar, parity)) return true;
-    if ((it & 63u) == 0) {
-      if (*c.abort) return false;
-      if (now_ns() - t0 > kWaitNs) {
-        atomicOr(c.err, code);
-        *c.abort = 1u;
-        return false;
-      }
-    }
-  }
-}
-
-__device__ __forceinline__ void tma_load_3d_hint(void* dst, const CUtensorMap* map, uint64_t* bar, int c0,
-                                                 int c1, int c2, uint64_t policy) {
-  asm volatile(
-      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint"
-      " [%0], [%1, {%3, %4, %5}], [%2], %6;" ::"r"(smem_u32(dst)),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(c0), "r"(c1), "r"(c2), "l"(policy)
-      : "memory");
-}
-// L2 policies: keep x resident between its first read and its re-read for y,
-// drop it (and the y stream) as soon as the re-read is done.
-__device__ __forceinline__ uint64_t policy_evict_last() {
-  uint64_t p;
-  asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
-  return p;
-}
-__device__ __forceinline__ uint64_t policy_evict_first() {
-  uint64_t p;
-  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
-  return p;
-}
-__device__ __forceinline__ uint4 ld_global_v4_hint(const void* ptr, uint64_t policy) {
-  uint4 v;
-  asm volatile("ld.global.nc.L1::no_allocate.L2::cache_hint.v4.u32 {%0, %1, %2, %3}, [%4], %5;"
-               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-               : "l"(ptr), "l"(policy));
-  return v;
-}
-__device__ __forceinline__ void st_global_v4_hint(void* ptr, uint4 v, uint64_t policy) {
-  asm volatile("st.global.L2::cache_hint.v4.b32 [%0], {%1, %2, %3, %4}, %5;" ::"l"(ptr), "r"(v.x), "r"(v.y),
-               "r"(v.z), "r"(v.w), "l"(policy)
-               : "memory");
-}
-__device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap* map) {
-  asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
-}
-
-__device__ __forceinline__ void tc_fence_before() {
-  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
-}
-__device__ __forceinline__ void tc_fence_after() {
-  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-}
-
-// K-major operand tile with 128-byte swizzle: rows of 128 bytes, 8-row
-// groups 1024 bytes apart (the layout TMA writes for a 64 x rows bf16 box).
-__device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
-  uint64_t d = 0;
-  d |= static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);   // start address
-  d |= static_cast<uint64_t>(1) << 16;                    // leading offset (unused here)
-  d |= static_cast<uint64_t>(1024 >> 4) << 32;            // stride between 8-row groups
-  d |= static_cast<uint64_t>(1) << 46;                    // descriptor version
-  d |= static_cast<uint64_t>(2) << 61;                    // 128-byte swizzle
-  return d;
-}
-
-// kind::f16 instruction descriptor: bf16 x bf16 -> fp32, both K-major.
-__host__ __device__ constexpr uint32_t idesc_bf16(int M, int N) {
-  return (1u << 4) | (1u << 7) | (1u << 10) | (static_cast<uint32_t>(N >> 3) << 17) |
-         (static_cast<uint32_t>(M >> 4) << 24);
-}
-
-__device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
-                                         uint32_t accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "setp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
-      : "memory");
-}
-__device__ __forceinline__ void mma_commit(uint64_t* bar) {
-  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
-                   smem_u32(bar))
-               : "memory");
-}
-
-// 16 consecutive fp32 columns of this warp's 32 TMEM lanes; the wait is part
-// of the same statement so no use of the registers can be hoisted above it.
-__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
-  uint32_t r[16];
-  asm volatile(
-      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15},"
-      " [%16];\n\t"
-      "tcgen05.wait::ld.sync.aligned;"
-      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
-        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
-        "=r"(r[14]), "=r"(r[15])
-      : "r"(taddr)
-      : "memory");
-#pragma unroll
-  for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
-}
-
-// 16-byte store to the same shared-memory offset in cluster member `rank`.
-__device__ __forceinline__ void st_dsmem_v4(float* local, uint32_t rank, float4 v) {
-  asm volatile(
-      "{\n\t.reg .b32 ra;\n\t"
-      "mapa.shared::cluster.u32 ra, %0, %1;\n\t"
-      "st.shared::cluster.v4.f32 [ra], {%2, %3, %4, %5};\n\t}" ::"r"(smem_u32(local)),
-      "r"(rank), "f"(v.x), "f"(v.y), "f"(v.z), "f"(v.w)
-      : "memory");
-}
-__device__ __forceinline__ void st_dsmem_f32(float* local, uint32_t rank, float v) {
-  asm volatile(
-      "{\n\t.reg .b32 ra;\n\t"
-      "mapa.shared::cluster.u32 ra, %0, %1;\n\t"
-      "st.shared::cluster.f32 [ra], %2;\n\t}" ::"r"(smem_u32(local)),
-      "r"(rank), "f"(v)
-      : "memory");
-}
-
-__device__ __forceinline__ uint32_t cluster_rank() {
-  uint32_t r;
-  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
-  return r;
-}
-__device__ __forceinline__ void cluster_sync_all() {
-  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::
-                   : "memory");
-}
-// Named barrier over one role's warps (ids 1.. are free; 0 is __syncthreads).
-template <int kId, int kCount>
-__device__ __forceinline__ void role_sync() {
-  asm volatile("bar.sync %0, %1;" ::"n"(kId), "n"(kCount) : "memory");
-}
-// The same barrier ANDing a flag over the role, so a wait that gave up in one
-// thread makes the whole role leave its loop together.
-template <int kId, int kCount>
-__device__ __forceinline__ bool role_all(bool ok) {
-  uint32_t r;
-  asm volatile(
-      "{\n\t.reg .pred p, q;\n\t"
-      "setp.ne.u32 p, %1, 0;\n\t"
-      "bar.red.and.pred q, %2, %3, p;\n\t"
-      "selp.u32 %0, 1, 0, q;\n\t}"
-      : "=r"(r)
-      : "r"((uint32_t)ok), "n"(kId), "n"(kCount)
-      : "memory");
-  return r != 0;
-}
 
 // ------------------------------------------------------------ kernel body
 template <int NS, int RR, int P>
@@ -300,18 +74,6 @@ constexpr int kWarpX = 0, kWarpMma = 1, kWarpW = 2, kWarpPub0 = 4, kWarpGate = 6
 constexpr int kYThreads = kThreads - kWarpYc0 * 32;   // 256
 // Named barriers: 1 = publish pair (64 threads), 2 = y warps.
 constexpr int kBarPub = 1, kBarY = 2;
-
-// Offset of 16-byte column c of row r in a 128-byte-swizzled tile.
-__device__ __forceinline__ int sw128(int r, int c) { return r * 128 + ((c ^ (r & 7)) << 4); }
-
-// 32 consecutive fp32 columns of this warp's 32 TMEM lanes (load + wait).
-__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
-  float a[16], b[16];
-  tmem_ld16(taddr, a);
-  tmem_ld16(taddr + 16, b);
-#pragma unroll
-  for (int i = 0; i < 16; ++i) { v[i] = a[i]; v[16 + i] = b[i]; }
-}
 
 template <int NS, int RR, int P>
 __global__ void __launch_bounds__(kThreads, 1)
@@ -404,7 +166,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       for (long long q = 0; q < (iss < XS ? iss : XS); ++q) {     // let issued copies land
         if (--xs < 0) { xs = XS - 1; xph ^= 1u; }
-        wait_bar<false>(&tail->x_full[xs], xph, ctl, kErrWaitTimeout);
+        mbar_drain(&tail->x_full[xs], xph);
       }
     }
   } else if (warp == kWarpW) {
@@ -429,7 +191,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       for (long long q = 0; q < (iss < WS ? iss : WS); ++q) {
         if (--ws < 0) { ws = WS - 1; wph ^= 1u; }
-        wait_bar<false>(&tail->w_full[ws], wph, ctl, kErrWaitTimeout);
+        mbar_drain(&tail->w_full[ws], wph);
       }
     }
   } else if (warp == kWarpMma) {
@@ -486,7 +248,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (++acc == C::kAccBufs) { acc = 0; acc_phase ^= 1u; }
       }
       mma_commit(&tail->mma_done);
-      wait_bar<false>(&tail->mma_done, 0, ctl, kErrWaitTimeout);
+      mbar_drain(&tail->mma_done, 0);
     }
   } else if (warp >= kWarpPub0 && warp < kWarpGate) {
     // ================================================= publish partial sums

@@ -90,12 +90,15 @@ def test_workspace_size(lib):
     st, n0 = mp.mhc_pre_workspace_size(h, 0)
     assert st == 0 and n0 == 0
     st, n1 = mp.mhc_pre_workspace_size(h, 64)
-    # header + stacked planes: NP = 3*24 rounded to 80 rows of n*D bf16
-    assert st == 0 and n1 == 256 + 80 * 4 * 256 * 2
+    # header + stacked planes (NP = 3*24 rounded to 80 rows of n*D bf16) +
+    # the grid-wide exchange rings: 4 slots x 128 tokens x 160 CTAs x 28
+    # floats of partials and 4 x 128 x n floats of y weights
+    rings = 4 * 128 * 160 * 28 * 4 + 4 * 128 * 4 * 4
+    assert st == 0 and n1 == 256 + 80 * 4 * 256 * 2 + rings
     st, _ = mp.mhc_pre_workspace_size(h, -1)
     assert st == mp.MHC_ERR_PARAM_INVALID
     h2 = _handle(impl_mode=1)
-    assert mp.mhc_pre_workspace_size(h2, 64)[1] == 256 + 48 * 4 * 256 * 2
+    assert mp.mhc_pre_workspace_size(h2, 64)[1] == 256 + 48 * 4 * 256 * 2 + rings
     mp.mhc_pre_destroy(h)
     mp.mhc_pre_destroy(h2)
 
