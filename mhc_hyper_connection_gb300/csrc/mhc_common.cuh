@@ -25,8 +25,9 @@ enum : uint32_t {
 // Workspace layout: [0, 256) header, then the phi planes, then the exchange
 // rings of the grid-wide forward.  Header words (uint32): 0 error word,
 // 1 grid-wide abort flag, [16, 32) partial-arrival counters, [32, 48)
-// gated-token counters, [48, 64) y-done counters, one per ring slot.  The
-// plane preparation kernel zeroes the whole header before every forward.
+// gated-token counters, [48, 64) y-done counters, one per (group, ring
+// slot).  The plane preparation kernel zeroes the whole header before every
+// forward.
 constexpr size_t kWsHeader = 256;
 constexpr int kHdrWords = 64;
 constexpr int kHdrAbort = 1, kHdrArrive = 16, kHdrReady = 32, kHdrYdone = 48;
@@ -301,14 +302,17 @@ cudaError_t tc_forward_occupancy(int n, int R, int P, size_t smem_bytes, int clu
 int tc_np(int R, int P);
 
 // ---------------------------------------------------------------------------
-// Grid-wide forward: every CTA (one per SM) owns a fixed set of (64-wide
-// d-chunk, stream) units and works on every 128-token tile; per-CTA partial
-// sums meet in a global ring, one CTA per token gates it, and y is formed by
-// each CTA for its own d-range.
+// Grid-wide forward: one CTA per SM, all resident (cooperative launch), split
+// into ng groups of G CTAs that take alternate 64-token tiles.  Every CTA of a
+// group owns a fixed run of 64-wide d-chunks of one stream and works on every
+// tile of its group; per-CTA partial sums meet in a global ring, one CTA per
+// token gates it, and each CTA forms y for its own d-range.
 // ---------------------------------------------------------------------------
-constexpr int kGwTile = 128;                  // tokens per tile (MMA M, TMEM lanes)
-constexpr int kGwUnitBytes = kGwTile * 128;   // one (d-chunk, stream) x box: 16 KB
-constexpr int kGwSlots = 4;                   // exchange-ring depth in tiles (<= 16)
+constexpr int kGwTile = 64;                   // tokens per tile (rows 0..63 of an M = 128 MMA)
+constexpr int kGwUnitBytes = kGwTile * 128;   // one (d-chunk, stream) x box: 8 KB
+constexpr int kGwSlots = 8;                   // exchange-ring depth per group, in tiles
+constexpr int kGwMaxGroups = 2;               // kGwMaxGroups * kGwSlots <= 16 header words
+constexpr int kGwSinkMax = 32;                // Sinkhorn tokens per batch (one per lane)
 
 __host__ __device__ constexpr int gw_np(int R, int P) { return ((P * R + 15) / 16) * 16; }
 
@@ -316,43 +320,52 @@ struct GwLayout {
   size_t phi, x, ycoef, sink, scnt, tail, total;
 };
 // Shared memory of the grid-wide kernel: the CTA's resident phi-plane blocks,
-// the x ring (xs slots of umax units), the y weights of one tile, the
-// Sinkhorn hand-off (two buffers of own_max tokens) and the barrier block.
-__host__ __device__ inline GwLayout gw_layout(int n, int R, int P, int umax, int xs, int own_max) {
+// the x ring (xs slots of umax units, plus one unit of slack that the M = 128
+// operand reads run into), the y weights of two tiles, two Sinkhorn batches
+// and the barrier block.
+__host__ __device__ inline GwLayout gw_layout(int n, int R, int P, int umax, int xs) {
   GwLayout L;
   size_t o = 0;
   L.phi = o;   o += (size_t)umax * gw_np(R, P) * 128;
-  L.x = o;     o += (size_t)xs * umax * kGwUnitBytes;
-  L.ycoef = o; o += (size_t)kGwTile * n * 4;
-  L.sink = o;  o += 2 * (size_t)own_max * n * n * 4;
-  L.scnt = o;  o += 16;
+  L.x = o;     o += ((size_t)xs * umax + 1) * kGwUnitBytes;
+  L.ycoef = o; o += 2 * (size_t)kGwTile * n * 4;
+  L.sink = o;  o += 2 * (size_t)kGwSinkMax * n * n * 4;
+  L.scnt = o;  o += 2 * (size_t)kGwSinkMax * 4;
   o = (o + 15) & ~size_t(15);
   L.tail = o;  o += kTailBytes;
   L.total = o + 1024;
   return L;
 }
-// Bytes of the exchange rings after the planes: partials [slots][128][grid][stride]
-// and y weights [slots][128][n].
-inline size_t gw_ring_bytes(int n, int R, int grid) {
-  return (size_t)kGwSlots * kGwTile * grid * partial_stride(R) * 4 + (size_t)kGwSlots * kGwTile * n * 4;
+// Bytes of the exchange rings after the planes for up to `ctas` CTAs in all:
+// partials [groups][slots][64][G][stride] and y weights [groups][slots][64][n].
+inline size_t gw_ring_bytes(int n, int R, int ctas) {
+  return (size_t)kGwSlots * kGwTile * ctas * partial_stride(R) * 4 +
+         (size_t)kGwMaxGroups * kGwSlots * kGwTile * n * 4;
 }
 
 struct GwGeom {
   int T, D, n;
-  int num_tiles;   // 128-token tiles
+  int num_tiles;   // 64-token tiles
   int nch;         // 64-wide d-chunks per stream
-  int umax;        // most units any CTA owns
+  int ng;          // groups (tiles k with k % ng == g go to group g)
+  int G;           // CTAs per group: n streams x gs CTAs per stream
+  int gs;          // CTAs per stream; CTA r takes stream r / gs, a run of its chunks
+  int box4d;       // 1: a CTA's chunks of a tile come as one 4-D box (D % 64 == 0)
+  int umax;        // most chunks any CTA owns
   int xstages;     // x ring depth
   int own_max;     // most tokens of one tile any CTA gates
+  int sink_batch;  // tiles per Sinkhorn batch (sink_batch * own_max <= kGwSinkMax)
+  int xlead;       // most tiles the x loads run ahead of this CTA's y (1..15)
 };
 
 struct GwLaunch {
   EpiParams epi;
   const void* x;           // bf16 [T, n, D] (re-read for y)
-  CUtensorMap tmap_x;      // x as (D, T, n): box (64, 128 tokens, 1 stream), 128B swizzle
-  CUtensorMap tmap_p;      // planes as (D, NP, n): box (64, NP, 1), 128B swizzle
+  CUtensorMap tmap_x;      // x as (64, T, chunks, n), box (64, 64 tokens, umax, 1), or as
+                           // (D, T, n), box (64, 64, 1) when D % 64 != 0; 128B swizzle
+  CUtensorMap tmap_p;      // planes as (64, NP, chunks, n), box (64, NP, umax, 1), or as
+                           // (D, NP, n), box (64, NP, 1); 128B swizzle
   int P;
-  int grid;                // CTAs, all resident at once (cooperative launch)
   GwGeom g;
   size_t smem_bytes;
   uint32_t* hdr;           // workspace header

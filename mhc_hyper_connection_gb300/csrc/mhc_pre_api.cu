@@ -70,6 +70,21 @@ bool encode_3d(CUtensorMap* map, const void* base, const uint64_t dims[3], const
   return r == CUDA_SUCCESS;
 }
 
+// 4-D bf16 map, same conventions (byte strides of dims 1..3 explicit).
+bool encode_4d(CUtensorMap* map, const void* base, const uint64_t dims[4], const uint64_t strides[3],
+               const uint32_t box[4]) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t d[4] = {dims[0], dims[1], dims[2], dims[3]};
+  cuuint64_t st[3] = {strides[0], strides[1], strides[2]};
+  cuuint32_t b[4] = {box[0], box[1], box[2], box[3]};
+  cuuint32_t estr[4] = {1, 1, 1, 1};
+  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), d, st, b, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
 struct DeviceInfo {
   bool ok = false;
   int sms = 0;
@@ -145,69 +160,97 @@ mhc::EpiParams epi_params(const mhc_pre_s* h, const mhc_pre_args* a) {
   return e;
 }
 
-// The grid-wide forward: one CTA per SM, each owning a run of (d-chunk,
-// stream) units; MHC_ERR_NOT_SUITABLE when its resident phi blocks and a
-// two-slot x ring do not fit, or the grid cannot be resident at once.
+// The grid-wide forward: one CTA per SM in ng groups of G = n * gs, CTA r of
+// a group owning a run of the d-chunks of stream r / gs; MHC_ERR_NOT_SUITABLE
+// when its resident phi blocks and a two-slot x ring do not fit, or the grid
+// cannot be resident at once.  Two groups when there are enough tiles to keep
+// both busy (MHC_PRE_GW_GROUPS overrides).
 mhc_status_t run_grid_wide(mhc_pre_s* h, const mhc_pre_args* a, const DeviceInfo& di,
                            __nv_bfloat16* planes, cudaStream_t s) {
   const int n = (int)h->cfg.n, D = (int)h->cfg.D, R = h->R, NP = h->NP;
   const int nch = (D + mhc::kChunkK - 1) / mhc::kChunkK;
-  const int units = nch * n;
-  int G = di.sms < kGwMaxGrid ? di.sms : kGwMaxGrid;
-  if (G > units) G = units;
-  if (G < 1) return MHC_ERR_NOT_SUITABLE;
-  const int umax = (units + G - 1) / G;
+  const int num_tiles = (int)((a->T + mhc::kGwTile - 1) / mhc::kGwTile);
+  const int sms = di.sms < kGwMaxGrid ? di.sms : kGwMaxGrid;
+  int ng = env_int("MHC_PRE_GW_GROUPS", num_tiles >= 8 ? 2 : 1);
+  ng = ng < 1 ? 1 : (ng > mhc::kGwMaxGroups ? mhc::kGwMaxGroups : ng);
+  int gs = sms / ng / n;
+  if (gs > nch) gs = nch;
+  if (gs < 1) return MHC_ERR_NOT_SUITABLE;
+  const int G = n * gs;
+  const int umax = (nch + gs - 1) / gs;
+  const bool box4d = (D % mhc::kChunkK) == 0;
   const int own_max = (mhc::kGwTile + G - 1) / G;
-  if (umax > 32) return MHC_ERR_NOT_SUITABLE;
+  if (umax > 32 || own_max > mhc::kGwSinkMax) return MHC_ERR_NOT_SUITABLE;
+  int sink_batch = mhc::kGwSinkMax / own_max;
+  if (sink_batch > 8) sink_batch = 8;
   int xmax = env_int("MHC_PRE_GW_XSTAGES", mhc::kMaxStages);
   xmax = xmax < 2 ? 2 : (xmax > mhc::kMaxStages ? mhc::kMaxStages : xmax);
   int xs = 0;
   for (int c = xmax; c >= 2 && !xs; --c)
-    if (mhc::gw_layout(n, R, h->P, umax, c, own_max).total <= di.max_smem) xs = c;
+    if (mhc::gw_layout(n, R, h->P, umax, c).total <= di.max_smem) xs = c;
   if (!xs) return MHC_ERR_NOT_SUITABLE;
-  const size_t smem = mhc::gw_layout(n, R, h->P, umax, xs, own_max).total;
+  const size_t smem = mhc::gw_layout(n, R, h->P, umax, xs).total;
   int cap = 0;
   if (mhc::gw_forward_capacity(n, R, h->P, smem, &cap) != cudaSuccess) {
     cudaGetLastError();
     return MHC_ERR_NOT_SUITABLE;
   }
-  if (cap < G) return MHC_ERR_NOT_SUITABLE;
+  if (cap < ng * G) return MHC_ERR_NOT_SUITABLE;
 
   mhc::GwLaunch L;
   memset(&L, 0, sizeof L);
   L.epi = epi_params(h, a);
   L.x = a->x;
   L.P = h->P;
-  L.grid = G;
   L.g.T = (int)a->T;
   L.g.D = D;
   L.g.n = n;
-  L.g.num_tiles = (int)((a->T + mhc::kGwTile - 1) / mhc::kGwTile);
+  L.g.num_tiles = num_tiles;
   L.g.nch = nch;
+  L.g.ng = ng;
+  L.g.G = G;
+  L.g.gs = gs;
+  L.g.box4d = box4d ? 1 : 0;
   L.g.umax = umax;
   L.g.xstages = xs;
   L.g.own_max = own_max;
+  L.g.sink_batch = sink_batch;
+  int xlead = env_int("MHC_PRE_GW_XLEAD", 6);
+  L.g.xlead = xlead < 1 ? 1 : (xlead > 15 ? 15 : xlead);
   L.smem_bytes = smem;
   uint8_t* ws = static_cast<uint8_t*>(a->workspace);
   L.hdr = reinterpret_cast<uint32_t*>(ws);
   L.partials = reinterpret_cast<float*>(ws + mhc::kWsHeader + planes_bytes(h));
-  L.coefs = L.partials + (size_t)mhc::kGwSlots * mhc::kGwTile * G * mhc::partial_stride(R);
+  L.coefs = L.partials + (size_t)mhc::kGwSlots * mhc::kGwTile * (ng * G) * mhc::partial_stride(R);
   {
-    // x [T][n][D] seen as (D, T, n), box (64, 128 tokens, 1 stream); the phi
-    // planes [NP][n][D] as (D, NP, n), box (64, NP, 1).
     const uint64_t K2 = (uint64_t)n * D * 2;
-    const uint64_t xd[3] = {(uint64_t)D, (uint64_t)a->T, (uint64_t)n};
-    const uint64_t st[2] = {K2, (uint64_t)D * 2};
-    const uint32_t xb[3] = {(uint32_t)mhc::kChunkK, (uint32_t)mhc::kGwTile, 1u};
-    const uint64_t pd[3] = {(uint64_t)D, (uint64_t)NP, (uint64_t)n};
-    const uint32_t pb[3] = {(uint32_t)mhc::kChunkK, (uint32_t)NP, 1u};
-    if (!encode_3d(&L.tmap_x, a->x, xd, st, xb) || !encode_3d(&L.tmap_p, planes, pd, st, pb))
-      return fail(MHC_ERR_RUNTIME, "tensor map encoding failed");
+    bool enc;
+    if (box4d) {
+      // x [T][n][D] seen as (64, T, chunk, n), box (64, 64 tokens, umax chunks, 1
+      // stream); the phi planes [NP][n][D] as (64, NP, chunk, n), box (64, NP,
+      // umax, 1).  Shared memory then holds one 64-row block per chunk.
+      const uint64_t xd[4] = {(uint64_t)mhc::kChunkK, (uint64_t)a->T, (uint64_t)nch, (uint64_t)n};
+      const uint64_t xst[3] = {K2, (uint64_t)mhc::kChunkK * 2, (uint64_t)D * 2};
+      const uint32_t xb[4] = {(uint32_t)mhc::kChunkK, (uint32_t)mhc::kGwTile, (uint32_t)umax, 1u};
+      const uint64_t pd[4] = {(uint64_t)mhc::kChunkK, (uint64_t)NP, (uint64_t)nch, (uint64_t)n};
+      const uint32_t pb[4] = {(uint32_t)mhc::kChunkK, (uint32_t)NP, (uint32_t)umax, 1u};
+      enc = encode_4d(&L.tmap_x, a->x, xd, xst, xb) && encode_4d(&L.tmap_p, planes, pd, xst, pb);
+    } else {
+      // x as (D, T, n), box (64, 64 tokens, 1 stream), one box per chunk; the
+      // planes as (D, NP, n), box (64, NP, 1).
+      const uint64_t xd[3] = {(uint64_t)D, (uint64_t)a->T, (uint64_t)n};
+      const uint64_t st[2] = {K2, (uint64_t)D * 2};
+      const uint32_t xb[3] = {(uint32_t)mhc::kChunkK, (uint32_t)mhc::kGwTile, 1u};
+      const uint64_t pd[3] = {(uint64_t)D, (uint64_t)NP, (uint64_t)n};
+      const uint32_t pb[3] = {(uint32_t)mhc::kChunkK, (uint32_t)NP, 1u};
+      enc = encode_3d(&L.tmap_x, a->x, xd, st, xb) && encode_3d(&L.tmap_p, planes, pd, st, pb);
+    }
+    if (!enc) return fail(MHC_ERR_RUNTIME, "tensor map encoding failed");
   }
   h->last_cluster = 0;
-  h->last_grid = G;
+  h->last_grid = ng * G;
   h->last_stages = xs;
-  h->last_ystages = umax;
+  h->last_ystages = ng;
   if (h->ev_before && cudaEventRecord(h->ev_before, s) != cudaSuccess)
     return fail(MHC_ERR_RUNTIME, "recording the timing event failed");
   if (mhc::launch_gw_forward(L, s) != cudaSuccess)

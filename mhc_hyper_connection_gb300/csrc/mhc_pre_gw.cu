@@ -5,28 +5,34 @@
 // how it is laid out on the GPU is this file's own design.
 //
 // The forward is bound by reading x, and y needs every byte of x a second
-// time once the token's gates are known.  The gates need the whole token
-// (a reduction over n*D), so the second read can only hit L2 if the bytes
-// loaded between a token's first touch and its gates stay small.  Here every
-// CTA (one per SM, all resident: cooperative launch) works on the SAME
-// 128-token tile at about the same time, each on its own slice of d:
+// time once the token's gates are known.  The gates need the whole token (a
+// reduction over n*D), so the second read only hits L2 if little is loaded
+// between a token's first touch and its gates.  Here the CTAs (one per SM,
+// all resident: cooperative launch) form ng groups of G; group g takes the
+// 64-token tiles k with k % ng == g, and all CTAs of a group work on the
+// same tile at about the same time, each on its own slice of d:
 //
-//  * CTA b owns a contiguous run of (64-wide d-chunk, stream) units.  Their
-//    phi-plane blocks stay in shared memory for the whole kernel; each tile
-//    brings one 16 KB x box per unit (TMA, 128-byte swizzle).
-//  * One thread issues tcgen05.mma over the CTA's units, M = 128 tokens,
-//    N = NP plane rows, fp32 accumulate in TMEM (two buffers).  Four warps
-//    add x^2 for their token rows from the same shared-memory boxes, read
-//    the accumulators (thread = token = TMEM lane), fold the precision planes
-//    and store the CTA's partial sums to a global ring.
-//  * Token t of tile k is gated by CTA (128k + t) mod grid: once every CTA
-//    has published tile k (a counter per ring slot), its gate warp sums the
-//    partials in CTA order, computes invRms and the gates, writes the y
-//    weights to the ring and counts the token as ready; the Sinkhorn warp
-//    then produces comb off the critical path.
-//  * When all tokens of tile k are ready, eight warps form y for the CTA's
-//    own d-range, re-reading x (loaded moments ago by the whole GPU: an L2
-//    hit) with plain 16-byte loads.
+//  * CTA r of a group owns a contiguous run of 64-wide d-chunks of one
+//    stream.  Their phi-plane blocks stay in shared memory for the whole
+//    kernel; each tile brings the run as one TMA box (8 KB per chunk,
+//    128-byte swizzle): one issue per tile, since a thread issues only a
+//    couple of boxes per microsecond whatever their size.
+//  * One thread issues tcgen05.mma over the units, M = 128 (tile rows 0..63),
+//    N = NP plane rows, fp32 accumulate in TMEM (two buffers).  Two warps add
+//    x^2 for their rows from the same boxes, read the accumulators (thread =
+//    token = TMEM lane), fold the precision planes and store the CTA's
+//    partial sums to a global ring; a signalling thread makes them visible
+//    and counts the CTA in, so the publishing warps never wait on the fence.
+//  * Local token t of the group's m-th tile is gated by CTA (64m + t) mod G.
+//    Two gate warps take alternate tiles: once every CTA of the group has
+//    counted in, a gate warp sums the partials in CTA order, computes invRms
+//    and the gates, writes the y weights to the ring and counts the token
+//    ready.  The Sinkhorn warp runs the tokens of several tiles at once, one
+//    per lane, off y's critical path.
+//  * One warp waits for each tile to be fully gated and stages its y
+//    weights in shared memory; seven warps form y for the CTA's own d-range,
+//    loading the tile's x (loaded moments ago by the group: an L2 hit)
+//    before the weights are there.
 //
 // Every wait is bounded by a timer.  A wait that gives up sets the error
 // word and a grid-wide abort flag, and every CTA winds down.
@@ -37,12 +43,16 @@ namespace {
 
 constexpr int kGwThreads = 512;
 // Warp roles.
-constexpr int kGwWarpX = 0, kGwWarpMma = 1, kGwWarpGate = 2, kGwWarpSink = 3, kGwWarpPub0 = 4,
-              kGwWarpY0 = 8;
-constexpr int kGwPubThreads = 128;
-constexpr int kGwYThreads = kGwThreads - kGwWarpY0 * 32;   // 256
-// Named barriers: 1 = publish warps, 2 = y warps.
-constexpr int kGwBarPub = 1, kGwBarY = 2;
+constexpr int kGwWarpX = 0, kGwWarpMma = 1, kGwWarpSig = 2, kGwWarpSink = 3, kGwWarpPub0 = 4,
+              kGwWarpGate0 = 6, kGwWarpY0 = 8;
+constexpr int kGwPubThreads = 64;                          // one per tile row (TMEM lanes 0..63)
+constexpr int kGwWarpYc0 = kGwWarpY0 + 1;                  // y warps after the weight stager
+constexpr int kGwYcWarps = kGwThreads / 32 - kGwWarpYc0;   // 7
+constexpr int kGwYcThreads = kGwYcWarps * 32;              // 224
+constexpr int kGwGateWarps = 2;
+constexpr int kGwPubRing = 4;                              // publish -> signaller hand-off depth
+// Named barrier 1: the publish warps.
+constexpr int kGwBarPub = 1;
 
 template <int NS, int RR, int P>
 struct GwCfg {
@@ -53,9 +63,7 @@ struct GwCfg {
   static constexpr int kPlaneBytes = kNP * 128;                 // one unit's phi-plane block
   static constexpr int kStr = partial_stride(RR);               // floats per partial
   static constexpr int kG4 = kStr / 4;                          // float4 groups per partial
-  static constexpr int kG4Pad = kG4 <= 4 ? 4 : kG4 <= 8 ? 8 : kG4 <= 16 ? 16 : 32;
-  static_assert(kG4 <= 32, "one lane per float4 group");
-  static constexpr int kLpg = 32 / kG4Pad;                      // lanes summing one group
+  static constexpr int kRounds = kG4 <= 8 ? 3 : 1;              // rounds of CTAs loaded at once
   static constexpr bool kThree = (RR == NS * NS + 2 * NS);
   static constexpr int kYB = NS <= 4 ? 4 : 2;                   // y items in flight per thread
 };
@@ -64,7 +72,11 @@ struct GwTail {
   uint64_t x_full[kMaxStages], x_empty[kMaxStages];
   uint64_t acc_full[2], acc_empty[2];
   uint64_t phi_full;
+  uint64_t pub_done[kGwPubRing], sig_free[kGwPubRing];
   uint64_t sink_full[2], sink_free[2];
+  uint64_t y_prog[kGwSlots];          // a tile of that ring slot is fully gated (seen by the watcher)
+  uint64_t ycoef_full[2], ycoef_free[2];   // y weights of a tile staged / consumed
+  uint64_t y_done[16];                     // this CTA's y warps finished tile m (index m % 16)
   uint64_t mma_done;
   uint32_t tmem_base;
   uint32_t abort;
@@ -108,17 +120,27 @@ __device__ __forceinline__ uint32_t ld_acquire_gpu(const uint32_t* p) {
   asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
   return v;
 }
+__device__ __forceinline__ uint32_t ld_relaxed_gpu(const uint32_t* p) {
+  uint32_t v;
+  asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+// Release at GPU scope: writes this thread made, or saw through a CTA barrier,
+// are visible before the count changes.
 __device__ __forceinline__ void red_release_gpu(uint32_t* p, uint32_t v) {
   asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
 }
 
 // Wait until a global counter written by other CTAs reaches `target`
-// (acquire: what they wrote before counting is visible afterwards).
+// (acquire: what they wrote before counting is visible afterwards).  While
+// it is short, poll with plain loads and back off, so a waiting thread does
+// not load the SM's memory pipeline; the final read is the acquire.
 __device__ __noinline__ bool gw_wait_count(const uint32_t* ctr, uint32_t target, const GwCtl& c) {
   if (ld_acquire_gpu(ctr) >= target) return true;
   const uint64_t t0 = now_ns();
   for (uint32_t it = 1;; ++it) {
-    if (ld_acquire_gpu(ctr) >= target) return true;
+    __nanosleep(128);
+    if (ld_relaxed_gpu(ctr) >= target) return ld_acquire_gpu(ctr) >= target;
     if ((it & 15u) == 0) {
       if (*c.abort || *c.gabort) {
         *c.abort = 1u;
@@ -132,8 +154,16 @@ __device__ __noinline__ bool gw_wait_count(const uint32_t* ctr, uint32_t target,
   }
 }
 
-__device__ __forceinline__ float f4_get(const float4& v, int i) {
-  return i == 0 ? v.x : i == 1 ? v.y : i == 2 ? v.z : v.w;
+// Lane 0 waits; the result reaches the whole warp.
+__device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, const GwCtl& c) {
+  bool ok = true;
+  if ((threadIdx.x & 31) == 0) ok = gw_wait(bar, parity, c);
+  return __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+}
+
+// First local row t of a tile that CTA r of the group gates: (64m + t) % G == r.
+__device__ __forceinline__ int first_owned(int m, int r, int G) {
+  return (int)(((long long)r - (long long)m * kGwTile % G + G) % G);
 }
 
 template <int NS, int RR, int P>
@@ -145,40 +175,56 @@ __global__ void __launch_bounds__(kGwThreads, 1)
   constexpr int NN = NS * NS;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  const GwLayout Ly = gw_layout(NS, RR, P, g.umax, g.xstages, g.own_max);
+  const GwLayout Ly = gw_layout(NS, RR, P, g.umax, g.xstages);
   const int XS = g.xstages;
   uint8_t* sPhi = smem + Ly.phi;
   uint8_t* sX = smem + Ly.x;
-  float* ycoef = reinterpret_cast<float*>(smem + Ly.ycoef);   // [128][NS]
-  float* sink_buf = reinterpret_cast<float*>(smem + Ly.sink); // [2][own_max][NN]
-  int* sink_cnt = reinterpret_cast<int*>(smem + Ly.scnt);     // [2]
+  float* ycoef = reinterpret_cast<float*>(smem + Ly.ycoef);   // [2][64][NS]
+  float* sink_buf = reinterpret_cast<float*>(smem + Ly.sink); // [2][kGwSinkMax][NN]
+  int* sink_cnt = reinterpret_cast<int*>(smem + Ly.scnt);     // [2][kGwSinkMax]: tokens per tile
   GwTail* tail = reinterpret_cast<GwTail*>(smem + Ly.tail);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int G = gridDim.x;
-  const int b = blockIdx.x;
-  const int units = g.nch * NS;
-  const int u0 = (int)((long long)b * units / G);
-  const int U = (int)((long long)(b + 1) * units / G) - u0;   // units this CTA owns (>= 1)
+  const int G = g.G;
+  const int grp = blockIdx.x / G;                 // group
+  const int r = blockIdx.x - grp * G;             // rank in the group
+  const int my_tiles = grp < g.num_tiles ? (g.num_tiles - grp + g.ng - 1) / g.ng : 0;
+  const int stream = r / g.gs;                     // this CTA's stream
+  const int rs = r - stream * g.gs;
+  const int j0 = (int)((long long)rs * g.nch / g.gs);
+  const int U = (int)((long long)(rs + 1) * g.nch / g.gs) - j0;   // chunks this CTA owns (>= 1)
   const size_t slot_bytes = (size_t)g.umax * kGwUnitBytes;
-  uint32_t* arrive = hdr + kHdrArrive;
-  uint32_t* ready = hdr + kHdrReady;
-  uint32_t* ydone = hdr + kHdrYdone;
+  const int SB = g.sink_batch;
+  uint32_t* arrive = hdr + kHdrArrive + grp * kGwSlots;
+  uint32_t* ready = hdr + kHdrReady + grp * kGwSlots;
+  uint32_t* ydone = hdr + kHdrYdone + grp * kGwSlots;
+  float* gpart = partials + (size_t)grp * kGwSlots * kGwTile * G * C::kStr;
+  float* gcoef = coefs + (size_t)grp * kGwSlots * kGwTile * NS;
   GwCtl ctl{&tail->abort, hdr + kHdrAbort, hdr};
 
   // ---- set-up
   if (threadIdx.x == 0) {
     for (int s = 0; s < XS; ++s) {
       mbar_init(&tail->x_full[s], 1);
-      mbar_init(&tail->x_empty[s], 1 + 4);      // MMA commit + the four sum-of-squares warps
+      mbar_init(&tail->x_empty[s], 1 + 2);      // MMA commit + the two sum-of-squares warps
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(&tail->acc_full[a], 1);
-      mbar_init(&tail->acc_empty[a], 4);        // four publish warps
-      mbar_init(&tail->sink_full[a], 1);
+      mbar_init(&tail->acc_empty[a], 2);        // two publish warps
+      mbar_init(&tail->sink_full[a], SB);       // one arrival per tile of a batch
       mbar_init(&tail->sink_free[a], 1);
     }
+    for (int j = 0; j < kGwPubRing; ++j) {
+      mbar_init(&tail->pub_done[j], 2);         // two publish warps
+      mbar_init(&tail->sig_free[j], 1);
+    }
+    for (int j = 0; j < kGwSlots; ++j) mbar_init(&tail->y_prog[j], 1);
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&tail->ycoef_full[b], 1);
+      mbar_init(&tail->ycoef_free[b], kGwYcWarps);
+    }
+    for (int j = 0; j < 16; ++j) mbar_init(&tail->y_done[j], kGwYcWarps);
     mbar_init(&tail->phi_full, 1);
     mbar_init(&tail->mma_done, 1);
     tail->abort = 0u;
@@ -200,28 +246,41 @@ __global__ void __launch_bounds__(kGwThreads, 1)
 
   if (warp == kGwWarpX) {
     // ================================================= TMA: phi planes once, then x
-    // Lane q issues unit q's box, so the CTA's boxes of one tile go out
-    // together.
+    // Lane q issues unit q's box, so the CTA's boxes of one tile go out together.
+    // A 4-D box carries all umax chunks at once (its tail past this CTA's
+    // run is the next CTA's data or zero fill, and is not used).
     const uint64_t keep = policy_evict_last();
-    if (lane == 0) mbar_expect_tx(&tail->phi_full, (uint32_t)(U * C::kPlaneBytes));
+    const int nbox = g.box4d ? 1 : U;
+    const uint32_t xbytes = (uint32_t)((g.box4d ? g.umax : U) * kGwUnitBytes);
+    if (lane == 0) mbar_expect_tx(&tail->phi_full, (uint32_t)((g.box4d ? g.umax : U) * C::kPlaneBytes));
     __syncwarp();
-    if (lane < U) {
-      const int u = u0 + lane, i = u / g.nch, j = u - i * g.nch;
-      tma_load_3d_hint(sPhi + (size_t)lane * C::kPlaneBytes, &tmap_p, &tail->phi_full, j * kChunkK, 0, i, keep);
+    if (lane < nbox) {
+      if (g.box4d)
+        tma_load_4d_hint(sPhi, &tmap_p, &tail->phi_full, 0, 0, j0, stream, keep);
+      else
+        tma_load_3d_hint(sPhi + (size_t)lane * C::kPlaneBytes, &tmap_p, &tail->phi_full, (j0 + lane) * kChunkK, 0,
+                         stream, keep);
     }
     int xs = 0;
     uint32_t xph = 0;
     int issued = 0;
-    for (int k = 0; k < g.num_tiles; ++k) {
-      bool ok = true;
-      if (lane == 0) ok = gw_wait(&tail->x_empty[xs], xph ^ 1u, ctl);
-      if (!__shfl_sync(0xffffffffu, ok ? 1 : 0, 0)) break;
-      if (lane == 0) mbar_expect_tx(&tail->x_full[xs], (uint32_t)(U * kGwUnitBytes));
+    for (int m = 0; m < my_tiles; ++m) {
+      if (!warp_wait(&tail->x_empty[xs], xph ^ 1u, ctl)) break;
+      // Load no further than xlead tiles ahead of this CTA's y warps, so the
+      // bytes loaded between a tile's first read and its re-read for y stay
+      // within what L2 keeps.
+      if (m >= g.xlead && !warp_wait(&tail->y_done[(m - g.xlead) & 15], (uint32_t)((m - g.xlead) >> 4) & 1u, ctl))
+        break;
+      if (lane == 0) mbar_expect_tx(&tail->x_full[xs], xbytes);
       __syncwarp();
-      if (lane < U) {
-        const int u = u0 + lane, i = u / g.nch, j = u - i * g.nch;
-        tma_load_3d_hint(sX + (size_t)xs * slot_bytes + (size_t)lane * kGwUnitBytes, &tmap_x, &tail->x_full[xs],
-                         j * kChunkK, k * kGwTile, i, keep);
+      if (lane < nbox) {
+        const int k = grp + m * g.ng;
+        uint8_t* dst = sX + (size_t)xs * slot_bytes;
+        if (g.box4d)
+          tma_load_4d_hint(dst, &tmap_x, &tail->x_full[xs], 0, k * kGwTile, j0, stream, keep);
+        else
+          tma_load_3d_hint(dst + (size_t)lane * kGwUnitBytes, &tmap_x, &tail->x_full[xs], (j0 + lane) * kChunkK,
+                           k * kGwTile, stream, keep);
       }
       ++issued;
       if (++xs == XS) { xs = 0; xph ^= 1u; }
@@ -241,15 +300,17 @@ __global__ void __launch_bounds__(kGwThreads, 1)
       bool ok = gw_wait(&tail->phi_full, 0, ctl);
       int xs = 0;
       uint32_t xph = 0;
-      for (int k = 0; k < g.num_tiles && ok; ++k) {
-        const int acc = k & 1;
-        const uint32_t acc_phase = (uint32_t)(k >> 1) & 1u;
+      for (int m = 0; m < my_tiles && ok; ++m) {
+        const int acc = m & 1;
+        const uint32_t acc_phase = (uint32_t)(m >> 1) & 1u;
         if (!gw_wait(&tail->acc_empty[acc], acc_phase ^ 1u, ctl)) break;
         if (!gw_wait(&tail->x_full[xs], xph, ctl)) break;
         tc_fence_after();
         const uint32_t d = tmem_base + (uint32_t)(acc * C::kAccCols);
         const uint32_t xb = smem_u32(sX + (size_t)xs * slot_bytes);
         for (int q = 0; q < U; ++q) {
+          // A: 128 rows from this unit's 64-row box (rows 64..127 run on into
+          // the next box and feed TMEM lanes that are never read).
           const uint32_t a0 = xb + (uint32_t)(q * kGwUnitBytes);
           const uint32_t b0 = phi0 + (uint32_t)(q * C::kPlaneBytes);
 #pragma unroll
@@ -263,34 +324,42 @@ __global__ void __launch_bounds__(kGwThreads, 1)
       mma_commit(&tail->mma_done);
       mbar_drain(&tail->mma_done, 0);
     }
-  } else if (warp >= kGwWarpPub0 && warp < kGwWarpY0) {
+  } else if (warp == kGwWarpPub0 || warp == kGwWarpPub0 + 1) {
     // ================================================= sum of squares + partials
-    // Thread = token row of the tile = TMEM lane.
-    const int t = threadIdx.x - kGwWarpPub0 * 32;   // 0..127
-    const int wq = warp & 3;                        // TMEM lane quarter
+    // Thread = tile row = TMEM lane (warps 4 and 5: lane quarters 0 and 1).
+    const int t = threadIdx.x - kGwWarpPub0 * 32;   // 0..63
+    const int wq = warp & 3;
     int xs = 0;
     uint32_t xph = 0;
-    for (int k = 0; k < g.num_tiles; ++k) {
-      const int acc = k & 1;
-      const uint32_t acc_phase = (uint32_t)(k >> 1) & 1u;
-      // x^2 over this CTA's units, straight from the swizzled boxes (the
-      // order of a row's 16-byte pieces does not matter for a sum).
+    for (int m = 0; m < my_tiles; ++m) {
+      const int acc = m & 1;
+      const uint32_t acc_phase = (uint32_t)(m >> 1) & 1u;
+      // x^2 over this CTA's chunks, straight from the swizzled boxes.  Lane t
+      // reads its row's 16-byte pieces in the order they sit in the 128-byte
+      // swizzle (piece c at c ^ (t & 7)), so a warp's loads spread over all
+      // banks; the order of a row's pieces does not matter for a sum.
       if (!role_all<kGwBarPub, kGwPubThreads>(gw_wait(&tail->x_full[xs], xph, ctl))) break;
-      float ssq = 0.0f;
+      float s8[8];
+#pragma unroll
+      for (int e = 0; e < 8; ++e) s8[e] = 0.0f;
       const uint8_t* xrow = sX + (size_t)xs * slot_bytes + (size_t)t * 128;
       for (int q = 0; q < U; ++q) {
+        uint4 v[8];
+#pragma unroll
+        for (int c = 0; c < 8; ++c)
+          v[c] = *reinterpret_cast<const uint4*>(xrow + (size_t)q * kGwUnitBytes + ((c ^ (t & 7)) << 4));
 #pragma unroll
         for (int c = 0; c < 8; ++c) {
-          const uint4 v = *reinterpret_cast<const uint4*>(xrow + (size_t)q * kGwUnitBytes + c * 16);
-          const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&v);
+          const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&v[c]);
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
             const float2 f = __bfloat1622float2(h[e]);
-            ssq = fmaf(f.x, f.x, ssq);
-            ssq = fmaf(f.y, f.y, ssq);
+            s8[2 * e] = fmaf(f.x, f.x, s8[2 * e]);
+            s8[2 * e + 1] = fmaf(f.y, f.y, s8[2 * e + 1]);
           }
         }
       }
+      const float ssq = tree_sum<8>(s8);
       __syncwarp();
       if (lane == 0) mbar_arrive(&tail->x_empty[xs]);
       if (++xs == XS) { xs = 0; xph ^= 1u; }
@@ -300,15 +369,15 @@ __global__ void __launch_bounds__(kGwThreads, 1)
       tc_fence_after();
       float mix[RR];
 #pragma unroll
-      for (int r = 0; r < RR; ++r) mix[r] = 0.0f;
+      for (int rr = 0; rr < RR; ++rr) mix[rr] = 0.0f;
       const uint32_t taddr = tmem_base + ((uint32_t)(wq * 32) << 16) + (uint32_t)(acc * C::kAccCols);
 #pragma unroll
-      for (int grp = 0; grp < C::kNP / 16; ++grp) {
+      for (int gq = 0; gq < C::kNP / 16; ++gq) {
         float v[16];
-        tmem_ld16(taddr + grp * 16, v);
+        tmem_ld16(taddr + gq * 16, v);
 #pragma unroll
         for (int e = 0; e < 16; ++e) {
-          const int col = grp * 16 + e;
+          const int col = gq * 16 + e;
           if (col < P * RR) mix[col % RR] += v[e];
         }
       }
@@ -316,153 +385,227 @@ __global__ void __launch_bounds__(kGwThreads, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(&tail->acc_empty[acc]);
 
-      // the ring slot is free once every token of tile k - kGwSlots is gated
-      const int gs = k % kGwSlots;
-      const uint32_t use = (uint32_t)(k / kGwSlots);
+      // The ring slot is free once every token of the slot's previous tile is
+      // gated, as the ring watcher reports.
+      const int slot = m % kGwSlots;
+      const uint32_t use = (uint32_t)(m / kGwSlots);
       bool ok = true;
-      if (use > 0 && t == 0) ok = gw_wait_count(&ready[gs], use * (uint32_t)kGwTile, ctl);
-      if (!role_all<kGwBarPub, kGwPubThreads>(ok)) break;
-      float* dst = partials + (((size_t)gs * kGwTile + t) * G + b) * C::kStr;
-#pragma unroll
-      for (int r = 0; r < C::kStr; r += 4) {
-        float4 v;
-        v.x = r < RR ? mix[r] : (r == RR ? ssq : 0.0f);
-        v.y = r + 1 < RR ? mix[r + 1] : (r + 1 == RR ? ssq : 0.0f);
-        v.z = r + 2 < RR ? mix[r + 2] : (r + 2 == RR ? ssq : 0.0f);
-        v.w = r + 3 < RR ? mix[r + 3] : (r + 3 == RR ? ssq : 0.0f);
-        __stcg(reinterpret_cast<float4*>(dst + r), v);
-      }
-      role_sync<kGwBarPub, kGwPubThreads>();
       if (t == 0) {
-        __threadfence();
-        red_release_gpu(&arrive[gs], 1u);
+        if (use > 0) ok = gw_wait(&tail->y_prog[slot], (use - 1u) & 1u, ctl);
+        if (ok && m >= kGwPubRing)
+          ok = gw_wait(&tail->sig_free[m % kGwPubRing], ((uint32_t)(m / kGwPubRing) - 1u) & 1u, ctl);
+      }
+      if (!role_all<kGwBarPub, kGwPubThreads>(ok)) break;
+      float* dst = gpart + (((size_t)slot * kGwTile + t) * G + r) * C::kStr;
+#pragma unroll
+      for (int e = 0; e < C::kStr; e += 4) {
+        float4 v;
+        v.x = e < RR ? mix[e] : (e == RR ? ssq : 0.0f);
+        v.y = e + 1 < RR ? mix[e + 1] : (e + 1 == RR ? ssq : 0.0f);
+        v.z = e + 2 < RR ? mix[e + 2] : (e + 2 == RR ? ssq : 0.0f);
+        v.w = e + 3 < RR ? mix[e + 3] : (e + 3 == RR ? ssq : 0.0f);
+        __stcg(reinterpret_cast<float4*>(dst + e), v);
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&tail->pub_done[m % kGwPubRing]);   // release: this warp's stores
+    }
+  } else if (warp == kGwWarpSig) {
+    // ================================================= count this CTA in
+    // One fence covers every tile whose partials are stored by then, so a
+    // signaller that fell behind catches up a batch at a time.
+    if (lane == 0) {
+      for (int m = 0; m < my_tiles;) {
+        if (!gw_wait(&tail->pub_done[m % kGwPubRing], (uint32_t)(m / kGwPubRing) & 1u, ctl)) break;
+        int last = m;
+        while (last + 1 < my_tiles && last + 1 < m + kGwPubRing &&
+               mbar_poll(&tail->pub_done[(last + 1) % kGwPubRing], (uint32_t)((last + 1) / kGwPubRing) & 1u))
+          ++last;
+        asm volatile("fence.acq_rel.gpu;" ::: "memory");
+        for (int j = m; j <= last; ++j) {
+          asm volatile("red.relaxed.gpu.global.add.u32 [%0], 1;" ::"l"(&arrive[j % kGwSlots]) : "memory");
+          mbar_arrive(&tail->sig_free[j % kGwPubRing]);
+        }
+        m = last + 1;
+      }
+    } else if (lane == 16) {
+      // Ring watcher: marks each tile fully gated as soon as the group has
+      // gated it, which frees its ring slot for the tile kGwSlots later (an
+      // owner counts a token only after it has read the token's partials).
+      for (int m = 0; m < my_tiles; ++m) {
+        const int k = grp + m * g.ng;
+        const int valid = min(kGwTile, g.T - k * kGwTile);
+        const uint32_t target = (uint32_t)(m / kGwSlots) * (uint32_t)kGwTile + (uint32_t)valid;
+        if (!gw_wait_count(&ready[m % kGwSlots], target, ctl)) break;
+        mbar_arrive(&tail->y_prog[m % kGwSlots]);
       }
     }
-  } else if (warp == kGwWarpGate) {
+  } else if (warp == kGwWarpGate0 || warp == kGwWarpGate0 + 1) {
     // ================================================= gates of the tokens this CTA owns
-    const int grp4 = lane % C::kG4Pad;
-    const int sub = lane / C::kG4Pad;
-    for (int k = 0; k < g.num_tiles; ++k) {
-      const int gs = k % kGwSlots;
-      const uint32_t use = (uint32_t)(k / kGwSlots);
+    const int gidx = warp - kGwWarpGate0;
+    for (int m = gidx; m < my_tiles; m += kGwGateWarps) {
+      const int k = grp + m * g.ng;
       const int tile0 = k * kGwTile;
       const int valid = min(kGwTile, g.T - tile0);
-      const int first = (int)(((long long)b - (long long)tile0 % G + G) % G);
-      const int sb = k & 1;
-      bool ok = true;
-      if (k >= 2 && lane == 0) ok = gw_wait(&tail->sink_free[sb], ((uint32_t)(k >> 1) - 1u) & 1u, ctl);
-      if (!__shfl_sync(0xffffffffu, ok ? 1 : 0, 0)) break;
+      const int slot = m % kGwSlots;
+      const uint32_t use = (uint32_t)(m / kGwSlots);
+      const int first = first_owned(m, r, G);
+      const int q = m / SB, sb = q & 1, e0 = (m - q * SB) * g.own_max;
+      // the Sinkhorn batch buffer is free once batch q - 2 is done
+      if (q >= 2 && (m - q * SB) < kGwGateWarps &&
+          !warp_wait(&tail->sink_free[sb], ((uint32_t)(q >> 1) - 1u) & 1u, ctl))
+        break;
       int cnt = 0;
       if (first < valid) {
+        bool ok = true;
         if (lane == 0) {
-          ok = gw_wait_count(&arrive[gs], (use + 1u) * (uint32_t)G, ctl);
-          if (ok && use > 0) ok = gw_wait_count(&ydone[gs], use * (uint32_t)G, ctl);
+          // The slot's previous weights must have been read by every CTA (a
+          // plain count: those reads completed before it was taken); the
+          // partials of this tile must all be in (acquire).
+          const uint32_t yd = use > 0 ? ld_relaxed_gpu(&ydone[slot]) : 0u;
+          ok = gw_wait_count(&arrive[slot], (use + 1u) * (uint32_t)G, ctl);
+          if (ok && use > 0 && yd < use * (uint32_t)G) ok = gw_wait_count(&ydone[slot], use * (uint32_t)G, ctl);
         }
         if (!__shfl_sync(0xffffffffu, ok ? 1 : 0, 0)) break;
         for (int t = first; t < valid; t += G, ++cnt) {
-          // sum the CTAs' partials of row t in a fixed order: lane (sub, grp4)
-          // adds CTAs sub, sub + kLpg, ... of float4 group grp4, then a fixed
-          // butterfly over the subs.
-          const float* src = partials + ((size_t)gs * kGwTile + t) * G * C::kStr;
-          float4 s4 = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
-          if (grp4 < C::kG4) {
-#pragma unroll 4
-            for (int c = sub; c < G; c += C::kLpg) {
-              const float4 v = __ldcg(reinterpret_cast<const float4*>(src + (size_t)c * C::kStr + grp4 * 4));
-              s4.x += v.x;
-              s4.y += v.y;
-              s4.z += v.z;
-              s4.w += v.w;
+          // Sum the CTAs' partials of row t in a fixed order: lane l adds
+          // CTAs l, l + 32, ... then a fixed butterfly adds the lanes.
+          const float* src = gpart + ((size_t)slot * kGwTile + t) * G * C::kStr;
+          float acc[C::kStr];
+#pragma unroll
+          for (int e = 0; e < C::kStr; ++e) acc[e] = 0.0f;
+          for (int rd0 = 0; rd0 * 32 < G; rd0 += C::kRounds) {
+            // kRounds rounds of CTAs per pass: every load of the pass is
+            // issued before the first add
+            float4 v[C::kRounds][C::kG4];
+#pragma unroll
+            for (int h = 0; h < C::kRounds; ++h) {
+              const int c = lane + 32 * (rd0 + h);
+              const float4* s4 = reinterpret_cast<const float4*>(src + (size_t)(c < G ? c : 0) * C::kStr);
+#pragma unroll
+              for (int q4 = 0; q4 < C::kG4; ++q4)
+                v[h][q4] = c < G ? __ldcg(s4 + q4) : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+            }
+#pragma unroll
+            for (int h = 0; h < C::kRounds; ++h) {
+#pragma unroll
+              for (int q4 = 0; q4 < C::kG4; ++q4) {
+                acc[4 * q4] += v[h][q4].x;
+                acc[4 * q4 + 1] += v[h][q4].y;
+                acc[4 * q4 + 2] += v[h][q4].z;
+                acc[4 * q4 + 3] += v[h][q4].w;
+              }
             }
           }
 #pragma unroll
-          for (int off = C::kG4Pad; off < 32; off <<= 1) {
-            s4.x += __shfl_xor_sync(0xffffffffu, s4.x, off);
-            s4.y += __shfl_xor_sync(0xffffffffu, s4.y, off);
-            s4.z += __shfl_xor_sync(0xffffffffu, s4.z, off);
-            s4.w += __shfl_xor_sync(0xffffffffu, s4.w, off);
-          }
-          float mix[RR];
+          for (int off = 16; off > 0; off >>= 1) {
 #pragma unroll
-          for (int r = 0; r < RR; ++r) mix[r] = __shfl_sync(0xffffffffu, f4_get(s4, r & 3), r >> 2);
-          const float ssq = __shfl_sync(0xffffffffu, f4_get(s4, RR & 3), RR >> 2);
+            for (int e = 0; e <= RR; ++e) acc[e] += __shfl_xor_sync(0xffffffffu, acc[e], off);
+          }
           if (lane == 0) {
+            float mix[RR];
+#pragma unroll
+            for (int e = 0; e < RR; ++e) mix[e] = acc[e];
             const int tok = tile0 + t;
             float cf[NS];
-            const float inv_rms = token_gates<NS, RR>(ep, tok, mix, ssq, true, cf);
-            float* cdst = coefs + ((size_t)gs * kGwTile + t) * NS;
+            const float inv_rms = token_gates<NS, RR>(ep, tok, mix, acc[RR], true, cf);
+            float* cdst = gcoef + ((size_t)slot * kGwTile + t) * NS;
 #pragma unroll
             for (int i = 0; i < NS; ++i) __stcg(cdst + i, cf[i]);
-            __threadfence();
-            red_release_gpu(&ready[gs], 1u);
+            red_release_gpu(&ready[slot], 1u);
             float H[NN];
             residual_logits<NS, RR>(ep, mix, inv_rms, H);
-            float* e = sink_buf + ((size_t)sb * g.own_max + cnt) * NN;
+            float* eb = sink_buf + ((size_t)sb * kGwSinkMax + e0 + cnt) * NN;
 #pragma unroll
-            for (int r = 0; r < NN; ++r) e[r] = H[r];
+            for (int i = 0; i < NN; ++i) eb[i] = H[i];
           }
         }
       }
       __syncwarp();
       if (lane == 0) {
-        sink_cnt[sb] = cnt;
+        sink_cnt[sb * kGwSinkMax + (m - q * SB)] = cnt;
         mbar_arrive(&tail->sink_full[sb]);
+        if (m == my_tiles - 1) {             // a short last batch: complete its phase
+          for (int extra = m - q * SB + 1; extra < SB; ++extra) mbar_arrive(&tail->sink_full[sb]);
+        }
       }
     }
   } else if (warp == kGwWarpSink) {
-    // ================================================= Sinkhorn for comb (off y's path)
-    for (int k = 0; k < g.num_tiles; ++k) {
-      const int sb = k & 1;
-      bool ok = true;
-      if (lane == 0) ok = gw_wait(&tail->sink_full[sb], (uint32_t)(k >> 1) & 1u, ctl);
-      if (!__shfl_sync(0xffffffffu, ok ? 1 : 0, 0)) break;
-      const int cnt = sink_cnt[sb];
-      const int tile0 = k * kGwTile;
-      const int first = (int)(((long long)b - (long long)tile0 % G + G) % G);
-      for (int o = lane; o < cnt; o += 32) {
-        const float* e = sink_buf + ((size_t)sb * g.own_max + o) * NN;
-        token_sinkhorn<NS, C::kThree>(ep, tile0 + first + o * G, e, true);
+    // ================================================= Sinkhorn for comb, a batch of tiles at once
+    const int batches = (my_tiles + SB - 1) / SB;
+    for (int q = 0; q < batches; ++q) {
+      const int sb = q & 1;
+      if (!warp_wait(&tail->sink_full[sb], (uint32_t)(q >> 1) & 1u, ctl)) break;
+      const int mt = lane / g.own_max, o = lane - mt * g.own_max;   // lane -> (tile of batch, token)
+      const int m = q * SB + mt;
+      if (mt < SB && m < my_tiles && o < sink_cnt[sb * kGwSinkMax + mt]) {
+        const int k = grp + m * g.ng;
+        const int t = first_owned(m, r, G) + o * G;
+        token_sinkhorn<NS, C::kThree>(ep, k * kGwTile + t,
+                                      sink_buf + ((size_t)sb * kGwSinkMax + mt * g.own_max + o) * NN, true);
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(&tail->sink_free[sb]);
     }
-  } else if (warp >= kGwWarpY0) {
+  } else if (warp == kGwWarpY0) {
+    // ================================================= y weights of each tile
+    // Waits until every token of the tile is gated, copies the weights into
+    // one of two shared buffers for the y warps and counts this CTA done with
+    // the slot.  A thread without loads of its own in flight does the
+    // acquiring poll, so the poll costs one round trip.
+    for (int m = 0; m < my_tiles; ++m) {
+      const int k = grp + m * g.ng;
+      const int valid = min(kGwTile, g.T - k * kGwTile);
+      const int slot = m % kGwSlots;
+      const uint32_t use = (uint32_t)(m / kGwSlots);
+      const int b = m & 1;
+      if (m >= 2 && !warp_wait(&tail->ycoef_free[b], ((uint32_t)(m >> 1) - 1u) & 1u, ctl)) break;
+      bool ok = true;
+      if (lane == 0) ok = gw_wait_count(&ready[slot], use * (uint32_t)kGwTile + (uint32_t)valid, ctl);
+      if (!__shfl_sync(0xffffffffu, ok ? 1 : 0, 0)) break;
+      const float* csrc = gcoef + (size_t)slot * kGwTile * NS;
+      float* cdst = ycoef + (size_t)b * kGwTile * NS;
+      for (int e = lane; e < valid * NS; e += 32) cdst[e] = __ldcg(csrc + e);
+      __syncwarp();
+      if (lane == 0) {
+        mbar_arrive(&tail->ycoef_full[b]);
+        atomicAdd(&ydone[slot], 1u);            // the slot's weights are no longer needed here
+      }
+    }
+  } else if (warp >= kGwWarpYc0) {
     // ================================================= y for this CTA's d-range
-    const int yt = threadIdx.x - kGwWarpY0 * 32;
+    const int yt = threadIdx.x - kGwWarpYc0 * 32;
     const int nvec = g.D >> 3;                      // 16-byte vectors per row
-    const int v0 = (int)((long long)b * nvec / G);
-    const int nv = (int)((long long)(b + 1) * nvec / G) - v0;
+    const int v0 = (int)((long long)r * nvec / G);
+    const int nv = (int)((long long)(r + 1) * nvec / G) - v0;
+    const int nvd = nv > 0 ? nv : 1;
     const uint64_t read_policy = policy_evict_first();
-    for (int k = 0; k < g.num_tiles; ++k) {
-      const int gs = k % kGwSlots;
-      const uint32_t use = (uint32_t)(k / kGwSlots);
+    for (int m = 0; m < my_tiles; ++m) {
+      const int k = grp + m * g.ng;
       const int tile0 = k * kGwTile;
       const int valid = min(kGwTile, g.T - tile0);
-      bool ok = true;
-      if (yt == 0) ok = gw_wait_count(&ready[gs], use * (uint32_t)kGwTile + (uint32_t)valid, ctl);
-      if (!role_all<kGwBarY, kGwYThreads>(ok)) break;
-      const float* csrc = coefs + (size_t)gs * kGwTile * NS;
-      for (int e = yt; e < valid * NS; e += kGwYThreads) ycoef[e] = __ldcg(csrc + e);
-      role_sync<kGwBarY, kGwYThreads>();
-      if (yt == 0) atomicAdd(&ydone[gs], 1u);       // this CTA is done reading slot gs
       const int items = valid * nv;
+      const int b = m & 1;
+      const float* w = ycoef + (size_t)b * kGwTile * NS;
       const __nv_bfloat16* xt = xg + (size_t)tile0 * NS * g.D;
       __nv_bfloat16* yo = ep.y + (size_t)tile0 * g.D;
-      for (int base = yt; base < items; base += kGwYThreads * C::kYB) {
-        uint4 xv[C::kYB][NS];
-        int rowv[C::kYB], dv[C::kYB];
+      // The first batch of x loads goes out before the weights are known.
+      uint4 xv[C::kYB][NS];
+      int rowv[C::kYB], dv[C::kYB];
+      auto load_batch = [&](int base) {
 #pragma unroll
         for (int q = 0; q < C::kYB; ++q) {
-          const int it = base + q * kGwYThreads;
-          const int row = it / max(nv, 1);
+          const int it = base + q * kGwYcThreads;
+          const int row = it / nvd;
           rowv[q] = it < items ? row : -1;
-          dv[q] = (v0 + (it - row * nv)) * 8;
+          dv[q] = (v0 + (it - row * nvd)) * 8;
           if (it < items) {
             const __nv_bfloat16* src = xt + (size_t)row * NS * g.D + dv[q];
 #pragma unroll
             for (int i = 0; i < NS; ++i) xv[q][i] = ld_global_v4_hint(src + (size_t)i * g.D, read_policy);
           }
         }
+      };
+      auto apply_batch = [&]() {
 #pragma unroll
         for (int q = 0; q < C::kYB; ++q) {
           if (rowv[q] < 0) continue;
@@ -471,13 +614,13 @@ __global__ void __launch_bounds__(kGwThreads, 1)
           for (int e = 0; e < 8; ++e) acc8[e] = 0.0f;
 #pragma unroll
           for (int i = 0; i < NS; ++i) {
-            const float m = ycoef[rowv[q] * NS + i];
+            const float wi = w[rowv[q] * NS + i];
             const __nv_bfloat162* hh = reinterpret_cast<const __nv_bfloat162*>(&xv[q][i]);
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
               const float2 f = __bfloat1622float2(hh[e]);
-              acc8[2 * e] = fmaf(m, f.x, acc8[2 * e]);
-              acc8[2 * e + 1] = fmaf(m, f.y, acc8[2 * e + 1]);
+              acc8[2 * e] = fmaf(wi, f.x, acc8[2 * e]);
+              acc8[2 * e + 1] = fmaf(wi, f.y, acc8[2 * e + 1]);
             }
           }
           uint4 o;
@@ -486,8 +629,28 @@ __global__ void __launch_bounds__(kGwThreads, 1)
           for (int e = 0; e < 4; ++e) ob[e] = __floats2bfloat162_rn(acc8[2 * e], acc8[2 * e + 1]);
           st_global_v4_hint(yo + (size_t)rowv[q] * g.D + dv[q], o, read_policy);
         }
+      };
+      load_batch(yt);
+      if (m + 1 < my_tiles) {
+        // bring the next tile's rows into L2 while this one waits for its weights
+        const int k1 = k + g.ng;
+        const int valid1 = min(kGwTile, g.T - k1 * kGwTile);
+        const __nv_bfloat16* x1 = xg + (size_t)k1 * kGwTile * NS * g.D + (size_t)v0 * 8;
+        for (int e = yt; e < valid1 * NS; e += kGwYcThreads)
+          for (int v = 0; v < nv; v += 8)
+            asm volatile("prefetch.global.L2::evict_last [%0];" ::"l"(x1 + (size_t)e * g.D + v * 8));
       }
-      role_sync<kGwBarY, kGwYThreads>();             // ycoef is rewritten for the next tile
+      if (!warp_wait(&tail->ycoef_full[b], (uint32_t)(m >> 1) & 1u, ctl)) break;
+      apply_batch();
+      for (int base = yt + kGwYcThreads * C::kYB; base < items; base += kGwYcThreads * C::kYB) {
+        load_batch(base);
+        apply_batch();
+      }
+      __syncwarp();
+      if (lane == 0) {
+        mbar_arrive(&tail->ycoef_free[b]);
+        mbar_arrive(&tail->y_done[m & 15]);
+      }
     }
   }
 
@@ -543,7 +706,7 @@ cudaError_t launch_gw_forward(const GwLaunch& L, cudaStream_t s) {
   attr[0].id = cudaLaunchAttributeCooperative;
   attr[0].val.cooperative = 1;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(L.grid, 1, 1);
+  cfg.gridDim = dim3(L.g.ng * L.g.G, 1, 1);
   cfg.blockDim = dim3(kGwThreads, 1, 1);
   cfg.dynamicSmemBytes = L.smem_bytes;
   cfg.stream = s;

@@ -91,9 +91,9 @@ def test_workspace_size(lib):
     assert st == 0 and n0 == 0
     st, n1 = mp.mhc_pre_workspace_size(h, 64)
     # header + stacked planes (NP = 3*24 rounded to 80 rows of n*D bf16) +
-    # the grid-wide exchange rings: 4 slots x 128 tokens x 160 CTAs x 28
-    # floats of partials and 4 x 128 x n floats of y weights
-    rings = 4 * 128 * 160 * 28 * 4 + 4 * 128 * 4 * 4
+    # the grid-wide exchange rings: 8 slots x 64 tokens x 160 CTAs x 28
+    # floats of partials and 2 groups x 8 x 64 x n floats of y weights
+    rings = 8 * 64 * 160 * 28 * 4 + 2 * 8 * 64 * 4 * 4
     assert st == 0 and n1 == 256 + 80 * 4 * 256 * 2 + rings
     st, _ = mp.mhc_pre_workspace_size(h, -1)
     assert st == mp.MHC_ERR_PARAM_INVALID
