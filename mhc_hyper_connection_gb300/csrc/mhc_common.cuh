@@ -265,7 +265,7 @@ __host__ __device__ inline SmemLayout smem_layout(int n, int R, int P, int xs, i
   size_t o = 0;
   L.x = o;    o += (size_t)xs * stream_group(n) * kStreamTile;
   L.w = o;    o += (size_t)ws * w_group(n, R, P) * plane_box_rows(R, P) * 128;
-  o += 8192;  // operand reads that run past the last w slot stay inside the window
+  o += 1024;  // the B operand of N = NP rows reads up to 8 rows past the last w box
   L.part = o; o += (size_t)kTileT * partial_stride(R) * 4;
   L.coef = o; o += (size_t)kCoefBufs * kTileT * n * 4;
   L.sink = o; o += 2 * (size_t)kTileT * sink_stride(n) * 4;
