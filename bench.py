@@ -153,7 +153,8 @@ def hbm_peak():
         return 6800.0, "fallback"
 
 
-KERNEL_SOURCES = {"mhc_pre_tc_kernel": "mhc_pre_tc.cu", "mhc_pre_gw_kernel": "mhc_pre_gw.cu"}
+KERNEL_SOURCES = {"mhc_pre_tc_kernel": "mhc_pre_tc.cu", "mhc_pre_gw_kernel": "mhc_pre_gw.cu",
+                  "mhc_pre_t128_kernel": "mhc_pre_t128.cu"}
 
 
 def kernel_hash(kernel):
@@ -259,7 +260,8 @@ def main():
         print(json.dumps(line))
         return 0
 
-    from mhc_hyper_connection_gb300 import MhcPre, mhc_pre_last_launch, mhc_pre_set_profile_events
+    from mhc_hyper_connection_gb300 import (MhcPre, mhc_pre_last_kernel, mhc_pre_last_launch,
+                                            mhc_pre_set_profile_events)
     from mhc_hyper_connection_gb300 import build as mbuild
     mbuild.build()
     case = make_case("prefill", device=device, T=T, impl_mode=args.mode, seed=rank)
@@ -308,6 +310,7 @@ def main():
     if op.status(out) != 0:
         raise RuntimeError("device-side error during the timed steps")
     cfg["launch"] = mhc_pre_last_launch(op.handle)[1]
+    cfg["launch"]["kernel"] = mhc_pre_last_kernel(op.handle)
     elapsed = e0.elapsed_time(e1) / 1e3
     kern = sum(a.elapsed_time(b) for a, b in ev_k) / K / 1e3
     elapsed_max = max_over_ranks(elapsed, world, device)
@@ -369,7 +372,7 @@ def main():
     peak, peak_src = hbm_peak()
     lb = launch_bytes(T, n, D)
     achieved = lb / kern / 1e9
-    kernel = "mhc_pre_gw_kernel" if cfg["launch"]["cluster"] == 0 else "mhc_pre_tc_kernel"
+    kernel = cfg["launch"]["kernel"]
     roof = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
             "frac": achieved / peak, "traffic": recorded_traffic(kernel, T),
             "kernel": kernel, "kernel_ms": kern * 1e3,

@@ -138,10 +138,17 @@ MHC_API mhc_status_t mhc_pre_status(mhc_pre_t h, const void *workspace, void *st
 MHC_API mhc_status_t mhc_pre_set_profile_events(mhc_pre_t h, void *before, void *after);
 
 /* Launch shape chosen by the last successful mhc_pre_run on this handle:
- * CTAs per cluster, grid size in CTAs, projection-ring and y-ring depths.
+ * CTAs per cluster (0 for the grid-wide kernel), grid size in CTAs, x-ring
+ * depth, and phi-ring depth (cluster kernels) or group count (grid-wide).
  * All zero before the first run.  Any output pointer may be NULL. */
 MHC_API mhc_status_t mhc_pre_last_launch(mhc_pre_t h, int32_t *cluster, int32_t *grid,
                                          int32_t *stages, int32_t *ystages);
+
+/* Name of the fused kernel the last successful mhc_pre_run on this handle
+ * launched ("" before the first run, or for a NULL handle).  The string is
+ * static and owned by the library.  A diagnostic for benchmarks and tests;
+ * the pages have no counterpart. */
+MHC_API const char *mhc_pre_last_kernel(mhc_pre_t h);
 
 /* Same forward as mhc_pre_run, for callers that cannot allocate device memory
  * at all -- for instance code running under an allocator lock, a host

@@ -77,6 +77,8 @@ def library() -> ctypes.CDLL:
             I32P = ctypes.POINTER(ctypes.c_int32)
             lib.mhc_pre_last_launch.argtypes = [_P, I32P, I32P, I32P, I32P]
             lib.mhc_pre_last_launch.restype = ctypes.c_int32
+            lib.mhc_pre_last_kernel.argtypes = [_P]
+            lib.mhc_pre_last_kernel.restype = ctypes.c_char_p
             lib.mhc_pre_destroy.argtypes = [_P]
             lib.mhc_pre_destroy.restype = None
             lib.mhc_pre_status_string.argtypes = [ctypes.c_int32]
@@ -130,6 +132,11 @@ def mhc_pre_last_launch(handle):
     v = [ctypes.c_int32(0) for _ in range(4)]
     st = library().mhc_pre_last_launch(handle, *[ctypes.byref(x) for x in v])
     return st, dict(zip(("cluster", "grid", "stages", "ystages"), (x.value for x in v)))
+
+
+def mhc_pre_last_kernel(handle) -> str:
+    """Name of the fused kernel the last run on this handle launched."""
+    return library().mhc_pre_last_kernel(handle).decode()
 
 
 def mhc_pre_destroy(handle) -> None:

@@ -212,11 +212,18 @@ __device__ __forceinline__ void token_sinkhorn(const EpiParams& p, int t, const 
 // Host-side launch descriptions shared by the API translation unit and the
 // kernel translation units.
 // ---------------------------------------------------------------------------
+// The phi planes are stored as the shared-memory image the MMA reads: for
+// each 64-wide d-chunk j and stream i a block of RB = P*R (rounded up to 8)
+// rows of 128 bytes (row p*R + r = plane p of phi row r; rows past P*R and
+// columns past D are zero), with the 128-byte swizzle already applied (the
+// 16-byte piece c of row r sits at c ^ (r & 7)).  Blocks are ordered
+// [chunk][stream], so the blocks of consecutive streams of one chunk are one
+// contiguous run that a single bulk copy brings in.
 struct PlaneParams {
-  const float* phi;        // [R, K]
-  const float* gamma;      // [K] or null
-  __nv_bfloat16* planes;   // [NP, K]
-  int R, K, NP, P;         // P = 3 (fp32) or 2 (tf32)
+  const float* phi;        // [R, n*D]
+  const float* gamma;      // [n*D] or null
+  __nv_bfloat16* planes;   // [nch][n][RB][64], swizzled
+  int R, P, n, D, nch, RB; // P = 3 (fp32) or 2 (tf32)
   int tf32;
   uint32_t* err_word;      // workspace header: all kHdrWords words are zeroed
 };
@@ -285,7 +292,7 @@ struct TcLaunch {
   EpiParams epi;
   const void* x;           // bf16 [T, n, D] (re-read for y)
   CUtensorMap tmap_x;      // x as (D, T, n): box (64, 64 tokens, stream group), 128B swizzle
-  CUtensorMap tmap_w;      // planes as (D, NP, n): box (64, plane rows, n), 128B swizzle
+  const __nv_bfloat16* planes;   // swizzled plane blocks (see PlaneParams)
   int NP, P;
   int cluster;             // CTAs per token tile (split over d-chunks)
   int grid;                // CTAs (multiple of cluster)
@@ -293,6 +300,29 @@ struct TcLaunch {
   size_t smem_bytes;
   uint32_t* err_word;
 };
+
+// ---------------------------------------------------------------------------
+// 128-token-tile cluster kernel (n = 4): x boxes (64 columns, 128 tokens, 2
+// streams) = 32 KB, the sum of squares on CUDA cores.
+// ---------------------------------------------------------------------------
+constexpr int kT128Tile = 128;
+__host__ __device__ inline SmemLayout t128_layout(int R, int P, int xs, int ws) {
+  SmemLayout L;
+  size_t o = 0;
+  L.x = o;    o += (size_t)xs * 2 * kT128Tile * 128;
+  L.w = o;    o += (size_t)ws * w_group(4, R, P) * plane_box_rows(R, P) * 128;
+  o += 1024;  // the B operand of N = NP rows reads up to 8 rows past the last w box
+  L.part = o; o += 2 * (size_t)kT128Tile * partial_stride(R) * 4;   // received partials + owned sums
+  L.coef = o; o += (size_t)kCoefBufs * kT128Tile * 4 * 4;
+  L.sink = o;
+  o = (o + 15) & ~size_t(15);
+  L.tail = o; o += kTailBytes;
+  L.total = o + 1024;
+  return L;
+}
+bool t128_supported(int n, int R, int P);
+cudaError_t t128_forward_occupancy(int n, int R, int P, size_t smem_bytes, int cluster, int* max_clusters);
+cudaError_t launch_t128_forward(const TcLaunch& L, cudaStream_t s);
 
 // Resolved by the kernel translation unit for the given (n, R, P).
 cudaError_t launch_tc_forward(const TcLaunch& L, cudaStream_t s);
@@ -319,14 +349,15 @@ __host__ __device__ constexpr int gw_np(int R, int P) { return ((P * R + 15) / 1
 struct GwLayout {
   size_t phi, x, ycoef, sink, scnt, tail, total;
 };
-// Shared memory of the grid-wide kernel: the CTA's resident phi-plane blocks,
+// Shared memory of the grid-wide kernel: the CTA's resident phi-plane blocks
+// (RB rows each, back to back, plus 1 KB that the N = NP operand reads run into),
 // the x ring (xs slots of umax units, plus one unit of slack that the M = 128
 // operand reads run into), the y weights of two tiles, two Sinkhorn batches
 // and the barrier block.
 __host__ __device__ inline GwLayout gw_layout(int n, int R, int P, int umax, int xs) {
   GwLayout L;
   size_t o = 0;
-  L.phi = o;   o += (size_t)umax * gw_np(R, P) * 128;
+  L.phi = o;   o += (size_t)umax * plane_box_rows(R, P) * 128 + 1024;   // + the N = NP over-read
   L.x = o;     o += ((size_t)xs * umax + 1) * kGwUnitBytes;
   L.ycoef = o; o += 2 * (size_t)kGwTile * n * 4;
   L.sink = o;  o += 2 * (size_t)kGwSinkMax * n * n * 4;
@@ -363,8 +394,7 @@ struct GwLaunch {
   const void* x;           // bf16 [T, n, D] (re-read for y)
   CUtensorMap tmap_x;      // x as (64, T, chunks, n), box (64, 64 tokens, umax, 1), or as
                            // (D, T, n), box (64, 64, 1) when D % 64 != 0; 128B swizzle
-  CUtensorMap tmap_p;      // planes as (64, NP, chunks, n), box (64, NP, umax, 1), or as
-                           // (D, NP, n), box (64, NP, 1); 128B swizzle
+  const __nv_bfloat16* planes;   // swizzled plane blocks (see PlaneParams)
   int P;
   GwGeom g;
   size_t smem_bytes;

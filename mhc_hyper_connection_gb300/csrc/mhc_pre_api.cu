@@ -21,6 +21,7 @@ struct mhc_pre_s {
   int NP;       // MMA N = P*R rounded up to 16
   cudaEvent_t ev_before = nullptr, ev_after = nullptr;   // optional timing hooks
   int last_cluster = 0, last_grid = 0, last_stages = 0, last_ystages = 0;   // last launch shape
+  const char* last_kernel = "";                                              // and its kernel
 };
 
 namespace {
@@ -113,9 +114,11 @@ DeviceInfo device_info(int dev) {
 
 bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
+// Swizzled plane blocks: [chunk][stream][RB rows][128 bytes].
 size_t planes_bytes(const mhc_pre_s* h) {
-  const size_t K = (size_t)(h->cfg.n * h->cfg.D);
-  return ((size_t)h->NP * K * 2 + 255) & ~size_t(255);
+  const size_t nch = (size_t)((h->cfg.D + mhc::kChunkK - 1) / mhc::kChunkK);
+  const size_t RB = (size_t)mhc::plane_box_rows(h->R, h->P);
+  return (nch * (size_t)h->cfg.n * RB * 128 + 255) & ~size_t(255);
 }
 
 // Exchange rings of the grid-wide forward, sized for its largest grid so the
@@ -222,32 +225,28 @@ mhc_status_t run_grid_wide(mhc_pre_s* h, const mhc_pre_args* a, const DeviceInfo
   L.hdr = reinterpret_cast<uint32_t*>(ws);
   L.partials = reinterpret_cast<float*>(ws + mhc::kWsHeader + planes_bytes(h));
   L.coefs = L.partials + (size_t)mhc::kGwSlots * mhc::kGwTile * (ng * G) * mhc::partial_stride(R);
+  L.planes = planes;
   {
     const uint64_t K2 = (uint64_t)n * D * 2;
     bool enc;
     if (box4d) {
       // x [T][n][D] seen as (64, T, chunk, n), box (64, 64 tokens, umax chunks, 1
-      // stream); the phi planes [NP][n][D] as (64, NP, chunk, n), box (64, NP,
-      // umax, 1).  Shared memory then holds one 64-row block per chunk.
+      // stream): shared memory then holds one 64-row block per chunk.
       const uint64_t xd[4] = {(uint64_t)mhc::kChunkK, (uint64_t)a->T, (uint64_t)nch, (uint64_t)n};
       const uint64_t xst[3] = {K2, (uint64_t)mhc::kChunkK * 2, (uint64_t)D * 2};
       const uint32_t xb[4] = {(uint32_t)mhc::kChunkK, (uint32_t)mhc::kGwTile, (uint32_t)umax, 1u};
-      const uint64_t pd[4] = {(uint64_t)mhc::kChunkK, (uint64_t)NP, (uint64_t)nch, (uint64_t)n};
-      const uint32_t pb[4] = {(uint32_t)mhc::kChunkK, (uint32_t)NP, (uint32_t)umax, 1u};
-      enc = encode_4d(&L.tmap_x, a->x, xd, xst, xb) && encode_4d(&L.tmap_p, planes, pd, xst, pb);
+      enc = encode_4d(&L.tmap_x, a->x, xd, xst, xb);
     } else {
-      // x as (D, T, n), box (64, 64 tokens, 1 stream), one box per chunk; the
-      // planes as (D, NP, n), box (64, NP, 1).
+      // x as (D, T, n), box (64, 64 tokens, 1 stream), one box per chunk.
       const uint64_t xd[3] = {(uint64_t)D, (uint64_t)a->T, (uint64_t)n};
       const uint64_t st[2] = {K2, (uint64_t)D * 2};
       const uint32_t xb[3] = {(uint32_t)mhc::kChunkK, (uint32_t)mhc::kGwTile, 1u};
-      const uint64_t pd[3] = {(uint64_t)D, (uint64_t)NP, (uint64_t)n};
-      const uint32_t pb[3] = {(uint32_t)mhc::kChunkK, (uint32_t)NP, 1u};
-      enc = encode_3d(&L.tmap_x, a->x, xd, st, xb) && encode_3d(&L.tmap_p, planes, pd, st, pb);
+      enc = encode_3d(&L.tmap_x, a->x, xd, st, xb);
     }
     if (!enc) return fail(MHC_ERR_RUNTIME, "tensor map encoding failed");
   }
   h->last_cluster = 0;
+  h->last_kernel = "mhc_pre_gw_kernel";
   h->last_grid = ng * G;
   h->last_stages = xs;
   h->last_ystages = ng;
@@ -371,9 +370,11 @@ mhc_status_t mhc_pre_run(mhc_pre_t h, const mhc_pre_args* a, void* stream) {
   pp.gamma = a->gamma;
   pp.planes = planes;
   pp.R = R;
-  pp.K = n * D;
-  pp.NP = NP;
   pp.P = h->P;
+  pp.n = n;
+  pp.D = D;
+  pp.nch = (D + mhc::kChunkK - 1) / mhc::kChunkK;
+  pp.RB = mhc::plane_box_rows(R, h->P);
   pp.tf32 = (c.impl_mode == MHC_IMPL_TF32);
   pp.err_word = err;
   if (mhc::launch_prepare_planes(pp, s) != cudaSuccess)
@@ -387,22 +388,29 @@ mhc_status_t mhc_pre_run(mhc_pre_t h, const mhc_pre_args* a, void* stream) {
     if (st != MHC_ERR_NOT_SUITABLE) return st;
     return fail(MHC_ERR_PARAM_INVALID, "the grid-wide forward does not fit this shape");
   }
+  // The 64-token-tile kernel, or the 128-token-tile kernel (n = 4) when
+  // MHC_PRE_TILE=128 selects it.  At prefill the 64-token kernel at cluster 2
+  // measured 0.688 ms against 0.702 ms for the best 128-token configuration.
+  const bool t128 = mhc::t128_supported(n, R, h->P) && env_int("MHC_PRE_TILE", 64) == 128;
+  const int tile_t = t128 ? mhc::kT128Tile : mhc::kTileT;
+  auto layout = [&](int xsn, int wsn) {
+    return t128 ? mhc::t128_layout(R, h->P, xsn, wsn) : mhc::smem_layout(n, R, h->P, xsn, wsn);
+  };
   mhc::TcLaunch L;
   memset(&L, 0, sizeof L);
   L.epi = epi_params(h, a);
   L.NP = NP;
   L.P = h->P;
   L.err_word = err;
+  L.planes = planes;
   {
-    // x [T][n][D] seen as (D, T, n); the phi planes [NP][n][D] as (D, NP, n).
+    // x [T][n][D] seen as (D, T, n), box (64, tile tokens, stream group); the
+    // plane blocks are read with bulk copies.
     const uint64_t K2 = (uint64_t)n * D * 2;
     const uint64_t xd[3] = {(uint64_t)D, (uint64_t)T, (uint64_t)n};
     const uint64_t xs[2] = {K2, (uint64_t)D * 2};
-    const uint32_t xb[3] = {(uint32_t)mhc::kChunkK, (uint32_t)mhc::kTileT, (uint32_t)mhc::stream_group(n)};
-    const uint64_t wd[3] = {(uint64_t)D, (uint64_t)NP, (uint64_t)n};
-    const uint32_t wb[3] = {(uint32_t)mhc::kChunkK, (uint32_t)mhc::plane_box_rows(R, h->P),
-                            (uint32_t)mhc::w_group(n, R, h->P)};
-    if (!encode_3d(&L.tmap_x, a->x, xd, xs, xb) || !encode_3d(&L.tmap_w, planes, wd, xs, wb))
+    const uint32_t xb[3] = {(uint32_t)mhc::kChunkK, (uint32_t)tile_t, (uint32_t)(t128 ? 2 : mhc::stream_group(n))};
+    if (!encode_3d(&L.tmap_x, a->x, xd, xs, xb))
       return fail(MHC_ERR_RUNTIME, "tensor map encoding failed");
   }
 
@@ -412,7 +420,7 @@ mhc_status_t mhc_pre_run(mhc_pre_t h, const mhc_pre_args* a, void* stream) {
   // the deepest phi ring (up to wmax) that leaves at least three x stages,
   // then the deepest x ring; failing that, the deepest x ring first.
   const int nd = (D + mhc::kChunkK - 1) / mhc::kChunkK;
-  const int num_tiles = (int)((T + mhc::kTileT - 1) / mhc::kTileT);
+  const int num_tiles = (int)((T + tile_t - 1) / tile_t);
   const size_t budget = di.max_smem;
   int xmax = env_int("MHC_PRE_XSTAGES", 6), wmax = env_int("MHC_PRE_WSTAGES", 3);
   xmax = xmax < 2 ? 2 : (xmax > mhc::kMaxStages ? mhc::kMaxStages : xmax);
@@ -420,20 +428,20 @@ mhc_status_t mhc_pre_run(mhc_pre_t h, const mhc_pre_args* a, void* stream) {
   int xst = 0, wst = 0;
   for (int wsn = wmax; wsn >= 2 && !xst; --wsn)
     for (int xsn = xmax; xsn >= 3; --xsn)
-      if (mhc::smem_layout(n, R, h->P, xsn, wsn).total <= budget) {
+      if (layout(xsn, wsn).total <= budget) {
         xst = xsn;
         wst = wsn;
         break;
       }
   for (int xsn = xmax; xsn >= 2 && !xst; --xsn)
     for (int wsn = wmax; wsn >= 2; --wsn)
-      if (mhc::smem_layout(n, R, h->P, xsn, wsn).total <= budget) {
+      if (layout(xsn, wsn).total <= budget) {
         xst = xsn;
         wst = wsn;
         break;
       }
   if (!xst) return fail(MHC_ERR_RUNTIME, "shape does not fit in shared memory");
-  const size_t smem = mhc::smem_layout(n, R, h->P, xst, wst).total;
+  const size_t smem = layout(xst, wst).total;
 
   // Cluster size: the one that keeps the most SMs busy on this many tiles.
   // Ties go to the larger cluster: each member then reduces and gates fewer
@@ -446,7 +454,9 @@ mhc_status_t mhc_pre_run(mhc_pre_t h, const mhc_pre_args* a, void* stream) {
   for (int cand : {1, 2, 4, 8, 16}) {
     if ((forced && cand != forced) || cand > nd) continue;
     int mc = 0;
-    if (mhc::tc_forward_occupancy(n, R, h->P, smem, cand, &mc) != cudaSuccess || mc <= 0) {
+    const cudaError_t oe = t128 ? mhc::t128_forward_occupancy(n, R, h->P, smem, cand, &mc)
+                                : mhc::tc_forward_occupancy(n, R, h->P, smem, cand, &mc);
+    if (oe != cudaSuccess || mc <= 0) {
       cudaGetLastError();
       continue;
     }
@@ -468,9 +478,10 @@ mhc_status_t mhc_pre_run(mhc_pre_t h, const mhc_pre_args* a, void* stream) {
   h->last_grid = L.grid;
   h->last_stages = xst;
   h->last_ystages = wst;
+  h->last_kernel = t128 ? "mhc_pre_t128_kernel" : "mhc_pre_tc_kernel";
   if (h->ev_before && cudaEventRecord(h->ev_before, s) != cudaSuccess)
     return fail(MHC_ERR_RUNTIME, "recording the timing event failed");
-  if (mhc::launch_tc_forward(L, s) != cudaSuccess)
+  if ((t128 ? mhc::launch_t128_forward(L, s) : mhc::launch_tc_forward(L, s)) != cudaSuccess)
     return fail(MHC_ERR_RUNTIME, "forward launch failed: %s", cudaGetErrorString(cudaGetLastError()));
   if (h->ev_after && cudaEventRecord(h->ev_after, s) != cudaSuccess)
     return fail(MHC_ERR_RUNTIME, "recording the timing event failed");
@@ -566,6 +577,8 @@ mhc_status_t mhc_pre_last_launch(mhc_pre_t h, int32_t* cluster, int32_t* grid, i
   if (ystages) *ystages = h->last_ystages;
   return MHC_OK;
 }
+
+const char* mhc_pre_last_kernel(mhc_pre_t h) { return h ? h->last_kernel : ""; }
 
 void mhc_pre_destroy(mhc_pre_t h) { delete h; }
 

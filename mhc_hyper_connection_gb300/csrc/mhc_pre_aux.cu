@@ -17,16 +17,26 @@ __device__ __forceinline__ float bf16_round(float v) { return __bfloat162float(_
 
 __global__ void __launch_bounds__(256) prepare_planes_kernel(PlaneParams pp) {
   if (blockIdx.x == 0 && threadIdx.x < kHdrWords && pp.err_word) pp.err_word[threadIdx.x] = 0u;
-  const long long total = (long long)pp.NP * pp.K;
+  const long long total = (long long)pp.nch * pp.n * pp.RB * 64;
+  const int K = pp.n * pp.D;
   for (long long idx = (long long)blockIdx.x * blockDim.x + threadIdx.x; idx < total;
        idx += (long long)gridDim.x * blockDim.x) {
-    const int row = (int)(idx / pp.K);
-    const int k = (int)(idx - (long long)row * pp.K);
-    const int plane = row / pp.R;
-    const int r = row - plane * pp.R;
+    // Element idx of the swizzled image: block (chunk j, stream i), row r,
+    // stored 16-byte piece e >> 3, which holds the row's logical piece
+    // (e >> 3) ^ (r & 7).
+    const int e = (int)(idx & 63);
+    const long long brow = idx >> 6;
+    const int r = (int)(brow % pp.RB);
+    const long long blk = brow / pp.RB;
+    const int i = (int)(blk % pp.n);
+    const int j = (int)(blk / pp.n);
+    const int d = j * 64 + ((((e >> 3) ^ (r & 7)) << 3) | (e & 7));
+    const int plane = r / pp.R;
+    const int rr = r - plane * pp.R;
     float out = 0.0f;
-    if (plane < pp.P) {
-      float v = __ldg(pp.phi + (size_t)r * pp.K + k);
+    if (plane < pp.P && d < pp.D) {
+      const int k = i * pp.D + d;
+      float v = __ldg(pp.phi + (size_t)rr * K + k);
       if (pp.gamma) v = v * __ldg(pp.gamma + k);
       if (pp.tf32) v = __uint_as_float(__float_as_uint(v) & 0xFFFFE000u);
       const float hi = bf16_round(v);
@@ -43,7 +53,7 @@ __global__ void __launch_bounds__(256) prepare_planes_kernel(PlaneParams pp) {
 }
 
 cudaError_t launch_prepare_planes(const PlaneParams& pp, cudaStream_t s) {
-  const long long total = (long long)pp.NP * pp.K;
+  const long long total = (long long)pp.nch * pp.n * pp.RB * 64;
   int blocks = (int)((total + 255) / 256);
   if (blocks > 4096) blocks = 4096;
   if (blocks < 1) blocks = 1;

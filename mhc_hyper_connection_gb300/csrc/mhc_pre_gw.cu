@@ -60,7 +60,7 @@ struct GwCfg {
   static_assert(kNP <= 256, "N of one MMA is at most 256");
   static constexpr int kAccCols = kNP <= 32 ? 32 : kNP <= 64 ? 64 : kNP <= 128 ? 128 : 256;
   static constexpr uint32_t kTmemCols = 2u * kAccCols;          // two accumulators
-  static constexpr int kPlaneBytes = kNP * 128;                 // one unit's phi-plane block
+  static constexpr int kPlaneBytes = plane_box_rows(RR, P) * 128;   // one chunk's plane block
   static constexpr int kStr = partial_stride(RR);               // floats per partial
   static constexpr int kG4 = kStr / 4;                          // float4 groups per partial
   static constexpr int kRounds = kG4 <= 8 ? 3 : 1;              // rounds of CTAs loaded at once
@@ -168,7 +168,7 @@ __device__ __forceinline__ int first_owned(int m, int r, int G) {
 
 template <int NS, int RR, int P>
 __global__ void __launch_bounds__(kGwThreads, 1)
-    mhc_pre_gw_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constant__ CUtensorMap tmap_p,
+    mhc_pre_gw_kernel(const __grid_constant__ CUtensorMap tmap_x, const __nv_bfloat16* __restrict__ planes,
                       const EpiParams ep, const __nv_bfloat16* __restrict__ xg, const GwGeom g, uint32_t* hdr,
                       float* partials, float* coefs) {
   using C = GwCfg<NS, RR, P>;
@@ -230,7 +230,6 @@ __global__ void __launch_bounds__(kGwThreads, 1)
     tail->abort = 0u;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     tma_prefetch_desc(&tmap_x);
-    tma_prefetch_desc(&tmap_p);
   }
   if (warp == kGwWarpMma) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
@@ -247,20 +246,18 @@ __global__ void __launch_bounds__(kGwThreads, 1)
   if (warp == kGwWarpX) {
     // ================================================= TMA: phi planes once, then x
     // Lane q issues unit q's box, so the CTA's boxes of one tile go out together.
-    // A 4-D box carries all umax chunks at once (its tail past this CTA's
-    // run is the next CTA's data or zero fill, and is not used).
+    // A 4-D x box carries all umax chunks at once (its tail past this CTA's
+    // run is the next CTA's data or zero fill, and is not used).  The plane
+    // blocks of the run come once, one bulk copy per chunk.
     const uint64_t keep = policy_evict_last();
     const int nbox = g.box4d ? 1 : U;
     const uint32_t xbytes = (uint32_t)((g.box4d ? g.umax : U) * kGwUnitBytes);
-    if (lane == 0) mbar_expect_tx(&tail->phi_full, (uint32_t)((g.box4d ? g.umax : U) * C::kPlaneBytes));
+    if (lane == 0) mbar_expect_tx(&tail->phi_full, (uint32_t)(U * C::kPlaneBytes));
     __syncwarp();
-    if (lane < nbox) {
-      if (g.box4d)
-        tma_load_4d_hint(sPhi, &tmap_p, &tail->phi_full, 0, 0, j0, stream, keep);
-      else
-        tma_load_3d_hint(sPhi + (size_t)lane * C::kPlaneBytes, &tmap_p, &tail->phi_full, (j0 + lane) * kChunkK, 0,
-                         stream, keep);
-    }
+    if (lane < U)
+      bulk_load_hint(sPhi + (size_t)lane * C::kPlaneBytes,
+                     planes + ((size_t)(j0 + lane) * NS + stream) * (C::kPlaneBytes / 2), (uint32_t)C::kPlaneBytes,
+                     &tail->phi_full, keep);
     int xs = 0;
     uint32_t xph = 0;
     int issued = 0;
@@ -713,7 +710,8 @@ cudaError_t launch_gw_forward(const GwLaunch& L, cudaStream_t s) {
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   const __nv_bfloat16* xg = static_cast<const __nv_bfloat16*>(L.x);
-  void* args[] = {const_cast<CUtensorMap*>(&L.tmap_x), const_cast<CUtensorMap*>(&L.tmap_p),
+  const __nv_bfloat16* planes = L.planes;
+  void* args[] = {const_cast<CUtensorMap*>(&L.tmap_x), const_cast<__nv_bfloat16**>(&planes),
                   const_cast<EpiParams*>(&L.epi), &xg, const_cast<GwGeom*>(&L.g),
                   const_cast<uint32_t**>(&L.hdr), const_cast<float**>(&L.partials),
                   const_cast<float**>(&L.coefs)};

@@ -77,7 +77,7 @@ constexpr int kBarPub = 1, kBarY = 2;
 
 template <int NS, int RR, int P>
 __global__ void __launch_bounds__(kThreads, 1)
-    mhc_pre_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constant__ CUtensorMap tmap_w,
+    mhc_pre_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const __nv_bfloat16* __restrict__ planes,
                       const EpiParams ep, const __nv_bfloat16* __restrict__ xg, Geometry g, uint32_t* err) {
   using C = Cfg<NS, RR, P>;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -129,7 +129,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     tail->abort = 0u;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     tma_prefetch_desc(&tmap_x);
-    tma_prefetch_desc(&tmap_w);
   }
   if (warp == kWarpMma) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
@@ -182,8 +181,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int wg = 0; wg < C::kWBoxes; ++wg) {
             if (!wait_bar<false>(&tail->w_empty[ws], wph ^ 1u, ctl, kErrWaitTimeout)) { ok = false; break; }
             mbar_expect_tx(&tail->w_full[ws], (uint32_t)C::kWBytes);
-            tma_load_3d_hint(sW + (size_t)ws * C::kWBytes, &tmap_w, &tail->w_full[ws], j * kChunkK, 0,
-                             wg * C::kWG, keep);
+            // the plane blocks of streams wg*kWG .. +kWG of chunk j: one run
+            bulk_load_hint(sW + (size_t)ws * C::kWBytes,
+                           planes + ((size_t)j * NS + (size_t)wg * C::kWG) * C::kWRows * kChunkK,
+                           (uint32_t)C::kWBytes, &tail->w_full[ws], keep);
             ++iss;
             if (++ws == WS) { ws = 0; wph ^= 1u; }
           }
@@ -556,7 +557,8 @@ cudaError_t launch_tc_forward(const TcLaunch& L, cudaStream_t s) {
   cudaLaunchAttribute attr[1];
   cudaLaunchConfig_t cfg = cluster_config(L.cluster, L.grid, L.smem_bytes, s, attr);
   const __nv_bfloat16* xg = static_cast<const __nv_bfloat16*>(L.x);
-  void* args[] = {const_cast<CUtensorMap*>(&L.tmap_x), const_cast<CUtensorMap*>(&L.tmap_w),
+  const __nv_bfloat16* planes = L.planes;
+  void* args[] = {const_cast<CUtensorMap*>(&L.tmap_x), const_cast<__nv_bfloat16**>(&planes),
                   const_cast<EpiParams*>(&L.epi), &xg, &g, const_cast<uint32_t**>(&L.err_word)};
   return cudaLaunchKernelExC(&cfg, k, args);
 }

@@ -122,6 +122,16 @@ __device__ __forceinline__ void tma_load_4d_hint(void* dst, const CUtensorMap* m
       "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "l"(policy)
       : "memory");
 }
+// Linear bulk copy global -> shared (16-byte aligned, size a multiple of 16),
+// completing on `bar` with its byte count.
+__device__ __forceinline__ void bulk_load_hint(void* dst, const void* src, uint32_t bytes, uint64_t* bar,
+                                               uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], %4;" ::"r"(
+          smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(smem_u32(bar)), "l"(policy)
+      : "memory");
+}
 // L2 policies: keep x resident between its first read and its re-read for y,
 // drop it (and the y stream) as soon as the re-read is done.
 __device__ __forceinline__ uint64_t policy_evict_last() {

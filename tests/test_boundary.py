@@ -90,15 +90,15 @@ def test_workspace_size(lib):
     st, n0 = mp.mhc_pre_workspace_size(h, 0)
     assert st == 0 and n0 == 0
     st, n1 = mp.mhc_pre_workspace_size(h, 64)
-    # header + stacked planes (NP = 3*24 rounded to 80 rows of n*D bf16) +
+    # header + swizzled plane blocks (4 chunks x 4 streams x 72 rows of 128 bytes) +
     # the grid-wide exchange rings: 8 slots x 64 tokens x 160 CTAs x 28
     # floats of partials and 2 groups x 8 x 64 x n floats of y weights
     rings = 8 * 64 * 160 * 28 * 4 + 2 * 8 * 64 * 4 * 4
-    assert st == 0 and n1 == 256 + 80 * 4 * 256 * 2 + rings
+    assert st == 0 and n1 == 256 + 4 * 4 * 72 * 128 + rings
     st, _ = mp.mhc_pre_workspace_size(h, -1)
     assert st == mp.MHC_ERR_PARAM_INVALID
     h2 = _handle(impl_mode=1)
-    assert mp.mhc_pre_workspace_size(h2, 64)[1] == 256 + 48 * 4 * 256 * 2 + rings
+    assert mp.mhc_pre_workspace_size(h2, 64)[1] == 256 + 4 * 4 * 48 * 128 + rings
     mp.mhc_pre_destroy(h)
     mp.mhc_pre_destroy(h2)
 

@@ -1,5 +1,6 @@
-"""Both forward kernels against the oracle: the cluster kernel (the default)
-and the grid-wide kernel, each selected with MHC_PRE_PATH."""
+"""Every forward kernel against the oracle: the default 64-token cluster
+kernel, the 128-token cluster kernel (n = 4) selected with MHC_PRE_TILE=128,
+and the grid-wide kernel selected with MHC_PRE_PATH=grid."""
 import pytest
 import torch
 
@@ -16,18 +17,25 @@ def built():
 
 
 def _run(case, path, monkeypatch):
-    from mhc_hyper_connection_gb300 import mhc_pre_last_launch
-    monkeypatch.setenv("MHC_PRE_PATH", path)
+    from mhc_hyper_connection_gb300 import mhc_pre_last_kernel
+    monkeypatch.delenv("MHC_PRE_PATH", raising=False)
+    monkeypatch.delenv("MHC_PRE_TILE", raising=False)
+    if path == "grid":
+        monkeypatch.setenv("MHC_PRE_PATH", "grid")
+        want = "mhc_pre_gw_kernel"
+    elif path == "tile128":   # 128-token tiles exist for n = 4 only
+        monkeypatch.setenv("MHC_PRE_TILE", "128")
+        want = "mhc_pre_t128_kernel" if case.n == 4 else "mhc_pre_tc_kernel"
+    else:
+        want = "mhc_pre_tc_kernel"
     op, out = run_cuda(case)
     torch.cuda.synchronize()
-    st, launch = mhc_pre_last_launch(op.handle)
-    assert st == 0
-    assert (launch["cluster"] == 0) == (path == "grid"), launch
+    assert mhc_pre_last_kernel(op.handle) == want
     compare(case, out, run_oracle(case))
     return out
 
 
-PATHS = ["grid", "cluster"]
+PATHS = ["default", "tile128", "grid"]
 
 
 @pytest.mark.parametrize("path", PATHS)
