@@ -10,6 +10,8 @@ Two independent statements of the same operator live here:
   the pages in a different shape (explicit segment slicing, Sinkhorn as
   diagonal scalings of the softmax), used only on tiny inputs to pin the C
   oracle's loops and indexing.
+
+``run_post`` is the C oracle of the post-mapping (``mhc_post_oracle.c``).
 """
 from __future__ import annotations
 
@@ -24,7 +26,7 @@ from typing import Optional
 import numpy as np
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
-_SRC = os.path.join(_HERE, "mhc_pre_oracle.c")
+_SRCS = [os.path.join(_HERE, "mhc_pre_oracle.c"), os.path.join(_HERE, "mhc_post_oracle.c")]
 _OUT_DIR = os.path.join(_HERE, "_build")
 _SO = os.path.join(_OUT_DIR, "libmhc_oracle.so")
 _lock = threading.Lock()
@@ -34,10 +36,10 @@ _lib = None
 def build(force: bool = False) -> str:
     """Compile the oracle with gcc (portable flags: no -march, no FMA contraction)."""
     os.makedirs(_OUT_DIR, exist_ok=True)
-    if force or not os.path.exists(_SO) or os.path.getmtime(_SO) < os.path.getmtime(_SRC):
+    if force or not os.path.exists(_SO) or any(os.path.getmtime(_SO) < os.path.getmtime(f) for f in _SRCS):
         tmp = _SO + f".tmp{os.getpid()}"
         subprocess.check_call(["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-pthread",
-                               "-ffp-contract=off", "-fno-fast-math", _SRC, "-o", tmp, "-lm"])
+                               "-ffp-contract=off", "-fno-fast-math", *_SRCS, "-o", tmp, "-lm"])
         os.replace(tmp, _SO)
     return _SO
 
@@ -53,6 +55,9 @@ def _load():
                           ctypes.c_int, ctypes.c_double, ctypes.c_double, ctypes.c_int,
                           P, P, P, P, P, P, P, P, P, P, P, P, P, P, ctypes.c_int]
             f.restype = ctypes.c_int
+            g = lib.mhc_oracle_post
+            g.argtypes = [ctypes.c_int64, ctypes.c_int64, ctypes.c_int64, P, P, P, P, P, ctypes.c_int]
+            g.restype = ctypes.c_int
             _lib = lib
     return _lib
 
@@ -108,6 +113,26 @@ def run(x_bits: np.ndarray, phi: np.ndarray, alpha: np.ndarray, bias: np.ndarray
     if rc != 0:
         raise ValueError("oracle rejected its arguments")
     return OracleOut(y, h_post, h_res, h_pre, inv_rms, h_mix, sum_out, norm_out)
+
+
+def run_post(x_bits: np.ndarray, residual_bits: np.ndarray, post: np.ndarray, comb: np.ndarray, *,
+             threads: Optional[int] = None) -> np.ndarray:
+    """Post-mapping oracle: out[t, j, d] = post[t, j] x[t, d] + sum_i comb[t, i, j]
+    residual[t, i, d], in double, unrounded.  x_bits: bf16 bits [T, D];
+    residual_bits: bf16 bits [T, n, D]; post [T, n]; comb [T, n, n]."""
+    residual_bits = np.ascontiguousarray(residual_bits).view(np.uint16)
+    T, n, D = residual_bits.shape
+    x_bits = np.ascontiguousarray(x_bits).view(np.uint16).reshape(T, D)
+    post = np.ascontiguousarray(post, dtype=np.float32).reshape(T, n)
+    comb = np.ascontiguousarray(comb, dtype=np.float32).reshape(T, n, n)
+    out = np.zeros((T, n, D))
+    if threads is None:
+        threads = os.cpu_count() or 1
+    rc = _load().mhc_oracle_post(T, n, D, _ptr(x_bits), _ptr(residual_bits), _ptr(post), _ptr(comb),
+                                 _ptr(out), int(threads))
+    if rc != 0:
+        raise ValueError("post oracle rejected its arguments")
+    return out
 
 
 # ---------------------------------------------------------------------------
