@@ -206,6 +206,117 @@ def oracle_rate(case, budget_s: float, max_tokens: int):
     return done / t_total, threads, f"{passes} pass(es) over {count} tokens", t_total
 
 
+# ----------------------------------------------------------------- post-mapping
+
+POST_METRIC = "tokens/s and achieved HBM GB/s (% of roofline), mHC post (hc_post) n=4 D=7168"
+
+
+def post_token_bytes(n, D):
+    """x + residual read, out written (bf16), post + comb read (fp32)."""
+    return 2 * D + 2 * n * D + 2 * n * D + 4 * n + 4 * n * n
+
+
+def bench_post(args, device, world, rank, local):
+    """hc_post at the prefill shape: device-timed steps, the roofline of its
+    one kernel, and the oracle on host cores for a bounded sample."""
+    import torch
+    from mhc_synth import make_post_case
+    T, n, D = args.tokens, WORKLOAD["n"], WORKLOAD["D"]
+    cfg = {"workload": f"hc_post T={T} n={n} D={D} (b=4, s=8192)", "tokens_per_rank": T, "n": n, "D": D,
+           "l2": "inputs exceed L2; no flush needed", "parallelism": f"token-sharded x{world} (no collective)"}
+    case = make_post_case(device=device, T=T, n=n, D=D, seed=rank)
+    if args.impl == "reference":
+        if rank != 0:
+            return 0
+        rate, threads, sample, dt = post_oracle_rate(case, 60.0 * args.steps / (args.steps + args.warmup))
+        print(json.dumps({"impl": "reference", "metric": POST_METRIC, "value": rate, "unit": "tokens/s",
+                          "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+                          "ms_per_step": 1e3 * T / rate, "higher_is_better": True, "scaling": "weak",
+                          "vs_baseline": None, "dtype": "f64", "data": "synthetic", "config": cfg,
+                          "cpu_baseline": {"value": rate, "unit": "tokens/s", "cores": threads, "kind": "oracle",
+                                           "sample": sample},
+                          "e2e": {"value": rate, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                                  "d2h_bytes_per_step": 0}}))
+        return 0
+    from mhc_hyper_connection_gb300 import build as mbuild, hc_post
+    mbuild.build()
+    stream = torch.cuda.current_stream(device)
+    out = torch.empty((T, n, D), dtype=torch.bfloat16, device=device)
+
+    def step():
+        hc_post(case.x, case.residual, case.post, case.comb, out=out, stream=stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    K = args.steps
+    clocks = ClockSampler(local)
+    clocks.start()
+    time.sleep(0.3)
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    clocks.mark(True)
+    e0.record(stream)
+    for _ in range(K):
+        step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    clocks.mark(False)
+    time.sleep(0.2)
+    clocks.stop()
+    elapsed = max_over_ranks(e0.elapsed_time(e1) / 1e3, world, device)
+    per_step = elapsed / K
+    lb = T * post_token_bytes(n, D)
+    peak, peak_src = hbm_peak()
+    achieved = lb / per_step / 1e9
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        rate, threads, sample, dt = post_oracle_rate(case, 10.0)
+        cpu = {"value": rate, "unit": "tokens/s", "cores": threads, "kind": "oracle", "sample": sample}
+    if rank == 0:
+        print(json.dumps({
+            "metric": POST_METRIC, "value": world * T * K / elapsed, "unit": "tokens/s", "n_gpus": world,
+            "steps": K, "warmup": args.warmup, "ms_per_step": per_step * 1e3, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic", "config": cfg,
+            "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
+                         "traffic": None, "kernel": "mhc_post_kernel", "kernel_ms": per_step * 1e3,
+                         "algorithmic_bytes": lb, "peak_source": f"hbm_gbs of {peak_src}"},
+            "cpu_baseline": cpu, "gpu_launches": K * world, "clocks": clocks.summary()}))
+    if world > 1:
+        torch.distributed.destroy_process_group()
+    return 0
+
+
+def post_oracle_rate(case, budget_s: float):
+    """Tokens/s of the post-mapping oracle on all host cores, over passes of a
+    bounded token sample, until about budget_s has elapsed."""
+    import numpy as np
+    import oracle
+    oracle.build()
+    threads = os.cpu_count() or 1
+    count = max(1, min(case.T, 2048))
+    xb = case.x[:count].contiguous().view(torch_int16()).cpu().numpy().view(np.uint16)
+    rb = case.residual[:count].contiguous().view(torch_int16()).cpu().numpy().view(np.uint16)
+    post = case.post[:count].cpu().numpy()
+    comb = case.comb[:count].cpu().numpy()
+    done, t_total, passes = 0, 0.0, 0
+    while passes == 0 or t_total < budget_s:
+        t0 = time.perf_counter()
+        oracle.run_post(xb, rb, post, comb, threads=threads)
+        t_total += time.perf_counter() - t0
+        done += count
+        passes += 1
+    return done / t_total, threads, f"{passes} pass(es) over {count} tokens of the hc_post workload ({t_total:.1f} s, double precision)", t_total
+
+
+def torch_int16():
+    import torch
+    return torch.int16
+
+
 # ----------------------------------------------------------------- main
 
 def main():
@@ -218,6 +329,8 @@ def main():
     ap.add_argument("--mode", type=int, default=WORKLOAD["impl_mode"], choices=[0, 1])
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--op", choices=["pre", "post"], default="pre",
+                    help="pre: the pre-mapping forward (the headline); post: the post-mapping (hc_post)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
@@ -239,6 +352,9 @@ def main():
            "tokens_per_rank": T, "n": n, "D": D, "num_iters": 20, "impl_mode": mode_name,
            "gamma": None, "l2": "inputs (2.35 GB/step) exceed L2; no flush needed",
            "parallelism": f"token-sharded x{world} (no collective)"}
+
+    if args.op == "post":
+        return bench_post(args, device, world, rank, local)
 
     if args.impl == "reference":
         if rank != 0:

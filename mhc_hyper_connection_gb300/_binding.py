@@ -77,6 +77,8 @@ def library() -> ctypes.CDLL:
             I32P = ctypes.POINTER(ctypes.c_int32)
             lib.mhc_pre_last_launch.argtypes = [_P, I32P, I32P, I32P, I32P]
             lib.mhc_pre_last_launch.restype = ctypes.c_int32
+            lib.mhc_post_run.argtypes = [ctypes.c_int64, ctypes.c_int64, ctypes.c_int64, _P, _P, _P, _P, _P, _P]
+            lib.mhc_post_run.restype = ctypes.c_int32
             lib.mhc_pre_last_kernel.argtypes = [_P]
             lib.mhc_pre_last_kernel.restype = ctypes.c_char_p
             lib.mhc_pre_destroy.argtypes = [_P]
@@ -137,6 +139,32 @@ def mhc_pre_last_launch(handle):
 def mhc_pre_last_kernel(handle) -> str:
     """Name of the fused kernel the last run on this handle launched."""
     return library().mhc_pre_last_kernel(handle).decode()
+
+
+def mhc_post_run(T: int, n: int, D: int, x: int, residual: int, post: int, comb: int, out: int,
+                 stream: int = 0) -> int:
+    """The post-mapping (include/mhc_post.h) on raw device pointers."""
+    return library().mhc_post_run(int(T), int(n), int(D), _P(x or None), _P(residual or None), _P(post or None),
+                                  _P(comb or None), _P(out or None), _P(stream or None))
+
+
+def hc_post(x, residual, post, comb, out=None, stream=None):
+    """out[t, j, d] = post[t, j] x[t, d] + sum_i comb[t, i, j] residual[t, i, d]
+    on torch tensors (x bf16 [T, D], residual bf16 [T, n, D], post fp32 [T, n],
+    comb fp32 [T, n, n]); returns out (bf16 [T, n, D]).  Raises MhcError on a
+    host-side rejection."""
+    import torch
+    T, n, D = residual.shape
+    if out is None:
+        out = torch.empty((T, n, D), dtype=torch.bfloat16, device=residual.device)
+    if stream is None:
+        stream = torch.cuda.current_stream(residual.device).cuda_stream
+    elif hasattr(stream, "cuda_stream"):
+        stream = stream.cuda_stream
+    st = mhc_post_run(T, n, D, _ptr(x), _ptr(residual), _ptr(post), _ptr(comb), _ptr(out), int(stream))
+    if st != MHC_OK:
+        raise MhcError(st, "mhc_post_run", last_error())
+    return out
 
 
 def mhc_pre_destroy(handle) -> None:

@@ -46,7 +46,7 @@ def _sources():
 
 def _deps():
     return _sources() + sorted(glob.glob(os.path.join(CSRC, "*.cuh"))) + \
-        [os.path.join(ROOT, "include", "mhc_pre.h"), os.path.abspath(__file__)]
+        sorted(glob.glob(os.path.join(ROOT, "include", "*.h"))) + [os.path.abspath(__file__)]
 
 
 def up_to_date() -> bool:

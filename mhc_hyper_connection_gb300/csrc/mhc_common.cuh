@@ -324,6 +324,19 @@ bool t128_supported(int n, int R, int P);
 cudaError_t t128_forward_occupancy(int n, int R, int P, size_t smem_bytes, int cluster, int* max_clusters);
 cudaError_t launch_t128_forward(const TcLaunch& L, cudaStream_t s);
 
+// ---------------------------------------------------------------------------
+// Post-mapping (hc_post): out[t][j] = post[t][j] x[t] + sum_i comb[t][i][j] residual[t][i].
+// ---------------------------------------------------------------------------
+struct PostLaunch {
+  int64_t T, n, D;
+  const void* x;           // bf16 [T, D]
+  const void* residual;    // bf16 [T, n, D]
+  const float* post;       // [T, n]
+  const float* comb;       // [T, n, n]
+  void* out;               // bf16 [T, n, D]
+};
+cudaError_t launch_post(const PostLaunch& L, cudaStream_t s);
+
 // Resolved by the kernel translation unit for the given (n, R, P).
 cudaError_t launch_tc_forward(const TcLaunch& L, cudaStream_t s);
 // Clusters of the given size that fit on the device at once (0: unsupported).

@@ -13,6 +13,7 @@
 
 #include "mhc_common.cuh"
 #include "../../include/mhc_pre.h"
+#include "../../include/mhc_post.h"
 
 struct mhc_pre_s {
   mhc_pre_config cfg;
@@ -579,6 +580,32 @@ mhc_status_t mhc_pre_last_launch(mhc_pre_t h, int32_t* cluster, int32_t* grid, i
 }
 
 const char* mhc_pre_last_kernel(mhc_pre_t h) { return h ? h->last_kernel : ""; }
+
+mhc_status_t mhc_post_run(int64_t T, int64_t n, int64_t D, const void* x, const void* residual, const float* post,
+                          const float* comb, void* out, void* stream) {
+  g_last_error[0] = 0;
+  if (T < 0 || T > (int64_t(1) << 30)) return fail(MHC_ERR_PARAM_INVALID, "T must be in [0, 2^30]");
+  if (n < 1 || n > 8) return fail(MHC_ERR_PARAM_INVALID, "n must be in [1, 8] (got %lld)", (long long)n);
+  if (D < 8 || D > (int64_t(1) << 20) || (D % 8) != 0)
+    return fail(MHC_ERR_PARAM_INVALID, "D must be a positive multiple of 8 (got %lld)", (long long)D);
+  if (T == 0) return MHC_OK;
+  if (!x || !residual || !post || !comb || !out) return fail(MHC_ERR_NULLPTR, "x, residual, post, comb, out are required");
+  if (!aligned(x, 16) || !aligned(residual, 16) || !aligned(out, 16))
+    return fail(MHC_ERR_PARAM_INVALID, "x, residual and out must be 16-byte aligned");
+  if (!aligned(post, 4) || !aligned(comb, 4)) return fail(MHC_ERR_PARAM_INVALID, "post and comb must be 4-byte aligned");
+  mhc::PostLaunch L;
+  L.T = T;
+  L.n = n;
+  L.D = D;
+  L.x = x;
+  L.residual = residual;
+  L.post = post;
+  L.comb = comb;
+  L.out = out;
+  if (mhc::launch_post(L, static_cast<cudaStream_t>(stream)) != cudaSuccess)
+    return fail(MHC_ERR_RUNTIME, "post-mapping launch failed: %s", cudaGetErrorString(cudaGetLastError()));
+  return MHC_OK;
+}
 
 void mhc_pre_destroy(mhc_pre_t h) { delete h; }
 

@@ -36,7 +36,7 @@ SPLITMIX_X_LIMIT = 1 << 25   # elements of x drawn on the host with SplitMix64
 
 # One key per tensor so that changing one shape never shifts another stream.
 _TAGS = {"x": 1, "phi": 2, "alpha": 3, "bias": 4, "gamma": 5, "pre_mix": 6,
-         "outlier": 7, "misc": 8}
+         "outlier": 7, "misc": 8, "post": 9, "comb": 10}
 
 
 def _mix64(z: np.ndarray) -> np.ndarray:
@@ -212,3 +212,27 @@ def sample_tokens(T: int, count: int, seed: int = 0, tile: int = 128) -> np.ndar
     picks.update(int(v) for v in rnd)
     out = np.array(sorted(p for p in picks if 0 <= p < T), dtype=np.int64)
     return out
+
+
+@dataclasses.dataclass
+class PostCase:
+    """Inputs of the post-mapping: layer output x bf16 [T, D], residual
+    streams bf16 [T, n, D], post fp32 [T, n] in (0, 2), comb fp32 [T, n, n]
+    with entries in [0, 1/n) (the scale of a doubly stochastic mix)."""
+    T: int
+    n: int
+    D: int
+    x: torch.Tensor
+    residual: torch.Tensor
+    post: torch.Tensor
+    comb: torch.Tensor
+
+
+def make_post_case(*, seed: int = 0, device="cpu", T: int = 64, n: int = 4, D: int = 256) -> PostCase:
+    x = _x_tensor(seed * 7 + 1, T, 1, D, False, device).reshape(T, D)
+    residual = _x_tensor(seed * 7 + 2, T, n, D, False, device)
+    post = torch.from_numpy((2.0 * uniform(stream_key(seed, "post"), T * n)).astype(np.float32)
+                            .reshape(T, n)).to(device)
+    comb = torch.from_numpy((uniform(stream_key(seed, "comb"), T * n * n) / n).astype(np.float32)
+                            .reshape(T, n, n)).to(device)
+    return PostCase(T=T, n=n, D=D, x=x, residual=residual, post=post, comb=comb)

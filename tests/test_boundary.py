@@ -1,6 +1,6 @@
 """The C ABI without a GPU: the library loads, exports every function that
-include/mhc_pre.h declares, and rejects bad arguments on the host, with the
-status codes of the pages, before any CUDA call."""
+include/*.h declares, and rejects bad arguments on the host, with the status
+codes of the pages, before any CUDA call."""
 import ctypes
 import os
 import re
@@ -11,7 +11,7 @@ import mhc_hyper_connection_gb300 as mp
 from mhc_hyper_connection_gb300 import build as mbuild
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
-HEADER = os.path.join(ROOT, "include", "mhc_pre.h")
+HEADERS = [os.path.join(ROOT, "include", h) for h in ("mhc_pre.h", "mhc_post.h")]
 
 
 @pytest.fixture(scope="module")
@@ -21,22 +21,24 @@ def lib():
 
 
 def declared_functions():
-    text = open(HEADER).read()
-    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
-    return sorted(set(re.findall(r"\b(mhc_pre_[a-z_]+)\s*\(", text)))
+    names = set()
+    for header in HEADERS:
+        text = re.sub(r"/\*.*?\*/", "", open(header).read(), flags=re.S)
+        names |= set(re.findall(r"\b(mhc_(?:pre|post)_[a-z_]+)\s*\(", text))
+    return sorted(names)
 
 
 def test_header_declares_the_api():
     names = declared_functions()
     for need in ("mhc_pre_create", "mhc_pre_workspace_size", "mhc_pre_run", "mhc_pre_status",
                  "mhc_pre_destroy", "mhc_pre_config_default", "mhc_pre_status_string",
-                 "mhc_pre_last_error"):
+                 "mhc_pre_last_error", "mhc_post_run"):
         assert need in names
 
 
 def test_library_exports_every_declared_symbol(lib):
     for name in declared_functions():
-        assert hasattr(lib, name), f"{name} declared in mhc_pre.h but not exported"
+        assert hasattr(lib, name), f"{name} declared in include/ but not exported"
 
 
 def test_struct_layouts_match_header():
@@ -177,3 +179,23 @@ def test_binding_raises_when_library_missing(monkeypatch, tmp_path):
     monkeypatch.setattr(_binding, "LIB_PATH", str(tmp_path / "absent.so"))
     with pytest.raises(RuntimeError, match="missing"):
         _binding.library()
+
+
+def test_post_host_validation(lib):
+    A = 1 << 20          # a 16-byte aligned fake device address (never dereferenced)
+    ok = dict(T=4, n=4, D=64, x=A, residual=A, post=A, comb=A, out=A)
+
+    def call(**kw):
+        a = dict(ok, **kw)
+        return mp.mhc_post_run(a["T"], a["n"], a["D"], a["x"], a["residual"], a["post"], a["comb"], a["out"])
+
+    assert call(T=0, x=0, residual=0, post=0, comb=0, out=0) == mp.MHC_OK
+    assert call(n=0) == mp.MHC_ERR_PARAM_INVALID
+    assert call(n=9) == mp.MHC_ERR_PARAM_INVALID
+    assert call(D=12) == mp.MHC_ERR_PARAM_INVALID
+    assert call(D=0) == mp.MHC_ERR_PARAM_INVALID
+    assert call(T=-1) == mp.MHC_ERR_PARAM_INVALID
+    assert call(comb=0) == mp.MHC_ERR_NULLPTR
+    assert call(x=A + 8) == mp.MHC_ERR_PARAM_INVALID
+    assert call(out=A + 2) == mp.MHC_ERR_PARAM_INVALID
+    assert call(post=A + 2) == mp.MHC_ERR_PARAM_INVALID
