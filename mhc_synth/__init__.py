@@ -36,7 +36,7 @@ SPLITMIX_X_LIMIT = 1 << 25   # elements of x drawn on the host with SplitMix64
 
 # One key per tensor so that changing one shape never shifts another stream.
 _TAGS = {"x": 1, "phi": 2, "alpha": 3, "bias": 4, "gamma": 5, "pre_mix": 6,
-         "outlier": 7, "misc": 8, "post": 9, "comb": 10}
+         "outlier": 7, "misc": 8, "post": 9, "comb": 10, "g_post": 11, "g_res": 12}
 
 
 def _mix64(z: np.ndarray) -> np.ndarray:
@@ -236,3 +236,26 @@ def make_post_case(*, seed: int = 0, device="cpu", T: int = 64, n: int = 4, D: i
     comb = torch.from_numpy((uniform(stream_key(seed, "comb"), T * n * n) / n).astype(np.float32)
                             .reshape(T, n, n)).to(device)
     return PostCase(T=T, n=n, D=D, x=x, residual=residual, post=post, comb=comb)
+
+
+@dataclasses.dataclass
+class BwdGrads:
+    """Upstream gradients of the pre-mapping's outputs: grad_h_in bf16 [T, D]
+    (of y), grad_h_post fp32 [T, n], grad_h_res fp32 [T, n, n] (of the
+    Sinkhorn output, or of the res logits), and optionally grad_x_post bf16
+    [T, n, D] (the post-mapping's gradient of x).  All N(0, 1)."""
+    g_in: torch.Tensor
+    g_post: torch.Tensor
+    g_res: torch.Tensor
+    g_x_post: Optional[torch.Tensor]
+
+
+def make_bwd_grads(*, seed: int = 0, device="cpu", T: int = 64, n: int = 4, D: int = 256,
+                   grad_x_post: bool = False) -> BwdGrads:
+    g_in = _x_tensor(seed * 7 + 3, T, 1, D, False, device).reshape(T, D)
+    g_post = torch.from_numpy(normal(stream_key(seed, "g_post"), T * n).astype(np.float32)
+                              .reshape(T, n)).to(device)
+    g_res = torch.from_numpy(normal(stream_key(seed, "g_res"), T * n * n).astype(np.float32)
+                             .reshape(T, n, n)).to(device)
+    gxp = _x_tensor(seed * 7 + 4, T, n, D, False, device) if grad_x_post else None
+    return BwdGrads(g_in=g_in, g_post=g_post, g_res=g_res, g_x_post=gxp)

@@ -11,7 +11,8 @@ Two independent statements of the same operator live here:
   diagonal scalings of the softmax), used only on tiny inputs to pin the C
   oracle's loops and indexing.
 
-``run_post`` is the C oracle of the post-mapping (``mhc_post_oracle.c``).
+``run_post`` is the C oracle of the post-mapping (``mhc_post_oracle.c``);
+``run_backward`` that of the pre-mapping's backward (``mhc_pre_bwd_oracle.c``).
 """
 from __future__ import annotations
 
@@ -26,7 +27,7 @@ from typing import Optional
 import numpy as np
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
-_SRCS = [os.path.join(_HERE, "mhc_pre_oracle.c"), os.path.join(_HERE, "mhc_post_oracle.c")]
+_SRCS = [os.path.join(_HERE, f) for f in ("mhc_pre_oracle.c", "mhc_post_oracle.c", "mhc_pre_bwd_oracle.c")]
 _OUT_DIR = os.path.join(_HERE, "_build")
 _SO = os.path.join(_OUT_DIR, "libmhc_oracle.so")
 _lock = threading.Lock()
@@ -58,6 +59,12 @@ def _load():
             g = lib.mhc_oracle_post
             g.argtypes = [ctypes.c_int64, ctypes.c_int64, ctypes.c_int64, P, P, P, P, P, ctypes.c_int]
             g.restype = ctypes.c_int
+            b = lib.mhc_oracle_pre_backward
+            I64 = ctypes.c_int64
+            b.argtypes = [I64, I64, I64, ctypes.c_int, ctypes.c_double,
+                          P, P, P, P, P, P, P, P, P, P, P, P, P, P,
+                          I64, P, I64, P, P, P, P, P, P, P, P, P, P, P, ctypes.c_int]
+            b.restype = ctypes.c_int
             _lib = lib
     return _lib
 
@@ -133,6 +140,77 @@ def run_post(x_bits: np.ndarray, residual_bits: np.ndarray, post: np.ndarray, co
     if rc != 0:
         raise ValueError("post oracle rejected its arguments")
     return out
+
+
+@dataclasses.dataclass
+class BwdOut:
+    grad_x: Optional[np.ndarray]          # [tokens, n, D] (selected tokens), unrounded
+    grad_x_abs: Optional[np.ndarray]      # sum of |terms| of each grad_x element
+    grad_phi: Optional[np.ndarray]        # [R, columns]
+    grad_phi_abs: Optional[np.ndarray]
+    grad_gamma: Optional[np.ndarray]      # [columns] (with gamma)
+    grad_gamma_abs: Optional[np.ndarray]
+    grad_alpha: np.ndarray                # [3]
+    grad_alpha_abs: np.ndarray
+    grad_bias: np.ndarray                 # [R]
+    grad_bias_abs: np.ndarray
+
+
+def _f64(a, shape=None):
+    if a is None:
+        return None
+    a = np.ascontiguousarray(a, dtype=np.float64)
+    return a if shape is None else a.reshape(shape)
+
+
+def run_backward(x_bits, phi, alpha, gamma, grad_h_in_bits, grad_h_post, grad_h_res,
+                 inv_rms, h_mix, h_pre, h_post, sum_out=None, norm_out=None,
+                 grad_x_post_bits=None, *, num_iters: int = 20, hc_eps: float = 1e-6,
+                 tokens=None, columns=None, want_grad_x: bool = True, want_grad_phi: bool = True,
+                 threads: Optional[int] = None) -> BwdOut:
+    """Backward oracle of the pre-mapping with Sinkhorn (three gates).
+
+    x_bits, grad_x_post_bits: bf16 bits [T, n, D]; grad_h_in_bits: bf16 bits
+    [T, D]; every other array is taken in float64 exactly as given (pass the
+    forward's fp32 intermediates to mirror the device, or double ones for the
+    analytic pins).  With sum_out / norm_out, grad_h_res is the gradient of
+    the Sinkhorn output; without them, of the res logits.  ``tokens`` selects
+    the rows of grad_x, ``columns`` the columns of grad_phi / grad_gamma."""
+    x_bits = np.ascontiguousarray(x_bits).view(np.uint16)
+    T, n, D = x_bits.shape
+    R, K = n * n + 2 * n, n * D
+    gh = np.ascontiguousarray(grad_h_in_bits).view(np.uint16).reshape(T, D)
+    gxp = None if grad_x_post_bits is None else \
+        np.ascontiguousarray(grad_x_post_bits).view(np.uint16).reshape(T, n, D)
+    phi = _f64(phi, (R, K))
+    alpha = _f64(alpha, (3,))
+    gamma = _f64(gamma, (K,))
+    ghp, ghr = _f64(grad_h_post, (T, n)), _f64(grad_h_res, (T, n, n))
+    ir, hm, hp, hq = _f64(inv_rms, (T,)), _f64(h_mix, (T, R)), _f64(h_pre, (T, n)), _f64(h_post, (T, n))
+    so = _f64(sum_out, (2 * num_iters, T, n))
+    no = _f64(norm_out, (2 * num_iters, T, n, n))
+    tok = None if tokens is None else np.ascontiguousarray(tokens, dtype=np.int64)
+    col = None if columns is None else np.ascontiguousarray(columns, dtype=np.int64)
+    nt = T if tok is None else len(tok)
+    nc = K if col is None else len(col)
+    gx = np.zeros((nt, n, D)) if want_grad_x else None
+    gxa = np.zeros((nt, n, D)) if want_grad_x else None
+    gp = np.zeros((R, nc)) if want_grad_phi else None
+    gpa = np.zeros((R, nc)) if want_grad_phi else None
+    gg = np.zeros(nc) if (want_grad_phi and gamma is not None) else None
+    gga = np.zeros(nc) if gg is not None else None
+    ga, gaa = np.zeros(3), np.zeros(3)
+    gb, gba = np.zeros(R), np.zeros(R)
+    if threads is None:
+        threads = os.cpu_count() or 1
+    rc = _load().mhc_oracle_pre_backward(
+        T, n, D, num_iters, hc_eps, _ptr(x_bits), _ptr(phi), _ptr(alpha), _ptr(gamma), _ptr(gh),
+        _ptr(ghp), _ptr(ghr), _ptr(ir), _ptr(hm), _ptr(hp), _ptr(hq), _ptr(so), _ptr(no), _ptr(gxp),
+        nt, _ptr(tok), nc, _ptr(col), _ptr(gx), _ptr(gxa), _ptr(gp), _ptr(gpa), _ptr(gg), _ptr(gga),
+        _ptr(ga), _ptr(gaa), _ptr(gb), _ptr(gba), int(threads))
+    if rc != 0:
+        raise ValueError("backward oracle rejected its arguments" if rc == 1 else "backward oracle: out of memory")
+    return BwdOut(gx, gxa, gp, gpa, gg, gga, ga, gaa, gb, gba)
 
 
 # ---------------------------------------------------------------------------
