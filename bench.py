@@ -154,7 +154,7 @@ def hbm_peak():
 
 
 KERNEL_SOURCES = {"mhc_pre_tc_kernel": "mhc_pre_tc.cu", "mhc_pre_gw_kernel": "mhc_pre_gw.cu",
-                  "mhc_pre_t128_kernel": "mhc_pre_t128.cu"}
+                  "mhc_pre_t128_kernel": "mhc_pre_t128.cu", "bw_main_kernel": "mhc_bwd.cu"}
 
 
 def kernel_hash(kernel):
@@ -312,6 +312,210 @@ def post_oracle_rate(case, budget_s: float):
     return done / t_total, threads, f"{passes} pass(es) over {count} tokens of the hc_post workload ({t_total:.1f} s, double precision)", t_total
 
 
+# ----------------------------------------------------------------- backward
+
+BWD_METRIC = "tokens/s and achieved HBM GB/s (% of roofline), mHC pre backward (Sinkhorn form) n=4 D=7168"
+
+
+def bwd_token_bytes(n, D, iters=20, grad_x_post=False):
+    """Per token: x, grad_h_in, grad_h_post, grad_h_res, invRms, hMix, hPre,
+    hPost, sumOut, normOut read, grad_x written (+ grad_x_post read)."""
+    R = n * n + 2 * n
+    b = 2 * n * D + 2 * D + 4 * n + 4 * n * n + 4 + 4 * R + 4 * n + 4 * n
+    b += 2 * iters * 4 * (n + n * n) + 2 * n * D
+    return b + (2 * n * D if grad_x_post else 0)
+
+
+def bwd_main_token_bytes(n, D):
+    """The contraction kernel's share: x and grad_h_in read, grad_x written."""
+    return 2 * n * D + 2 * D + 2 * n * D
+
+
+def bwd_inputs(device, T, n, D, seed, mode):
+    """Forward inputs, the forward's saved intermediates (made by the library's
+    own forward: these are benchmark inputs, not parity references) and
+    upstream gradients."""
+    import torch
+    from mhc_hyper_connection_gb300 import MhcPre
+    from mhc_synth import make_bwd_grads, make_case
+    case = make_case("prefill", device=device, T=T, impl_mode=mode, seed=seed, need_backward=True)
+    fwd = MhcPre(n, D, alpha_len=3, num_iters=20, impl_mode=mode, need_backward=True)
+    out = fwd.allocate(T, device)
+    fwd.run(case.x, case.phi, case.alpha, case.bias, out)
+    torch.cuda.synchronize()
+    if fwd.status(out) != 0:
+        raise RuntimeError("device-side error in the forward that makes the saved intermediates")
+    saved = {k: out[k] for k in ("inv_rms", "h_mix", "h_pre", "h_post", "sum_out", "norm_out")}
+    g = make_bwd_grads(seed=seed, device=device, T=T, n=n, D=D)
+    return case, saved, g
+
+
+def bwd_oracle_rate(case, saved, g, budget_s: float, max_tokens: int):
+    """Tokens/s of the backward oracle on all host cores over passes of a
+    bounded token sample (all five gradients of that sample)."""
+    import numpy as np
+    import oracle
+    oracle.build()
+    threads = os.cpu_count() or 1
+    count = max(1, min(case.T, max_tokens))
+    bits = lambda t: t[:count].contiguous().view(torch_int16()).cpu().numpy().view(np.uint16)
+    sv = {k: v[:count].cpu().numpy() if k not in ("sum_out", "norm_out") else v[:, :count].contiguous().cpu().numpy()
+          for k, v in saved.items()}
+    args = (bits(case.x), case.phi.cpu().numpy(), case.alpha.cpu().numpy(), None, bits(g.g_in),
+            g.g_post[:count].cpu().numpy(), g.g_res[:count].cpu().numpy(), sv["inv_rms"], sv["h_mix"],
+            sv["h_pre"], sv["h_post"], sv["sum_out"], sv["norm_out"])
+    done, t_total, passes = 0, 0.0, 0
+    while passes == 0 or t_total < budget_s:
+        t0 = time.perf_counter()
+        oracle.run_backward(*args, num_iters=case.num_iters, threads=threads)
+        t_total += time.perf_counter() - t0
+        done += count
+        passes += 1
+    return done / t_total, threads, (f"{passes} pass(es) over {count} tokens of the backward workload "
+                                     f"({t_total:.1f} s, double precision, all five gradients)"), t_total
+
+
+def bench_bwd(args, device, world, rank, local):
+    """The backward at the prefill shape (Sinkhorn form, no gamma): device-timed
+    steps of the four launches, the roofline of the contraction kernel, an
+    end-to-end number with host buffers, and the oracle on host cores."""
+    import torch
+    T, n, D = args.tokens, WORKLOAD["n"], WORKLOAD["D"]
+    mode_name = "fp32" if args.mode == 0 else "tf32"
+    cfg = {"workload": f"pre backward T={T} n={n} D={D} iters=20 {mode_name} Sinkhorn form (b=4, s=8192)",
+           "tokens_per_rank": T, "n": n, "D": D, "num_iters": 20, "impl_mode": mode_name, "gamma": None,
+           "grad_x_post": None, "l2": "inputs (4.3 GB/step) exceed L2; no flush needed",
+           "parallelism": f"token-sharded x{world} (grad_phi/alpha/bias/gamma would need a sum over ranks)"}
+    from mhc_hyper_connection_gb300 import build as mbuild
+    mbuild.build()
+    case, saved, g = bwd_inputs(device, T, n, D, rank, args.mode)
+    if args.impl == "reference":
+        if rank != 0:
+            return 0
+        per_step = 60.0 / (args.steps + args.warmup)
+        probe, _, _, _ = bwd_oracle_rate(case, saved, g, 0.0, 64)
+        tokens = int(max(1, min(T, probe * per_step)))
+        rate, threads, sample, dt = bwd_oracle_rate(case, saved, g, 60.0 * args.steps / (args.steps + args.warmup),
+                                                    tokens)
+        print(json.dumps({"impl": "reference", "metric": BWD_METRIC, "value": rate, "unit": "tokens/s",
+                          "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+                          "ms_per_step": 1e3 * T / rate, "higher_is_better": True, "scaling": "weak",
+                          "vs_baseline": None, "dtype": "f64", "data": "synthetic", "config": cfg,
+                          "cpu_baseline": {"value": rate, "unit": "tokens/s", "cores": threads, "kind": "oracle",
+                                           "sample": sample},
+                          "e2e": {"value": rate, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                                  "d2h_bytes_per_step": 0}}))
+        return 0
+    from mhc_hyper_connection_gb300 import MhcPre, mhc_pre_last_launch, mhc_pre_set_profile_events
+    op = MhcPre(n, D, alpha_len=3, num_iters=20, impl_mode=args.mode, need_backward=True)
+    grads = op.allocate_backward(T, device)
+    stream = torch.cuda.current_stream(device)
+
+    def step(gr=grads):
+        op.backward(case.x, case.phi, case.alpha, None, g.g_in, g.g_post, g.g_res, saved, gr, stream=stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    if op.status(grads) != 0:
+        raise RuntimeError("device-side error during warm-up")
+    K = args.steps
+    ev_k = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+    for a, b in ev_k:
+        a.record(stream)
+        b.record(stream)
+    torch.cuda.synchronize()
+    clocks = ClockSampler(local)
+    clocks.start()
+    time.sleep(0.3)
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    clocks.mark(True)
+    e0.record(stream)
+    for i in range(K):
+        mhc_pre_set_profile_events(op.handle, ev_k[i][0].cuda_event, ev_k[i][1].cuda_event)
+        step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    clocks.mark(False)
+    if world > 1:
+        torch.distributed.barrier()
+    mhc_pre_set_profile_events(op.handle, 0, 0)
+    time.sleep(0.2)
+    clocks.stop()
+    if op.status(grads) != 0:
+        raise RuntimeError("device-side error during the timed steps")
+    cfg["launch"] = mhc_pre_last_launch(op.handle)[1]
+    cfg["launch"]["kernel"] = "bw_main_kernel"
+    elapsed = max_over_ranks(e0.elapsed_time(e1) / 1e3, world, device)
+    kern = sum(a.elapsed_time(b) for a, b in ev_k) / K / 1e3
+    per_step = elapsed / K
+
+    # ---- end to end with host buffers: every step copies its inputs in from
+    # pinned host memory and the five gradients back out, on one stream
+    e2e = None
+    if not args.no_e2e:
+        names_in = [("x", case.x), ("g_in", g.g_in), ("g_post", g.g_post), ("g_res", g.g_res)] + \
+                   [(k, v) for k, v in saved.items()]
+        host_in = {k: v.cpu().pin_memory() for k, v in names_in}
+        dev_in = {k: torch.empty_like(v) for k, v in names_in}
+        outs = ("grad_x", "grad_phi", "grad_alpha", "grad_bias")
+        host_out = {k: torch.empty_like(grads[k], device="cpu").pin_memory() for k in outs}
+        sv = {k: dev_in[k] for k in saved}
+
+        def e2e_step():
+            for k, v in host_in.items():
+                dev_in[k].copy_(v, non_blocking=True)
+            op.backward(dev_in["x"], case.phi, case.alpha, None, dev_in["g_in"], dev_in["g_post"],
+                        dev_in["g_res"], sv, grads, stream=stream)
+            for k in outs:
+                host_out[k].copy_(grads[k], non_blocking=True)
+
+        e2e_step()
+        torch.cuda.synchronize()
+        Ke = max(3, min(K, 10))
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(Ke):
+            e2e_step()
+        b.record(stream)
+        torch.cuda.synchronize()
+        t_e2e = max_over_ranks(a.elapsed_time(b) / 1e3, world, device)
+        h2d = sum(v.numel() * v.element_size() for v in host_in.values())
+        d2h = sum(v.numel() * v.element_size() for v in host_out.values())
+        e2e = {"value": world * T * Ke / t_e2e, "unit": "tokens/s", "h2d_bytes_per_step": h2d,
+               "d2h_bytes_per_step": d2h, "steps": Ke}
+        del host_in, dev_in, host_out
+
+    peak, peak_src = hbm_peak()
+    lb_main = T * bwd_main_token_bytes(n, D)
+    lb_step = T * bwd_token_bytes(n, D) + 2 * 4 * (n * n + 2 * n) * n * D
+    achieved = lb_main / kern / 1e9
+    roof = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
+            "traffic": recorded_traffic("bw_main_kernel", T), "kernel": "bw_main_kernel", "kernel_ms": kern * 1e3,
+            "algorithmic_bytes": lb_main, "peak_source": f"hbm_gbs of {peak_src}"}
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        probe, _, _, _ = bwd_oracle_rate(case, saved, g, 0.0, 64)
+        rate, threads, sample, dt = bwd_oracle_rate(case, saved, g, 10.0, int(max(64, min(T, probe * 3))))
+        cpu = {"value": rate, "unit": "tokens/s", "cores": threads, "kind": "oracle", "sample": sample}
+    if rank == 0:
+        print(json.dumps({
+            "metric": BWD_METRIC, "value": world * T * K / elapsed, "unit": "tokens/s", "n_gpus": world,
+            "steps": K, "warmup": args.warmup, "ms_per_step": per_step * 1e3, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic", "config": cfg,
+            "hbm_gbs_step": lb_step / per_step / 1e9, "hbm_frac_step": lb_step / per_step / 1e9 / peak,
+            "roofline": roof, "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": 4 * K * world,
+            "clocks": clocks.summary()}))
+    if world > 1:
+        torch.distributed.destroy_process_group()
+    return 0
+
+
 def torch_int16():
     import torch
     return torch.int16
@@ -329,8 +533,9 @@ def main():
     ap.add_argument("--mode", type=int, default=WORKLOAD["impl_mode"], choices=[0, 1])
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--op", choices=["pre", "post"], default="pre",
-                    help="pre: the pre-mapping forward (the headline); post: the post-mapping (hc_post)")
+    ap.add_argument("--op", choices=["pre", "post", "bwd"], default="pre",
+                    help="pre: the pre-mapping forward (the headline); post: the post-mapping (hc_post); "
+                         "bwd: the pre-mapping backward")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
@@ -355,6 +560,8 @@ def main():
 
     if args.op == "post":
         return bench_post(args, device, world, rank, local)
+    if args.op == "bwd":
+        return bench_bwd(args, device, world, rank, local)
 
     if args.impl == "reference":
         if rank != 0:

@@ -132,20 +132,25 @@ MHC_API mhc_status_t mhc_pre_status(mhc_pre_t h, const void *workspace, void *st
 
 /* Optional timing hooks.  When set, mhc_pre_run records `before` on its
  * stream just before it launches the fused forward kernel and `after` just
- * after (both cudaEvent_t; pass NULL, NULL to clear).  This lets a caller time
- * that kernel alone, with CUDA events on the stream it runs on.  The events
- * are borrowed, not owned.  MHC_ERR_NULLPTR if h is NULL. */
+ * after (both cudaEvent_t; pass NULL, NULL to clear); mhc_pre_backward_run
+ * (mhc_pre_backward.h) does the same around its contraction kernel.  This
+ * lets a caller time that kernel alone, with CUDA events on the stream it
+ * runs on.  The events are borrowed, not owned.  MHC_ERR_NULLPTR if h is
+ * NULL. */
 MHC_API mhc_status_t mhc_pre_set_profile_events(mhc_pre_t h, void *before, void *after);
 
 /* Launch shape chosen by the last successful mhc_pre_run on this handle:
  * CTAs per cluster (0 for the grid-wide kernel), grid size in CTAs, x-ring
  * depth, and phi-ring depth (cluster kernels) or group count (grid-wide).
- * All zero before the first run.  Any output pointer may be NULL. */
+ * After mhc_pre_backward_run: 1, the contraction kernel's grid, its stage
+ * count, and the token-stage block count.  All zero before the first run.
+ * Any output pointer may be NULL. */
 MHC_API mhc_status_t mhc_pre_last_launch(mhc_pre_t h, int32_t *cluster, int32_t *grid,
                                          int32_t *stages, int32_t *ystages);
 
 /* Name of the fused kernel the last successful mhc_pre_run on this handle
- * launched ("" before the first run, or for a NULL handle).  The string is
+ * launched, or "bw_main_kernel" after mhc_pre_backward_run ("" before the
+ * first run, or for a NULL handle).  The string is
  * static and owned by the library.  A diagnostic for benchmarks and tests;
  * the pages have no counterpart. */
 MHC_API const char *mhc_pre_last_kernel(mhc_pre_t h);

@@ -40,6 +40,15 @@ class MhcPreArgs(ctypes.Structure):
                 ("norm_out", _P), ("workspace", _P), ("workspace_bytes", ctypes.c_size_t)]
 
 
+class MhcPreBwdArgs(ctypes.Structure):
+    _fields_ = [("T", ctypes.c_int64), ("x", _P), ("phi", _P), ("alpha", _P), ("gamma", _P),
+                ("grad_h_in", _P), ("grad_h_post", _P), ("grad_h_res", _P), ("inv_rms", _P),
+                ("h_mix", _P), ("h_pre", _P), ("h_post", _P), ("sum_out", _P), ("norm_out", _P),
+                ("grad_x_post", _P), ("grad_x", _P), ("grad_phi", _P), ("grad_alpha", _P),
+                ("grad_bias", _P), ("grad_gamma", _P), ("workspace", _P),
+                ("workspace_bytes", ctypes.c_size_t)]
+
+
 class MhcError(RuntimeError):
     def __init__(self, status: int, where: str, detail: str = ""):
         self.status = status
@@ -79,6 +88,10 @@ def library() -> ctypes.CDLL:
             lib.mhc_pre_last_launch.restype = ctypes.c_int32
             lib.mhc_post_run.argtypes = [ctypes.c_int64, ctypes.c_int64, ctypes.c_int64, _P, _P, _P, _P, _P, _P]
             lib.mhc_post_run.restype = ctypes.c_int32
+            lib.mhc_pre_backward_workspace_size.argtypes = [_P, ctypes.c_int64, ctypes.POINTER(ctypes.c_size_t)]
+            lib.mhc_pre_backward_workspace_size.restype = ctypes.c_int32
+            lib.mhc_pre_backward_run.argtypes = [_P, ctypes.POINTER(MhcPreBwdArgs), _P]
+            lib.mhc_pre_backward_run.restype = ctypes.c_int32
             lib.mhc_pre_last_kernel.argtypes = [_P]
             lib.mhc_pre_last_kernel.restype = ctypes.c_char_p
             lib.mhc_pre_destroy.argtypes = [_P]
@@ -165,6 +178,16 @@ def hc_post(x, residual, post, comb, out=None, stream=None):
     if st != MHC_OK:
         raise MhcError(st, "mhc_post_run", last_error())
     return out
+
+
+def mhc_pre_backward_workspace_size(handle, T: int):
+    n = ctypes.c_size_t(0)
+    st = library().mhc_pre_backward_workspace_size(handle, int(T), ctypes.byref(n))
+    return st, n.value
+
+
+def mhc_pre_backward_run(handle, args: MhcPreBwdArgs, stream: int = 0) -> int:
+    return library().mhc_pre_backward_run(handle, ctypes.byref(args), _P(stream or None))
 
 
 def mhc_pre_destroy(handle) -> None:
@@ -266,6 +289,60 @@ class MhcPre:
         if st != MHC_OK:
             raise MhcError(st, "mhc_pre_run", last_error())
         return out
+
+    def backward_workspace_size(self, T: int) -> int:
+        st, n = mhc_pre_backward_workspace_size(self.handle, T)
+        if st != MHC_OK:
+            raise MhcError(st, "mhc_pre_backward_workspace_size", last_error())
+        return n
+
+    def allocate_backward(self, T: int, device, *, gamma: bool = False):
+        """Gradient outputs and workspace for T tokens (torch supplies the memory)."""
+        import torch
+        n, D, R = self.n, self.D, self.R
+        f32 = dict(dtype=torch.float32, device=device)
+        return {"grad_x": torch.empty((T, n, D), dtype=torch.bfloat16, device=device),
+                "grad_phi": torch.empty((R, n * D), **f32),
+                "grad_alpha": torch.empty((3,), **f32),
+                "grad_bias": torch.empty((R,), **f32),
+                "grad_gamma": torch.empty((n, D), **f32) if gamma else None,
+                "workspace": torch.zeros((max(self.backward_workspace_size(T), 256),),
+                                         dtype=torch.uint8, device=device)}
+
+    def make_backward_args(self, x, phi, alpha, gamma, grad_h_in, grad_h_post, grad_h_res, saved,
+                           grads, grad_x_post=None) -> MhcPreBwdArgs:
+        """saved: the forward's outputs (inv_rms, h_mix, h_pre, h_post and,
+        for the Sinkhorn form, sum_out / norm_out -- None selects the logit
+        form); grads: from allocate_backward."""
+        a = MhcPreBwdArgs()
+        a.T = int(x.shape[0])
+        a.x, a.phi, a.alpha, a.gamma = _ptr(x), _ptr(phi), _ptr(alpha), _ptr(gamma)
+        a.grad_h_in, a.grad_h_post, a.grad_h_res = _ptr(grad_h_in), _ptr(grad_h_post), _ptr(grad_h_res)
+        for k in ("inv_rms", "h_mix", "h_pre", "h_post", "sum_out", "norm_out"):
+            setattr(a, k, _ptr(saved.get(k)))
+        a.grad_x_post = _ptr(grad_x_post)
+        for k in ("grad_x", "grad_phi", "grad_alpha", "grad_bias", "grad_gamma"):
+            setattr(a, k, _ptr(grads.get(k)))
+        ws = grads.get("workspace")
+        a.workspace = _ptr(ws)
+        a.workspace_bytes = 0 if ws is None else ws.numel() * ws.element_size()
+        return a
+
+    def backward(self, x, phi, alpha, gamma, grad_h_in, grad_h_post, grad_h_res, saved, grads,
+                 grad_x_post=None, stream=None):
+        """Enqueue the backward on `stream` (default: torch's current stream).
+        Raises MhcError on a host-side rejection."""
+        args = self.make_backward_args(x, phi, alpha, gamma, grad_h_in, grad_h_post, grad_h_res, saved,
+                                       grads, grad_x_post)
+        if stream is None:
+            import torch
+            stream = torch.cuda.current_stream(x.device).cuda_stream
+        elif hasattr(stream, "cuda_stream"):
+            stream = stream.cuda_stream
+        st = mhc_pre_backward_run(self.handle, args, int(stream))
+        if st != MHC_OK:
+            raise MhcError(st, "mhc_pre_backward_run", last_error())
+        return grads
 
     def status(self, out=None, stream=None) -> int:
         ws = None if out is None else out.get("workspace")

@@ -1,0 +1,706 @@
+// mhc_bwd.cu -- the sm_103a backward of the mHC pre-mapping with Sinkhorn
+// (n = 4, three gates).
+//
+// What is computed follows "CANN ops-transformer 算子解析：MhcPreBackward 反向
+// 梯度算子实现与 aclnn 调用指南" §三 3.1-3.8 (the outputs are the gradients of
+// the forward, §一), with the Sinkhorn variant's saved sums and matrices of
+// "aclnnMhcPreSinkhorn 接口与 MhcPreSinkhorn 实现剖析" §3.2 carried back first.
+// How it is laid out on the GPU is this file's own design:
+//
+//  * Token stage (one warp per token): H_pre_grad = grad_h_in . x over the
+//    whole row (the only full-row reduction of the backward), the Sinkhorn
+//    backward on 16 lanes from the saved steps, the gate backward, and
+//    G = H_mix_grad with the RMS factor c = -inv_rms_grad invRms^3 / (nD).
+//    G goes out as exact bf16 planes in a per-64-token tile record laid out
+//    for the tensor core, next to hPre and c of the tile's tokens.
+//  * Main kernel (one CTA per SM): the work units are (64-column slab of all
+//    four streams, one of nq contiguous chunks of the 64-token tiles); CTA b
+//    takes units b, b + grid, ...  With grid a multiple of nq, the CTAs that
+//    share b mod nq sweep the same tokens at the same time over different
+//    slabs, so together they read whole rows of x (DRAM-page friendly).
+//    Per tile, TMA brings x [4][64 tokens][64], grad_h_in
+//    [64 tokens][64] and the tile record; tcgen05 forms
+//      - G phi' (phi' = phi . gamma in planes, resident per slab) as
+//        D1[k][token] in TMEM (M = 128 columns k of two streams, N = 64
+//        tokens, K = the 24 gate rows per plane product), and
+//      - x^T G accumulated in TMEM across the run's tiles of one slab
+//        (M = 128 columns k, N = P * 32 plane rows, K = 16 tokens per step).
+//    Sixteen epilogue warps (32 tokens of one M-group each) form
+//    grad_x = hPre grad_h_in + D1 + c x (+ grad_x_post) in fp32 and round
+//    it to bf16 over the x tile in place; a store warp writes the tile out
+//    with one TMA store and hands the slot back.  At the end of a unit
+//    eight of them write x^T G, summed over the planes, to the unit's
+//    partial buffer.
+//  * Final kernel: grad_phi = gamma . sum(x^T G), grad_gamma = sum_r phi .
+//    sum(x^T G), summing a slab's units in chunk order; grad_alpha and
+//    grad_bias from the token stage's per-warp partials in warp order.
+//  * Every wait is bounded; a wait that gives up sets the error word and the
+//    kernel winds down.
+#include "mhc_ptx.cuh"
+
+namespace mhc {
+namespace {
+
+__device__ __forceinline__ float bf16_round(float v) { return __bfloat162float(__float2bfloat16_rn(v)); }
+
+// Plane `plane` of the exact split v = hi + mid + lo (three planes), or of
+// v truncated to 10 mantissa bits and split hi + lo (two planes).
+__device__ __forceinline__ float plane_part(float v, int plane, int tf32) {
+  if (tf32) v = __uint_as_float(__float_as_uint(v) & 0xFFFFE000u);
+  const float hi = bf16_round(v);
+  if (plane == 0) return hi;
+  const float rem = v - hi;               // exact
+  const float mid = bf16_round(rem);
+  if (plane == 1) return mid;
+  return bf16_round(rem - mid);           // rem - mid exact
+}
+
+// Byte offset of element (row, col) (col < 64) in a 128-byte-swizzled tile.
+__device__ __forceinline__ uint32_t swz(int row, int col) {
+  return (uint32_t)(row * 128 + ((((col >> 3) ^ (row & 7)) << 4) | ((col & 7) << 1)));
+}
+
+// =================================================================== planes
+__global__ void __launch_bounds__(256) bw_planes_kernel(BwPlaneParams pp) {
+  if (blockIdx.x == 0 && threadIdx.x < kHdrWords && pp.hdr) pp.hdr[threadIdx.x] = 0u;
+  const int rows = pp.P * kBwRp;                        // rows of one stream block
+  const long long total = (long long)pp.nslab * kBwNS * rows * 64;
+  const int K = kBwNS * pp.D;
+  for (long long idx = (long long)blockIdx.x * blockDim.x + threadIdx.x; idx < total;
+       idx += (long long)gridDim.x * blockDim.x) {
+    const int e = (int)(idx & 63);
+    const long long grow = idx >> 6;
+    const int rr = (int)(grow % rows);                  // row in the stream block
+    const long long blk = grow / rows;
+    const int i = (int)(blk % kBwNS);
+    const int j = (int)(blk / kBwNS);
+    const int plane = rr / kBwRp, r = rr % kBwRp;
+    const int d = j * 64 + ((((e >> 3) ^ (rr & 7)) << 3) | (e & 7));
+    float out = 0.0f;
+    if (r < kBwR) {
+      const int k = i * pp.D + d;
+      float v = __ldg(pp.phi + (size_t)r * K + k);
+      if (pp.gamma) v *= __ldg(pp.gamma + k);
+      out = plane_part(v, plane, pp.tf32);
+    }
+    pp.planes[idx] = __float2bfloat16_rn(out);          // exact
+  }
+}
+
+// =============================================================== token stage
+constexpr int kSinkChunk = 16;   // saved Sinkhorn steps staged per round
+constexpr int kVec = 3;          // 16-byte column vectors per lane in flight (x 4 streams + grad_h_in each)
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+
+__global__ void __launch_bounds__(kBwTokenWarps * 32) bw_token_kernel(BwTokenParams p) {
+  constexpr int NS = kBwNS, R = kBwR, NN = NS * NS;
+  __shared__ float stage[kBwTokenWarps][kSinkChunk][NN + NS];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int gw = blockIdx.x * kBwTokenWarps + warp;
+  const int nw = gridDim.x * kBwTokenWarps;
+  const int Tpad = p.ntiles * kBwTile;
+  const int nv = p.D >> 3;                              // 16-byte vectors per row
+  const float a0 = __ldg(p.alpha), a1 = __ldg(p.alpha + 1), a2 = __ldg(p.alpha + 2);
+  const float eps = p.hc_eps;
+  const int rec_bytes = bw_tile_rec_bytes(p.P);
+  float acc_bias = 0.0f, acc_alpha = 0.0f;              // this lane's partial sums
+  float (*st)[NN + NS] = stage[warp];
+
+  for (int t = gw; t < Tpad; t += nw) {
+    uint8_t* rec = p.tiles + (size_t)(t / kBwTile) * rec_bytes;
+    const int col = t % kBwTile;
+    float* scal = reinterpret_cast<float*>(rec + p.P * kBwPlaneBytes) + col * 8;
+    if (t >= p.T) {                                     // padding token of the last tile
+      for (int pl = 0; pl < p.P; ++pl)
+        *reinterpret_cast<__nv_bfloat16*>(rec + pl * kBwPlaneBytes + swz(lane, col)) = __float2bfloat16_rn(0.0f);
+      if (lane < 8) scal[lane] = 0.0f;
+      continue;
+    }
+    // ---- 3.1: H_pre_grad[i] = sum_d grad_h_in[d] x[i][d]
+    float hg[NS] = {0.0f, 0.0f, 0.0f, 0.0f};
+    {
+      const __nv_bfloat16* xr = p.x + (size_t)t * NS * p.D;
+      const __nv_bfloat16* gr = p.g_in + (size_t)t * p.D;
+      for (int v0 = lane; v0 < nv; v0 += 32 * kVec) {
+        uint4 gv[kVec], xv[kVec][NS];
+#pragma unroll
+        for (int b = 0; b < kVec; ++b) {
+          const int v = v0 + 32 * b;
+          if (v < nv) {
+            gv[b] = __ldg(reinterpret_cast<const uint4*>(gr) + v);
+#pragma unroll
+            for (int i = 0; i < NS; ++i) xv[b][i] = __ldg(reinterpret_cast<const uint4*>(xr + (size_t)i * p.D) + v);
+          }
+        }
+#pragma unroll
+        for (int b = 0; b < kVec; ++b) {
+          if (v0 + 32 * b >= nv) continue;
+          const __nv_bfloat162* g2 = reinterpret_cast<const __nv_bfloat162*>(&gv[b]);
+#pragma unroll
+          for (int i = 0; i < NS; ++i) {
+            const __nv_bfloat162* x2 = reinterpret_cast<const __nv_bfloat162*>(&xv[b][i]);
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const float2 gf = __bfloat1622float2(g2[e]), xf = __bfloat1622float2(x2[e]);
+              hg[i] = fmaf(gf.x, xf.x, hg[i]);
+              hg[i] = fmaf(gf.y, xf.y, hg[i]);
+            }
+          }
+        }
+      }
+#pragma unroll
+      for (int i = 0; i < NS; ++i) hg[i] = warp_sum(hg[i]);
+    }
+    const float ir = __ldg(p.inv_rms + t);
+    const float hmix_r = lane < R ? __ldg(p.h_mix + (size_t)t * R + lane) : 0.0f;
+
+    // ---- Sinkhorn backward (lane = i*4 + j on lanes 0..15; 16..31 mirror them)
+    const int el = lane & (NN - 1);
+    float g = __ldg(p.g_res + (size_t)t * NN + el);
+    if (p.norm_out) {
+      for (int kh = 2 * p.num_iters - 1; kh >= 1; kh -= kSinkChunk) {
+        const int klo = max(1, kh - kSinkChunk + 1);
+        const int cnt = kh - klo + 1;
+        __syncwarp();
+        for (int e = lane; e < cnt * NN; e += 32)
+          st[e / NN][e % NN] = __ldg(p.norm_out + ((size_t)(klo + e / NN) * p.T + t) * NN + e % NN);
+        for (int e = lane; e < cnt * NS; e += 32)
+          st[e / NS][NN + e % NS] = __ldg(p.sum_out + ((size_t)(klo + e / NS) * p.T + t) * NS + e % NS);
+        __syncwarp();
+        for (int k = kh; k >= klo; --k) {
+          const float* row = st[k - klo];
+          const float prod = g * row[el];
+          float dot, s;
+          if (k & 1) {            // column step: sum over i, divide by column sum j
+            dot = prod + __shfl_xor_sync(0xffffffffu, prod, 4);
+            dot += __shfl_xor_sync(0xffffffffu, dot, 8);
+            s = row[NN + (el & 3)];
+          } else {                // row step: sum over j, divide by row sum i
+            dot = prod + __shfl_xor_sync(0xffffffffu, prod, 1);
+            dot += __shfl_xor_sync(0xffffffffu, dot, 2);
+            s = row[NN + (el >> 2)];
+          }
+          g = __fdiv_rn(g - dot, s);
+        }
+      }
+      // the row softmax (+ eps): S = normOut[0] - eps
+      const float S = __ldg(p.norm_out + (size_t)t * NN + el) - eps;
+      const float prod = g * S;
+      float dot = prod + __shfl_xor_sync(0xffffffffu, prod, 1);
+      dot += __shfl_xor_sync(0xffffffffu, dot, 2);
+      g = S * (g - dot);
+    }
+    const float gres = __shfl_sync(0xffffffffu, g, (lane - 2 * NS) & 31);
+
+    // ---- gates (3.2-3.4), lane r = gate row
+    float gt = 0.0f, aterm = 0.0f, bterm = 0.0f;
+    if (lane < NS) {
+      const float s = __ldg(p.h_pre + (size_t)t * NS + lane) - eps;
+      float h = hg[0];
+#pragma unroll
+      for (int i = 1; i < NS; ++i) h = (lane == i) ? hg[i] : h;
+      bterm = h * s * (1.0f - s);
+      gt = bterm * a0;
+    } else if (lane < 2 * NS) {
+      const float hp = __ldg(p.h_post + (size_t)t * NS + lane - NS);
+      bterm = __ldg(p.g_post + (size_t)t * NS + lane - NS) * hp * (1.0f - 0.5f * hp);
+      gt = bterm * a1;
+    } else if (lane < R) {
+      bterm = gres;
+      gt = bterm * a2;
+    }
+    aterm = bterm * (hmix_r * ir);
+    acc_bias += bterm;
+    acc_alpha += aterm;
+    // ---- 3.5: G = [alpha g] invRms; inv_rms_grad = sum [alpha g] hMix
+    const float irg = warp_sum(gt * hmix_r);
+    const float G = gt * ir;
+    const float c = -(irg * ir * ir * ir) / (float)(NS * p.D);
+    for (int pl = 0; pl < p.P; ++pl)
+      *reinterpret_cast<__nv_bfloat16*>(rec + pl * kBwPlaneBytes + swz(lane, col)) =
+          __float2bfloat16_rn(plane_part(G, pl, p.tf32));
+    if (lane < 2 * NS) scal[lane] = (lane & 1) ? c : __ldg(p.h_pre + (size_t)t * NS + (lane >> 1));
+  }
+  // ---- this warp's partial sums: [0, R) bias, R.. R+2 alpha by segment
+  float seg0 = lane < NS ? acc_alpha : 0.0f;
+  float seg1 = (lane >= NS && lane < 2 * NS) ? acc_alpha : 0.0f;
+  float seg2 = (lane >= 2 * NS && lane < R) ? acc_alpha : 0.0f;
+  seg0 = warp_sum(seg0);
+  seg1 = warp_sum(seg1);
+  seg2 = warp_sum(seg2);
+  float* out = p.partials + (size_t)gw * 32;
+  float v = lane < R ? acc_bias : 0.0f;
+  if (lane == R) v = seg0;
+  if (lane == R + 1) v = seg1;
+  if (lane == R + 2) v = seg2;
+  out[lane] = v;
+}
+
+// ================================================================ main kernel
+// Warps: 0 TMA producer, 1 MMA issuer (and TMEM owner), 2 grad_x store,
+// 3..18 epilogue.  Epilogue warp e works on TMEM lane quarter (warp % 4),
+// M-group (e >> 3) and token half ((e >> 2) & 1) of each tile.
+constexpr int kWarpProd = 0, kWarpMma = 1, kWarpStore = 2, kWarpEpi0 = 3;
+constexpr int kEpiWarps = 16;
+constexpr int kMainThreads = (kWarpEpi0 + kEpiWarps) * 32;
+constexpr int kMaxStages = 4;
+constexpr int kXBytes = kBwNS * kBwTile * 128;    // x tile of all streams (32 KB)
+constexpr int kGinBytes = kBwTile * 128;          // grad_h_in tile (8 KB)
+constexpr int kGroups = kBwNS / 2;                // M = 128 columns = two streams
+constexpr int kHalf = kBwTile / 2;                // tokens per epilogue warp
+
+struct MainTail {
+  uint64_t full[kMaxStages], empty[kMaxStages], out_ready[kMaxStages];
+  uint64_t a_full, a_free;
+  uint64_t d1_full[2], d1_empty[2];
+  uint64_t mt_full, mt_empty;
+  uint64_t mma_done;
+  uint32_t tmem_base;
+  uint32_t abort;
+};
+static_assert(sizeof(MainTail) <= kBwTailBytes, "barrier block outgrew its reservation");
+
+// Plane products of G phi' as (G plane, phi' plane).  Three planes keep the
+// six of combined order up to 2^-16 (hi.hi, hi.mid, mid.hi, hi.lo, lo.hi,
+// mid.mid); two planes the first three (hi.hi, hi.lo, lo.hi).
+__device__ __forceinline__ void product_planes(int q, int& gp, int& pp) {
+  const int g3[6] = {0, 0, 1, 0, 2, 1}, p3[6] = {0, 1, 0, 2, 0, 1};
+  gp = g3[q];
+  pp = p3[q];
+}
+
+template <int P, bool kGxp>
+__global__ void __launch_bounds__(kMainThreads, 1)
+    bw_main_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constant__ CUtensorMap tmap_gin,
+                   const __grid_constant__ CUtensorMap tmap_gx, const __grid_constant__ CUtensorMap tmap_gxp,
+                   const __nv_bfloat16* __restrict__ planes, const uint8_t* __restrict__ tiles,
+                   float* __restrict__ pieces, uint32_t* err, int ntiles, int nslab, int nq, int stages) {
+  constexpr int kABlk = P * kBwPlaneBytes;            // one stream's block of the phi' slab
+  constexpr int kABytes = kBwNS * kABlk;
+  constexpr int kRec = bw_tile_rec_bytes(P);
+  constexpr int kMtCols = bw_mt_cols(P);              // N of x^T G
+  constexpr int kNQ = P == 3 ? 6 : 3;                 // plane products of G phi'
+  constexpr int kMtCol0 = 2 * kGroups * kBwTile;      // after two D1 buffers
+  constexpr uint32_t kTmemCols = 512;
+  constexpr int kStageBytes = bw_stage_bytes(P, kGxp);
+  // stage layout: x | grad_x_post (optional) | grad_h_in | tile record
+  constexpr int offGxp = kXBytes;
+  constexpr int offGin = kXBytes * (kGxp ? 2 : 1);
+  constexpr int offRec = offGin + kGinBytes;
+  static_assert(kMtCol0 + kGroups * kMtCols <= (int)kTmemCols, "TMEM budget");
+
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* sA = smem;
+  uint8_t* sStage = smem + kABytes;
+  MainTail* tail = reinterpret_cast<MainTail*>(sStage + (size_t)stages * kStageBytes);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  // Work units u = slab * nq + chunk (chunk: a contiguous nq-th of the token
+  // tiles), CTA b taking u = b, b + grid, ...; a unit is one run of x^T G.
+  const int nunits = nslab * nq;
+  Ctl ctl{&tail->abort, err};
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < stages; ++s) {
+      mbar_init(&tail->full[s], 1);
+      mbar_init(&tail->empty[s], 1);
+      mbar_init(&tail->out_ready[s], kEpiWarps);
+    }
+    mbar_init(&tail->a_full, 1);
+    mbar_init(&tail->a_free, 1);
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&tail->d1_full[b], 1);
+      mbar_init(&tail->d1_empty[b], kEpiWarps);
+    }
+    mbar_init(&tail->mt_full, 1);
+    mbar_init(&tail->mt_empty, kEpiWarps / 2);
+    mbar_init(&tail->mma_done, 1);
+    tail->abort = 0u;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    tma_prefetch_desc(&tmap_x);
+    tma_prefetch_desc(&tmap_gin);
+    tma_prefetch_desc(&tmap_gx);
+    if (kGxp) tma_prefetch_desc(&tmap_gxp);
+  }
+  if (warp == kWarpMma) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                     smem_u32(&tail->tmem_base)),
+                 "r"(kTmemCols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = tail->tmem_base;
+
+  if (warp == kWarpProd) {
+    // ===================================================== TMA producer
+    if (lane == 0) {
+      const uint64_t once = policy_evict_first();
+      const uint64_t keep = policy_evict_last();
+      int s = 0;
+      uint32_t ph = 0;
+      long long iss = 0;
+      int piece = 0;
+      bool ok = true, a_pending = false;
+      for (int u = blockIdx.x; u < nunits && ok; u += gridDim.x) {
+        const int slab = u / nq, chunk = u % nq;
+        const int t0 = (int)((long long)chunk * ntiles / nq), t1 = (int)((long long)(chunk + 1) * ntiles / nq);
+        if (t0 == t1) continue;
+        if (piece > 0 && !wait_bar<false>(&tail->a_free, (uint32_t)(piece - 1) & 1u, ctl, kErrWaitTimeout)) break;
+        mbar_expect_tx(&tail->a_full, (uint32_t)kABytes);
+        bulk_load_hint(sA, planes + (size_t)slab * (kABytes / 2), (uint32_t)kABytes, &tail->a_full, keep);
+        a_pending = true;
+        ++piece;
+        for (int tile = t0; tile < t1; ++tile) {
+          if (!wait_bar<false>(&tail->empty[s], ph ^ 1u, ctl, kErrWaitTimeout)) { ok = false; break; }
+          uint8_t* st = sStage + (size_t)s * kStageBytes;
+          mbar_expect_tx(&tail->full[s], (uint32_t)kStageBytes);
+          tma_load_4d_hint(st, &tmap_x, &tail->full[s], 0, tile * kBwTile, slab, 0, once);
+          if (kGxp) tma_load_4d_hint(st + offGxp, &tmap_gxp, &tail->full[s], 0, tile * kBwTile, slab, 0, once);
+          tma_load_3d_hint(st + offGin, &tmap_gin, &tail->full[s], 0, tile * kBwTile, slab, once);
+          bulk_load_hint(st + offRec, tiles + (size_t)tile * kRec, (uint32_t)kRec, &tail->full[s], keep);
+          ++iss;
+          if (++s == stages) { s = 0; ph ^= 1u; }
+        }
+      }
+      for (long long q = 0; q < (iss < stages ? iss : stages); ++q) {   // let issued copies land
+        if (--s < 0) { s = stages - 1; ph ^= 1u; }
+        mbar_drain(&tail->full[s], ph);
+      }
+      if (a_pending) mbar_drain(&tail->a_full, (uint32_t)(piece - 1) & 1u);
+    }
+  } else if (warp == kWarpMma) {
+    // ===================================================== MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t idesc_mt = idesc_bf16_major(128, kMtCols, true, false);
+      constexpr uint32_t idesc_d1 = idesc_bf16_major(128, kBwTile, true, true);
+      const uint32_t a_addr = smem_u32(sA);
+      int s = 0;
+      uint32_t ph = 0;
+      long long k = 0;
+      int piece = 0;
+      bool ok = true;
+      for (int u = blockIdx.x; u < nunits && ok; u += gridDim.x) {
+        const int chunk = u % nq;
+        const int t0 = (int)((long long)chunk * ntiles / nq), t1 = (int)((long long)(chunk + 1) * ntiles / nq);
+        for (int tile = t0; tile < t1; ++tile, ++k) {
+          const bool first = tile == t0, last = tile == t1 - 1;
+          if (!wait_bar<false>(&tail->full[s], ph, ctl, kErrWaitTimeout)) { ok = false; break; }
+          if (first) {
+            if (!wait_bar<false>(&tail->a_full, (uint32_t)piece & 1u, ctl, kErrWaitTimeout)) { ok = false; break; }
+            if (piece > 0 &&
+                !wait_bar<false>(&tail->mt_empty, (uint32_t)(piece - 1) & 1u, ctl, kErrWaitTimeout)) {
+              ok = false;
+              break;
+            }
+          }
+          tc_fence_after();
+          const uint32_t x_addr = smem_u32(sStage + (size_t)s * kStageBytes);
+          const uint32_t gt_addr = x_addr + (uint32_t)offRec;
+          // x^T G: A = x tile seen MN-major (rows = tokens = K), B = G planes K-major
+#pragma unroll
+          for (int g = 0; g < kGroups; ++g) {
+#pragma unroll
+            for (int ks = 0; ks < kBwTile / 16; ++ks)
+              mma_bf16(tmem_base + (uint32_t)(kMtCol0 + g * kMtCols),
+                       sw128_desc_mn(x_addr + (uint32_t)(g * 2 * kBwTile * 128 + ks * 2048), kBwTile * 128),
+                       sw128_desc(gt_addr + (uint32_t)(ks * 32)), idesc_mt, (first && ks == 0) ? 0u : 1u);
+          }
+          const int b = (int)(k & 1);
+          if (!wait_bar<false>(&tail->d1_empty[b], ((uint32_t)(k >> 1) & 1u) ^ 1u, ctl, kErrWaitTimeout)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          // G phi': A = phi' slab MN-major (rows = gate rows = K), B = G planes
+          // MN-major with N = 64 tokens, one 128-byte row (its atom stride is unused)
+#pragma unroll
+          for (int g = 0; g < kGroups; ++g) {
+#pragma unroll
+            for (int q = 0; q < kNQ; ++q) {
+              int gp, pp;
+              product_planes(q, gp, pp);
+#pragma unroll
+              for (int ks = 0; ks < kBwRp / 16; ++ks)
+                mma_bf16(tmem_base + (uint32_t)(b * kGroups * kBwTile + g * kBwTile),
+                         sw128_desc_mn(a_addr + (uint32_t)(g * 2 * kABlk + pp * kBwPlaneBytes + ks * 2048), kABlk),
+                         sw128_desc_mn(gt_addr + (uint32_t)(gp * kBwPlaneBytes + ks * 2048), 1024), idesc_d1,
+                         (q == 0 && ks == 0) ? 0u : 1u);
+            }
+          }
+          mma_commit(&tail->d1_full[b]);
+          if (last) {
+            mma_commit(&tail->mt_full);
+            mma_commit(&tail->a_free);
+            ++piece;
+          }
+          if (++s == stages) { s = 0; ph ^= 1u; }
+        }
+      }
+      mma_commit(&tail->mma_done);
+      mbar_drain(&tail->mma_done, 0);
+    }
+  } else if (warp == kWarpStore) {
+    // ===================================================== grad_x store
+    // Once all epilogue warps have written a tile's grad_x over its x slot,
+    // one TMA store writes it out; the slot goes back to the producer as
+    // soon as the store has read it.
+    if (lane == 0) {
+      int s = 0;
+      uint32_t ph = 0;
+      bool ok = true;
+      for (int u = blockIdx.x; u < nunits && ok; u += gridDim.x) {
+        const int slab = u / nq, chunk = u % nq;
+        const int t0 = (int)((long long)chunk * ntiles / nq), t1 = (int)((long long)(chunk + 1) * ntiles / nq);
+        for (int tile = t0; tile < t1; ++tile) {
+          if (!wait_bar<false>(&tail->out_ready[s], ph, ctl, kErrWaitTimeout)) { ok = false; break; }
+          tma_store_4d(&tmap_gx, sStage + (size_t)s * kStageBytes, 0, tile * kBwTile, slab, 0);
+          bulk_commit();
+          bulk_wait_read<0>();
+          mbar_arrive(&tail->empty[s]);
+          if (++s == stages) { s = 0; ph ^= 1u; }
+        }
+      }
+      bulk_wait<0>();                           // every grad_x store has landed
+    }
+  } else {
+    // ===================================================== epilogue
+    const int ew = warp - kWarpEpi0;          // 0..15
+    const int grp = ew >> 3;                  // M-group: streams 2grp, 2grp+1
+    const int half = (ew >> 2) & 1;           // tokens half*32 .. +32
+    const int q = warp & 3;                   // TMEM lane quarter of this warp
+    const int m = q * 32 + lane;              // row of the group (0..127)
+    const int i = grp * 2 + (m >> 6);         // stream
+    const int d = m & 63;                     // column of the slab
+    int s = 0;
+    uint32_t ph = 0;
+    long long k = 0;
+    int piece = 0;
+    bool run = true;
+    for (int u = blockIdx.x; u < nunits && run; u += gridDim.x) {
+      const int chunk = u % nq;
+      const int t0 = (int)((long long)chunk * ntiles / nq), t1 = (int)((long long)(chunk + 1) * ntiles / nq);
+      for (int tile = t0; tile < t1; ++tile, ++k) {
+        const bool last = tile == t1 - 1;
+        const int b = (int)(k & 1);
+        if (!wait_bar<false>(&tail->full[s], ph, ctl, kErrWaitTimeout) ||
+            !wait_bar<false>(&tail->d1_full[b], (uint32_t)(k >> 1) & 1u, ctl, kErrWaitTimeout)) {
+          run = false;
+          break;
+        }
+        tc_fence_after();
+        uint8_t* st = sStage + (size_t)s * kStageBytes;
+        uint8_t* xs = st + i * (kBwTile * 128);
+        const uint8_t* gxs = st + offGxp + i * (kBwTile * 128);
+        const uint8_t* gin = st + offGin;
+        const float* scal = reinterpret_cast<const float*>(st + offRec + P * kBwPlaneBytes);
+        float acc[kHalf];
+        {
+          const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16) +
+                                 (uint32_t)(b * kGroups * kBwTile + grp * kBwTile + half * kHalf);
+          float v0[16], v1[16];
+          tmem_ld16(taddr, v0);
+          tmem_ld16(taddr + 16, v1);
+#pragma unroll
+          for (int e = 0; e < 16; ++e) { acc[e] = v0[e]; acc[16 + e] = v1[e]; }
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&tail->d1_empty[b]);
+        // Lanes 2p, 2p+1 hold columns d, d+1 (d even).  Each pair trades
+        // one value so that the even lane forms both columns of token e and
+        // the odd lane both columns of token e + 4 (rows 4 apart sit in
+        // different bank groups of the swizzle): 4-byte shared accesses.
+        const int odd = lane & 1;
+        const int dp = d & ~1;
+        const uint32_t pair_off = (uint32_t)(dp & 7) << 1;
+#pragma unroll
+        for (int e0 = 0; e0 < kHalf; e0 += 8) {
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            const int ea = e0 + j, eb = ea + 4;
+            const float sendv = odd ? acc[ea] : acc[eb];
+            const float recv = __shfl_xor_sync(0xffffffffu, sendv, 1);
+            const float lo = odd ? recv : acc[ea];
+            const float hi = odd ? acc[eb] : recv;
+            const int e = odd ? eb : ea;
+            const int c = half * kHalf + e;
+            const uint32_t off = (uint32_t)(c * 128) + ((uint32_t)(((dp >> 3) ^ (e & 7))) << 4) + pair_off;
+            const float2 xf = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(xs + off));
+            const float2 gf = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(gin + off));
+            const float2 hc = *reinterpret_cast<const float2*>(scal + c * 8 + 2 * i);   // (hPre_i, RMS factor)
+            float vlo = fmaf(hc.x, gf.x, lo), vhi = fmaf(hc.x, gf.y, hi);
+            vlo = fmaf(hc.y, xf.x, vlo);
+            vhi = fmaf(hc.y, xf.y, vhi);
+            if constexpr (kGxp) {
+              const float2 pf = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(gxs + off));
+              vlo += pf.x;
+              vhi += pf.y;
+            }
+            *reinterpret_cast<__nv_bfloat162*>(xs + off) = __floats2bfloat162_rn(vlo, vhi);
+          }
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&tail->out_ready[s]);
+        if (last && half == 0) {
+          // x^T G of this unit, summed over the planes -> partial buffer [u][r][k]
+          if (!wait_bar<false>(&tail->mt_full, (uint32_t)piece & 1u, ctl, kErrWaitTimeout)) {
+            run = false;
+            break;
+          }
+          tc_fence_after();
+          float* dst = pieces + (size_t)u * kBwRp * (kBwNS * 64) + grp * 128 + m;
+          const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(kMtCol0 + grp * kMtCols);
+#pragma unroll
+          for (int c0 = 0; c0 < kBwR; c0 += 8) {
+            float sum[8];
+#pragma unroll
+            for (int pl = 0; pl < P; ++pl) {
+              float v[8];
+              tmem_ld8(taddr + (uint32_t)(pl * kBwRp + c0), v);
+#pragma unroll
+              for (int e = 0; e < 8; ++e) sum[e] = pl == 0 ? v[e] : sum[e] + v[e];
+            }
+#pragma unroll
+            for (int e = 0; e < 8; ++e) dst[(size_t)(c0 + e) * (kBwNS * 64)] = sum[e];
+          }
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&tail->mt_empty);
+        }
+        if (last) ++piece;
+        if (++s == stages) { s = 0; ph ^= 1u; }
+      }
+    }
+  }
+
+  // ---- teardown
+  tc_fence_before();
+  __syncthreads();
+  if (warp == kWarpMma) {
+    __syncwarp();
+    tc_fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base), "r"(kTmemCols)
+                 : "memory");
+  }
+}
+
+// =============================================================== final sums
+constexpr int kFinalThreads = 256;
+
+__global__ void __launch_bounds__(kFinalThreads) bw_final_kernel(BwFinalParams p, int col_blocks) {
+  const int K = kBwNS * p.D;
+  if ((int)blockIdx.x < col_blocks) {
+    const int k = blockIdx.x * kFinalThreads + threadIdx.x;
+    if (k >= K) return;
+    const int i = k / p.D, dd = k % p.D;
+    const int slab = dd / 64;
+    const int mloc = i * 64 + (dd & 63);
+    float acc[kBwR];
+#pragma unroll
+    for (int r = 0; r < kBwR; ++r) acc[r] = 0.0f;
+    for (int c = 0; c < p.nq; ++c) {                  // the slab's units, in order
+      const float* src = p.pieces + (size_t)(slab * p.nq + c) * kBwRp * (kBwNS * 64) + mloc;
+#pragma unroll
+      for (int r = 0; r < kBwR; ++r) acc[r] += src[(size_t)r * (kBwNS * 64)];
+    }
+    const float gm = p.gamma ? __ldg(p.gamma + k) : 1.0f;
+    float gg = 0.0f;
+#pragma unroll
+    for (int r = 0; r < kBwR; ++r) {
+      p.grad_phi[(size_t)r * K + k] = gm * acc[r];
+      gg = fmaf(__ldg(p.phi + (size_t)r * K + k), acc[r], gg);
+    }
+    if (p.grad_gamma) p.grad_gamma[k] = gg;
+    return;
+  }
+  // grad_bias[v] (v < R) and grad_alpha[v - R]: fixed-order sums of the partials
+  __shared__ float red[kFinalThreads];
+  const int v = blockIdx.x - col_blocks;
+  const int colp = v;                       // column of the partial records
+  float sacc = 0.0f;
+  for (int j = threadIdx.x; j < p.nparts; j += kFinalThreads) sacc += p.partials[(size_t)j * 32 + colp];
+  red[threadIdx.x] = sacc;
+  __syncthreads();
+  for (int o = kFinalThreads / 2; o > 0; o >>= 1) {
+    if ((int)threadIdx.x < o) red[threadIdx.x] += red[threadIdx.x + o];
+    __syncthreads();
+  }
+  if (threadIdx.x == 0) {
+    if (v < kBwR) p.grad_bias[v] = red[0];
+    else p.grad_alpha[v - kBwR] = red[0];
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_bw_planes(const BwPlaneParams& pp, cudaStream_t s) {
+  const long long total = (long long)pp.nslab * kBwNS * pp.P * kBwRp * 64;
+  int blocks = (int)((total + 255) / 256);
+  if (blocks > 4096) blocks = 4096;
+  if (blocks < 1) blocks = 1;
+  bw_planes_kernel<<<blocks, 256, 0, s>>>(pp);
+  return cudaGetLastError();
+}
+
+cudaError_t bw_token_blocks(int* blocks) {
+  int dev = 0, sms = 0, per_sm = 0;
+  cudaError_t e;
+  if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
+  if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
+  if ((e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, bw_token_kernel, kBwTokenWarps * 32, 0)) !=
+      cudaSuccess)
+    return e;
+  long long b = (long long)sms * (per_sm > 0 ? per_sm : 1);
+  if (b > kBwMaxTokenBlocks) b = kBwMaxTokenBlocks;
+  *blocks = (int)b;
+  return cudaSuccess;
+}
+
+cudaError_t launch_bw_token(const BwTokenParams& p, int blocks, cudaStream_t s) {
+  bw_token_kernel<<<blocks, kBwTokenWarps * 32, 0, s>>>(p);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_bw_main(const BwMainLaunch& L, cudaStream_t s) {
+  const void* k = nullptr;
+  if (L.P == 3) k = L.has_gxp ? reinterpret_cast<const void*>(&bw_main_kernel<3, true>)
+                              : reinterpret_cast<const void*>(&bw_main_kernel<3, false>);
+  else k = L.has_gxp ? reinterpret_cast<const void*>(&bw_main_kernel<2, true>)
+                     : reinterpret_cast<const void*>(&bw_main_kernel<2, false>);
+  cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)L.smem_bytes);
+  if (e != cudaSuccess) return e;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(L.grid, 1, 1);
+  cfg.blockDim = dim3(kMainThreads, 1, 1);
+  cfg.dynamicSmemBytes = L.smem_bytes;
+  cfg.stream = s;
+  int ntiles = L.ntiles, nslab = L.nslab, nq = L.nq, stages = L.stages;
+  const __nv_bfloat16* planes = L.planes;
+  const uint8_t* tiles = L.tiles;
+  float* pieces = L.pieces;
+  uint32_t* err = L.err;
+  void* args[] = {const_cast<CUtensorMap*>(&L.tmap_x), const_cast<CUtensorMap*>(&L.tmap_gin),
+                  const_cast<CUtensorMap*>(&L.tmap_gx), const_cast<CUtensorMap*>(&L.tmap_gxp),
+                  &planes, &tiles, &pieces, &err, &ntiles, &nslab, &nq, &stages};
+  return cudaLaunchKernelExC(&cfg, k, args);
+}
+
+cudaError_t launch_bw_final(const BwFinalParams& p, cudaStream_t s) {
+  const int K = kBwNS * p.D;
+  const int col_blocks = (K + kFinalThreads - 1) / kFinalThreads;
+  const int blocks = col_blocks + kBwR + 3;
+  bw_final_kernel<<<blocks, kFinalThreads, 0, s>>>(p, col_blocks);
+  return cudaGetLastError();
+}
+
+}  // namespace mhc

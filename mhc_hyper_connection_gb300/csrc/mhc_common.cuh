@@ -421,4 +421,89 @@ struct GwLaunch {
 cudaError_t gw_forward_capacity(int n, int R, int P, size_t smem_bytes, int* max_ctas);
 cudaError_t launch_gw_forward(const GwLaunch& L, cudaStream_t s);
 
+// ---------------------------------------------------------------------------
+// Backward of the pre-mapping (n = 4, three gates).  Four launches:
+//  1. planes: phi . gamma per 64-column slab as P bf16 planes, row-padded to
+//     kBwRp rows, swizzled for the tensor core; zeroes the header;
+//  2. token stage: per token the gate and Sinkhorn backward -> G = H_mix_grad
+//     (as P bf16 planes in a per-64-token tile record) and the RMS factor;
+//     per-warp partial sums of grad_alpha / grad_bias;
+//  3. main: per (slab, token tile) grad_x = gx3 + G phi' + c x (+ grad_x_post)
+//     and x^T G accumulated over the tiles of a unit (slab, token chunk);
+//  4. final: grad_phi / grad_gamma from the run partials, grad_alpha /
+//     grad_bias from the warp partials, all in fixed order.
+constexpr int kBwNS = 4, kBwR = 24, kBwRp = 32;   // streams, gate rows, rows padded to the MMA K step
+constexpr int kBwTile = 64;                        // tokens per tile
+constexpr int kBwPlaneBytes = kBwRp * 128;         // one plane: kBwRp rows of 64 bf16
+constexpr int kBwScalarBytes = kBwTile * 32;       // per token: hPre[4], RMS factor, 3 pad
+constexpr int kBwMaxMainGrid = 160;                // main-kernel CTAs the workspace is sized for
+constexpr int kBwMaxTokenBlocks = 1024;            // token-stage blocks (8 warps each)
+constexpr int kBwTokenWarps = 8;
+
+__host__ __device__ constexpr int bw_slab_bytes(int P) { return kBwNS * P * kBwPlaneBytes; }
+__host__ __device__ constexpr int bw_tile_rec_bytes(int P) { return P * kBwPlaneBytes + kBwScalarBytes; }
+__host__ __device__ constexpr int bw_mt_cols(int P) { return P * kBwRp; }
+__host__ __device__ constexpr int bw_stage_bytes(int P, bool gxp) {
+  return kBwNS * kBwTile * 128 * (gxp ? 2 : 1) + kBwTile * 128 + bw_tile_rec_bytes(P);
+}
+constexpr int kBwTailBytes = 1024;
+
+constexpr int kBwMaxChunks = 8;                    // token chunks per slab (units = slabs x chunks)
+__host__ __device__ constexpr size_t bw_piece_bytes() { return (size_t)kBwRp * kBwNS * 64 * 4; }
+
+struct BwPlaneParams {
+  const float* phi;        // [R, nD]
+  const float* gamma;      // [nD] or null
+  __nv_bfloat16* planes;   // [nslab][NS][P][kBwRp][64], swizzled
+  uint32_t* hdr;           // workspace header (zeroed)
+  int D, nslab, P, tf32;
+};
+
+struct BwTokenParams {
+  int T, D, ntiles, num_iters, P, tf32;
+  float hc_eps;
+  const __nv_bfloat16* x;      // [T, n, D]
+  const __nv_bfloat16* g_in;   // [T, D]
+  const float* g_post;         // [T, n]
+  const float* g_res;          // [T, n, n]
+  const float* inv_rms;        // [T]
+  const float* h_mix;          // [T, R]
+  const float* h_pre;          // [T, n]
+  const float* h_post;         // [T, n]
+  const float* sum_out;        // [2I, T, n] or null
+  const float* norm_out;       // [2I, T, n, n] or null
+  const float* alpha;          // [3]
+  uint8_t* tiles;              // [ntiles] tile records
+  float* partials;             // [blocks * 8][32]
+};
+
+struct BwMainLaunch {
+  CUtensorMap tmap_x, tmap_gin, tmap_gx, tmap_gxp;
+  const __nv_bfloat16* planes;
+  const uint8_t* tiles;
+  float* pieces;               // [nslab * nq][kBwRp][NS * 64]: x^T G per unit, planes summed
+  uint32_t* err;
+  int T, D, ntiles, nslab, nq, P, stages, has_gxp, grid;
+  size_t smem_bytes;
+};
+
+struct BwFinalParams {
+  int D, nslab, nq;
+  const float* pieces;
+  const float* phi;                // [R, nD]
+  const float* gamma;              // [nD] or null
+  float* grad_phi;                 // [R, nD]
+  float* grad_gamma;               // [nD] or null
+  const float* partials;           // [nparts][32]
+  int nparts;
+  float* grad_alpha;               // [3]
+  float* grad_bias;                // [R]
+};
+
+cudaError_t launch_bw_planes(const BwPlaneParams& p, cudaStream_t s);
+cudaError_t bw_token_blocks(int* blocks);      // token-stage grid for this device
+cudaError_t launch_bw_token(const BwTokenParams& p, int blocks, cudaStream_t s);
+cudaError_t launch_bw_main(const BwMainLaunch& L, cudaStream_t s);
+cudaError_t launch_bw_final(const BwFinalParams& p, cudaStream_t s);
+
 }  // namespace mhc

@@ -14,6 +14,7 @@
 #include "mhc_common.cuh"
 #include "../../include/mhc_pre.h"
 #include "../../include/mhc_post.h"
+#include "../../include/mhc_pre_backward.h"
 
 struct mhc_pre_s {
   mhc_pre_config cfg;
@@ -608,5 +609,218 @@ mhc_status_t mhc_post_run(int64_t T, int64_t n, int64_t D, const void* x, const 
 }
 
 void mhc_pre_destroy(mhc_pre_t h) { delete h; }
+
+}  // extern "C"
+
+// ---------------------------------------------------------------- backward
+namespace {
+
+// Backward workspace: [0, 256) header | phi . gamma planes per slab | tile
+// records (G planes + hPre + RMS factor) | x^T G partial sums of the work
+// units (slab, token chunk) | token-stage partial sums.
+struct BwLayout {
+  size_t planes, tiles, pieces, partials, total;
+};
+
+BwLayout bw_layout(const mhc_pre_s* h, int64_t T) {
+  const int P = h->P;
+  const size_t nslab = (size_t)(h->cfg.D / 64);
+  const size_t ntiles = (size_t)((T + mhc::kBwTile - 1) / mhc::kBwTile);
+  auto up = [](size_t v) { return (v + 255) & ~size_t(255); };
+  BwLayout L;
+  L.planes = mhc::kWsHeader;
+  L.tiles = L.planes + up(nslab * (size_t)mhc::bw_slab_bytes(P));
+  L.pieces = L.tiles + up(ntiles * (size_t)mhc::bw_tile_rec_bytes(P));
+  L.partials = L.pieces + up(nslab * mhc::kBwMaxChunks * mhc::bw_piece_bytes());
+  L.total = L.partials + up((size_t)mhc::kBwMaxTokenBlocks * mhc::kBwTokenWarps * 32 * sizeof(float));
+  return L;
+}
+
+mhc_status_t bw_scope(const mhc_pre_s* h) {
+  if (h->cfg.alpha_len != 3) return fail(MHC_ERR_PARAM_INVALID, "the backward needs a three-gate handle (alpha_len 3)");
+  if (h->cfg.n != 4) return fail(MHC_ERR_PARAM_INVALID, "the backward supports n = 4 (got %lld)", (long long)h->cfg.n);
+  if (h->cfg.D % 64 != 0)
+    return fail(MHC_ERR_PARAM_INVALID, "the backward needs D a multiple of 64 (got %lld)", (long long)h->cfg.D);
+  return MHC_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+mhc_status_t mhc_pre_backward_workspace_size(mhc_pre_t h, int64_t T, size_t* bytes) {
+  g_last_error[0] = 0;
+  if (!h || !bytes) return fail(MHC_ERR_NULLPTR, "handle and bytes must be non-NULL");
+  if (T < 0 || T > (int64_t(1) << 30)) return fail(MHC_ERR_PARAM_INVALID, "T must be in [0, 2^30]");
+  const mhc_status_t sc = bw_scope(h);
+  if (sc != MHC_OK) return sc;
+  *bytes = (T == 0) ? 0 : bw_layout(h, T).total;
+  return MHC_OK;
+}
+
+mhc_status_t mhc_pre_backward_run(mhc_pre_t h, const mhc_pre_bwd_args* a, void* stream) {
+  g_last_error[0] = 0;
+  if (!h || !a) return fail(MHC_ERR_NULLPTR, "handle and args must be non-NULL");
+  const mhc_status_t sc = bw_scope(h);
+  if (sc != MHC_OK) return sc;
+  const int64_t T = a->T;
+  if (T < 0 || T > (int64_t(1) << 30)) return fail(MHC_ERR_PARAM_INVALID, "T must be in [0, 2^30]");
+  if (T == 0) return MHC_OK;
+  if (!a->x || !a->phi || !a->alpha || !a->grad_h_in || !a->grad_h_post || !a->grad_h_res || !a->inv_rms ||
+      !a->h_mix || !a->h_pre || !a->h_post || !a->grad_x || !a->grad_phi || !a->grad_alpha || !a->grad_bias ||
+      !a->workspace)
+    return fail(MHC_ERR_NULLPTR, "a required tensor or the workspace is NULL");
+  if ((a->sum_out == nullptr) != (a->norm_out == nullptr))
+    return fail(MHC_ERR_PARAM_INVALID, "sum_out and norm_out go together (both or neither)");
+  if ((a->gamma == nullptr) != (a->grad_gamma == nullptr))
+    return fail(MHC_ERR_PARAM_INVALID, "grad_gamma is required exactly when gamma is given");
+  const void* v16[] = {a->x, a->grad_h_in, a->grad_x, a->grad_x_post, a->workspace};
+  for (const void* p : v16)
+    if (p && !aligned(p, 16)) return fail(MHC_ERR_PARAM_INVALID, "bf16 tensors and the workspace must be 16-byte aligned");
+  const void* v4[] = {a->phi, a->alpha, a->gamma, a->grad_h_post, a->grad_h_res, a->inv_rms, a->h_mix, a->h_pre,
+                      a->h_post, a->sum_out, a->norm_out, a->grad_phi, a->grad_alpha, a->grad_bias, a->grad_gamma};
+  for (const void* p : v4)
+    if (p && !aligned(p, 4)) return fail(MHC_ERR_PARAM_INVALID, "fp32 tensors must be 4-byte aligned");
+  const BwLayout L = bw_layout(h, T);
+  if (a->workspace_bytes < L.total)
+    return fail(MHC_ERR_PARAM_INVALID, "workspace too small: %zu bytes given, %zu needed", a->workspace_bytes, L.total);
+
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return fail(MHC_ERR_RUNTIME, "no CUDA device");
+  const DeviceInfo di = device_info(dev);
+  if (!di.ok) return fail(MHC_ERR_RUNTIME, "device %d is not an sm_103 GPU", dev);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const int n = (int)h->cfg.n, D = (int)h->cfg.D, P = h->P;
+  const int nslab = D / 64;
+  const int ntiles = (int)((T + mhc::kBwTile - 1) / mhc::kBwTile);
+  uint8_t* ws = static_cast<uint8_t*>(a->workspace);
+  uint32_t* err = reinterpret_cast<uint32_t*>(ws);
+  __nv_bfloat16* planes = reinterpret_cast<__nv_bfloat16*>(ws + L.planes);
+  uint8_t* tiles = ws + L.tiles;
+  float* pieces = reinterpret_cast<float*>(ws + L.pieces);
+  float* partials = reinterpret_cast<float*>(ws + L.partials);
+
+  // main-kernel geometry
+  const bool gxp = a->grad_x_post != nullptr;
+  const size_t fixed = (size_t)mhc::bw_slab_bytes(P) + mhc::kBwTailBytes + 1024;
+  const size_t stage = (size_t)mhc::bw_stage_bytes(P, gxp);
+  int stages = (int)((di.max_smem - fixed) / stage);
+  if (stages > 4) stages = 4;
+  if (stages < 2) return fail(MHC_ERR_RUNTIME, "not enough shared memory for the backward pipeline");
+  // Token chunks per slab: the count (at most kBwMaxChunks and the tile
+  // count) whose units fill whole waves of the grid best; ties go to fewer
+  // chunks (fewer partial sums).
+  long long grid = di.sms < mhc::kBwMaxMainGrid ? di.sms : mhc::kBwMaxMainGrid;
+  int nq = 1;
+  double best = -1.0;
+  for (int q = 1; q <= mhc::kBwMaxChunks && q <= ntiles; ++q) {
+    const long long units = (long long)nslab * q;
+    const long long waves = (units + grid - 1) / grid;
+    const double eff = (double)units / (double)(waves * grid);
+    if (eff > best + 1e-9) {
+      best = eff;
+      nq = q;
+    }
+  }
+  if (grid > (long long)nslab * nq) grid = (long long)nslab * nq;
+
+  mhc::BwMainLaunch M;
+  {
+    const uint64_t dims[4] = {64, (uint64_t)T, (uint64_t)nslab, (uint64_t)n};
+    const uint64_t strides[3] = {(uint64_t)n * D * 2, 128, (uint64_t)D * 2};
+    const uint32_t box[4] = {64, (uint32_t)mhc::kBwTile, 1, (uint32_t)n};
+    if (!encode_4d(&M.tmap_x, a->x, dims, strides, box) || !encode_4d(&M.tmap_gx, a->grad_x, dims, strides, box) ||
+        !encode_4d(&M.tmap_gxp, gxp ? a->grad_x_post : a->x, dims, strides, box))
+      return fail(MHC_ERR_RUNTIME, "encoding the x / grad_x tensor maps failed");
+    const uint64_t gd[3] = {64, (uint64_t)T, (uint64_t)nslab};
+    const uint64_t gs[2] = {(uint64_t)D * 2, 128};
+    const uint32_t gb[3] = {64, (uint32_t)mhc::kBwTile, 1};
+    if (!encode_3d(&M.tmap_gin, a->grad_h_in, gd, gs, gb))
+      return fail(MHC_ERR_RUNTIME, "encoding the grad_h_in tensor map failed");
+  }
+  M.planes = planes;
+  M.tiles = tiles;
+  M.pieces = pieces;
+  M.err = err;
+  M.T = (int)T;
+  M.D = D;
+  M.ntiles = ntiles;
+  M.nslab = nslab;
+  M.P = P;
+  M.stages = stages;
+  M.has_gxp = gxp ? 1 : 0;
+  M.grid = (int)grid;
+  M.nq = nq;
+  M.smem_bytes = fixed + (size_t)stages * stage;
+
+  mhc::BwPlaneParams pp;
+  pp.phi = a->phi;
+  pp.gamma = a->gamma;
+  pp.planes = planes;
+  pp.hdr = err;
+  pp.D = D;
+  pp.nslab = nslab;
+  pp.P = P;
+  pp.tf32 = (h->cfg.impl_mode == MHC_IMPL_TF32) ? 1 : 0;
+
+  mhc::BwTokenParams tp;
+  tp.T = (int)T;
+  tp.D = D;
+  tp.ntiles = ntiles;
+  tp.num_iters = (int)h->cfg.num_iters;
+  tp.P = P;
+  tp.tf32 = pp.tf32;
+  tp.hc_eps = (float)h->cfg.hc_eps;
+  tp.x = static_cast<const __nv_bfloat16*>(a->x);
+  tp.g_in = static_cast<const __nv_bfloat16*>(a->grad_h_in);
+  tp.g_post = a->grad_h_post;
+  tp.g_res = a->grad_h_res;
+  tp.inv_rms = a->inv_rms;
+  tp.h_mix = a->h_mix;
+  tp.h_pre = a->h_pre;
+  tp.h_post = a->h_post;
+  tp.sum_out = a->sum_out;
+  tp.norm_out = a->norm_out;
+  tp.alpha = a->alpha;
+  tp.tiles = tiles;
+  tp.partials = partials;
+  int tblocks = 0;
+  if (mhc::bw_token_blocks(&tblocks) != cudaSuccess)
+    return fail(MHC_ERR_RUNTIME, "token-stage occupancy query failed: %s", cudaGetErrorString(cudaGetLastError()));
+  const long long tmax = ((long long)ntiles * mhc::kBwTile + mhc::kBwTokenWarps - 1) / mhc::kBwTokenWarps;
+  if (tblocks > tmax) tblocks = (int)tmax;
+
+  mhc::BwFinalParams fp;
+  fp.D = D;
+  fp.nslab = nslab;
+  fp.nq = nq;
+  fp.pieces = pieces;
+  fp.phi = a->phi;
+  fp.gamma = a->gamma;
+  fp.grad_phi = a->grad_phi;
+  fp.grad_gamma = a->grad_gamma;
+  fp.partials = partials;
+  fp.nparts = tblocks * mhc::kBwTokenWarps;
+  fp.grad_alpha = a->grad_alpha;
+  fp.grad_bias = a->grad_bias;
+
+  cudaError_t e;
+  if ((e = mhc::launch_bw_planes(pp, s)) != cudaSuccess)
+    return fail(MHC_ERR_RUNTIME, "backward plane launch failed: %s", cudaGetErrorString(e));
+  if ((e = mhc::launch_bw_token(tp, tblocks, s)) != cudaSuccess)
+    return fail(MHC_ERR_RUNTIME, "backward token-stage launch failed: %s", cudaGetErrorString(e));
+  if (h->ev_before) cudaEventRecord(h->ev_before, s);
+  if ((e = mhc::launch_bw_main(M, s)) != cudaSuccess)
+    return fail(MHC_ERR_RUNTIME, "backward main launch failed: %s", cudaGetErrorString(e));
+  if (h->ev_after) cudaEventRecord(h->ev_after, s);
+  if ((e = mhc::launch_bw_final(fp, s)) != cudaSuccess)
+    return fail(MHC_ERR_RUNTIME, "backward final launch failed: %s", cudaGetErrorString(e));
+  h->last_cluster = 1;
+  h->last_grid = (int)grid;
+  h->last_stages = stages;
+  h->last_ystages = tblocks;
+  h->last_kernel = "bw_main_kernel";
+  return MHC_OK;
+}
 
 }  // extern "C"

@@ -156,6 +156,30 @@ __device__ __forceinline__ void st_global_v4_hint(void* ptr, uint4 v, uint64_t p
                "r"(v.z), "r"(v.w), "l"(policy)
                : "memory");
 }
+// Tiled store shared -> global of a 4-D box (rows outside the tensor are
+// not written); completion tracked by bulk groups.
+__device__ __forceinline__ void tma_store_4d(const CUtensorMap* map, const void* src, int c0, int c1, int c2,
+                                             int c3) {
+  asm volatile("cp.async.bulk.tensor.4d.global.shared::cta.bulk_group [%0, {%2, %3, %4, %5}], [%1];" ::"l"(
+                   reinterpret_cast<uint64_t>(map)),
+               "r"(smem_u32(src)), "r"(c0), "r"(c1), "r"(c2), "r"(c3)
+               : "memory");
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+// Wait until at most N committed bulk groups still read shared memory.
+template <int N>
+__device__ __forceinline__ void bulk_wait_read() {
+  asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(N) : "memory");
+}
+template <int N>
+__device__ __forceinline__ void bulk_wait() {
+  asm volatile("cp.async.bulk.wait_group %0;" ::"n"(N) : "memory");
+}
+// Make this thread's generic-proxy shared-memory writes visible to the bulk
+// copy engine.
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
 __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap* map) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }
@@ -179,10 +203,28 @@ __device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
   return d;
 }
 
+// MN-major operand with 128-byte swizzle: each 128-byte row holds 64
+// consecutive M (or N) elements, rows are consecutive K; 8-row groups are
+// 1024 bytes apart and the next 64 M elements start `lbo` bytes further.
+__device__ __forceinline__ uint64_t sw128_desc_mn(uint32_t saddr, uint32_t lbo) {
+  uint64_t d = 0;
+  d |= static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);   // start address
+  d |= static_cast<uint64_t>((lbo >> 4) & 0x3FFFu) << 16; // next 64 M/N elements
+  d |= static_cast<uint64_t>(1024 >> 4) << 32;            // next 8 K rows
+  d |= static_cast<uint64_t>(1) << 46;                    // descriptor version
+  d |= static_cast<uint64_t>(2) << 61;                    // 128-byte swizzle
+  return d;
+}
+
 // kind::f16 instruction descriptor: bf16 x bf16 -> fp32, both K-major.
 __host__ __device__ constexpr uint32_t idesc_bf16(int M, int N) {
   return (1u << 4) | (1u << 7) | (1u << 10) | (static_cast<uint32_t>(N >> 3) << 17) |
          (static_cast<uint32_t>(M >> 4) << 24);
+}
+
+// The same with the operands' major-ness chosen: bit 15 A, bit 16 B (1 = MN-major).
+__host__ __device__ constexpr uint32_t idesc_bf16_major(int M, int N, bool a_mn, bool b_mn) {
+  return idesc_bf16(M, N) | (a_mn ? (1u << 15) : 0u) | (b_mn ? (1u << 16) : 0u);
 }
 
 __device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
@@ -267,6 +309,19 @@ __device__ __forceinline__ bool role_all(bool ok) {
 
 // Offset of 16-byte column c of row r in a 128-byte-swizzled tile.
 __device__ __forceinline__ int sw128(int r, int c) { return r * 128 + ((c ^ (r & 7)) << 4); }
+
+// 8 consecutive fp32 columns of this warp's 32 TMEM lanes (load + wait).
+__device__ __forceinline__ void tmem_ld8(uint32_t taddr, float (&v)[8]) {
+  uint32_t r[8];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];\n\t"
+      "tcgen05.wait::ld.sync.aligned;"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7])
+      : "r"(taddr)
+      : "memory");
+#pragma unroll
+  for (int i = 0; i < 8; ++i) v[i] = __uint_as_float(r[i]);
+}
 
 // 32 consecutive fp32 columns of this warp's 32 TMEM lanes (load + wait).
 __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {

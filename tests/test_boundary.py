@@ -11,7 +11,7 @@ import mhc_hyper_connection_gb300 as mp
 from mhc_hyper_connection_gb300 import build as mbuild
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
-HEADERS = [os.path.join(ROOT, "include", h) for h in ("mhc_pre.h", "mhc_post.h")]
+HEADERS = [os.path.join(ROOT, "include", h) for h in ("mhc_pre.h", "mhc_post.h", "mhc_pre_backward.h")]
 
 
 @pytest.fixture(scope="module")
@@ -32,7 +32,8 @@ def test_header_declares_the_api():
     names = declared_functions()
     for need in ("mhc_pre_create", "mhc_pre_workspace_size", "mhc_pre_run", "mhc_pre_status",
                  "mhc_pre_destroy", "mhc_pre_config_default", "mhc_pre_status_string",
-                 "mhc_pre_last_error", "mhc_post_run"):
+                 "mhc_pre_last_error", "mhc_post_run", "mhc_pre_backward_workspace_size",
+                 "mhc_pre_backward_run"):
         assert need in names
 
 
@@ -45,6 +46,7 @@ def test_struct_layouts_match_header():
     # Field order/sizes in the binding mirror the header (x86-64 and aarch64 LP64).
     assert ctypes.sizeof(mp.MhcPreConfig) == 8 + 8 + 4 + 4 + 8 + 8 + 4 + 4
     assert ctypes.sizeof(mp.MhcPreArgs) == 8 + 15 * 8 + 8
+    assert ctypes.sizeof(mp.MhcPreBwdArgs) == 8 + 20 * 8 + 8
 
 
 def test_defaults(lib):
@@ -199,3 +201,81 @@ def test_post_host_validation(lib):
     assert call(x=A + 8) == mp.MHC_ERR_PARAM_INVALID
     assert call(out=A + 2) == mp.MHC_ERR_PARAM_INVALID
     assert call(post=A + 2) == mp.MHC_ERR_PARAM_INVALID
+
+
+# ------------------------------------------------------------------ backward
+
+def _bwd_args(T=64, **over):
+    a = mp.MhcPreBwdArgs()
+    A = 1 << 20          # aligned fake device address, never dereferenced
+    a.T = T
+    for k in ("x", "phi", "alpha", "grad_h_in", "grad_h_post", "grad_h_res", "inv_rms", "h_mix", "h_pre",
+              "h_post", "sum_out", "norm_out", "grad_x", "grad_phi", "grad_alpha", "grad_bias"):
+        setattr(a, k, A)
+    a.workspace = A
+    a.workspace_bytes = 1 << 34
+    for k, v in over.items():
+        setattr(a, k, v)
+    return a
+
+
+def test_backward_workspace_size(lib):
+    h = _handle(D=7168)
+    st, n = mp.mhc_pre_backward_workspace_size(h, 0)
+    assert st == mp.MHC_OK and n == 0
+    st, n = mp.mhc_pre_backward_workspace_size(h, 100)
+    up = lambda v: (v + 255) // 256 * 256
+    planes = up(112 * 4 * 3 * 32 * 128)
+    tiles = up(2 * (3 * 32 * 128 + 64 * 32))
+    pieces = up(112 * 8 * 32 * 256 * 4)
+    parts = up(1024 * 8 * 32 * 4)
+    assert st == mp.MHC_OK and n == 256 + planes + tiles + pieces + parts
+    assert mp.mhc_pre_backward_workspace_size(h, -1)[0] == mp.MHC_ERR_PARAM_INVALID
+    mp.mhc_pre_destroy(h)
+    h = _handle(D=7168, impl_mode=1)
+    st, n2 = mp.mhc_pre_backward_workspace_size(h, 100)
+    assert st == mp.MHC_OK and n2 < n
+    mp.mhc_pre_destroy(h)
+
+
+@pytest.mark.parametrize("cfg", [dict(n=6), dict(n=8), dict(alpha_len=2), dict(D=96)])
+def test_backward_scope(lib, cfg):
+    h = _handle(**cfg)
+    assert mp.mhc_pre_backward_workspace_size(h, 64)[0] == mp.MHC_ERR_PARAM_INVALID
+    assert mp.mhc_pre_backward_run(h, _bwd_args()) == mp.MHC_ERR_PARAM_INVALID
+    mp.mhc_pre_destroy(h)
+
+
+@pytest.mark.parametrize("field", ["x", "phi", "alpha", "grad_h_in", "grad_h_post", "grad_h_res", "inv_rms",
+                                   "h_mix", "h_pre", "h_post", "grad_x", "grad_phi", "grad_alpha",
+                                   "grad_bias", "workspace"])
+def test_backward_null_required(lib, field):
+    h = _handle(D=256)
+    assert mp.mhc_pre_backward_run(h, _bwd_args(**{field: None})) == mp.MHC_ERR_NULLPTR
+    mp.mhc_pre_destroy(h)
+
+
+def test_backward_groups_alignment_workspace(lib):
+    h = _handle(D=256)
+    A = 1 << 20
+    assert mp.mhc_pre_backward_run(h, _bwd_args(sum_out=None)) == mp.MHC_ERR_PARAM_INVALID
+    assert mp.mhc_pre_backward_run(h, _bwd_args(norm_out=None)) == mp.MHC_ERR_PARAM_INVALID
+    assert mp.mhc_pre_backward_run(h, _bwd_args(gamma=A)) == mp.MHC_ERR_PARAM_INVALID
+    assert mp.mhc_pre_backward_run(h, _bwd_args(grad_gamma=A)) == mp.MHC_ERR_PARAM_INVALID
+    assert mp.mhc_pre_backward_run(h, _bwd_args(x=A + 8)) == mp.MHC_ERR_PARAM_INVALID
+    assert mp.mhc_pre_backward_run(h, _bwd_args(grad_x=A + 2)) == mp.MHC_ERR_PARAM_INVALID
+    assert mp.mhc_pre_backward_run(h, _bwd_args(grad_x_post=A + 4)) == mp.MHC_ERR_PARAM_INVALID
+    assert mp.mhc_pre_backward_run(h, _bwd_args(h_mix=A + 2)) == mp.MHC_ERR_PARAM_INVALID
+    assert mp.mhc_pre_backward_run(h, _bwd_args(workspace_bytes=1000)) == mp.MHC_ERR_PARAM_INVALID
+    assert mp.mhc_pre_backward_run(h, _bwd_args(T=-1)) == mp.MHC_ERR_PARAM_INVALID
+    assert mp.mhc_pre_backward_run(h, _bwd_args(T=0, x=None, workspace=None)) == mp.MHC_OK
+    mp.mhc_pre_destroy(h)
+
+
+def test_backward_without_gpu_fails_loudly(lib):
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    h = _handle(D=256)
+    assert mp.mhc_pre_backward_run(h, _bwd_args()) == mp.MHC_ERR_RUNTIME
+    mp.mhc_pre_destroy(h)
