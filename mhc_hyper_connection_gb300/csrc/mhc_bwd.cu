@@ -7,9 +7,11 @@
 // "aclnnMhcPreSinkhorn 接口与 MhcPreSinkhorn 实现剖析" §3.2 carried back first.
 // How it is laid out on the GPU is this file's own design:
 //
-//  * Token stage (one warp per token): H_pre_grad = grad_h_in . x over the
-//    whole row (the only full-row reduction of the backward), the Sinkhorn
-//    backward on 16 lanes from the saved steps, the gate backward, and
+//  * Row dot (one CTA per SM): H_pre_grad = grad_h_in . x over the whole
+//    row (the only full-row reduction of the backward), whole token rows
+//    brought in by bulk copy.
+//  * Token stage (one warp per token): the Sinkhorn backward on 16 lanes
+//    from the saved steps, the gate backward, and
 //    G = H_mix_grad with the RMS factor c = -inv_rms_grad invRms^3 / (nD).
 //    G goes out as exact bf16 planes in a per-64-token tile record laid out
 //    for the tensor core, next to hPre and c of the tile's tokens.
@@ -55,6 +57,12 @@ __device__ __forceinline__ float plane_part(float v, int plane, int tf32) {
   return bf16_round(rem - mid);           // rem - mid exact
 }
 
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+
 // Byte offset of element (row, col) (col < 64) in a 128-byte-swizzled tile.
 __device__ __forceinline__ uint32_t swz(int row, int col) {
   return (uint32_t)(row * 128 + ((((col >> 3) ^ (row & 7)) << 4) | ((col & 7) << 1)));
@@ -87,15 +95,112 @@ __global__ void __launch_bounds__(256) bw_planes_kernel(BwPlaneParams pp) {
   }
 }
 
-// =============================================================== token stage
-constexpr int kSinkChunk = 16;   // saved Sinkhorn steps staged per round
-constexpr int kVec = 3;          // 16-byte column vectors per lane in flight (x 4 streams + grad_h_in each)
+// ================================================================== row dot
+// H_pre_grad[t][i] = sum_d grad_h_in[t][d] x[t][i][d] (stage 3.1).  Token
+// rows of x (n*D contiguous) and grad_h_in (D contiguous) arrive whole by
+// bulk copy into a ring of shared-memory stages (tps tokens each); eight
+// warps form the four dot products of each token, reduced in a fixed order.
+constexpr int kRdWarps = 8;
+constexpr int kRdThreads = (kRdWarps + 1) * 32;   // + one producer warp
+constexpr int kRdMaxStages = 4;
 
-__device__ __forceinline__ float warp_sum(float v) {
+struct RdTail {
+  uint64_t full[kRdMaxStages], empty[kRdMaxStages];
+  uint32_t abort;
+  float red[2][kRdWarps][kBwNS];
+};
+
+__global__ void __launch_bounds__(kRdThreads, 1) bw_rowdot_kernel(BwRowdotParams p) {
+  constexpr int NS = kBwNS;
+  extern __shared__ __align__(128) uint8_t rd_smem[];
+  const size_t xrow = (size_t)NS * p.D * 2, grow = (size_t)p.D * 2;
+  const size_t stage_bytes = (size_t)p.tps * (xrow + grow);
+  RdTail* tail = reinterpret_cast<RdTail*>(rd_smem + (size_t)p.stages * stage_bytes);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int ngroups = (p.T + p.tps - 1) / p.tps;
+  Ctl ctl{&tail->abort, p.err};
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < p.stages; ++s) {
+      mbar_init(&tail->full[s], 1);
+      mbar_init(&tail->empty[s], kRdWarps);
+    }
+    tail->abort = 0u;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  __syncthreads();
+  if (warp == kRdWarps) {
+    if (lane == 0) {
+      const uint64_t keep = policy_evict_last();
+      int s = 0;
+      uint32_t ph = 0;
+      long long iss = 0;
+      for (int gi = blockIdx.x; gi < ngroups; gi += gridDim.x) {
+        const int t0 = gi * p.tps, cnt = min(p.tps, p.T - t0);
+        if (!wait_bar<false>(&tail->empty[s], ph ^ 1u, ctl, kErrWaitTimeout)) break;
+        uint8_t* st = rd_smem + (size_t)s * stage_bytes;
+        mbar_expect_tx(&tail->full[s], (uint32_t)((size_t)cnt * (xrow + grow)));
+        bulk_load_hint(st, p.x + (size_t)t0 * NS * p.D, (uint32_t)((size_t)cnt * xrow), &tail->full[s], keep);
+        bulk_load_hint(st + (size_t)p.tps * xrow, p.g_in + (size_t)t0 * p.D, (uint32_t)((size_t)cnt * grow),
+                       &tail->full[s], keep);
+        ++iss;
+        if (++s == p.stages) { s = 0; ph ^= 1u; }
+      }
+      for (long long q = 0; q < (iss < p.stages ? iss : p.stages); ++q) {
+        if (--s < 0) { s = p.stages - 1; ph ^= 1u; }
+        mbar_drain(&tail->full[s], ph);
+      }
+    }
+    return;
+  }
+  const int nv = p.D >> 3;                 // 16-byte vectors per stream row
+  int s = 0, par = 0;
+  uint32_t ph = 0;
+  for (int gi = blockIdx.x; gi < ngroups; gi += gridDim.x) {
+    const int t0 = gi * p.tps, cnt = min(p.tps, p.T - t0);
+    // all compute warps leave together (they meet at a named barrier below)
+    if (!role_all<1, kRdWarps * 32>(wait_bar<false>(&tail->full[s], ph, ctl, kErrWaitTimeout))) break;
+    const uint8_t* st = rd_smem + (size_t)s * stage_bytes;
+    for (int k = 0; k < cnt; ++k, par ^= 1) {
+      const uint4* xs = reinterpret_cast<const uint4*>(st + (size_t)k * xrow);
+      const uint4* gs = reinterpret_cast<const uint4*>(st + (size_t)p.tps * xrow + (size_t)k * grow);
+      float acc[NS] = {0.0f, 0.0f, 0.0f, 0.0f};
+      for (int v = threadIdx.x; v < nv; v += kRdWarps * 32) {
+        const uint4 gv = gs[v];
+        const __nv_bfloat162* g2 = reinterpret_cast<const __nv_bfloat162*>(&gv);
 #pragma unroll
-  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-  return v;
+        for (int i = 0; i < NS; ++i) {
+          const uint4 xv = xs[(size_t)i * nv + v];
+          const __nv_bfloat162* x2 = reinterpret_cast<const __nv_bfloat162*>(&xv);
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const float2 gf = __bfloat1622float2(g2[e]), xf = __bfloat1622float2(x2[e]);
+            acc[i] = fmaf(gf.x, xf.x, acc[i]);
+            acc[i] = fmaf(gf.y, xf.y, acc[i]);
+          }
+        }
+      }
+#pragma unroll
+      for (int i = 0; i < NS; ++i) acc[i] = warp_sum(acc[i]);
+      if (lane == 0) {
+#pragma unroll
+        for (int i = 0; i < NS; ++i) tail->red[par][warp][i] = acc[i];
+      }
+      role_sync<1, kRdWarps * 32>();
+      if (threadIdx.x < NS) {
+        float tot = 0.0f;
+#pragma unroll
+        for (int w = 0; w < kRdWarps; ++w) tot += tail->red[par][w][threadIdx.x];
+        p.hg[(size_t)(t0 + k) * NS + threadIdx.x] = tot;
+      }
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&tail->empty[s]);
+    if (++s == p.stages) { s = 0; ph ^= 1u; }
+  }
 }
+
+// =============================================================== token stage
+constexpr int kSinkChunk = 40;   // saved Sinkhorn steps staged per round (numIters 20: one round)
 
 __global__ void __launch_bounds__(kBwTokenWarps * 32) bw_token_kernel(BwTokenParams p) {
   constexpr int NS = kBwNS, R = kBwR, NN = NS * NS;
@@ -104,7 +209,6 @@ __global__ void __launch_bounds__(kBwTokenWarps * 32) bw_token_kernel(BwTokenPar
   const int gw = blockIdx.x * kBwTokenWarps + warp;
   const int nw = gridDim.x * kBwTokenWarps;
   const int Tpad = p.ntiles * kBwTile;
-  const int nv = p.D >> 3;                              // 16-byte vectors per row
   const float a0 = __ldg(p.alpha), a1 = __ldg(p.alpha + 1), a2 = __ldg(p.alpha + 2);
   const float eps = p.hc_eps;
   const int rec_bytes = bw_tile_rec_bytes(p.P);
@@ -114,48 +218,16 @@ __global__ void __launch_bounds__(kBwTokenWarps * 32) bw_token_kernel(BwTokenPar
   for (int t = gw; t < Tpad; t += nw) {
     uint8_t* rec = p.tiles + (size_t)(t / kBwTile) * rec_bytes;
     const int col = t % kBwTile;
-    float* scal = reinterpret_cast<float*>(rec + p.P * kBwPlaneBytes) + col * 8;
+    float* scal = reinterpret_cast<float*>(rec + p.P * kBwPlaneBytes) + col * 2;
     if (t >= p.T) {                                     // padding token of the last tile
       for (int pl = 0; pl < p.P; ++pl)
         *reinterpret_cast<__nv_bfloat16*>(rec + pl * kBwPlaneBytes + swz(lane, col)) = __float2bfloat16_rn(0.0f);
-      if (lane < 8) scal[lane] = 0.0f;
+      if (lane < 2 * NS) scal[(lane >> 1) * (2 * kBwTile) + (lane & 1)] = 0.0f;
       continue;
     }
-    // ---- 3.1: H_pre_grad[i] = sum_d grad_h_in[d] x[i][d]
-    float hg[NS] = {0.0f, 0.0f, 0.0f, 0.0f};
-    {
-      const __nv_bfloat16* xr = p.x + (size_t)t * NS * p.D;
-      const __nv_bfloat16* gr = p.g_in + (size_t)t * p.D;
-      for (int v0 = lane; v0 < nv; v0 += 32 * kVec) {
-        uint4 gv[kVec], xv[kVec][NS];
-#pragma unroll
-        for (int b = 0; b < kVec; ++b) {
-          const int v = v0 + 32 * b;
-          if (v < nv) {
-            gv[b] = __ldg(reinterpret_cast<const uint4*>(gr) + v);
-#pragma unroll
-            for (int i = 0; i < NS; ++i) xv[b][i] = __ldg(reinterpret_cast<const uint4*>(xr + (size_t)i * p.D) + v);
-          }
-        }
-#pragma unroll
-        for (int b = 0; b < kVec; ++b) {
-          if (v0 + 32 * b >= nv) continue;
-          const __nv_bfloat162* g2 = reinterpret_cast<const __nv_bfloat162*>(&gv[b]);
-#pragma unroll
-          for (int i = 0; i < NS; ++i) {
-            const __nv_bfloat162* x2 = reinterpret_cast<const __nv_bfloat162*>(&xv[b][i]);
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              const float2 gf = __bfloat1622float2(g2[e]), xf = __bfloat1622float2(x2[e]);
-              hg[i] = fmaf(gf.x, xf.x, hg[i]);
-              hg[i] = fmaf(gf.y, xf.y, hg[i]);
-            }
-          }
-        }
-      }
-#pragma unroll
-      for (int i = 0; i < NS; ++i) hg[i] = warp_sum(hg[i]);
-    }
+    // ---- 3.1: H_pre_grad[i] = sum_d grad_h_in[d] x[i][d], from the row-dot kernel
+    const float4 hg4 = __ldg(reinterpret_cast<const float4*>(p.hg) + t);
+    const float hg[NS] = {hg4.x, hg4.y, hg4.z, hg4.w};
     const float ir = __ldg(p.inv_rms + t);
     const float hmix_r = lane < R ? __ldg(p.h_mix + (size_t)t * R + lane) : 0.0f;
 
@@ -167,10 +239,24 @@ __global__ void __launch_bounds__(kBwTokenWarps * 32) bw_token_kernel(BwTokenPar
         const int klo = max(1, kh - kSinkChunk + 1);
         const int cnt = kh - klo + 1;
         __syncwarp();
-        for (int e = lane; e < cnt * NN; e += 32)
-          st[e / NN][e % NN] = __ldg(p.norm_out + ((size_t)(klo + e / NN) * p.T + t) * NN + e % NN);
-        for (int e = lane; e < cnt * NS; e += 32)
-          st[e / NS][NN + e % NS] = __ldg(p.sum_out + ((size_t)(klo + e / NS) * p.T + t) * NS + e % NS);
+        // the chunk's saved matrices and sums, eight loads in flight per lane
+        const int nm = cnt * NN, ntot = nm + cnt * NS;
+        for (int e0 = lane; e0 < ntot; e0 += 32 * 8) {
+          float v[8];
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            const int e = e0 + 32 * j;
+            v[j] = 0.0f;
+            if (e < nm) v[j] = __ldg(p.norm_out + ((size_t)(klo + e / NN) * p.T + t) * NN + e % NN);
+            else if (e < ntot) v[j] = __ldg(p.sum_out + ((size_t)(klo + (e - nm) / NS) * p.T + t) * NS + (e - nm) % NS);
+          }
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            const int e = e0 + 32 * j;
+            if (e < nm) st[e / NN][e % NN] = v[j];
+            else if (e < ntot) st[(e - nm) / NS][NN + (e - nm) % NS] = v[j];
+          }
+        }
         __syncwarp();
         for (int k = kh; k >= klo; --k) {
           const float* row = st[k - klo];
@@ -185,7 +271,7 @@ __global__ void __launch_bounds__(kBwTokenWarps * 32) bw_token_kernel(BwTokenPar
             dot += __shfl_xor_sync(0xffffffffu, dot, 2);
             s = row[NN + (el >> 2)];
           }
-          g = __fdiv_rn(g - dot, s);
+          g = __fdividef(g - dot, s);      // s is a sum plus eps: >= eps, well inside the fast range
         }
       }
       // the row softmax (+ eps): S = normOut[0] - eps
@@ -224,7 +310,9 @@ __global__ void __launch_bounds__(kBwTokenWarps * 32) bw_token_kernel(BwTokenPar
     for (int pl = 0; pl < p.P; ++pl)
       *reinterpret_cast<__nv_bfloat16*>(rec + pl * kBwPlaneBytes + swz(lane, col)) =
           __float2bfloat16_rn(plane_part(G, pl, p.tf32));
-    if (lane < 2 * NS) scal[lane] = (lane & 1) ? c : __ldg(p.h_pre + (size_t)t * NS + (lane >> 1));
+    // per stream i, per token: (hPre_i, RMS factor) -- [i][token] pairs
+    if (lane < 2 * NS)
+      scal[(lane >> 1) * (2 * kBwTile) + (lane & 1)] = (lane & 1) ? c : __ldg(p.h_pre + (size_t)t * NS + (lane >> 1));
   }
   // ---- this warp's partial sums: [0, R) bias, R.. R+2 alpha by segment
   float seg0 = lane < NS ? acc_alpha : 0.0f;
@@ -354,13 +442,13 @@ __global__ void __launch_bounds__(kMainThreads, 1)
         const int slab = u / nq, chunk = u % nq;
         const int t0 = (int)((long long)chunk * ntiles / nq), t1 = (int)((long long)(chunk + 1) * ntiles / nq);
         if (t0 == t1) continue;
-        if (piece > 0 && !wait_bar<false>(&tail->a_free, (uint32_t)(piece - 1) & 1u, ctl, kErrWaitTimeout)) break;
+        if (piece > 0 && !wait_bar_sleep(&tail->a_free, (uint32_t)(piece - 1) & 1u, ctl, kErrWaitTimeout)) break;
         mbar_expect_tx(&tail->a_full, (uint32_t)kABytes);
         bulk_load_hint(sA, planes + (size_t)slab * (kABytes / 2), (uint32_t)kABytes, &tail->a_full, keep);
         a_pending = true;
         ++piece;
         for (int tile = t0; tile < t1; ++tile) {
-          if (!wait_bar<false>(&tail->empty[s], ph ^ 1u, ctl, kErrWaitTimeout)) { ok = false; break; }
+          if (!wait_bar_sleep(&tail->empty[s], ph ^ 1u, ctl, kErrWaitTimeout)) { ok = false; break; }
           uint8_t* st = sStage + (size_t)s * kStageBytes;
           mbar_expect_tx(&tail->full[s], (uint32_t)kStageBytes);
           tma_load_4d_hint(st, &tmap_x, &tail->full[s], 0, tile * kBwTile, slab, 0, once);
@@ -393,11 +481,11 @@ __global__ void __launch_bounds__(kMainThreads, 1)
         const int t0 = (int)((long long)chunk * ntiles / nq), t1 = (int)((long long)(chunk + 1) * ntiles / nq);
         for (int tile = t0; tile < t1; ++tile, ++k) {
           const bool first = tile == t0, last = tile == t1 - 1;
-          if (!wait_bar<false>(&tail->full[s], ph, ctl, kErrWaitTimeout)) { ok = false; break; }
+          if (!wait_bar_sleep(&tail->full[s], ph, ctl, kErrWaitTimeout)) { ok = false; break; }
           if (first) {
-            if (!wait_bar<false>(&tail->a_full, (uint32_t)piece & 1u, ctl, kErrWaitTimeout)) { ok = false; break; }
+            if (!wait_bar_sleep(&tail->a_full, (uint32_t)piece & 1u, ctl, kErrWaitTimeout)) { ok = false; break; }
             if (piece > 0 &&
-                !wait_bar<false>(&tail->mt_empty, (uint32_t)(piece - 1) & 1u, ctl, kErrWaitTimeout)) {
+                !wait_bar_sleep(&tail->mt_empty, (uint32_t)(piece - 1) & 1u, ctl, kErrWaitTimeout)) {
               ok = false;
               break;
             }
@@ -415,7 +503,7 @@ __global__ void __launch_bounds__(kMainThreads, 1)
                        sw128_desc(gt_addr + (uint32_t)(ks * 32)), idesc_mt, (first && ks == 0) ? 0u : 1u);
           }
           const int b = (int)(k & 1);
-          if (!wait_bar<false>(&tail->d1_empty[b], ((uint32_t)(k >> 1) & 1u) ^ 1u, ctl, kErrWaitTimeout)) {
+          if (!wait_bar_sleep(&tail->d1_empty[b], ((uint32_t)(k >> 1) & 1u) ^ 1u, ctl, kErrWaitTimeout)) {
             ok = false;
             break;
           }
@@ -461,7 +549,7 @@ __global__ void __launch_bounds__(kMainThreads, 1)
         const int slab = u / nq, chunk = u % nq;
         const int t0 = (int)((long long)chunk * ntiles / nq), t1 = (int)((long long)(chunk + 1) * ntiles / nq);
         for (int tile = t0; tile < t1; ++tile) {
-          if (!wait_bar<false>(&tail->out_ready[s], ph, ctl, kErrWaitTimeout)) { ok = false; break; }
+          if (!wait_bar_sleep(&tail->out_ready[s], ph, ctl, kErrWaitTimeout)) { ok = false; break; }
           tma_store_4d(&tmap_gx, sStage + (size_t)s * kStageBytes, 0, tile * kBwTile, slab, 0);
           bulk_commit();
           bulk_wait_read<0>();
@@ -491,8 +579,8 @@ __global__ void __launch_bounds__(kMainThreads, 1)
       for (int tile = t0; tile < t1; ++tile, ++k) {
         const bool last = tile == t1 - 1;
         const int b = (int)(k & 1);
-        if (!wait_bar<false>(&tail->full[s], ph, ctl, kErrWaitTimeout) ||
-            !wait_bar<false>(&tail->d1_full[b], (uint32_t)(k >> 1) & 1u, ctl, kErrWaitTimeout)) {
+        if (!wait_bar_sleep(&tail->full[s], ph, ctl, kErrWaitTimeout) ||
+            !wait_bar_sleep(&tail->d1_full[b], (uint32_t)(k >> 1) & 1u, ctl, kErrWaitTimeout)) {
           run = false;
           break;
         }
@@ -536,7 +624,7 @@ __global__ void __launch_bounds__(kMainThreads, 1)
             const uint32_t off = (uint32_t)(c * 128) + ((uint32_t)(((dp >> 3) ^ (e & 7))) << 4) + pair_off;
             const float2 xf = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(xs + off));
             const float2 gf = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(gin + off));
-            const float2 hc = *reinterpret_cast<const float2*>(scal + c * 8 + 2 * i);   // (hPre_i, RMS factor)
+            const float2 hc = *reinterpret_cast<const float2*>(scal + i * (2 * kBwTile) + 2 * c);   // (hPre_i, RMS factor)
             float vlo = fmaf(hc.x, gf.x, lo), vhi = fmaf(hc.x, gf.y, hi);
             vlo = fmaf(hc.y, xf.x, vlo);
             vhi = fmaf(hc.y, xf.y, vhi);
@@ -553,7 +641,7 @@ __global__ void __launch_bounds__(kMainThreads, 1)
         if (lane == 0) mbar_arrive(&tail->out_ready[s]);
         if (last && half == 0) {
           // x^T G of this unit, summed over the planes -> partial buffer [u][r][k]
-          if (!wait_bar<false>(&tail->mt_full, (uint32_t)piece & 1u, ctl, kErrWaitTimeout)) {
+          if (!wait_bar_sleep(&tail->mt_full, (uint32_t)piece & 1u, ctl, kErrWaitTimeout)) {
             run = false;
             break;
           }
@@ -649,6 +737,26 @@ cudaError_t launch_bw_planes(const BwPlaneParams& pp, cudaStream_t s) {
   if (blocks > 4096) blocks = 4096;
   if (blocks < 1) blocks = 1;
   bw_planes_kernel<<<blocks, 256, 0, s>>>(pp);
+  return cudaGetLastError();
+}
+
+void bw_rowdot_shape(int D, size_t max_smem, int* tps, int* stages, size_t* smem_bytes) {
+  const size_t tok = (size_t)(kBwNS + 1) * D * 2;
+  size_t t = 65536 / tok;
+  if (t < 1) t = 1;
+  if (t > 16) t = 16;
+  const size_t avail = max_smem > sizeof(RdTail) + 128 ? max_smem - sizeof(RdTail) - 128 : 0;
+  size_t st = avail / (t * tok);
+  if (st > (size_t)kRdMaxStages) st = kRdMaxStages;
+  *tps = (int)t;
+  *stages = st >= 2 ? (int)st : 0;
+  *smem_bytes = (size_t)(*stages) * t * tok + sizeof(RdTail);
+}
+
+cudaError_t launch_bw_rowdot(const BwRowdotParams& p, int grid, size_t smem_bytes, cudaStream_t s) {
+  cudaError_t e = cudaFuncSetAttribute(bw_rowdot_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_bytes);
+  if (e != cudaSuccess) return e;
+  bw_rowdot_kernel<<<grid, kRdThreads, smem_bytes, s>>>(p);
   return cudaGetLastError();
 }
 

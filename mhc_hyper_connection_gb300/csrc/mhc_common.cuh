@@ -425,7 +425,9 @@ cudaError_t launch_gw_forward(const GwLaunch& L, cudaStream_t s);
 // Backward of the pre-mapping (n = 4, three gates).  Four launches:
 //  1. planes: phi . gamma per 64-column slab as P bf16 planes, row-padded to
 //     kBwRp rows, swizzled for the tensor core; zeroes the header;
-//  2. token stage: per token the gate and Sinkhorn backward -> G = H_mix_grad
+//  2. row dot: H_pre_grad[t][i] = grad_h_in[t] . x[t][i] (whole rows streamed
+//     through a bulk-copy ring);
+//  2b. token stage: per token the gate and Sinkhorn backward -> G = H_mix_grad
 //     (as P bf16 planes in a per-64-token tile record) and the RMS factor;
 //     per-warp partial sums of grad_alpha / grad_bias;
 //  3. main: per (slab, token tile) grad_x = gx3 + G phi' + c x (+ grad_x_post)
@@ -435,7 +437,7 @@ cudaError_t launch_gw_forward(const GwLaunch& L, cudaStream_t s);
 constexpr int kBwNS = 4, kBwR = 24, kBwRp = 32;   // streams, gate rows, rows padded to the MMA K step
 constexpr int kBwTile = 64;                        // tokens per tile
 constexpr int kBwPlaneBytes = kBwRp * 128;         // one plane: kBwRp rows of 64 bf16
-constexpr int kBwScalarBytes = kBwTile * 32;       // per token: hPre[4], RMS factor, 3 pad
+constexpr int kBwScalarBytes = kBwTile * 32;       // [stream][token] (hPre_i, RMS factor) pairs
 constexpr int kBwMaxMainGrid = 160;                // main-kernel CTAs the workspace is sized for
 constexpr int kBwMaxTokenBlocks = 1024;            // token-stage blocks (8 warps each)
 constexpr int kBwTokenWarps = 8;
@@ -459,11 +461,18 @@ struct BwPlaneParams {
   int D, nslab, P, tf32;
 };
 
+struct BwRowdotParams {
+  int T, D, tps, stages;       // tokens per ring stage, ring depth
+  const __nv_bfloat16* x;      // [T, n, D]
+  const __nv_bfloat16* g_in;   // [T, D]
+  float* hg;                   // [T, n]: H_pre_grad
+  uint32_t* err;
+};
+
 struct BwTokenParams {
   int T, D, ntiles, num_iters, P, tf32;
   float hc_eps;
-  const __nv_bfloat16* x;      // [T, n, D]
-  const __nv_bfloat16* g_in;   // [T, D]
+  const float* hg;             // [T, n]: H_pre_grad from the row-dot kernel
   const float* g_post;         // [T, n]
   const float* g_res;          // [T, n, n]
   const float* inv_rms;        // [T]
@@ -501,6 +510,10 @@ struct BwFinalParams {
 };
 
 cudaError_t launch_bw_planes(const BwPlaneParams& p, cudaStream_t s);
+// Row-dot ring: tokens per stage and stage count for this shape (0 stages:
+// does not fit), and its launch.
+void bw_rowdot_shape(int D, size_t max_smem, int* tps, int* stages, size_t* smem_bytes);
+cudaError_t launch_bw_rowdot(const BwRowdotParams& p, int grid, size_t smem_bytes, cudaStream_t s);
 cudaError_t bw_token_blocks(int* blocks);      // token-stage grid for this device
 cudaError_t launch_bw_token(const BwTokenParams& p, int blocks, cudaStream_t s);
 cudaError_t launch_bw_main(const BwMainLaunch& L, cudaStream_t s);

@@ -617,9 +617,9 @@ namespace {
 
 // Backward workspace: [0, 256) header | phi . gamma planes per slab | tile
 // records (G planes + hPre + RMS factor) | x^T G partial sums of the work
-// units (slab, token chunk) | token-stage partial sums.
+// units (slab, token chunk) | token-stage partial sums | H_pre_grad [T][n].
 struct BwLayout {
-  size_t planes, tiles, pieces, partials, total;
+  size_t planes, tiles, pieces, partials, hg, total;
 };
 
 BwLayout bw_layout(const mhc_pre_s* h, int64_t T) {
@@ -632,7 +632,8 @@ BwLayout bw_layout(const mhc_pre_s* h, int64_t T) {
   L.tiles = L.planes + up(nslab * (size_t)mhc::bw_slab_bytes(P));
   L.pieces = L.tiles + up(ntiles * (size_t)mhc::bw_tile_rec_bytes(P));
   L.partials = L.pieces + up(nslab * mhc::kBwMaxChunks * mhc::bw_piece_bytes());
-  L.total = L.partials + up((size_t)mhc::kBwMaxTokenBlocks * mhc::kBwTokenWarps * 32 * sizeof(float));
+  L.hg = L.partials + up((size_t)mhc::kBwMaxTokenBlocks * mhc::kBwTokenWarps * 32 * sizeof(float));
+  L.total = L.hg + up((size_t)T * mhc::kBwNS * sizeof(float));
   return L;
 }
 
@@ -763,7 +764,21 @@ mhc_status_t mhc_pre_backward_run(mhc_pre_t h, const mhc_pre_bwd_args* a, void* 
   pp.P = P;
   pp.tf32 = (h->cfg.impl_mode == MHC_IMPL_TF32) ? 1 : 0;
 
+  mhc::BwRowdotParams rp;
+  rp.T = (int)T;
+  rp.D = D;
+  rp.x = static_cast<const __nv_bfloat16*>(a->x);
+  rp.g_in = static_cast<const __nv_bfloat16*>(a->grad_h_in);
+  rp.hg = reinterpret_cast<float*>(ws + L.hg);
+  rp.err = err;
+  size_t rd_smem = 0;
+  mhc::bw_rowdot_shape(D, di.max_smem, &rp.tps, &rp.stages, &rd_smem);
+  if (rp.stages < 2) return fail(MHC_ERR_RUNTIME, "not enough shared memory for the row-dot ring");
+  const long long rd_groups = (T + rp.tps - 1) / rp.tps;
+  const int rd_grid = (int)(rd_groups < di.sms ? rd_groups : di.sms);
+
   mhc::BwTokenParams tp;
+  tp.hg = rp.hg;
   tp.T = (int)T;
   tp.D = D;
   tp.ntiles = ntiles;
@@ -771,8 +786,6 @@ mhc_status_t mhc_pre_backward_run(mhc_pre_t h, const mhc_pre_bwd_args* a, void* 
   tp.P = P;
   tp.tf32 = pp.tf32;
   tp.hc_eps = (float)h->cfg.hc_eps;
-  tp.x = static_cast<const __nv_bfloat16*>(a->x);
-  tp.g_in = static_cast<const __nv_bfloat16*>(a->grad_h_in);
   tp.g_post = a->grad_h_post;
   tp.g_res = a->grad_h_res;
   tp.inv_rms = a->inv_rms;
@@ -807,6 +820,8 @@ mhc_status_t mhc_pre_backward_run(mhc_pre_t h, const mhc_pre_bwd_args* a, void* 
   cudaError_t e;
   if ((e = mhc::launch_bw_planes(pp, s)) != cudaSuccess)
     return fail(MHC_ERR_RUNTIME, "backward plane launch failed: %s", cudaGetErrorString(e));
+  if ((e = mhc::launch_bw_rowdot(rp, rd_grid, rd_smem, s)) != cudaSuccess)
+    return fail(MHC_ERR_RUNTIME, "backward row-dot launch failed: %s", cudaGetErrorString(e));
   if ((e = mhc::launch_bw_token(tp, tblocks, s)) != cudaSuccess)
     return fail(MHC_ERR_RUNTIME, "backward token-stage launch failed: %s", cudaGetErrorString(e));
   if (h->ev_before) cudaEventRecord(h->ev_before, s);

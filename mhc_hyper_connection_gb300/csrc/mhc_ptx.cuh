@@ -84,6 +84,38 @@ __device__ __noinline__ bool wait_bar(uint64_t* bar, uint32_t parity, const Ctl&
   }
 }
 
+// As mbar_test, but a thread whose phase is not complete may sleep up to
+// `hint_ns` (woken early when the phase completes) instead of returning at
+// once: waiting warps then take few issue slots from working ones.
+__device__ __forceinline__ bool mbar_test_sleep(uint64_t* bar, uint32_t parity, uint32_t hint_ns) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity), "r"(hint_ns)
+      : "memory");
+  return ok != 0;
+}
+
+// wait_bar with sleeping probes (CTA-local barriers only).
+static __device__ __noinline__ bool wait_bar_sleep(uint64_t* bar, uint32_t parity, const Ctl& c, uint32_t code) {
+  if (mbar_test(bar, parity)) return true;
+  const uint64_t t0 = now_ns();
+  for (uint32_t it = 1;; ++it) {
+    if (mbar_test_sleep(bar, parity, 20000u)) return true;
+    if ((it & 7u) == 0) {
+      if (*c.abort) return false;
+      if (now_ns() - t0 > kWaitNs) {
+        atomicOr(c.err, code);
+        *c.abort = 1u;
+        return false;
+      }
+    }
+  }
+}
+
 // Non-blocking probe of a phase (test_wait never suspends the thread).
 __device__ __forceinline__ bool mbar_poll(uint64_t* bar, uint32_t parity) {
   uint32_t ok;

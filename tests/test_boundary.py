@@ -229,7 +229,8 @@ def test_backward_workspace_size(lib):
     tiles = up(2 * (3 * 32 * 128 + 64 * 32))
     pieces = up(112 * 8 * 32 * 256 * 4)
     parts = up(1024 * 8 * 32 * 4)
-    assert st == mp.MHC_OK and n == 256 + planes + tiles + pieces + parts
+    hg = up(100 * 4 * 4)
+    assert st == mp.MHC_OK and n == 256 + planes + tiles + pieces + parts + hg
     assert mp.mhc_pre_backward_workspace_size(h, -1)[0] == mp.MHC_ERR_PARAM_INVALID
     mp.mhc_pre_destroy(h)
     h = _handle(D=7168, impl_mode=1)
