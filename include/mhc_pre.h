@@ -64,9 +64,24 @@ typedef int32_t mhc_status_t;
 
 typedef struct mhc_pre_s *mhc_pre_t;
 
+/* Element type of x and y (bf16 x is what every page's example uses; fp16 is
+ * the other type the MhcPreSinkhorn page lists for x). */
+#define MHC_DTYPE_BF16 0
+#define MHC_DTYPE_FP16 1
+
 /* Fixed per handle.  Defaults (mhc_pre_config_default): n = 4, D = 0 (must be
  * set), alpha_len = 3, num_iters = 20, norm_eps = hc_eps = 1e-6,
- * impl_mode = MHC_IMPL_FP32, need_backward = 0. */
+ * impl_mode = MHC_IMPL_FP32, need_backward = 0, batch_consistent = 0,
+ * x_dtype = MHC_DTYPE_BF16.
+ *
+ * batch_consistent (the Sinkhorn page's §8.1 "Batch 一致性", off by default
+ * there too): every token's outputs are bitwise the same whatever T and
+ * whatever other tokens share the call.  The forward then always runs the
+ * 64-token cluster kernel at cluster size 2 (the reduction of a token over
+ * its n*D columns is split the same way for every T), which can be slower
+ * for small T.  With it off the cluster size follows T and the last bits of
+ * a token's results may change with T (still deterministic for a given T:
+ * the default is a fixed reduction order, as the pages require). */
 typedef struct {
     int64_t n;              /* residual streams: 4, 6 or 8                          */
     int64_t D;              /* stream width: 16 <= D <= 16384, D % 16 == 0          */
@@ -76,6 +91,8 @@ typedef struct {
     double  hc_eps;         /* gate / Sinkhorn epsilon                              */
     int32_t impl_mode;      /* MHC_IMPL_FP32 or MHC_IMPL_TF32                       */
     int32_t need_backward;  /* 1: also write inv_rms, h_mix, sum_out, norm_out      */
+    int32_t batch_consistent; /* 1: results per token independent of T (see above)  */
+    int32_t x_dtype;        /* MHC_DTYPE_BF16 (x and y bf16) or MHC_DTYPE_FP16       */
 } mhc_pre_config;
 
 /* Per call.  R = n*n + 2n (alpha_len 3) or 2n (alpha_len 2); I = num_iters. */

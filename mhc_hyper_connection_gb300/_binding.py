@@ -18,6 +18,8 @@ MHC_ERR_PARAM_INVALID = 161002
 MHC_ERR_RUNTIME = 361001
 MHC_IMPL_FP32 = 0
 MHC_IMPL_TF32 = 1
+MHC_DTYPE_BF16 = 0
+MHC_DTYPE_FP16 = 1
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_PKG, "libmhc_pre.so")
@@ -27,7 +29,8 @@ class MhcPreConfig(ctypes.Structure):
     _fields_ = [("n", ctypes.c_int64), ("D", ctypes.c_int64), ("alpha_len", ctypes.c_int32),
                 ("num_iters", ctypes.c_int32), ("norm_eps", ctypes.c_double),
                 ("hc_eps", ctypes.c_double), ("impl_mode", ctypes.c_int32),
-                ("need_backward", ctypes.c_int32)]
+                ("need_backward", ctypes.c_int32), ("batch_consistent", ctypes.c_int32),
+                ("x_dtype", ctypes.c_int32)]
 
 
 _P = ctypes.c_void_p
@@ -164,12 +167,14 @@ def mhc_post_run(T: int, n: int, D: int, x: int, residual: int, post: int, comb:
 def hc_post(x, residual, post, comb, out=None, stream=None):
     """out[t, j, d] = post[t, j] x[t, d] + sum_i comb[t, i, j] residual[t, i, d]
     on torch tensors (x bf16 [T, D], residual bf16 [T, n, D], post fp32 [T, n],
-    comb fp32 [T, n, n]); returns out (bf16 [T, n, D]).  Raises MhcError on a
+    comb fp32 [T, n, n]; or the BSND layout with leading dims (B, S) in place
+    of T); returns out (bf16, shaped like residual).  Raises MhcError on a
     host-side rejection."""
     import torch
-    T, n, D = residual.shape
+    n, D = residual.shape[-2:]
+    T = _tokens(residual.shape[:-2])
     if out is None:
-        out = torch.empty((T, n, D), dtype=torch.bfloat16, device=residual.device)
+        out = torch.empty(residual.shape, dtype=torch.bfloat16, device=residual.device)
     if stream is None:
         stream = torch.cuda.current_stream(residual.device).cuda_stream
     elif hasattr(stream, "cuda_stream"):
@@ -205,7 +210,22 @@ def last_error() -> str:
 # ------------------------------------------------------------- torch marshalling
 
 def _ptr(t) -> Optional[int]:
-    return None if t is None else int(t.data_ptr())
+    """Device address of a tensor; the library takes contiguous tensors only
+    (the pages do not support non-contiguous inputs), so anything else is
+    refused here rather than misread."""
+    if t is None:
+        return None
+    if not t.is_contiguous():
+        raise ValueError("tensors passed to the mHC library must be contiguous")
+    return int(t.data_ptr())
+
+
+def _tokens(lead) -> int:
+    """Token count of the leading dims: (T,) in TND layout or (B, S) in BSND."""
+    lead = tuple(int(v) for v in lead)
+    if len(lead) not in (1, 2):
+        raise ValueError("leading dims must be (T,) or (B, S)")
+    return lead[0] * (lead[1] if len(lead) == 2 else 1)
 
 
 class MhcPre:
@@ -213,11 +233,13 @@ class MhcPre:
 
     def __init__(self, n: int, D: int, *, alpha_len: int = 3, num_iters: int = 20,
                  norm_eps: float = 1e-6, hc_eps: float = 1e-6, impl_mode: int = MHC_IMPL_FP32,
-                 need_backward: bool = False):
+                 need_backward: bool = False, batch_consistent: bool = False,
+                 x_dtype: int = MHC_DTYPE_BF16):
         cfg = mhc_pre_config_default()
         cfg.n, cfg.D, cfg.alpha_len, cfg.num_iters = n, D, alpha_len, num_iters
         cfg.norm_eps, cfg.hc_eps = norm_eps, hc_eps
         cfg.impl_mode, cfg.need_backward = impl_mode, int(bool(need_backward))
+        cfg.batch_consistent, cfg.x_dtype = int(bool(batch_consistent)), int(x_dtype)
         st, h = mhc_pre_create(cfg)
         if st != MHC_OK:
             raise MhcError(st, "mhc_pre_create", last_error())
@@ -243,22 +265,27 @@ class MhcPre:
             raise MhcError(st, "mhc_pre_workspace_size", last_error())
         return n
 
-    def allocate(self, T: int, device, *, h_res: bool = True, h_pre: bool = True):
-        """Output and workspace tensors for T tokens (torch supplies the memory)."""
+    def allocate(self, T, device, *, h_res: bool = True, h_pre: bool = True):
+        """Output and workspace tensors (torch supplies the memory) for T
+        tokens, or for a (B, S) batch in the BSND layout: outputs then carry
+        the leading dims (B, S) (hIn [B, S, D], hPost [B, S, n], ...), the
+        same memory as T = B * S tokens."""
         import torch
+        lead = (T,) if isinstance(T, int) else tuple(T)
+        T = _tokens(lead)
         n, D, R, I = self.n, self.D, self.R, self.num_iters
         f32 = dict(dtype=torch.float32, device=device)
-        out = {"y": torch.empty((T, D), dtype=torch.bfloat16, device=device),
-               "h_post": torch.empty((T, n), **f32),
-               "h_res": torch.empty((T, n, n), **f32) if (h_res or self.alpha_len == 3) else None,
-               "h_pre": torch.empty((T, n), **f32) if (h_pre or self.need_backward) else None,
+        out = {"y": torch.empty(lead + (D,), dtype=torch.bfloat16, device=device),
+               "h_post": torch.empty(lead + (n,), **f32),
+               "h_res": torch.empty(lead + (n, n), **f32) if (h_res or self.alpha_len == 3) else None,
+               "h_pre": torch.empty(lead + (n,), **f32) if (h_pre or self.need_backward) else None,
                "inv_rms": None, "h_mix": None, "sum_out": None, "norm_out": None}
         if self.need_backward:
-            out["inv_rms"] = torch.empty((T,), **f32)
-            out["h_mix"] = torch.empty((T, R), **f32)
+            out["inv_rms"] = torch.empty(lead, **f32)
+            out["h_mix"] = torch.empty(lead + (R,), **f32)
             if self.alpha_len == 3:
-                out["sum_out"] = torch.empty((2 * I, T, n), **f32)
-                out["norm_out"] = torch.empty((2 * I, T, n, n), **f32)
+                out["sum_out"] = torch.empty((2 * I,) + lead + (n,), **f32)
+                out["norm_out"] = torch.empty((2 * I,) + lead + (n, n), **f32)
         ws = self.workspace_size(T)
         # At least the 256-byte header, zeroed, so a status read is defined even for T = 0.
         out["workspace"] = torch.zeros((max(ws, 256),), dtype=torch.uint8, device=device)
@@ -266,7 +293,7 @@ class MhcPre:
 
     def make_args(self, x, phi, alpha, bias, out, gamma=None, pre_mix=None) -> MhcPreArgs:
         a = MhcPreArgs()
-        a.T = int(x.shape[0]) if x is not None else 0
+        a.T = _tokens(x.shape[:-2]) if x is not None else 0
         a.x, a.phi, a.alpha, a.bias = _ptr(x), _ptr(phi), _ptr(alpha), _ptr(bias)
         a.gamma, a.pre_mix = _ptr(gamma), _ptr(pre_mix)
         for k in ("y", "h_post", "h_res", "h_pre", "inv_rms", "h_mix", "sum_out", "norm_out"):
@@ -296,12 +323,15 @@ class MhcPre:
             raise MhcError(st, "mhc_pre_backward_workspace_size", last_error())
         return n
 
-    def allocate_backward(self, T: int, device, *, gamma: bool = False):
-        """Gradient outputs and workspace for T tokens (torch supplies the memory)."""
+    def allocate_backward(self, T, device, *, gamma: bool = False):
+        """Gradient outputs and workspace for T tokens, or a (B, S) batch in
+        the BSND layout (torch supplies the memory)."""
         import torch
+        lead = (T,) if isinstance(T, int) else tuple(T)
+        T = _tokens(lead)
         n, D, R = self.n, self.D, self.R
         f32 = dict(dtype=torch.float32, device=device)
-        return {"grad_x": torch.empty((T, n, D), dtype=torch.bfloat16, device=device),
+        return {"grad_x": torch.empty(lead + (n, D), dtype=torch.bfloat16, device=device),
                 "grad_phi": torch.empty((R, n * D), **f32),
                 "grad_alpha": torch.empty((3,), **f32),
                 "grad_bias": torch.empty((R,), **f32),
@@ -315,7 +345,7 @@ class MhcPre:
         for the Sinkhorn form, sum_out / norm_out -- None selects the logit
         form); grads: from allocate_backward."""
         a = MhcPreBwdArgs()
-        a.T = int(x.shape[0])
+        a.T = _tokens(x.shape[:-2])
         a.x, a.phi, a.alpha, a.gamma = _ptr(x), _ptr(phi), _ptr(alpha), _ptr(gamma)
         a.grad_h_in, a.grad_h_post, a.grad_h_res = _ptr(grad_h_in), _ptr(grad_h_post), _ptr(grad_h_res)
         for k in ("inv_rms", "h_mix", "h_pre", "h_post", "sum_out", "norm_out"):

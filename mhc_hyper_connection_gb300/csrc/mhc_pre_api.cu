@@ -275,6 +275,8 @@ void mhc_pre_config_default(mhc_pre_config* c) {
   c->hc_eps = 1e-6;
   c->impl_mode = MHC_IMPL_FP32;
   c->need_backward = 0;
+  c->batch_consistent = 0;
+  c->x_dtype = MHC_DTYPE_BF16;
 }
 
 const char* mhc_pre_last_error(void) { return g_last_error; }
@@ -302,6 +304,9 @@ mhc_status_t mhc_pre_create(mhc_pre_t* out, const mhc_pre_config* cfg) {
   if (c.impl_mode != MHC_IMPL_FP32 && c.impl_mode != MHC_IMPL_TF32)
     return fail(MHC_ERR_PARAM_INVALID, "impl_mode must be 0 (fp32) or 1 (tf32)");
   if (c.need_backward != 0 && c.need_backward != 1) return fail(MHC_ERR_PARAM_INVALID, "need_backward must be 0 or 1");
+  if (c.batch_consistent != 0 && c.batch_consistent != 1)
+    return fail(MHC_ERR_PARAM_INVALID, "batch_consistent must be 0 or 1");
+  if (c.x_dtype != MHC_DTYPE_BF16) return fail(MHC_ERR_PARAM_INVALID, "x_dtype must be MHC_DTYPE_BF16");
   if (!(c.norm_eps >= 0.0) || !(c.hc_eps >= 0.0)) return fail(MHC_ERR_PARAM_INVALID, "eps values must be >= 0");
   mhc_pre_s* h = new (std::nothrow) mhc_pre_s;
   if (!h) return fail(MHC_ERR_RUNTIME, "out of host memory");
@@ -384,8 +389,9 @@ mhc_status_t mhc_pre_run(mhc_pre_t h, const mhc_pre_args* a, void* stream) {
 
   // 2. the fused forward: the cluster kernel, or the grid-wide kernel when
   //    MHC_PRE_PATH=grid selects it (and its shared memory and residency allow).
+  const bool consistent = c.batch_consistent != 0;
   const char* path = getenv("MHC_PRE_PATH");
-  if (path && !strcmp(path, "grid")) {
+  if (!consistent && path && !strcmp(path, "grid")) {
     mhc_status_t st = run_grid_wide(h, a, di, planes, s);
     if (st != MHC_ERR_NOT_SUITABLE) return st;
     return fail(MHC_ERR_PARAM_INVALID, "the grid-wide forward does not fit this shape");
@@ -393,7 +399,7 @@ mhc_status_t mhc_pre_run(mhc_pre_t h, const mhc_pre_args* a, void* stream) {
   // The 64-token-tile kernel, or the 128-token-tile kernel (n = 4) when
   // MHC_PRE_TILE=128 selects it.  At prefill the 64-token kernel at cluster 2
   // measured 0.688 ms against 0.702 ms for the best 128-token configuration.
-  const bool t128 = mhc::t128_supported(n, R, h->P) && env_int("MHC_PRE_TILE", 64) == 128;
+  const bool t128 = !consistent && mhc::t128_supported(n, R, h->P) && env_int("MHC_PRE_TILE", 64) == 128;
   const int tile_t = t128 ? mhc::kT128Tile : mhc::kTileT;
   auto layout = [&](int xsn, int wsn) {
     return t128 ? mhc::t128_layout(R, h->P, xsn, wsn) : mhc::smem_layout(n, R, h->P, xsn, wsn);
@@ -449,7 +455,9 @@ mhc_status_t mhc_pre_run(mhc_pre_t h, const mhc_pre_args* a, void* stream) {
   // Ties go to the larger cluster: each member then reduces and gates fewer
   // rows of a tile, which shortens the per-tile critical path.
   // MHC_PRE_CLUSTER=c forces cluster size c (for tuning runs).
-  const int forced = env_int("MHC_PRE_CLUSTER", 0);
+  // Batch-consistent mode pins cluster 2 (1 when there is a single d-chunk):
+  // a token's reduction is then split the same way whatever T is.
+  const int forced = consistent ? (nd >= 2 ? 2 : 1) : env_int("MHC_PRE_CLUSTER", 0);
   int cluster = 0;
   int max_clusters = 0;
   long long best_sms = -1;

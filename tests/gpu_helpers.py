@@ -5,8 +5,13 @@ tolerances.
 Tolerances (against the double-precision oracle):
   * hPre, hPost, comb: max |err| <= 1e-4 (fp32 mode), <= 3e-3 (tf32 mode);
   * y (bf16): |err| <= 2^-7 |ref| + 1e-3 elementwise;
-  * intermediates (fp32 mode): invRms rel 1e-5; hMix |err| <= 2e-4 (1 + |ref|)
+  * intermediates (fp32 mode): invRms rel 1e-4; hMix |err| <= 2e-4 (1 + |ref|)
     -- fp32 accumulation over n*D products; sumOut rel 1e-4; normOut 1e-4.
+    The invRms bound: Sigma x^2 is accumulated on the tensor core in fp32
+    over n*D/C products per CTA (C = cluster size), 16 per step; with each
+    step off by at most an ulp (2^-23) in the same direction the sum is off
+    by at most (n*D/(16 C)) 2^-23 -- 1.07e-4 at n*D = 28672, C = 2 -- and
+    invRms by half of that, 5.3e-5 (measured up to 2.6e-5).
 """
 from __future__ import annotations
 
@@ -80,10 +85,10 @@ def compare(case, out, ref, tokens=None, tol=None, check_intermediates=True):
     if case.need_backward and check_intermediates and case.impl_mode == 0:
         ir = _sel(out["inv_rms"], tokens)
         errs["inv_rms"] = float(np.abs(ir / ref.inv_rms - 1).max())
-        assert errs["inv_rms"] <= 1e-5
+        assert errs["inv_rms"] <= 1e-4, errs
         hm = _sel(out["h_mix"], tokens)
         errs["h_mix"] = float((np.abs(hm - ref.h_mix) / (1 + np.abs(ref.h_mix))).max())
-        assert errs["h_mix"] <= 2e-4
+        assert errs["h_mix"] <= 2e-4, errs
         if case.alpha_len == 3:
             so = _sel(out["sum_out"], tokens, axis=1)
             no = _sel(out["norm_out"], tokens, axis=1)

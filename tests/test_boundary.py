@@ -44,7 +44,7 @@ def test_library_exports_every_declared_symbol(lib):
 
 def test_struct_layouts_match_header():
     # Field order/sizes in the binding mirror the header (x86-64 and aarch64 LP64).
-    assert ctypes.sizeof(mp.MhcPreConfig) == 8 + 8 + 4 + 4 + 8 + 8 + 4 + 4
+    assert ctypes.sizeof(mp.MhcPreConfig) == 8 + 8 + 4 + 4 + 8 + 8 + 4 + 4 + 4 + 4
     assert ctypes.sizeof(mp.MhcPreArgs) == 8 + 15 * 8 + 8
     assert ctypes.sizeof(mp.MhcPreBwdArgs) == 8 + 20 * 8 + 8
 
@@ -52,12 +52,15 @@ def test_struct_layouts_match_header():
 def test_defaults(lib):
     c = mp.mhc_pre_config_default()
     assert (c.n, c.D, c.alpha_len, c.num_iters, c.impl_mode, c.need_backward) == (4, 0, 3, 20, 0, 0)
+    assert (c.batch_consistent, c.x_dtype) == (0, mp.MHC_DTYPE_BF16)
     assert c.norm_eps == 1e-6 and c.hc_eps == 1e-6
 
 
 @pytest.mark.parametrize("field,value", [("n", 5), ("n", 2), ("D", 0), ("D", 24), ("D", 16400),
                                          ("alpha_len", 1), ("num_iters", 0), ("impl_mode", 2),
-                                         ("impl_mode", -1), ("need_backward", 2)])
+                                         ("impl_mode", -1), ("need_backward", 2),
+                                         ("batch_consistent", 2), ("batch_consistent", -1),
+                                         ("x_dtype", 2), ("x_dtype", -1)])
 def test_create_rejects_bad_config(lib, field, value):
     c = mp.mhc_pre_config_default()
     c.D = 256
@@ -280,3 +283,17 @@ def test_backward_without_gpu_fails_loudly(lib):
     h = _handle(D=256)
     assert mp.mhc_pre_backward_run(h, _bwd_args()) == mp.MHC_ERR_RUNTIME
     mp.mhc_pre_destroy(h)
+
+
+def test_binding_refuses_non_contiguous_and_bad_layouts(lib):
+    import torch
+    from mhc_hyper_connection_gb300._binding import _tokens
+    op = mp.MhcPre(4, 64)
+    x = torch.zeros((8, 64, 4), dtype=torch.bfloat16).transpose(1, 2)    # [8, 4, 64], not contiguous
+    phi = torch.zeros((24, 256))
+    with pytest.raises(ValueError, match="contiguous"):
+        op.make_args(x, phi, torch.ones(3), torch.zeros(24), {"y": None, "h_post": None})
+    assert _tokens((6,)) == 6 and _tokens((2, 3)) == 6
+    with pytest.raises(ValueError):
+        _tokens((2, 3, 4))
+    op.close()
