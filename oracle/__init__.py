@@ -10,5 +10,5 @@ binding) never does, and this package never imports the product.
 ``run_backward()`` and ``run_post()`` call them through ctypes on numpy arrays
 and return the outputs in float64.
 """
-from .oracle import (build, run, run_backward, run_post, OracleOut, BwdOut,  # noqa: F401
+from .oracle import (build, run, run_backward, run_post, half_value, OracleOut, BwdOut,  # noqa: F401
                      brute_force_decimal)

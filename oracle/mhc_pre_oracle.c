@@ -7,6 +7,9 @@
  * benchmark's CPU-baseline leg may build, load or call it.  It shares no
  * code, header or constant with the CUDA path.
  *
+ * x arrives as bf16 bit patterns (mhc_oracle_pre) or IEEE fp16 ones
+ * (mhc_oracle_pre_f16); both are exact in double.
+ *
  * Sources (page title, then the section / formula followed):
  *  [V2]  "CANN ops-transformer 中 aclnnMhcPreV2 算子接口全解析：MHC 架构 H 投影
  *        矩阵与 hIn 计算实战指南", §三 (complete forward formula) and §7.3
@@ -39,7 +42,7 @@
 
 typedef struct {
     int64_t T, n, D;
-    int alpha_len, num_iters, hf32;
+    int alpha_len, num_iters, hf32, x_fp16;
     double norm_eps, hc_eps;
     const uint16_t *x;      /* bf16 bits [T][n][D] */
     const float *phi;       /* [R][n*D] */
@@ -50,6 +53,22 @@ typedef struct {
     double *y, *h_post, *h_res, *h_pre, *inv_rms, *h_mix, *sum_out, *norm_out;
     int64_t t_begin, t_end;
 } oracle_job;
+
+/* IEEE 754 binary16: 1 sign bit, 5 exponent bits (bias 15), 10 fraction
+ * bits; exponent 0 holds the subnormals 2^-14 * f / 1024, exponent 31 the
+ * infinities and NaNs. */
+double mhc_oracle_half_value(uint16_t bits)
+{
+    const int sign = bits >> 15, e = (bits >> 10) & 31, f = bits & 1023;
+    double v;
+    if (e == 0)
+        v = ldexp((double)f, -24);
+    else if (e == 31)
+        v = f ? NAN : INFINITY;
+    else
+        v = ldexp(1024.0 + (double)f, e - 25);
+    return sign ? -v : v;
+}
 
 static double bf16_value(uint16_t bits)
 {
@@ -82,7 +101,7 @@ static void one_token(const oracle_job *J, int64_t t, double *w, double *P)
     /* [V2] §三: invRms = (mean(xFlat^2) + normEps)^(-1/2), raw x, mean over nD. */
     double ss = 0.0;
     for (int64_t k = 0; k < K; ++k) {
-        double v = bf16_value(xt[k]);
+        double v = J->x_fp16 ? mhc_oracle_half_value(xt[k]) : bf16_value(xt[k]);
         ss += v * v;
     }
     double inv_rms = 1.0 / sqrt(ss / (double)K + J->norm_eps);
@@ -92,7 +111,7 @@ static void one_token(const oracle_job *J, int64_t t, double *w, double *P)
         const float *phi_r = J->phi + r * K;
         double acc = 0.0;
         for (int64_t k = 0; k < K; ++k) {
-            double g = bf16_value(xt[k]);
+            double g = J->x_fp16 ? mhc_oracle_half_value(xt[k]) : bf16_value(xt[k]);
             double p = phi_r[k];
             if (J->gamma) {
                 if (J->hf32)
@@ -188,7 +207,7 @@ static void one_token(const oracle_job *J, int64_t t, double *w, double *P)
         double acc = 0.0;
         for (int64_t i = 0; i < n; ++i) {
             double m = J->pre_mix ? (double)J->pre_mix[t * n + i] : h_pre[i];
-            acc += m * bf16_value(xt[i * D + d]);
+            acc += m * (J->x_fp16 ? mhc_oracle_half_value(xt[i * D + d]) : bf16_value(xt[i * D + d]));
         }
         J->y[t * D + d] = acc;
     }
@@ -211,8 +230,8 @@ static void *worker(void *arg)
  * laid out like the operator's: y [T][D], h_post/h_pre [T][n],
  * h_res [T][n][n] (may be NULL), inv_rms [T], h_mix [T][R] (may be NULL),
  * sum_out [2I][T][n] and norm_out [2I][T][n][n] (may be NULL). */
-int mhc_oracle_pre(int64_t T, int64_t n, int64_t D, int alpha_len, int num_iters,
-                   double norm_eps, double hc_eps, int hf32,
+static int run_pre(int64_t T, int64_t n, int64_t D, int alpha_len, int num_iters,
+                   double norm_eps, double hc_eps, int hf32, int x_fp16,
                    const uint16_t *x, const float *phi, const float *alpha,
                    const float *bias, const float *gamma, const float *pre_mix,
                    double *y, double *h_post, double *h_res, double *h_pre,
@@ -231,6 +250,7 @@ int mhc_oracle_pre(int64_t T, int64_t n, int64_t D, int alpha_len, int num_iters
     memset(&base, 0, sizeof base);
     base.T = T; base.n = n; base.D = D;
     base.alpha_len = alpha_len; base.num_iters = num_iters; base.hf32 = hf32;
+    base.x_fp16 = x_fp16;
     base.norm_eps = norm_eps; base.hc_eps = hc_eps;
     base.x = x; base.phi = phi; base.alpha = alpha; base.bias = bias;
     base.gamma = gamma; base.pre_mix = pre_mix;
@@ -251,4 +271,33 @@ int mhc_oracle_pre(int64_t T, int64_t n, int64_t D, int alpha_len, int num_iters
     free(jobs);
     free(tid);
     return 0;
+}
+
+/* The forward with x given as bf16 bit patterns (the pages' examples)... */
+int mhc_oracle_pre(int64_t T, int64_t n, int64_t D, int alpha_len, int num_iters,
+                   double norm_eps, double hc_eps, int hf32,
+                   const uint16_t *x, const float *phi, const float *alpha,
+                   const float *bias, const float *gamma, const float *pre_mix,
+                   double *y, double *h_post, double *h_res, double *h_pre,
+                   double *inv_rms, double *h_mix, double *sum_out,
+                   double *norm_out, int nthreads)
+{
+    return run_pre(T, n, D, alpha_len, num_iters, norm_eps, hc_eps, hf32, 0, x, phi, alpha, bias,
+                   gamma, pre_mix, y, h_post, h_res, h_pre, inv_rms, h_mix, sum_out, norm_out,
+                   nthreads);
+}
+
+/* ...or as fp16 (IEEE binary16) bit patterns, the other x type the
+ * Sinkhorn page lists; everything after reading x is the same. */
+int mhc_oracle_pre_f16(int64_t T, int64_t n, int64_t D, int alpha_len, int num_iters,
+                       double norm_eps, double hc_eps, int hf32,
+                       const uint16_t *x, const float *phi, const float *alpha,
+                       const float *bias, const float *gamma, const float *pre_mix,
+                       double *y, double *h_post, double *h_res, double *h_pre,
+                       double *inv_rms, double *h_mix, double *sum_out,
+                       double *norm_out, int nthreads)
+{
+    return run_pre(T, n, D, alpha_len, num_iters, norm_eps, hc_eps, hf32, 1, x, phi, alpha, bias,
+                   gamma, pre_mix, y, h_post, h_res, h_pre, inv_rms, h_mix, sum_out, norm_out,
+                   nthreads);
 }

@@ -56,6 +56,12 @@ def _load():
                           ctypes.c_int, ctypes.c_double, ctypes.c_double, ctypes.c_int,
                           P, P, P, P, P, P, P, P, P, P, P, P, P, P, ctypes.c_int]
             f.restype = ctypes.c_int
+            f16 = lib.mhc_oracle_pre_f16
+            f16.argtypes = f.argtypes
+            f16.restype = ctypes.c_int
+            hv = lib.mhc_oracle_half_value
+            hv.argtypes = [ctypes.c_uint16]
+            hv.restype = ctypes.c_double
             g = lib.mhc_oracle_post
             g.argtypes = [ctypes.c_int64, ctypes.c_int64, ctypes.c_int64, P, P, P, P, P, ctypes.c_int]
             g.restype = ctypes.c_int
@@ -88,8 +94,10 @@ def _ptr(a):
 def run(x_bits: np.ndarray, phi: np.ndarray, alpha: np.ndarray, bias: np.ndarray,
         gamma: Optional[np.ndarray] = None, pre_mix: Optional[np.ndarray] = None, *,
         num_iters: int = 20, norm_eps: float = 1e-6, hc_eps: float = 1e-6,
-        hf32: bool = False, backward: bool = True, threads: Optional[int] = None) -> OracleOut:
-    """Evaluate the oracle.  x_bits: uint16/int16 bf16 bit patterns [T, n, D]."""
+        hf32: bool = False, backward: bool = True, threads: Optional[int] = None,
+        x_fp16: bool = False) -> OracleOut:
+    """Evaluate the oracle.  x_bits: uint16/int16 bit patterns [T, n, D] of bf16
+    values, or of IEEE fp16 values with x_fp16=True."""
     x_bits = np.ascontiguousarray(x_bits).view(np.uint16)
     T, n, D = x_bits.shape
     alpha = np.ascontiguousarray(alpha, dtype=np.float32)
@@ -112,7 +120,8 @@ def run(x_bits: np.ndarray, phi: np.ndarray, alpha: np.ndarray, bias: np.ndarray
     norm_out = np.zeros((2 * num_iters, T, n, n)) if sb else None
     if threads is None:
         threads = os.cpu_count() or 1
-    rc = _load().mhc_oracle_pre(
+    fn = _load().mhc_oracle_pre_f16 if x_fp16 else _load().mhc_oracle_pre
+    rc = fn(
         T, n, D, alpha_len, num_iters, norm_eps, hc_eps, int(bool(hf32)),
         _ptr(x_bits), _ptr(phi), _ptr(alpha), _ptr(bias), _ptr(gamma), _ptr(pre_mix),
         _ptr(y), _ptr(h_post), _ptr(h_res), _ptr(h_pre), _ptr(inv_rms), _ptr(h_mix),
@@ -120,6 +129,11 @@ def run(x_bits: np.ndarray, phi: np.ndarray, alpha: np.ndarray, bias: np.ndarray
     if rc != 0:
         raise ValueError("oracle rejected its arguments")
     return OracleOut(y, h_post, h_res, h_pre, inv_rms, h_mix, sum_out, norm_out)
+
+
+def half_value(bits: int) -> float:
+    """The oracle's decoding of one IEEE fp16 bit pattern (for its pin)."""
+    return float(_load().mhc_oracle_half_value(int(bits) & 0xFFFF))
 
 
 def run_post(x_bits: np.ndarray, residual_bits: np.ndarray, post: np.ndarray, comb: np.ndarray, *,
