@@ -92,19 +92,24 @@ typedef struct {
     int32_t impl_mode;      /* MHC_IMPL_FP32 or MHC_IMPL_TF32                       */
     int32_t need_backward;  /* 1: also write inv_rms, h_mix, sum_out, norm_out      */
     int32_t batch_consistent; /* 1: results per token independent of T (see above)  */
-    int32_t x_dtype;        /* MHC_DTYPE_BF16 (x and y bf16) or MHC_DTYPE_FP16       */
+    int32_t x_dtype;        /* MHC_DTYPE_BF16 (x and y bf16) or MHC_DTYPE_FP16 (x and
+                               y fp16; n = 4; the backward takes bf16 only). fp16
+                               x runs the projection on fp16 planes of phi . gamma,
+                               so every |phi . gamma| must be <= 65504: a larger
+                               one sets bit 3 of the device error word, which
+                               mhc_pre_status reports                              */
 } mhc_pre_config;
 
 /* Per call.  R = n*n + 2n (alpha_len 3) or 2n (alpha_len 2); I = num_iters. */
 typedef struct {
     int64_t      T;         /* tokens; 0 returns MHC_OK at once (pointers unchecked)  */
-    const void  *x;         /* bf16 [T, n, D]                          required       */
+    const void  *x;         /* [T, n, D] of x_dtype (bf16 or fp16)     required       */
     const float *phi;       /* fp32 [R, n*D]                           required       */
     const float *alpha;     /* fp32 [alpha_len]                        required       */
     const float *bias;      /* fp32 [R]                                required       */
     const float *gamma;     /* fp32 [n, D] or NULL (no scaling)                       */
     const float *pre_mix;   /* fp32 [T, n] or NULL (y weights = hPre)                 */
-    void        *y;         /* bf16 [T, D]                             required       */
+    void        *y;         /* [T, D] of x_dtype                       required       */
     float       *h_post;    /* fp32 [T, n]                             required       */
     float       *h_res;     /* fp32 [T, n, n] comb after Sinkhorn; required when
                                alpha_len == 3; optional (filled with 0) when 2        */

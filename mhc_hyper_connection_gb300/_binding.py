@@ -246,6 +246,7 @@ class MhcPre:
         self.handle = h
         self.n, self.D, self.alpha_len, self.num_iters = n, D, alpha_len, num_iters
         self.need_backward = bool(need_backward)
+        self.x_dtype = int(x_dtype)
         self.R = n * n + 2 * n if alpha_len == 3 else 2 * n
 
     def close(self):
@@ -275,7 +276,8 @@ class MhcPre:
         T = _tokens(lead)
         n, D, R, I = self.n, self.D, self.R, self.num_iters
         f32 = dict(dtype=torch.float32, device=device)
-        out = {"y": torch.empty(lead + (D,), dtype=torch.bfloat16, device=device),
+        ydt = torch.float16 if self.x_dtype == MHC_DTYPE_FP16 else torch.bfloat16
+        out = {"y": torch.empty(lead + (D,), dtype=ydt, device=device),
                "h_post": torch.empty(lead + (n,), **f32),
                "h_res": torch.empty(lead + (n, n), **f32) if (h_res or self.alpha_len == 3) else None,
                "h_pre": torch.empty(lead + (n,), **f32) if (h_pre or self.need_backward) else None,

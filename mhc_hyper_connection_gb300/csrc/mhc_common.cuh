@@ -10,6 +10,7 @@
 
 #include <cuda.h>
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -20,7 +21,29 @@ enum : uint32_t {
   kErrWaitTimeout = 1u << 0,   // an mbarrier wait gave up
   kErrClusterWait = 1u << 1,   // a cluster exchange wait gave up
   kErrGridWait = 1u << 2,      // a wait on another CTA's global counter gave up
+  kErrPlaneRange = 1u << 3,    // fp16 x: a phi . gamma entry lies outside the fp16 range
 };
+
+// Element type of x and y: the conversions the kernels need.
+template <bool kF16>
+struct XType;
+template <>
+struct XType<false> {
+  using T2 = __nv_bfloat162;
+  static __device__ __forceinline__ float2 to_f2(T2 v) { return __bfloat1622float2(v); }
+  static __device__ __forceinline__ T2 from_f2(float a, float b) { return __floats2bfloat162_rn(a, b); }
+};
+template <>
+struct XType<true> {
+  using T2 = __half2;
+  static __device__ __forceinline__ float2 to_f2(T2 v) { return __half22float2(v); }
+  static __device__ __forceinline__ T2 from_f2(float a, float b) { return __floats2half2_rn(a, b); }
+};
+// fp16 planes hold phi . gamma as h0 + h1 2^-11 + h2 2^-22 (each plane
+// scaled into fp16's range); bf16 planes need no scale.
+__host__ __device__ constexpr float plane_scale(bool f16, int plane) {
+  return !f16 ? 1.0f : plane == 0 ? 1.0f : plane == 1 ? 1.0f / 2048.0f : 1.0f / 4194304.0f;
+}
 
 // Workspace layout: [0, 256) header, then the phi planes, then the exchange
 // rings of the grid-wide forward.  Header words (uint32): 0 error word,
@@ -225,6 +248,7 @@ struct PlaneParams {
   __nv_bfloat16* planes;   // [nch][n][RB][64], swizzled
   int R, P, n, D, nch, RB; // P = 3 (fp32) or 2 (tf32)
   int tf32;
+  int fp16;                // planes in fp16 (scaled, see plane_scale) for fp16 x
   uint32_t* err_word;      // workspace header: all kHdrWords words are zeroed
 };
 
@@ -294,6 +318,7 @@ struct TcLaunch {
   CUtensorMap tmap_x;      // x as (D, T, n): box (64, 64 tokens, stream group), 128B swizzle
   const __nv_bfloat16* planes;   // swizzled plane blocks (see PlaneParams)
   int NP, P;
+  int fp16;                // x and y fp16 (planes fp16)
   int cluster;             // CTAs per token tile (split over d-chunks)
   int grid;                // CTAs (multiple of cluster)
   int xstages, wstages;
@@ -340,7 +365,7 @@ cudaError_t launch_post(const PostLaunch& L, cudaStream_t s);
 // Resolved by the kernel translation unit for the given (n, R, P).
 cudaError_t launch_tc_forward(const TcLaunch& L, cudaStream_t s);
 // Clusters of the given size that fit on the device at once (0: unsupported).
-cudaError_t tc_forward_occupancy(int n, int R, int P, size_t smem_bytes, int cluster,
+cudaError_t tc_forward_occupancy(int n, int R, int P, bool fp16, size_t smem_bytes, int cluster,
                                  int* max_clusters);
 int tc_np(int R, int P);
 

@@ -306,7 +306,10 @@ mhc_status_t mhc_pre_create(mhc_pre_t* out, const mhc_pre_config* cfg) {
   if (c.need_backward != 0 && c.need_backward != 1) return fail(MHC_ERR_PARAM_INVALID, "need_backward must be 0 or 1");
   if (c.batch_consistent != 0 && c.batch_consistent != 1)
     return fail(MHC_ERR_PARAM_INVALID, "batch_consistent must be 0 or 1");
-  if (c.x_dtype != MHC_DTYPE_BF16) return fail(MHC_ERR_PARAM_INVALID, "x_dtype must be MHC_DTYPE_BF16");
+  if (c.x_dtype != MHC_DTYPE_BF16 && c.x_dtype != MHC_DTYPE_FP16)
+    return fail(MHC_ERR_PARAM_INVALID, "x_dtype must be MHC_DTYPE_BF16 or MHC_DTYPE_FP16");
+  if (c.x_dtype == MHC_DTYPE_FP16 && c.n != 4)
+    return fail(MHC_ERR_PARAM_INVALID, "fp16 x is supported for n = 4");
   if (!(c.norm_eps >= 0.0) || !(c.hc_eps >= 0.0)) return fail(MHC_ERR_PARAM_INVALID, "eps values must be >= 0");
   mhc_pre_s* h = new (std::nothrow) mhc_pre_s;
   if (!h) return fail(MHC_ERR_RUNTIME, "out of host memory");
@@ -383,15 +386,18 @@ mhc_status_t mhc_pre_run(mhc_pre_t h, const mhc_pre_args* a, void* stream) {
   pp.nch = (D + mhc::kChunkK - 1) / mhc::kChunkK;
   pp.RB = mhc::plane_box_rows(R, h->P);
   pp.tf32 = (c.impl_mode == MHC_IMPL_TF32);
+  pp.fp16 = (c.x_dtype == MHC_DTYPE_FP16);
   pp.err_word = err;
   if (mhc::launch_prepare_planes(pp, s) != cudaSuccess)
     return fail(MHC_ERR_RUNTIME, "plane preparation launch failed: %s", cudaGetErrorString(cudaGetLastError()));
 
   // 2. the fused forward: the cluster kernel, or the grid-wide kernel when
   //    MHC_PRE_PATH=grid selects it (and its shared memory and residency allow).
+  // fp16 x runs on the 64-token cluster kernel only
+  const bool fp16 = c.x_dtype == MHC_DTYPE_FP16;
   const bool consistent = c.batch_consistent != 0;
   const char* path = getenv("MHC_PRE_PATH");
-  if (!consistent && path && !strcmp(path, "grid")) {
+  if (!consistent && !fp16 && path && !strcmp(path, "grid")) {
     mhc_status_t st = run_grid_wide(h, a, di, planes, s);
     if (st != MHC_ERR_NOT_SUITABLE) return st;
     return fail(MHC_ERR_PARAM_INVALID, "the grid-wide forward does not fit this shape");
@@ -399,7 +405,7 @@ mhc_status_t mhc_pre_run(mhc_pre_t h, const mhc_pre_args* a, void* stream) {
   // The 64-token-tile kernel, or the 128-token-tile kernel (n = 4) when
   // MHC_PRE_TILE=128 selects it.  At prefill the 64-token kernel at cluster 2
   // measured 0.688 ms against 0.702 ms for the best 128-token configuration.
-  const bool t128 = !consistent && mhc::t128_supported(n, R, h->P) && env_int("MHC_PRE_TILE", 64) == 128;
+  const bool t128 = !consistent && !fp16 && mhc::t128_supported(n, R, h->P) && env_int("MHC_PRE_TILE", 64) == 128;
   const int tile_t = t128 ? mhc::kT128Tile : mhc::kTileT;
   auto layout = [&](int xsn, int wsn) {
     return t128 ? mhc::t128_layout(R, h->P, xsn, wsn) : mhc::smem_layout(n, R, h->P, xsn, wsn);
@@ -409,6 +415,7 @@ mhc_status_t mhc_pre_run(mhc_pre_t h, const mhc_pre_args* a, void* stream) {
   L.epi = epi_params(h, a);
   L.NP = NP;
   L.P = h->P;
+  L.fp16 = fp16 ? 1 : 0;
   L.err_word = err;
   L.planes = planes;
   {
@@ -465,7 +472,7 @@ mhc_status_t mhc_pre_run(mhc_pre_t h, const mhc_pre_args* a, void* stream) {
     if ((forced && cand != forced) || cand > nd) continue;
     int mc = 0;
     const cudaError_t oe = t128 ? mhc::t128_forward_occupancy(n, R, h->P, smem, cand, &mc)
-                                : mhc::tc_forward_occupancy(n, R, h->P, smem, cand, &mc);
+                                : mhc::tc_forward_occupancy(n, R, h->P, fp16, smem, cand, &mc);
     if (oe != cudaSuccess || mc <= 0) {
       cudaGetLastError();
       continue;
@@ -508,6 +515,8 @@ mhc_status_t mhc_pre_status(mhc_pre_t h, const void* workspace, void* stream) {
     uint32_t word = 0;
     e = cudaMemcpy(&word, workspace, sizeof word, cudaMemcpyDeviceToHost);
     if (e != cudaSuccess) return fail(MHC_ERR_RUNTIME, "reading the error word: %s", cudaGetErrorString(e));
+    if (word & mhc::kErrPlaneRange)
+      return fail(MHC_ERR_RUNTIME, "phi . gamma has an entry outside the fp16 range (error word 0x%x)", word);
     if (word != 0) return fail(MHC_ERR_RUNTIME, "device-side wait gave up (error word 0x%x)", word);
   }
   return MHC_OK;
@@ -650,6 +659,7 @@ mhc_status_t bw_scope(const mhc_pre_s* h) {
   if (h->cfg.n != 4) return fail(MHC_ERR_PARAM_INVALID, "the backward supports n = 4 (got %lld)", (long long)h->cfg.n);
   if (h->cfg.D % 64 != 0)
     return fail(MHC_ERR_PARAM_INVALID, "the backward needs D a multiple of 64 (got %lld)", (long long)h->cfg.D);
+  if (h->cfg.x_dtype != MHC_DTYPE_BF16) return fail(MHC_ERR_PARAM_INVALID, "the backward takes bf16 x");
   return MHC_OK;
 }
 

@@ -75,7 +75,7 @@ constexpr int kYThreads = kThreads - kWarpYc0 * 32;   // 256
 // Named barriers: 1 = publish pair (64 threads), 2 = y warps.
 constexpr int kBarPub = 1, kBarY = 2;
 
-template <int NS, int RR, int P>
+template <int NS, int RR, int P, bool F16>
 __global__ void __launch_bounds__(kThreads, 1)
     mhc_pre_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const __nv_bfloat16* __restrict__ planes,
                       const EpiParams ep, const __nv_bfloat16* __restrict__ xg, Geometry g, uint32_t* err) {
@@ -200,8 +200,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     // Per stream of each d-chunk: the projection (N = NP) and x.x^T (N = 64,
     // whose diagonal is each token's sum of squares), both into TMEM.
     if (lane == 0) {
-      constexpr uint32_t idesc_proj = idesc_bf16(kMmaM, C::kNP);
-      constexpr uint32_t idesc_ssq = idesc_bf16(kMmaM, kTileT);
+      constexpr uint32_t idesc_proj = F16 ? idesc_f16(kMmaM, C::kNP) : idesc_bf16(kMmaM, C::kNP);
+      constexpr uint32_t idesc_ssq = F16 ? idesc_f16(kMmaM, kTileT) : idesc_bf16(kMmaM, kTileT);
       int xs = 0, ws = 0, acc = 0;
       uint32_t xph = 0, wph = 0, acc_phase = 0;
       bool ok = true;
@@ -277,7 +277,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int e = 0; e < 16; ++e) {
           const int col = grp * 16 + e;
-          if (col < P * RR) mix[col % RR] += v[e];
+          if (col < P * RR) mix[col % RR] += F16 ? v[e] * plane_scale(true, col / RR) : v[e];
         }
       }
       float ssq = 0.0f;
@@ -458,18 +458,18 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int i = 0; i < NS; ++i) {
             const float m = coef[rowv[b] * NS + i];
-            const __nv_bfloat162* hh = reinterpret_cast<const __nv_bfloat162*>(&xv[b][i]);
+            const typename XType<F16>::T2* hh = reinterpret_cast<const typename XType<F16>::T2*>(&xv[b][i]);
 #pragma unroll
             for (int q2 = 0; q2 < 4; ++q2) {
-              const float2 f = __bfloat1622float2(hh[q2]);
+              const float2 f = XType<F16>::to_f2(hh[q2]);
               acc8[2 * q2] = fmaf(m, f.x, acc8[2 * q2]);
               acc8[2 * q2 + 1] = fmaf(m, f.y, acc8[2 * q2 + 1]);
             }
           }
           uint4 o;
-          __nv_bfloat162* ob = reinterpret_cast<__nv_bfloat162*>(&o);
+          typename XType<F16>::T2* ob = reinterpret_cast<typename XType<F16>::T2*>(&o);
 #pragma unroll
-          for (int q2 = 0; q2 < 4; ++q2) ob[q2] = __floats2bfloat162_rn(acc8[2 * q2], acc8[2 * q2 + 1]);
+          for (int q2 = 0; q2 < 4; ++q2) ob[q2] = XType<F16>::from_f2(acc8[2 * q2], acc8[2 * q2 + 1]);
           st_global_v4_hint(yt_out + (size_t)rowv[b] * g.D + dv[b], o, ystore_policy);
         }
       }
@@ -491,18 +491,23 @@ __global__ void __launch_bounds__(kThreads, 1)
   cluster_sync_all();
 }
 
-template <int NS, int RR, int P>
+template <int NS, int RR, int P, bool F16>
 const void* kernel_ptr() {
-  return reinterpret_cast<const void*>(&mhc_pre_tc_kernel<NS, RR, P>);
+  return reinterpret_cast<const void*>(&mhc_pre_tc_kernel<NS, RR, P, F16>);
 }
 
-const void* select_kernel(int n, int R, int P) {
+// bf16 x: every n; fp16 x: n = 4.
+const void* select_kernel(int n, int R, int P, bool fp16) {
 #define MHC_CASE(NS_, RR_, P_) \
-  if (n == NS_ && R == RR_ && P == P_) return kernel_ptr<NS_, RR_, P_>();
+  if (!fp16 && n == NS_ && R == RR_ && P == P_) return kernel_ptr<NS_, RR_, P_, false>();
+#define MHC_CASE16(NS_, RR_, P_) \
+  if (fp16 && n == NS_ && R == RR_ && P == P_) return kernel_ptr<NS_, RR_, P_, true>();
   MHC_CASE(4, 24, 3) MHC_CASE(4, 24, 2) MHC_CASE(4, 8, 3) MHC_CASE(4, 8, 2)
   MHC_CASE(6, 48, 3) MHC_CASE(6, 48, 2) MHC_CASE(6, 12, 3) MHC_CASE(6, 12, 2)
   MHC_CASE(8, 80, 3) MHC_CASE(8, 80, 2) MHC_CASE(8, 16, 3) MHC_CASE(8, 16, 2)
+  MHC_CASE16(4, 24, 3) MHC_CASE16(4, 24, 2) MHC_CASE16(4, 8, 3) MHC_CASE16(4, 8, 2)
 #undef MHC_CASE
+#undef MHC_CASE16
   return nullptr;
 }
 
@@ -526,9 +531,10 @@ cudaLaunchConfig_t cluster_config(int cluster, int grid, size_t smem, cudaStream
 
 int tc_np(int R, int P) { return ((P * R + 15) / 16) * 16; }
 
-cudaError_t tc_forward_occupancy(int n, int R, int P, size_t smem_bytes, int cluster, int* max_clusters) {
+cudaError_t tc_forward_occupancy(int n, int R, int P, bool fp16, size_t smem_bytes, int cluster,
+                                 int* max_clusters) {
   *max_clusters = 0;
-  const void* k = select_kernel(n, R, P);
+  const void* k = select_kernel(n, R, P, fp16);
   if (!k) return cudaErrorInvalidValue;
   cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_bytes);
   if (e != cudaSuccess) return e;
@@ -543,7 +549,7 @@ cudaError_t tc_forward_occupancy(int n, int R, int P, size_t smem_bytes, int clu
 
 cudaError_t launch_tc_forward(const TcLaunch& L, cudaStream_t s) {
   const int n = L.epi.n, R = L.epi.R;
-  const void* k = select_kernel(n, R, L.P);
+  const void* k = select_kernel(n, R, L.P, L.fp16 != 0);
   if (!k) return cudaErrorInvalidValue;
   Geometry g;
   g.T = L.epi.T;

@@ -254,6 +254,12 @@ __host__ __device__ constexpr uint32_t idesc_bf16(int M, int N) {
          (static_cast<uint32_t>(M >> 4) << 24);
 }
 
+// kind::f16 instruction descriptor with fp16 operands (A and B of one MMA
+// always share their type).
+__host__ __device__ constexpr uint32_t idesc_f16(int M, int N) {
+  return idesc_bf16(M, N) & ~((1u << 7) | (1u << 10));
+}
+
 // The same with the operands' major-ness chosen: bit 15 A, bit 16 B (1 = MN-major).
 __host__ __device__ constexpr uint32_t idesc_bf16_major(int M, int N, bool a_mn, bool b_mn) {
   return idesc_bf16(M, N) | (a_mn ? (1u << 15) : 0u) | (b_mn ? (1u << 16) : 0u);

@@ -137,13 +137,18 @@ WORKLOADS = {
 }
 
 
-def _x_tensor(seed, T, n, D, outliers, device):
+def _x_tensor(seed, T, n, D, outliers, device, dtype=None):
+    """x drawn N(0, 1) (with the decode workload's outliers), rounded to
+    bf16 (default) or to fp16 (round to nearest even in both)."""
+    dtype = torch.bfloat16 if dtype is None else dtype
     numel = T * n * D
     if numel <= SPLITMIX_X_LIMIT:
         v = normal(stream_key(seed, "x"), numel)
         if outliers:
             hit = uniform(stream_key(seed, "outlier"), numel) < 0.01
             v = np.where(hit, v * 20.0, v)
+        if dtype == torch.float16:
+            return torch.from_numpy(v.astype(np.float16).reshape(T, n, D)).to(device)
         bits = to_bf16_bits(v).view(np.int16).reshape(T, n, D)
         return torch.from_numpy(bits.copy()).view(torch.bfloat16).to(device)
     g = torch.Generator(device=device)
@@ -152,15 +157,17 @@ def _x_tensor(seed, T, n, D, outliers, device):
     if outliers:
         hit = torch.rand((T, n, D), generator=g, device=device) < 0.01
         x = torch.where(hit, x * 20.0, x)
-    return x.to(torch.bfloat16)
+    return x.to(dtype)
 
 
 def make_case(name: str, *, seed: int = 0, device="cpu", T: Optional[int] = None,
               n: Optional[int] = None, D: Optional[int] = None,
               impl_mode: Optional[int] = None, num_iters: int = 20,
               need_backward: Optional[bool] = None, gamma: Optional[bool] = None,
-              pre_mix: Optional[bool] = None, alpha_len: Optional[int] = None) -> Case:
-    """Build a workload by name; any shape or flag may be overridden."""
+              pre_mix: Optional[bool] = None, alpha_len: Optional[int] = None,
+              x_dtype=None) -> Case:
+    """Build a workload by name; any shape or flag may be overridden
+    (x_dtype: torch.bfloat16, the default, or torch.float16)."""
     w = dict(WORKLOADS[name])
     T = w["T"] if T is None else T
     n = w["n"] if n is None else n
@@ -171,7 +178,7 @@ def make_case(name: str, *, seed: int = 0, device="cpu", T: Optional[int] = None
     R_full = n * n + 2 * n
     R = R_full if alpha_len == 3 else 2 * n
 
-    x = _x_tensor(seed, T, n, D, w.get("outliers", False), device)
+    x = _x_tensor(seed, T, n, D, w.get("outliers", False), device, x_dtype)
     # phi: N(0, 1/sqrt(K)) over the full [n^2+2n, K] matrix; the two-gate
     # variant takes its first 2n rows (same stream, so rows agree).
     phi_full = normal(stream_key(seed, "phi"), R_full * K, std=1.0 / math.sqrt(K))

@@ -4,7 +4,9 @@ tolerances.
 
 Tolerances (against the double-precision oracle):
   * hPre, hPost, comb: max |err| <= 1e-4 (fp32 mode), <= 3e-3 (tf32 mode);
-  * y (bf16): |err| <= 2^-7 |ref| + 1e-3 elementwise;
+  * y (bf16 or fp16): |err| <= 2^-7 |ref| + 1e-3 elementwise, plus, in tf32
+    mode, 3e-3 * sum_i |x_i| (y = sum_i hPre_i x_i and hPre may be off by
+    3e-3 there);
   * intermediates (fp32 mode): invRms rel 1e-4; hMix |err| <= 2e-4 (1 + |ref|)
     -- fp32 accumulation over n*D products; sumOut rel 1e-4; normOut 1e-4.
     The invRms bound: Sigma x^2 is accumulated on the tensor core in fp32
@@ -25,9 +27,11 @@ TOL = {0: 1e-4, 1: 3e-3}
 
 
 def run_cuda(case, stream=None, out=None, op=None):
+    from mhc_hyper_connection_gb300 import MHC_DTYPE_BF16, MHC_DTYPE_FP16
     op = op or MhcPre(case.n, case.D, alpha_len=case.alpha_len, num_iters=case.num_iters,
                       norm_eps=case.norm_eps, hc_eps=case.hc_eps, impl_mode=case.impl_mode,
-                      need_backward=case.need_backward)
+                      need_backward=case.need_backward,
+                      x_dtype=MHC_DTYPE_FP16 if case.x.dtype == torch.float16 else MHC_DTYPE_BF16)
     if out is None:
         out = op.allocate(case.T, case.x.device)
     op.run(case.x, case.phi, case.alpha, case.bias, out, gamma=case.gamma,
@@ -51,7 +55,7 @@ def run_oracle(case, tokens=None, hf32=False):
                       case.bias.cpu().numpy(),
                       None if case.gamma is None else case.gamma.cpu().numpy(), pm,
                       num_iters=case.num_iters, norm_eps=case.norm_eps, hc_eps=case.hc_eps,
-                      hf32=hf32, backward=case.need_backward)
+                      hf32=hf32, backward=case.need_backward, x_fp16=case.x.dtype == torch.float16)
 
 
 def _sel(t, tokens, axis=0):
@@ -77,6 +81,11 @@ def compare(case, out, ref, tokens=None, tol=None, check_intermediates=True):
             assert errs[k] <= tol, f"{case.name}: {k} max err {errs[k]:.3g} > {tol}"
     y = _sel(out["y"], tokens).astype(np.float64)
     bound = 2.0 ** -7 * np.abs(ref.y) + 1e-3
+    if case.impl_mode == 1 and case.pre_mix is None:
+        # tf32 mode: the weights hPre carry up to TOL[1] of error, so y =
+        # sum_i hPre_i x_i may carry TOL[1] * sum_i |x_i| on top
+        xs = case.x if tokens is None else case.x[torch.as_tensor(tokens, device=case.x.device)]
+        bound = bound + TOL[1] * xs.float().abs().sum(dim=1).cpu().numpy().astype(np.float64)
     bad = np.abs(y - ref.y) > bound
     errs["y_viol"] = int(bad.sum())
     errs["y"] = float(np.abs(y - ref.y).max())

@@ -40,7 +40,7 @@ def test_tiny_iterations(cuda_device, iters):
 
 def test_training_shaped_with_backward_outputs(cuda_device):
     out, errs = _full(make_case("training", device=cuda_device))
-    assert errs["inv_rms"] <= 1e-5
+    assert errs["inv_rms"] <= 1e-4
 
 
 def test_decode_shaped_outliers(cuda_device):
