@@ -199,7 +199,8 @@ def oracle_rate(case, budget_s: float, max_tokens: int):
     done, t_total, passes = 0, 0.0, 0
     while passes == 0 or t_total < budget_s:
         t0 = time.perf_counter()
-        oracle.run(x, phi, alpha, bias, num_iters=case.num_iters, backward=False, threads=threads)
+        oracle.run(x, phi, alpha, bias, num_iters=case.num_iters, backward=False, threads=threads,
+                   x_fp16=case.x.dtype == torch.float16)
         t_total += time.perf_counter() - t0
         done += count
         passes += 1
@@ -532,6 +533,10 @@ def main():
     ap.add_argument("--tokens", type=int, default=WORKLOAD["T"])
     ap.add_argument("--mode", type=int, default=WORKLOAD["impl_mode"], choices=[0, 1])
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--x-dtype", choices=["bf16", "fp16"], default="bf16",
+                    help="element type of x and y (forward)")
+    ap.add_argument("--batch-consistent", action="store_true",
+                    help="forward in batch-consistent mode (results per token independent of T)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--op", choices=["pre", "post", "bwd"], default="pre",
                     help="pre: the pre-mapping forward (the headline); post: the post-mapping (hc_post); "
@@ -557,6 +562,10 @@ def main():
            "tokens_per_rank": T, "n": n, "D": D, "num_iters": 20, "impl_mode": mode_name,
            "gamma": None, "l2": "inputs (2.35 GB/step) exceed L2; no flush needed",
            "parallelism": f"token-sharded x{world} (no collective)"}
+    if args.x_dtype != "bf16" or args.batch_consistent:
+        cfg["x_dtype"] = args.x_dtype
+        cfg["batch_consistent"] = bool(args.batch_consistent)
+        cfg["workload"] += f" x={args.x_dtype}" + (" batch-consistent" if args.batch_consistent else "")
 
     if args.op == "post":
         return bench_post(args, device, world, rank, local)
@@ -585,10 +594,12 @@ def main():
 
     from mhc_hyper_connection_gb300 import (MhcPre, mhc_pre_last_kernel, mhc_pre_last_launch,
                                             mhc_pre_set_profile_events)
-    from mhc_hyper_connection_gb300 import build as mbuild
+    from mhc_hyper_connection_gb300 import build as mbuild, MHC_DTYPE_BF16, MHC_DTYPE_FP16
     mbuild.build()
-    case = make_case("prefill", device=device, T=T, impl_mode=args.mode, seed=rank)
-    op = MhcPre(n, D, alpha_len=3, num_iters=20, impl_mode=args.mode)
+    xdt = torch.float16 if args.x_dtype == "fp16" else torch.bfloat16
+    case = make_case("prefill", device=device, T=T, impl_mode=args.mode, seed=rank, x_dtype=xdt)
+    op = MhcPre(n, D, alpha_len=3, num_iters=20, impl_mode=args.mode, batch_consistent=args.batch_consistent,
+                x_dtype=MHC_DTYPE_FP16 if args.x_dtype == "fp16" else MHC_DTYPE_BF16)
     out = op.allocate(T, device)
     stream = torch.cuda.current_stream(device)
 
@@ -710,7 +721,7 @@ def main():
     if rank == 0:
         line = {"metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
                 "steps": K, "warmup": args.warmup, "ms_per_step": elapsed_max / K * 1e3,
-                "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+                "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": args.x_dtype,
                 "data": "synthetic", "config": cfg,
                 "hbm_gbs_step": lb / (elapsed_max / K) / 1e9,
                 "roofline": roof, "cpu_baseline": cpu, "e2e": e2e,
