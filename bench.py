@@ -535,6 +535,8 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--x-dtype", choices=["bf16", "fp16"], default="bf16",
                     help="element type of x and y (forward)")
+    ap.add_argument("--route", choices=["fused", "composite"], default="fused",
+                    help="forward: the fused kernel, or the composite three-launch route (a debug aid)")
     ap.add_argument("--batch-consistent", action="store_true",
                     help="forward in batch-consistent mode (results per token independent of T)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -562,6 +564,9 @@ def main():
            "tokens_per_rank": T, "n": n, "D": D, "num_iters": 20, "impl_mode": mode_name,
            "gamma": None, "l2": "inputs (2.35 GB/step) exceed L2; no flush needed",
            "parallelism": f"token-sharded x{world} (no collective)"}
+    if args.route == "composite":
+        cfg["route"] = "composite (inv_rms, mixes, sinkhorn launches)"
+        cfg["workload"] += " composite route"
     if args.x_dtype != "bf16" or args.batch_consistent:
         cfg["x_dtype"] = args.x_dtype
         cfg["batch_consistent"] = bool(args.batch_consistent)
@@ -604,7 +609,10 @@ def main():
     stream = torch.cuda.current_stream(device)
 
     def step():
-        op.run(case.x, case.phi, case.alpha, case.bias, out, stream=stream)
+        if args.route == "composite":
+            op.run_composite(case.x, case.phi, case.alpha, case.bias, out, stream=stream)
+        else:
+            op.run(case.x, case.phi, case.alpha, case.bias, out, stream=stream)
 
     for _ in range(args.warmup):
         step()
@@ -648,6 +656,10 @@ def main():
     elapsed = e0.elapsed_time(e1) / 1e3
     kern = sum(a.elapsed_time(b) for a, b in ev_k) / K / 1e3
     elapsed_max = max_over_ranks(elapsed, world, device)
+    if args.route == "composite":
+        # three launches and no single fused kernel: the roofline is the route's
+        cfg["launch"] = {"kernel": "composite route (stage_inv_rms, stage_mixes, stage_sinkhorn)"}
+        kern = elapsed_max / K
     value = world * T * K / elapsed_max
 
     # ---- end to end through the C ABI with host buffers
@@ -708,7 +720,7 @@ def main():
     achieved = lb / kern / 1e9
     kernel = cfg["launch"]["kernel"]
     roof = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
-            "frac": achieved / peak, "traffic": recorded_traffic(kernel, T),
+            "frac": achieved / peak, "traffic": recorded_traffic(kernel, T) if kernel in KERNEL_SOURCES else None,
             "kernel": kernel, "kernel_ms": kern * 1e3,
             "algorithmic_bytes": lb, "peak_source": f"hbm_gbs of {peak_src}"}
 
@@ -725,7 +737,7 @@ def main():
                 "data": "synthetic", "config": cfg,
                 "hbm_gbs_step": lb / (elapsed_max / K) / 1e9,
                 "roofline": roof, "cpu_baseline": cpu, "e2e": e2e,
-                "gpu_launches": 2 * K * world, "clocks": clocks.summary()}
+                "gpu_launches": (3 if args.route == "composite" else 2) * K * world, "clocks": clocks.summary()}
         print(json.dumps(line))
     if world > 1:
         torch.distributed.destroy_process_group()

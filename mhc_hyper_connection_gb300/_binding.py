@@ -95,6 +95,12 @@ def library() -> ctypes.CDLL:
             lib.mhc_pre_backward_workspace_size.restype = ctypes.c_int32
             lib.mhc_pre_backward_run.argtypes = [_P, ctypes.POINTER(MhcPreBwdArgs), _P]
             lib.mhc_pre_backward_run.restype = ctypes.c_int32
+            lib.mhc_pre_inv_rms_run.argtypes = [_P, ctypes.c_int64, _P, _P, _P]
+            lib.mhc_pre_inv_rms_run.restype = ctypes.c_int32
+            lib.mhc_pre_mixes_run.argtypes = [_P, ctypes.c_int64, _P, _P, _P, _P, _P]
+            lib.mhc_pre_mixes_run.restype = ctypes.c_int32
+            lib.mhc_pre_sinkhorn_run.argtypes = [_P, ctypes.POINTER(MhcPreArgs), _P, _P, _P]
+            lib.mhc_pre_sinkhorn_run.restype = ctypes.c_int32
             lib.mhc_pre_last_kernel.argtypes = [_P]
             lib.mhc_pre_last_kernel.restype = ctypes.c_char_p
             lib.mhc_pre_destroy.argtypes = [_P]
@@ -193,6 +199,20 @@ def mhc_pre_backward_workspace_size(handle, T: int):
 
 def mhc_pre_backward_run(handle, args: MhcPreBwdArgs, stream: int = 0) -> int:
     return library().mhc_pre_backward_run(handle, ctypes.byref(args), _P(stream or None))
+
+
+def mhc_pre_inv_rms_run(handle, T: int, x: int, inv_rms: int, stream: int = 0) -> int:
+    return library().mhc_pre_inv_rms_run(handle, int(T), _P(x or None), _P(inv_rms or None), _P(stream or None))
+
+
+def mhc_pre_mixes_run(handle, T: int, x: int, phi: int, gamma: int, mixes: int, stream: int = 0) -> int:
+    return library().mhc_pre_mixes_run(handle, int(T), _P(x or None), _P(phi or None), _P(gamma or None),
+                                       _P(mixes or None), _P(stream or None))
+
+
+def mhc_pre_sinkhorn_run(handle, args: MhcPreArgs, mixes: int, inv_rms: int, stream: int = 0) -> int:
+    return library().mhc_pre_sinkhorn_run(handle, ctypes.byref(args), _P(mixes or None), _P(inv_rms or None),
+                                          _P(stream or None))
 
 
 def mhc_pre_destroy(handle) -> None:
@@ -375,6 +395,32 @@ class MhcPre:
         if st != MHC_OK:
             raise MhcError(st, "mhc_pre_backward_run", last_error())
         return grads
+
+    def run_composite(self, x, phi, alpha, bias, out, gamma=None, pre_mix=None, stream=None):
+        """The composite route (include/mhc_pre_stages.h): invRms, the mixes,
+        then gates + Sinkhorn + y, as three launches on `stream`; fills the
+        same outputs as run().  A debug aid: slower than the fused run()."""
+        import torch
+        T = _tokens(x.shape[:-2])
+        if stream is None:
+            stream = torch.cuda.current_stream(x.device).cuda_stream
+        elif hasattr(stream, "cuda_stream"):
+            stream = stream.cuda_stream
+        ir = out.get("inv_rms")
+        ir = ir if ir is not None else torch.empty((T,), dtype=torch.float32, device=x.device)
+        mx = out.get("h_mix")
+        mx = mx if mx is not None else torch.empty((T, self.R), dtype=torch.float32, device=x.device)
+        st = mhc_pre_inv_rms_run(self.handle, T, _ptr(x), _ptr(ir), int(stream))
+        if st != MHC_OK:
+            raise MhcError(st, "mhc_pre_inv_rms_run", last_error())
+        st = mhc_pre_mixes_run(self.handle, T, _ptr(x), _ptr(phi), _ptr(gamma), _ptr(mx), int(stream))
+        if st != MHC_OK:
+            raise MhcError(st, "mhc_pre_mixes_run", last_error())
+        args = self.make_args(x, phi, alpha, bias, out, gamma, pre_mix)
+        st = mhc_pre_sinkhorn_run(self.handle, args, _ptr(mx), _ptr(ir), int(stream))
+        if st != MHC_OK:
+            raise MhcError(st, "mhc_pre_sinkhorn_run", last_error())
+        return out
 
     def status(self, out=None, stream=None) -> int:
         ws = None if out is None else out.get("workspace")

@@ -118,12 +118,23 @@ __device__ __forceinline__ void sinkhorn_row(float* P, float eps, bool wb, float
 // the RMS reciprocal.  RR = NS*NS + 2*NS is the three-gate form, RR = 2*NS
 // the two-gate form (hPost + hcEps, no residual path).
 template <int NS, int RR>
+__device__ __forceinline__ float token_gates_r(const EpiParams& p, int t, const float (&mix)[RR], float inv_rms,
+                                               bool write, float (&coef)[NS]);
+
+template <int NS, int RR>
 __device__ __forceinline__ float token_gates(const EpiParams& p, int t, const float (&mix)[RR], float ssq,
                                              bool write, float (&coef)[NS]) {
+  const float K = (float)(NS * p.D);
+  return token_gates_r<NS, RR>(p, t, mix, __frsqrt_rn(ssq / K + p.norm_eps), write, coef);
+}
+
+// The same gates from a given RMS reciprocal (the composite route's
+// Sinkhorn stage receives it from its own stage).
+template <int NS, int RR>
+__device__ __forceinline__ float token_gates_r(const EpiParams& p, int t, const float (&mix)[RR], float inv_rms,
+                                               bool write, float (&coef)[NS]) {
   constexpr bool kThree = (RR == NS * NS + 2 * NS);
   static_assert(kThree || RR == 2 * NS, "R must be n*n+2n or 2n");
-  const float K = (float)(NS * p.D);
-  const float inv_rms = __frsqrt_rn(ssq / K + p.norm_eps);
   const float hc_eps = p.hc_eps;
   const float a0 = __ldg(p.alpha), a1 = __ldg(p.alpha + 1);
   if (write) {
@@ -361,6 +372,25 @@ struct PostLaunch {
   void* out;               // bf16 [T, n, D]
 };
 cudaError_t launch_post(const PostLaunch& L, cudaStream_t s);
+
+// ---------------------------------------------------------------------------
+// Composite route (the pages' two-operator path, a debug aid): invRms, the
+// projection ("mixes"), then gates + Sinkhorn + y from them.
+struct StageLaunch {
+  int T, n, D, R, fp16;
+  float norm_eps;
+  const void* x;               // [T, n, D] bf16 or fp16
+  const float* phi;            // [R, nD]
+  const float* gamma;          // [nD] or null
+  float* inv_rms;              // [T]
+  float* mixes;                // [T, R]
+};
+cudaError_t launch_stage_inv_rms(const StageLaunch& L, cudaStream_t s);
+cudaError_t launch_stage_mixes(const StageLaunch& L, cudaStream_t s);
+// ep holds the outputs (y, h_post, h_res, h_pre, sum_out, norm_out and, when
+// set, copies of inv_rms / h_mix); mixes and inv_rms are the stage inputs.
+cudaError_t launch_stage_sinkhorn(const EpiParams& ep, const void* x, const float* mixes, const float* inv_rms,
+                                  int fp16, cudaStream_t s);
 
 // Resolved by the kernel translation unit for the given (n, R, P).
 cudaError_t launch_tc_forward(const TcLaunch& L, cudaStream_t s);

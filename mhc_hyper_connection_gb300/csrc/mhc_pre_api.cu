@@ -15,6 +15,7 @@
 #include "../../include/mhc_pre.h"
 #include "../../include/mhc_post.h"
 #include "../../include/mhc_pre_backward.h"
+#include "../../include/mhc_pre_stages.h"
 
 struct mhc_pre_s {
   mhc_pre_config cfg;
@@ -853,6 +854,111 @@ mhc_status_t mhc_pre_backward_run(mhc_pre_t h, const mhc_pre_bwd_args* a, void* 
   h->last_stages = stages;
   h->last_ystages = tblocks;
   h->last_kernel = "bw_main_kernel";
+  return MHC_OK;
+}
+
+}  // extern "C"
+
+// ---------------------------------------------------------- composite route
+namespace {
+
+mhc_status_t stage_device(cudaStream_t* s, void* stream) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return fail(MHC_ERR_RUNTIME, "no CUDA device");
+  if (!device_info(dev).ok) return fail(MHC_ERR_RUNTIME, "device %d is not an sm_103 GPU", dev);
+  *s = static_cast<cudaStream_t>(stream);
+  return MHC_OK;
+}
+
+mhc::StageLaunch stage_launch(const mhc_pre_s* h, int64_t T, const void* x) {
+  mhc::StageLaunch L;
+  memset(&L, 0, sizeof L);
+  L.T = (int)T;
+  L.n = (int)h->cfg.n;
+  L.D = (int)h->cfg.D;
+  L.R = h->R;
+  L.fp16 = h->cfg.x_dtype == MHC_DTYPE_FP16 ? 1 : 0;
+  L.norm_eps = (float)h->cfg.norm_eps;
+  L.x = x;
+  return L;
+}
+
+}  // namespace
+
+extern "C" {
+
+mhc_status_t mhc_pre_inv_rms_run(mhc_pre_t h, int64_t T, const void* x, float* inv_rms, void* stream) {
+  g_last_error[0] = 0;
+  if (!h) return fail(MHC_ERR_NULLPTR, "handle must be non-NULL");
+  if (T < 0 || T > (int64_t(1) << 30)) return fail(MHC_ERR_PARAM_INVALID, "T must be in [0, 2^30]");
+  if (T == 0) return MHC_OK;
+  if (!x || !inv_rms) return fail(MHC_ERR_NULLPTR, "x and inv_rms are required");
+  if (!aligned(x, 16) || !aligned(inv_rms, 4)) return fail(MHC_ERR_PARAM_INVALID, "x must be 16-byte aligned");
+  cudaStream_t s;
+  const mhc_status_t st = stage_device(&s, stream);
+  if (st != MHC_OK) return st;
+  mhc::StageLaunch L = stage_launch(h, T, x);
+  L.inv_rms = inv_rms;
+  if (mhc::launch_stage_inv_rms(L, s) != cudaSuccess)
+    return fail(MHC_ERR_RUNTIME, "inv_rms launch failed: %s", cudaGetErrorString(cudaGetLastError()));
+  return MHC_OK;
+}
+
+mhc_status_t mhc_pre_mixes_run(mhc_pre_t h, int64_t T, const void* x, const float* phi, const float* gamma,
+                               float* mixes, void* stream) {
+  g_last_error[0] = 0;
+  if (!h) return fail(MHC_ERR_NULLPTR, "handle must be non-NULL");
+  if (T < 0 || T > (int64_t(1) << 30)) return fail(MHC_ERR_PARAM_INVALID, "T must be in [0, 2^30]");
+  if (T == 0) return MHC_OK;
+  if (!x || !phi || !mixes) return fail(MHC_ERR_NULLPTR, "x, phi and mixes are required");
+  if (!aligned(x, 16)) return fail(MHC_ERR_PARAM_INVALID, "x must be 16-byte aligned");
+  if (!aligned(phi, 4) || !aligned(mixes, 4) || (gamma && !aligned(gamma, 4)))
+    return fail(MHC_ERR_PARAM_INVALID, "fp32 tensors must be 4-byte aligned");
+  cudaStream_t s;
+  const mhc_status_t st = stage_device(&s, stream);
+  if (st != MHC_OK) return st;
+  mhc::StageLaunch L = stage_launch(h, T, x);
+  L.phi = phi;
+  L.gamma = gamma;
+  L.mixes = mixes;
+  if (mhc::launch_stage_mixes(L, s) != cudaSuccess)
+    return fail(MHC_ERR_RUNTIME, "mixes launch failed: %s", cudaGetErrorString(cudaGetLastError()));
+  return MHC_OK;
+}
+
+mhc_status_t mhc_pre_sinkhorn_run(mhc_pre_t h, const mhc_pre_args* a, const float* mixes, const float* inv_rms,
+                                  void* stream) {
+  g_last_error[0] = 0;
+  if (!h || !a) return fail(MHC_ERR_NULLPTR, "handle and args must be non-NULL");
+  const mhc_pre_config& c = h->cfg;
+  const int64_t T = a->T;
+  if (T < 0 || T > (int64_t(1) << 30)) return fail(MHC_ERR_PARAM_INVALID, "T must be in [0, 2^30]");
+  if (T == 0) return MHC_OK;
+  if (!a->x || !a->alpha || !a->bias || !a->y || !a->h_post || !mixes || !inv_rms)
+    return fail(MHC_ERR_NULLPTR, "x, alpha, bias, y, h_post, mixes and inv_rms are required");
+  if (c.alpha_len == 3 && !a->h_res) return fail(MHC_ERR_NULLPTR, "h_res is required with alpha of length 3");
+  if (a->pre_mix && !a->h_pre) return fail(MHC_ERR_NULLPTR, "h_pre is required when pre_mix is given");
+  if (c.need_backward) {
+    if (!a->h_pre || !a->inv_rms || !a->h_mix)
+      return fail(MHC_ERR_NULLPTR, "need_backward: h_pre, inv_rms and h_mix are required");
+    if (c.alpha_len == 3 && (!a->sum_out || !a->norm_out))
+      return fail(MHC_ERR_NULLPTR, "need_backward: sum_out and norm_out are required");
+    if (c.alpha_len == 2 && (a->sum_out || a->norm_out))
+      return fail(MHC_ERR_PARAM_INVALID, "sum_out / norm_out do not exist without the residual path");
+  } else if (a->inv_rms || a->h_mix || a->sum_out || a->norm_out) {
+    return fail(MHC_ERR_PARAM_INVALID, "inv_rms, h_mix, sum_out, norm_out must be NULL unless need_backward");
+  }
+  if (!aligned(a->x, 16) || !aligned(a->y, 16)) return fail(MHC_ERR_PARAM_INVALID, "x and y must be 16-byte aligned");
+  const void* f32[] = {a->alpha, a->bias, a->pre_mix, a->h_post, a->h_res, a->h_pre, a->inv_rms,
+                       a->h_mix, a->sum_out, a->norm_out, mixes, inv_rms};
+  for (const void* p : f32)
+    if (p && !aligned(p, 4)) return fail(MHC_ERR_PARAM_INVALID, "fp32 tensors must be 4-byte aligned");
+  cudaStream_t s;
+  const mhc_status_t st = stage_device(&s, stream);
+  if (st != MHC_OK) return st;
+  const mhc::EpiParams ep = epi_params(h, a);
+  if (mhc::launch_stage_sinkhorn(ep, a->x, mixes, inv_rms, c.x_dtype == MHC_DTYPE_FP16 ? 1 : 0, s) != cudaSuccess)
+    return fail(MHC_ERR_RUNTIME, "sinkhorn-stage launch failed: %s", cudaGetErrorString(cudaGetLastError()));
   return MHC_OK;
 }
 

@@ -11,7 +11,8 @@ import mhc_hyper_connection_gb300 as mp
 from mhc_hyper_connection_gb300 import build as mbuild
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
-HEADERS = [os.path.join(ROOT, "include", h) for h in ("mhc_pre.h", "mhc_post.h", "mhc_pre_backward.h")]
+HEADERS = [os.path.join(ROOT, "include", h)
+           for h in ("mhc_pre.h", "mhc_post.h", "mhc_pre_backward.h", "mhc_pre_stages.h")]
 
 
 @pytest.fixture(scope="module")
@@ -297,3 +298,22 @@ def test_binding_refuses_non_contiguous_and_bad_layouts(lib):
     with pytest.raises(ValueError):
         _tokens((2, 3, 4))
     op.close()
+
+
+def test_composite_route_host_validation(lib):
+    h = _handle(D=256)
+    A = 1 << 20
+    assert mp.mhc_pre_inv_rms_run(h, 0, 0, 0) == mp.MHC_OK
+    assert mp.mhc_pre_inv_rms_run(h, 4, 0, A) == mp.MHC_ERR_NULLPTR
+    assert mp.mhc_pre_inv_rms_run(h, 4, A + 8, A) == mp.MHC_ERR_PARAM_INVALID
+    assert mp.mhc_pre_inv_rms_run(h, -1, A, A) == mp.MHC_ERR_PARAM_INVALID
+    assert mp.mhc_pre_mixes_run(h, 4, A, 0, 0, A) == mp.MHC_ERR_NULLPTR
+    assert mp.mhc_pre_mixes_run(h, 4, A, A + 2, 0, A) == mp.MHC_ERR_PARAM_INVALID
+    assert mp.mhc_pre_sinkhorn_run(h, _args(), 0, A) == mp.MHC_ERR_NULLPTR
+    assert mp.mhc_pre_sinkhorn_run(h, _args(y=A + 2), A, A) == mp.MHC_ERR_PARAM_INVALID
+    assert mp.mhc_pre_sinkhorn_run(h, _args(T=0), 0, 0) == mp.MHC_OK
+    import torch
+    if not torch.cuda.is_available():
+        assert mp.mhc_pre_inv_rms_run(h, 4, A, A) == mp.MHC_ERR_RUNTIME
+        assert mp.mhc_pre_sinkhorn_run(h, _args(), A, A) == mp.MHC_ERR_RUNTIME
+    mp.mhc_pre_destroy(h)
