@@ -378,7 +378,7 @@ def bwd_oracle_rate(case, saved, g, budget_s: float, max_tokens: int):
 
 def bench_bwd(args, device, world, rank, local):
     """The backward at the prefill shape (Sinkhorn form, no gamma): device-timed
-    steps of the four launches, the roofline of the contraction kernel, an
+    steps of the five launches, the roofline of the contraction kernel, an
     end-to-end number with host buffers, and the oracle on host cores."""
     import torch
     T, n, D = args.tokens, WORKLOAD["n"], WORKLOAD["D"]
@@ -510,7 +510,7 @@ def bench_bwd(args, device, world, rank, local):
             "steps": K, "warmup": args.warmup, "ms_per_step": per_step * 1e3, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic", "config": cfg,
             "hbm_gbs_step": lb_step / per_step / 1e9, "hbm_frac_step": lb_step / per_step / 1e9 / peak,
-            "roofline": roof, "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": 4 * K * world,
+            "roofline": roof, "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": 5 * K * world,
             "clocks": clocks.summary()}))
     if world > 1:
         torch.distributed.destroy_process_group()

@@ -84,11 +84,12 @@ typedef struct {
  * scope above. */
 MHC_API mhc_status_t mhc_pre_backward_workspace_size(mhc_pre_t h, int64_t T, size_t *bytes);
 
-/* Second phase: validate, then enqueue four kernels on `stream` (a
- * cudaStream_t, NULL = legacy default): the phi . gamma planes, the per-token
- * stage (3.1-3.5 and the Sinkhorn backward), the contraction kernel (3.6-3.8
- * and the per-range partial sums of grad_phi) and the fixed-order
- * reductions.  Asynchronous; the inputs must stay valid until the stream
+/* Second phase: validate, then enqueue five kernels on `stream` (a
+ * cudaStream_t, NULL = legacy default): the phi . gamma planes, the row dot
+ * products grad_h_in . x (stage 3.1), the per-token stage (3.2-3.5 and the
+ * Sinkhorn backward), the contraction kernel (3.6-3.8 and the per-unit
+ * partial sums of grad_phi) and the fixed-order reductions.  Asynchronous;
+ * the inputs must stay valid until the stream
  * reaches the end of this call.  MHC_ERR_NULLPTR for a missing required
  * pointer, MHC_ERR_PARAM_INVALID for a shape, alignment, optional-group or
  * workspace-size problem, MHC_ERR_RUNTIME for a launch failure

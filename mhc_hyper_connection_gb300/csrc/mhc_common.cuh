@@ -477,7 +477,7 @@ cudaError_t gw_forward_capacity(int n, int R, int P, size_t smem_bytes, int* max
 cudaError_t launch_gw_forward(const GwLaunch& L, cudaStream_t s);
 
 // ---------------------------------------------------------------------------
-// Backward of the pre-mapping (n = 4, three gates).  Four launches:
+// Backward of the pre-mapping (n = 4, three gates).  Five launches:
 //  1. planes: phi . gamma per 64-column slab as P bf16 planes, row-padded to
 //     kBwRp rows, swizzled for the tensor core; zeroes the header;
 //  2. row dot: H_pre_grad[t][i] = grad_h_in[t] . x[t][i] (whole rows streamed
