@@ -7,12 +7,11 @@
 // scale each stream by its row sum).
 //
 // A pure streaming op: per token it reads 2D + 2nD bytes and writes 2nD,
-// against (n + n^2) coefficients.  One CTA takes a token at a time (grid
-// stride over tokens): the token's coefficients go to shared memory, then
-// each thread forms all n outputs of a few 16-byte column vectors, issuing
-// all their n + 1 loads each before any arithmetic; fp32 accumulation,
-// RN-even bf16 rounding.  Loads of x and residual are marked evict-first
-// (read once), as are the stores.
+// against (n + n^2) coefficients.  One warp takes a token at a time (grid
+// stride over tokens, no block-wide barrier); each lane forms all n outputs
+// of a few 16-byte column vectors, issuing all their n + 1 loads each before
+// any arithmetic; fp32 accumulation, RN-even bf16 rounding.  Loads of x and
+// residual are marked evict-first (read once), as are the stores.
 #include "mhc_ptx.cuh"
 
 namespace mhc {
@@ -20,28 +19,33 @@ namespace {
 
 constexpr int kPostThreads = 256;
 
+// One warp per token (grid stride over tokens, no block-wide barrier): each
+// lane loads the token's n + n^2 coefficients through the read-only cache
+// (the same addresses across the warp), then forms all n outputs of kV
+// 16-byte column vectors per pass with all their loads in flight.
 template <int NS>
 __global__ void __launch_bounds__(kPostThreads)
     mhc_post_kernel(int T, int D, const __nv_bfloat16* __restrict__ x, const __nv_bfloat16* __restrict__ res,
                     const float* __restrict__ post, const float* __restrict__ comb, __nv_bfloat16* __restrict__ out) {
-  __shared__ float co[NS + NS * NS];          // post[j], then comb[i][j]
+  constexpr int kV = NS <= 4 ? 4 : 2;
+  const int lane = threadIdx.x & 31;
+  const int gw = (blockIdx.x * kPostThreads + threadIdx.x) >> 5, nw = (gridDim.x * kPostThreads) >> 5;
   const int nv = D >> 3;                      // 16-byte vectors per row
   const uint64_t once = policy_evict_first();
-  for (int t = blockIdx.x; t < T; t += gridDim.x) {
-    __syncthreads();                          // the previous token's coefficients are no longer read
-    if (threadIdx.x < NS) co[threadIdx.x] = __ldg(post + (size_t)t * NS + threadIdx.x);
-    else if (threadIdx.x < NS + NS * NS) co[threadIdx.x] = __ldg(comb + (size_t)t * NS * NS + threadIdx.x - NS);
-    __syncthreads();
+  for (int t = gw; t < T; t += nw) {
+    float pc[NS], cm[NS * NS];
+#pragma unroll
+    for (int j = 0; j < NS; ++j) pc[j] = __ldg(post + (size_t)t * NS + j);
+#pragma unroll
+    for (int e = 0; e < NS * NS; ++e) cm[e] = __ldg(comb + (size_t)t * NS * NS + e);
     const __nv_bfloat16* xt = x + (size_t)t * D;
     const __nv_bfloat16* rt = res + (size_t)t * NS * D;
     __nv_bfloat16* ot = out + (size_t)t * NS * D;
-    // kV vectors per thread per pass, all their loads issued before any math
-    constexpr int kV = NS <= 4 ? 4 : 2;
-    for (int v0 = threadIdx.x; v0 < nv; v0 += kPostThreads * kV) {
+    for (int v0 = lane; v0 < nv; v0 += 32 * kV) {
       uint4 xv[kV], rv[kV][NS];
 #pragma unroll
       for (int q = 0; q < kV; ++q) {
-        const int v = v0 + q * kPostThreads;
+        const int v = v0 + q * 32;
         if (v < nv) {
           xv[q] = ld_global_v4_hint(xt + (size_t)v * 8, once);
 #pragma unroll
@@ -50,22 +54,21 @@ __global__ void __launch_bounds__(kPostThreads)
       }
 #pragma unroll
       for (int q = 0; q < kV; ++q) {
-        const int v = v0 + q * kPostThreads;
+        const int v = v0 + q * 32;
         if (v >= nv) continue;
 #pragma unroll
         for (int j = 0; j < NS; ++j) {
-          const float p = co[j];
           float acc[8];
           const __nv_bfloat162* hx = reinterpret_cast<const __nv_bfloat162*>(&xv[q]);
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
             const float2 f = __bfloat1622float2(hx[e]);
-            acc[2 * e] = p * f.x;
-            acc[2 * e + 1] = p * f.y;
+            acc[2 * e] = pc[j] * f.x;
+            acc[2 * e + 1] = pc[j] * f.y;
           }
 #pragma unroll
           for (int i = 0; i < NS; ++i) {
-            const float c = co[NS + i * NS + j];
+            const float c = cm[i * NS + j];
             const __nv_bfloat162* hr = reinterpret_cast<const __nv_bfloat162*>(&rv[q][i]);
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
@@ -95,7 +98,8 @@ cudaError_t launch_ns(const PostLaunch& L, cudaStream_t s) {
       cudaSuccess)
     return e;
   long long grid = (long long)sms * (per_sm > 0 ? per_sm : 1);
-  if (grid > L.T) grid = L.T;
+  const long long need = (L.T * 32 + kPostThreads - 1) / kPostThreads;   // one warp per token
+  if (grid > need) grid = need;
   mhc_post_kernel<NS><<<(int)grid, kPostThreads, 0, s>>>(
       (int)L.T, (int)L.D, static_cast<const __nv_bfloat16*>(L.x), static_cast<const __nv_bfloat16*>(L.residual),
       L.post, L.comb, static_cast<__nv_bfloat16*>(L.out));
