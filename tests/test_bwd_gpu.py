@@ -178,3 +178,21 @@ def test_prefill_sampled(cuda_device):
     toks = sample_tokens(32768, 16, seed=1, tile=64)
     cols = np.array(sorted({0, 63, 64, 7167, 7168, 14335, 20000, 28671}), dtype=np.int64)
     print(_check(S, grads, _run_oracle(S, tokens=toks, columns=cols), tokens=toks, columns=cols))
+
+
+def test_training_shape(cuda_device):
+    """The training workload (T = 4096, n = 4, D = 4096, gamma, alpha U(0.5,
+    1.5)): every output on sampled tokens and columns."""
+    S = _setup(cuda_device, 4096, 4096, gamma=True, seed=4, name="training")
+    grads = _run_gpu(S)
+    toks = sample_tokens(4096, 24, seed=2, tile=64)
+    cols = np.array(sorted({0, 5, 63, 64, 4095, 4096, 8191, 9000, 16383}), dtype=np.int64)
+    print(_check(S, grads, _run_oracle(S, tokens=toks, columns=cols), tokens=toks, columns=cols))
+
+
+@pytest.mark.parametrize("T", [16, 64])
+def test_decode_sized(cuda_device, T):
+    """Decode-sized batches at D = 7168: fewer token tiles than CTAs."""
+    S = _setup(cuda_device, T, 7168, gamma=False, seed=T, name="decode")
+    grads = _run_gpu(S)
+    print(_check(S, grads, _run_oracle(S)))
