@@ -341,6 +341,10 @@ constexpr int kXBytes = kBwNS * kBwTile * 128;    // x tile of all streams (32 K
 constexpr int kGinBytes = kBwTile * 128;          // grad_h_in tile (8 KB)
 constexpr int kGroups = kBwNS / 2;                // M = 128 columns = two streams
 constexpr int kHalf = kBwTile / 2;                // tokens per epilogue warp
+#ifndef MHC_BW_PREFETCH
+#define MHC_BW_PREFETCH 2
+#endif
+constexpr int kPrefetch = MHC_BW_PREFETCH;        // tiles of L2 prefetch ahead of the copy
 
 struct MainTail {
   uint64_t full[kMaxStages], empty[kMaxStages], out_ready[kMaxStages];
@@ -448,6 +452,14 @@ __global__ void __launch_bounds__(kMainThreads, 1)
         a_pending = true;
         ++piece;
         for (int tile = t0; tile < t1; ++tile) {
+          // L2 prefetch of the tile kPrefetch ahead: its later copy hits L2
+          if (kPrefetch > 0 && tile + kPrefetch < t1) {
+            const int pt = tile + kPrefetch;
+            tma_prefetch_l2_4d(&tmap_x, 0, pt * kBwTile, slab, 0);
+            if (kGxp) tma_prefetch_l2_4d(&tmap_gxp, 0, pt * kBwTile, slab, 0);
+            tma_prefetch_l2_3d(&tmap_gin, 0, pt * kBwTile, slab);
+            bulk_prefetch_l2(tiles + (size_t)pt * kRec, (uint32_t)kRec);
+          }
           if (!wait_bar_sleep(&tail->empty[s], ph ^ 1u, ctl, kErrWaitTimeout)) { ok = false; break; }
           uint8_t* st = sStage + (size_t)s * kStageBytes;
           mbar_expect_tx(&tail->full[s], (uint32_t)kStageBytes);
@@ -568,6 +580,19 @@ __global__ void __launch_bounds__(kMainThreads, 1)
     const int m = q * 32 + lane;              // row of the group (0..127)
     const int i = grp * 2 + (m >> 6);         // stream
     const int d = m & 63;                     // column of the slab
+    // Per-lane byte offsets of the epilogue's shared-memory accesses: x /
+    // grad_h_in / grad_x element pair (token half*32 + j + 4*odd, columns
+    // dp, dp+1) in the swizzled tile, and the (hPre_i, RMS factor) pair of
+    // that token; iteration e0 adds e0 rows (multiples of 8: the swizzle
+    // phase is unchanged).
+    const int odd = lane & 1, dp = d & ~1;
+    uint32_t xoff[4], soff[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int ej = j + 4 * odd;
+      xoff[j] = (uint32_t)((half * kHalf + ej) * 128) + ((uint32_t)((dp >> 3) ^ ej) << 4) + ((uint32_t)(dp & 7) << 1);
+      soff[j] = (uint32_t)((i * (2 * kBwTile) + 2 * (half * kHalf + ej)) * 4);
+    }
     int s = 0;
     uint32_t ph = 0;
     long long k = 0;
@@ -606,25 +631,23 @@ __global__ void __launch_bounds__(kMainThreads, 1)
         // Lanes 2p, 2p+1 hold columns d, d+1 (d even).  Each pair trades
         // one value so that the even lane forms both columns of token e and
         // the odd lane both columns of token e + 4 (rows 4 apart sit in
-        // different bank groups of the swizzle): 4-byte shared accesses.
-        const int odd = lane & 1;
-        const int dp = d & ~1;
-        const uint32_t pair_off = (uint32_t)(dp & 7) << 1;
+        // different bank groups of the swizzle): 4-byte shared accesses at
+        // per-lane offsets fixed for the kernel plus compile-time steps.
+        const uint8_t* xg = xs;
+        const uint8_t* gg = gin;
+        const uint8_t* sg = reinterpret_cast<const uint8_t*>(scal);
 #pragma unroll
         for (int e0 = 0; e0 < kHalf; e0 += 8) {
 #pragma unroll
           for (int j = 0; j < 4; ++j) {
-            const int ea = e0 + j, eb = ea + 4;
-            const float sendv = odd ? acc[ea] : acc[eb];
+            const float sendv = odd ? acc[e0 + j] : acc[e0 + j + 4];
             const float recv = __shfl_xor_sync(0xffffffffu, sendv, 1);
-            const float lo = odd ? recv : acc[ea];
-            const float hi = odd ? acc[eb] : recv;
-            const int e = odd ? eb : ea;
-            const int c = half * kHalf + e;
-            const uint32_t off = (uint32_t)(c * 128) + ((uint32_t)(((dp >> 3) ^ (e & 7))) << 4) + pair_off;
-            const float2 xf = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(xs + off));
-            const float2 gf = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(gin + off));
-            const float2 hc = *reinterpret_cast<const float2*>(scal + i * (2 * kBwTile) + 2 * c);   // (hPre_i, RMS factor)
+            const float lo = odd ? recv : acc[e0 + j];
+            const float hi = odd ? acc[e0 + j + 4] : recv;
+            const uint32_t off = xoff[j] + (uint32_t)(e0 * 128);
+            const float2 xf = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(xg + off));
+            const float2 gf = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(gg + off));
+            const float2 hc = *reinterpret_cast<const float2*>(sg + soff[j] + (uint32_t)(e0 * 8));
             float vlo = fmaf(hc.x, gf.x, lo), vhi = fmaf(hc.x, gf.y, hi);
             vlo = fmaf(hc.y, xf.x, vlo);
             vhi = fmaf(hc.y, xf.y, vhi);
