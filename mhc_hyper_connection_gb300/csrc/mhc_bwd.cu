@@ -240,18 +240,20 @@ __global__ void __launch_bounds__(kBwTokenWarps * 32) bw_token_kernel(BwTokenPar
         const int cnt = kh - klo + 1;
         __syncwarp();
         // the chunk's saved matrices and sums, eight loads in flight per lane
+        // (more raises the registers and costs occupancy: 25 measured slower)
         const int nm = cnt * NN, ntot = nm + cnt * NS;
-        for (int e0 = lane; e0 < ntot; e0 += 32 * 8) {
-          float v[8];
+        constexpr int kBatch = 8;
+        for (int e0 = lane; e0 < ntot; e0 += 32 * kBatch) {
+          float v[kBatch];
 #pragma unroll
-          for (int j = 0; j < 8; ++j) {
+          for (int j = 0; j < kBatch; ++j) {
             const int e = e0 + 32 * j;
             v[j] = 0.0f;
             if (e < nm) v[j] = __ldg(p.norm_out + ((size_t)(klo + e / NN) * p.T + t) * NN + e % NN);
             else if (e < ntot) v[j] = __ldg(p.sum_out + ((size_t)(klo + (e - nm) / NS) * p.T + t) * NS + (e - nm) % NS);
           }
 #pragma unroll
-          for (int j = 0; j < 8; ++j) {
+          for (int j = 0; j < kBatch; ++j) {
             const int e = e0 + 32 * j;
             if (e < nm) st[e / NN][e % NN] = v[j];
             else if (e < ntot) st[(e - nm) / NS][NN + (e - nm) % NS] = v[j];
