@@ -173,7 +173,7 @@ mhc::EpiParams epi_params(const mhc_pre_s* h, const mhc_pre_args* a) {
 // both busy (MHC_PRE_GW_GROUPS overrides).
 mhc_status_t run_grid_wide(mhc_pre_s* h, const mhc_pre_args* a, const DeviceInfo& di,
                            __nv_bfloat16* planes, cudaStream_t s) {
-  const int n = (int)h->cfg.n, D = (int)h->cfg.D, R = h->R, NP = h->NP;
+  const int n = (int)h->cfg.n, D = (int)h->cfg.D, R = h->R;
   const int nch = (D + mhc::kChunkK - 1) / mhc::kChunkK;
   const int num_tiles = (int)((a->T + mhc::kGwTile - 1) / mhc::kGwTile);
   const int sms = di.sms < kGwMaxGrid ? di.sms : kGwMaxGrid;

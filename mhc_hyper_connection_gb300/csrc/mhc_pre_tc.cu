@@ -99,7 +99,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int num_clusters = gridDim.x / CL;
   const int c0 = (int)((long long)rank * g.nd / CL);
   const int c1 = (int)((long long)(rank + 1) * g.nd / CL);
-  const int my_chunks = c1 - c0;                  // d-chunks owned by this CTA
   const int rpo = kTileT / CL;                    // tile rows each member reduces (owns)
   Ctl ctl{&tail->abort, err};
 
