@@ -456,41 +456,58 @@ def bench_bwd(args, device, world, rank, local):
     per_step = elapsed / K
 
     # ---- end to end with host buffers: every step copies its inputs in from
-    # pinned host memory and the five gradients back out, on one stream
+    # pinned host memory and the four fp32/bf16 gradients back out.  Steps are
+    # pipelined over three streams with two buffer sets (copy-in of step i+1,
+    # compute of step i, copy-out of step i-1 overlap).
     e2e = None
     if not args.no_e2e:
         names_in = [("x", case.x), ("g_in", g.g_in), ("g_post", g.g_post), ("g_res", g.g_res)] + \
                    [(k, v) for k, v in saved.items()]
         host_in = {k: v.cpu().pin_memory() for k, v in names_in}
-        dev_in = {k: torch.empty_like(v) for k, v in names_in}
+        dev_in = [{k: torch.empty_like(v) for k, v in names_in} for _ in range(2)]
         outs = ("grad_x", "grad_phi", "grad_alpha", "grad_bias")
-        host_out = {k: torch.empty_like(grads[k], device="cpu").pin_memory() for k in outs}
-        sv = {k: dev_in[k] for k in saved}
+        gsets = [grads, op.allocate_backward(T, device)]
+        host_out = [{k: torch.empty_like(grads[k], device="cpu").pin_memory() for k in outs} for _ in range(2)]
+        s_in, s_out = torch.cuda.Stream(device), torch.cuda.Stream(device)
+        ev = {k: [torch.cuda.Event(), torch.cuda.Event()] for k in ("in", "comp", "out")}
 
-        def e2e_step():
-            for k, v in host_in.items():
-                dev_in[k].copy_(v, non_blocking=True)
-            op.backward(dev_in["x"], case.phi, case.alpha, None, dev_in["g_in"], dev_in["g_post"],
-                        dev_in["g_res"], sv, grads, stream=stream)
-            for k in outs:
-                host_out[k].copy_(grads[k], non_blocking=True)
+        def e2e_steps(n_steps, first):
+            for i in range(n_steps):
+                bi = i % 2
+                if i >= 2 or not first:
+                    s_in.wait_event(ev["comp"][bi])          # buffer bi's inputs are free
+                with torch.cuda.stream(s_in):
+                    for k, v in host_in.items():
+                        dev_in[bi][k].copy_(v, non_blocking=True)
+                ev["in"][bi].record(s_in)
+                stream.wait_event(ev["in"][bi])
+                if i >= 2 or not first:
+                    stream.wait_event(ev["out"][bi])         # buffer bi's gradients are copied out
+                d = dev_in[bi]
+                op.backward(d["x"], case.phi, case.alpha, None, d["g_in"], d["g_post"], d["g_res"],
+                            {k: d[k] for k in saved}, gsets[bi], stream=stream)
+                ev["comp"][bi].record(stream)
+                s_out.wait_event(ev["comp"][bi])
+                with torch.cuda.stream(s_out):
+                    for k in outs:
+                        host_out[bi][k].copy_(gsets[bi][k], non_blocking=True)
+                ev["out"][bi].record(s_out)
 
-        e2e_step()
+        e2e_steps(2, True)
         torch.cuda.synchronize()
         Ke = max(3, min(K, 10))
         a = torch.cuda.Event(enable_timing=True)
         b = torch.cuda.Event(enable_timing=True)
-        a.record(stream)
-        for _ in range(Ke):
-            e2e_step()
-        b.record(stream)
+        a.record(s_in)
+        e2e_steps(Ke, False)
+        b.record(s_out)
         torch.cuda.synchronize()
         t_e2e = max_over_ranks(a.elapsed_time(b) / 1e3, world, device)
         h2d = sum(v.numel() * v.element_size() for v in host_in.values())
-        d2h = sum(v.numel() * v.element_size() for v in host_out.values())
+        d2h = sum(v.numel() * v.element_size() for v in host_out[0].values())
         e2e = {"value": world * T * Ke / t_e2e, "unit": "tokens/s", "h2d_bytes_per_step": h2d,
                "d2h_bytes_per_step": d2h, "steps": Ke}
-        del host_in, dev_in, host_out
+        del host_in, dev_in, host_out, gsets
 
     peak, peak_src = hbm_peak()
     lb_main = T * bwd_main_token_bytes(n, D)
