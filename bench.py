@@ -351,6 +351,19 @@ def bwd_inputs(device, T, n, D, seed, mode):
     return case, saved, g
 
 
+def allreduce_weight_grads(grads, world: int):
+    """Data-parallel backward: the weight gradients (grad_phi, grad_alpha,
+    grad_bias and grad_gamma when present) are sums over every rank's tokens,
+    the one exchange step of the sharded backward; grad_x stays per rank."""
+    if world <= 1:
+        return
+    import torch.distributed as dist
+    for k in ("grad_phi", "grad_alpha", "grad_bias", "grad_gamma"):
+        t = grads.get(k)
+        if t is not None:
+            dist.all_reduce(t, op=dist.ReduceOp.SUM)
+
+
 def bwd_oracle_rate(case, saved, g, budget_s: float, max_tokens: int):
     """Tokens/s of the backward oracle on all host cores over passes of a
     bounded token sample (all five gradients of that sample)."""
@@ -386,7 +399,7 @@ def bench_bwd(args, device, world, rank, local):
     cfg = {"workload": f"pre backward T={T} n={n} D={D} iters=20 {mode_name} Sinkhorn form (b=4, s=8192)",
            "tokens_per_rank": T, "n": n, "D": D, "num_iters": 20, "impl_mode": mode_name, "gamma": None,
            "grad_x_post": None, "l2": "inputs (4.3 GB/step) exceed L2; no flush needed",
-           "parallelism": f"token-sharded x{world} (grad_phi/alpha/bias/gamma would need a sum over ranks)"}
+           "parallelism": f"token-sharded x{world}" + (" + all-reduce of grad_phi/alpha/bias" if world > 1 else "")}
     from mhc_hyper_connection_gb300 import build as mbuild
     mbuild.build()
     case, saved, g = bwd_inputs(device, T, n, D, rank, args.mode)
@@ -414,6 +427,7 @@ def bench_bwd(args, device, world, rank, local):
 
     def step(gr=grads):
         op.backward(case.x, case.phi, case.alpha, None, g.g_in, g.g_post, g.g_res, saved, gr, stream=stream)
+        allreduce_weight_grads(gr, world)
 
     for _ in range(args.warmup):
         step()

@@ -1,5 +1,6 @@
 """The N > 1 path of bench.py on CPU: two gloo ranks shard tokens without a
-collective on the data path and agree on the max-over-ranks time."""
+collective on the forward's data path, agree on the max-over-ranks time,
+and sum the backward's weight gradients over ranks (its one exchange)."""
 import os
 import socket
 
@@ -26,8 +27,12 @@ def _worker(rank, world, port, q):
     w, r, l = bench.dist_env()
     lo, hi = bench.shard_tokens(1000, w, r)
     t = bench.max_over_ranks(1.0 + r, w)
+    grads = {"grad_phi": torch.full((2, 3), float(r + 1)), "grad_alpha": torch.tensor([r, 1.0, 2.0]),
+             "grad_bias": torch.ones(4) * (r + 1), "grad_gamma": None, "grad_x": torch.full((2,), float(r))}
+    bench.allreduce_weight_grads(grads, w)
     dist.barrier()
-    q.put((r, lo, hi, t))
+    q.put((r, lo, hi, t, grads["grad_phi"].tolist(), grads["grad_alpha"].tolist(), grads["grad_bias"].tolist(),
+           grads["grad_x"].tolist()))
     dist.destroy_process_group()
 
 
@@ -44,6 +49,9 @@ def test_two_rank_sharding_and_max_time():
         assert p.exitcode == 0
     assert res[0][1:3] == (0, 1000) and res[1][1:3] == (1000, 2000)   # disjoint token ranges
     assert res[0][3] == res[1][3] == 2.0                               # slowest rank's time
+    for r in res:
+        assert r[4] == [[3.0] * 3] * 2 and r[5] == [1.0, 2.0, 4.0] and r[6] == [3.0] * 4   # summed
+    assert res[0][7] == [0.0, 0.0] and res[1][7] == [1.0, 1.0]         # grad_x stays per rank
 
 
 def test_single_rank_helpers():
