@@ -69,29 +69,49 @@ __device__ __forceinline__ uint32_t swz(int row, int col) {
 }
 
 // =================================================================== planes
+// One thread per stored 16-byte piece: eight consecutive columns of one
+// plane row (D is a multiple of 64 here, so every piece is inside D).
 __global__ void __launch_bounds__(256) bw_planes_kernel(BwPlaneParams pp) {
   if (blockIdx.x == 0 && threadIdx.x < kHdrWords && pp.hdr) pp.hdr[threadIdx.x] = 0u;
   const int rows = pp.P * kBwRp;                        // rows of one stream block
-  const long long total = (long long)pp.nslab * kBwNS * rows * 64;
+  const long long pieces = (long long)pp.nslab * kBwNS * rows * 8;
   const int K = kBwNS * pp.D;
-  for (long long idx = (long long)blockIdx.x * blockDim.x + threadIdx.x; idx < total;
-       idx += (long long)gridDim.x * blockDim.x) {
-    const int e = (int)(idx & 63);
-    const long long grow = idx >> 6;
+  for (long long q = (long long)blockIdx.x * blockDim.x + threadIdx.x; q < pieces;
+       q += (long long)gridDim.x * blockDim.x) {
+    const int e = (int)(q & 7);
+    const long long grow = q >> 3;
     const int rr = (int)(grow % rows);                  // row in the stream block
     const long long blk = grow / rows;
     const int i = (int)(blk % kBwNS);
     const int j = (int)(blk / kBwNS);
     const int plane = rr / kBwRp, r = rr % kBwRp;
-    const int d = j * 64 + ((((e >> 3) ^ (rr & 7)) << 3) | (e & 7));
-    float out = 0.0f;
+    const int d0 = j * 64 + ((e ^ (rr & 7)) << 3);
+    float out[8];
+#pragma unroll
+    for (int c = 0; c < 8; ++c) out[c] = 0.0f;
     if (r < kBwR) {
-      const int k = i * pp.D + d;
-      float v = __ldg(pp.phi + (size_t)r * K + k);
-      if (pp.gamma) v *= __ldg(pp.gamma + k);
-      out = plane_part(v, plane, pp.tf32);
+      const int k = i * pp.D + d0;
+      const float4* src = reinterpret_cast<const float4*>(pp.phi + (size_t)r * K + k);
+      float v[8];
+      if (pp.vec16) {                                  // phi and gamma 16-byte aligned
+        const float4 a = __ldg(src), b = __ldg(src + 1);
+        v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w; v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
+      } else {
+#pragma unroll
+        for (int c = 0; c < 8; ++c) v[c] = __ldg(reinterpret_cast<const float*>(src) + c);
+      }
+      if (pp.gamma) {
+#pragma unroll
+        for (int c = 0; c < 8; ++c) v[c] *= __ldg(pp.gamma + k + c);
+      }
+#pragma unroll
+      for (int c = 0; c < 8; ++c) out[c] = plane_part(v[c], plane, pp.tf32);
     }
-    pp.planes[idx] = __float2bfloat16_rn(out);          // exact
+    uint4 o;
+    __nv_bfloat162* h = reinterpret_cast<__nv_bfloat162*>(&o);
+#pragma unroll
+    for (int c = 0; c < 4; ++c) h[c] = __floats2bfloat162_rn(out[2 * c], out[2 * c + 1]);   // exact
+    reinterpret_cast<uint4*>(pp.planes)[q] = o;
   }
 }
 
@@ -757,7 +777,7 @@ __global__ void __launch_bounds__(kFinalThreads) bw_final_kernel(BwFinalParams p
 }  // namespace
 
 cudaError_t launch_bw_planes(const BwPlaneParams& pp, cudaStream_t s) {
-  const long long total = (long long)pp.nslab * kBwNS * pp.P * kBwRp * 64;
+  const long long total = (long long)pp.nslab * kBwNS * pp.P * kBwRp * 8;   // 16-byte pieces
   int blocks = (int)((total + 255) / 256);
   if (blocks > 4096) blocks = 4096;
   if (blocks < 1) blocks = 1;

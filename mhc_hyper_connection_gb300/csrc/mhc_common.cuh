@@ -260,6 +260,7 @@ struct PlaneParams {
   int R, P, n, D, nch, RB; // P = 3 (fp32) or 2 (tf32)
   int tf32;
   int fp16;                // planes in fp16 (scaled, see plane_scale) for fp16 x
+  int vec16;               // phi (and gamma) 16-byte aligned: vector loads
   uint32_t* err_word;      // workspace header: all kHdrWords words are zeroed
 };
 
@@ -514,6 +515,7 @@ struct BwPlaneParams {
   __nv_bfloat16* planes;   // [nslab][NS][P][kBwRp][64], swizzled
   uint32_t* hdr;           // workspace header (zeroed)
   int D, nslab, P, tf32;
+  int vec16;               // phi (and gamma) 16-byte aligned: vector loads
 };
 
 struct BwRowdotParams {

@@ -388,6 +388,7 @@ mhc_status_t mhc_pre_run(mhc_pre_t h, const mhc_pre_args* a, void* stream) {
   pp.RB = mhc::plane_box_rows(R, h->P);
   pp.tf32 = (c.impl_mode == MHC_IMPL_TF32);
   pp.fp16 = (c.x_dtype == MHC_DTYPE_FP16);
+  pp.vec16 = aligned(a->phi, 16) && (!a->gamma || aligned(a->gamma, 16));
   pp.err_word = err;
   if (mhc::launch_prepare_planes(pp, s) != cudaSuccess)
     return fail(MHC_ERR_RUNTIME, "plane preparation launch failed: %s", cudaGetErrorString(cudaGetLastError()));
@@ -782,6 +783,7 @@ mhc_status_t mhc_pre_backward_run(mhc_pre_t h, const mhc_pre_bwd_args* a, void* 
   pp.nslab = nslab;
   pp.P = P;
   pp.tf32 = (h->cfg.impl_mode == MHC_IMPL_TF32) ? 1 : 0;
+  pp.vec16 = aligned(a->phi, 16) && (!a->gamma || aligned(a->gamma, 16));
 
   mhc::BwRowdotParams rp;
   rp.T = (int)T;

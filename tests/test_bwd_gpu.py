@@ -196,3 +196,18 @@ def test_decode_sized(cuda_device, T):
     S = _setup(cuda_device, T, 7168, gamma=False, seed=T, name="decode")
     grads = _run_gpu(S)
     print(_check(S, grads, _run_oracle(S)))
+
+
+def test_phi_gamma_at_4_byte_offset(cuda_device):
+    S = _setup(cuda_device, 130, 256, seed=17)
+    ref = _run_gpu(S)
+    c = S.case
+    buf = torch.empty(c.phi.numel() + 1, device=cuda_device)
+    buf[1:].copy_(c.phi.reshape(-1))
+    gbuf = torch.empty(c.gamma.numel() + 1, device=cuda_device)
+    gbuf[1:].copy_(c.gamma.reshape(-1))
+    c.phi = buf[1:].view(c.phi.shape)
+    c.gamma = gbuf[1:].view(c.gamma.shape)
+    out = _run_gpu(S)
+    for k in ("grad_x", "grad_phi", "grad_alpha", "grad_bias", "grad_gamma"):
+        assert torch.equal(out[k], ref[k]), k

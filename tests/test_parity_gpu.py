@@ -133,3 +133,21 @@ def test_stream_and_reuse(cuda_device):
     run_cuda(c2, stream=s, out=out, op=op)
     torch.cuda.synchronize()
     compare(c2, out, run_oracle(c2))
+
+
+def test_phi_gamma_at_4_byte_offset(cuda_device):
+    """phi and gamma need only 4-byte alignment: the plane preparation takes
+    the scalar-load path then, with the same results bit for bit."""
+    case = make_case("training", device=cuda_device, T=100, D=512, need_backward=True)
+    _, ref = run_cuda(case)
+    buf = torch.empty(case.phi.numel() + 1, device=cuda_device)
+    buf[1:].copy_(case.phi.reshape(-1))
+    gbuf = torch.empty(case.gamma.numel() + 1, device=cuda_device)
+    gbuf[1:].copy_(case.gamma.reshape(-1))
+    case.phi = buf[1:].view(case.phi.shape)
+    case.gamma = gbuf[1:].view(case.gamma.shape)
+    assert case.phi.data_ptr() % 16 == 4
+    _, out = run_cuda(case)
+    torch.cuda.synchronize()
+    for k in ("y", "h_post", "h_res", "h_pre", "inv_rms", "h_mix"):
+        assert torch.equal(out[k], ref[k]), k
