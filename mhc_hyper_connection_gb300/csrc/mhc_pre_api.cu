@@ -393,16 +393,22 @@ mhc_status_t mhc_pre_run(mhc_pre_t h, const mhc_pre_args* a, void* stream) {
   if (mhc::launch_prepare_planes(pp, s) != cudaSuccess)
     return fail(MHC_ERR_RUNTIME, "plane preparation launch failed: %s", cudaGetErrorString(cudaGetLastError()));
 
-  // 2. the fused forward: the cluster kernel, or the grid-wide kernel when
-  //    MHC_PRE_PATH=grid selects it (and its shared memory and residency allow).
-  // fp16 x runs on the 64-token cluster kernel only
+  // 2. the fused forward.  The grid-wide kernel spreads a few token tiles
+  //    over every SM and is the faster one up to kGwAutoMaxT tokens (T = 64 at
+  //    D = 7168: 22.5 against 28.9 us; T = 512: 35.6 against 40.2 us; T =
+  //    2048: 110 against 73 us); the cluster kernel takes larger batches.
+  //    MHC_PRE_PATH=grid or =cluster forces one (tests and tuning runs).
+  //    fp16 x and batch-consistent mode always run the cluster kernel.
   const bool fp16 = c.x_dtype == MHC_DTYPE_FP16;
   const bool consistent = c.batch_consistent != 0;
   const char* path = getenv("MHC_PRE_PATH");
-  if (!consistent && !fp16 && path && !strcmp(path, "grid")) {
+  const bool force_grid = path && !strcmp(path, "grid");
+  const bool force_cluster = path && !strcmp(path, "cluster");
+  constexpr int64_t kGwAutoMaxT = 512;
+  if (!consistent && !fp16 && (force_grid || (!force_cluster && T <= kGwAutoMaxT))) {
     mhc_status_t st = run_grid_wide(h, a, di, planes, s);
     if (st != MHC_ERR_NOT_SUITABLE) return st;
-    return fail(MHC_ERR_PARAM_INVALID, "the grid-wide forward does not fit this shape");
+    if (force_grid) return fail(MHC_ERR_PARAM_INVALID, "the grid-wide forward does not fit this shape");
   }
   // The 64-token-tile kernel, or the 128-token-tile kernel (n = 4) when
   // MHC_PRE_TILE=128 selects it.  At prefill the 64-token kernel at cluster 2

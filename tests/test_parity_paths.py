@@ -1,6 +1,8 @@
-"""Every forward kernel against the oracle: the default 64-token cluster
-kernel, the 128-token cluster kernel (n = 4) selected with MHC_PRE_TILE=128,
-and the grid-wide kernel selected with MHC_PRE_PATH=grid."""
+"""Every forward kernel against the oracle: the 64-token cluster kernel
+(forced with MHC_PRE_PATH=cluster), the 128-token cluster kernel (n = 4)
+selected with MHC_PRE_TILE=128, the grid-wide kernel forced with
+MHC_PRE_PATH=grid, and the automatic choice (grid-wide up to 512 tokens,
+cluster above)."""
 import pytest
 import torch
 
@@ -24,10 +26,14 @@ def _run(case, path, monkeypatch):
         monkeypatch.setenv("MHC_PRE_PATH", "grid")
         want = "mhc_pre_gw_kernel"
     elif path == "tile128":   # 128-token tiles exist for n = 4 only
+        monkeypatch.setenv("MHC_PRE_PATH", "cluster")
         monkeypatch.setenv("MHC_PRE_TILE", "128")
         want = "mhc_pre_t128_kernel" if case.n == 4 else "mhc_pre_tc_kernel"
-    else:
+    elif path == "cluster":
+        monkeypatch.setenv("MHC_PRE_PATH", "cluster")
         want = "mhc_pre_tc_kernel"
+    else:                     # automatic: grid-wide up to 512 tokens
+        want = "mhc_pre_gw_kernel" if case.T <= 512 else "mhc_pre_tc_kernel"
     op, out = run_cuda(case)
     torch.cuda.synchronize()
     assert mhc_pre_last_kernel(op.handle) == want
@@ -35,7 +41,7 @@ def _run(case, path, monkeypatch):
     return out
 
 
-PATHS = ["default", "tile128", "grid"]
+PATHS = ["auto", "cluster", "tile128", "grid"]
 
 
 @pytest.mark.parametrize("path", PATHS)
