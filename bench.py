@@ -364,6 +364,30 @@ def allreduce_weight_grads(grads, world: int):
             dist.all_reduce(t, op=dist.ReduceOp.SUM)
 
 
+def bwd_reference_inputs(device, T, n, D, mode, max_tokens):
+    """Inputs of the reference arm: the first max_tokens tokens of the same
+    workload, their saved intermediates from the oracle's forward (fp32, as
+    the forward hands them on); no kernel of the library runs."""
+    import types
+    import numpy as np
+    import torch
+    import oracle
+    from mhc_synth import make_bwd_grads, make_case
+    case = make_case("prefill", device=device, T=T, impl_mode=mode, seed=0, need_backward=True)
+    Ts = min(T, max_tokens)
+    x = case.x[:Ts].contiguous()
+    fw = oracle.run(x.view(torch_int16()).cpu().numpy().view(np.uint16), case.phi.cpu().numpy(),
+                    case.alpha.cpu().numpy(), case.bias.cpu().numpy(), num_iters=case.num_iters, backward=True,
+                    threads=os.cpu_count() or 1)
+    f32 = lambda a: torch.from_numpy(np.ascontiguousarray(a, dtype=np.float32))
+    saved = {"inv_rms": f32(fw.inv_rms), "h_mix": f32(fw.h_mix), "h_pre": f32(fw.h_pre),
+             "h_post": f32(fw.h_post), "sum_out": f32(fw.sum_out), "norm_out": f32(fw.norm_out)}
+    g = make_bwd_grads(seed=0, device=device, T=T, n=n, D=D)
+    sub = types.SimpleNamespace(x=x, phi=case.phi, alpha=case.alpha, T=Ts, num_iters=case.num_iters)
+    gs = types.SimpleNamespace(g_in=g.g_in[:Ts].contiguous(), g_post=g.g_post[:Ts], g_res=g.g_res[:Ts])
+    return sub, saved, gs
+
+
 def bwd_oracle_rate(case, saved, g, budget_s: float, max_tokens: int):
     """Tokens/s of the backward oracle on all host cores over passes of a
     bounded token sample (all five gradients of that sample)."""
@@ -400,15 +424,15 @@ def bench_bwd(args, device, world, rank, local):
            "tokens_per_rank": T, "n": n, "D": D, "num_iters": 20, "impl_mode": mode_name, "gamma": None,
            "grad_x_post": None, "l2": "inputs (4.3 GB/step) exceed L2; no flush needed",
            "parallelism": f"token-sharded x{world}" + (" + all-reduce of grad_phi/alpha/bias" if world > 1 else "")}
-    from mhc_hyper_connection_gb300 import build as mbuild
-    mbuild.build()
-    case, saved, g = bwd_inputs(device, T, n, D, rank, args.mode)
     if args.impl == "reference":
+        # the oracle alone: its own forward makes the saved intermediates of
+        # the sampled tokens, then its backward is timed on them
         if rank != 0:
             return 0
+        case, saved, g = bwd_reference_inputs(device, T, n, D, args.mode, 20000)
         per_step = 60.0 / (args.steps + args.warmup)
         probe, _, _, _ = bwd_oracle_rate(case, saved, g, 0.0, 64)
-        tokens = int(max(1, min(T, probe * per_step)))
+        tokens = int(max(1, min(case.T, probe * per_step)))
         rate, threads, sample, dt = bwd_oracle_rate(case, saved, g, 60.0 * args.steps / (args.steps + args.warmup),
                                                     tokens)
         print(json.dumps({"impl": "reference", "metric": BWD_METRIC, "value": rate, "unit": "tokens/s",
@@ -420,6 +444,9 @@ def bench_bwd(args, device, world, rank, local):
                           "e2e": {"value": rate, "unit": "tokens/s", "h2d_bytes_per_step": 0,
                                   "d2h_bytes_per_step": 0}}))
         return 0
+    from mhc_hyper_connection_gb300 import build as mbuild
+    mbuild.build()
+    case, saved, g = bwd_inputs(device, T, n, D, rank, args.mode)
     from mhc_hyper_connection_gb300 import MhcPre, mhc_pre_last_launch, mhc_pre_set_profile_events
     op = MhcPre(n, D, alpha_len=3, num_iters=20, impl_mode=args.mode, need_backward=True)
     grads = op.allocate_backward(T, device)
