@@ -10,8 +10,8 @@
 //  * Row dot (one CTA per SM): H_pre_grad = grad_h_in . x over the whole
 //    row (the only full-row reduction of the backward), whole token rows
 //    brought in by bulk copy.
-//  * Token stage (one warp per token): the Sinkhorn backward on 16 lanes
-//    from the saved steps, the gate backward, and
+//  * Token stage (one half-warp per token): the Sinkhorn backward on 16
+//    lanes from the saved steps, the gate backward, and
 //    G = H_mix_grad with the RMS factor c = -inv_rms_grad invRms^3 / (nD).
 //    G goes out as exact bf16 planes in a per-64-token tile record laid out
 //    for the tensor core, next to hPre and c of the tile's tokens.
@@ -220,61 +220,69 @@ __global__ void __launch_bounds__(kRdThreads, 1) bw_rowdot_kernel(BwRowdotParams
 }
 
 // =============================================================== token stage
-constexpr int kSinkChunk = 40;   // saved Sinkhorn steps staged per round (numIters 20: one round)
+constexpr int kSinkChunk = 20;   // saved Sinkhorn steps staged per round and token
 
+// One token per half-warp (two per warp, so twice the tokens in flight):
+// lane hl = i*4 + j of the half holds the Sinkhorn element (i, j) and gate
+// rows hl and hl + 16.  Both halves run every shuffle (all of them stay
+// inside a half); a padding token of the last tile runs the same code on
+// zeros and writes zero G planes.
 __global__ void __launch_bounds__(kBwTokenWarps * 32) bw_token_kernel(BwTokenParams p) {
   constexpr int NS = kBwNS, R = kBwR, NN = NS * NS;
-  __shared__ float stage[kBwTokenWarps][kSinkChunk][NN + NS];
+  static_assert(NN == 16 && R <= 32, "the half-warp layout is for n = 4");
+  __shared__ float stage[kBwTokenWarps][2][kSinkChunk][NN + NS];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int half = lane >> 4, hl = lane & 15;
   const int gw = blockIdx.x * kBwTokenWarps + warp;
   const int nw = gridDim.x * kBwTokenWarps;
   const int Tpad = p.ntiles * kBwTile;
   const float a0 = __ldg(p.alpha), a1 = __ldg(p.alpha + 1), a2 = __ldg(p.alpha + 2);
   const float eps = p.hc_eps;
   const int rec_bytes = bw_tile_rec_bytes(p.P);
-  float acc_bias = 0.0f, acc_alpha = 0.0f;              // this lane's partial sums
-  float (*st)[NN + NS] = stage[warp];
+  const int r0 = hl, r1 = hl + 16;                      // this lane's gate rows
+  float acc_b0 = 0.0f, acc_b1 = 0.0f, acc_a0 = 0.0f, acc_a1 = 0.0f;   // partial sums per row
+  float (*st)[NN + NS] = stage[warp][half];
 
-  for (int t = gw; t < Tpad; t += nw) {
+  for (int tb = 2 * gw; tb < Tpad; tb += 2 * nw) {      // warp-uniform (Tpad is a multiple of 64)
+    const int t = tb + half;
+    const bool valid = t < p.T;
+    const int tv = valid ? t : 0;                       // a token that exists, for loads
     uint8_t* rec = p.tiles + (size_t)(t / kBwTile) * rec_bytes;
     const int col = t % kBwTile;
     float* scal = reinterpret_cast<float*>(rec + p.P * kBwPlaneBytes) + col * 2;
-    if (t >= p.T) {                                     // padding token of the last tile
-      for (int pl = 0; pl < p.P; ++pl)
-        *reinterpret_cast<__nv_bfloat16*>(rec + pl * kBwPlaneBytes + swz(lane, col)) = __float2bfloat16_rn(0.0f);
-      if (lane < 2 * NS) scal[(lane >> 1) * (2 * kBwTile) + (lane & 1)] = 0.0f;
-      continue;
-    }
-    // ---- 3.1: H_pre_grad[i] = sum_d grad_h_in[d] x[i][d], from the row-dot kernel
-    const float4 hg4 = __ldg(reinterpret_cast<const float4*>(p.hg) + t);
+    // ---- 3.1: H_pre_grad[i], from the row-dot kernel
+    const float4 hg4 = __ldg(reinterpret_cast<const float4*>(p.hg) + tv);
     const float hg[NS] = {hg4.x, hg4.y, hg4.z, hg4.w};
-    const float ir = __ldg(p.inv_rms + t);
-    const float hmix_r = lane < R ? __ldg(p.h_mix + (size_t)t * R + lane) : 0.0f;
+    const float ir = __ldg(p.inv_rms + tv);
+    const float hm0 = __ldg(p.h_mix + (size_t)tv * R + r0);
+    const float hm1 = r1 < R ? __ldg(p.h_mix + (size_t)tv * R + r1) : 0.0f;
 
-    // ---- Sinkhorn backward (lane = i*4 + j on lanes 0..15; 16..31 mirror them)
-    const int el = lane & (NN - 1);
-    float g = __ldg(p.g_res + (size_t)t * NN + el);
+    // ---- Sinkhorn backward (element (i, j) = lane hl of the half)
+    float g = valid ? __ldg(p.g_res + (size_t)tv * NN + hl) : 0.0f;
     if (p.norm_out) {
       for (int kh = 2 * p.num_iters - 1; kh >= 1; kh -= kSinkChunk) {
         const int klo = max(1, kh - kSinkChunk + 1);
         const int cnt = kh - klo + 1;
         __syncwarp();
-        // the chunk's saved matrices and sums, eight loads in flight per lane
-        // (more raises the registers and costs occupancy: 25 measured slower)
+        // the chunk's saved matrices and sums of this half's token, eight
+        // loads in flight per lane (sums of a padding token read as 1)
         const int nm = cnt * NN, ntot = nm + cnt * NS;
         constexpr int kBatch = 8;
-        for (int e0 = lane; e0 < ntot; e0 += 32 * kBatch) {
+        for (int e0 = hl; e0 < ntot; e0 += 16 * kBatch) {
           float v[kBatch];
 #pragma unroll
           for (int j = 0; j < kBatch; ++j) {
-            const int e = e0 + 32 * j;
+            const int e = e0 + 16 * j;
             v[j] = 0.0f;
-            if (e < nm) v[j] = __ldg(p.norm_out + ((size_t)(klo + e / NN) * p.T + t) * NN + e % NN);
-            else if (e < ntot) v[j] = __ldg(p.sum_out + ((size_t)(klo + (e - nm) / NS) * p.T + t) * NS + (e - nm) % NS);
+            if (e < nm) {
+              if (valid) v[j] = __ldg(p.norm_out + ((size_t)(klo + e / NN) * p.T + tv) * NN + e % NN);
+            } else if (e < ntot) {
+              v[j] = valid ? __ldg(p.sum_out + ((size_t)(klo + (e - nm) / NS) * p.T + tv) * NS + (e - nm) % NS) : 1.0f;
+            }
           }
 #pragma unroll
           for (int j = 0; j < kBatch; ++j) {
-            const int e = e0 + 32 * j;
+            const int e = e0 + 16 * j;
             if (e < nm) st[e / NN][e % NN] = v[j];
             else if (e < ntot) st[(e - nm) / NS][NN + (e - nm) % NS] = v[j];
           }
@@ -282,69 +290,84 @@ __global__ void __launch_bounds__(kBwTokenWarps * 32) bw_token_kernel(BwTokenPar
         __syncwarp();
         for (int k = kh; k >= klo; --k) {
           const float* row = st[k - klo];
-          const float prod = g * row[el];
-          float dot, s;
+          const float prod = g * row[hl];
+          float dot, sv;
           if (k & 1) {            // column step: sum over i, divide by column sum j
             dot = prod + __shfl_xor_sync(0xffffffffu, prod, 4);
             dot += __shfl_xor_sync(0xffffffffu, dot, 8);
-            s = row[NN + (el & 3)];
+            sv = row[NN + (hl & 3)];
           } else {                // row step: sum over j, divide by row sum i
             dot = prod + __shfl_xor_sync(0xffffffffu, prod, 1);
             dot += __shfl_xor_sync(0xffffffffu, dot, 2);
-            s = row[NN + (el >> 2)];
+            sv = row[NN + (hl >> 2)];
           }
-          g = __fdividef(g - dot, s);      // s is a sum plus eps: >= eps, well inside the fast range
+          g = __fdividef(g - dot, sv);     // sv is a sum plus eps: >= eps, well inside the fast range
         }
       }
       // the row softmax (+ eps): S = normOut[0] - eps
-      const float S = __ldg(p.norm_out + (size_t)t * NN + el) - eps;
+      const float S = valid ? __ldg(p.norm_out + (size_t)tv * NN + hl) - eps : 0.0f;
       const float prod = g * S;
       float dot = prod + __shfl_xor_sync(0xffffffffu, prod, 1);
       dot += __shfl_xor_sync(0xffffffffu, dot, 2);
       g = S * (g - dot);
     }
-    const float gres = __shfl_sync(0xffffffffu, g, (lane - 2 * NS) & 31);
+    // res logit gradients of rows r0 (hl >= 8: element hl - 8) and r1 (element hl + 8)
+    const float gres0 = __shfl_sync(0xffffffffu, g, (half << 4) + ((hl - 8) & 15));
+    const float gres1 = __shfl_sync(0xffffffffu, g, (half << 4) + ((hl + 8) & 15));
 
-    // ---- gates (3.2-3.4), lane r = gate row
-    float gt = 0.0f, aterm = 0.0f, bterm = 0.0f;
-    if (lane < NS) {
-      const float s = __ldg(p.h_pre + (size_t)t * NS + lane) - eps;
-      float h = hg[0];
+    // ---- gates (3.2-3.4) of rows r0, r1
+    float b0 = 0.0f, gt0 = 0.0f, b1 = 0.0f, gt1 = 0.0f;
+    if (r0 < NS) {
+      const float sg = __ldg(p.h_pre + (size_t)tv * NS + r0) - eps;
+      float hh = hg[0];
 #pragma unroll
-      for (int i = 1; i < NS; ++i) h = (lane == i) ? hg[i] : h;
-      bterm = h * s * (1.0f - s);
-      gt = bterm * a0;
-    } else if (lane < 2 * NS) {
-      const float hp = __ldg(p.h_post + (size_t)t * NS + lane - NS);
-      bterm = __ldg(p.g_post + (size_t)t * NS + lane - NS) * hp * (1.0f - 0.5f * hp);
-      gt = bterm * a1;
-    } else if (lane < R) {
-      bterm = gres;
-      gt = bterm * a2;
+      for (int i = 1; i < NS; ++i) hh = (r0 == i) ? hg[i] : hh;
+      b0 = hh * sg * (1.0f - sg);
+      gt0 = b0 * a0;
+    } else if (r0 < 2 * NS) {
+      const float hp = __ldg(p.h_post + (size_t)tv * NS + r0 - NS);
+      b0 = __ldg(p.g_post + (size_t)tv * NS + r0 - NS) * hp * (1.0f - 0.5f * hp);
+      gt0 = b0 * a1;
+    } else {
+      b0 = gres0;
+      gt0 = b0 * a2;
     }
-    aterm = bterm * (hmix_r * ir);
-    acc_bias += bterm;
-    acc_alpha += aterm;
-    // ---- 3.5: G = [alpha g] invRms; inv_rms_grad = sum [alpha g] hMix
-    const float irg = warp_sum(gt * hmix_r);
-    const float G = gt * ir;
-    const float c = -(irg * ir * ir * ir) / (float)(NS * p.D);
-    for (int pl = 0; pl < p.P; ++pl)
-      *reinterpret_cast<__nv_bfloat16*>(rec + pl * kBwPlaneBytes + swz(lane, col)) =
-          __float2bfloat16_rn(plane_part(G, pl, p.tf32));
+    if (r1 < R) {
+      b1 = gres1;
+      gt1 = b1 * a2;
+    }
+    if (!valid) b0 = gt0 = b1 = gt1 = 0.0f;
+    acc_b0 += b0;
+    acc_b1 += b1;
+    acc_a0 += b0 * (hm0 * ir);
+    acc_a1 += b1 * (hm1 * ir);
+    // ---- 3.5: G = [alpha g] invRms; inv_rms_grad = sum [alpha g] hMix (over the half)
+    float irg = gt0 * hm0 + gt1 * hm1;
+#pragma unroll
+    for (int o = 8; o > 0; o >>= 1) irg += __shfl_xor_sync(0xffffffffu, irg, o);
+    const float G0 = gt0 * ir, G1 = gt1 * ir;
+    const float c = valid ? -(irg * ir * ir * ir) / (float)(NS * p.D) : 0.0f;
+    for (int pl = 0; pl < p.P; ++pl) {
+      *reinterpret_cast<__nv_bfloat16*>(rec + pl * kBwPlaneBytes + swz(r0, col)) =
+          __float2bfloat16_rn(plane_part(G0, pl, p.tf32));
+      *reinterpret_cast<__nv_bfloat16*>(rec + pl * kBwPlaneBytes + swz(r1, col)) =
+          __float2bfloat16_rn(plane_part(G1, pl, p.tf32));
+    }
     // per stream i, per token: (hPre_i, RMS factor) -- [i][token] pairs
-    if (lane < 2 * NS)
-      scal[(lane >> 1) * (2 * kBwTile) + (lane & 1)] = (lane & 1) ? c : __ldg(p.h_pre + (size_t)t * NS + (lane >> 1));
+    if (hl < 2 * NS) {
+      const float hp = valid ? __ldg(p.h_pre + (size_t)tv * NS + (hl >> 1)) : 0.0f;
+      scal[(hl >> 1) * (2 * kBwTile) + (hl & 1)] = (hl & 1) ? c : hp;
+    }
   }
-  // ---- this warp's partial sums: [0, R) bias, R.. R+2 alpha by segment
-  float seg0 = lane < NS ? acc_alpha : 0.0f;
-  float seg1 = (lane >= NS && lane < 2 * NS) ? acc_alpha : 0.0f;
-  float seg2 = (lane >= 2 * NS && lane < R) ? acc_alpha : 0.0f;
-  seg0 = warp_sum(seg0);
-  seg1 = warp_sum(seg1);
-  seg2 = warp_sum(seg2);
+  // ---- this warp's partial sums: [0, R) bias, R .. R+2 alpha by segment
+  const float bs0 = acc_b0 + __shfl_xor_sync(0xffffffffu, acc_b0, 16);   // rows 0..15
+  const float bs1 = acc_b1 + __shfl_xor_sync(0xffffffffu, acc_b1, 16);   // rows 16..31
+  const float seg0 = warp_sum(hl < NS ? acc_a0 : 0.0f);
+  const float seg1 = warp_sum((hl >= NS && hl < 2 * NS) ? acc_a0 : 0.0f);
+  const float seg2 = warp_sum((hl >= 2 * NS ? acc_a0 : 0.0f) + acc_a1);
+  const float hi_rows = __shfl_sync(0xffffffffu, bs1, lane & 15);
   float* out = p.partials + (size_t)gw * 32;
-  float v = lane < R ? acc_bias : 0.0f;
+  float v = lane < 16 ? bs0 : (lane < R ? hi_rows : 0.0f);
   if (lane == R) v = seg0;
   if (lane == R + 1) v = seg1;
   if (lane == R + 2) v = seg2;

@@ -827,7 +827,8 @@ mhc_status_t mhc_pre_backward_run(mhc_pre_t h, const mhc_pre_bwd_args* a, void* 
   int tblocks = 0;
   if (mhc::bw_token_blocks(&tblocks) != cudaSuccess)
     return fail(MHC_ERR_RUNTIME, "token-stage occupancy query failed: %s", cudaGetErrorString(cudaGetLastError()));
-  const long long tmax = ((long long)ntiles * mhc::kBwTile + mhc::kBwTokenWarps - 1) / mhc::kBwTokenWarps;
+  // two tokens per warp
+  const long long tmax = ((long long)ntiles * mhc::kBwTile + 2 * mhc::kBwTokenWarps - 1) / (2 * mhc::kBwTokenWarps);
   if (tblocks > tmax) tblocks = (int)tmax;
 
   mhc::BwFinalParams fp;
