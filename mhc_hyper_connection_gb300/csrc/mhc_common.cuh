@@ -301,7 +301,7 @@ __host__ __device__ constexpr int sink_stride(int n) { return n * n; }
 // and w rings are back to back, so an operand read that runs past a slot
 // stays inside the window.
 struct SmemLayout {
-  size_t x, w, part, coef, sink, tail, total;
+  size_t x, w, part, coef, tail, total;
 };
 __host__ __device__ inline SmemLayout smem_layout(int n, int R, int P, int xs, int ws) {
   SmemLayout L;
@@ -309,9 +309,8 @@ __host__ __device__ inline SmemLayout smem_layout(int n, int R, int P, int xs, i
   L.x = o;    o += (size_t)xs * stream_group(n) * kStreamTile;
   L.w = o;    o += (size_t)ws * w_group(n, R, P) * plane_box_rows(R, P) * 128;
   o += 1024;  // the B operand of N = NP rows reads up to 8 rows past the last w box
-  L.part = o; o += (size_t)kTileT * partial_stride(R) * 4;
+  L.part = o; o += 2 * (size_t)kTileT * partial_stride(R) * 4;   // two partials per member and row
   L.coef = o; o += (size_t)kCoefBufs * kTileT * n * 4;
-  L.sink = o; o += 2 * (size_t)kTileT * sink_stride(n) * 4;
   o = (o + 15) & ~size_t(15);
   L.tail = o; o += kTailBytes;
   L.total = o + 1024;
@@ -351,7 +350,6 @@ __host__ __device__ inline SmemLayout t128_layout(int R, int P, int xs, int ws) 
   o += 1024;  // the B operand of N = NP rows reads up to 8 rows past the last w box
   L.part = o; o += 2 * (size_t)kT128Tile * partial_stride(R) * 4;   // received partials + owned sums
   L.coef = o; o += (size_t)kCoefBufs * kT128Tile * 4 * 4;
-  L.sink = o;
   o = (o + 15) & ~size_t(15);
   L.tail = o; o += kTailBytes;
   L.total = o + 1024;

@@ -154,11 +154,15 @@ __device__ __noinline__ bool gw_wait_count(const uint32_t* ctr, uint32_t target,
   }
 }
 
-// Lane 0 waits; the result reaches the whole warp.
+// Lane 0 waits; the result reaches the whole warp, and the warp barrier
+// orders the other lanes' later reads after lane 0's acquire (a shuffle
+// alone would let the compiler hoist those reads above the wait).
 __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, const GwCtl& c) {
   bool ok = true;
   if ((threadIdx.x & 31) == 0) ok = gw_wait(bar, parity, c);
-  return __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+  ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+  __syncwarp();
+  return ok;
 }
 
 // First local row t of a tile that CTA r of the group gates: (64m + t) % G == r.
@@ -463,6 +467,7 @@ __global__ void __launch_bounds__(kGwThreads, 1)
           if (ok && use > 0 && yd < use * (uint32_t)G) ok = gw_wait_count(&ydone[slot], use * (uint32_t)G, ctl);
         }
         if (!__shfl_sync(0xffffffffu, ok ? 1 : 0, 0)) break;
+        __syncwarp();                              // the lanes' reads below follow lane 0's acquire
         for (int t = first; t < valid; t += G, ++cnt) {
           // Sum the CTAs' partials of row t in a fixed order: lane l adds
           // CTAs l, l + 32, ... then a fixed butterfly adds the lanes.
@@ -559,6 +564,7 @@ __global__ void __launch_bounds__(kGwThreads, 1)
       bool ok = true;
       if (lane == 0) ok = gw_wait_count(&ready[slot], use * (uint32_t)kGwTile + (uint32_t)valid, ctl);
       if (!__shfl_sync(0xffffffffu, ok ? 1 : 0, 0)) break;
+      __syncwarp();                                // the lanes' reads below follow lane 0's acquire
       const float* csrc = gcoef + (size_t)slot * kGwTile * NS;
       float* cdst = ycoef + (size_t)b * kGwTile * NS;
       for (int e = lane; e < valid * NS; e += 32) cdst[e] = __ldcg(csrc + e);

@@ -254,10 +254,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int e = 0; e < 8; ++e) s8[e] = 0.0f;
       for (int j = c0; j < c1 && ok; ++j) {
         for (int grp = 0; grp < C::kGroups; ++grp) {
-          // each warp takes the box on its own: lane 0 waits, the warp reads
-          bool got = true;
-          if (lane == 0) got = wait_bar<false>(&tail->x_full[xs], xph, ctl, kErrWaitTimeout);
-          if (!__shfl_sync(0xffffffffu, got ? 1 : 0, 0)) {
+          // each warp takes the box on its own and releases it after reading
+          // every lane waits on the barrier itself: each lane's own acquire
+          // orders its reads of the box after the copy landed
+          if (!__all_sync(0xffffffffu, wait_bar<false>(&tail->x_full[xs], xph, ctl, kErrWaitTimeout))) {
             ok = false;
             break;
           }

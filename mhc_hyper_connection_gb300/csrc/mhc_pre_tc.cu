@@ -11,12 +11,13 @@
 //    streams, so each byte of x is read from HBM once per tile.
 //  * Per chunk, TMA brings x[64 tokens][64] of a group of streams (bf16,
 //    128-byte swizzle) and the matching 64 columns of the stacked phi planes;
-//    one thread issues tcgen05.mma (K = 16 each), N = NP into one TMEM block
-//    and x.x^T (N = 64) into another, whose diagonal is each token's sum of
-//    squares.
-//  * Two publish warps read the accumulators (thread = token), fold the
-//    precision planes and push the CTA's partial sums to the member that
-//    owns the row (distributed shared memory).  The owner's gate warp sums
+//    one thread issues tcgen05.mma (K = 16 each), N = NP into TMEM.
+//  * Two publish warps (thread = token) sum each token's squares from every
+//    x box as it lands (CUDA cores: an x.x^T block on the tensor core would
+//    double its operand reads from shared memory, which bound the MMA), then
+//    read the accumulators, fold the precision planes and push the CTA's
+//    partial sums to the member that owns the row (distributed shared
+//    memory).  The owner's gate warp sums
 //    them in rank order, computes invRms and the gates, and sends the y
 //    weights to every member; a Sinkhorn warp produces comb off y's path.
 //  * Eight warps form y for the CTA's d-range by re-reading x from global
@@ -35,11 +36,7 @@ template <int NS, int RR, int P>
 struct Cfg {
   static constexpr int kNP = ((P * RR + 15) / 16) * 16;          // MMA N of the projection
   static_assert(kNP <= 256, "N of one MMA is at most 256");
-  static constexpr int kSsqCol = kNP;                            // x.x^T block (64 columns) after it
-  static constexpr int kCols = kNP + kTileT;
-  static constexpr int kAccCols = kCols <= 64 ? 64 : kCols <= 128 ? 128 : kCols <= 256 ? 256 : 512;
-  static constexpr int kAccBufs = 512 / kAccCols >= 2 ? 2 : 1;   // accumulator buffers
-  static constexpr uint32_t kTmemCols = (uint32_t)(kAccCols * kAccBufs);
+  static constexpr int kAccBufs = 2;                             // accumulator buffers
   static constexpr int kSG = stream_group(NS);                   // streams per x box
   static constexpr int kGroups = NS / kSG;                       // x boxes per d-chunk
   static_assert(NS % kSG == 0, "stream groups tile the streams");
@@ -48,8 +45,20 @@ struct Cfg {
   static constexpr int kWG = w_group(NS, RR, P);                 // streams per w box
   static constexpr int kWBoxes = NS / kWG;                       // w boxes per d-chunk
   static constexpr int kWBytes = kWG * kWRows * 128;             // one w box
+  // Stream pairs: one MMA (M = 128, N = 2 kWRows) takes streams i and i+1
+  // at once -- A rows 0..63 are stream i's tokens, rows 64..127 stream
+  // i+1's (the next 8 KB of the x box), B is both streams' plane rows back
+  // to back in the w box; accumulator rows 0..63 x columns [0, kWRows) and
+  // rows 64..127 x columns [kWRows, 2 kWRows) are the two streams' partial
+  // projections (the off-diagonal blocks are never read).  Without pairs
+  // the MMA runs N = NP per stream and rows 64..127 are never read.
+  static constexpr bool kPair = kSG % 2 == 0 && kWG % 2 == 0 && 2 * kWRows <= 256;
+  static constexpr int kStep = kPair ? 2 : 1;                    // streams per MMA
+  static constexpr int kMmaN = kPair ? 2 * kWRows : kNP;
+  static constexpr int kAccCols = kMmaN <= 64 ? 64 : kMmaN <= 128 ? 128 : 256;
+  static constexpr uint32_t kTmemCols = (uint32_t)(kAccCols * kAccBufs);
+  static_assert(kMmaN % 16 == 0 && kMmaN <= 256, "M = 128 takes N = 16 .. 256 in steps of 16");
   static constexpr int kStr = partial_stride(RR);                // floats per published partial
-  static constexpr int kSink = sink_stride(NS);
   static constexpr bool kThree = (RR == NS * NS + 2 * NS);
   static constexpr int kYBatch = NS <= 4 ? 4 : 2;               // y items in flight per thread
 };
@@ -60,7 +69,6 @@ struct SmemTail {
   uint64_t acc_full[2], acc_empty[2];
   uint64_t part_full, part_free;
   uint64_t coef_full[kCoefBufs], coef_free[kCoefBufs];
-  uint64_t sink_full[2], sink_free[2];
   uint64_t mma_done;
   uint32_t tmem_base;
   uint32_t abort;
@@ -68,12 +76,31 @@ struct SmemTail {
 static_assert(sizeof(SmemTail) <= kTailBytes, "barrier block outgrew its reservation");
 
 // Warp roles: one TMA producer per ring, so each ring has its own issuing
-// thread; warp 3 has no role.
-constexpr int kWarpX = 0, kWarpMma = 1, kWarpW = 2, kWarpPub0 = 4, kWarpGate = 6, kWarpSink = 7,
-              kWarpYc0 = 8;
+// thread; warps 4..7 cover the four TMEM lane quarters.
+constexpr int kWarpX = 0, kWarpMma = 1, kWarpW = 2, kWarpGate = 3, kWarpPub0 = 4, kWarpYc0 = 8;
+constexpr int kPubThreads = 128;
 constexpr int kYThreads = kThreads - kWarpYc0 * 32;   // 256
 // Named barriers: 1 = publish pair (64 threads), 2 = y warps.
 constexpr int kBarPub = 1, kBarY = 2;
+
+// Adds accumulator columns [CB, CB + P RR) of this warp's TMEM lanes, read
+// in 16-column groups from a 16-aligned start, into the R projection sums
+// (column CB + p R + r is plane p of row r).
+template <int RR, int P, int CB, bool F16>
+__device__ __forceinline__ void fold_planes(uint32_t taddr, float (&mix)[RR]) {
+  constexpr int CA = CB & ~15;
+  constexpr int kGroups = (CB + P * RR - CA + 15) / 16;
+#pragma unroll
+  for (int grp = 0; grp < kGroups; ++grp) {
+    float v[16];
+    tmem_ld16(taddr + (uint32_t)(CA + grp * 16), v);
+#pragma unroll
+    for (int e = 0; e < 16; ++e) {
+      const int col = CA + grp * 16 + e - CB;
+      if (col >= 0 && col < P * RR) mix[col % RR] += F16 ? v[e] * plane_scale(true, col / RR) : v[e];
+    }
+  }
+}
 
 template <int NS, int RR, int P, bool F16>
 __global__ void __launch_bounds__(kThreads, 1)
@@ -86,9 +113,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int XS = g.xstages, WS = g.wstages;
   uint8_t* sX = smem + Ly.x;
   uint8_t* sW = smem + Ly.w;
-  float* recv = reinterpret_cast<float*>(smem + Ly.part);     // [CL][64/CL][kStr]
+  float* recv = reinterpret_cast<float*>(smem + Ly.part);     // [CL][2][64/CL][kStr]
   float* coef_buf = reinterpret_cast<float*>(smem + Ly.coef); // [kCoefBufs][64][NS]
-  float* sink_buf = reinterpret_cast<float*>(smem + Ly.sink); // [2][64][n*n] residual logits
   SmemTail* tail = reinterpret_cast<SmemTail*>(smem + Ly.tail);
 
   const int warp = threadIdx.x >> 5;
@@ -106,7 +132,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0) {
     for (int s = 0; s < XS; ++s) {
       mbar_init(&tail->x_full[s], 1);
-      mbar_init(&tail->x_empty[s], 1);          // MMA commit
+      mbar_init(&tail->x_empty[s], 1 + 4);      // MMA commit + the four sum-of-squares warps
     }
     for (int s = 0; s < WS; ++s) {
       mbar_init(&tail->w_full[s], 1);
@@ -114,15 +140,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&tail->acc_full[b], 1);
-      mbar_init(&tail->acc_empty[b], 2);        // two publish warps
-      mbar_init(&tail->sink_full[b], 1);
-      mbar_init(&tail->sink_free[b], 1);
+      mbar_init(&tail->acc_empty[b], 4);        // four publish warps
     }
     for (int b = 0; b < kCoefBufs; ++b) {
       mbar_init(&tail->coef_full[b], CL);
       mbar_init(&tail->coef_free[b], CL);
     }
-    mbar_init(&tail->part_full, CL);            // one arrival per cluster member
+    mbar_init(&tail->part_full, 2 * CL);        // two arrivals per cluster member
     mbar_init(&tail->part_free, CL);
     mbar_init(&tail->mma_done, 1);
     tail->abort = 0u;
@@ -196,11 +220,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp == kWarpMma) {
     // ================================================= MMA issuer
-    // Per stream of each d-chunk: the projection (N = NP) and x.x^T (N = 64,
-    // whose diagonal is each token's sum of squares), both into TMEM.
+    // Per stream (or stream pair) of each d-chunk: the projection into TMEM.
     if (lane == 0) {
-      constexpr uint32_t idesc_proj = F16 ? idesc_f16(kMmaM, C::kNP) : idesc_bf16(kMmaM, C::kNP);
-      constexpr uint32_t idesc_ssq = F16 ? idesc_f16(kMmaM, kTileT) : idesc_bf16(kMmaM, kTileT);
+      constexpr uint32_t idesc_proj = F16 ? idesc_f16(kMmaM, C::kMmaN) : idesc_bf16(kMmaM, C::kMmaN);
       int xs = 0, ws = 0, acc = 0;
       uint32_t xph = 0, wph = 0, acc_phase = 0;
       bool ok = true;
@@ -208,11 +230,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!wait_bar<false>(&tail->acc_empty[acc], acc_phase ^ 1u, ctl, kErrWaitTimeout)) break;
         tc_fence_after();
         const uint32_t d_proj = tmem_base + (uint32_t)(acc * C::kAccCols);
-        const uint32_t d_ssq = d_proj + (uint32_t)C::kSsqCol;
         bool first = true;
         for (int j = c0; j < c1 && ok; ++j) {
           uint32_t xbase = 0, wbase = 0;
-          for (int i = 0; i < NS; ++i) {
+          for (int i = 0; i < NS; i += C::kStep) {
             if (i % C::kWG == 0) {
               if (!wait_bar<false>(&tail->w_full[ws], wph, ctl, kErrWaitTimeout)) { ok = false; break; }
               wbase = smem_u32(sW + (size_t)ws * C::kWBytes);
@@ -222,22 +243,22 @@ __global__ void __launch_bounds__(kThreads, 1)
               xbase = smem_u32(sX + (size_t)xs * C::kXBytes);
             }
             tc_fence_after();
-            // A: 128 rows from this stream's token tile (rows 64..127 run on
-            // into the next tile and feed lanes that are never read).
+            // A: 128 rows from this stream's token tile (rows 64..127: the
+            // pair's second stream, or rows that run on into the next tile
+            // and feed lanes that are never read).
             const uint32_t a0 = xbase + (uint32_t)((i % C::kSG) * kStreamTile);
             const uint32_t b0 = wbase + (uint32_t)((i % C::kWG) * C::kWRows * 128);
 #pragma unroll
             for (int kk = 0; kk < kChunkK / 16; ++kk) {
               const uint32_t acc_in = first ? 0u : 1u;
               mma_bf16(d_proj, sw128_desc(a0 + kk * 32), sw128_desc(b0 + kk * 32), idesc_proj, acc_in);
-              mma_bf16(d_ssq, sw128_desc(a0 + kk * 32), sw128_desc(a0 + kk * 32), idesc_ssq, acc_in);
               first = false;
             }
-            if (i % C::kSG == C::kSG - 1) {          // frees the x slot when these MMAs finish
+            if ((i + C::kStep) % C::kSG == 0) {      // frees the x slot when these MMAs finish
               mma_commit(&tail->x_empty[xs]);
               if (++xs == XS) { xs = 0; xph ^= 1u; }
             }
-            if (i % C::kWG == C::kWG - 1) {
+            if ((i + C::kStep) % C::kWG == 0) {
               mma_commit(&tail->w_empty[ws]);
               if (++ws == WS) { ws = 0; wph ^= 1u; }
             }
@@ -250,51 +271,83 @@ __global__ void __launch_bounds__(kThreads, 1)
       mma_commit(&tail->mma_done);
       mbar_drain(&tail->mma_done, 0);
     }
-  } else if (warp >= kWarpPub0 && warp < kWarpGate) {
-    // ================================================= publish partial sums
-    // Thread = tile row = TMEM lane.  Each row's partial projection (this
-    // member's d-range) and partial sum of squares go to the member that
-    // owns the row.
-    const int et = threadIdx.x - kWarpPub0 * 32;   // 0..63
-    const int wq = warp & 3;                       // TMEM lane quarter (0 or 1)
+  } else if (warp >= kWarpPub0 && warp < kWarpYc0) {
+    // ================================================= sums of squares + partials
+    // Warp 4 + q reads TMEM lane quarter q.  Half h = q / 2 of the warps
+    // takes tile rows et = 0..63 (lane 64 h + et): its share of each row's
+    // sum of squares (streams [sg0, sg1) of every x box, read in swizzled
+    // order as the box lands, the box released after) and of the partial
+    // projection (half 0: the unpaired or first-of-pair streams, half 1: the
+    // second-of-pair streams), pushed to the member that owns the row.
+    const int q = warp - kWarpPub0;                // TMEM lane quarter 0..3
+    const int half = q >> 1;
+    const int et = (q & 1) * 32 + lane;            // tile row 0..63
     const int owner = et / rpo;
     const int slot = et - owner * rpo;
-    int acc = 0;
-    uint32_t acc_phase = 0;
+    constexpr int kSgHalf = (C::kSG + 1) / 2;
+    const int sg0 = half * kSgHalf;
+    const int sg1 = min(C::kSG, sg0 + kSgHalf);
+    int acc = 0, xs = 0;
+    uint32_t acc_phase = 0, xph = 0;
     uint32_t k = 0;
-    for (int tile = cluster_id; tile < g.num_tiles; tile += num_clusters, ++k) {
-      if (!role_all<kBarPub, 64>(wait_bar<false>(&tail->acc_full[acc], acc_phase, ctl, kErrWaitTimeout))) break;
+    bool ok = true;
+    for (int tile = cluster_id; tile < g.num_tiles && ok; tile += num_clusters, ++k) {
+      float s8[8];
+#pragma unroll
+      for (int e = 0; e < 8; ++e) s8[e] = 0.0f;
+      for (int j = c0; j < c1 && ok; ++j) {
+        for (int grp = 0; grp < C::kGroups; ++grp) {
+          // every lane waits on the barrier itself: each lane's own acquire
+          // orders its reads of the box after the copy landed
+          if (!__all_sync(0xffffffffu, wait_bar<false>(&tail->x_full[xs], xph, ctl, kErrWaitTimeout))) {
+            ok = false;
+            break;
+          }
+          const uint8_t* rowp = sX + (size_t)xs * C::kXBytes + (size_t)et * 128;
+          for (int sg = sg0; sg < sg1; ++sg) {
+            uint4 v[8];
+#pragma unroll
+            for (int c = 0; c < 8; ++c)
+              v[c] = *reinterpret_cast<const uint4*>(rowp + (size_t)sg * kStreamTile + ((c ^ (et & 7)) << 4));
+#pragma unroll
+            for (int c = 0; c < 8; ++c) {
+              const typename XType<F16>::T2* h2 = reinterpret_cast<const typename XType<F16>::T2*>(&v[c]);
+#pragma unroll
+              for (int e = 0; e < 4; ++e) {
+                const float2 f = XType<F16>::to_f2(h2[e]);
+                s8[2 * e] = fmaf(f.x, f.x, s8[2 * e]);
+                s8[2 * e + 1] = fmaf(f.y, f.y, s8[2 * e + 1]);
+              }
+            }
+          }
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&tail->x_empty[xs]);
+          if (++xs == XS) { xs = 0; xph ^= 1u; }
+        }
+      }
+      // all four warps leave together if any gave up (the producer stops on
+      // the abort flag, so the others' waits end too)
+      if (!role_all<kBarPub, kPubThreads>(ok)) break;
+      const float ssq = tree_sum<8>(s8);
+      if (!role_all<kBarPub, kPubThreads>(wait_bar<false>(&tail->acc_full[acc], acc_phase, ctl, kErrWaitTimeout)))
+        break;
       tc_fence_after();
       float mix[RR];
 #pragma unroll
       for (int r = 0; r < RR; ++r) mix[r] = 0.0f;
-      const uint32_t taddr = tmem_base + ((uint32_t)(wq * 32) << 16) + (uint32_t)(acc * C::kAccCols);
-#pragma unroll
-      for (int grp = 0; grp < C::kNP / 16; ++grp) {
-        float v[16];
-        tmem_ld16(taddr + grp * 16, v);
-#pragma unroll
-        for (int e = 0; e < 16; ++e) {
-          const int col = grp * 16 + e;
-          if (col < P * RR) mix[col % RR] += F16 ? v[e] * plane_scale(true, col / RR) : v[e];
-        }
-      }
-      float ssq = 0.0f;
-      {
-        float v[32];
-        tmem_ld32(taddr + (uint32_t)(C::kSsqCol + wq * 32), v);
-#pragma unroll
-        for (int e = 0; e < 32; ++e) ssq = (e == lane) ? v[e] : ssq;   // diagonal of x.x^T
-      }
+      const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * C::kAccCols);
+      if (half == 0) fold_planes<RR, P, 0, F16>(taddr, mix);
+      else if (C::kPair) fold_planes<RR, P, C::kWRows, F16>(taddr, mix);
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&tail->acc_empty[acc]);
       if (++acc == C::kAccBufs) { acc = 0; acc_phase ^= 1u; }
 
       // every owner must have consumed the previous tile's partials
-      if (k > 0 && !role_all<kBarPub, 64>(wait_bar<true>(&tail->part_free, (k - 1) & 1u, ctl, kErrClusterWait)))
+      if (k > 0 &&
+          !role_all<kBarPub, kPubThreads>(wait_bar<true>(&tail->part_free, (k - 1) & 1u, ctl, kErrClusterWait)))
         break;
-      float* dst = recv + ((size_t)((int)rank * rpo + slot)) * C::kStr;
+      float* dst = recv + ((size_t)(((int)rank * 2 + half) * rpo + slot)) * C::kStr;
 #pragma unroll
       for (int r = 0; r < C::kStr; r += 4) {
         float4 v;
@@ -304,14 +357,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         v.w = r + 3 < RR ? mix[r + 3] : (r + 3 == RR ? ssq : 0.0f);
         st_dsmem_v4(dst + r, (uint32_t)owner, v);
       }
-      role_sync<kBarPub, 64>();
-      if (et < CL) mbar_arrive_remote(&tail->part_full, (uint32_t)et);
+      role_sync<kBarPub, kPubThreads>();
+      // one arrival per half at every owner
+      if ((q & 1) == 0 && lane < CL) mbar_arrive_remote(&tail->part_full, (uint32_t)lane);
     }
   } else if (warp == kWarpGate) {
-    // ================================================= gates (critical for y)
-    // Owned rows: sum the members' partials in rank order, compute invRms and
-    // the gates, publish the y weights to every member, hand the row to the
-    // Sinkhorn warp.
+    // ================================================= gates (critical for y), then Sinkhorn
+    // Owned rows: sum the members' two partials each in (rank, half) order,
+    // compute invRms and the gates, publish the y weights to every member,
+    // then run the rows' Sinkhorn for comb (off y's path).
     uint32_t k = 0;
     for (int tile = cluster_id; tile < g.num_tiles; tile += num_clusters, ++k) {
       if (!__all_sync(0xffffffffu, wait_bar<true>(&tail->part_full, k & 1u, ctl, kErrClusterWait))) break;
@@ -324,7 +378,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           float tot[C::kStr];
 #pragma unroll
           for (int r = 0; r < C::kStr; ++r) tot[r] = 0.0f;
-          for (int cr = 0; cr < CL; ++cr) {
+          for (int cr = 0; cr < 2 * CL; ++cr) {
             const float* src = recv + ((size_t)(cr * rpo + ot)) * C::kStr;
 #pragma unroll
             for (int r = 0; r < C::kStr; r += 4) {
@@ -348,7 +402,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (cuse > 0 &&
           !__all_sync(0xffffffffu, wait_bar<true>(&tail->coef_free[cb], (cuse - 1) & 1u, ctl, kErrClusterWait)))
         break;
-      float inv_rms[2] = {0.0f, 0.0f};
+      float H[2][NS * NS];                         // residual logits, kept for the Sinkhorn
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
         const int ot = lane + 32 * h;
@@ -356,7 +410,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int row = (int)rank * rpo + ot;
           const int tok = tile * kTileT + row;
           float cf[NS];
-          inv_rms[h] = token_gates<NS, RR>(ep, tok, mix[h], ssq[h], tok < g.T, cf);
+          const float inv_rms = token_gates<NS, RR>(ep, tok, mix[h], ssq[h], tok < g.T, cf);
+          residual_logits<NS, RR>(ep, mix[h], inv_rms, H[h]);
           float* dst = coef_buf + ((size_t)cb * kTileT + row) * NS;
           for (int cr = 0; cr < CL; ++cr) {
             if constexpr (NS % 4 == 0) {
@@ -372,43 +427,16 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       __syncwarp();
       if (lane < CL) mbar_arrive_remote(&tail->coef_full[cb], (uint32_t)lane);
-      // hand the owned rows to the Sinkhorn warp
-      const int sb = (int)(k & 1u);
-      if ((k >> 1) > 0 &&
-          !__all_sync(0xffffffffu, wait_bar<false>(&tail->sink_free[sb], ((k >> 1) - 1) & 1u, ctl, kErrWaitTimeout)))
-        break;
+      // Sinkhorn for comb: y no longer waits on this tile
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
         const int ot = lane + 32 * h;
         if (ot < rpo) {
-          float H[NS * NS];
-          residual_logits<NS, RR>(ep, mix[h], inv_rms[h], H);
-          float* e = sink_buf + ((size_t)sb * kTileT + ot) * C::kSink;
-#pragma unroll
-          for (int r = 0; r < NS * NS; ++r) e[r] = H[r];
-        }
-      }
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&tail->sink_full[sb]);
-    }
-  } else if (warp == kWarpSink) {
-    // ================================================= Sinkhorn for comb (off y's path)
-    uint32_t k = 0;
-    for (int tile = cluster_id; tile < g.num_tiles; tile += num_clusters, ++k) {
-      const int sb = (int)(k & 1u);
-      if (!__all_sync(0xffffffffu, wait_bar<false>(&tail->sink_full[sb], (k >> 1) & 1u, ctl, kErrWaitTimeout)))
-        break;
-#pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        const int ot = lane + 32 * h;
-        if (ot < rpo) {
-          const float* e = sink_buf + ((size_t)sb * kTileT + ot) * C::kSink;
           const int tok = tile * kTileT + (int)rank * rpo + ot;
-          token_sinkhorn<NS, C::kThree>(ep, tok, e, tok < g.T);
+          token_sinkhorn<NS, C::kThree>(ep, tok, H[h], tok < g.T);
         }
       }
       __syncwarp();
-      if (lane == 0) mbar_arrive(&tail->sink_free[sb]);
     }
   } else if (warp >= kWarpYc0) {
     // ================================================= y for this member's d-range

@@ -72,3 +72,28 @@ def test_grid_path_deterministic(cuda_device, monkeypatch):
     torch.cuda.synchronize()
     for k in ("y", "h_post", "h_res", "h_pre", "inv_rms", "h_mix", "sum_out", "norm_out"):
         assert torch.equal(a[k], b[k]), k
+
+
+@pytest.mark.parametrize("path", ["cluster", "tile128", "grid"])
+@pytest.mark.parametrize("x_dtype", [torch.bfloat16, torch.float16])
+def test_repeated_runs_bitwise(cuda_device, monkeypatch, path, x_dtype):
+    """Twenty runs of one input agree bit for bit on every output: the
+    reductions run in a fixed order, so any difference is a read of a
+    buffer before its data is in (or after it is reused)."""
+    if x_dtype == torch.float16 and path != "cluster":
+        pytest.skip("fp16 x runs on the 64-token cluster kernel only")
+    monkeypatch.delenv("MHC_PRE_PATH", raising=False)
+    monkeypatch.delenv("MHC_PRE_TILE", raising=False)
+    monkeypatch.setenv("MHC_PRE_PATH", "grid" if path == "grid" else "cluster")
+    if path == "tile128":
+        monkeypatch.setenv("MHC_PRE_TILE", "128")
+    case = make_case("training", device=cuda_device, x_dtype=x_dtype)
+    op, ref = run_cuda(case)
+    torch.cuda.synchronize()
+    ref = {k: v.clone() for k, v in ref.items() if isinstance(v, torch.Tensor)}
+    out = op.allocate(case.T, cuda_device)
+    for _ in range(20):
+        run_cuda(case, op=op, out=out)
+        torch.cuda.synchronize()
+        for k, v in ref.items():
+            assert torch.equal(out[k], v), k
