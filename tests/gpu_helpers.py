@@ -9,11 +9,13 @@ Tolerances (against the double-precision oracle):
     3e-3 there);
   * intermediates (fp32 mode): invRms rel 1e-4; hMix |err| <= 2e-4 (1 + |ref|)
     -- fp32 accumulation over n*D products; sumOut rel 1e-4; normOut 1e-4.
-    The invRms bound: Sigma x^2 is accumulated on the tensor core in fp32
-    over n*D/C products per CTA (C = cluster size), 16 per step; with each
-    step off by at most an ulp (2^-23) in the same direction the sum is off
-    by at most (n*D/(16 C)) 2^-23 -- 1.07e-4 at n*D = 28672, C = 2 -- and
-    invRms by half of that, 5.3e-5 (measured up to 2.6e-5).
+    The invRms bound: Sigma x^2 is accumulated in fp32, each token's squares
+    split over 2 C partial sums (C = cluster size, two halves of the
+    streams per member) of 8 running sums each, so a running sum takes
+    n*D/(16 C) additions; with each addition off by at most an ulp (2^-23)
+    in the same direction the total is off by at most (n*D/(16 C)) 2^-23
+    -- 1.07e-4 at n*D = 28672, C = 2 -- and invRms by half of that, 5.3e-5
+    (measured up to 2.6e-5).
 """
 from __future__ import annotations
 
