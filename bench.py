@@ -157,15 +157,29 @@ KERNEL_SOURCES = {"mhc_pre_tc_kernel": "mhc_pre_tc.cu", "mhc_pre_gw_kernel": "mh
                   "mhc_pre_t128_kernel": "mhc_pre_t128.cu", "bw_main_kernel": "mhc_bwd.cu"}
 
 
+def _code_only(text):
+    """Source text without // comments, trailing blanks and blank lines, so
+    that editing a comment leaves the hash of the code alone."""
+    out = []
+    for line in text.splitlines():
+        i = line.find("//")
+        if i >= 0:
+            line = line[:i]
+        line = line.rstrip()
+        if line:
+            out.append(line)
+    return "\n".join(out)
+
+
 def kernel_hash(kernel):
-    """Hash of a fused kernel's device sources (its traffic record is void
-    once they change)."""
+    """Hash of a fused kernel's device code (its traffic record is void once
+    the code changes; comments do not count)."""
     h = hashlib.sha256()
     d = os.path.join(ROOT, "mhc_hyper_connection_gb300", "csrc")
     for name in ("mhc_common.cuh", "mhc_ptx.cuh", KERNEL_SOURCES[kernel]):
-        with open(os.path.join(d, name), "rb") as f:
+        with open(os.path.join(d, name), encoding="utf-8") as f:
             h.update(name.encode())
-            h.update(f.read())
+            h.update(_code_only(f.read()).encode())
     return h.hexdigest()[:16]
 
 

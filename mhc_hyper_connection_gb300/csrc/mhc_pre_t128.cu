@@ -327,8 +327,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp == kW_GATE) {
     // ================================================= gates (critical for y)
     // Owned rows (lane + 32 h): sum the members' partials in rank order,
-    // compute invRms and the gates, send the y weights to every member, hand
-    // the row's residual logits to the Sinkhorn warp.
+    // compute invRms and the gates, send the y weights to every member, then
+    // run the rows' Sinkhorn.
     uint32_t k = 0;
     for (int tile = cluster_id; tile < g.num_tiles; tile += num_clusters, ++k) {
       if (!__all_sync(0xffffffffu, wait_bar<true>(&tail->part_full, k & 1u, ctl, kErrClusterWait))) break;

@@ -5,21 +5,24 @@
 // 全解析" §三 and "aclnnMhcPreSinkhorn 接口与 MhcPreSinkhorn 实现剖析" §3.2;
 // how it is laid out on the GPU is this file's own design:
 //
-//  * A token tile is 64 tokens: rows 0..63 of an M = 128 MMA (rows 64..127
-//    are never read).  A cluster of C CTAs shares one tile; CTA c owns a
-//    contiguous range of 64-wide d-chunks and streams those chunks of all n
-//    streams, so each byte of x is read from HBM once per tile.
+//  * A token tile is 64 tokens.  A cluster of C CTAs shares one tile; CTA c
+//    owns a contiguous range of 64-wide d-chunks and streams those chunks of
+//    all n streams, so each byte of x is read from HBM once per tile.
 //  * Per chunk, TMA brings x[64 tokens][64] of a group of streams (bf16,
 //    128-byte swizzle) and the matching 64 columns of the stacked phi planes;
-//    one thread issues tcgen05.mma (K = 16 each), N = NP into TMEM.
-//  * Two publish warps (thread = token) sum each token's squares from every
-//    x box as it lands (CUDA cores: an x.x^T block on the tensor core would
-//    double its operand reads from shared memory, which bound the MMA), then
-//    read the accumulators, fold the precision planes and push the CTA's
-//    partial sums to the member that owns the row (distributed shared
-//    memory).  The owner's gate warp sums
-//    them in rank order, computes invRms and the gates, and sends the y
-//    weights to every member; a Sinkhorn warp produces comb off y's path.
+//    one thread issues tcgen05.mma (M = 128, K = 16 each) into TMEM, two
+//    streams per MMA where their planes fit N <= 256 (A rows 0..63 and
+//    64..127 are the two streams' tokens), else one stream per MMA with A
+//    rows 64..127 unused.
+//  * Four publish warps (thread = token, one warp per TMEM lane quarter) sum
+//    each token's squares from every x box as it lands (CUDA cores: an
+//    x.x^T block on the tensor core would double its operand reads from
+//    shared memory, which bound the MMA), then read the accumulators, fold
+//    the precision planes and push the CTA's partial sums to the member that
+//    owns the row (distributed shared memory).  The owner's gate warp sums
+//    them in (rank, half) order, computes invRms and the gates, sends the y
+//    weights to every member, then runs the rows' Sinkhorn for comb, off
+//    y's path.
 //  * Eight warps form y for the CTA's d-range by re-reading x from global
 //    memory, newest chunk first.
 //  * This kernel serves shapes whose phi blocks are too large to stay
