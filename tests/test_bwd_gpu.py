@@ -211,3 +211,17 @@ def test_phi_gamma_at_4_byte_offset(cuda_device):
     out = _run_gpu(S)
     for k in ("grad_x", "grad_phi", "grad_alpha", "grad_bias", "grad_gamma"):
         assert torch.equal(out[k], ref[k]), k
+
+
+def test_repeated_runs_bitwise(cuda_device):
+    """Twenty runs of one backward agree bit for bit on every gradient (the
+    reductions run in a fixed order, so any difference is a read of a
+    buffer before its data is in, or after it is reused)."""
+    S = _setup(cuda_device, 2048, 1024, seed=5, gxp=True)
+    ref = _run_gpu(S)
+    ref = {k: v.clone() for k, v in ref.items() if isinstance(v, torch.Tensor)}
+    grads = S.op.allocate_backward(S.case.T, cuda_device, gamma=True)
+    for _ in range(20):
+        _run_gpu(S, grads)
+        for k, v in ref.items():
+            assert torch.equal(grads[k], v), k
