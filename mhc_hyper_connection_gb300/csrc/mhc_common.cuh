@@ -291,6 +291,11 @@ __host__ __device__ constexpr int w_group(int n, int R, int P) {
          : (n % 2 == 0 && 2 * plane_box_rows(R, P) * 128 <= 36864) ? 2
                                                                     : 1;
 }
+// Whether the 64-token kernel runs two streams per MMA: the box holds an
+// even number of streams, and two streams' plane rows fit N <= 256.
+__host__ __device__ constexpr bool stream_pairs(int n, int R, int P) {
+  return stream_group(n) % 2 == 0 && w_group(n, R, P) % 2 == 0 && 2 * plane_box_rows(R, P) <= 256;
+}
 // Floats per published partial (R sums + the sum of squares), padded to 16 bytes.
 __host__ __device__ constexpr int partial_stride(int R) { return ((R + 1 + 3) / 4) * 4; }
 // Floats per Sinkhorn hand-off entry: the n*n residual logits of one token.
@@ -309,7 +314,9 @@ __host__ __device__ inline SmemLayout smem_layout(int n, int R, int P, int xs, i
   L.x = o;    o += (size_t)xs * stream_group(n) * kStreamTile;
   L.w = o;    o += (size_t)ws * w_group(n, R, P) * plane_box_rows(R, P) * 128;
   o += 1024;  // the B operand of N = NP rows reads up to 8 rows past the last w box
-  L.part = o; o += 2 * (size_t)kTileT * partial_stride(R) * 4;   // two partials per member and row
+  // two partials per member and row with stream pairs (each half of the
+  // publish warps has projection sums), else one
+  L.part = o; o += (stream_pairs(n, R, P) ? 2 : 1) * (size_t)kTileT * partial_stride(R) * 4;
   L.coef = o; o += (size_t)kCoefBufs * kTileT * n * 4;
   o = (o + 15) & ~size_t(15);
   L.tail = o; o += kTailBytes;

@@ -55,7 +55,8 @@ struct Cfg {
   // rows 64..127 x columns [kWRows, 2 kWRows) are the two streams' partial
   // projections (the off-diagonal blocks are never read).  Without pairs
   // the MMA runs N = NP per stream and rows 64..127 are never read.
-  static constexpr bool kPair = kSG % 2 == 0 && kWG % 2 == 0 && 2 * kWRows <= 256;
+  static constexpr bool kPair = stream_pairs(NS, RR, P);
+  static constexpr int kHalves = kPair ? 2 : 1;                  // published partials per member and row
   static constexpr int kStep = kPair ? 2 : 1;                    // streams per MMA
   static constexpr int kMmaN = kPair ? 2 * kWRows : kNP;
   static constexpr int kAccCols = kMmaN <= 64 ? 64 : kMmaN <= 128 ? 128 : 256;
@@ -75,6 +76,7 @@ struct SmemTail {
   uint64_t mma_done;
   uint32_t tmem_base;
   uint32_t abort;
+  float ssq_hand[kTileT];                       // unpaired shapes: half 1's sums of squares for half 0
 };
 static_assert(sizeof(SmemTail) <= kTailBytes, "barrier block outgrew its reservation");
 
@@ -116,7 +118,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int XS = g.xstages, WS = g.wstages;
   uint8_t* sX = smem + Ly.x;
   uint8_t* sW = smem + Ly.w;
-  float* recv = reinterpret_cast<float*>(smem + Ly.part);     // [CL][2][64/CL][kStr]
+  float* recv = reinterpret_cast<float*>(smem + Ly.part);     // [CL][kHalves][64/CL][kStr]
   float* coef_buf = reinterpret_cast<float*>(smem + Ly.coef); // [kCoefBufs][64][NS]
   SmemTail* tail = reinterpret_cast<SmemTail*>(smem + Ly.tail);
 
@@ -149,7 +151,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&tail->coef_full[b], CL);
       mbar_init(&tail->coef_free[b], CL);
     }
-    mbar_init(&tail->part_full, 2 * CL);        // two arrivals per cluster member
+    mbar_init(&tail->part_full, C::kHalves * CL);   // one arrival per member and published half
     mbar_init(&tail->part_free, CL);
     mbar_init(&tail->mma_done, 1);
     tail->abort = 0u;
@@ -331,9 +333,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       // all four warps leave together if any gave up (the producer stops on
       // the abort flag, so the others' waits end too)
       if (!role_all<kBarPub, kPubThreads>(ok)) break;
-      const float ssq = tree_sum<8>(s8);
+      float ssq = tree_sum<8>(s8);
+      // unpaired: half 1 has no projection sums, so half 0 publishes its
+      // sums of squares too (read after the barrier below; half 1 writes the
+      // next tile's only after the barrier that ends this tile's publish)
+      if (!C::kPair && half == 1) tail->ssq_hand[et] = ssq;
       if (!role_all<kBarPub, kPubThreads>(wait_bar<false>(&tail->acc_full[acc], acc_phase, ctl, kErrWaitTimeout)))
         break;
+      if (!C::kPair && half == 0) ssq += tail->ssq_hand[et];
       tc_fence_after();
       float mix[RR];
 #pragma unroll
@@ -350,19 +357,21 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (k > 0 &&
           !role_all<kBarPub, kPubThreads>(wait_bar<true>(&tail->part_free, (k - 1) & 1u, ctl, kErrClusterWait)))
         break;
-      float* dst = recv + ((size_t)(((int)rank * 2 + half) * rpo + slot)) * C::kStr;
+      if (C::kPair || half == 0) {
+        float* dst = recv + ((size_t)(((int)rank * C::kHalves + half) * rpo + slot)) * C::kStr;
 #pragma unroll
-      for (int r = 0; r < C::kStr; r += 4) {
-        float4 v;
-        v.x = r < RR ? mix[r] : (r == RR ? ssq : 0.0f);
-        v.y = r + 1 < RR ? mix[r + 1] : (r + 1 == RR ? ssq : 0.0f);
-        v.z = r + 2 < RR ? mix[r + 2] : (r + 2 == RR ? ssq : 0.0f);
-        v.w = r + 3 < RR ? mix[r + 3] : (r + 3 == RR ? ssq : 0.0f);
-        st_dsmem_v4(dst + r, (uint32_t)owner, v);
+        for (int r = 0; r < C::kStr; r += 4) {
+          float4 v;
+          v.x = r < RR ? mix[r] : (r == RR ? ssq : 0.0f);
+          v.y = r + 1 < RR ? mix[r + 1] : (r + 1 == RR ? ssq : 0.0f);
+          v.z = r + 2 < RR ? mix[r + 2] : (r + 2 == RR ? ssq : 0.0f);
+          v.w = r + 3 < RR ? mix[r + 3] : (r + 3 == RR ? ssq : 0.0f);
+          st_dsmem_v4(dst + r, (uint32_t)owner, v);
+        }
       }
       role_sync<kBarPub, kPubThreads>();
-      // one arrival per half at every owner
-      if ((q & 1) == 0 && lane < CL) mbar_arrive_remote(&tail->part_full, (uint32_t)lane);
+      // one arrival per published half at every owner
+      if ((q & 1) == 0 && (C::kPair || half == 0) && lane < CL) mbar_arrive_remote(&tail->part_full, (uint32_t)lane);
     }
   } else if (warp == kWarpGate) {
     // ================================================= gates (critical for y), then Sinkhorn
@@ -381,7 +390,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           float tot[C::kStr];
 #pragma unroll
           for (int r = 0; r < C::kStr; ++r) tot[r] = 0.0f;
-          for (int cr = 0; cr < 2 * CL; ++cr) {
+          for (int cr = 0; cr < C::kHalves * CL; ++cr) {
             const float* src = recv + ((size_t)(cr * rpo + ot)) * C::kStr;
 #pragma unroll
             for (int r = 0; r < C::kStr; r += 4) {

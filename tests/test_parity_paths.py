@@ -97,3 +97,23 @@ def test_repeated_runs_bitwise(cuda_device, monkeypatch, path, x_dtype):
         torch.cuda.synchronize()
         for k, v in ref.items():
             assert torch.equal(out[k], v), k
+
+
+@pytest.mark.parametrize("name,kw", [("generic_a", {}), ("tiny", {"n": 6, "D": 592, "alpha_len": 3})])
+def test_repeated_runs_bitwise_unpaired(cuda_device, monkeypatch, name, kw):
+    """As above for shapes that run one stream per MMA (n = 8 three-gate,
+    n = 6), whose sums of squares take the single-partial hand-off."""
+    monkeypatch.delenv("MHC_PRE_TILE", raising=False)
+    monkeypatch.setenv("MHC_PRE_PATH", "cluster")
+    case = make_case(name, device=cuda_device, **kw)
+    op, ref = run_cuda(case)
+    torch.cuda.synchronize()
+    compare(case, ref, run_oracle(case, tokens=list(range(0, case.T, max(1, case.T // 64)))),
+            tokens=list(range(0, case.T, max(1, case.T // 64))))
+    ref = {k: v.clone() for k, v in ref.items() if isinstance(v, torch.Tensor)}
+    out = op.allocate(case.T, cuda_device)
+    for _ in range(10):
+        run_cuda(case, op=op, out=out)
+        torch.cuda.synchronize()
+        for k, v in ref.items():
+            assert torch.equal(out[k], v), k
