@@ -54,7 +54,6 @@ struct T128Cfg {
   static constexpr int kWBoxes = NS / kWG;                       // phi runs per d-chunk
   static constexpr int kWBytes = kWG * kWRows * 128;
   static constexpr int kStr = partial_stride(RR);                // floats per published partial
-  static constexpr int kSink = NS * NS;
   static constexpr bool kThree = (RR == NS * NS + 2 * NS);
   static constexpr int kYBatch = 4;                              // y items in flight per thread
 };
@@ -380,7 +379,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           // keep the residual logits in the row's own owned-sum slot for the
           // Sinkhorn below (the two-gate form has none)
           if constexpr (C::kThree) {
-            static_assert(C::kSink <= C::kStr, "logits fit the owned-sum slot");
+            static_assert(NS * NS <= C::kStr, "logits fit the owned-sum slot");
             float H[NS * NS];
             residual_logits<NS, RR>(ep, mix, inv_rms, H);
             float* ho = owned + (size_t)ot * C::kStr;
