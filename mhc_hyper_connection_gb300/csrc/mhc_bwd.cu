@@ -817,7 +817,10 @@ void bw_rowdot_shape(int D, size_t max_smem, int* tps, int* stages, size_t* smem
   size_t st = avail / (t * tok);
   if (st > (size_t)kRdMaxStages) st = kRdMaxStages;
   *tps = (int)t;
-  *stages = st >= 2 ? (int)st : 0;
+  // one stage when two whole token rows do not fit (D above ~11.6 k): each
+  // CTA then loads and reduces one token at a time, and the 152 SMs' rows in
+  // flight still cover HBM latency
+  *stages = st >= 1 ? (int)st : 0;
   *smem_bytes = (size_t)(*stages) * t * tok + sizeof(RdTail);
 }
 

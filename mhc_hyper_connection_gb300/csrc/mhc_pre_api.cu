@@ -800,7 +800,7 @@ mhc_status_t mhc_pre_backward_run(mhc_pre_t h, const mhc_pre_bwd_args* a, void* 
   rp.err = err;
   size_t rd_smem = 0;
   mhc::bw_rowdot_shape(D, di.max_smem, &rp.tps, &rp.stages, &rd_smem);
-  if (rp.stages < 2) return fail(MHC_ERR_RUNTIME, "not enough shared memory for the row-dot ring");
+  if (rp.stages < 1) return fail(MHC_ERR_RUNTIME, "not enough shared memory for the row-dot ring");
   const long long rd_groups = (T + rp.tps - 1) / rp.tps;
   const int rd_grid = (int)(rd_groups < di.sms ? rd_groups : di.sms);
 

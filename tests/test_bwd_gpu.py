@@ -225,3 +225,15 @@ def test_repeated_runs_bitwise(cuda_device):
         _run_gpu(S, grads)
         for k, v in ref.items():
             assert torch.equal(grads[k], v), k
+
+
+@pytest.mark.parametrize("D", [11264, 16384])
+def test_widest_rows(cuda_device, D):
+    """The widest D (16384, the pages' bound with 64-element alignment) and
+    the widest that still takes a two-stage row-dot ring: every output on
+    sampled tokens and columns."""
+    S = _setup(cuda_device, 130, D, gamma=True, seed=D)
+    grads = _run_gpu(S)
+    toks = np.array(sorted({0, 1, 63, 64, 65, 127, 128, 129}), dtype=np.int64)
+    cols = np.array(sorted({0, 63, 64, D - 1, D, 2 * D + 5, 4 * D - 1}), dtype=np.int64)
+    print(_check(S, grads, _run_oracle(S, tokens=toks, columns=cols), tokens=toks, columns=cols))

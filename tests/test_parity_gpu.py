@@ -151,3 +151,10 @@ def test_phi_gamma_at_4_byte_offset(cuda_device):
     torch.cuda.synchronize()
     for k in ("y", "h_post", "h_res", "h_pre", "inv_rms", "h_mix"):
         assert torch.equal(out[k], ref[k]), k
+
+
+@pytest.mark.parametrize("n", [4, 6, 8])
+def test_widest_rows(cuda_device, n):
+    """D = 16384, the largest width the pages allow, for every n (n*D up to
+    131072): a ragged token count with the backward outputs, in full."""
+    _full(make_case("tiny", device=cuda_device, T=130, n=n, D=16384, need_backward=True, gamma=True))
