@@ -158,3 +158,81 @@ def test_widest_rows(cuda_device, n):
     """D = 16384, the largest width the pages allow, for every n (n*D up to
     131072): a ragged token count with the backward outputs, in full."""
     _full(make_case("tiny", device=cuda_device, T=130, n=n, D=16384, need_backward=True, gamma=True))
+
+
+# ------------------------------------------------------------ degenerate inputs
+
+def _case(name, x, phi, alpha, bias, gamma=None, impl_mode=0, need_backward=False):
+    from mhc_synth import Case
+    T, n, D = x.shape
+    return Case(name=name, T=T, n=n, D=D, alpha_len=alpha.numel(), num_iters=20, norm_eps=1e-6, hc_eps=1e-6,
+                impl_mode=impl_mode, need_backward=need_backward, x=x, phi=phi, alpha=alpha, bias=bias,
+                gamma=gamma, pre_mix=None)
+
+
+def _uniform_comb(n, iters, eps):
+    # equal logits: softmax gives 1/n, then every normalisation maps a -> a / (n a + eps)
+    a = 1.0 / n + eps
+    a = a / (n * a + eps)
+    for _ in range(iters - 1):
+        a = a / (n * a + eps)
+        a = a / (n * a + eps)
+    return a
+
+
+@pytest.mark.parametrize("mode", [0, 1])
+def test_all_ones_example(cuda_device, mode):
+    """The MhcPreV2 page's worked call (x = phi = alpha = bias = gamma = 1,
+    T = 2048, n = 4, D = 2560): the gates saturate and the softmax sees equal
+    logits of about 10241, so this checks the max subtraction on the GPU.
+    Closed forms: hPre = 1 + eps, hPost = 2, comb = the uniform scalar map,
+    y = 4 (1 + eps), which rounds to 4.0 in bf16."""
+    T, n, D = 2048, 4, 2560
+    R, K = n * n + 2 * n, n * D
+    f32 = dict(dtype=torch.float32, device=cuda_device)
+    case = _case("all_ones", torch.ones((T, n, D), dtype=torch.bfloat16, device=cuda_device),
+                 torch.ones((R, K), **f32), torch.ones(3, **f32), torch.ones(R, **f32), torch.ones((n, D), **f32),
+                 impl_mode=mode)
+    _, out = run_cuda(case)
+    torch.cuda.synchronize()
+    tol = 1e-4 if mode == 0 else 3e-3
+    assert torch.all(out["y"] == 4.0)
+    assert (out["h_pre"] - (1 + 1e-6)).abs().max().item() <= tol
+    assert (out["h_post"] - 2.0).abs().max().item() <= tol
+    assert (out["h_res"] - _uniform_comb(n, 20, 1e-6)).abs().max().item() <= tol
+    compare(case, out, run_oracle(case, [0, 1, 1000, 2047]), tokens=[0, 1, 1000, 2047])
+
+
+def test_alpha_zero(cuda_device):
+    """alpha = 0: the gates reduce to the biases (hPre = sigmoid(b) + eps,
+    hPost = 2 sigmoid(b)) and comb is the Sinkhorn of the bias matrix, the
+    same for every token -- independent of x, phi and the projection."""
+    case = make_case("training", device=cuda_device, T=1000)
+    case.alpha = torch.zeros(3, dtype=torch.float32, device=cuda_device)
+    _, out = run_cuda(case)
+    torch.cuda.synchronize()
+    n = case.n
+    b = case.bias.double()
+    pre = torch.sigmoid(b[:n]) + 1e-6
+    post = 2 * torch.sigmoid(b[n:2 * n])
+    assert (out["h_pre"].double() - pre).abs().max().item() <= 1e-4
+    assert (out["h_post"].double() - post).abs().max().item() <= 1e-4
+    assert torch.equal(out["h_res"], out["h_res"][:1].expand_as(out["h_res"]))
+    compare(case, out, run_oracle(case, list(range(0, 1000, 37))), tokens=list(range(0, 1000, 37)))
+
+
+def test_stable_inputs(cuda_device):
+    """The Sinkhorn page's stable inputs (phi = 1/sqrt(nD), alpha = 0.25,
+    bias = 0): every projection row of a token is the same number, so the
+    four hPre of a token agree and comb is the uniform scalar map."""
+    case = make_case("tiny", device=cuda_device, T=300, D=1024)
+    K = case.n * case.D
+    case.phi = torch.full_like(case.phi, 1.0 / K ** 0.5)
+    case.alpha = torch.full((3,), 0.25, dtype=torch.float32, device=cuda_device)
+    case.bias = torch.zeros_like(case.bias)
+    _, out = run_cuda(case)
+    torch.cuda.synchronize()
+    hp = out["h_pre"]
+    assert (hp - hp[:, :1]).abs().max().item() <= 1e-6
+    assert (out["h_res"] - _uniform_comb(case.n, 20, 1e-6)).abs().max().item() <= 1e-6
+    compare(case, out, run_oracle(case))
