@@ -237,3 +237,17 @@ def test_widest_rows(cuda_device, D):
     toks = np.array(sorted({0, 1, 63, 64, 65, 127, 128, 129}), dtype=np.int64)
     cols = np.array(sorted({0, 63, 64, D - 1, D, 2 * D + 5, 4 * D - 1}), dtype=np.int64)
     print(_check(S, grads, _run_oracle(S, tokens=toks, columns=cols), tokens=toks, columns=cols))
+
+
+def test_zero_upstream_gradients(cuda_device):
+    """Zero gradients of y, hPost and comb give zero gradients everywhere,
+    and grad_x_post passes through to grad_x unchanged (one bf16 value plus
+    zero)."""
+    S = _setup(cuda_device, 200, 512, seed=9, gxp=True)
+    S.g.g_in.zero_()
+    S.g.g_post.zero_()
+    S.g.g_res.zero_()
+    grads = _run_gpu(S)
+    assert torch.equal(grads["grad_x"], S.g.g_x_post)
+    for k in ("grad_phi", "grad_alpha", "grad_bias", "grad_gamma"):
+        assert torch.count_nonzero(grads[k]).item() == 0, k

@@ -82,3 +82,10 @@ def test_stream_and_determinism(cuda_device):
     torch.cuda.synchronize()
     assert torch.equal(a, b)
     _check(case, a)
+
+
+@pytest.mark.parametrize("n", [4, 8])
+def test_widest_rows(cuda_device, n):
+    """D = 16384, the widest hidden size of the pre-mapping it follows."""
+    case = make_post_case(device=cuda_device, T=9, n=n, D=16384, seed=n)
+    _check(case, _run(case))
