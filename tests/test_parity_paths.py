@@ -117,3 +117,35 @@ def test_repeated_runs_bitwise_unpaired(cuda_device, monkeypatch, name, kw):
         torch.cuda.synchronize()
         for k, v in ref.items():
             assert torch.equal(out[k], v), k
+
+
+def _random_configs(count=24, seed=20261202):
+    """Seeded random shapes and flags over the forward's whole scope."""
+    import random
+    rnd = random.Random(seed)
+    out = []
+    for k in range(count):
+        n = rnd.choice([4, 4, 6, 8])
+        out.append(dict(T=rnd.choice([1, 2, 63, 64, 65, 127, 200, 513, 700]),
+                        n=n, D=16 * rnd.randint(1, 96), alpha_len=rnd.choice([2, 3]),
+                        impl_mode=rnd.choice([0, 1]), gamma=rnd.random() < 0.5,
+                        pre_mix=rnd.random() < 0.3, need_backward=rnd.random() < 0.5,
+                        path=rnd.choice(["auto", "cluster", "grid"]), seed=k))
+    return out
+
+
+@pytest.mark.parametrize("cfg", _random_configs(), ids=lambda c: "T{T}_n{n}_D{D}_a{alpha_len}_m{impl_mode}_{path}".format(**c))
+def test_random_shapes(cuda_device, monkeypatch, cfg):
+    """Seeded random shapes, gate forms, modes and optional inputs on every
+    forward path, each compared in full with the oracle."""
+    cfg = dict(cfg)
+    path = cfg.pop("path")
+    seed = cfg.pop("seed")
+    case = make_case("tiny", device=cuda_device, seed=seed, **cfg)
+    monkeypatch.delenv("MHC_PRE_TILE", raising=False)
+    monkeypatch.delenv("MHC_PRE_PATH", raising=False)
+    if path != "auto":
+        monkeypatch.setenv("MHC_PRE_PATH", path)
+    op, out = run_cuda(case)
+    torch.cuda.synchronize()
+    compare(case, out, run_oracle(case))
