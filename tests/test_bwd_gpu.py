@@ -251,3 +251,22 @@ def test_zero_upstream_gradients(cuda_device):
     assert torch.equal(grads["grad_x"], S.g.g_x_post)
     for k in ("grad_phi", "grad_alpha", "grad_bias", "grad_gamma"):
         assert torch.count_nonzero(grads[k]).item() == 0, k
+
+
+def _random_bwd_configs(count=12, seed=77):
+    import random
+    rnd = random.Random(seed)
+    return [dict(T=rnd.choice([1, 2, 63, 64, 65, 129, 300, 700]), D=64 * rnd.randint(1, 40),
+                 gamma=rnd.random() < 0.5, sinkhorn=rnd.random() < 0.7, gxp=rnd.random() < 0.4,
+                 impl_mode=rnd.choice([0, 0, 1]), seed=k) for k in range(count)]
+
+
+@pytest.mark.parametrize("cfg", _random_bwd_configs(),
+                         ids=lambda c: "T{T}_D{D}_g{gamma:d}_s{sinkhorn:d}_x{gxp:d}_m{impl_mode}".format(**c))
+def test_random_shapes(cuda_device, cfg):
+    """Seeded random token counts, widths and forms, each in full against the
+    backward oracle."""
+    S = _setup(cuda_device, cfg["T"], cfg["D"], gamma=cfg["gamma"], sinkhorn=cfg["sinkhorn"], gxp=cfg["gxp"],
+               impl_mode=cfg["impl_mode"], seed=cfg["seed"] + 1000)
+    grads = _run_gpu(S)
+    _check(S, grads, _run_oracle(S))
