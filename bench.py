@@ -39,13 +39,15 @@ WORKLOAD = dict(name="prefill", T=32768, n=4, D=7168, impl_mode=0, num_iters=20)
 
 
 def per_token_bytes(n, D, need_backward=False, pre_mix=False, alpha_len=3, iters=20):
-    """Algorithmic bytes per token: x in, y out, hPost + comb + hPre out."""
+    """Algorithmic bytes per token: x in, y out, hPost + hPre out, and comb
+    with three gates (the two-gate form's optional comb is all zeros and not
+    counted)."""
     R = n * n + 2 * n if alpha_len == 3 else 2 * n
-    b = 2 * n * D + 2 * D + 4 * (n * n + 2 * n)
+    b = 2 * n * D + 2 * D + 4 * (2 * n) + (4 * n * n if alpha_len == 3 else 0)
     if pre_mix:
         b += 4 * n
     if need_backward:
-        b += 4 + 4 * R + 2 * iters * 4 * (n + n * n)
+        b += 4 + 4 * R + (2 * iters * 4 * (n + n * n) if alpha_len == 3 else 0)
     return b
 
 

@@ -58,3 +58,23 @@ def test_single_rank_helpers():
     assert bench.max_over_ranks(3.5, 1) == 3.5
     assert bench.per_token_bytes(4, 7168) == 71776
     assert bench.launch_bytes(32768, 4, 7168) == 32768 * 71776 + 4 * 24 * 28672
+
+
+def test_algorithmic_bytes_of_every_workload():
+    """The per-token byte counts the roofline divides by, for each workload:
+    x in, y out, the gate outputs (comb only with three gates), pre_mix in,
+    and the backward outputs (invRms, hMix, every Sinkhorn step's sums and
+    matrices) when asked for."""
+    assert bench.per_token_bytes(4, 256) == 2 * 4 * 256 + 2 * 256 + 4 * 24            # tiny: 2,656
+    assert bench.per_token_bytes(4, 256) == 2656
+    assert bench.per_token_bytes(4, 4096, need_backward=True) == 41056 + 3300         # training
+    assert bench.per_token_bytes(4, 7168) == 71776                                     # decode, prefill
+    assert bench.per_token_bytes(8, 2048, pre_mix=True) == 37216                       # generic A
+    assert bench.per_token_bytes(8, 2048, alpha_len=2) == 36928                        # generic B
+    # two gates with the backward outputs: invRms and the 2n mixes, no Sinkhorn steps
+    assert bench.per_token_bytes(4, 64, need_backward=True, alpha_len=2) == 2 * 256 + 128 + 32 + 4 + 32
+    # the backward and its contraction kernel; the post-mapping
+    assert bench.bwd_token_bytes(4, 7168) == 132436
+    assert bench.bwd_main_token_bytes(4, 7168) == 129024
+    # x read (2D), residual read and out written (2nD each), post (4n) and comb (4n^2) read
+    assert bench.post_token_bytes(4, 7168) == 2 * 7168 + 2 * (2 * 4 * 7168) + 4 * 4 + 4 * 16 == 129104
