@@ -394,21 +394,24 @@ mhc_status_t mhc_pre_run(mhc_pre_t h, const mhc_pre_args* a, void* stream) {
     return fail(MHC_ERR_RUNTIME, "plane preparation launch failed: %s", cudaGetErrorString(cudaGetLastError()));
 
   // 2. the fused forward.  The grid-wide kernel spreads a few token tiles
-  //    over every SM and is the faster one up to kGwAutoMaxT tokens (T = 64 at
-  //    D = 7168: 22.5 against 28.9 us; T = 512: 35.6 against 40.2 us; T =
-  //    2048: 110 against 73 us); the cluster kernel takes larger batches.
-  //    MHC_PRE_PATH=grid or =cluster forces one (tests and tuning runs).
-  //    fp16 x and batch-consistent mode always run the cluster kernel.
+  //    over every SM; up to kGwAutoMaxT tokens it runs when the cluster kernel
+  //    would have a single tile or need more than one round of clusters, the
+  //    cases where it is faster (D = 7168, kernel time: T = 64 22.8 against
+  //    26.7 us, T = 512 36.2 against 39.9 us; but T = 256 35.0 against 26.7,
+  //    and T = 768 43.3 against 40.3).  MHC_PRE_PATH=grid or =cluster forces
+  //    one (tests and tuning runs).  fp16 x and batch-consistent mode always
+  //    run the cluster kernel.
   const bool fp16 = c.x_dtype == MHC_DTYPE_FP16;
   const bool consistent = c.batch_consistent != 0;
   const char* path = getenv("MHC_PRE_PATH");
   const bool force_grid = path && !strcmp(path, "grid");
   const bool force_cluster = path && !strcmp(path, "cluster");
   constexpr int64_t kGwAutoMaxT = 512;
-  if (!consistent && !fp16 && (force_grid || (!force_cluster && T <= kGwAutoMaxT))) {
+  const bool gw_ok = !consistent && !fp16;
+  if (gw_ok && force_grid) {
     mhc_status_t st = run_grid_wide(h, a, di, planes, s);
     if (st != MHC_ERR_NOT_SUITABLE) return st;
-    if (force_grid) return fail(MHC_ERR_PARAM_INVALID, "the grid-wide forward does not fit this shape");
+    return fail(MHC_ERR_PARAM_INVALID, "the grid-wide forward does not fit this shape");
   }
   // The 64-token-tile kernel, or the 128-token-tile kernel (n = 4) when
   // MHC_PRE_TILE=128 selects it.  At prefill the 64-token kernel at cluster 2
@@ -493,6 +496,13 @@ mhc_status_t mhc_pre_run(mhc_pre_t h, const mhc_pre_args* a, void* stream) {
     }
   }
   if (max_clusters <= 0) return fail(MHC_ERR_RUNTIME, "no cluster configuration fits this device");
+  if (gw_ok && !force_cluster && !t128 && T <= kGwAutoMaxT) {
+    const int rounds = (num_tiles + max_clusters - 1) / max_clusters;
+    if (num_tiles == 1 || rounds > 1) {
+      mhc_status_t st = run_grid_wide(h, a, di, planes, s);
+      if (st != MHC_ERR_NOT_SUITABLE) return st;
+    }
+  }
   L.cluster = cluster;
   L.grid = (num_tiles < max_clusters ? num_tiles : max_clusters) * cluster;
   L.x = a->x;
