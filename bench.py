@@ -69,6 +69,37 @@ def shard_tokens(T_per_rank: int, world: int, rank: int):
     return rank * T_per_rank, (rank + 1) * T_per_rank
 
 
+# Per-token fields of the input records (cut along their first dimension).
+TOKEN_FIELDS = ("x", "pre_mix", "residual", "post", "comb", "g_in", "g_post", "g_res", "g_x_post")
+
+
+def take_tokens(rec, lo: int, hi: int):
+    """Tokens [lo, hi) of an input record (a dataclass of tensors): its
+    per-token tensors cut, everything else (weights) kept."""
+    import dataclasses
+    changes = {}
+    for f in dataclasses.fields(rec):
+        v = getattr(rec, f.name)
+        if f.name == "T":
+            changes["T"] = hi - lo
+        elif f.name in TOKEN_FIELDS and v is not None:
+            changes[f.name] = v[lo:hi].clone()
+    return dataclasses.replace(rec, **changes)
+
+
+def rank_shard(make, T_per_rank: int, world: int, rank: int):
+    """This rank's part of one global batch: `make(T=world * T_per_rank,
+    seed=0)` draws the whole batch from one seed, and the rank keeps the
+    tokens shard_tokens gives it."""
+    full = make(T=world * T_per_rank, seed=0)
+    if world == 1:
+        return full
+    lo, hi = shard_tokens(T_per_rank, world, rank)
+    part = take_tokens(full, lo, hi)
+    del full
+    return part
+
+
 def max_over_ranks(value: float, world: int, device=None) -> float:
     if world == 1:
         return value
@@ -241,7 +272,7 @@ def bench_post(args, device, world, rank, local):
     T, n, D = args.tokens, WORKLOAD["n"], WORKLOAD["D"]
     cfg = {"workload": f"hc_post T={T} n={n} D={D} (b=4, s=8192)", "tokens_per_rank": T, "n": n, "D": D,
            "l2": "inputs exceed L2; no flush needed", "parallelism": f"token-sharded x{world} (no collective)"}
-    case = make_post_case(device=device, T=T, n=n, D=D, seed=rank)
+    case = rank_shard(lambda **k: make_post_case(device=device, n=n, D=D, **k), T, world, rank)
     if args.impl == "reference":
         if rank != 0:
             return 0
@@ -348,14 +379,15 @@ def bwd_main_token_bytes(n, D):
     return 2 * n * D + 2 * D + 2 * n * D
 
 
-def bwd_inputs(device, T, n, D, seed, mode):
+def bwd_inputs(device, T, n, D, world, rank, mode):
     """Forward inputs, the forward's saved intermediates (made by the library's
     own forward: these are benchmark inputs, not parity references) and
-    upstream gradients."""
+    upstream gradients, for this rank's shard of the global batch."""
     import torch
     from mhc_hyper_connection_gb300 import MhcPre
     from mhc_synth import make_bwd_grads, make_case
-    case = make_case("prefill", device=device, T=T, impl_mode=mode, seed=seed, need_backward=True)
+    case = rank_shard(lambda **k: make_case("prefill", device=device, impl_mode=mode, need_backward=True, **k),
+                      T, world, rank)
     fwd = MhcPre(n, D, alpha_len=3, num_iters=20, impl_mode=mode, need_backward=True)
     out = fwd.allocate(T, device)
     fwd.run(case.x, case.phi, case.alpha, case.bias, out)
@@ -363,7 +395,7 @@ def bwd_inputs(device, T, n, D, seed, mode):
     if fwd.status(out) != 0:
         raise RuntimeError("device-side error in the forward that makes the saved intermediates")
     saved = {k: out[k] for k in ("inv_rms", "h_mix", "h_pre", "h_post", "sum_out", "norm_out")}
-    g = make_bwd_grads(seed=seed, device=device, T=T, n=n, D=D)
+    g = rank_shard(lambda **k: make_bwd_grads(device=device, n=n, D=D, **k), T, world, rank)
     return case, saved, g
 
 
@@ -462,7 +494,7 @@ def bench_bwd(args, device, world, rank, local):
         return 0
     from mhc_hyper_connection_gb300 import build as mbuild
     mbuild.build()
-    case, saved, g = bwd_inputs(device, T, n, D, rank, args.mode)
+    case, saved, g = bwd_inputs(device, T, n, D, world, rank, args.mode)
     from mhc_hyper_connection_gb300 import MhcPre, mhc_pre_last_launch, mhc_pre_set_profile_events
     op = MhcPre(n, D, alpha_len=3, num_iters=20, impl_mode=args.mode, need_backward=True)
     grads = op.allocate_backward(T, device)
@@ -509,7 +541,7 @@ def bench_bwd(args, device, world, rank, local):
     cfg["launch"] = mhc_pre_last_launch(op.handle)[1]
     cfg["launch"]["kernel"] = "bw_main_kernel"
     elapsed = max_over_ranks(e0.elapsed_time(e1) / 1e3, world, device)
-    kern = sum(a.elapsed_time(b) for a, b in ev_k) / K / 1e3
+    kern = statistics.median(a.elapsed_time(b) for a, b in ev_k) / 1e3   # median launch
     per_step = elapsed / K
 
     # ---- end to end with host buffers: every step copies its inputs in from
@@ -676,7 +708,8 @@ def main():
     from mhc_hyper_connection_gb300 import build as mbuild, MHC_DTYPE_BF16, MHC_DTYPE_FP16
     mbuild.build()
     xdt = torch.float16 if args.x_dtype == "fp16" else torch.bfloat16
-    case = make_case("prefill", device=device, T=T, impl_mode=args.mode, seed=rank, x_dtype=xdt)
+    case = rank_shard(lambda **k: make_case("prefill", device=device, impl_mode=args.mode, x_dtype=xdt, **k),
+                      T, world, rank)
     op = MhcPre(n, D, alpha_len=3, num_iters=20, impl_mode=args.mode, batch_consistent=args.batch_consistent,
                 x_dtype=MHC_DTYPE_FP16 if args.x_dtype == "fp16" else MHC_DTYPE_BF16)
     out = op.allocate(T, device)
@@ -728,7 +761,7 @@ def main():
     cfg["launch"] = mhc_pre_last_launch(op.handle)[1]
     cfg["launch"]["kernel"] = mhc_pre_last_kernel(op.handle)
     elapsed = e0.elapsed_time(e1) / 1e3
-    kern = sum(a.elapsed_time(b) for a, b in ev_k) / K / 1e3
+    kern = statistics.median(a.elapsed_time(b) for a, b in ev_k) / 1e3   # median launch
     elapsed_max = max_over_ranks(elapsed, world, device)
     if args.route == "composite":
         # three launches and no single fused kernel: the roofline is the route's

@@ -69,10 +69,23 @@ typedef struct mhc_pre_s *mhc_pre_t;
 #define MHC_DTYPE_BF16 0
 #define MHC_DTYPE_FP16 1
 
+/* Which fused forward kernel runs (mhc_pre_config.kernel).  AUTO lets the
+ * library choose by shape; the others force one, for benchmarks and tests.
+ * Every kernel computes the same results within the stated tolerances. */
+#define MHC_KERNEL_AUTO    0
+#define MHC_KERNEL_CLUSTER 1   /* 64-token tiles shared by a thread-block cluster   */
+#define MHC_KERNEL_GRID    2   /* every SM on a few tiles (small T, bf16 x)         */
+
 /* Fixed per handle.  Defaults (mhc_pre_config_default): n = 4, D = 0 (must be
  * set), alpha_len = 3, num_iters = 20, norm_eps = hc_eps = 1e-6,
  * impl_mode = MHC_IMPL_FP32, need_backward = 0, batch_consistent = 0,
- * x_dtype = MHC_DTYPE_BF16.
+ * x_dtype = MHC_DTYPE_BF16, and every launch-choice field 0 (automatic).
+ *
+ * Launch choice (kernel .. gw_x_lead): 0 means "let the library choose";
+ * a non-zero value fixes one choice of kernel or launch shape, for
+ * benchmarks and tests.  None of them changes what is computed.  A forced
+ * choice that does not fit the shape or device makes mhc_pre_run return
+ * MHC_ERR_PARAM_INVALID.  The library reads no environment variable.
  *
  * batch_consistent (the Sinkhorn page's §8.1 "Batch 一致性", off by default
  * there too): every token's outputs are bitwise the same whatever T and
@@ -98,6 +111,15 @@ typedef struct {
                                so every |phi . gamma| must be <= 65504: a larger
                                one sets bit 3 of the device error word, which
                                mhc_pre_status reports                              */
+    int32_t kernel;         /* MHC_KERNEL_AUTO / _CLUSTER / _GRID (grid: bf16 x,
+                               not batch_consistent)                               */
+    int32_t cluster;        /* cluster kernel: CTAs per cluster, 1, 2, 4, 8 or 16   */
+    int32_t x_stages;       /* cluster kernel: deepest x ring tried, 2..8           */
+    int32_t w_stages;       /* cluster kernel: deepest phi-plane ring tried, 2..8   */
+    int32_t gw_groups;      /* grid-wide kernel: CTA groups, 1 or 2                 */
+    int32_t gw_x_stages;    /* grid-wide kernel: deepest x ring tried, 2..8         */
+    int32_t gw_x_lead;      /* grid-wide kernel: tiles its loads may run ahead of
+                               its own y, 1..15                                     */
 } mhc_pre_config;
 
 /* Per call.  R = n*n + 2n (alpha_len 3) or 2n (alpha_len 2); I = num_iters. */
@@ -148,8 +170,10 @@ MHC_API mhc_status_t mhc_pre_workspace_size(mhc_pre_t h, int64_t T, size_t *byte
 MHC_API mhc_status_t mhc_pre_run(mhc_pre_t h, const mhc_pre_args *args, void *stream);
 
 /* Synchronise `stream`, then report MHC_ERR_RUNTIME if a CUDA error is
- * pending or the last run's device error word (in `workspace`, which may be
- * NULL to skip that check) is set; else MHC_OK. */
+ * pending or the last run's device error word is set; else MHC_OK.  The
+ * word is read from `workspace` when it is given.  With workspace NULL it is
+ * read from the library's fixed scratch array if the handle's last run was
+ * mhc_pre_run_noalloc, and not read at all otherwise. */
 MHC_API mhc_status_t mhc_pre_status(mhc_pre_t h, const void *workspace, void *stream);
 
 /* Optional timing hooks.  When set, mhc_pre_run records `before` on its
@@ -160,6 +184,21 @@ MHC_API mhc_status_t mhc_pre_status(mhc_pre_t h, const void *workspace, void *st
  * runs on.  The events are borrowed, not owned.  MHC_ERR_NULLPTR if h is
  * NULL. */
 MHC_API mhc_status_t mhc_pre_set_profile_events(mhc_pre_t h, void *before, void *after);
+
+/* Device wait limit and a test of the give-up path.  Every wait inside the
+ * forward kernels is bounded: after wait_limit_us microseconds (0 restores
+ * the default, 2 s; at most 10 s) it gives up, sets the device error word and
+ * the kernel winds down, so that mhc_pre_status reports MHC_ERR_RUNTIME and
+ * the CUDA context stays usable (the status codes of the MhcPreSinkhorn page,
+ * §6).  withhold_last_x_copy = 1 makes the next runs on this handle leave out
+ * one copy of x -- the last one the first CTA would issue -- so that the
+ * waits on it give up: a host-requested test of that path which faults
+ * nothing (no copy is left in flight, every other wait still ends).  Those
+ * runs' outputs are then incomplete.  Set it back to 0 for normal runs.
+ * Applies to the fused forward kernels of mhc_pre_run and
+ * mhc_pre_run_noalloc.  MHC_ERR_NULLPTR if h is NULL; MHC_ERR_PARAM_INVALID
+ * for a value outside these ranges. */
+MHC_API mhc_status_t mhc_pre_set_wait_test(mhc_pre_t h, uint32_t wait_limit_us, int32_t withhold_last_x_copy);
 
 /* Launch shape chosen by the last successful mhc_pre_run on this handle:
  * CTAs per cluster (0 for the grid-wide kernel), grid size in CTAs, x-ring
@@ -196,7 +235,12 @@ MHC_API const char *mhc_pre_last_kernel(mhc_pre_t h);
  *    whose work overlaps on the GPU (different streams, no ordering between
  *    them) race on it: serialise them.
  *  - The device error word lives in that array; check a run with
- *    mhc_pre_status(h, NULL, stream), which reports CUDA errors only.
+ *    mhc_pre_status(h, NULL, stream), which reads it from there (a wait
+ *    that gave up, or an fp16 weight out of range, gives MHC_ERR_RUNTIME
+ *    as it does after mhc_pre_run).
+ *  - The array's address is cached per device together with the CUDA
+ *    context it was looked up in; if the context changes (for instance
+ *    after cudaDeviceReset) the next call looks it up again.
  * This entry point is a property of this library; the pages' operator has no
  * counterpart.  Other arguments and status codes as mhc_pre_run. */
 #define MHC_PRE_STATIC_SCRATCH_BYTES ((size_t)16 << 20)

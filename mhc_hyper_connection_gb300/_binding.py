@@ -20,6 +20,9 @@ MHC_IMPL_FP32 = 0
 MHC_IMPL_TF32 = 1
 MHC_DTYPE_BF16 = 0
 MHC_DTYPE_FP16 = 1
+MHC_KERNEL_AUTO = 0
+MHC_KERNEL_CLUSTER = 1
+MHC_KERNEL_GRID = 2
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_PKG, "libmhc_pre.so")
@@ -30,7 +33,13 @@ class MhcPreConfig(ctypes.Structure):
                 ("num_iters", ctypes.c_int32), ("norm_eps", ctypes.c_double),
                 ("hc_eps", ctypes.c_double), ("impl_mode", ctypes.c_int32),
                 ("need_backward", ctypes.c_int32), ("batch_consistent", ctypes.c_int32),
-                ("x_dtype", ctypes.c_int32)]
+                ("x_dtype", ctypes.c_int32), ("kernel", ctypes.c_int32), ("cluster", ctypes.c_int32),
+                ("x_stages", ctypes.c_int32), ("w_stages", ctypes.c_int32), ("gw_groups", ctypes.c_int32),
+                ("gw_x_stages", ctypes.c_int32), ("gw_x_lead", ctypes.c_int32)]
+
+# Launch-choice fields of MhcPreConfig (0 = automatic); MhcPre takes them as
+# keyword arguments.
+LAUNCH_FIELDS = ("kernel", "cluster", "x_stages", "w_stages", "gw_groups", "gw_x_stages", "gw_x_lead")
 
 
 _P = ctypes.c_void_p
@@ -84,6 +93,8 @@ def library() -> ctypes.CDLL:
             lib.mhc_pre_run_noalloc.restype = ctypes.c_int32
             lib.mhc_pre_status.argtypes = [_P, _P, _P]
             lib.mhc_pre_status.restype = ctypes.c_int32
+            lib.mhc_pre_set_wait_test.argtypes = [_P, ctypes.c_uint32, ctypes.c_int32]
+            lib.mhc_pre_set_wait_test.restype = ctypes.c_int32
             lib.mhc_pre_set_profile_events.argtypes = [_P, _P, _P]
             lib.mhc_pre_set_profile_events.restype = ctypes.c_int32
             I32P = ctypes.POINTER(ctypes.c_int32)
@@ -145,6 +156,10 @@ def mhc_pre_run_noalloc(handle, args: MhcPreArgs, stream: int = 0) -> int:
 
 def mhc_pre_status(handle, workspace: int = 0, stream: int = 0) -> int:
     return library().mhc_pre_status(handle, _P(workspace or None), _P(stream or None))
+
+
+def mhc_pre_set_wait_test(handle, wait_limit_us: int = 0, withhold_last_x_copy: int = 0) -> int:
+    return library().mhc_pre_set_wait_test(handle, int(wait_limit_us), int(withhold_last_x_copy))
 
 
 def mhc_pre_set_profile_events(handle, before: int = 0, after: int = 0) -> int:
@@ -249,17 +264,25 @@ def _tokens(lead) -> int:
 
 
 class MhcPre:
-    """One configured forward (n, D, alpha_len, num_iters, eps, mode, backward)."""
+    """One configured forward (n, D, alpha_len, num_iters, eps, mode, backward).
+
+    Launch-choice keywords (kernel, cluster, x_stages, w_stages, gw_groups,
+    gw_x_stages, gw_x_lead; 0 = automatic) go to the matching
+    mhc_pre_config fields."""
 
     def __init__(self, n: int, D: int, *, alpha_len: int = 3, num_iters: int = 20,
                  norm_eps: float = 1e-6, hc_eps: float = 1e-6, impl_mode: int = MHC_IMPL_FP32,
                  need_backward: bool = False, batch_consistent: bool = False,
-                 x_dtype: int = MHC_DTYPE_BF16):
+                 x_dtype: int = MHC_DTYPE_BF16, **launch):
         cfg = mhc_pre_config_default()
         cfg.n, cfg.D, cfg.alpha_len, cfg.num_iters = n, D, alpha_len, num_iters
         cfg.norm_eps, cfg.hc_eps = norm_eps, hc_eps
         cfg.impl_mode, cfg.need_backward = impl_mode, int(bool(need_backward))
         cfg.batch_consistent, cfg.x_dtype = int(bool(batch_consistent)), int(x_dtype)
+        for k, v in launch.items():
+            if k not in LAUNCH_FIELDS:
+                raise TypeError(f"MhcPre() got an unexpected keyword argument {k!r}")
+            setattr(cfg, k, int(v))
         st, h = mhc_pre_create(cfg)
         if st != MHC_OK:
             raise MhcError(st, "mhc_pre_create", last_error())

@@ -267,7 +267,7 @@ struct PlaneParams {
 cudaError_t launch_prepare_planes(const PlaneParams& pp, cudaStream_t s);
 
 constexpr int kMmaM = 128;         // rows of one tcgen05.mma (TMEM lanes)
-constexpr int kTileT = 64;         // tokens per tile: MMA rows 0..63 (rows 64..127 unused)
+constexpr int kTileT = 64;         // tokens per tile: MMA rows 0..63 (rows 64..127: a stream pair's second stream)
 constexpr int kChunkK = 64;        // bf16 elements per 128-byte swizzle row
 constexpr int kStreamTile = kTileT * 128;   // one stream of one d-chunk of a tile (8 KB)
 constexpr int kThreads = 512;      // 16 warps: 2 TMA producers, MMA, 2 publish, gates, Sinkhorn, 8 y
@@ -324,10 +324,21 @@ __host__ __device__ inline SmemLayout smem_layout(int n, int R, int P, int xs, i
   return L;
 }
 
+// Wait limit and test hook shared by the forward kernels: wait_ns bounds
+// every wait; withhold_x = 1 makes CTA 0's x producer leave out its last
+// copy (it issues nothing for it), so the waits on it give up and the run
+// ends through the abort path with the error word set -- a host-requested
+// test of that path that faults nothing.
+struct WaitTest {
+  uint64_t wait_ns;
+  int withhold_x;
+};
+
 struct Geometry {
   int T, D, n;
   int num_tiles, nd;           // token tiles; 64-wide d-chunks per stream
   int cluster, xstages, wstages;
+  WaitTest wt;
 };
 
 struct TcLaunch {
@@ -342,29 +353,8 @@ struct TcLaunch {
   int xstages, wstages;
   size_t smem_bytes;
   uint32_t* err_word;
+  WaitTest wt;
 };
-
-// ---------------------------------------------------------------------------
-// 128-token-tile cluster kernel (n = 4): x boxes (64 columns, 128 tokens, 2
-// streams) = 32 KB, the sum of squares on CUDA cores.
-// ---------------------------------------------------------------------------
-constexpr int kT128Tile = 128;
-__host__ __device__ inline SmemLayout t128_layout(int R, int P, int xs, int ws) {
-  SmemLayout L;
-  size_t o = 0;
-  L.x = o;    o += (size_t)xs * 2 * kT128Tile * 128;
-  L.w = o;    o += (size_t)ws * w_group(4, R, P) * plane_box_rows(R, P) * 128;
-  o += 1024;  // the B operand of N = NP rows reads up to 8 rows past the last w box
-  L.part = o; o += 2 * (size_t)kT128Tile * partial_stride(R) * 4;   // received partials + owned sums
-  L.coef = o; o += (size_t)kCoefBufs * kT128Tile * 4 * 4;
-  o = (o + 15) & ~size_t(15);
-  L.tail = o; o += kTailBytes;
-  L.total = o + 1024;
-  return L;
-}
-bool t128_supported(int n, int R, int P);
-cudaError_t t128_forward_occupancy(int n, int R, int P, size_t smem_bytes, int cluster, int* max_clusters);
-cudaError_t launch_t128_forward(const TcLaunch& L, cudaStream_t s);
 
 // ---------------------------------------------------------------------------
 // Post-mapping (hc_post): out[t][j] = post[t][j] x[t] + sum_i comb[t][i][j] residual[t][i].
@@ -461,6 +451,7 @@ struct GwGeom {
   int own_max;     // most tokens of one tile any CTA gates
   int sink_batch;  // tiles per Sinkhorn batch (sink_batch * own_max <= kGwSinkMax)
   int xlead;       // most tiles the x loads run ahead of this CTA's y (1..15)
+  WaitTest wt;
 };
 
 struct GwLaunch {

@@ -25,6 +25,8 @@ struct mhc_pre_s {
   cudaEvent_t ev_before = nullptr, ev_after = nullptr;   // optional timing hooks
   int last_cluster = 0, last_grid = 0, last_stages = 0, last_ystages = 0;   // last launch shape
   const char* last_kernel = "";                                              // and its kernel
+  void* last_noalloc_word = nullptr;   // error word of the last run when it was mhc_pre_run_noalloc
+  mhc::WaitTest wait_test{2000000000ull, 0};   // device wait limit and test hook (mhc_pre_set_wait_test)
 };
 
 namespace {
@@ -43,6 +45,23 @@ typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t,
                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*,
                                   CUtensorMapInterleave, CUtensorMapSwizzle, CUtensorMapL2promotion,
                                   CUtensorMapFloatOOBfill);
+
+typedef CUresult (*CtxGetCurrentFn)(CUcontext*);
+
+// cuCtxGetCurrent through the runtime's driver entry-point lookup (the
+// library does not link the driver library directly).
+CtxGetCurrentFn ctx_get_current_fn() {
+  static CtxGetCurrentFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<CtxGetCurrentFn>(p);
+  });
+  return fn;
+}
 
 EncodeTiledFn encode_fn() {
   static EncodeTiledFn fn = nullptr;
@@ -131,12 +150,6 @@ size_t gw_rings_bytes(const mhc_pre_s* h) {
   return mhc::gw_ring_bytes((int)h->cfg.n, h->R, kGwMaxGrid);
 }
 
-int env_int(const char* name, int dflt) {
-  const char* v = getenv(name);
-  if (!v || !*v) return dflt;
-  return atoi(v);
-}
-
 // Returned by run_grid_wide when the shape or device does not suit it.
 constexpr mhc_status_t MHC_ERR_NOT_SUITABLE = -1;
 
@@ -170,14 +183,14 @@ mhc::EpiParams epi_params(const mhc_pre_s* h, const mhc_pre_args* a) {
 // a group owning a run of the d-chunks of stream r / gs; MHC_ERR_NOT_SUITABLE
 // when its resident phi blocks and a two-slot x ring do not fit, or the grid
 // cannot be resident at once.  Two groups when there are enough tiles to keep
-// both busy (MHC_PRE_GW_GROUPS overrides).
+// both busy (the handle's gw_groups overrides).
 mhc_status_t run_grid_wide(mhc_pre_s* h, const mhc_pre_args* a, const DeviceInfo& di,
                            __nv_bfloat16* planes, cudaStream_t s) {
   const int n = (int)h->cfg.n, D = (int)h->cfg.D, R = h->R;
   const int nch = (D + mhc::kChunkK - 1) / mhc::kChunkK;
   const int num_tiles = (int)((a->T + mhc::kGwTile - 1) / mhc::kGwTile);
   const int sms = di.sms < kGwMaxGrid ? di.sms : kGwMaxGrid;
-  int ng = env_int("MHC_PRE_GW_GROUPS", num_tiles >= 8 ? 2 : 1);
+  int ng = h->cfg.gw_groups ? h->cfg.gw_groups : (num_tiles >= 8 ? 2 : 1);
   ng = ng < 1 ? 1 : (ng > mhc::kGwMaxGroups ? mhc::kGwMaxGroups : ng);
   int gs = sms / ng / n;
   if (gs > nch) gs = nch;
@@ -189,7 +202,7 @@ mhc_status_t run_grid_wide(mhc_pre_s* h, const mhc_pre_args* a, const DeviceInfo
   if (umax > 32 || own_max > mhc::kGwSinkMax) return MHC_ERR_NOT_SUITABLE;
   int sink_batch = mhc::kGwSinkMax / own_max;
   if (sink_batch > 8) sink_batch = 8;
-  int xmax = env_int("MHC_PRE_GW_XSTAGES", mhc::kMaxStages);
+  int xmax = h->cfg.gw_x_stages ? h->cfg.gw_x_stages : mhc::kMaxStages;
   xmax = xmax < 2 ? 2 : (xmax > mhc::kMaxStages ? mhc::kMaxStages : xmax);
   int xs = 0;
   for (int c = xmax; c >= 2 && !xs; --c)
@@ -221,8 +234,9 @@ mhc_status_t run_grid_wide(mhc_pre_s* h, const mhc_pre_args* a, const DeviceInfo
   L.g.xstages = xs;
   L.g.own_max = own_max;
   L.g.sink_batch = sink_batch;
-  int xlead = env_int("MHC_PRE_GW_XLEAD", 6);
+  int xlead = h->cfg.gw_x_lead ? h->cfg.gw_x_lead : 6;
   L.g.xlead = xlead < 1 ? 1 : (xlead > 15 ? 15 : xlead);
+  L.g.wt = h->wait_test;
   L.smem_bytes = smem;
   uint8_t* ws = static_cast<uint8_t*>(a->workspace);
   L.hdr = reinterpret_cast<uint32_t*>(ws);
@@ -278,6 +292,13 @@ void mhc_pre_config_default(mhc_pre_config* c) {
   c->need_backward = 0;
   c->batch_consistent = 0;
   c->x_dtype = MHC_DTYPE_BF16;
+  c->kernel = MHC_KERNEL_AUTO;
+  c->cluster = 0;
+  c->x_stages = 0;
+  c->w_stages = 0;
+  c->gw_groups = 0;
+  c->gw_x_stages = 0;
+  c->gw_x_lead = 0;
 }
 
 const char* mhc_pre_last_error(void) { return g_last_error; }
@@ -312,6 +333,19 @@ mhc_status_t mhc_pre_create(mhc_pre_t* out, const mhc_pre_config* cfg) {
   if (c.x_dtype == MHC_DTYPE_FP16 && c.n != 4)
     return fail(MHC_ERR_PARAM_INVALID, "fp16 x is supported for n = 4");
   if (!(c.norm_eps >= 0.0) || !(c.hc_eps >= 0.0)) return fail(MHC_ERR_PARAM_INVALID, "eps values must be >= 0");
+  if (c.kernel != MHC_KERNEL_AUTO && c.kernel != MHC_KERNEL_CLUSTER && c.kernel != MHC_KERNEL_GRID)
+    return fail(MHC_ERR_PARAM_INVALID, "kernel must be MHC_KERNEL_AUTO, _CLUSTER or _GRID");
+  if (c.cluster != 0 && c.cluster != 1 && c.cluster != 2 && c.cluster != 4 && c.cluster != 8 && c.cluster != 16)
+    return fail(MHC_ERR_PARAM_INVALID, "cluster must be 0 (automatic), 1, 2, 4, 8 or 16");
+  if ((c.x_stages != 0 && (c.x_stages < 2 || c.x_stages > mhc::kMaxStages)) ||
+      (c.w_stages != 0 && (c.w_stages < 2 || c.w_stages > mhc::kMaxStages)) ||
+      (c.gw_x_stages != 0 && (c.gw_x_stages < 2 || c.gw_x_stages > mhc::kMaxStages)))
+    return fail(MHC_ERR_PARAM_INVALID, "ring depths must be 0 (automatic) or 2..%d", mhc::kMaxStages);
+  if (c.gw_groups < 0 || c.gw_groups > mhc::kGwMaxGroups)
+    return fail(MHC_ERR_PARAM_INVALID, "gw_groups must be 0 (automatic), 1 or %d", mhc::kGwMaxGroups);
+  if (c.gw_x_lead < 0 || c.gw_x_lead > 15) return fail(MHC_ERR_PARAM_INVALID, "gw_x_lead must be 0..15");
+  if (c.batch_consistent && c.cluster != 0)
+    return fail(MHC_ERR_PARAM_INVALID, "batch_consistent fixes the cluster size; leave cluster 0");
   mhc_pre_s* h = new (std::nothrow) mhc_pre_s;
   if (!h) return fail(MHC_ERR_RUNTIME, "out of host memory");
   h->cfg = c;
@@ -333,6 +367,7 @@ mhc_status_t mhc_pre_workspace_size(mhc_pre_t h, int64_t T, size_t* bytes) {
 mhc_status_t mhc_pre_run(mhc_pre_t h, const mhc_pre_args* a, void* stream) {
   g_last_error[0] = 0;
   if (!h || !a) return fail(MHC_ERR_NULLPTR, "handle and args must be non-NULL");
+  h->last_noalloc_word = nullptr;
   const mhc_pre_config& c = h->cfg;
   const int64_t T = a->T;
   if (T < 0 || T > (int64_t(1) << 30)) return fail(MHC_ERR_PARAM_INVALID, "T must be in [0, 2^30]");
@@ -398,29 +433,23 @@ mhc_status_t mhc_pre_run(mhc_pre_t h, const mhc_pre_args* a, void* stream) {
   //    would have a single tile or need more than one round of clusters, the
   //    cases where it is faster (D = 7168, kernel time: T = 64 22.8 against
   //    26.7 us, T = 512 36.2 against 39.9 us; but T = 256 35.0 against 26.7,
-  //    and T = 768 43.3 against 40.3).  MHC_PRE_PATH=grid or =cluster forces
+  //    and T = 768 43.3 against 40.3).  The handle's `kernel` field forces
   //    one (tests and tuning runs).  fp16 x and batch-consistent mode always
   //    run the cluster kernel.
   const bool fp16 = c.x_dtype == MHC_DTYPE_FP16;
   const bool consistent = c.batch_consistent != 0;
-  const char* path = getenv("MHC_PRE_PATH");
-  const bool force_grid = path && !strcmp(path, "grid");
-  const bool force_cluster = path && !strcmp(path, "cluster");
+  const bool force_grid = c.kernel == MHC_KERNEL_GRID;
+  const bool force_cluster = c.kernel == MHC_KERNEL_CLUSTER;
   constexpr int64_t kGwAutoMaxT = 512;
   const bool gw_ok = !consistent && !fp16;
-  if (gw_ok && force_grid) {
+  if (force_grid) {
+    if (!gw_ok) return fail(MHC_ERR_PARAM_INVALID, "the grid-wide forward takes bf16 x outside batch-consistent mode");
     mhc_status_t st = run_grid_wide(h, a, di, planes, s);
     if (st != MHC_ERR_NOT_SUITABLE) return st;
     return fail(MHC_ERR_PARAM_INVALID, "the grid-wide forward does not fit this shape");
   }
-  // The 64-token-tile kernel, or the 128-token-tile kernel (n = 4) when
-  // MHC_PRE_TILE=128 selects it.  At prefill the 64-token kernel at cluster 2
-  // measured 0.688 ms against 0.702 ms for the best 128-token configuration.
-  const bool t128 = !consistent && !fp16 && mhc::t128_supported(n, R, h->P) && env_int("MHC_PRE_TILE", 64) == 128;
-  const int tile_t = t128 ? mhc::kT128Tile : mhc::kTileT;
-  auto layout = [&](int xsn, int wsn) {
-    return t128 ? mhc::t128_layout(R, h->P, xsn, wsn) : mhc::smem_layout(n, R, h->P, xsn, wsn);
-  };
+  const int tile_t = mhc::kTileT;
+  auto layout = [&](int xsn, int wsn) { return mhc::smem_layout(n, R, h->P, xsn, wsn); };
   mhc::TcLaunch L;
   memset(&L, 0, sizeof L);
   L.epi = epi_params(h, a);
@@ -429,13 +458,14 @@ mhc_status_t mhc_pre_run(mhc_pre_t h, const mhc_pre_args* a, void* stream) {
   L.fp16 = fp16 ? 1 : 0;
   L.err_word = err;
   L.planes = planes;
+  L.wt = h->wait_test;
   {
     // x [T][n][D] seen as (D, T, n), box (64, tile tokens, stream group); the
     // plane blocks are read with bulk copies.
     const uint64_t K2 = (uint64_t)n * D * 2;
     const uint64_t xd[3] = {(uint64_t)D, (uint64_t)T, (uint64_t)n};
     const uint64_t xs[2] = {K2, (uint64_t)D * 2};
-    const uint32_t xb[3] = {(uint32_t)mhc::kChunkK, (uint32_t)tile_t, (uint32_t)(t128 ? 2 : mhc::stream_group(n))};
+    const uint32_t xb[3] = {(uint32_t)mhc::kChunkK, (uint32_t)tile_t, (uint32_t)mhc::stream_group(n)};
     if (!encode_3d(&L.tmap_x, a->x, xd, xs, xb))
       return fail(MHC_ERR_RUNTIME, "tensor map encoding failed");
   }
@@ -448,7 +478,7 @@ mhc_status_t mhc_pre_run(mhc_pre_t h, const mhc_pre_args* a, void* stream) {
   const int nd = (D + mhc::kChunkK - 1) / mhc::kChunkK;
   const int num_tiles = (int)((T + tile_t - 1) / tile_t);
   const size_t budget = di.max_smem;
-  int xmax = env_int("MHC_PRE_XSTAGES", 6), wmax = env_int("MHC_PRE_WSTAGES", 3);
+  int xmax = c.x_stages ? c.x_stages : 6, wmax = c.w_stages ? c.w_stages : 3;
   xmax = xmax < 2 ? 2 : (xmax > mhc::kMaxStages ? mhc::kMaxStages : xmax);
   wmax = wmax < 2 ? 2 : (wmax > mhc::kMaxStages ? mhc::kMaxStages : wmax);
   int xst = 0, wst = 0;
@@ -472,18 +502,18 @@ mhc_status_t mhc_pre_run(mhc_pre_t h, const mhc_pre_args* a, void* stream) {
   // Cluster size: the one that keeps the most SMs busy on this many tiles.
   // Ties go to the larger cluster: each member then reduces and gates fewer
   // rows of a tile, which shortens the per-tile critical path.
-  // MHC_PRE_CLUSTER=c forces cluster size c (for tuning runs).
+  // The handle's `cluster` field forces a size (for tuning runs).
   // Batch-consistent mode pins cluster 2 (1 when there is a single d-chunk):
   // a token's reduction is then split the same way whatever T is.
-  const int forced = consistent ? (nd >= 2 ? 2 : 1) : env_int("MHC_PRE_CLUSTER", 0);
+  const int forced = consistent ? (nd >= 2 ? 2 : 1) : (int)c.cluster;
+  if (forced > nd) return fail(MHC_ERR_PARAM_INVALID, "cluster %d exceeds the %d d-chunks of a stream", forced, nd);
   int cluster = 0;
   int max_clusters = 0;
   long long best_sms = -1;
   for (int cand : {1, 2, 4, 8, 16}) {
     if ((forced && cand != forced) || cand > nd) continue;
     int mc = 0;
-    const cudaError_t oe = t128 ? mhc::t128_forward_occupancy(n, R, h->P, smem, cand, &mc)
-                                : mhc::tc_forward_occupancy(n, R, h->P, fp16, smem, cand, &mc);
+    const cudaError_t oe = mhc::tc_forward_occupancy(n, R, h->P, fp16, smem, cand, &mc);
     if (oe != cudaSuccess || mc <= 0) {
       cudaGetLastError();
       continue;
@@ -495,8 +525,9 @@ mhc_status_t mhc_pre_run(mhc_pre_t h, const mhc_pre_args* a, void* stream) {
       max_clusters = mc;
     }
   }
-  if (max_clusters <= 0) return fail(MHC_ERR_RUNTIME, "no cluster configuration fits this device");
-  if (gw_ok && !force_cluster && !t128 && T <= kGwAutoMaxT) {
+  if (max_clusters <= 0)
+    return fail(forced ? MHC_ERR_PARAM_INVALID : MHC_ERR_RUNTIME, "no cluster configuration fits this device");
+  if (gw_ok && !force_cluster && !forced && T <= kGwAutoMaxT) {
     const int rounds = (num_tiles + max_clusters - 1) / max_clusters;
     if (num_tiles == 1 || rounds > 1) {
       mhc_status_t st = run_grid_wide(h, a, di, planes, s);
@@ -513,10 +544,10 @@ mhc_status_t mhc_pre_run(mhc_pre_t h, const mhc_pre_args* a, void* stream) {
   h->last_grid = L.grid;
   h->last_stages = xst;
   h->last_ystages = wst;
-  h->last_kernel = t128 ? "mhc_pre_t128_kernel" : "mhc_pre_tc_kernel";
+  h->last_kernel = "mhc_pre_tc_kernel";
   if (h->ev_before && cudaEventRecord(h->ev_before, s) != cudaSuccess)
     return fail(MHC_ERR_RUNTIME, "recording the timing event failed");
-  if ((t128 ? mhc::launch_t128_forward(L, s) : mhc::launch_tc_forward(L, s)) != cudaSuccess)
+  if (mhc::launch_tc_forward(L, s) != cudaSuccess)
     return fail(MHC_ERR_RUNTIME, "forward launch failed: %s", cudaGetErrorString(cudaGetLastError()));
   if (h->ev_after && cudaEventRecord(h->ev_after, s) != cudaSuccess)
     return fail(MHC_ERR_RUNTIME, "recording the timing event failed");
@@ -529,9 +560,12 @@ mhc_status_t mhc_pre_status(mhc_pre_t h, const void* workspace, void* stream) {
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   cudaError_t e = cudaStreamSynchronize(s);
   if (e != cudaSuccess) return fail(MHC_ERR_RUNTIME, "stream error: %s", cudaGetErrorString(e));
-  if (workspace) {
+  // the error word: in the caller's workspace, or, after a no-alloc run, in
+  // the library's fixed scratch array
+  const void* word_at = workspace ? workspace : h->last_noalloc_word;
+  if (word_at) {
     uint32_t word = 0;
-    e = cudaMemcpy(&word, workspace, sizeof word, cudaMemcpyDeviceToHost);
+    e = cudaMemcpy(&word, word_at, sizeof word, cudaMemcpyDeviceToHost);
     if (e != cudaSuccess) return fail(MHC_ERR_RUNTIME, "reading the error word: %s", cudaGetErrorString(e));
     if (word & mhc::kErrPlaneRange)
       return fail(MHC_ERR_RUNTIME, "phi . gamma has an entry outside the fp16 range (error word 0x%x)", word);
@@ -548,24 +582,36 @@ mhc_status_t mhc_pre_status(mhc_pre_t h, const void* workspace, void* stream) {
 static __device__ __align__(256) unsigned char g_noalloc_scratch[MHC_PRE_STATIC_SCRATCH_BYTES];
 
 namespace {
-// Device address of g_noalloc_scratch, looked up once per device with that
-// device current (host code cannot use the symbol itself as a pointer).
+// Device address of g_noalloc_scratch, looked up with the device current
+// (host code cannot use the symbol itself as a pointer) and cached per device
+// together with the context it belongs to: a new context on that device (a
+// cudaDeviceReset in between) makes the next call look it up again.
 void* noalloc_scratch(int dev, cudaError_t* err) {
   static std::mutex mu;
   static void* addr[64] = {};
+  static CUcontext ctx_of[64] = {};
   std::lock_guard<std::mutex> lk(mu);
   *err = cudaSuccess;
   if (dev < 0 || dev >= 64) {
     *err = cudaErrorInvalidDevice;
     return nullptr;
   }
-  if (!addr[dev]) {
-    void* p = nullptr;
-    *err = cudaGetSymbolAddress(&p, g_noalloc_scratch);
-    if (*err != cudaSuccess) return nullptr;
-    addr[dev] = p;
+  const CtxGetCurrentFn ctx_current = ctx_get_current_fn();
+  CUcontext ctx = nullptr;
+  if (addr[dev] && ctx_current && ctx_current(&ctx) == CUDA_SUCCESS && ctx && ctx == ctx_of[dev]) return addr[dev];
+  // first call on this device, or a different context: the lookup binds the
+  // device's primary context, which is then the current one
+  void* p = nullptr;
+  *err = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+  if (*err != cudaSuccess) return nullptr;
+  ctx = nullptr;
+  if (!ctx_current || ctx_current(&ctx) != CUDA_SUCCESS || !ctx) {
+    *err = cudaErrorDeviceUninitialized;
+    return nullptr;
   }
-  return addr[dev];
+  addr[dev] = p;
+  ctx_of[dev] = ctx;
+  return p;
 }
 }  // namespace
 
@@ -593,7 +639,20 @@ mhc_status_t mhc_pre_run_noalloc(mhc_pre_t h, const mhc_pre_args* a, void* strea
   mhc_pre_args b = *a;
   b.workspace = scratch;
   b.workspace_bytes = MHC_PRE_STATIC_SCRATCH_BYTES;
-  return mhc_pre_run(h, &b, stream);
+  const mhc_status_t rs = mhc_pre_run(h, &b, stream);
+  if (rs == MHC_OK) h->last_noalloc_word = scratch;   // mhc_pre_status(h, NULL, s) reads it there
+  return rs;
+}
+
+mhc_status_t mhc_pre_set_wait_test(mhc_pre_t h, uint32_t wait_limit_us, int32_t withhold_last_x_copy) {
+  g_last_error[0] = 0;
+  if (!h) return fail(MHC_ERR_NULLPTR, "handle must be non-NULL");
+  if (withhold_last_x_copy != 0 && withhold_last_x_copy != 1)
+    return fail(MHC_ERR_PARAM_INVALID, "withhold_last_x_copy must be 0 or 1");
+  if (wait_limit_us > 10000000u) return fail(MHC_ERR_PARAM_INVALID, "wait_limit_us must be at most 10 s");
+  h->wait_test.wait_ns = wait_limit_us ? (uint64_t)wait_limit_us * 1000ull : 2000000000ull;
+  h->wait_test.withhold_x = withhold_last_x_copy;
+  return MHC_OK;
 }
 
 mhc_status_t mhc_pre_set_profile_events(mhc_pre_t h, void* before, void* after) {

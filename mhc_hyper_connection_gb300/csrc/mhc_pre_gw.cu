@@ -87,6 +87,7 @@ struct GwCtl {
   volatile uint32_t* abort;    // shared: this CTA is winding down
   volatile uint32_t* gabort;   // global: some CTA gave up
   uint32_t* err;               // global error word
+  uint64_t wait_ns;            // how long one wait may take before it gives up
 };
 
 __device__ __noinline__ void gw_fail(const GwCtl& c, uint32_t code) {
@@ -95,8 +96,8 @@ __device__ __noinline__ void gw_fail(const GwCtl& c, uint32_t code) {
   atomicExch(const_cast<uint32_t*>(c.gabort), 1u);
 }
 
-// Wait for phase `parity` of a local mbarrier; gives up after kWaitNs or as
-// soon as this CTA or any other has given up.
+// Wait for phase `parity` of a local mbarrier; gives up after c.wait_ns or
+// as soon as this CTA or any other has given up.
 __device__ __noinline__ bool gw_wait(uint64_t* bar, uint32_t parity, const GwCtl& c) {
   if (mbar_test(bar, parity)) return true;
   const uint64_t t0 = now_ns();
@@ -107,7 +108,7 @@ __device__ __noinline__ bool gw_wait(uint64_t* bar, uint32_t parity, const GwCtl
         *c.abort = 1u;
         return false;
       }
-      if (now_ns() - t0 > kWaitNs) {
+      if (now_ns() - t0 > c.wait_ns) {
         gw_fail(c, kErrWaitTimeout);
         return false;
       }
@@ -146,7 +147,7 @@ __device__ __noinline__ bool gw_wait_count(const uint32_t* ctr, uint32_t target,
         *c.abort = 1u;
         return false;
       }
-      if (now_ns() - t0 > kWaitNs) {
+      if (now_ns() - t0 > c.wait_ns) {
         gw_fail(c, kErrGridWait);
         return false;
       }
@@ -205,7 +206,7 @@ __global__ void __launch_bounds__(kGwThreads, 1)
   uint32_t* ydone = hdr + kHdrYdone + grp * kGwSlots;
   float* gpart = partials + (size_t)grp * kGwSlots * kGwTile * G * C::kStr;
   float* gcoef = coefs + (size_t)grp * kGwSlots * kGwTile * NS;
-  GwCtl ctl{&tail->abort, hdr + kHdrAbort, hdr};
+  GwCtl ctl{&tail->abort, hdr + kHdrAbort, hdr, g.wt.wait_ns};
 
   // ---- set-up
   if (threadIdx.x == 0) {
@@ -272,6 +273,7 @@ __global__ void __launch_bounds__(kGwThreads, 1)
       // within what L2 keeps.
       if (m >= g.xlead && !warp_wait(&tail->y_done[(m - g.xlead) & 15], (uint32_t)((m - g.xlead) >> 4) & 1u, ctl))
         break;
+      if (g.wt.withhold_x && blockIdx.x == 0 && m == my_tiles - 1) break;   // test hook (see WaitTest)
       if (lane == 0) mbar_expect_tx(&tail->x_full[xs], xbytes);
       __syncwarp();
       if (lane < nbox) {

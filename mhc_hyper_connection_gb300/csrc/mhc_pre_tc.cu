@@ -131,7 +131,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int c0 = (int)((long long)rank * g.nd / CL);
   const int c1 = (int)((long long)(rank + 1) * g.nd / CL);
   const int rpo = kTileT / CL;                    // tile rows each member reduces (owns)
-  Ctl ctl{&tail->abort, err};
+  Ctl ctl{&tail->abort, err, g.wt.wait_ns};
 
   // ---- set-up
   if (threadIdx.x == 0) {
@@ -179,10 +179,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t xph = 0;
       long long iss = 0;
       bool ok = true;
+      // test hook: CTA 0 leaves out its last box (see WaitTest)
+      const int last_tile = cluster_id + ((g.num_tiles - 1 - cluster_id) / num_clusters) * num_clusters;
       for (int tile = cluster_id; tile < g.num_tiles && ok; tile += num_clusters) {
         for (int j = c0; j < c1 && ok; ++j) {
           for (int grp = 0; grp < C::kGroups; ++grp) {
             if (!wait_bar<false>(&tail->x_empty[xs], xph ^ 1u, ctl, kErrWaitTimeout)) { ok = false; break; }
+            if (g.wt.withhold_x && blockIdx.x == 0 && tile == last_tile && j == c1 - 1 && grp == C::kGroups - 1)
+              break;
             mbar_expect_tx(&tail->x_full[xs], (uint32_t)C::kXBytes);
             tma_load_3d_hint(sX + (size_t)xs * C::kXBytes, &tmap_x, &tail->x_full[xs], j * kChunkK,
                              tile * kTileT, grp * C::kSG, keep);
@@ -616,6 +620,7 @@ cudaError_t launch_tc_forward(const TcLaunch& L, cudaStream_t s) {
   g.n = n;
   g.xstages = L.xstages;
   g.wstages = L.wstages;
+  g.wt = L.wt;
   cudaLaunchAttribute attr[1];
   cudaLaunchConfig_t cfg = cluster_config(L.cluster, L.grid, L.smem_bytes, s, attr);
   const __nv_bfloat16* xg = static_cast<const __nv_bfloat16*>(L.x);

@@ -7,7 +7,7 @@
 
 namespace mhc {
 
-constexpr uint64_t kWaitNs = 2000000000ull;   // 2 s per wait before giving up
+constexpr uint64_t kWaitNs = 2000000000ull;   // default: 2 s per wait before giving up
 
 // ----------------------------------------------------------------- PTX glue
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
@@ -63,10 +63,11 @@ __device__ __forceinline__ bool mbar_test_cluster(uint64_t* bar, uint32_t parity
 struct Ctl {
   volatile uint32_t* abort;   // shared: set once any wait in this CTA gave up
   uint32_t* err;              // global error word
+  uint64_t wait_ns = kWaitNs; // how long one wait may take before it gives up
 };
 
 // Wait for phase `parity` of `bar`.  Returns false (and raises the abort flag
-// and error word) after kWaitNs, or as soon as another role has aborted.
+// and error word) after c.wait_ns, or as soon as another role has aborted.
 template <bool kCluster>
 __device__ __noinline__ bool wait_bar(uint64_t* bar, uint32_t parity, const Ctl& c, uint32_t code) {
   if (kCluster ? mbar_test_cluster(bar, parity) : mbar_test(bar, parity)) return true;
@@ -75,7 +76,7 @@ __device__ __noinline__ bool wait_bar(uint64_t* bar, uint32_t parity, const Ctl&
     if (kCluster ? mbar_test_cluster(bar, parity) : mbar_test(bar, parity)) return true;
     if ((it & 63u) == 0) {
       if (*c.abort) return false;
-      if (now_ns() - t0 > kWaitNs) {
+      if (now_ns() - t0 > c.wait_ns) {
         atomicOr(c.err, code);
         *c.abort = 1u;
         return false;
@@ -107,7 +108,7 @@ static __device__ __noinline__ bool wait_bar_sleep(uint64_t* bar, uint32_t parit
     if (mbar_test_sleep(bar, parity, 20000u)) return true;
     if ((it & 7u) == 0) {
       if (*c.abort) return false;
-      if (now_ns() - t0 > kWaitNs) {
+      if (now_ns() - t0 > c.wait_ns) {
         atomicOr(c.err, code);
         *c.abort = 1u;
         return false;

@@ -24,6 +24,12 @@
  *        simulation: clear the low 13 mantissa bits of each fp32 matmul
  *        operand, round toward zero, before multiplying).
  *
+ * hf32 selects the projection's precision: 0 exact; 1 the HF32 simulation
+ * on the matmul operands x (.) gamma and phi as [HC] states it; 2 the same
+ * truncation applied to the folded weight gamma (.) phi (rounded to fp32
+ * first) with x exact -- the reading of HF32 for a projection that carries
+ * gamma on the weight side.  Without gamma, 1 and 2 are the same.
+ *
  * Readings where the pages are silent or garbled (each is listed in the
  * design notes as well):
  *  - the RMS mean runs over all n*D elements of the token, from raw x;
@@ -113,14 +119,23 @@ static void one_token(const oracle_job *J, int64_t t, double *w, double *P)
         for (int64_t k = 0; k < K; ++k) {
             double g = J->x_fp16 ? mhc_oracle_half_value(xt[k]) : bf16_value(xt[k]);
             double p = phi_r[k];
-            if (J->gamma) {
-                if (J->hf32)
-                    g = hf32_value((float)(g * (double)J->gamma[k]));
+            if (J->hf32 == 2) {
+                /* HF32 on the folded weight: gamma (.) phi rounded to fp32,
+                 * then truncated (x is exact in the HF32 format). */
+                if (J->gamma)
+                    p = hf32_value((float)((double)phi_r[k] * (double)J->gamma[k]));
                 else
-                    g = g * (double)J->gamma[k];
+                    p = hf32_value(phi_r[k]);
+            } else {
+                if (J->gamma) {
+                    if (J->hf32)
+                        g = hf32_value((float)(g * (double)J->gamma[k]));
+                    else
+                        g = g * (double)J->gamma[k];
+                }
+                if (J->hf32)
+                    p = hf32_value(phi_r[k]);
             }
-            if (J->hf32)
-                p = hf32_value(phi_r[k]);
             acc += g * p;
         }
         if (J->h_mix)

@@ -94,10 +94,16 @@ def _ptr(a):
 def run(x_bits: np.ndarray, phi: np.ndarray, alpha: np.ndarray, bias: np.ndarray,
         gamma: Optional[np.ndarray] = None, pre_mix: Optional[np.ndarray] = None, *,
         num_iters: int = 20, norm_eps: float = 1e-6, hc_eps: float = 1e-6,
-        hf32: bool = False, backward: bool = True, threads: Optional[int] = None,
+        hf32: int = 0, backward: bool = True, threads: Optional[int] = None,
         x_fp16: bool = False) -> OracleOut:
     """Evaluate the oracle.  x_bits: uint16/int16 bit patterns [T, n, D] of bf16
-    values, or of IEEE fp16 values with x_fp16=True."""
+    values, or of IEEE fp16 values with x_fp16=True.  hf32: 0 exact projection;
+    1 (or True) the HcPre page's HF32 simulation on the operands x (.) gamma and
+    phi; 2 that truncation on the folded weight gamma (.) phi (rounded to fp32
+    first), x exact."""
+    hf32 = int(hf32)
+    if hf32 not in (0, 1, 2):
+        raise ValueError("hf32 must be 0, 1 or 2")
     x_bits = np.ascontiguousarray(x_bits).view(np.uint16)
     T, n, D = x_bits.shape
     alpha = np.ascontiguousarray(alpha, dtype=np.float32)
@@ -122,7 +128,7 @@ def run(x_bits: np.ndarray, phi: np.ndarray, alpha: np.ndarray, bias: np.ndarray
         threads = os.cpu_count() or 1
     fn = _load().mhc_oracle_pre_f16 if x_fp16 else _load().mhc_oracle_pre
     rc = fn(
-        T, n, D, alpha_len, num_iters, norm_eps, hc_eps, int(bool(hf32)),
+        T, n, D, alpha_len, num_iters, norm_eps, hc_eps, int(hf32),
         _ptr(x_bits), _ptr(phi), _ptr(alpha), _ptr(bias), _ptr(gamma), _ptr(pre_mix),
         _ptr(y), _ptr(h_post), _ptr(h_res), _ptr(h_pre), _ptr(inv_rms), _ptr(h_mix),
         _ptr(sum_out), _ptr(norm_out), int(threads))

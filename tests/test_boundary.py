@@ -45,7 +45,7 @@ def test_library_exports_every_declared_symbol(lib):
 
 def test_struct_layouts_match_header():
     # Field order/sizes in the binding mirror the header (x86-64 and aarch64 LP64).
-    assert ctypes.sizeof(mp.MhcPreConfig) == 8 + 8 + 4 + 4 + 8 + 8 + 4 + 4 + 4 + 4
+    assert ctypes.sizeof(mp.MhcPreConfig) == 8 + 8 + 4 + 4 + 8 + 8 + 4 + 4 + 4 + 4 + 7 * 4 + 4   # tail padding
     assert ctypes.sizeof(mp.MhcPreArgs) == 8 + 15 * 8 + 8
     assert ctypes.sizeof(mp.MhcPreBwdArgs) == 8 + 20 * 8 + 8
 
@@ -55,13 +55,19 @@ def test_defaults(lib):
     assert (c.n, c.D, c.alpha_len, c.num_iters, c.impl_mode, c.need_backward) == (4, 0, 3, 20, 0, 0)
     assert (c.batch_consistent, c.x_dtype) == (0, mp.MHC_DTYPE_BF16)
     assert c.norm_eps == 1e-6 and c.hc_eps == 1e-6
+    assert all(getattr(c, f) == 0 for f in mp.LAUNCH_FIELDS)
+    assert c.kernel == mp.MHC_KERNEL_AUTO
 
 
 @pytest.mark.parametrize("field,value", [("n", 5), ("n", 2), ("D", 0), ("D", 24), ("D", 16400),
                                          ("alpha_len", 1), ("num_iters", 0), ("impl_mode", 2),
                                          ("impl_mode", -1), ("need_backward", 2),
                                          ("batch_consistent", 2), ("batch_consistent", -1),
-                                         ("x_dtype", 2), ("x_dtype", -1)])
+                                         ("x_dtype", 2), ("x_dtype", -1),
+                                         ("kernel", 3), ("kernel", -1), ("cluster", 3), ("cluster", 32),
+                                         ("x_stages", 1), ("x_stages", 9), ("w_stages", 1), ("w_stages", 9),
+                                         ("gw_groups", 3), ("gw_groups", -1), ("gw_x_stages", 1),
+                                         ("gw_x_lead", 16), ("gw_x_lead", -1)])
 def test_create_rejects_bad_config(lib, field, value):
     c = mp.mhc_pre_config_default()
     c.D = 256
@@ -69,6 +75,30 @@ def test_create_rejects_bad_config(lib, field, value):
     st, h = mp.mhc_pre_create(c)
     assert st == mp.MHC_ERR_PARAM_INVALID and h is None
     assert mp.last_error()
+
+
+def test_create_accepts_launch_choices(lib):
+    for kw in ({"kernel": mp.MHC_KERNEL_CLUSTER, "cluster": 4, "x_stages": 3, "w_stages": 2},
+               {"kernel": mp.MHC_KERNEL_GRID, "gw_groups": 1, "gw_x_stages": 4, "gw_x_lead": 3}):
+        op = mp.MhcPre(4, 256, **kw)
+        assert op.handle is not None
+        op.close()
+    with pytest.raises(TypeError):
+        mp.MhcPre(4, 256, tile=128)
+    # batch-consistent mode fixes the cluster size itself
+    c = mp.mhc_pre_config_default()
+    c.D, c.batch_consistent, c.cluster = 256, 1, 4
+    st, h = mp.mhc_pre_create(c)
+    assert st == mp.MHC_ERR_PARAM_INVALID and h is None
+
+
+def test_library_reads_no_environment():
+    """Launch choices are handle fields: no C source of the library reads an
+    environment variable."""
+    csrc = os.path.join(ROOT, "mhc_hyper_connection_gb300", "csrc")
+    for name in os.listdir(csrc):
+        text = open(os.path.join(csrc, name)).read()
+        assert "getenv" not in text and "environ" not in text, name
 
 
 def test_create_null(lib):

@@ -1,6 +1,7 @@
-"""The N > 1 path of bench.py on CPU: two gloo ranks shard tokens without a
-collective on the forward's data path, agree on the max-over-ranks time,
-and sum the backward's weight gradients over ranks (its one exchange)."""
+"""The N > 1 path of bench.py on CPU: two gloo ranks take their shards of one
+global batch through the same calls bench.py makes (rank_shard, shard_tokens),
+with no collective on the forward's data path, agree on the max-over-ranks
+time, and sum the backward's weight gradients over ranks (its one exchange)."""
 import os
 import socket
 
@@ -26,13 +27,23 @@ def _worker(rank, world, port, q):
     dist.init_process_group("gloo", rank=rank, world_size=world)
     w, r, l = bench.dist_env()
     lo, hi = bench.shard_tokens(1000, w, r)
+    # the inputs bench.py gives this rank: its shard of one global batch
+    from mhc_synth import make_case, make_post_case
+    part = bench.rank_shard(lambda **k: make_case("tiny", device="cpu", pre_mix=True, **k), 40, w, r)
+    xs = [torch.empty_like(part.x.float()) for _ in range(w)]
+    dist.all_gather(xs, part.x.float().contiguous())          # bf16 values, exact in fp32
+    pms = [torch.empty_like(part.pre_mix) for _ in range(w)]
+    dist.all_gather(pms, part.pre_mix.contiguous())
+    post = bench.rank_shard(lambda **k: make_post_case(device="cpu", **k), 24, w, r)
+    shard_info = (part.T, tuple(part.x.shape), torch.cat(xs).numpy().tobytes(), torch.cat(pms).numpy().tobytes(),
+                  post.T, tuple(post.residual.shape))
     t = bench.max_over_ranks(1.0 + r, w)
     grads = {"grad_phi": torch.full((2, 3), float(r + 1)), "grad_alpha": torch.tensor([r, 1.0, 2.0]),
              "grad_bias": torch.ones(4) * (r + 1), "grad_gamma": None, "grad_x": torch.full((2,), float(r))}
     bench.allreduce_weight_grads(grads, w)
     dist.barrier()
     q.put((r, lo, hi, t, grads["grad_phi"].tolist(), grads["grad_alpha"].tolist(), grads["grad_bias"].tolist(),
-           grads["grad_x"].tolist()))
+           grads["grad_x"].tolist(), shard_info))
     dist.destroy_process_group()
 
 
@@ -52,6 +63,28 @@ def test_two_rank_sharding_and_max_time():
     for r in res:
         assert r[4] == [[3.0] * 3] * 2 and r[5] == [1.0, 2.0, 4.0] and r[6] == [3.0] * 4   # summed
     assert res[0][7] == [0.0, 0.0] and res[1][7] == [1.0, 1.0]         # grad_x stays per rank
+    # each rank held its own 40 tokens, and together they are the global batch
+    # of 80 tokens drawn from one seed, in rank order
+    from mhc_synth import make_case
+    full = make_case("tiny", device="cpu", T=80, seed=0, pre_mix=True)
+    for r in res:
+        T_r, shape, xs, pms, post_T, post_shape = r[8]
+        assert T_r == 40 and shape == (40, 4, 256) and post_T == 24 and post_shape == (24, 4, 256)
+        assert xs == full.x.float().numpy().tobytes()
+        assert pms == full.pre_mix.numpy().tobytes()
+
+
+def test_take_tokens_cuts_only_per_token_tensors():
+    from mhc_synth import make_bwd_grads, make_case
+    c = make_case("tiny", device="cpu", T=10, gamma=True, pre_mix=True)
+    p = bench.take_tokens(c, 3, 7)
+    assert p.T == 4 and torch.equal(p.x, c.x[3:7]) and torch.equal(p.pre_mix, c.pre_mix[3:7])
+    assert p.phi is c.phi and p.gamma is c.gamma and p.bias is c.bias
+    g = make_bwd_grads(device="cpu", T=10, grad_x_post=True)
+    q = bench.take_tokens(g, 2, 5)
+    assert torch.equal(q.g_in, g.g_in[2:5]) and torch.equal(q.g_res, g.g_res[2:5])
+    assert torch.equal(q.g_x_post, g.g_x_post[2:5])
+    assert bench.rank_shard(lambda **k: make_case("tiny", device="cpu", **k), 16, 1, 0).T == 16
 
 
 def test_single_rank_helpers():

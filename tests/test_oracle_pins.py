@@ -306,6 +306,45 @@ def test_hf32_truncates_operands():
     assert 1e-6 < rel < 2e-3
 
 
+def test_hf32_on_the_folded_weight():
+    """hf32=2 truncates the folded weight gamma (.) phi (rounded to fp32), x
+    exact.  Closed form from the HF32 format (10 fraction bits): with
+    phi = gamma = 1 + 2^-10 (both exact in HF32) the fp32 product is
+    1 + 2^-9 + 2^-20, which HF32 cuts to 1 + 2^-9; the operand-wise
+    simulation (hf32=1) keeps both factors and so the 2^-20 term.  With
+    x = 1 everywhere each projection row is then K (1 + 2^-9) against
+    K (1 + 2^-9 + 2^-20).  Without gamma the two variants agree exactly."""
+    T, n, D = 2, 4, 8
+    K = n * D
+    R = n * n + 2 * n
+    x = np.full((T, n, D), 0x3F80, dtype=np.uint16)            # bf16 1.0
+    v = np.float32(1.0 + 2.0 ** -10)
+    phi = np.full((R, K), v, dtype=np.float32)
+    gamma = np.full((n, D), v, dtype=np.float32)
+    alpha = np.array([0.5, 0.5, 0.5], dtype=np.float32)
+    bias = np.zeros(R, dtype=np.float32)
+    folded = oracle.run(x, phi, alpha, bias, gamma, hf32=2)
+    operand = oracle.run(x, phi, alpha, bias, gamma, hf32=1)
+    exact = oracle.run(x, phi, alpha, bias, gamma)
+    np.testing.assert_array_equal(folded.h_mix, np.full((T, R), K * (1 + 2.0 ** -9)))
+    np.testing.assert_array_equal(operand.h_mix, np.full((T, R), K * (1 + 2.0 ** -9 + 2.0 ** -20)))
+    np.testing.assert_array_equal(exact.h_mix, operand.h_mix)
+    # random inputs without gamma: 1 and 2 are the same simulation
+    x, phi, alpha, bias, _, _ = rand_inputs(3, 4, 64)
+    a = oracle.run(x, phi, alpha, bias, hf32=1)
+    b = oracle.run(x, phi, alpha, bias, hf32=2)
+    for key in ("y", "h_pre", "h_post", "h_res", "h_mix"):
+        np.testing.assert_array_equal(getattr(a, key), getattr(b, key))
+    # with gamma, the folded variant equals the exact projection of the
+    # truncated fp32 product weights
+    x, phi, alpha, bias, g, _ = rand_inputs(3, 4, 64, gamma=True)
+    w = (phi.astype(np.float32) * g.reshape(-1).astype(np.float32)).astype(np.float32)
+    w = (w.view(np.uint32) & np.uint32(0xFFFFE000)).view(np.float32)
+    c = oracle.run(x, phi, alpha, bias, g, hf32=2)
+    d = oracle.run(x, w, alpha, bias)
+    np.testing.assert_allclose(c.h_mix, d.h_mix, rtol=1e-15, atol=1e-15)
+
+
 def test_empty_and_threads_agree():
     x, phi, alpha, bias, g, _ = rand_inputs(7, 4, 16, gamma=True)
     a = oracle.run(x, phi, alpha, bias, g, threads=1)

@@ -43,8 +43,11 @@ def test_training_shaped_with_backward_outputs(cuda_device):
     assert errs["inv_rms"] <= 1e-4
 
 
-def test_decode_shaped_outliers(cuda_device):
-    _full(make_case("decode", device=cuda_device))
+@pytest.mark.parametrize("mode", [0, 1])
+def test_decode_shaped_outliers(cuda_device, mode):
+    """Decode workload (1% of x scaled by 20).  In tf32 mode y is held to the
+    same bound as in fp32 mode, against the HF32 simulation of the oracle."""
+    _full(make_case("decode", device=cuda_device, impl_mode=mode))
 
 
 @pytest.mark.parametrize("mode", [0, 1])
@@ -61,9 +64,17 @@ def test_generic_n8_pre_mix(cuda_device):
     _full(make_case("generic_a", device=cuda_device))
 
 
-def test_generic_n8_two_gates(cuda_device):
-    out, _ = _full(make_case("generic_b", device=cuda_device))
+@pytest.mark.parametrize("mode", [0, 1])
+def test_generic_n8_two_gates(cuda_device, mode):
+    out, _ = _full(make_case("generic_b", device=cuda_device, impl_mode=mode))
     assert torch.all(out["h_res"] == 0)
+
+
+@pytest.mark.parametrize("gamma", [False, True])
+def test_training_tf32(cuda_device, gamma):
+    """tf32 mode on the training shape, with and without gamma, intermediates
+    included, against the oracle's HF32 simulation on the folded weight."""
+    _full(make_case("training", device=cuda_device, impl_mode=1, gamma=gamma))
 
 
 def _every_token_properties(case, out):

@@ -1,9 +1,8 @@
 """Every forward kernel against the oracle: the 64-token cluster kernel
-(forced with MHC_PRE_PATH=cluster), the 128-token cluster kernel (n = 4)
-selected with MHC_PRE_TILE=128, the grid-wide kernel forced with
-MHC_PRE_PATH=grid, and the automatic choice (up to 512 tokens the grid-wide
-kernel when the cluster kernel would have a single tile or need more than
-one round of clusters; the cluster kernel otherwise)."""
+(forced with the handle's kernel = MHC_KERNEL_CLUSTER), the grid-wide kernel
+(kernel = MHC_KERNEL_GRID), and the automatic choice (up to 512 tokens the
+grid-wide kernel when the cluster kernel would have a single tile or need
+more than one round of clusters; the cluster kernel otherwise)."""
 import pytest
 import torch
 
@@ -19,23 +18,18 @@ def built():
     build.build()
 
 
-def _run(case, path, monkeypatch):
+def launch_of(path):
+    """Handle launch-choice fields that force a forward path."""
+    from mhc_hyper_connection_gb300 import MHC_KERNEL_CLUSTER, MHC_KERNEL_GRID
+    return {"grid": {"kernel": MHC_KERNEL_GRID}, "cluster": {"kernel": MHC_KERNEL_CLUSTER}}.get(path, {})
+
+
+def _run(case, path):
     from mhc_hyper_connection_gb300 import mhc_pre_last_kernel
-    monkeypatch.delenv("MHC_PRE_PATH", raising=False)
-    monkeypatch.delenv("MHC_PRE_TILE", raising=False)
-    if path == "grid":
-        monkeypatch.setenv("MHC_PRE_PATH", "grid")
-        want = "mhc_pre_gw_kernel"
-    elif path == "tile128":   # 128-token tiles exist for n = 4 only
-        monkeypatch.setenv("MHC_PRE_PATH", "cluster")
-        monkeypatch.setenv("MHC_PRE_TILE", "128")
-        want = "mhc_pre_t128_kernel" if case.n == 4 else "mhc_pre_tc_kernel"
-    elif path == "cluster":
-        monkeypatch.setenv("MHC_PRE_PATH", "cluster")
+    want = {"grid": "mhc_pre_gw_kernel", "cluster": "mhc_pre_tc_kernel"}.get(path)
+    if path == "auto" and case.T > 512:
         want = "mhc_pre_tc_kernel"
-    else:                     # automatic: grid-wide for some batches up to 512 tokens, cluster above
-        want = None if case.T <= 512 else "mhc_pre_tc_kernel"
-    op, out = run_cuda(case)
+    op, out = run_cuda(case, **launch_of(path))
     torch.cuda.synchronize()
     got = mhc_pre_last_kernel(op.handle)
     assert got == want if want else got in ("mhc_pre_gw_kernel", "mhc_pre_tc_kernel")
@@ -43,54 +37,48 @@ def _run(case, path, monkeypatch):
     return out
 
 
-PATHS = ["auto", "cluster", "tile128", "grid"]
+PATHS = ["auto", "cluster", "grid"]
 
 
 @pytest.mark.parametrize("path", PATHS)
 @pytest.mark.parametrize("name", ["tiny", "training", "decode", "generic_a", "generic_b"])
-def test_workloads(cuda_device, monkeypatch, path, name):
-    _run(make_case(name, device=cuda_device), path, monkeypatch)
+def test_workloads(cuda_device, path, name):
+    _run(make_case(name, device=cuda_device), path)
 
 
 @pytest.mark.parametrize("path", PATHS)
 @pytest.mark.parametrize("T", [1, 127, 130, 1000])
-def test_ragged_tokens(cuda_device, monkeypatch, path, T):
-    _run(make_case("tiny", device=cuda_device, T=T, D=1024, need_backward=True), path, monkeypatch)
+def test_ragged_tokens(cuda_device, path, T):
+    _run(make_case("tiny", device=cuda_device, T=T, D=1024, need_backward=True), path)
 
 
 @pytest.mark.parametrize("path", PATHS)
 @pytest.mark.parametrize("n,alpha_len", [(6, 3), (8, 2), (8, 3)])
 @pytest.mark.parametrize("D", [16, 592])
-def test_streams(cuda_device, monkeypatch, path, n, alpha_len, D):
+def test_streams(cuda_device, path, n, alpha_len, D):
     _run(make_case("tiny", device=cuda_device, T=300, n=n, D=D, alpha_len=alpha_len,
-                   need_backward=True, gamma=True), path, monkeypatch)
+                   need_backward=True, gamma=True), path)
 
 
-def test_grid_path_deterministic(cuda_device, monkeypatch):
-    monkeypatch.setenv("MHC_PRE_PATH", "grid")
+def test_grid_path_deterministic(cuda_device):
     case = make_case("training", device=cuda_device, T=777)
-    op, a = run_cuda(case)
+    op, a = run_cuda(case, **launch_of("grid"))
     _, b = run_cuda(case, op=op)
     torch.cuda.synchronize()
     for k in ("y", "h_post", "h_res", "h_pre", "inv_rms", "h_mix", "sum_out", "norm_out"):
         assert torch.equal(a[k], b[k]), k
 
 
-@pytest.mark.parametrize("path", ["cluster", "tile128", "grid"])
+@pytest.mark.parametrize("path", ["cluster", "grid"])
 @pytest.mark.parametrize("x_dtype", [torch.bfloat16, torch.float16])
-def test_repeated_runs_bitwise(cuda_device, monkeypatch, path, x_dtype):
+def test_repeated_runs_bitwise(cuda_device, path, x_dtype):
     """Twenty runs of one input agree bit for bit on every output: the
     reductions run in a fixed order, so any difference is a read of a
     buffer before its data is in (or after it is reused)."""
     if x_dtype == torch.float16 and path != "cluster":
         pytest.skip("fp16 x runs on the 64-token cluster kernel only")
-    monkeypatch.delenv("MHC_PRE_PATH", raising=False)
-    monkeypatch.delenv("MHC_PRE_TILE", raising=False)
-    monkeypatch.setenv("MHC_PRE_PATH", "grid" if path == "grid" else "cluster")
-    if path == "tile128":
-        monkeypatch.setenv("MHC_PRE_TILE", "128")
     case = make_case("training", device=cuda_device, x_dtype=x_dtype)
-    op, ref = run_cuda(case)
+    op, ref = run_cuda(case, **launch_of(path))
     torch.cuda.synchronize()
     ref = {k: v.clone() for k, v in ref.items() if isinstance(v, torch.Tensor)}
     out = op.allocate(case.T, cuda_device)
@@ -102,13 +90,11 @@ def test_repeated_runs_bitwise(cuda_device, monkeypatch, path, x_dtype):
 
 
 @pytest.mark.parametrize("name,kw", [("generic_a", {}), ("tiny", {"n": 6, "D": 592, "alpha_len": 3})])
-def test_repeated_runs_bitwise_unpaired(cuda_device, monkeypatch, name, kw):
+def test_repeated_runs_bitwise_unpaired(cuda_device, name, kw):
     """As above for shapes that run one stream per MMA (n = 8 three-gate,
     n = 6), whose sums of squares take the single-partial hand-off."""
-    monkeypatch.delenv("MHC_PRE_TILE", raising=False)
-    monkeypatch.setenv("MHC_PRE_PATH", "cluster")
     case = make_case(name, device=cuda_device, **kw)
-    op, ref = run_cuda(case)
+    op, ref = run_cuda(case, **launch_of("cluster"))
     torch.cuda.synchronize()
     compare(case, ref, run_oracle(case, tokens=list(range(0, case.T, max(1, case.T // 64)))),
             tokens=list(range(0, case.T, max(1, case.T // 64))))
@@ -137,17 +123,13 @@ def _random_configs(count=24, seed=20261202):
 
 
 @pytest.mark.parametrize("cfg", _random_configs(), ids=lambda c: "T{T}_n{n}_D{D}_a{alpha_len}_m{impl_mode}_{path}".format(**c))
-def test_random_shapes(cuda_device, monkeypatch, cfg):
+def test_random_shapes(cuda_device, cfg):
     """Seeded random shapes, gate forms, modes and optional inputs on every
     forward path, each compared in full with the oracle."""
     cfg = dict(cfg)
     path = cfg.pop("path")
     seed = cfg.pop("seed")
     case = make_case("tiny", device=cuda_device, seed=seed, **cfg)
-    monkeypatch.delenv("MHC_PRE_TILE", raising=False)
-    monkeypatch.delenv("MHC_PRE_PATH", raising=False)
-    if path != "auto":
-        monkeypatch.setenv("MHC_PRE_PATH", path)
-    op, out = run_cuda(case)
+    op, out = run_cuda(case, **launch_of(path))
     torch.cuda.synchronize()
     compare(case, out, run_oracle(case))
