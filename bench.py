@@ -186,8 +186,8 @@ def hbm_peak():
         return 6800.0, "fallback"
 
 
-KERNEL_SOURCES = {"mhc_pre_tc_kernel": "mhc_pre_tc.cu", "mhc_pre_gw_kernel": "mhc_pre_gw.cu",
-                  "mhc_pre_t128_kernel": "mhc_pre_t128.cu", "bw_main_kernel": "mhc_bwd.cu"}
+KERNEL_SOURCES = {"mhc_pre_tc_kernel": "mhc_pre_tc.cu", "mhc_pre_tc_kernel_resident": "mhc_pre_tc.cu",
+                  "mhc_pre_gw_kernel": "mhc_pre_gw.cu", "bw_main_kernel": "mhc_bwd.cu"}
 
 
 def _code_only(text):
@@ -646,6 +646,10 @@ def main():
     ap.add_argument("--batch-consistent", action="store_true",
                     help="forward in batch-consistent mode (results per token independent of T)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--kernel", choices=["auto", "cluster", "grid", "resident"], default="auto",
+                    help="forward: force a fused kernel (default: the library's choice)")
+    ap.add_argument("--cluster", type=int, default=0, help="forward: force a cluster size (0: the library's)")
+    ap.add_argument("--tm-buffers", type=int, default=0, help="resident forward: TMEM chunk buffers (0: the library's)")
     ap.add_argument("--op", choices=["pre", "post", "bwd"], default="pre",
                     help="pre: the pre-mapping forward (the headline); post: the post-mapping (hc_post); "
                          "bwd: the pre-mapping backward")
@@ -710,8 +714,10 @@ def main():
     xdt = torch.float16 if args.x_dtype == "fp16" else torch.bfloat16
     case = rank_shard(lambda **k: make_case("prefill", device=device, impl_mode=args.mode, x_dtype=xdt, **k),
                       T, world, rank)
+    kernel_code = {"auto": 0, "cluster": 1, "grid": 2, "resident": 3}[args.kernel]
     op = MhcPre(n, D, alpha_len=3, num_iters=20, impl_mode=args.mode, batch_consistent=args.batch_consistent,
-                x_dtype=MHC_DTYPE_FP16 if args.x_dtype == "fp16" else MHC_DTYPE_BF16)
+                x_dtype=MHC_DTYPE_FP16 if args.x_dtype == "fp16" else MHC_DTYPE_BF16,
+                kernel=kernel_code, cluster=args.cluster, tm_buffers=args.tm_buffers)
     out = op.allocate(T, device)
     stream = torch.cuda.current_stream(device)
 

@@ -75,6 +75,8 @@ typedef struct mhc_pre_s *mhc_pre_t;
 #define MHC_KERNEL_AUTO    0
 #define MHC_KERNEL_CLUSTER 1   /* 64-token tiles shared by a thread-block cluster   */
 #define MHC_KERNEL_GRID    2   /* every SM on a few tiles (small T, bf16 x)         */
+#define MHC_KERNEL_RESIDENT 3  /* cluster kernel keeping the last chunks of x in
+                                  tensor memory for y (n = 4)                        */
 
 /* Fixed per handle.  Defaults (mhc_pre_config_default): n = 4, D = 0 (must be
  * set), alpha_len = 3, num_iters = 20, norm_eps = hc_eps = 1e-6,
@@ -111,8 +113,8 @@ typedef struct {
                                so every |phi . gamma| must be <= 65504: a larger
                                one sets bit 3 of the device error word, which
                                mhc_pre_status reports                              */
-    int32_t kernel;         /* MHC_KERNEL_AUTO / _CLUSTER / _GRID (grid: bf16 x,
-                               not batch_consistent)                               */
+    int32_t kernel;         /* MHC_KERNEL_AUTO / _CLUSTER / _GRID / _RESIDENT (grid:
+                               bf16 x; grid and resident: not batch_consistent)    */
     int32_t cluster;        /* cluster kernel: CTAs per cluster, 1, 2, 4, 8 or 16   */
     int32_t x_stages;       /* cluster kernel: deepest x ring tried, 2..8           */
     int32_t w_stages;       /* cluster kernel: deepest phi-plane ring tried, 2..8   */
@@ -120,6 +122,9 @@ typedef struct {
     int32_t gw_x_stages;    /* grid-wide kernel: deepest x ring tried, 2..8         */
     int32_t gw_x_lead;      /* grid-wide kernel: tiles its loads may run ahead of
                                its own y, 1..15                                     */
+    int32_t tm_buffers;     /* resident kernel: tensor-memory chunk buffers, 1 or 2
+                               (2: alternate tiles use their own, so a tile does
+                               not wait for the previous one's y)                  */
 } mhc_pre_config;
 
 /* Per call.  R = n*n + 2n (alpha_len 3) or 2n (alpha_len 2); I = num_iters. */

@@ -7,7 +7,7 @@ and marshals arguments; importing it does not load the library until a
 function is called.
 """
 from ._binding import (  # noqa: F401
-    LAUNCH_FIELDS, LIB_PATH, MHC_DTYPE_BF16, MHC_DTYPE_FP16, MHC_KERNEL_AUTO, MHC_KERNEL_CLUSTER, MHC_KERNEL_GRID, MHC_ERR_NULLPTR, MHC_ERR_PARAM_INVALID, MHC_ERR_RUNTIME, MHC_IMPL_FP32,
+    LAUNCH_FIELDS, LIB_PATH, MHC_DTYPE_BF16, MHC_DTYPE_FP16, MHC_KERNEL_AUTO, MHC_KERNEL_CLUSTER, MHC_KERNEL_GRID, MHC_KERNEL_RESIDENT, MHC_ERR_NULLPTR, MHC_ERR_PARAM_INVALID, MHC_ERR_RUNTIME, MHC_IMPL_FP32,
     MHC_IMPL_TF32, MHC_OK, MhcError, MhcPre, MhcPreArgs, MhcPreBwdArgs, MhcPreConfig, hc_post, last_error,
     library, mhc_post_run, mhc_pre_backward_run, mhc_pre_backward_workspace_size, mhc_pre_inv_rms_run,
     mhc_pre_mixes_run, mhc_pre_sinkhorn_run,

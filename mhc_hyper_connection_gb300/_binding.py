@@ -23,6 +23,7 @@ MHC_DTYPE_FP16 = 1
 MHC_KERNEL_AUTO = 0
 MHC_KERNEL_CLUSTER = 1
 MHC_KERNEL_GRID = 2
+MHC_KERNEL_RESIDENT = 3
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_PKG, "libmhc_pre.so")
@@ -35,11 +36,11 @@ class MhcPreConfig(ctypes.Structure):
                 ("need_backward", ctypes.c_int32), ("batch_consistent", ctypes.c_int32),
                 ("x_dtype", ctypes.c_int32), ("kernel", ctypes.c_int32), ("cluster", ctypes.c_int32),
                 ("x_stages", ctypes.c_int32), ("w_stages", ctypes.c_int32), ("gw_groups", ctypes.c_int32),
-                ("gw_x_stages", ctypes.c_int32), ("gw_x_lead", ctypes.c_int32)]
+                ("gw_x_stages", ctypes.c_int32), ("gw_x_lead", ctypes.c_int32), ("tm_buffers", ctypes.c_int32)]
 
 # Launch-choice fields of MhcPreConfig (0 = automatic); MhcPre takes them as
 # keyword arguments.
-LAUNCH_FIELDS = ("kernel", "cluster", "x_stages", "w_stages", "gw_groups", "gw_x_stages", "gw_x_lead")
+LAUNCH_FIELDS = ("kernel", "cluster", "x_stages", "w_stages", "gw_groups", "gw_x_stages", "gw_x_lead", "tm_buffers")
 
 
 _P = ctypes.c_void_p

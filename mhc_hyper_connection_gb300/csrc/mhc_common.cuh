@@ -306,7 +306,7 @@ __host__ __device__ constexpr int sink_stride(int n) { return n * n; }
 // and w rings are back to back, so an operand read that runs past a slot
 // stays inside the window.
 struct SmemLayout {
-  size_t x, w, part, coef, tail, total;
+  size_t x, w, part, coef, sink, tail, total;
 };
 __host__ __device__ inline SmemLayout smem_layout(int n, int R, int P, int xs, int ws) {
   SmemLayout L;
@@ -318,6 +318,7 @@ __host__ __device__ inline SmemLayout smem_layout(int n, int R, int P, int xs, i
   // publish warps has projection sums), else one
   L.part = o; o += (stream_pairs(n, R, P) ? 2 : 1) * (size_t)kTileT * partial_stride(R) * 4;
   L.coef = o; o += (size_t)kCoefBufs * kTileT * n * 4;
+  L.sink = o; o += (size_t)32 * n * n * 4 + 32 * 4;   // a Sinkhorn batch: 32 tokens' logits and indices
   o = (o + 15) & ~size_t(15);
   L.tail = o; o += kTailBytes;
   L.total = o + 1024;
@@ -338,6 +339,7 @@ struct Geometry {
   int T, D, n;
   int num_tiles, nd;           // token tiles; 64-wide d-chunks per stream
   int cluster, xstages, wstages;
+  int tm_bufs;                 // resident mode: TMEM chunk buffers (1 or 2)
   WaitTest wt;
 };
 
@@ -348,6 +350,8 @@ struct TcLaunch {
   const __nv_bfloat16* planes;   // swizzled plane blocks (see PlaneParams)
   int NP, P;
   int fp16;                // x and y fp16 (planes fp16)
+  int resident;            // 1: the last chunks of each CTA's range stay in TMEM for y
+  int tm_bufs;             // resident mode: TMEM chunk buffers used by alternate tiles (1 or 2)
   int cluster;             // CTAs per token tile (split over d-chunks)
   int grid;                // CTAs (multiple of cluster)
   int xstages, wstages;
@@ -391,8 +395,10 @@ cudaError_t launch_stage_sinkhorn(const EpiParams& ep, const void* x, const floa
 // Resolved by the kernel translation unit for the given (n, R, P).
 cudaError_t launch_tc_forward(const TcLaunch& L, cudaStream_t s);
 // Clusters of the given size that fit on the device at once (0: unsupported).
-cudaError_t tc_forward_occupancy(int n, int R, int P, bool fp16, size_t smem_bytes, int cluster,
+cudaError_t tc_forward_occupancy(int n, int R, int P, bool fp16, bool resident, size_t smem_bytes, int cluster,
                                  int* max_clusters);
+// Shapes the resident mode of the cluster kernel takes (n = 4, stream pairs).
+bool tc_resident_supported(int n, int R, int P);
 int tc_np(int R, int P);
 
 // ---------------------------------------------------------------------------

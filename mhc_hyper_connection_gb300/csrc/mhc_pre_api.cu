@@ -299,6 +299,7 @@ void mhc_pre_config_default(mhc_pre_config* c) {
   c->gw_groups = 0;
   c->gw_x_stages = 0;
   c->gw_x_lead = 0;
+  c->tm_buffers = 0;
 }
 
 const char* mhc_pre_last_error(void) { return g_last_error; }
@@ -333,8 +334,9 @@ mhc_status_t mhc_pre_create(mhc_pre_t* out, const mhc_pre_config* cfg) {
   if (c.x_dtype == MHC_DTYPE_FP16 && c.n != 4)
     return fail(MHC_ERR_PARAM_INVALID, "fp16 x is supported for n = 4");
   if (!(c.norm_eps >= 0.0) || !(c.hc_eps >= 0.0)) return fail(MHC_ERR_PARAM_INVALID, "eps values must be >= 0");
-  if (c.kernel != MHC_KERNEL_AUTO && c.kernel != MHC_KERNEL_CLUSTER && c.kernel != MHC_KERNEL_GRID)
-    return fail(MHC_ERR_PARAM_INVALID, "kernel must be MHC_KERNEL_AUTO, _CLUSTER or _GRID");
+  if (c.kernel != MHC_KERNEL_AUTO && c.kernel != MHC_KERNEL_CLUSTER && c.kernel != MHC_KERNEL_GRID &&
+      c.kernel != MHC_KERNEL_RESIDENT)
+    return fail(MHC_ERR_PARAM_INVALID, "kernel must be MHC_KERNEL_AUTO, _CLUSTER, _GRID or _RESIDENT");
   if (c.cluster != 0 && c.cluster != 1 && c.cluster != 2 && c.cluster != 4 && c.cluster != 8 && c.cluster != 16)
     return fail(MHC_ERR_PARAM_INVALID, "cluster must be 0 (automatic), 1, 2, 4, 8 or 16");
   if ((c.x_stages != 0 && (c.x_stages < 2 || c.x_stages > mhc::kMaxStages)) ||
@@ -344,6 +346,7 @@ mhc_status_t mhc_pre_create(mhc_pre_t* out, const mhc_pre_config* cfg) {
   if (c.gw_groups < 0 || c.gw_groups > mhc::kGwMaxGroups)
     return fail(MHC_ERR_PARAM_INVALID, "gw_groups must be 0 (automatic), 1 or %d", mhc::kGwMaxGroups);
   if (c.gw_x_lead < 0 || c.gw_x_lead > 15) return fail(MHC_ERR_PARAM_INVALID, "gw_x_lead must be 0..15");
+  if (c.tm_buffers < 0 || c.tm_buffers > 2) return fail(MHC_ERR_PARAM_INVALID, "tm_buffers must be 0, 1 or 2");
   if (c.batch_consistent && c.cluster != 0)
     return fail(MHC_ERR_PARAM_INVALID, "batch_consistent fixes the cluster size; leave cluster 0");
   mhc_pre_s* h = new (std::nothrow) mhc_pre_s;
@@ -448,6 +451,16 @@ mhc_status_t mhc_pre_run(mhc_pre_t h, const mhc_pre_args* a, void* stream) {
     if (st != MHC_ERR_NOT_SUITABLE) return st;
     return fail(MHC_ERR_PARAM_INVALID, "the grid-wide forward does not fit this shape");
   }
+  // Resident mode of the cluster kernel: the last chunks of each CTA's
+  // range stay in TMEM for y, so y re-reads only the others.  Chosen
+  // automatically for n = 4 from 4096 tokens (measured at D = 7168: T = 4096
+  // 105 against 107 us, 8192 190 against 199, 32768 645 against 666 us, at
+  // cluster 4; at D = 4096 it ties with the plain kernel at cluster 2).
+  constexpr int64_t kResAutoMinT = 4096;
+  const bool res_ok = !consistent && mhc::tc_resident_supported(n, R, h->P);
+  const bool resident = c.kernel == MHC_KERNEL_RESIDENT || (c.kernel == MHC_KERNEL_AUTO && res_ok && T >= kResAutoMinT);
+  if (resident && !res_ok)
+    return fail(MHC_ERR_PARAM_INVALID, "the resident forward takes n = 4 outside batch-consistent mode");
   const int tile_t = mhc::kTileT;
   auto layout = [&](int xsn, int wsn) { return mhc::smem_layout(n, R, h->P, xsn, wsn); };
   mhc::TcLaunch L;
@@ -505,7 +518,13 @@ mhc_status_t mhc_pre_run(mhc_pre_t h, const mhc_pre_args* a, void* stream) {
   // The handle's `cluster` field forces a size (for tuning runs).
   // Batch-consistent mode pins cluster 2 (1 when there is a single d-chunk):
   // a token's reduction is then split the same way whatever T is.
-  const int forced = consistent ? (nd >= 2 ? 2 : 1) : (int)c.cluster;
+  // Resident mode without a forced size: 4 CTAs per cluster from D = 6144
+  // (144 SMs busy; the re-read chunks are read again sooner than at 2),
+  // else 2.
+  int res_cluster = D >= 6144 ? 4 : 2;
+  while (res_cluster > nd) res_cluster >>= 1;
+  const int forced = consistent ? (nd >= 2 ? 2 : 1)
+                                : (c.cluster ? (int)c.cluster : (resident && c.kernel == MHC_KERNEL_AUTO ? res_cluster : 0));
   if (forced > nd) return fail(MHC_ERR_PARAM_INVALID, "cluster %d exceeds the %d d-chunks of a stream", forced, nd);
   int cluster = 0;
   int max_clusters = 0;
@@ -513,7 +532,7 @@ mhc_status_t mhc_pre_run(mhc_pre_t h, const mhc_pre_args* a, void* stream) {
   for (int cand : {1, 2, 4, 8, 16}) {
     if ((forced && cand != forced) || cand > nd) continue;
     int mc = 0;
-    const cudaError_t oe = mhc::tc_forward_occupancy(n, R, h->P, fp16, smem, cand, &mc);
+    const cudaError_t oe = mhc::tc_forward_occupancy(n, R, h->P, fp16, resident, smem, cand, &mc);
     if (oe != cudaSuccess || mc <= 0) {
       cudaGetLastError();
       continue;
@@ -527,13 +546,15 @@ mhc_status_t mhc_pre_run(mhc_pre_t h, const mhc_pre_args* a, void* stream) {
   }
   if (max_clusters <= 0)
     return fail(forced ? MHC_ERR_PARAM_INVALID : MHC_ERR_RUNTIME, "no cluster configuration fits this device");
-  if (gw_ok && !force_cluster && !forced && T <= kGwAutoMaxT) {
+  if (gw_ok && !force_cluster && !resident && !c.cluster && T <= kGwAutoMaxT) {
     const int rounds = (num_tiles + max_clusters - 1) / max_clusters;
     if (num_tiles == 1 || rounds > 1) {
       mhc_status_t st = run_grid_wide(h, a, di, planes, s);
       if (st != MHC_ERR_NOT_SUITABLE) return st;
     }
   }
+  L.resident = resident ? 1 : 0;
+  L.tm_bufs = c.tm_buffers ? c.tm_buffers : 1;
   L.cluster = cluster;
   L.grid = (num_tiles < max_clusters ? num_tiles : max_clusters) * cluster;
   L.x = a->x;
@@ -544,7 +565,7 @@ mhc_status_t mhc_pre_run(mhc_pre_t h, const mhc_pre_args* a, void* stream) {
   h->last_grid = L.grid;
   h->last_stages = xst;
   h->last_ystages = wst;
-  h->last_kernel = "mhc_pre_tc_kernel";
+  h->last_kernel = resident ? "mhc_pre_tc_kernel_resident" : "mhc_pre_tc_kernel";
   if (h->ev_before && cudaEventRecord(h->ev_before, s) != cudaSuccess)
     return fail(MHC_ERR_RUNTIME, "recording the timing event failed");
   if (mhc::launch_tc_forward(L, s) != cudaSuccess)

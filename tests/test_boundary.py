@@ -45,7 +45,7 @@ def test_library_exports_every_declared_symbol(lib):
 
 def test_struct_layouts_match_header():
     # Field order/sizes in the binding mirror the header (x86-64 and aarch64 LP64).
-    assert ctypes.sizeof(mp.MhcPreConfig) == 8 + 8 + 4 + 4 + 8 + 8 + 4 + 4 + 4 + 4 + 7 * 4 + 4   # tail padding
+    assert ctypes.sizeof(mp.MhcPreConfig) == 8 + 8 + 4 + 4 + 8 + 8 + 4 + 4 + 4 + 4 + 8 * 4
     assert ctypes.sizeof(mp.MhcPreArgs) == 8 + 15 * 8 + 8
     assert ctypes.sizeof(mp.MhcPreBwdArgs) == 8 + 20 * 8 + 8
 
@@ -64,10 +64,11 @@ def test_defaults(lib):
                                          ("impl_mode", -1), ("need_backward", 2),
                                          ("batch_consistent", 2), ("batch_consistent", -1),
                                          ("x_dtype", 2), ("x_dtype", -1),
-                                         ("kernel", 3), ("kernel", -1), ("cluster", 3), ("cluster", 32),
+                                         ("kernel", 4), ("kernel", -1), ("cluster", 3), ("cluster", 32),
                                          ("x_stages", 1), ("x_stages", 9), ("w_stages", 1), ("w_stages", 9),
                                          ("gw_groups", 3), ("gw_groups", -1), ("gw_x_stages", 1),
-                                         ("gw_x_lead", 16), ("gw_x_lead", -1)])
+                                         ("gw_x_lead", 16), ("gw_x_lead", -1), ("tm_buffers", 3),
+                                         ("tm_buffers", -1)])
 def test_create_rejects_bad_config(lib, field, value):
     c = mp.mhc_pre_config_default()
     c.D = 256

@@ -1,8 +1,10 @@
 """Every forward kernel against the oracle: the 64-token cluster kernel
-(forced with the handle's kernel = MHC_KERNEL_CLUSTER), the grid-wide kernel
-(kernel = MHC_KERNEL_GRID), and the automatic choice (up to 512 tokens the
-grid-wide kernel when the cluster kernel would have a single tile or need
-more than one round of clusters; the cluster kernel otherwise)."""
+(forced with the handle's kernel = MHC_KERNEL_CLUSTER), its resident mode
+(MHC_KERNEL_RESIDENT, n = 4: the last chunks of each CTA's range kept in
+tensor memory for y), the grid-wide kernel (kernel = MHC_KERNEL_GRID), and
+the automatic choice (up to 512 tokens the grid-wide kernel when the cluster
+kernel would have a single tile or need more than one round of clusters; the
+cluster kernel otherwise)."""
 import pytest
 import torch
 
@@ -18,17 +20,24 @@ def built():
     build.build()
 
 
+KERNEL_OF = {"grid": "mhc_pre_gw_kernel", "cluster": "mhc_pre_tc_kernel", "resident": "mhc_pre_tc_kernel_resident"}
+
+
 def launch_of(path):
     """Handle launch-choice fields that force a forward path."""
-    from mhc_hyper_connection_gb300 import MHC_KERNEL_CLUSTER, MHC_KERNEL_GRID
-    return {"grid": {"kernel": MHC_KERNEL_GRID}, "cluster": {"kernel": MHC_KERNEL_CLUSTER}}.get(path, {})
+    from mhc_hyper_connection_gb300 import MHC_KERNEL_CLUSTER, MHC_KERNEL_GRID, MHC_KERNEL_RESIDENT
+    return {"grid": {"kernel": MHC_KERNEL_GRID}, "cluster": {"kernel": MHC_KERNEL_CLUSTER},
+            "resident": {"kernel": MHC_KERNEL_RESIDENT},
+            "resident2": {"kernel": MHC_KERNEL_RESIDENT, "tm_buffers": 2, "cluster": 16}}.get(path, {})
 
 
 def _run(case, path):
     from mhc_hyper_connection_gb300 import mhc_pre_last_kernel
-    want = {"grid": "mhc_pre_gw_kernel", "cluster": "mhc_pre_tc_kernel"}.get(path)
-    if path == "auto" and case.T > 512:
-        want = "mhc_pre_tc_kernel"
+    if path == "resident" and case.n != 4:
+        pytest.skip("the resident mode takes n = 4")
+    want = KERNEL_OF.get(path)
+    if path == "auto" and case.T > 512:     # resident mode from 4096 tokens at n = 4
+        want = "mhc_pre_tc_kernel_resident" if (case.T >= 4096 and case.n == 4) else "mhc_pre_tc_kernel"
     op, out = run_cuda(case, **launch_of(path))
     torch.cuda.synchronize()
     got = mhc_pre_last_kernel(op.handle)
@@ -37,7 +46,7 @@ def _run(case, path):
     return out
 
 
-PATHS = ["auto", "cluster", "grid"]
+PATHS = ["auto", "cluster", "grid", "resident"]
 
 
 @pytest.mark.parametrize("path", PATHS)
@@ -69,14 +78,14 @@ def test_grid_path_deterministic(cuda_device):
         assert torch.equal(a[k], b[k]), k
 
 
-@pytest.mark.parametrize("path", ["cluster", "grid"])
+@pytest.mark.parametrize("path", ["cluster", "grid", "resident", "resident2"])
 @pytest.mark.parametrize("x_dtype", [torch.bfloat16, torch.float16])
 def test_repeated_runs_bitwise(cuda_device, path, x_dtype):
     """Twenty runs of one input agree bit for bit on every output: the
     reductions run in a fixed order, so any difference is a read of a
     buffer before its data is in (or after it is reused)."""
-    if x_dtype == torch.float16 and path != "cluster":
-        pytest.skip("fp16 x runs on the 64-token cluster kernel only")
+    if x_dtype == torch.float16 and path == "grid":
+        pytest.skip("fp16 x runs on the cluster kernel (plain or resident) only")
     case = make_case("training", device=cuda_device, x_dtype=x_dtype)
     op, ref = run_cuda(case, **launch_of(path))
     torch.cuda.synchronize()
@@ -131,5 +140,47 @@ def test_random_shapes(cuda_device, cfg):
     seed = cfg.pop("seed")
     case = make_case("tiny", device=cuda_device, seed=seed, **cfg)
     op, out = run_cuda(case, **launch_of(path))
+    torch.cuda.synchronize()
+    compare(case, out, run_oracle(case))
+
+
+@pytest.mark.parametrize("bufs", [1, 2])
+@pytest.mark.parametrize("cluster", [1, 2, 4, 8, 16])
+@pytest.mark.parametrize("mode", [0, 1])
+def test_resident_cluster_sizes(cuda_device, cluster, mode, bufs):
+    """Resident mode at every cluster size: 16 d-chunks per stream split over
+    the cluster, so a CTA keeps 1 .. 4 (fp32 mode) or 1 .. 6 (tf32 mode)
+    chunks in tensor memory (in one buffer, or half as many per tile in two
+    buffers used by alternate tiles) and re-reads the rest, if any, from L2;
+    ragged token count, backward outputs, gamma."""
+    from mhc_hyper_connection_gb300 import mhc_pre_last_kernel, mhc_pre_last_launch
+    case = make_case("tiny", device=cuda_device, T=333, D=1024, impl_mode=mode, need_backward=True, gamma=True)
+    op, out = run_cuda(case, cluster=cluster, tm_buffers=bufs, **launch_of("resident"))
+    torch.cuda.synchronize()
+    assert mhc_pre_last_kernel(op.handle) == "mhc_pre_tc_kernel_resident"
+    assert mhc_pre_last_launch(op.handle)[1]["cluster"] == cluster
+    compare(case, out, run_oracle(case))
+
+
+@pytest.mark.parametrize("D", [16, 80, 592, 7168])
+@pytest.mark.parametrize("x_dtype", [torch.bfloat16, torch.float16])
+def test_resident_widths(cuda_device, D, x_dtype):
+    """Resident mode on ragged widths (the last chunk partly past D) and the
+    prefill width, both x types."""
+    case = make_case("tiny", device=cuda_device, T=200, D=D, x_dtype=x_dtype, need_backward=True)
+    op, out = run_cuda(case, **launch_of("resident"))
+    torch.cuda.synchronize()
+    compare(case, out, run_oracle(case))
+
+
+@pytest.mark.parametrize("cfg", _random_configs(count=12, seed=7102026), ids=lambda c: "T{T}_D{D}_a{alpha_len}_m{impl_mode}".format(**c))
+def test_random_shapes_resident(cuda_device, cfg):
+    """Seeded random shapes (n = 4) on the resident mode, in full."""
+    cfg = dict(cfg)
+    cfg.pop("path")
+    seed = cfg.pop("seed")
+    cfg["n"] = 4
+    case = make_case("tiny", device=cuda_device, seed=seed, **cfg)
+    op, out = run_cuda(case, **launch_of("resident"))
     torch.cuda.synchronize()
     compare(case, out, run_oracle(case))

@@ -4,7 +4,8 @@ out its last x copy (nothing is issued for it, so no copy is in flight) and
 shortens the wait limit.  The waits on that copy give up, the kernel winds
 down through its abort path, mhc_pre_status reports MHC_ERR_RUNTIME (the
 MhcPreSinkhorn page's 361001), and the same handle's next normal run matches
-the oracle -- on the cluster kernel and on the grid-wide kernel."""
+the oracle -- on the cluster kernel, its resident mode and the grid-wide
+kernel."""
 import pytest
 import torch
 
@@ -21,10 +22,11 @@ def built():
 
 
 @pytest.mark.parametrize("path,name,T", [("cluster", "tiny", 300), ("cluster", "decode", 64),
-                                         ("grid", "decode", 64), ("grid", "tiny", 700)])
+                                         ("grid", "decode", 64), ("grid", "tiny", 700),
+                                         ("resident", "tiny", 300), ("resident", "decode", 640)])
 def test_wait_gives_up_then_next_run_is_clean(cuda_device, path, name, T):
     import mhc_hyper_connection_gb300 as mp
-    kernel = {"cluster": mp.MHC_KERNEL_CLUSTER, "grid": mp.MHC_KERNEL_GRID}[path]
+    kernel = {"cluster": mp.MHC_KERNEL_CLUSTER, "grid": mp.MHC_KERNEL_GRID, "resident": mp.MHC_KERNEL_RESIDENT}[path]
     case = make_case(name, device=cuda_device, T=T, D=1024 if name == "tiny" else None)
     op = make_op(case, kernel=kernel)
     out = op.allocate(case.T, cuda_device)
@@ -35,7 +37,8 @@ def test_wait_gives_up_then_next_run_is_clean(cuda_device, path, name, T):
     assert "gave up" in mp.last_error()
     word = int(out["workspace"][:4].view(torch.int32).item())
     assert word != 0 and (word & 8) == 0                # a wait bit, not the fp16 range bit
-    assert mp.mhc_pre_last_kernel(op.handle) == {"cluster": "mhc_pre_tc_kernel", "grid": "mhc_pre_gw_kernel"}[path]
+    assert mp.mhc_pre_last_kernel(op.handle) == {"cluster": "mhc_pre_tc_kernel", "grid": "mhc_pre_gw_kernel",
+                                                  "resident": "mhc_pre_tc_kernel_resident"}[path]
 
     assert mp.mhc_pre_set_wait_test(op.handle, 0, 0) == mp.MHC_OK
     op.run(case.x, case.phi, case.alpha, case.bias, out)
