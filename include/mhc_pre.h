@@ -148,6 +148,10 @@ typedef struct {
     float       *norm_out;  /* fp32 [2I, T, n, n]} need_backward == 0: all NULL       */
     void        *workspace;       /* device scratch, >= mhc_pre_workspace_size bytes   */
     size_t       workspace_bytes; /* its size                                          */
+    const void  *weights;   /* NULL, or phi (.) gamma prepared by
+                               mhc_pre_prepare_weights with this handle: the run
+                               then uses it and neither reads phi nor gamma (they
+                               may be NULL) nor launches the preparation          */
 } mhc_pre_args;
 
 /* Fill *cfg with the defaults listed above.  NULL cfg is ignored. */
@@ -162,6 +166,27 @@ MHC_API mhc_status_t mhc_pre_create(mhc_pre_t *out, const mhc_pre_config *cfg);
  * pages' two-phase call).  Depends on the handle's shape and mode and on T;
  * T == 0 gives 0.  MHC_ERR_NULLPTR / MHC_ERR_PARAM_INVALID (T < 0). */
 MHC_API mhc_status_t mhc_pre_workspace_size(mhc_pre_t h, int64_t T, size_t *bytes);
+
+/* Weights phase, for calls that reuse one phi and gamma (the decode steps of
+ * a layer): the projection's weight side, phi (.) gamma split into the
+ * precision planes the tensor cores read, depends on phi, gamma and the
+ * handle's n, D, alpha_len, impl_mode and x_dtype only.  mhc_pre_weights_size
+ * gives the bytes of that form (a 256-byte header, then the planes);
+ * mhc_pre_prepare_weights writes it into `weights` (a caller-owned device
+ * buffer, 256-byte aligned, at least that size) on `stream`.  A run given
+ * args->weights then skips its own preparation launch: one copy of the
+ * 256-byte header into the workspace and one kernel.  The buffer stays
+ * valid until phi or gamma change; it must come from a handle with the same
+ * n, D, alpha_len, impl_mode and x_dtype.  fp16 x: an entry of phi (.) gamma
+ * beyond fp16's range is recorded in the buffer's header and reported by
+ * mhc_pre_status after each run that uses it.  The pages' operator
+ * re-derives nothing per call either: its weight-side tiling is fixed at
+ * set-up (the MhcPreV2 page, §十).  MHC_ERR_NULLPTR for a NULL handle,
+ * bytes, phi or weights; MHC_ERR_PARAM_INVALID for misalignment or a small
+ * buffer; MHC_ERR_RUNTIME if the launch fails. */
+MHC_API mhc_status_t mhc_pre_weights_size(mhc_pre_t h, size_t *bytes);
+MHC_API mhc_status_t mhc_pre_prepare_weights(mhc_pre_t h, const float *phi, const float *gamma, void *weights,
+                                             size_t weights_bytes, void *stream);
 
 /* Second phase: check args, then enqueue the forward on `stream` (a
  * cudaStream_t; NULL = legacy default stream).  Host-side checks return

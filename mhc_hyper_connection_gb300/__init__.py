@@ -11,5 +11,5 @@ from ._binding import (  # noqa: F401
     MHC_IMPL_TF32, MHC_OK, MhcError, MhcPre, MhcPreArgs, MhcPreBwdArgs, MhcPreConfig, hc_post, last_error,
     library, mhc_post_run, mhc_pre_backward_run, mhc_pre_backward_workspace_size, mhc_pre_inv_rms_run,
     mhc_pre_mixes_run, mhc_pre_sinkhorn_run,
-    mhc_pre_config_default, mhc_pre_create, mhc_pre_destroy, mhc_pre_last_kernel, mhc_pre_last_launch, mhc_pre_run, mhc_pre_run_noalloc, mhc_pre_set_profile_events, mhc_pre_set_wait_test, mhc_pre_status,
+    mhc_pre_config_default, mhc_pre_create, mhc_pre_destroy, mhc_pre_last_kernel, mhc_pre_last_launch, mhc_pre_run, mhc_pre_run_noalloc, mhc_pre_set_profile_events, mhc_pre_set_wait_test, mhc_pre_status, mhc_pre_weights_size, mhc_pre_prepare_weights,
     mhc_pre_workspace_size, status_string)

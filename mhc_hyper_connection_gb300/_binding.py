@@ -50,7 +50,7 @@ class MhcPreArgs(ctypes.Structure):
     _fields_ = [("T", ctypes.c_int64), ("x", _P), ("phi", _P), ("alpha", _P), ("bias", _P),
                 ("gamma", _P), ("pre_mix", _P), ("y", _P), ("h_post", _P), ("h_res", _P),
                 ("h_pre", _P), ("inv_rms", _P), ("h_mix", _P), ("sum_out", _P),
-                ("norm_out", _P), ("workspace", _P), ("workspace_bytes", ctypes.c_size_t)]
+                ("norm_out", _P), ("workspace", _P), ("workspace_bytes", ctypes.c_size_t), ("weights", _P)]
 
 
 class MhcPreBwdArgs(ctypes.Structure):
@@ -94,6 +94,10 @@ def library() -> ctypes.CDLL:
             lib.mhc_pre_run_noalloc.restype = ctypes.c_int32
             lib.mhc_pre_status.argtypes = [_P, _P, _P]
             lib.mhc_pre_status.restype = ctypes.c_int32
+            lib.mhc_pre_weights_size.argtypes = [_P, ctypes.POINTER(ctypes.c_size_t)]
+            lib.mhc_pre_weights_size.restype = ctypes.c_int32
+            lib.mhc_pre_prepare_weights.argtypes = [_P, _P, _P, _P, ctypes.c_size_t, _P]
+            lib.mhc_pre_prepare_weights.restype = ctypes.c_int32
             lib.mhc_pre_set_wait_test.argtypes = [_P, ctypes.c_uint32, ctypes.c_int32]
             lib.mhc_pre_set_wait_test.restype = ctypes.c_int32
             lib.mhc_pre_set_profile_events.argtypes = [_P, _P, _P]
@@ -157,6 +161,17 @@ def mhc_pre_run_noalloc(handle, args: MhcPreArgs, stream: int = 0) -> int:
 
 def mhc_pre_status(handle, workspace: int = 0, stream: int = 0) -> int:
     return library().mhc_pre_status(handle, _P(workspace or None), _P(stream or None))
+
+
+def mhc_pre_weights_size(handle):
+    """Returns (status, bytes of the prepared-weights form)."""
+    n = ctypes.c_size_t(0)
+    st = library().mhc_pre_weights_size(handle, ctypes.byref(n))
+    return st, n.value
+
+
+def mhc_pre_prepare_weights(handle, phi: int, gamma: int, weights: int, weights_bytes: int, stream: int = 0) -> int:
+    return library().mhc_pre_prepare_weights(handle, phi, gamma, weights, weights_bytes, stream)
 
 
 def mhc_pre_set_wait_test(handle, wait_limit_us: int = 0, withhold_last_x_copy: int = 0) -> int:
@@ -337,7 +352,24 @@ class MhcPre:
         out["workspace"] = torch.zeros((max(ws, 256),), dtype=torch.uint8, device=device)
         return out
 
-    def make_args(self, x, phi, alpha, bias, out, gamma=None, pre_mix=None) -> MhcPreArgs:
+    def prepare_weights(self, phi, gamma=None, stream=None):
+        """phi (.) gamma in the form a run takes as `weights` (a uint8 tensor on
+        phi's device), for repeated calls with the same weights."""
+        import torch
+        st, nbytes = mhc_pre_weights_size(self.handle)
+        if st != MHC_OK:
+            raise MhcError(st, "mhc_pre_weights_size", last_error())
+        w = torch.empty((nbytes,), dtype=torch.uint8, device=phi.device)
+        if stream is None:
+            stream = torch.cuda.current_stream(phi.device).cuda_stream
+        elif hasattr(stream, "cuda_stream"):
+            stream = stream.cuda_stream
+        st = mhc_pre_prepare_weights(self.handle, _ptr(phi), _ptr(gamma), _ptr(w), nbytes, int(stream))
+        if st != MHC_OK:
+            raise MhcError(st, "mhc_pre_prepare_weights", last_error())
+        return w
+
+    def make_args(self, x, phi, alpha, bias, out, gamma=None, pre_mix=None, weights=None) -> MhcPreArgs:
         a = MhcPreArgs()
         a.T = _tokens(x.shape[:-2]) if x is not None else 0
         a.x, a.phi, a.alpha, a.bias = _ptr(x), _ptr(phi), _ptr(alpha), _ptr(bias)
@@ -347,12 +379,14 @@ class MhcPre:
         ws = out.get("workspace")
         a.workspace = _ptr(ws)
         a.workspace_bytes = 0 if ws is None else ws.numel() * ws.element_size()
+        a.weights = _ptr(weights)
         return a
 
-    def run(self, x, phi, alpha, bias, out, gamma=None, pre_mix=None, stream=None):
+    def run(self, x, phi, alpha, bias, out, gamma=None, pre_mix=None, stream=None, weights=None):
         """Enqueue the forward on `stream` (torch stream or raw handle; default:
-        torch's current stream).  Raises MhcError on a host-side rejection."""
-        args = self.make_args(x, phi, alpha, bias, out, gamma, pre_mix)
+        torch's current stream).  `weights` (from prepare_weights) replaces
+        phi and gamma.  Raises MhcError on a host-side rejection."""
+        args = self.make_args(x, phi, alpha, bias, out, gamma, pre_mix, weights)
         if stream is None:
             import torch
             stream = torch.cuda.current_stream(x.device).cuda_stream

@@ -375,8 +375,10 @@ mhc_status_t mhc_pre_run(mhc_pre_t h, const mhc_pre_args* a, void* stream) {
   const int64_t T = a->T;
   if (T < 0 || T > (int64_t(1) << 30)) return fail(MHC_ERR_PARAM_INVALID, "T must be in [0, 2^30]");
   if (T == 0) return MHC_OK;   // empty input: nothing to check or launch (pointers may be NULL)
-  if (!a->x || !a->phi || !a->alpha || !a->bias || !a->y || !a->h_post)
-    return fail(MHC_ERR_NULLPTR, "x, phi, alpha, bias, y and h_post are required");
+  if (!a->x || (!a->phi && !a->weights) || !a->alpha || !a->bias || !a->y || !a->h_post)
+    return fail(MHC_ERR_NULLPTR, "x, phi (or weights), alpha, bias, y and h_post are required");
+  if (a->weights && !aligned(a->weights, 256))
+    return fail(MHC_ERR_PARAM_INVALID, "weights must be 256-byte aligned");
   if (c.alpha_len == 3 && !a->h_res) return fail(MHC_ERR_NULLPTR, "h_res is required with alpha of length 3");
   if (a->pre_mix && !a->h_pre) return fail(MHC_ERR_NULLPTR, "h_pre is required when pre_mix is given");
   if (c.need_backward) {
@@ -414,6 +416,13 @@ mhc_status_t mhc_pre_run(mhc_pre_t h, const mhc_pre_args* a, void* stream) {
   __nv_bfloat16* planes = reinterpret_cast<__nv_bfloat16*>(ws + mhc::kWsHeader);
 
   // 1. phi (x gamma) -> stacked bf16 precision planes; clears the error word.
+  //    With prepared weights: their header (zeroed, or the fp16 range bit)
+  //    becomes the workspace header and their planes are used as they are.
+  if (a->weights) {
+    planes = reinterpret_cast<__nv_bfloat16*>(static_cast<uint8_t*>(const_cast<void*>(a->weights)) + mhc::kWsHeader);
+    const cudaError_t ce = cudaMemcpyAsync(ws, a->weights, mhc::kWsHeader, cudaMemcpyDeviceToDevice, s);
+    if (ce != cudaSuccess) return fail(MHC_ERR_RUNTIME, "copying the weights header failed: %s", cudaGetErrorString(ce));
+  }
   mhc::PlaneParams pp;
   pp.phi = a->phi;
   pp.gamma = a->gamma;
@@ -428,7 +437,7 @@ mhc_status_t mhc_pre_run(mhc_pre_t h, const mhc_pre_args* a, void* stream) {
   pp.fp16 = (c.x_dtype == MHC_DTYPE_FP16);
   pp.vec16 = aligned(a->phi, 16) && (!a->gamma || aligned(a->gamma, 16));
   pp.err_word = err;
-  if (mhc::launch_prepare_planes(pp, s) != cudaSuccess)
+  if (!a->weights && mhc::launch_prepare_planes(pp, s) != cudaSuccess)
     return fail(MHC_ERR_RUNTIME, "plane preparation launch failed: %s", cudaGetErrorString(cudaGetLastError()));
 
   // 2. the fused forward.  The grid-wide kernel spreads a few token tiles
@@ -663,6 +672,48 @@ mhc_status_t mhc_pre_run_noalloc(mhc_pre_t h, const mhc_pre_args* a, void* strea
   const mhc_status_t rs = mhc_pre_run(h, &b, stream);
   if (rs == MHC_OK) h->last_noalloc_word = scratch;   // mhc_pre_status(h, NULL, s) reads it there
   return rs;
+}
+
+mhc_status_t mhc_pre_weights_size(mhc_pre_t h, size_t* bytes) {
+  g_last_error[0] = 0;
+  if (!h || !bytes) return fail(MHC_ERR_NULLPTR, "handle and bytes must be non-NULL");
+  *bytes = mhc::kWsHeader + planes_bytes(h);
+  return MHC_OK;
+}
+
+mhc_status_t mhc_pre_prepare_weights(mhc_pre_t h, const float* phi, const float* gamma, void* weights,
+                                     size_t weights_bytes, void* stream) {
+  g_last_error[0] = 0;
+  if (!h || !phi || !weights) return fail(MHC_ERR_NULLPTR, "handle, phi and weights must be non-NULL");
+  if (!aligned(weights, 256)) return fail(MHC_ERR_PARAM_INVALID, "weights must be 256-byte aligned");
+  if (!aligned(phi, 4) || (gamma && !aligned(gamma, 4)))
+    return fail(MHC_ERR_PARAM_INVALID, "phi and gamma must be 4-byte aligned");
+  size_t need = 0;
+  mhc_pre_weights_size(h, &need);
+  if (weights_bytes < need)
+    return fail(MHC_ERR_PARAM_INVALID, "weights buffer too small: %zu < %zu bytes", weights_bytes, need);
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return fail(MHC_ERR_RUNTIME, "no CUDA device");
+  if (!device_info(dev).ok) return fail(MHC_ERR_RUNTIME, "device %d is not an sm_103 GPU", dev);
+  const mhc_pre_config& c = h->cfg;
+  uint8_t* wb = static_cast<uint8_t*>(weights);
+  mhc::PlaneParams pp;
+  pp.phi = phi;
+  pp.gamma = gamma;
+  pp.planes = reinterpret_cast<__nv_bfloat16*>(wb + mhc::kWsHeader);
+  pp.R = h->R;
+  pp.P = h->P;
+  pp.n = (int)c.n;
+  pp.D = (int)c.D;
+  pp.nch = (int)((c.D + mhc::kChunkK - 1) / mhc::kChunkK);
+  pp.RB = mhc::plane_box_rows(h->R, h->P);
+  pp.tf32 = (c.impl_mode == MHC_IMPL_TF32);
+  pp.fp16 = (c.x_dtype == MHC_DTYPE_FP16);
+  pp.vec16 = aligned(phi, 16) && (!gamma || aligned(gamma, 16));
+  pp.err_word = reinterpret_cast<uint32_t*>(wb);   // the header: zeroed, or the fp16 range bit
+  if (mhc::launch_prepare_planes(pp, static_cast<cudaStream_t>(stream)) != cudaSuccess)
+    return fail(MHC_ERR_RUNTIME, "plane preparation launch failed: %s", cudaGetErrorString(cudaGetLastError()));
+  return MHC_OK;
 }
 
 mhc_status_t mhc_pre_set_wait_test(mhc_pre_t h, uint32_t wait_limit_us, int32_t withhold_last_x_copy) {

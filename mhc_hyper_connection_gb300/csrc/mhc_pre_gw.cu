@@ -97,13 +97,15 @@ __device__ __noinline__ void gw_fail(const GwCtl& c, uint32_t code) {
 }
 
 // Wait for phase `parity` of a local mbarrier; gives up after c.wait_ns or
-// as soon as this CTA or any other has given up.
+// as soon as this CTA or any other has given up.  A waiting thread sleeps in
+// the barrier (woken when the phase completes), so waiting warps leave the
+// issue slots to the working ones.
 __device__ __noinline__ bool gw_wait(uint64_t* bar, uint32_t parity, const GwCtl& c) {
   if (mbar_test(bar, parity)) return true;
   const uint64_t t0 = now_ns();
   for (uint32_t it = 1;; ++it) {
-    if (mbar_test(bar, parity)) return true;
-    if ((it & 63u) == 0) {
+    if (mbar_test_sleep(bar, parity, 1000u)) return true;
+    if ((it & 7u) == 0) {
       if (*c.abort || *c.gabort) {
         *c.abort = 1u;
         return false;
@@ -539,6 +541,13 @@ __global__ void __launch_bounds__(kGwThreads, 1)
     for (int q = 0; q < batches; ++q) {
       const int sb = q & 1;
       if (!warp_wait(&tail->sink_full[sb], (uint32_t)(q >> 1) & 1u, ctl)) break;
+      int total = 0;                               // tokens this CTA owns in the batch
+      for (int mt = 0; mt < SB && q * SB + mt < my_tiles; ++mt) total += sink_cnt[sb * kGwSinkMax + mt];
+      if (total == 0) {
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&tail->sink_free[sb]);
+        continue;
+      }
       const int mt = lane / g.own_max, o = lane - mt * g.own_max;   // lane -> (tile of batch, token)
       const int m = q * SB + mt;
       if (mt < SB && m < my_tiles && o < sink_cnt[sb * kGwSinkMax + mt]) {
@@ -569,7 +578,19 @@ __global__ void __launch_bounds__(kGwThreads, 1)
       __syncwarp();                                // the lanes' reads below follow lane 0's acquire
       const float* csrc = gcoef + (size_t)slot * kGwTile * NS;
       float* cdst = ycoef + (size_t)b * kGwTile * NS;
-      for (int e = lane; e < valid * NS; e += 32) cdst[e] = __ldcg(csrc + e);
+      // every load in flight before the first store (one round trip)
+      constexpr int kPer = (kGwTile * NS + 31) / 32;
+      float cv[kPer];
+#pragma unroll
+      for (int q = 0; q < kPer; ++q) {
+        const int e = lane + 32 * q;
+        cv[q] = e < valid * NS ? __ldcg(csrc + e) : 0.0f;
+      }
+#pragma unroll
+      for (int q = 0; q < kPer; ++q) {
+        const int e = lane + 32 * q;
+        if (e < valid * NS) cdst[e] = cv[q];
+      }
       __syncwarp();
       if (lane == 0) {
         mbar_arrive(&tail->ycoef_full[b]);

@@ -46,7 +46,7 @@ def test_library_exports_every_declared_symbol(lib):
 def test_struct_layouts_match_header():
     # Field order/sizes in the binding mirror the header (x86-64 and aarch64 LP64).
     assert ctypes.sizeof(mp.MhcPreConfig) == 8 + 8 + 4 + 4 + 8 + 8 + 4 + 4 + 4 + 4 + 8 * 4
-    assert ctypes.sizeof(mp.MhcPreArgs) == 8 + 15 * 8 + 8
+    assert ctypes.sizeof(mp.MhcPreArgs) == 8 + 15 * 8 + 8 + 8
     assert ctypes.sizeof(mp.MhcPreBwdArgs) == 8 + 20 * 8 + 8
 
 
@@ -140,6 +140,28 @@ def test_workspace_size(lib):
     assert mp.mhc_pre_workspace_size(h2, 64)[1] == 256 + 4 * 4 * 48 * 128 + rings
     mp.mhc_pre_destroy(h)
     mp.mhc_pre_destroy(h2)
+
+
+def test_weights_phase_host_checks(lib):
+    h = _handle()
+    st, nb = mp.mhc_pre_weights_size(h)
+    assert st == 0 and nb == 256 + 4 * 4 * 72 * 128          # header + the planes (D = 256)
+    assert mp.mhc_pre_weights_size(None)[0] == mp.MHC_ERR_NULLPTR
+    fake = 1 << 20
+    assert mp.mhc_pre_prepare_weights(h, 0, 0, fake, nb) == mp.MHC_ERR_NULLPTR        # no phi
+    assert mp.mhc_pre_prepare_weights(h, fake, 0, 0, nb) == mp.MHC_ERR_NULLPTR        # no buffer
+    assert mp.mhc_pre_prepare_weights(h, fake, 0, fake + 16, nb) == mp.MHC_ERR_PARAM_INVALID   # alignment
+    assert mp.mhc_pre_prepare_weights(h, fake, 0, fake, nb - 1) == mp.MHC_ERR_PARAM_INVALID    # too small
+    # without a GPU the checks pass and the launch fails loudly
+    assert mp.mhc_pre_prepare_weights(h, fake, 0, fake, nb) == mp.MHC_ERR_RUNTIME
+    # a run given weights needs no phi; misaligned weights are refused
+    a = _args(phi=0)
+    assert lib.mhc_pre_run(h, ctypes.byref(a), None) == mp.MHC_ERR_NULLPTR
+    a = _args(phi=0, weights=fake + 16)
+    assert lib.mhc_pre_run(h, ctypes.byref(a), None) == mp.MHC_ERR_PARAM_INVALID
+    a = _args(phi=0, weights=fake)
+    assert lib.mhc_pre_run(h, ctypes.byref(a), None) == mp.MHC_ERR_RUNTIME
+    mp.mhc_pre_destroy(h)
 
 
 def _args(T=64, **over):
