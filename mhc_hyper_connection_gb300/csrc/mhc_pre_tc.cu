@@ -73,7 +73,10 @@ struct Cfg {
   static_assert(kMmaN % 16 == 0 && kMmaN <= 256, "M = 128 takes N = 16 .. 256 in steps of 16");
   static constexpr int kStr = partial_stride(RR);                // floats per published partial
   static constexpr bool kThree = (RR == NS * NS + 2 * NS);
-  static constexpr int kYBatch = NS <= 4 ? 4 : 2;               // y items in flight per thread
+  // y items in flight per thread (re-read loads: 3 x NS x 16 B).  Four
+  // measured the same at cluster 4 and 2% slower in tf32 mode and at cluster
+  // 8; six spill.
+  static constexpr int kYBatch = NS <= 4 ? 3 : 2;
 };
 
 struct SmemTail {
