@@ -51,8 +51,8 @@ constexpr int kGwYcWarps = kGwThreads / 32 - kGwWarpYc0;   // 7
 constexpr int kGwYcThreads = kGwYcWarps * 32;              // 224
 constexpr int kGwGateWarps = 2;
 constexpr int kGwPubRing = 4;                              // publish -> signaller hand-off depth
-// Named barrier 1: the publish warps.
-constexpr int kGwBarPub = 1;
+// Named barriers: 1 = the publish warps, 2 = the two gate warps.
+constexpr int kGwBarPub = 1, kGwBarGate = 2;
 
 template <int NS, int RR, int P>
 struct GwCfg {
@@ -80,6 +80,7 @@ struct GwTail {
   uint64_t mma_done;
   uint32_t tmem_base;
   uint32_t abort;
+  float gate_half[96];                // single-tile runs: the second gate warp's half sum of a row
 };
 static_assert(sizeof(GwTail) <= kTailBytes, "barrier block outgrew its reservation");
 
@@ -447,7 +448,11 @@ __global__ void __launch_bounds__(kGwThreads, 1)
   } else if (warp == kGwWarpGate0 || warp == kGwWarpGate0 + 1) {
     // ================================================= gates of the tokens this CTA owns
     const int gidx = warp - kGwWarpGate0;
-    for (int m = gidx; m < my_tiles; m += kGwGateWarps) {
+    // With one tile (decode sizes) the other gate warp has nothing to do:
+    // both take tile 0, each adds half of a row's partials (one pass of
+    // loads each) and the first adds the second's half, in that order.
+    const bool split = my_tiles == 1;
+    for (int m = split ? 0 : gidx; m < my_tiles; m += kGwGateWarps) {
       const int k = grp + m * g.ng;
       const int tile0 = k * kGwTile;
       const int valid = min(kGwTile, g.T - tile0);
@@ -470,26 +475,30 @@ __global__ void __launch_bounds__(kGwThreads, 1)
           ok = gw_wait_count(&arrive[slot], (use + 1u) * (uint32_t)G, ctl);
           if (ok && use > 0 && yd < use * (uint32_t)G) ok = gw_wait_count(&ydone[slot], use * (uint32_t)G, ctl);
         }
-        if (!__shfl_sync(0xffffffffu, ok ? 1 : 0, 0)) break;
+        // both warps of a split pair leave together if either gave up
+        if (split ? !role_all<kGwBarGate, 64>(ok) : !__shfl_sync(0xffffffffu, ok ? 1 : 0, 0)) break;
         __syncwarp();                              // the lanes' reads below follow lane 0's acquire
+        const int c_lo = split ? gidx * ((G + 1) / 2) : 0;
+        const int c_hi = split ? min(G, (gidx + 1) * ((G + 1) / 2)) : G;
         for (int t = first; t < valid; t += G, ++cnt) {
           // Sum the CTAs' partials of row t in a fixed order: lane l adds
-          // CTAs l, l + 32, ... then a fixed butterfly adds the lanes.
+          // CTAs c_lo + l, c_lo + l + 32, ... then a fixed butterfly adds the
+          // lanes.
           const float* src = gpart + ((size_t)slot * kGwTile + t) * G * C::kStr;
           float acc[C::kStr];
 #pragma unroll
           for (int e = 0; e < C::kStr; ++e) acc[e] = 0.0f;
-          for (int rd0 = 0; rd0 * 32 < G; rd0 += C::kRounds) {
+          for (int rd0 = 0; c_lo + rd0 * 32 < c_hi; rd0 += C::kRounds) {
             // kRounds rounds of CTAs per pass: every load of the pass is
             // issued before the first add
             float4 v[C::kRounds][C::kG4];
 #pragma unroll
             for (int h = 0; h < C::kRounds; ++h) {
-              const int c = lane + 32 * (rd0 + h);
-              const float4* s4 = reinterpret_cast<const float4*>(src + (size_t)(c < G ? c : 0) * C::kStr);
+              const int c = c_lo + lane + 32 * (rd0 + h);
+              const float4* s4 = reinterpret_cast<const float4*>(src + (size_t)(c < c_hi ? c : 0) * C::kStr);
 #pragma unroll
               for (int q4 = 0; q4 < C::kG4; ++q4)
-                v[h][q4] = c < G ? __ldcg(s4 + q4) : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+                v[h][q4] = c < c_hi ? __ldcg(s4 + q4) : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
             }
 #pragma unroll
             for (int h = 0; h < C::kRounds; ++h) {
@@ -507,25 +516,41 @@ __global__ void __launch_bounds__(kGwThreads, 1)
 #pragma unroll
             for (int e = 0; e <= RR; ++e) acc[e] += __shfl_xor_sync(0xffffffffu, acc[e], off);
           }
+          if (split) {
+            if (gidx == 1 && lane == 0) {
+#pragma unroll
+              for (int e = 0; e <= RR; ++e) tail->gate_half[e] = acc[e];
+            }
+            role_sync<kGwBarGate, 64>();           // the second half is in
+            if (gidx == 0 && lane == 0) {
+#pragma unroll
+              for (int e = 0; e <= RR; ++e) acc[e] += tail->gate_half[e];
+            }
+            role_sync<kGwBarGate, 64>();           // and read before the next row overwrites it
+            if (gidx == 1) continue;
+          }
           if (lane == 0) {
+            // gates and logits first: the Sinkhorn warp may start as soon as
+            // the tile's logits are in; the y weights are counted ready once
+            // for the tile, after the loop
             float mix[RR];
 #pragma unroll
             for (int e = 0; e < RR; ++e) mix[e] = acc[e];
             const int tok = tile0 + t;
             float cf[NS];
             const float inv_rms = token_gates<NS, RR>(ep, tok, mix, acc[RR], true, cf);
-            float* cdst = gcoef + ((size_t)slot * kGwTile + t) * NS;
-#pragma unroll
-            for (int i = 0; i < NS; ++i) __stcg(cdst + i, cf[i]);
-            red_release_gpu(&ready[slot], 1u);
             float H[NN];
             residual_logits<NS, RR>(ep, mix, inv_rms, H);
             float* eb = sink_buf + ((size_t)sb * kGwSinkMax + e0 + cnt) * NN;
 #pragma unroll
             for (int i = 0; i < NN; ++i) eb[i] = H[i];
+            float* cdst = gcoef + ((size_t)slot * kGwTile + t) * NS;
+#pragma unroll
+            for (int i = 0; i < NS; ++i) __stcg(cdst + i, cf[i]);
           }
         }
       }
+      if (split && gidx == 1) break;               // the helper warp is done
       __syncwarp();
       if (lane == 0) {
         sink_cnt[sb * kGwSinkMax + (m - q * SB)] = cnt;
@@ -533,6 +558,8 @@ __global__ void __launch_bounds__(kGwThreads, 1)
         if (m == my_tiles - 1) {             // a short last batch: complete its phase
           for (int extra = m - q * SB + 1; extra < SB; ++extra) mbar_arrive(&tail->sink_full[sb]);
         }
+        // this tile's y weights, stored above, become visible with the count
+        if (cnt > 0) red_release_gpu(&ready[slot], (uint32_t)cnt);
       }
     }
   } else if (warp == kGwWarpSink) {
