@@ -222,6 +222,14 @@ __device__ __forceinline__ void token_sinkhorn(const EpiParams& p, int t, const 
 #pragma unroll
       for (int e = 0; e < NN; ++e) p.norm_out[Tnn + (size_t)t * NN + e] = P[e];
     }
+    // without the backward's outputs the steps run with no stores between
+    // them (the same arithmetic, a tighter loop)
+    if (!wb) {
+      for (int it = 1; it < p.num_iters; ++it) {
+        sinkhorn_row<NS>(P, hc_eps, false, nullptr);
+        sinkhorn_col<NS>(P, hc_eps, false, nullptr);
+      }
+    } else
     for (int it = 1; it < p.num_iters; ++it) {
       const int k = 2 * it;
       sinkhorn_row<NS>(P, hc_eps, wb, wb ? sums + k * Tn + (size_t)t * NS : nullptr);
