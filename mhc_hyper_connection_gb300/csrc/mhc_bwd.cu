@@ -375,10 +375,10 @@ __global__ void __launch_bounds__(kBwTokenWarps * 32) bw_token_kernel(BwTokenPar
 }
 
 // ================================================================ main kernel
-// Warps: 0 TMA producer, 1 MMA issuer (and TMEM owner), 2 grad_x store,
-// 3..18 epilogue.  Epilogue warp e works on TMEM lane quarter (warp % 4),
-// M-group (e >> 3) and token half ((e >> 2) & 1) of each tile.
-constexpr int kWarpProd = 0, kWarpMma = 1, kWarpStore = 2, kWarpEpi0 = 3;
+// Warps: 0 TMA producer, 1 MMA issuer (and TMEM owner), 2..17 epilogue.
+// Epilogue warp e works on TMEM lane quarter (warp % 4), M-group (e >> 3)
+// and token half ((e >> 2) & 1) of each tile.
+constexpr int kWarpProd = 0, kWarpMma = 1, kWarpEpi0 = 2;
 constexpr int kEpiWarps = 16;
 constexpr int kMainThreads = (kWarpEpi0 + kEpiWarps) * 32;
 constexpr int kMaxStages = 4;
@@ -392,8 +392,8 @@ constexpr int kHalf = kBwTile / 2;                // tokens per epilogue warp
 constexpr int kPrefetch = MHC_BW_PREFETCH;        // tiles of L2 prefetch ahead of the copy
 
 struct MainTail {
-  uint64_t full[kMaxStages], empty[kMaxStages], out_ready[kMaxStages];
-  uint64_t a_full, a_free;
+  uint64_t full[kMaxStages], empty[kMaxStages];
+  uint64_t a_full, a_free, at_full;
   uint64_t d1_full[2], d1_empty[2];
   uint64_t mt_full, mt_empty;
   uint64_t mma_done;
@@ -414,22 +414,29 @@ __device__ __forceinline__ void product_planes(int q, int& gp, int& pp) {
 template <int P, bool kGxp>
 __global__ void __launch_bounds__(kMainThreads, 1)
     bw_main_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constant__ CUtensorMap tmap_gin,
-                   const __grid_constant__ CUtensorMap tmap_gx, const __grid_constant__ CUtensorMap tmap_gxp,
-                   const __nv_bfloat16* __restrict__ planes, const uint8_t* __restrict__ tiles,
-                   float* __restrict__ pieces, uint32_t* err, int ntiles, int nslab, int nq, int stages) {
+                   const __grid_constant__ CUtensorMap tmap_gxp, const __nv_bfloat16* __restrict__ planes,
+                   const uint8_t* __restrict__ tiles, float* __restrict__ pieces, __nv_bfloat16* __restrict__ gx,
+                   uint32_t* err, int T, int D, int ntiles, int nslab, int nq, int stages) {
   constexpr int kABlk = P * kBwPlaneBytes;            // one stream's block of the phi' slab
   constexpr int kABytes = kBwNS * kABlk;
   constexpr int kRec = bw_tile_rec_bytes(P);
   constexpr int kMtCols = bw_mt_cols(P);              // N of x^T G
   constexpr int kNQ = P == 3 ? 6 : 3;                 // plane products of G phi'
   constexpr int kMtCol0 = 2 * kGroups * kBwTile;      // after two D1 buffers
+  // fp32 mode (three planes) reads phi' planes 0 and 1 from tensor memory
+  // (five of the six plane products), which relieves the shared-memory
+  // port that the epilogue and the other operands share; with two planes
+  // (tf32 mode) the shared slab measured faster.
+  constexpr bool kTmA = P == 3;
+  constexpr int kAtCol0 = kMtCol0 + kGroups * kMtCols;  // phi' planes 0 and 1 as tensor-memory A operands
+  constexpr int kAtCols = 2 * kBwRp / 2;              // two planes of 32 rows, two bf16 per column
   constexpr uint32_t kTmemCols = 512;
   constexpr int kStageBytes = bw_stage_bytes(P, kGxp);
   // stage layout: x | grad_x_post (optional) | grad_h_in | tile record
   constexpr int offGxp = kXBytes;
   constexpr int offGin = kXBytes * (kGxp ? 2 : 1);
   constexpr int offRec = offGin + kGinBytes;
-  static_assert(kMtCol0 + kGroups * kMtCols <= (int)kTmemCols, "TMEM budget");
+  static_assert(kAtCol0 + kGroups * kAtCols <= (int)kTmemCols, "TMEM budget");
 
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -446,11 +453,11 @@ __global__ void __launch_bounds__(kMainThreads, 1)
   if (threadIdx.x == 0) {
     for (int s = 0; s < stages; ++s) {
       mbar_init(&tail->full[s], 1);
-      mbar_init(&tail->empty[s], 1);
-      mbar_init(&tail->out_ready[s], kEpiWarps);
+      mbar_init(&tail->empty[s], kEpiWarps + 1);    // the epilogue warps + the MMAs that read the slot
     }
     mbar_init(&tail->a_full, 1);
     mbar_init(&tail->a_free, 1);
+    mbar_init(&tail->at_full, 4);                  // one filling warp per TMEM lane quarter
     for (int b = 0; b < 2; ++b) {
       mbar_init(&tail->d1_full[b], 1);
       mbar_init(&tail->d1_empty[b], kEpiWarps);
@@ -462,7 +469,6 @@ __global__ void __launch_bounds__(kMainThreads, 1)
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     tma_prefetch_desc(&tmap_x);
     tma_prefetch_desc(&tmap_gin);
-    tma_prefetch_desc(&tmap_gx);
     if (kGxp) tma_prefetch_desc(&tmap_gxp);
   }
   if (warp == kWarpMma) {
@@ -527,6 +533,7 @@ __global__ void __launch_bounds__(kMainThreads, 1)
     if (lane == 0) {
       constexpr uint32_t idesc_mt = idesc_bf16_major(128, kMtCols, true, false);
       constexpr uint32_t idesc_d1 = idesc_bf16_major(128, kBwTile, true, true);
+      constexpr uint32_t idesc_d1_ta = idesc_bf16_major(128, kBwTile, false, true);
       const uint32_t a_addr = smem_u32(sA);
       int s = 0;
       uint32_t ph = 0;
@@ -538,19 +545,52 @@ __global__ void __launch_bounds__(kMainThreads, 1)
         const int t0 = (int)((long long)chunk * ntiles / nq), t1 = (int)((long long)(chunk + 1) * ntiles / nq);
         for (int tile = t0; tile < t1; ++tile, ++k) {
           const bool first = tile == t0, last = tile == t1 - 1;
-          if (!wait_bar_sleep(&tail->full[s], ph, ctl, kErrWaitTimeout)) { ok = false; break; }
-          if (first) {
-            if (!wait_bar_sleep(&tail->a_full, (uint32_t)piece & 1u, ctl, kErrWaitTimeout)) { ok = false; break; }
-            if (piece > 0 &&
-                !wait_bar_sleep(&tail->mt_empty, (uint32_t)(piece - 1) & 1u, ctl, kErrWaitTimeout)) {
-              ok = false;
-              break;
-            }
+          const int b = (int)(k & 1);
+          if (!wait_bar_sleep(&tail->full[s], ph, ctl, kErrWaitTimeout) ||
+              (first && !wait_bar_sleep(&tail->a_full, (uint32_t)piece & 1u, ctl, kErrWaitTimeout)) ||
+              (kTmA && first && !wait_bar_sleep(&tail->at_full, (uint32_t)piece & 1u, ctl, kErrWaitTimeout)) ||
+              !wait_bar_sleep(&tail->d1_empty[b], ((uint32_t)(k >> 1) & 1u) ^ 1u, ctl, kErrWaitTimeout)) {
+            ok = false;
+            break;
           }
           tc_fence_after();
           const uint32_t x_addr = smem_u32(sStage + (size_t)s * kStageBytes);
           const uint32_t gt_addr = x_addr + (uint32_t)offRec;
-          // x^T G: A = x tile seen MN-major (rows = tokens = K), B = G planes K-major
+          // G phi' first (the epilogue waits for it).  A = phi' planes 0 and
+          // 1 from tensor memory in fp32 mode (filled once per unit), else
+          // the shared slab MN-major (rows = gate rows = K); B = G planes
+          // MN-major with N = 64 tokens, one 128-byte row (its atom stride is
+          // unused)
+#pragma unroll
+          for (int g = 0; g < kGroups; ++g) {
+#pragma unroll
+            for (int q = 0; q < kNQ; ++q) {
+              int gp, pp;
+              product_planes(q, gp, pp);
+#pragma unroll
+              for (int ks = 0; ks < kBwRp / 16; ++ks) {
+                const uint32_t dcol = tmem_base + (uint32_t)(b * kGroups * kBwTile + g * kBwTile);
+                const uint64_t bdesc = sw128_desc_mn(gt_addr + (uint32_t)(gp * kBwPlaneBytes + ks * 2048), 1024);
+                const uint32_t acc = (q == 0 && ks == 0) ? 0u : 1u;
+                if (kTmA && pp < 2)
+                  mma_bf16_ta(dcol, tmem_base + (uint32_t)(kAtCol0 + g * kAtCols + pp * (kBwRp / 2) + ks * 8),
+                              bdesc, idesc_d1_ta, acc);
+                else
+                  mma_bf16(dcol, sw128_desc_mn(a_addr + (uint32_t)(g * 2 * kABlk + pp * kBwPlaneBytes + ks * 2048), kABlk),
+                           bdesc, idesc_d1, acc);
+              }
+            }
+          }
+          mma_commit(&tail->d1_full[b]);
+          // then x^T G, accumulated over the unit (the previous unit's sum
+          // must have been read out first): A = x tile seen MN-major (rows =
+          // tokens = K), B = G planes K-major
+          if (first && piece > 0 &&
+              !wait_bar_sleep(&tail->mt_empty, (uint32_t)(piece - 1) & 1u, ctl, kErrWaitTimeout)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
 #pragma unroll
           for (int g = 0; g < kGroups; ++g) {
 #pragma unroll
@@ -559,29 +599,7 @@ __global__ void __launch_bounds__(kMainThreads, 1)
                        sw128_desc_mn(x_addr + (uint32_t)(g * 2 * kBwTile * 128 + ks * 2048), kBwTile * 128),
                        sw128_desc(gt_addr + (uint32_t)(ks * 32)), idesc_mt, (first && ks == 0) ? 0u : 1u);
           }
-          const int b = (int)(k & 1);
-          if (!wait_bar_sleep(&tail->d1_empty[b], ((uint32_t)(k >> 1) & 1u) ^ 1u, ctl, kErrWaitTimeout)) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
-          // G phi': A = phi' slab MN-major (rows = gate rows = K), B = G planes
-          // MN-major with N = 64 tokens, one 128-byte row (its atom stride is unused)
-#pragma unroll
-          for (int g = 0; g < kGroups; ++g) {
-#pragma unroll
-            for (int q = 0; q < kNQ; ++q) {
-              int gp, pp;
-              product_planes(q, gp, pp);
-#pragma unroll
-              for (int ks = 0; ks < kBwRp / 16; ++ks)
-                mma_bf16(tmem_base + (uint32_t)(b * kGroups * kBwTile + g * kBwTile),
-                         sw128_desc_mn(a_addr + (uint32_t)(g * 2 * kABlk + pp * kBwPlaneBytes + ks * 2048), kABlk),
-                         sw128_desc_mn(gt_addr + (uint32_t)(gp * kBwPlaneBytes + ks * 2048), 1024), idesc_d1,
-                         (q == 0 && ks == 0) ? 0u : 1u);
-            }
-          }
-          mma_commit(&tail->d1_full[b]);
+          mma_commit(&tail->empty[s]);                // the slot's operands have been read
           if (last) {
             mma_commit(&tail->mt_full);
             mma_commit(&tail->a_free);
@@ -593,29 +611,6 @@ __global__ void __launch_bounds__(kMainThreads, 1)
       mma_commit(&tail->mma_done);
       mbar_drain(&tail->mma_done, 0);
     }
-  } else if (warp == kWarpStore) {
-    // ===================================================== grad_x store
-    // Once all epilogue warps have written a tile's grad_x over its x slot,
-    // one TMA store writes it out; the slot goes back to the producer as
-    // soon as the store has read it.
-    if (lane == 0) {
-      int s = 0;
-      uint32_t ph = 0;
-      bool ok = true;
-      for (int u = blockIdx.x; u < nunits && ok; u += gridDim.x) {
-        const int slab = u / nq, chunk = u % nq;
-        const int t0 = (int)((long long)chunk * ntiles / nq), t1 = (int)((long long)(chunk + 1) * ntiles / nq);
-        for (int tile = t0; tile < t1; ++tile) {
-          if (!wait_bar_sleep(&tail->out_ready[s], ph, ctl, kErrWaitTimeout)) { ok = false; break; }
-          tma_store_4d(&tmap_gx, sStage + (size_t)s * kStageBytes, 0, tile * kBwTile, slab, 0);
-          bulk_commit();
-          bulk_wait_read<0>();
-          mbar_arrive(&tail->empty[s]);
-          if (++s == stages) { s = 0; ph ^= 1u; }
-        }
-      }
-      bulk_wait<0>();                           // every grad_x store has landed
-    }
   } else {
     // ===================================================== epilogue
     const int ew = warp - kWarpEpi0;          // 0..15
@@ -625,11 +620,11 @@ __global__ void __launch_bounds__(kMainThreads, 1)
     const int m = q * 32 + lane;              // row of the group (0..127)
     const int i = grp * 2 + (m >> 6);         // stream
     const int d = m & 63;                     // column of the slab
-    // Per-lane byte offsets of the epilogue's shared-memory accesses: x /
-    // grad_h_in / grad_x element pair (token half*32 + j + 4*odd, columns
-    // dp, dp+1) in the swizzled tile, and the (hPre_i, RMS factor) pair of
-    // that token; iteration e0 adds e0 rows (multiples of 8: the swizzle
-    // phase is unchanged).
+    // Per-lane byte offsets of the epilogue's shared-memory reads: x /
+    // grad_h_in element pair (token half*32 + j + 4*odd, columns dp, dp+1)
+    // in the swizzled tile, and the (hPre_i, RMS factor) pair of that token;
+    // iteration e0 adds e0 rows (multiples of 8: the swizzle phase is
+    // unchanged).  grad_x goes straight to global memory from registers.
     const int odd = lane & 1, dp = d & ~1;
     uint32_t xoff[4], soff[4];
 #pragma unroll
@@ -638,25 +633,59 @@ __global__ void __launch_bounds__(kMainThreads, 1)
       xoff[j] = (uint32_t)((half * kHalf + ej) * 128) + ((uint32_t)((dp >> 3) ^ ej) << 4) + ((uint32_t)(dp & 7) << 1);
       soff[j] = (uint32_t)((i * (2 * kBwTile) + 2 * (half * kHalf + ej)) * 4);
     }
+    const uint32_t trow = (uint32_t)(kBwNS * D);   // elements from one token to the next
     int s = 0;
     uint32_t ph = 0;
     long long k = 0;
     int piece = 0;
     bool run = true;
     for (int u = blockIdx.x; u < nunits && run; u += gridDim.x) {
-      const int chunk = u % nq;
+      const int slab = u / nq, chunk = u % nq;
       const int t0 = (int)((long long)chunk * ntiles / nq), t1 = (int)((long long)(chunk + 1) * ntiles / nq);
+      if (kTmA && t0 < t1 && ew < 4) {
+        // One warp per TMEM lane quarter copies phi' planes 0 and 1 of the
+        // unit's slab into tensor memory as the A operand of G phi': lane m
+        // = column m of group g, column c = gate rows 2c (low half) and
+        // 2c + 1.  The slab is in shared memory once a_full completes, which
+        // is after the previous unit's MMAs have all finished (a_free).
+        if (!wait_bar_sleep(&tail->a_full, (uint32_t)piece & 1u, ctl, kErrWaitTimeout)) {
+          run = false;
+          break;
+        }
+#pragma unroll 1
+        for (int g = 0; g < kGroups; ++g) {
+          const int mm = q * 32 + lane;
+          const uint8_t* src = sA + (g * 2 + (mm >> 6)) * kABlk;
+          const int dc = mm & 63;
+          uint32_t w[2 * (kBwRp / 2)];
+#pragma unroll
+          for (int c = 0; c < 2 * (kBwRp / 2); ++c) {
+            const int pl = c / (kBwRp / 2), r = 2 * (c % (kBwRp / 2));
+            const uint16_t lo = *reinterpret_cast<const uint16_t*>(src + pl * kBwPlaneBytes + swz(r, dc));
+            const uint16_t hi = *reinterpret_cast<const uint16_t*>(src + pl * kBwPlaneBytes + swz(r + 1, dc));
+            w[c] = (uint32_t)lo | ((uint32_t)hi << 16);
+          }
+          tmem_st32(tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(kAtCol0 + g * kAtCols), w);
+        }
+        tmem_st_wait();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&tail->at_full);
+      }
       for (int tile = t0; tile < t1; ++tile, ++k) {
         const bool last = tile == t1 - 1;
         const int b = (int)(k & 1);
+        const int tok0 = tile * kBwTile + half * kHalf + 4 * odd;   // this lane's token at (e0, j) = (0, 0)
+        const int lim = T - tok0;                                    // its tokens e0 + j < lim exist
+        __nv_bfloat16* gout = gx + (size_t)tok0 * trow + (size_t)i * D + slab * 64 + dp;
         if (!wait_bar_sleep(&tail->full[s], ph, ctl, kErrWaitTimeout) ||
             !wait_bar_sleep(&tail->d1_full[b], (uint32_t)(k >> 1) & 1u, ctl, kErrWaitTimeout)) {
           run = false;
           break;
         }
         tc_fence_after();
-        uint8_t* st = sStage + (size_t)s * kStageBytes;
-        uint8_t* xs = st + i * (kBwTile * 128);
+        const uint8_t* st = sStage + (size_t)s * kStageBytes;
+        const uint8_t* xs = st + i * (kBwTile * 128);
         const uint8_t* gxs = st + offGxp + i * (kBwTile * 128);
         const uint8_t* gin = st + offGin;
         const float* scal = reinterpret_cast<const float*>(st + offRec + P * kBwPlaneBytes);
@@ -701,12 +730,14 @@ __global__ void __launch_bounds__(kMainThreads, 1)
               vlo += pf.x;
               vhi += pf.y;
             }
-            *reinterpret_cast<__nv_bfloat162*>(xs + off) = __floats2bfloat162_rn(vlo, vhi);
+            if (e0 + j < lim) {
+              const __nv_bfloat162 o = __floats2bfloat162_rn(vlo, vhi);
+              __stcs(reinterpret_cast<unsigned int*>(gout + (e0 + j) * trow), *reinterpret_cast<const unsigned int*>(&o));
+            }
           }
         }
-        fence_proxy_async_smem();
         __syncwarp();
-        if (lane == 0) mbar_arrive(&tail->out_ready[s]);
+        if (lane == 0) mbar_arrive(&tail->empty[s]);      // this warp has read the slot
         if (last && half == 0) {
           // x^T G of this unit, summed over the planes -> partial buffer [u][r][k]
           if (!wait_bar_sleep(&tail->mt_full, (uint32_t)piece & 1u, ctl, kErrWaitTimeout)) {
@@ -863,14 +894,15 @@ cudaError_t launch_bw_main(const BwMainLaunch& L, cudaStream_t s) {
   cfg.blockDim = dim3(kMainThreads, 1, 1);
   cfg.dynamicSmemBytes = L.smem_bytes;
   cfg.stream = s;
-  int ntiles = L.ntiles, nslab = L.nslab, nq = L.nq, stages = L.stages;
+  int T = L.T, D = L.D, ntiles = L.ntiles, nslab = L.nslab, nq = L.nq, stages = L.stages;
   const __nv_bfloat16* planes = L.planes;
   const uint8_t* tiles = L.tiles;
   float* pieces = L.pieces;
+  __nv_bfloat16* gx = L.grad_x;
   uint32_t* err = L.err;
   void* args[] = {const_cast<CUtensorMap*>(&L.tmap_x), const_cast<CUtensorMap*>(&L.tmap_gin),
-                  const_cast<CUtensorMap*>(&L.tmap_gx), const_cast<CUtensorMap*>(&L.tmap_gxp),
-                  &planes, &tiles, &pieces, &err, &ntiles, &nslab, &nq, &stages};
+                  const_cast<CUtensorMap*>(&L.tmap_gxp), &planes, &tiles, &pieces, &gx, &err,
+                  &T, &D, &ntiles, &nslab, &nq, &stages};
   return cudaLaunchKernelExC(&cfg, k, args);
 }
 

@@ -554,8 +554,9 @@ struct BwTokenParams {
 };
 
 struct BwMainLaunch {
-  CUtensorMap tmap_x, tmap_gin, tmap_gx, tmap_gxp;
+  CUtensorMap tmap_x, tmap_gin, tmap_gxp;
   const __nv_bfloat16* planes;
+  __nv_bfloat16* grad_x;       // [T][n][D], written by the epilogue warps
   const uint8_t* tiles;
   float* pieces;               // [nslab * nq][kBwRp][NS * 64]: x^T G per unit, planes summed
   uint32_t* err;

@@ -897,9 +897,9 @@ mhc_status_t mhc_pre_backward_run(mhc_pre_t h, const mhc_pre_bwd_args* a, void* 
     const uint64_t dims[4] = {64, (uint64_t)T, (uint64_t)nslab, (uint64_t)n};
     const uint64_t strides[3] = {(uint64_t)n * D * 2, 128, (uint64_t)D * 2};
     const uint32_t box[4] = {64, (uint32_t)mhc::kBwTile, 1, (uint32_t)n};
-    if (!encode_4d(&M.tmap_x, a->x, dims, strides, box) || !encode_4d(&M.tmap_gx, a->grad_x, dims, strides, box) ||
+    if (!encode_4d(&M.tmap_x, a->x, dims, strides, box) ||
         !encode_4d(&M.tmap_gxp, gxp ? a->grad_x_post : a->x, dims, strides, box))
-      return fail(MHC_ERR_RUNTIME, "encoding the x / grad_x tensor maps failed");
+      return fail(MHC_ERR_RUNTIME, "encoding the x / grad_x_post tensor maps failed");
     const uint64_t gd[3] = {64, (uint64_t)T, (uint64_t)nslab};
     const uint64_t gs[2] = {(uint64_t)D * 2, 128};
     const uint32_t gb[3] = {64, (uint32_t)mhc::kBwTile, 1};
@@ -907,6 +907,7 @@ mhc_status_t mhc_pre_backward_run(mhc_pre_t h, const mhc_pre_bwd_args* a, void* 
       return fail(MHC_ERR_RUNTIME, "encoding the grad_h_in tensor map failed");
   }
   M.planes = planes;
+  M.grad_x = static_cast<__nv_bfloat16*>(a->grad_x);
   M.tiles = tiles;
   M.pieces = pieces;
   M.err = err;
