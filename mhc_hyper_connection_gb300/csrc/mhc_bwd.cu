@@ -68,10 +68,19 @@ __device__ __forceinline__ uint32_t swz(int row, int col) {
   return (uint32_t)(row * 128 + ((((col >> 3) ^ (row & 7)) << 4) | ((col & 7) << 1)));
 }
 
+// The backward's launches after the first are programmatic dependents of
+// the one before (their launch and set-up overlap its tail): each kernel
+// lets its dependent launch as soon as all of its own CTAs run, and waits
+// for its predecessor's grid (complete, memory visible) before it reads
+// anything.  Without the launch attribute both instructions are no-ops.
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 // =================================================================== planes
 // One thread per stored 16-byte piece: eight consecutive columns of one
 // plane row (D is a multiple of 64 here, so every piece is inside D).
 __global__ void __launch_bounds__(256) bw_planes_kernel(BwPlaneParams pp) {
+  pdl_trigger();
   if (blockIdx.x == 0 && threadIdx.x < kHdrWords && pp.hdr) pp.hdr[threadIdx.x] = 0u;
   const int rows = pp.P * kBwRp;                        // rows of one stream block
   const long long pieces = (long long)pp.nslab * kBwNS * rows * 8;
@@ -139,6 +148,8 @@ __global__ void __launch_bounds__(kRdThreads, 1) bw_rowdot_kernel(BwRowdotParams
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int ngroups = (p.T + p.tps - 1) / p.tps;
   Ctl ctl{&tail->abort, p.err};
+  pdl_trigger();
+  pdl_wait();
   if (threadIdx.x == 0) {
     for (int s = 0; s < p.stages; ++s) {
       mbar_init(&tail->full[s], 1);
@@ -231,6 +242,8 @@ __global__ void __launch_bounds__(kBwTokenWarps * 32) bw_token_kernel(BwTokenPar
   constexpr int NS = kBwNS, R = kBwR, NN = NS * NS;
   static_assert(NN == 16 && R <= 32, "the half-warp layout is for n = 4");
   __shared__ float stage[kBwTokenWarps][2][kSinkChunk][NN + NS];
+  pdl_trigger();
+  pdl_wait();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int half = lane >> 4, hl = lane & 15;
   const int gw = blockIdx.x * kBwTokenWarps + warp;
@@ -482,6 +495,8 @@ __global__ void __launch_bounds__(kMainThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = tail->tmem_base;
+  pdl_trigger();
+  pdl_wait();                                    // tile records and planes are the earlier launches'
 
   if (warp == kWarpProd) {
     // ===================================================== TMA producer
@@ -782,43 +797,71 @@ __global__ void __launch_bounds__(kMainThreads, 1)
 }
 
 // =============================================================== final sums
-constexpr int kFinalThreads = 256;
+// Column blocks: kFinCols columns k, three groups of eight gate rows each
+// (one thread per column and group: all of a thread's unit loads are
+// independent, and three times the threads of one per column); the groups'
+// grad_gamma terms are added in group order.  Reduction blocks: one of
+// grad_bias / grad_alpha each.
+constexpr int kFinCols = 128, kFinGroups = 3, kFinRows = kBwR / kFinGroups;
+constexpr int kFinalThreads = kFinCols * kFinGroups;
+static_assert(kFinRows * kFinGroups == kBwR, "gate rows split evenly");
 
 __global__ void __launch_bounds__(kFinalThreads) bw_final_kernel(BwFinalParams p, int col_blocks) {
+  pdl_wait();
   const int K = kBwNS * p.D;
+  __shared__ float red[kFinalThreads];
   if ((int)blockIdx.x < col_blocks) {
-    const int k = blockIdx.x * kFinalThreads + threadIdx.x;
-    if (k >= K) return;
-    const int i = k / p.D, dd = k % p.D;
-    const int slab = dd / 64;
-    const int mloc = i * 64 + (dd & 63);
-    float acc[kBwR];
-#pragma unroll
-    for (int r = 0; r < kBwR; ++r) acc[r] = 0.0f;
-    for (int c = 0; c < p.nq; ++c) {                  // the slab's units, in order
-      const float* src = p.pieces + (size_t)(slab * p.nq + c) * kBwRp * (kBwNS * 64) + mloc;
-#pragma unroll
-      for (int r = 0; r < kBwR; ++r) acc[r] += src[(size_t)r * (kBwNS * 64)];
-    }
-    const float gm = p.gamma ? __ldg(p.gamma + k) : 1.0f;
+    const int grp = threadIdx.x / kFinCols, kk = threadIdx.x % kFinCols;
+    const int k = blockIdx.x * kFinCols + kk;
     float gg = 0.0f;
+    if (k < K) {
+      const int i = k / p.D, dd = k % p.D;
+      const int slab = dd / 64;
+      const int mloc = i * 64 + (dd & 63);
+      const int r0 = grp * kFinRows;
+      float acc[kFinRows];
 #pragma unroll
-    for (int r = 0; r < kBwR; ++r) {
-      p.grad_phi[(size_t)r * K + k] = gm * acc[r];
-      gg = fmaf(__ldg(p.phi + (size_t)r * K + k), acc[r], gg);
+      for (int r = 0; r < kFinRows; ++r) acc[r] = 0.0f;
+#pragma unroll
+      for (int c = 0; c < kBwMaxChunks; ++c) {        // the slab's units, in order
+        if (c < p.nq) {
+          const float* src = p.pieces + (size_t)(slab * p.nq + c) * kBwRp * (kBwNS * 64) + (size_t)r0 * (kBwNS * 64) + mloc;
+#pragma unroll
+          for (int r = 0; r < kFinRows; ++r) acc[r] += src[(size_t)r * (kBwNS * 64)];
+        }
+      }
+      const float gm = p.gamma ? __ldg(p.gamma + k) : 1.0f;
+#pragma unroll
+      for (int r = 0; r < kFinRows; ++r) {
+        p.grad_phi[(size_t)(r0 + r) * K + k] = gm * acc[r];
+        gg = fmaf(__ldg(p.phi + (size_t)(r0 + r) * K + k), acc[r], gg);
+      }
     }
-    if (p.grad_gamma) p.grad_gamma[k] = gg;
+    red[threadIdx.x] = gg;
+    __syncthreads();
+    if (grp == 0 && k < K && p.grad_gamma) {
+      float t = red[kk];
+#pragma unroll
+      for (int q = 1; q < kFinGroups; ++q) t += red[q * kFinCols + kk];
+      p.grad_gamma[k] = t;
+    }
     return;
   }
   // grad_bias[v] (v < R) and grad_alpha[v - R]: fixed-order sums of the partials
-  __shared__ float red[kFinalThreads];
   const int v = blockIdx.x - col_blocks;
   const int colp = v;                       // column of the partial records
   float sacc = 0.0f;
   for (int j = threadIdx.x; j < p.nparts; j += kFinalThreads) sacc += p.partials[(size_t)j * 32 + colp];
   red[threadIdx.x] = sacc;
   __syncthreads();
-  for (int o = kFinalThreads / 2; o > 0; o >>= 1) {
+  if ((int)threadIdx.x < kFinCols) {
+    float t = red[threadIdx.x];
+#pragma unroll
+    for (int q = 1; q < kFinGroups; ++q) t += red[q * kFinCols + threadIdx.x];
+    red[threadIdx.x] = t;                   // reads only entries no thread writes in this step
+  }
+  __syncthreads();
+  for (int o = kFinCols / 2; o > 0; o >>= 1) {
     if ((int)threadIdx.x < o) red[threadIdx.x] += red[threadIdx.x + o];
     __syncthreads();
   }
@@ -826,6 +869,24 @@ __global__ void __launch_bounds__(kFinalThreads) bw_final_kernel(BwFinalParams p
     if (v < kBwR) p.grad_bias[v] = red[0];
     else p.grad_alpha[v - kBwR] = red[0];
   }
+}
+
+// A launch that may begin while the previous launch on the stream finishes
+// (the kernel itself waits for it: pdl_wait).
+template <typename... KArgs, typename... Args>
+cudaError_t launch_dependent(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                             Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, args...);
 }
 
 }  // namespace
@@ -858,8 +919,7 @@ void bw_rowdot_shape(int D, size_t max_smem, int* tps, int* stages, size_t* smem
 cudaError_t launch_bw_rowdot(const BwRowdotParams& p, int grid, size_t smem_bytes, cudaStream_t s) {
   cudaError_t e = cudaFuncSetAttribute(bw_rowdot_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_bytes);
   if (e != cudaSuccess) return e;
-  bw_rowdot_kernel<<<grid, kRdThreads, smem_bytes, s>>>(p);
-  return cudaGetLastError();
+  return launch_dependent(bw_rowdot_kernel, dim3(grid), dim3(kRdThreads), smem_bytes, s, p);
 }
 
 cudaError_t bw_token_blocks(int* blocks) {
@@ -877,8 +937,7 @@ cudaError_t bw_token_blocks(int* blocks) {
 }
 
 cudaError_t launch_bw_token(const BwTokenParams& p, int blocks, cudaStream_t s) {
-  bw_token_kernel<<<blocks, kBwTokenWarps * 32, 0, s>>>(p);
-  return cudaGetLastError();
+  return launch_dependent(bw_token_kernel, dim3(blocks), dim3(kBwTokenWarps * 32), 0, s, p);
 }
 
 cudaError_t launch_bw_main(const BwMainLaunch& L, cudaStream_t s) {
@@ -894,6 +953,11 @@ cudaError_t launch_bw_main(const BwMainLaunch& L, cudaStream_t s) {
   cfg.blockDim = dim3(kMainThreads, 1, 1);
   cfg.dynamicSmemBytes = L.smem_bytes;
   cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
   int T = L.T, D = L.D, ntiles = L.ntiles, nslab = L.nslab, nq = L.nq, stages = L.stages;
   const __nv_bfloat16* planes = L.planes;
   const uint8_t* tiles = L.tiles;
@@ -908,10 +972,9 @@ cudaError_t launch_bw_main(const BwMainLaunch& L, cudaStream_t s) {
 
 cudaError_t launch_bw_final(const BwFinalParams& p, cudaStream_t s) {
   const int K = kBwNS * p.D;
-  const int col_blocks = (K + kFinalThreads - 1) / kFinalThreads;
+  const int col_blocks = (K + kFinCols - 1) / kFinCols;
   const int blocks = col_blocks + kBwR + 3;
-  bw_final_kernel<<<blocks, kFinalThreads, 0, s>>>(p, col_blocks);
-  return cudaGetLastError();
+  return launch_dependent(bw_final_kernel, dim3(blocks), dim3(kFinalThreads), 0, s, p, col_blocks);
 }
 
 }  // namespace mhc
