@@ -22,17 +22,18 @@
 //    slabs, so together they read whole rows of x (DRAM-page friendly).
 //    Per tile, TMA brings x [4][64 tokens][64], grad_h_in
 //    [64 tokens][64] and the tile record; tcgen05 forms
-//      - G phi' (phi' = phi . gamma in planes, resident per slab) as
-//        D1[k][token] in TMEM (M = 128 columns k of two streams, N = 64
-//        tokens, K = the 24 gate rows per plane product), and
+//      - G phi' (phi' = phi . gamma in planes, resident per slab; in fp32
+//        mode planes 0 and 1 are read from tensor memory) as D1[k][token]
+//        in TMEM (M = 128 columns k of two streams, N = 64 tokens, K = the
+//        24 gate rows per plane product), then
 //      - x^T G accumulated in TMEM across the run's tiles of one slab
 //        (M = 128 columns k, N = P * 32 plane rows, K = 16 tokens per step).
 //    Sixteen epilogue warps (32 tokens of one M-group each) form
-//    grad_x = hPre grad_h_in + D1 + c x (+ grad_x_post) in fp32 and round
-//    it to bf16 over the x tile in place; a store warp writes the tile out
-//    with one TMA store and hands the slot back.  At the end of a unit
-//    eight of them write x^T G, summed over the planes, to the unit's
-//    partial buffer.
+//    grad_x = hPre grad_h_in + D1 + c x (+ grad_x_post) in fp32, round it
+//    to bf16 and store it from registers; the slot goes back to the
+//    producer once they and the tile's MMAs are done with it.  At the end
+//    of a unit eight of them write x^T G, summed over the planes, to the
+//    unit's partial buffer.
 //  * Final kernel: grad_phi = gamma . sum(x^T G), grad_gamma = sum_r phi .
 //    sum(x^T G), summing a slab's units in chunk order; grad_alpha and
 //    grad_bias from the token stage's per-warp partials in warp order.
