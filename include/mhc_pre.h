@@ -226,8 +226,10 @@ MHC_API mhc_status_t mhc_pre_set_profile_events(mhc_pre_t h, void *before, void 
  * nothing (no copy is left in flight, every other wait still ends).  Those
  * runs' outputs are then incomplete.  Set it back to 0 for normal runs.
  * Applies to the fused forward kernels of mhc_pre_run and
- * mhc_pre_run_noalloc.  MHC_ERR_NULLPTR if h is NULL; MHC_ERR_PARAM_INVALID
- * for a value outside these ranges. */
+ * mhc_pre_run_noalloc and to the contraction kernel of mhc_pre_backward_run
+ * (there the first CTA leaves out the copies of its last tile).
+ * MHC_ERR_NULLPTR if h is NULL; MHC_ERR_PARAM_INVALID for a value outside
+ * these ranges. */
 MHC_API mhc_status_t mhc_pre_set_wait_test(mhc_pre_t h, uint32_t wait_limit_us, int32_t withhold_last_x_copy);
 
 /* Launch shape chosen by the last successful mhc_pre_run on this handle:

@@ -430,7 +430,7 @@ __global__ void __launch_bounds__(kMainThreads, 1)
     bw_main_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constant__ CUtensorMap tmap_gin,
                    const __grid_constant__ CUtensorMap tmap_gxp, const __nv_bfloat16* __restrict__ planes,
                    const uint8_t* __restrict__ tiles, float* __restrict__ pieces, __nv_bfloat16* __restrict__ gx,
-                   uint32_t* err, int T, int D, int ntiles, int nslab, int nq, int stages) {
+                   uint32_t* err, int T, int D, int ntiles, int nslab, int nq, int stages, WaitTest wt) {
   constexpr int kABlk = P * kBwPlaneBytes;            // one stream's block of the phi' slab
   constexpr int kABytes = kBwNS * kABlk;
   constexpr int kRec = bw_tile_rec_bytes(P);
@@ -462,7 +462,7 @@ __global__ void __launch_bounds__(kMainThreads, 1)
   // Work units u = slab * nq + chunk (chunk: a contiguous nq-th of the token
   // tiles), CTA b taking u = b, b + grid, ...; a unit is one run of x^T G.
   const int nunits = nslab * nq;
-  Ctl ctl{&tail->abort, err};
+  Ctl ctl{&tail->abort, err, wt.wait_ns};
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < stages; ++s) {
@@ -528,6 +528,12 @@ __global__ void __launch_bounds__(kMainThreads, 1)
             bulk_prefetch_l2(tiles + (size_t)pt * kRec, (uint32_t)kRec);
           }
           if (!wait_bar_sleep(&tail->empty[s], ph ^ 1u, ctl, kErrWaitTimeout)) { ok = false; break; }
+          // test hook: CTA 0 issues nothing for its last tile, so the waits
+          // on that stage give up (no copy is left in flight)
+          if (wt.withhold_x && blockIdx.x == 0 && tile == t1 - 1 && u + (int)gridDim.x >= nunits) {
+            ok = false;
+            break;
+          }
           uint8_t* st = sStage + (size_t)s * kStageBytes;
           mbar_expect_tx(&tail->full[s], (uint32_t)kStageBytes);
           tma_load_4d_hint(st, &tmap_x, &tail->full[s], 0, tile * kBwTile, slab, 0, once);
@@ -960,6 +966,7 @@ cudaError_t launch_bw_main(const BwMainLaunch& L, cudaStream_t s) {
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   int T = L.T, D = L.D, ntiles = L.ntiles, nslab = L.nslab, nq = L.nq, stages = L.stages;
+  WaitTest wt = L.wt;
   const __nv_bfloat16* planes = L.planes;
   const uint8_t* tiles = L.tiles;
   float* pieces = L.pieces;
@@ -967,7 +974,7 @@ cudaError_t launch_bw_main(const BwMainLaunch& L, cudaStream_t s) {
   uint32_t* err = L.err;
   void* args[] = {const_cast<CUtensorMap*>(&L.tmap_x), const_cast<CUtensorMap*>(&L.tmap_gin),
                   const_cast<CUtensorMap*>(&L.tmap_gxp), &planes, &tiles, &pieces, &gx, &err,
-                  &T, &D, &ntiles, &nslab, &nq, &stages};
+                  &T, &D, &ntiles, &nslab, &nq, &stages, &wt};
   return cudaLaunchKernelExC(&cfg, k, args);
 }
 

@@ -562,6 +562,7 @@ struct BwMainLaunch {
   uint32_t* err;
   int T, D, ntiles, nslab, nq, P, stages, has_gxp, grid;
   size_t smem_bytes;
+  WaitTest wt;                 // wait limit; withhold_x: CTA 0 leaves out its last tile's copies
 };
 
 struct BwFinalParams {

@@ -921,6 +921,7 @@ mhc_status_t mhc_pre_backward_run(mhc_pre_t h, const mhc_pre_bwd_args* a, void* 
   M.grid = (int)grid;
   M.nq = nq;
   M.smem_bytes = fixed + (size_t)stages * stage;
+  M.wt = h->wait_test;
 
   mhc::BwPlaneParams pp;
   pp.phi = a->phi;

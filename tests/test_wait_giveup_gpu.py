@@ -1,4 +1,4 @@
-"""The forward kernels' bounded waits, made to run out on purpose and without
+"""The forward and backward kernels' bounded waits, made to run out on purpose and without
 any fault: with mhc_pre_set_wait_test the host asks the first CTA to leave
 out its last x copy (nothing is issued for it, so no copy is in flight) and
 shortens the wait limit.  The waits on that copy give up, the kernel winds
@@ -53,3 +53,21 @@ def test_wait_test_arguments(cuda_device):
     assert mp.mhc_pre_set_wait_test(op.handle, 0, 2) == mp.MHC_ERR_PARAM_INVALID
     assert mp.mhc_pre_set_wait_test(op.handle, 10_000_001, 0) == mp.MHC_ERR_PARAM_INVALID
     assert mp.mhc_pre_set_wait_test(None, 0, 0) == mp.MHC_ERR_NULLPTR
+
+
+def test_backward_wait_gives_up_then_next_run_is_clean(cuda_device):
+    """The same for the backward: the contraction kernel's first CTA leaves
+    out the copies of its last tile, its waits give up, the status reports
+    MHC_ERR_RUNTIME, and the next normal run matches the oracle."""
+    import mhc_hyper_connection_gb300 as mp
+    from test_bwd_gpu import _check, _run_gpu, _run_oracle, _setup
+    S = _setup(cuda_device, 300, 1024, seed=5)
+    c = S.case
+    grads = S.op.allocate_backward(c.T, cuda_device, gamma=True)
+    assert mp.mhc_pre_set_wait_test(S.op.handle, 2000, 1) == mp.MHC_OK
+    S.op.backward(c.x, c.phi, c.alpha, c.gamma, S.g.g_in, S.g.g_post, S.g.g_res, S.saved, grads)
+    assert S.op.status(grads) == mp.MHC_ERR_RUNTIME
+    assert "gave up" in mp.last_error()
+    assert mp.mhc_pre_set_wait_test(S.op.handle, 0, 0) == mp.MHC_OK
+    grads = _run_gpu(S, grads)
+    _check(S, grads, _run_oracle(S))
