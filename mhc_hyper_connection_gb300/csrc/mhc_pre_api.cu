@@ -1046,7 +1046,7 @@ mhc_status_t mhc_pre_inv_rms_run(mhc_pre_t h, int64_t T, const void* x, float* i
   if (T == 0) return MHC_OK;
   if (!x || !inv_rms) return fail(MHC_ERR_NULLPTR, "x and inv_rms are required");
   if (!aligned(x, 16) || !aligned(inv_rms, 4)) return fail(MHC_ERR_PARAM_INVALID, "x must be 16-byte aligned");
-  cudaStream_t s;
+  cudaStream_t s = nullptr;
   const mhc_status_t st = stage_device(&s, stream);
   if (st != MHC_OK) return st;
   mhc::StageLaunch L = stage_launch(h, T, x);
@@ -1066,7 +1066,7 @@ mhc_status_t mhc_pre_mixes_run(mhc_pre_t h, int64_t T, const void* x, const floa
   if (!aligned(x, 16)) return fail(MHC_ERR_PARAM_INVALID, "x must be 16-byte aligned");
   if (!aligned(phi, 4) || !aligned(mixes, 4) || (gamma && !aligned(gamma, 4)))
     return fail(MHC_ERR_PARAM_INVALID, "fp32 tensors must be 4-byte aligned");
-  cudaStream_t s;
+  cudaStream_t s = nullptr;
   const mhc_status_t st = stage_device(&s, stream);
   if (st != MHC_OK) return st;
   mhc::StageLaunch L = stage_launch(h, T, x);
@@ -1105,7 +1105,7 @@ mhc_status_t mhc_pre_sinkhorn_run(mhc_pre_t h, const mhc_pre_args* a, const floa
                        a->h_mix, a->sum_out, a->norm_out, mixes, inv_rms};
   for (const void* p : f32)
     if (p && !aligned(p, 4)) return fail(MHC_ERR_PARAM_INVALID, "fp32 tensors must be 4-byte aligned");
-  cudaStream_t s;
+  cudaStream_t s = nullptr;
   const mhc_status_t st = stage_device(&s, stream);
   if (st != MHC_OK) return st;
   const mhc::EpiParams ep = epi_params(h, a);
