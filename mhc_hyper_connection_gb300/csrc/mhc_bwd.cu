@@ -234,6 +234,13 @@ __global__ void __launch_bounds__(kRdThreads, 1) bw_rowdot_kernel(BwRowdotParams
 // =============================================================== token stage
 constexpr int kSinkChunk = 20;   // saved Sinkhorn steps staged per round and token
 
+// 16-byte global -> shared copy that bypasses the registers (completes at
+// cp_async_wait_all of the issuing thread).
+__device__ __forceinline__ void cp_async16(void* dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(dst)), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
+
 // One token per half-warp (two per warp, so twice the tokens in flight):
 // lane hl = i*4 + j of the half holds the Sinkhorn element (i, j) and gate
 // rows hl and hl + 16.  Both halves run every shuffle (all of them stay
@@ -242,7 +249,7 @@ constexpr int kSinkChunk = 20;   // saved Sinkhorn steps staged per round and to
 __global__ void __launch_bounds__(kBwTokenWarps * 32) bw_token_kernel(BwTokenParams p) {
   constexpr int NS = kBwNS, R = kBwR, NN = NS * NS;
   static_assert(NN == 16 && R <= 32, "the half-warp layout is for n = 4");
-  __shared__ float stage[kBwTokenWarps][2][kSinkChunk][NN + NS];
+  __shared__ __align__(16) float stage[kBwTokenWarps][2][kSinkChunk][NN + NS];
   pdl_trigger();
   pdl_wait();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -278,10 +285,21 @@ __global__ void __launch_bounds__(kBwTokenWarps * 32) bw_token_kernel(BwTokenPar
         const int klo = max(1, kh - kSinkChunk + 1);
         const int cnt = kh - klo + 1;
         __syncwarp();
-        // the chunk's saved matrices and sums of this half's token, eight
+        // the chunk's saved matrices and sums of this half's token: with
+        // 16-byte aligned tensors all of them at once as asynchronous copies
+        // (four pieces of a step's matrix and one of its sums), else eight
         // loads in flight per lane (sums of a padding token read as 1)
         const int nm = cnt * NN, ntot = nm + cnt * NS;
         constexpr int kBatch = 8;
+        if (p.saved16 && valid) {
+          for (int q = hl; q < cnt * 5; q += 16) {
+            const int s = q / 5, part = q - 5 * s;
+            const float* src = part < 4 ? p.norm_out + ((size_t)(klo + s) * p.T + tv) * NN + part * 4
+                                        : p.sum_out + ((size_t)(klo + s) * p.T + tv) * NS;
+            cp_async16(&st[s][part * 4], src);
+          }
+          cp_async_wait_all();
+        } else
         for (int e0 = hl; e0 < ntot; e0 += 16 * kBatch) {
           float v[kBatch];
 #pragma unroll

@@ -551,6 +551,7 @@ struct BwTokenParams {
   const float* alpha;          // [3]
   uint8_t* tiles;              // [ntiles] tile records
   float* partials;             // [blocks * 8][32]
+  int saved16;                 // sum_out and norm_out 16-byte aligned: asynchronous 16-byte copies
 };
 
 struct BwMainLaunch {

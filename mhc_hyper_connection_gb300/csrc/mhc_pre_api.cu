@@ -964,6 +964,7 @@ mhc_status_t mhc_pre_backward_run(mhc_pre_t h, const mhc_pre_bwd_args* a, void* 
   tp.h_post = a->h_post;
   tp.sum_out = a->sum_out;
   tp.norm_out = a->norm_out;
+  tp.saved16 = aligned(a->sum_out, 16) && aligned(a->norm_out, 16) ? 1 : 0;
   tp.alpha = a->alpha;
   tp.tiles = tiles;
   tp.partials = partials;
