@@ -565,15 +565,28 @@ mhc_status_t mhc_pre_run(mhc_pre_t h, const mhc_pre_args* a, void* stream) {
     }
   }
   // Resident mode keeps each cluster's tile slice of x (64 tokens of all n
-  // streams) in flight from its first read to y's re-read.  When those
-  // slices overflow L2 by a little, running two fewer clusters than fit
-  // keeps more of the re-read in L2: at prefill (D = 7168, 36 clusters of 4
-  // possible, 35 slices fit) 34 clusters measured 1.7% faster in both
-  // precision modes.  Only a trim of at most a tenth of the clusters.
-  if (resident && !c.cluster && di.l2_bytes > 0) {
-    const double slice = (double)mhc::kTileT * n * D * 2.0;
-    const long long fit = (long long)((double)di.l2_bytes / slice) - 2;
-    if (fit < max_clusters && 10 * fit >= 9LL * max_clusters) max_clusters = (int)fit;
+  // streams) in flight from its first read to y's re-read, so fewer
+  // clusters in flight keep more of the re-read in L2.  (1) As few clusters
+  // as take the same number of rounds of tiles (T = 16384: 64 instead of 76
+  // clusters of 2 at D = 4096, 32 instead of 36 clusters of 4 at D = 7168;
+  // 2-3% faster).  (2) When the slices overflow L2 by a little, two fewer
+  // clusters than fit -- if that trims at most a tenth of the clusters and
+  // adds at most a last round of a tenth of them: at prefill (D = 7168,
+  // T = 32768, 35 slices fit) 34 clusters of 4 measured 1.7% faster than 35
+  // and 36 in both precision modes.
+  if (resident && !c.cluster) {
+    const long long tiles = num_tiles;
+    const long long rounds = (tiles + max_clusters - 1) / max_clusters;
+    long long cl = (tiles + rounds - 1) / rounds;
+    if (di.l2_bytes > 0) {
+      const double slice = (double)mhc::kTileT * n * D * 2.0;
+      const long long fit = (long long)((double)di.l2_bytes / slice) - 2;
+      if (fit > 0 && fit < cl && 10 * fit >= 9LL * max_clusters) {
+        const long long r2 = (tiles + fit - 1) / fit;
+        if (r2 == rounds || (r2 == rounds + 1 && 10 * (tiles - rounds * fit) <= fit)) cl = fit;
+      }
+    }
+    if (cl < max_clusters) max_clusters = (int)cl;
   }
   L.resident = resident ? 1 : 0;
   L.tm_bufs = c.tm_buffers ? c.tm_buffers : 1;
