@@ -564,17 +564,18 @@ mhc_status_t mhc_pre_run(mhc_pre_t h, const mhc_pre_args* a, void* stream) {
       if (st != MHC_ERR_NOT_SUITABLE) return st;
     }
   }
-  // Resident mode keeps each cluster's tile slice of x (64 tokens of all n
-  // streams) in flight from its first read to y's re-read, so fewer
-  // clusters in flight keep more of the re-read in L2.  (1) As few clusters
-  // as take the same number of rounds of tiles (T = 16384: 64 instead of 76
-  // clusters of 2 at D = 4096, 32 instead of 36 clusters of 4 at D = 7168;
-  // 2-3% faster).  (2) When the slices overflow L2 by a little, two fewer
-  // clusters than fit -- if that trims at most a tenth of the clusters and
-  // adds at most a last round of a tenth of them: at prefill (D = 7168,
-  // T = 32768, 35 slices fit) 34 clusters of 4 measured 1.7% faster than 35
-  // and 36 in both precision modes.
-  if (resident && !c.cluster) {
+  // Each cluster keeps its tile slice of x (64 tokens of all n streams) in
+  // flight from its first read to y's re-read, so fewer clusters in flight
+  // keep more of the re-read in L2.  (1) As few clusters as take the same
+  // number of rounds of tiles (T = 16384: 64 instead of 76 clusters of 2 at
+  // D = 4096, 32 instead of 36 clusters of 4 at D = 7168; 1-5% faster for
+  // the resident and the plain kernel, n = 4 and 8).  (2) When the slices
+  // overflow L2 by a little, two fewer clusters than fit -- if that trims at
+  // most a tenth of the clusters and adds at most a last round of a tenth of
+  // them: at prefill (D = 7168, T = 32768, 35 slices fit) 34 clusters of 4
+  // measured 1.7% faster than 35 and 36 in both precision modes.  Not in
+  // batch-consistent mode, whose launch shape stays fixed.
+  if (!c.cluster && !consistent) {
     const long long tiles = num_tiles;
     const long long rounds = (tiles + max_clusters - 1) / max_clusters;
     long long cl = (tiles + rounds - 1) / rounds;
