@@ -572,7 +572,7 @@ mhc_status_t mhc_pre_run(mhc_pre_t h, const mhc_pre_args* a, void* stream) {
   // the resident and the plain kernel, n = 4 and 8).  (2) When the slices
   // overflow L2 by a little, two fewer clusters than fit -- if that trims at
   // most a tenth of the clusters and adds at most a last round of a tenth of
-  // them: at prefill (D = 7168, T = 32768, 35 slices fit) 34 clusters of 4
+  // them to ten or more full rounds: at prefill (D = 7168, T = 32768, 35 slices fit) 34 clusters of 4
   // measured 1.7% faster than 35 and 36 in both precision modes.  Not in
   // batch-consistent mode, whose launch shape stays fixed.
   if (!c.cluster && !consistent) {
@@ -584,7 +584,7 @@ mhc_status_t mhc_pre_run(mhc_pre_t h, const mhc_pre_args* a, void* stream) {
       const long long fit = (long long)((double)di.l2_bytes / slice) - 2;
       if (fit > 0 && fit < cl && 10 * fit >= 9LL * max_clusters) {
         const long long r2 = (tiles + fit - 1) / fit;
-        if (r2 == rounds || (r2 == rounds + 1 && 10 * (tiles - rounds * fit) <= fit)) cl = fit;
+        if (r2 == rounds || (r2 == rounds + 1 && rounds >= 10 && 10 * (tiles - rounds * fit) <= fit)) cl = fit;
       }
     }
     if (cl < max_clusters) max_clusters = (int)cl;
